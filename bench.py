@@ -1,0 +1,503 @@
+#!/usr/bin/env python
+"""Benchmark of the Cassandra bit-split hot path on GB300.
+
+One step = one self-speculative decode step of a Llama-3-8B-shaped decoder
+stack (32 layers, hidden 4096, FFN 14336, GQA 32q/8kv, head_dim 128) with
+random-init Student-t(4) bf16 weights split at keep 50% / 3 mantissa bits
+(Cassandra-1), batch 1, draft length 4, and a compressed KV cache of 32K tokens
+(bf16 K/V ~ N(0,1) x LogNormal(0,0.5) channel scales):
+  4 draft forwards  : per layer draft GEMV (Wqkv), draft attention over the
+                      speculation KV + bf16 tail, draft GEMV (Wo, Wgate|up, Wdown);
+  1 verify forward  : per layer verify GEMM (T=5), online KV append of the 5
+                      tokens, verify attention, verify GEMMs;
+  then the 5 tokens are rolled back (fixed schedule: acceptance has no meaning
+  on random weights).
+Activations fed to each kernel are synthetic device vectors (the norm / RoPE /
+activation glue between kernels is not part of the measured path).
+
+Headline value: draft decode+GEMV GB/s over the algorithmic bytes of the
+speculation streams read (plus x read and y written), timed with CUDA events on
+the launching stream around the draft-GEMV launches of the timed steps.
+Also reported: verify GEMM GB/s, microseconds per decode step, roofline of the
+draft GEMV against the measured HBM copy bandwidth, the end-to-end number
+through the C ABI with host buffers, and the CPU oracle as a reported baseline.
+
+--impl reference times the CPU oracle (the plain C restatement) on the host
+cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "draft decode+GEMV GB/s (% of HBM peak); verify GEMM GB/s; µs per decode step"
+WORKLOAD = "llama3-8b-stack speculative decode step"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="cas", choices=["cas", "reference"])
+    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--ctx", type=int, default=32768)
+    ap.add_argument("--keep", type=int, default=64)
+    ap.add_argument("--mant", type=int, default=3)
+    ap.add_argument("--draft-len", type=int, default=4)
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--no-attn", action="store_true", help="weights only (no KV cache)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------- helpers
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during timing."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.rows, self.proc = index, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:  # noqa: BLE001
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:  # noqa: BLE001
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in self.rows if len(r) > 8 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) > 8 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows if len(r) > 8 for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ---------------------------------------------------------------------- CPU oracle baseline
+def cpu_baseline(seconds: float, keep: int, mant: int):
+    """Oracle draft decode + GEMV (plain C, one thread) on a bounded sample: one
+    1024x4096 Student-t(4) matrix of the same stack, repeated for ~`seconds`."""
+    import numpy as np
+
+    import oracle
+    import synthetic
+    N, K = 1024, 4096
+    W = synthetic.t4_weight(N, K, seed=0).numpy().view(np.uint16)
+    x = synthetic.activations(1, K, seed=1).numpy().view(np.uint16)
+    enc = oracle.encode(W, 1, keep, mant)
+    spec = enc.spec_bytes() + K * 2 + N * 4
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        d = oracle.decode(enc, False)
+        oracle.matvec(d, x)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": spec * reps / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{reps} x oracle draft decode + float64 GEMV of one 1024x4096 t4 matrix "
+                      f"(keep {keep}/128, m={mant}, Cassandra-1), {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------------- workload
+class Stack:
+    """Encoded Llama-3-8B-shaped stack plus its compressed KV caches."""
+
+    def __init__(self, cas, args, dev):
+        import torch
+
+        import synthetic
+        self.cas, self.args, self.dev = cas, args, dev
+        shp = dict(synthetic.LLAMA3_8B)
+        self.L = args.layers
+        h, f = shp["hidden"], shp["ffn"]
+        self.hidden, self.ffn, self.nq, self.nkv, self.hd = h, f, shp["n_q"], shp["n_kv"], shp["head_dim"]
+        self.mats = []  # per layer: dict name -> EncodedWeights
+        t0 = time.time()
+        for layer in range(self.L):
+            names = synthetic.layer_matrices(shp)
+            raw = {}
+            for idx, (nm, N, K) in enumerate(names):
+                raw[nm] = synthetic.t4_weight(N, K, seed=layer * 16 + idx, device=dev)
+            fused = {
+                "qkv": torch.cat([raw["wq"], raw["wk"], raw["wv"]], 0),
+                "o": raw["wo"],
+                "gateup": torch.cat([raw["wgate"], raw["wup"]], 0),
+                "down": raw["wdown"],
+            }
+            del raw
+            enc = {nm: cas.encode_weights(W, 1, args.keep, args.mant) for nm, W in fused.items()}
+            del fused
+            self.mats.append(enc)
+        torch.cuda.synchronize()
+        self.encode_s = time.time() - t0
+        self.kv = None
+        if not args.no_attn and hasattr(cas, "KVCache"):
+            self._fill_kv()
+
+    def _fill_kv(self):
+        import torch
+
+        import synthetic
+        cas, args, dev = self.cas, self.args, self.dev
+        T = args.ctx
+        self.kv = []
+        p = cas.params(1, args.keep, args.mant)
+        chunk = 2048
+        for layer in range(self.L):
+            layer_kv = []
+            for b in range(args.batch):
+                sk = synthetic.kv_scales(layer, self.nkv, 0, device=dev)
+                sv = synthetic.kv_scales(layer, self.nkv, 1, device=dev)
+                Kc = synthetic.kv_tokens(T, self.nkv, seed=100 * layer + 2 * b, scales=sk, device=dev)
+                Vc = synthetic.kv_tokens(T, self.nkv, seed=100 * layer + 2 * b + 1, scales=sv, device=dev)
+                kv = cas.KVCache(self.nkv, T + 64, p, Kc[:128], Vc[:128])
+                for t0 in range(0, T, chunk):
+                    kv.append(Kc[t0:t0 + chunk], Vc[t0:t0 + chunk])
+                layer_kv.append(kv)
+                del Kc, Vc
+            self.kv.append(layer_kv)
+        torch.cuda.synchronize()
+        for layer_kv in self.kv:
+            for kv in layer_kv:
+                n, st = kv.status()
+                assert st == 0 and n == T, (n, st)
+
+
+def run_cas(args):
+    import torch
+    import torch.distributed as dist
+
+    import bit_level_weight_gb300 as cas
+    import synthetic
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from bit_level_weight_gb300 import build as _b
+    _b.build()
+
+    stk = Stack(cas, args, dev)
+    st = torch.cuda.current_stream()
+    D, B = args.draft_len, args.batch
+    nvec = B
+    xs = {"qkv": synthetic.activations(nvec, stk.hidden, seed=1, device=dev),
+          "o": synthetic.activations(nvec, stk.hidden, seed=2, device=dev),
+          "gateup": synthetic.activations(nvec, stk.hidden, seed=3, device=dev),
+          "down": synthetic.activations(nvec, stk.ffn, seed=4, device=dev)}
+    T = B * (D + 1)
+    Xs = {"qkv": synthetic.activations(T, stk.hidden, seed=5, device=dev),
+          "o": synthetic.activations(T, stk.hidden, seed=6, device=dev),
+          "gateup": synthetic.activations(T, stk.hidden, seed=7, device=dev),
+          "down": synthetic.activations(T, stk.ffn, seed=8, device=dev)}
+    ys = {nm: torch.empty(nvec, stk.mats[0][nm].N, dtype=torch.float32, device=dev) for nm in xs}
+    Ys = {nm: torch.empty(T, stk.mats[0][nm].N, dtype=torch.float32, device=dev) for nm in Xs}
+
+    gemv = [{nm: cas.prepare("cas_draft_gemv", stk.mats[l][nm], xs[nm], nvec, ys[nm], st) for nm in xs}
+            for l in range(stk.L)]
+    gemm = [{nm: cas.prepare("cas_verify_gemm", stk.mats[l][nm], Xs[nm], T, Ys[nm], st) for nm in Xs}
+            for l in range(stk.L)]
+    draft_bytes_layer = {nm: stk.mats[0][nm].spec_bytes() + nvec * stk.mats[0][nm].K * 2 + nvec * stk.mats[0][nm].N * 4
+                         for nm in xs}
+    verify_bytes_layer = {nm: stk.mats[0][nm].all_bytes() + T * stk.mats[0][nm].K * 2 + T * stk.mats[0][nm].N * 4
+                          for nm in Xs}
+    draft_bytes = {nm: sum(stk.mats[l][nm].spec_bytes() + nvec * stk.mats[l][nm].K * 2 + nvec * stk.mats[l][nm].N * 4
+                           for l in range(stk.L)) for nm in xs}
+    verify_bytes = {nm: sum(stk.mats[l][nm].all_bytes() + T * stk.mats[l][nm].K * 2 + T * stk.mats[l][nm].N * 4
+                            for l in range(stk.L)) for nm in Xs}
+    del draft_bytes_layer, verify_bytes_layer
+
+    attn = stk.kv is not None
+    if attn:
+        q_d = synthetic.activations(B, stk.nq * stk.hd, seed=20, device=dev).view(B, stk.nq, stk.hd)
+        tail_k = synthetic.activations(B * D, stk.nkv * stk.hd, seed=21, device=dev).view(B, D, stk.nkv, stk.hd)
+        tail_v = synthetic.activations(B * D, stk.nkv * stk.hd, seed=22, device=dev).view(B, D, stk.nkv, stk.hd)
+        q_v = synthetic.activations(B * (D + 1), stk.nq * stk.hd, seed=23, device=dev).view(B, D + 1, stk.nq, stk.hd)
+        newk = synthetic.activations(D + 1, stk.nkv * stk.hd, seed=24, device=dev).view(D + 1, stk.nkv, stk.hd)
+        newv = synthetic.activations(D + 1, stk.nkv * stk.hd, seed=25, device=dev).view(D + 1, stk.nkv, stk.hd)
+        ws = torch.empty(cas.cas_attn_workspace_bytes(B, stk.nq, D + 1, args.ctx + 64), dtype=torch.uint8, device=dev)
+        o_d = torch.empty(B, stk.nq, stk.hd, dtype=torch.float32, device=dev)
+        o_v = torch.empty(B, D + 1, stk.nq, stk.hd, dtype=torch.float32, device=dev)
+        dattn = [[cas.prepare_draft_attn(stk.kv[l], q_d, tail_k[:, :d + 1].contiguous(), tail_v[:, :d + 1].contiguous(),
+                                         o_d, ws, st) for d in range(D)] for l in range(stk.L)]
+        vattn = [cas.prepare_verify_attn(stk.kv[l], q_v, o_v, ws, st) for l in range(stk.L)]
+        appends = [[kv.prepare_append(newk, newv, st) for kv in stk.kv[l]] for l in range(stk.L)]
+        truncs = [[kv.prepare_truncate(args.ctx, st) for kv in stk.kv[l]] for l in range(stk.L)]
+
+    n_ev = 4 * stk.L * D + 4 * stk.L
+    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    ev = evsets[0]
+
+    def step(record: bool, ev=ev):
+        """One speculative step; with record=True brackets the GEMV / GEMM runs
+        with events (pairs: draft GEMV runs first, then verify GEMM runs)."""
+        e = 0
+        for d in range(D):
+            for l in range(stk.L):
+                g = gemv[l]
+                if record:
+                    ev[e].record(st); e += 1
+                g["qkv"]()
+                if record:
+                    ev[e].record(st); e += 1
+                if attn:
+                    dattn[l][d]()
+                if record:
+                    ev[e].record(st); e += 1
+                g["o"](); g["gateup"](); g["down"]()
+                if record:
+                    ev[e].record(st); e += 1
+        for l in range(stk.L):
+            g = gemm[l]
+            if record:
+                ev[e].record(st); e += 1
+            g["qkv"]()
+            if record:
+                ev[e].record(st); e += 1
+            if attn:
+                for a in appends[l]:
+                    a()
+                vattn[l]()
+            if record:
+                ev[e].record(st); e += 1
+            g["o"](); g["gateup"](); g["down"]()
+            if record:
+                ev[e].record(st); e += 1
+        if attn:
+            for l in range(stk.L):
+                for t in truncs[l]:
+                    t()
+        return e
+
+    launches_per_step = D * stk.L * 4 + stk.L * 4
+    if attn:
+        launches_per_step += D * stk.L * 2 + stk.L * (2 * B + 2) + stk.L * B
+
+    for _ in range(max(args.warmup, 3)):
+        step(False)
+    torch.cuda.synchronize()
+
+    # ---- timed region
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    gemv_ms, gemm_ms = 0.0, 0.0
+    with ClockSampler(local) as clk:
+        t_start.record(st)
+        for i in range(args.steps):
+            step(True, evsets[i])
+        t_end.record(st)
+        torch.cuda.synchronize()
+        for ev in evsets:
+            e = 0
+            for d in range(D):
+                for l in range(stk.L):
+                    gemv_ms += ev[e].elapsed_time(ev[e + 1]) + ev[e + 2].elapsed_time(ev[e + 3])
+                    e += 4
+            for l in range(stk.L):
+                gemm_ms += ev[e].elapsed_time(ev[e + 1]) + ev[e + 2].elapsed_time(ev[e + 3])
+                e += 4
+    total_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        dist.barrier()
+
+    steps = args.steps
+    d_bytes = sum(draft_bytes.values()) * D * steps
+    v_bytes = sum(verify_bytes.values()) * steps
+    gemv_gbs = d_bytes / (gemv_ms * 1e-3) / 1e9
+    gemm_gbs = v_bytes / (gemm_ms * 1e-3) / 1e9
+    ms_per_step = total_ms / steps
+
+    # ---- e2e: draft GEMV pass of the whole stack through the C ABI with the
+    # activation in pinned host memory (H2D) and every output read back (D2H)
+    e2e = e2e_draft_pass(cas, stk, xs, ys, nvec, st, steps=max(3, steps))
+
+    vals = torch.tensor([gemv_gbs, gemm_gbs, ms_per_step], dtype=torch.float64, device=dev)
+    if world > 1:
+        # throughput aggregate over replicas; the slowest rank bounds the job
+        g = [torch.zeros_like(vals) for _ in range(world)]
+        dist.all_gather(g, vals)
+        gemv_gbs = min(float(t[0]) for t in g) * world
+        gemm_gbs = min(float(t[1]) for t in g) * world
+        ms_per_step = max(float(t[2]) for t in g)
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    peak, peak_kind = peaks()
+    per_launch_bytes = sum(draft_bytes.values()) / (4 * stk.L)
+    per_launch_ms = gemv_ms / (steps * D * stk.L * 4)
+    achieved = per_launch_bytes / (per_launch_ms * 1e-3) / 1e9
+    out = {
+        "metric": METRIC,
+        "value": round(gemv_gbs, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": WORKLOAD,
+            "layers": stk.L, "hidden": stk.hidden, "ffn": stk.ffn, "heads": f"{stk.nq}q/{stk.nkv}kv x {stk.hd}",
+            "batch": B, "draft_len": D, "verify_tokens": T, "ctx": args.ctx if attn else 0,
+            "keep_per_block": args.keep, "mant_bits": args.mant, "variant": "Cassandra-1",
+            "weights": "Student-t(4) x 0.02/sqrt(2), fused qkv and gate|up",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "l2": "inputs larger than L2 (3.5 GB speculation stream per draft pass)",
+        },
+        "verify_gemm_gbs": round(gemm_gbs, 1),
+        "us_per_decode_step": round(ms_per_step * 1e3, 1),
+        "draft_gemv_frac_of_hbm": round(gemv_gbs / world / peak, 4),
+        "draft_gemv_frac_of_8tbs_nominal": round(gemv_gbs / world / 8000.0, 4),
+        "verify_gemm_frac_of_hbm": round(gemm_gbs / world / peak, 4),
+        "roofline": {"kernel": "draft_gemv_kernel<1,1>", "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
+                     "traffic": PROFILED_TRAFFIC,
+                     "algorithmic_bytes_per_launch": int(per_launch_bytes)},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * steps,
+        "encode_s": round(stk.encode_s, 2),
+    }
+    out["clocks"] = clk.summary()
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.cpu_seconds, args.keep, args.mant)
+    print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# traffic (dram bytes read + written) of one draft_gemv launch from ncu, or None
+PROFILED_TRAFFIC = None
+
+
+def e2e_draft_pass(cas, stk, xs, ys, nvec, st, steps):
+    import torch
+    host_x = {nm: x.cpu().pin_memory() for nm, x in xs.items()}
+    host_y = {nm: torch.empty(stk.L, *y.shape, dtype=torch.float32).pin_memory() for nm, y in ys.items()}
+    dev_y = {nm: torch.empty(stk.L, *y.shape, dtype=torch.float32, device=y.device) for nm, y in ys.items()}
+    calls = [{nm: cas.prepare("cas_draft_gemv", stk.mats[l][nm], xs[nm], nvec, dev_y[nm][l], st) for nm in xs}
+             for l in range(stk.L)]
+    h2d = sum(t.numel() * t.element_size() for t in host_x.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_y.values())
+    spec = sum(stk.mats[l][nm].spec_bytes() + nvec * stk.mats[l][nm].K * 2 + nvec * stk.mats[l][nm].N * 4
+               for l in range(stk.L) for nm in xs)
+
+    def one():
+        for nm in xs:
+            xs[nm].copy_(host_x[nm], non_blocking=True)
+        for l in range(stk.L):
+            c = calls[l]
+            c["qkv"](); c["o"](); c["gateup"](); c["down"]()
+        for nm in ys:
+            host_y[nm].copy_(dev_y[nm], non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(steps):
+        one()
+    b.record(st)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return {"value": round(spec / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "what": "one draft GEMV pass over all 32 layers' matrices via "
+            "cas_draft_gemv, x copied in from pinned host memory and all outputs copied out, per step"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    K, W = args.steps, max(args.warmup, 3)
+    per = max(1.0, min(args.cpu_seconds, 90.0 / (K + W)))
+    for _ in range(W):
+        cpu_baseline(per / 4, args.keep, args.mant)
+    vals = [cpu_baseline(per, args.keep, args.mant) for _ in range(K)]
+    v = statistics.median(x["value"] for x in vals)
+    import synthetic
+    shp = synthetic.LLAMA3_8B
+    spec_per_step = None
+    out = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "layers": args.layers, "hidden": shp["hidden"], "ffn": shp["ffn"],
+                   "batch": args.batch, "draft_len": args.draft_len, "keep_per_block": args.keep,
+                   "mant_bits": args.mant, "variant": "Cassandra-1"},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": vals[0]["sample"]},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "note": "CPU oracle (plain C, one thread) on a bounded sample of the draft GEMV; spec_per_step "
+                f"{spec_per_step}",
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_cas(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,100 @@
+// api.cu - status strings, argument checks and descriptor views of libcas.
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "common.cuh"
+
+extern "C" const char* cas_status_str(int s) {
+  switch (s) {
+    case CAS_OK: return "ok";
+    case CAS_ERR_INVALID: return "invalid argument";
+    case CAS_ERR_SHAPE: return "K (or head_dim) is not a multiple of 128";
+    case CAS_ERR_NONFINITE: return "NaN or Inf in a tensor to encode";
+    case CAS_ERR_CAPACITY: return "KV cache capacity exhausted";
+    case CAS_ERR_CUDA: return "CUDA error";
+    case CAS_ERR_BUFFER: return "buffer or workspace too small";
+    case CAS_ERR_TIMEOUT: return "bounded device wait gave up";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int32_t cas_keep_from_ratio(double r) {
+  if (!(r >= 0.0)) return 0;
+  if (r >= 1.0) return CAS_BLK;
+  return (int32_t)std::floor(128.0 * r + 0.5);
+}
+
+namespace cas {
+int gemv_wait_status(bool clear);
+}  // namespace cas
+
+extern "C" int cas_device_status(void* stream) {
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return CAS_ERR_CUDA;
+  int s = cas::gemv_wait_status(true);
+  return s;
+}
+
+namespace cas {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int sm_count() {
+  static int cached = 0;
+  if (!cached) {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached = n > 0 ? n : 1;
+  }
+  return cached;
+}
+
+int launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? CAS_OK : CAS_ERR_CUDA;
+}
+
+int check_weights(const cas_weights* W) {
+  if (!W || !W->base) return CAS_ERR_INVALID;
+  if (W->N < 0 || W->K < 0 || (W->K % CAS_BLK)) return CAS_ERR_SHAPE;
+  if (W->p.variant != 1 && W->p.variant != 2) return CAS_ERR_INVALID;
+  if (W->p.keep_per_block < 0 || W->p.keep_per_block > CAS_BLK) return CAS_ERR_INVALID;
+  if (W->p.mant_bits < 0 || W->p.mant_bits > 7) return CAS_ERR_INVALID;
+  return CAS_OK;
+}
+
+WView make_view(const cas_weights* W) {
+  WView v{};
+  const uint8_t* b = (const uint8_t*)W->base;
+  auto w32 = [&](int s) { return (const uint32_t*)(b + W->off[s]); };
+  v.mask = w32(CAS_SEC_MASK);
+  v.ssm = w32(CAS_SEC_SPEC_SM);
+  v.sexp = w32(CAS_SEC_SPEC_EXP);
+  v.sidx = w32(CAS_SEC_SPEC_SBIDX);
+  v.smx = b + W->off[CAS_SEC_SPEC_MX];
+  v.sq = w32(CAS_SEC_SPEC_Q);
+  v.vlo = w32(CAS_SEC_VER_LO);
+  v.vd = w32(CAS_SEC_VER_D);
+  v.vdidx = w32(CAS_SEC_VER_D_SBIDX);
+  v.vres = w32(CAS_SEC_VER_RES);
+  v.vresidx = w32(CAS_SEC_VER_RES_SBIDX);
+  v.vpr = w32(CAS_SEC_VER_PR);
+  v.vexp = w32(CAS_SEC_VER_EXP);
+  v.vidx = w32(CAS_SEC_VER_SBIDX);
+  v.N = W->N;
+  v.K = W->K;
+  v.nbr = (int)(W->K / CAS_BLK);
+  v.nsr = (v.nbr + CAS_SB - 1) / CAS_SB;
+  v.nsb = W->N * v.nsr;
+  v.variant = W->p.variant;
+  v.k = W->p.keep_per_block;
+  v.m = W->p.mant_bits;
+  v.rec_sm = rec_words(v.k, v.m + 1);
+  v.rec_q = rec_words(v.k, v.m + 2);
+  v.rec_lo = rec_words(v.k, 7 - v.m);
+  v.rec_pr = rec_words(CAS_BLK - v.k, 8);
+  return v;
+}
+
+}  // namespace cas

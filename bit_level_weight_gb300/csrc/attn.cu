@@ -1,0 +1,333 @@
+// attn.cu - attention over the compressed KV cache.
+//
+// Draft decode (Cassandra blog review, section 3.1: the draft reads only the
+// speculation data, zero-filled): softmax(q K~^T / sqrt(128)) V~ with K~, V~
+// the draft values of the cache, then the exact bf16 tail tokens.
+// Verify: T queries over the exact cache (both streams merged, lossless),
+// causal among the last T tokens.
+//
+// Split over tokens (flash decoding): a CTA takes one (sequence, kv head,
+// 256-token chunk). Per 32-token step its 4 warps each decode one superblock
+// of K and of V into shared-memory tiles (fp32); then warp w runs the query
+// vectors w, w+4, ... of that kv head (GQA: the q heads h*G .. h*G+G-1, times
+// the T query tokens): scores with lane = token, online softmax, and the
+// P.V update with lane = 4 head dimensions. Chunk partials (max, sum,
+// unnormalised output) go to the workspace; a combine kernel merges them,
+// adds the tail tokens and normalises.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "kvview.cuh"
+#include "sbdecode.cuh"
+
+namespace cas {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kWarps = 4;
+constexpr int kChunk = 256;      // tokens per CTA
+constexpr int kStepTok = 32;     // tokens per step (4 superblocks)
+constexpr int kRow = CAS_BLK + 4;  // fp32 tile row stride
+constexpr int kPart = CAS_BLK + 2; // floats per partial: o[128], m, l
+constexpr int kMaxBatch = 8;
+constexpr int kMaxT = 16;
+
+constexpr int kQvPerCta = 32;  // query vectors per CTA (8 per warp)
+
+struct AttnArgs {
+  KvDev kv[kMaxBatch];
+  const uint16_t* q;  // [B][T][Hq][128]
+  float* part;        // [B][T][Hq][nchunk][kPart]
+  int B, T, Hq, G, nchunk, ngroups;
+  float scale;
+};
+
+__device__ __forceinline__ float warp_maxf(float v) {
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) v = fmaxf(v, __shfl_xor_sync(CAS_FULL, v, d));
+  return v;
+}
+
+// Decodes superblock sb of stream st (n tokens) into tile rows [row0, row0+8)
+// as fp32; rows of tokens that do not exist are zero.
+template <bool FULL>
+__device__ __forceinline__ void decode_sb_tile(const KvDev& d, int st, int64_t n, int64_t sb, float* tile, int row0,
+                                               const uint8_t* lut, SbScratch sc, int lane) {
+  int64_t nsb = (n + CAS_SB - 1) / CAS_SB;
+  uint32_t v[16];
+  int nb = 0;
+  if (sb < nsb) {
+    WView w = kv_stream_view(d, st, n);
+    SbInfo in = sb_prepare<1, FULL>(w, sb, lut, sc, lane);
+    nb = in.nb;
+    if (lane < 4 * nb) sb_rebuild_word<1, FULL>(w, in, sc, lane, v);
+  }
+  float* dst = tile + (row0 + (lane >> 2)) * kRow + 32 * (lane & 3);
+  if (lane < 4 * nb) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float4 f = make_float4(__uint_as_float(v[2 * i] << 16), __uint_as_float(v[2 * i] & 0xFFFF0000u),
+                             __uint_as_float(v[2 * i + 1] << 16), __uint_as_float(v[2 * i + 1] & 0xFFFF0000u));
+      reinterpret_cast<float4*>(dst)[i] = f;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) reinterpret_cast<float4*>(dst)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  __syncwarp();
+}
+
+template <bool FULL, int QPW>
+__global__ void __launch_bounds__(kThreads) attn_chunk_kernel(AttnArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  float* Kt = reinterpret_cast<float*>(smem);
+  float* Vt = Kt + kStepTok * kRow;
+  float* Qs = Vt + kStepTok * kRow;  // [kQvPerCta][128], pre-scaled
+  uint8_t* lutK = reinterpret_cast<uint8_t*>(Qs + kQvPerCta * CAS_BLK);
+  uint8_t* lutV = lutK + 256;
+  uint8_t* scr = lutV + 256;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  SbScratch sc{scr + warp * 2048, scr + warp * 2048 + 1024, nullptr};
+  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z / a.ngroups;
+  const int qv0 = (blockIdx.z % a.ngroups) * kQvPerCta;
+  const KvDev& d = a.kv[b];
+  const int H = d.H, T = a.T, G = a.G, nq = min(T * G - qv0, kQvPerCta);
+  const int64_t n = *(volatile const int64_t*)&kv_state(d)->n_tokens;
+  const int64_t t_begin = (int64_t)chunk * kChunk;
+  const int64_t t_end = min(n, t_begin + kChunk);
+
+  // query vectors qv = j * G + g (query token j, head h*G+g), scaled; this
+  // CTA takes qv0 .. qv0 + nq - 1 (local index qv - qv0)
+  for (int i = threadIdx.x; i < nq * CAS_BLK; i += kThreads) {
+    int qv = qv0 + i / CAS_BLK, dd = i % CAS_BLK;
+    int j = qv / G, g = qv % G;
+    Qs[i] = bf2f(a.q[(((int64_t)b * T + j) * a.Hq + h * G + g) * CAS_BLK + dd]) * a.scale;
+  }
+  for (int i = threadIdx.x; i < 256; i += kThreads) {
+    lutK[i] = kv_exp_of_rank(d, h)[i];
+    lutV[i] = kv_exp_of_rank(d, H + h)[i];
+  }
+  __syncthreads();
+
+  float m_[QPW], l_[QPW], o_[QPW][4];
+#pragma unroll
+  for (int i = 0; i < QPW; ++i) {
+    m_[i] = -INFINITY;
+    l_[i] = 0.f;
+    o_[i][0] = o_[i][1] = o_[i][2] = o_[i][3] = 0.f;
+  }
+  for (int64_t t0 = t_begin; t0 < t_end; t0 += kStepTok) {
+    int64_t sb = t0 / CAS_SB + warp;
+    decode_sb_tile<FULL>(d, h, n, sb, Kt, warp * CAS_SB, lutK, sc, lane);
+    decode_sb_tile<FULL>(d, H + h, n, sb, Vt, warp * CAS_SB, lutV, sc, lane);
+    __syncthreads();
+    const int64_t tok = t0 + lane;
+    // scores: lane = token
+    float s[QPW];
+#pragma unroll
+    for (int i = 0; i < QPW; ++i) s[i] = 0.f;
+    const float4* krow = reinterpret_cast<const float4*>(Kt + lane * kRow);
+    for (int c = 0; c < CAS_BLK / 4; ++c) {
+      float4 k4 = krow[c];
+#pragma unroll
+      for (int i = 0; i < QPW; ++i) {
+        int qv = warp + kWarps * i;
+        if (qv < nq) {
+          float4 q4 = reinterpret_cast<const float4*>(Qs + qv * CAS_BLK)[c];
+          s[i] = fmaf(q4.x, k4.x, fmaf(q4.y, k4.y, fmaf(q4.z, k4.z, fmaf(q4.w, k4.w, s[i]))));
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < QPW; ++i) {
+      int qv = warp + kWarps * i;
+      if (qv >= nq) continue;
+      int64_t last = FULL ? n - T + (qv0 + qv) / G : n - 1;  // causal among the last T tokens (verify)
+      float si = (tok < t_end && tok <= last) ? s[i] : -INFINITY;
+      float mx = warp_maxf(si);
+      float mnew = fmaxf(m_[i], mx);
+      float p = (si == -INFINITY) ? 0.f : __expf(si - mnew);
+      float corr = (m_[i] == -INFINITY) ? 0.f : __expf(m_[i] - mnew);
+      if (mnew == -INFINITY) corr = 1.f;
+      l_[i] = l_[i] * corr + warp_sumf(p);
+      m_[i] = mnew;
+      float acc0 = o_[i][0] * corr, acc1 = o_[i][1] * corr, acc2 = o_[i][2] * corr, acc3 = o_[i][3] * corr;
+      for (int t = 0; t < kStepTok; ++t) {
+        float pt = __shfl_sync(CAS_FULL, p, t);
+        float4 v4 = reinterpret_cast<const float4*>(Vt + t * kRow)[lane];
+        acc0 = fmaf(pt, v4.x, acc0);
+        acc1 = fmaf(pt, v4.y, acc1);
+        acc2 = fmaf(pt, v4.z, acc2);
+        acc3 = fmaf(pt, v4.w, acc3);
+      }
+      o_[i][0] = acc0; o_[i][1] = acc1; o_[i][2] = acc2; o_[i][3] = acc3;
+    }
+    __syncthreads();
+  }
+  // partials
+#pragma unroll
+  for (int i = 0; i < QPW; ++i) {
+    int qv = warp + kWarps * i;
+    if (qv >= nq) continue;
+    int j = (qv0 + qv) / G, g = (qv0 + qv) % G;
+    float* dst = a.part + ((((int64_t)b * T + j) * a.Hq + h * G + g) * a.nchunk + chunk) * kPart;
+    reinterpret_cast<float2*>(dst)[2 * lane] = make_float2(o_[i][0], o_[i][1]);
+    reinterpret_cast<float2*>(dst)[2 * lane + 1] = make_float2(o_[i][2], o_[i][3]);
+    if (lane == 0) {
+      dst[CAS_BLK] = m_[i];
+      dst[CAS_BLK + 1] = l_[i];
+    }
+  }
+}
+
+struct CombineArgs {
+  const float* part;
+  const uint16_t* q;       // [B][T][Hq][128]
+  const uint16_t* tail_k;  // [B][n_tail][Hkv][128] or null
+  const uint16_t* tail_v;
+  float* o;                // [B][T][Hq][128]
+  const int64_t* ntok[kMaxBatch];
+  int T, Hq, Hkv, G, nchunk, n_tail;
+  float scale;
+};
+
+// One CTA of 128 threads per (sequence, query token, q head): thread = dim.
+__global__ void __launch_bounds__(128) attn_combine_kernel(CombineArgs a) {
+  __shared__ float red[4];
+  __shared__ float ts[kMaxT];
+  const int hq = blockIdx.x, j = blockIdx.y, b = blockIdx.z, dd = threadIdx.x;
+  const int lane = dd & 31, warp = dd >> 5;
+  const int64_t n = *(volatile const int64_t*)a.ntok[b];
+  const int used = (int)min((int64_t)a.nchunk, (n + kChunk - 1) / kChunk);
+  const float* P = a.part + (((int64_t)b * a.T + j) * a.Hq + hq) * a.nchunk * kPart;
+  const int hk = hq / a.G;
+  // tail scores (exact bf16 tokens)
+  float qd = bf2f(a.q[(((int64_t)b * a.T + j) * a.Hq + hq) * CAS_BLK + dd]) * a.scale;
+  for (int t = 0; t < a.n_tail; ++t) {
+    float kd = bf2f(a.tail_k[(((int64_t)b * a.n_tail + t) * a.Hkv + hk) * CAS_BLK + dd]);
+    float s = warp_sumf(qd * kd);
+    if (lane == 0) red[warp] = s;
+    __syncthreads();
+    if (dd == 0) ts[t] = red[0] + red[1] + red[2] + red[3];
+    __syncthreads();
+  }
+  float M = -INFINITY;
+  for (int c = 0; c < used; ++c) M = fmaxf(M, P[c * kPart + CAS_BLK]);
+  for (int t = 0; t < a.n_tail; ++t) M = fmaxf(M, ts[t]);
+  float L = 0.f, O = 0.f;
+  for (int c = 0; c < used; ++c) {
+    float mc = P[c * kPart + CAS_BLK];
+    if (mc == -INFINITY) continue;
+    float w = __expf(mc - M);
+    L += P[c * kPart + CAS_BLK + 1] * w;
+    O += P[c * kPart + dd] * w;
+  }
+  for (int t = 0; t < a.n_tail; ++t) {
+    float w = __expf(ts[t] - M);
+    L += w;
+    O += w * bf2f(a.tail_v[(((int64_t)b * a.n_tail + t) * a.Hkv + hk) * CAS_BLK + dd]);
+  }
+  a.o[(((int64_t)b * a.T + j) * a.Hq + hq) * CAS_BLK + dd] = L > 0.f ? O / L : 0.f;
+}
+
+size_t chunk_smem() { return (size_t)2 * kStepTok * kRow * 4 + (size_t)kQvPerCta * CAS_BLK * 4 + 512 + kWarps * 2048; }
+
+template <bool FULL, int QPW>
+int launch_chunk(const AttnArgs& a, int Hkv, cudaStream_t st) {
+  size_t smem = chunk_smem();
+  auto kern = attn_chunk_kernel<FULL, QPW>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return CAS_ERR_CUDA;
+  dim3 grid(a.nchunk, Hkv, a.B * a.ngroups);
+  kern<<<grid, kThreads, smem, st>>>(a);
+  return launch_status();
+}
+
+int nchunks(int64_t max_tokens) { return (int)((max_tokens + kChunk - 1) / kChunk); }
+
+int run_attn(bool full, const cas_kv* const* kv, int B, const uint16_t* q, int T, int Hq, const uint16_t* tail_k,
+             const uint16_t* tail_v, int n_tail, float* o, void* ws, uint64_t ws_bytes, cudaStream_t st) {
+  if (!kv || B < 1 || B > kMaxBatch || !q || !o || T < 1 || T > kMaxT || Hq < 1 || !aligned16(q) || !aligned16(o))
+    return CAS_ERR_INVALID;
+  if (n_tail < 0 || n_tail > kMaxT || (n_tail > 0 && (!tail_k || !tail_v))) return CAS_ERR_INVALID;
+  int Hkv = 0;
+  int64_t Tm = 0;
+  AttnArgs a{};
+  CombineArgs c{};
+  for (int i = 0; i < B; ++i) {
+    int s = check_kv(kv[i]);
+    if (s) return s;
+    if (i == 0) Hkv = kv[i]->n_kv_heads;
+    if (kv[i]->n_kv_heads != Hkv || kv[i]->p.keep_per_block != kv[0]->p.keep_per_block ||
+        kv[i]->p.mant_bits != kv[0]->p.mant_bits)
+      return CAS_ERR_INVALID;
+    Tm = std::max(Tm, kv[i]->max_tokens);
+    a.kv[i] = make_kv_dev(kv[i]);
+    c.ntok[i] = (const int64_t*)((uint8_t*)kv[i]->base + kv[i]->off[CAS_KV_STATE]);
+  }
+  if (Hq % Hkv) return CAS_ERR_INVALID;
+  int G = Hq / Hkv;
+  if (T * G > kWarps * 16) return CAS_ERR_INVALID;
+  uint64_t need = cas_attn_workspace_bytes(B, Hq, T, Tm);
+  if (!ws || ws_bytes < need || !aligned16(ws)) return CAS_ERR_BUFFER;
+  a.q = q;
+  a.part = (float*)ws;
+  a.B = B;
+  a.T = T;
+  a.Hq = Hq;
+  a.G = G;
+  a.nchunk = nchunks(Tm);
+  a.scale = 1.0f / std::sqrt((float)CAS_BLK);
+  a.ngroups = (T * G + kQvPerCta - 1) / kQvPerCta;
+  int qpw = (std::min(T * G, kQvPerCta) + kWarps - 1) / kWarps;
+  int s;
+  if (!full) {
+    if (qpw <= 1) s = launch_chunk<false, 1>(a, Hkv, st);
+    else if (qpw <= 4) s = launch_chunk<false, 4>(a, Hkv, st);
+    else s = launch_chunk<false, 8>(a, Hkv, st);
+  } else {
+    if (qpw <= 1) s = launch_chunk<true, 1>(a, Hkv, st);
+    else if (qpw <= 4) s = launch_chunk<true, 4>(a, Hkv, st);
+    else s = launch_chunk<true, 8>(a, Hkv, st);
+  }
+  if (s) return s;
+  c.part = a.part;
+  c.q = q;
+  c.tail_k = tail_k;
+  c.tail_v = tail_v;
+  c.o = o;
+  c.T = T;
+  c.Hq = Hq;
+  c.Hkv = Hkv;
+  c.G = G;
+  c.nchunk = a.nchunk;
+  c.n_tail = full ? 0 : n_tail;
+  c.scale = a.scale;
+  attn_combine_kernel<<<dim3(Hq, T, B), 128, 0, st>>>(c);
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace cas
+
+using namespace cas;
+
+extern "C" uint64_t cas_attn_workspace_bytes(int B, int Hq, int T, int64_t max_tokens) {
+  if (B < 1 || Hq < 1 || T < 1 || max_tokens < 1) return 0;
+  return (uint64_t)B * T * Hq * nchunks(max_tokens) * kPart * sizeof(float);
+}
+
+extern "C" int cas_draft_attn_decode(const cas_kv* const* kv, int batch, const uint16_t* q, int n_q_heads,
+                                     const uint16_t* tail_k, const uint16_t* tail_v, int n_tail, float* o,
+                                     void* workspace, uint64_t workspace_bytes, void* stream) {
+  return run_attn(false, kv, batch, q, 1, n_q_heads, tail_k, tail_v, n_tail, o, workspace, workspace_bytes,
+                  (cudaStream_t)stream);
+}
+
+extern "C" int cas_verify_attn(const cas_kv* const* kv, int batch, const uint16_t* q, int T, int n_q_heads, float* o,
+                               void* workspace, uint64_t workspace_bytes, void* stream) {
+  return run_attn(true, kv, batch, q, T, n_q_heads, nullptr, nullptr, 0, o, workspace, workspace_bytes,
+                  (cudaStream_t)stream);
+}

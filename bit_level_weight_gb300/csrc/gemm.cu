@@ -1,0 +1,174 @@
+// gemm.cu - verify: lossless reconstruct + GEMM, Y[t][n] = sum_k W[n][k] X[t][k].
+//
+// The target merges speculation and verification data back to the original
+// bits (Cassandra blog review, section 3.1) and runs T = draft length + 1
+// tokens at once, so the product is a small dense contraction. A CTA takes a
+// tile of 16 rows by one superblock column (up to 1024 k): its 8 warps
+// rebuild the 16 row-superblocks bit-exactly into a shared-memory tile, then
+// split the k16 steps of the tile among themselves on the tensor cores
+// (mma m16n8k16, bf16 inputs, fp32 accumulation; T <= 8 uses one n8 tile, T <= 16
+// two). Warp partials are summed in shared memory and added to Y with fp32
+// atomics; Y is cleared first.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "sbdecode.cuh"
+
+namespace cas {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kRows = 16;
+constexpr int kTileStride = CAS_BLK * CAS_SB + 8;  // bf16 per tile row (+8: conflict-free ldmatrix)
+
+struct GemmArgs {
+  WView w;
+  Lut lut;
+  const uint16_t* X;
+  float* Y;
+  int T;
+};
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t r[4], const void* p) {
+  uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+__device__ __forceinline__ void mma_bf16(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int VAR, int NT>
+__global__ void __launch_bounds__(kThreads) verify_gemm_kernel(GemmArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const WView& w = a.w;
+  uint16_t* tile = reinterpret_cast<uint16_t*>(smem);                       // [16][kTileStride]
+  float* red = reinterpret_cast<float*>(smem + kRows * kTileStride * 2);    // [8][16][16]
+  uint8_t* s_lut = reinterpret_cast<uint8_t*>(red + kWarps * 256);
+  uint8_t* scratch = s_lut + 256;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  SbScratch sc{scratch + warp * (2048 + kResWords * 4), scratch + warp * (2048 + kResWords * 4) + 1024,
+               reinterpret_cast<uint32_t*>(scratch + warp * (2048 + kResWords * 4) + 2048)};
+  for (int i = threadIdx.x; i < 256; i += kThreads) s_lut[i] = a.lut.v[i];
+  __syncthreads();
+
+  const int64_t ntile = (w.N + kRows - 1) / kRows;
+  const int64_t ntasks = ntile * w.nsr;
+  const int K = (int)w.K, T = a.T;
+  const uint32_t* X32 = reinterpret_cast<const uint32_t*>(a.X);
+  for (int64_t task = blockIdx.x; task < ntasks; task += gridDim.x) {
+    int64_t rt = task / w.nsr;
+    int j = (int)(task % w.nsr);
+    int nb = min(CAS_SB, w.nbr - CAS_SB * j);
+    // 1) rebuild rows rt*16 + {warp, warp + 8}
+    for (int r = warp; r < kRows; r += kWarps) {
+      int64_t n = rt * kRows + r;
+      uint4* dst = reinterpret_cast<uint4*>(tile + r * kTileStride + 32 * lane);
+      if (n < w.N) {
+        SbInfo in = sb_prepare<VAR, true>(w, n * w.nsr + j, s_lut, sc, lane);
+        if (lane < 4 * nb) {
+          uint32_t v[16];
+          sb_rebuild_word<VAR, true>(w, in, sc, lane, v);
+          dst[0] = make_uint4(v[0], v[1], v[2], v[3]);
+          dst[1] = make_uint4(v[4], v[5], v[6], v[7]);
+          dst[2] = make_uint4(v[8], v[9], v[10], v[11]);
+          dst[3] = make_uint4(v[12], v[13], v[14], v[15]);
+        }
+        __syncwarp();
+      } else if (lane < 4 * nb) {
+        uint4 z = make_uint4(0, 0, 0, 0);
+        dst[0] = z; dst[1] = z; dst[2] = z; dst[3] = z;
+      }
+    }
+    __syncthreads();
+    // 2) tensor-core product of the tile with X[:, tile columns]
+    float c[NT][4];
+#pragma unroll
+    for (int q = 0; q < NT; ++q) c[q][0] = c[q][1] = c[q][2] = c[q][3] = 0.f;
+    const int g = lane >> 2, tq = lane & 3;
+    const int ksteps = nb * (CAS_BLK / 16);
+    for (int ks = warp; ks < ksteps; ks += kWarps) {
+      uint32_t af[4];
+      ldmatrix_x4(af, tile + (lane & 15) * kTileStride + ks * 16 + (lane >> 4) * 8);
+      int col = CAS_BLK * CAS_SB * j + ks * 16 + 2 * tq;
+#pragma unroll
+      for (int q = 0; q < NT; ++q) {
+        int tok = q * 8 + g;
+        uint32_t b0 = 0, b1 = 0;
+        if (tok < T) {
+          b0 = __ldg(X32 + ((int64_t)tok * K + col) / 2);
+          b1 = __ldg(X32 + ((int64_t)tok * K + col + 8) / 2);
+        }
+        mma_bf16(c[q], af, b0, b1);
+      }
+    }
+    // 3) reduce warp partials: red[warp][row][token]
+    float* rw = red + warp * 256;
+#pragma unroll
+    for (int q = 0; q < NT; ++q) {
+      rw[g * 16 + q * 8 + 2 * tq] = c[q][0];
+      rw[g * 16 + q * 8 + 2 * tq + 1] = c[q][1];
+      rw[(g + 8) * 16 + q * 8 + 2 * tq] = c[q][2];
+      rw[(g + 8) * 16 + q * 8 + 2 * tq + 1] = c[q][3];
+    }
+    __syncthreads();
+    {
+      int r = threadIdx.x >> 4, tt = threadIdx.x & 15;
+      int64_t n = rt * kRows + r;
+      if (tt < T && tt < NT * 8 && n < w.N) {
+        float sum = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < kWarps; ++ww) sum += red[ww * 256 + r * 16 + tt];
+        atomicAdd(a.Y + (int64_t)tt * w.N + n, sum);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+template <int VAR, int NT>
+int launch(const GemmArgs& a, cudaStream_t st) {
+  size_t smem = (size_t)kRows * kTileStride * 2 + kWarps * 256 * 4 + 256 + kWarps * (2048 + kResWords * 4);
+  auto kern = verify_gemm_kernel<VAR, NT>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return CAS_ERR_CUDA;
+  int per_sm = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+  per_sm = std::max(per_sm, 1);
+  int64_t ntasks = (a.w.N + kRows - 1) / kRows * a.w.nsr;
+  int g = (int)std::max<int64_t>(1, std::min<int64_t>(ntasks, (int64_t)sm_count() * per_sm));
+  kern<<<g, kThreads, smem, st>>>(a);
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace cas
+
+using namespace cas;
+
+extern "C" int cas_verify_gemm(const cas_weights* W, const uint16_t* X, int T, float* Y, void* stream) {
+  int s = check_weights(W);
+  if (s) return s;
+  if (T < 1 || T > 16) return CAS_ERR_INVALID;
+  if (W->N == 0) return CAS_OK;  // nothing to write (Y may be an empty tensor)
+  if (!X || !Y || !aligned16(X) || !aligned16(Y)) return CAS_ERR_INVALID;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(Y, 0, sizeof(float) * T * W->N, st) != cudaSuccess) return CAS_ERR_CUDA;
+  if (W->K == 0) return CAS_OK;
+  GemmArgs a;
+  a.w = make_view(W);
+  for (int i = 0; i < 256; ++i) a.lut.v[i] = W->exp_of_rank[i];
+  a.X = X;
+  a.Y = Y;
+  a.T = T;
+  bool v1 = W->p.variant == 1;
+  if (T <= 8) return v1 ? launch<1, 1>(a, st) : launch<2, 1>(a, st);
+  return v1 ? launch<1, 2>(a, st) : launch<2, 2>(a, st);
+}

@@ -1,0 +1,251 @@
+/*
+ * cas.h - C ABI of libcas, a GB300 (sm_103a) implementation of the Cassandra
+ * bit-level split of bf16 weights and KV cache into speculation data (read by
+ * the draft) and verification data (which completes the value).
+ *
+ * Method sources, cited per entry point below:
+ *   [B3.1] Cassandra blog review (marsggbo.github.io/blog/2026/20260722-cassandra),
+ *          section 3.1 - value pruning and mantissa truncation split every value
+ *          into speculation and verification data; the draft zero-fills, the
+ *          target merges both losslessly; the draft runs full-size FLOPs and
+ *          saves only bandwidth.
+ *   [B3.2] same page, section 3.2 - exponent coding: frequency-ranked unary codes
+ *          (Cassandra-1, lossless) or MX shared exponents (Cassandra-2).
+ *   [B3.3] same page, section 3.3 - the KV cache is produced at inference time
+ *          and encoded online.
+ *   [F11]  Cassandra paper (arXiv 2605.26558), Fig. 11 - superblock-based data
+ *          management.
+ *   [ABS]  Cassandra paper abstract - draft built from the most salient values
+ *          of weights and KV cache, verified at full precision.
+ *
+ * Conventions for every entry point:
+ *   - Tensors are DEVICE pointers unless stated. bf16 values travel as uint16_t
+ *     bit patterns. Row-major. Pointers to bf16 / float data must be 16-byte
+ *     aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - The library never allocates or frees device memory. Buffers and
+ *     workspaces are owned by the caller; their sizes come from the *_plan /
+ *     *_workspace_bytes calls.
+ *   - Entry points are asynchronous on `stream` unless marked "synchronises".
+ *   - Argument errors return at once and launch nothing. CAS_ERR_CUDA reports a
+ *     launch or runtime error. Data errors found on the device while the KV
+ *     cache is appended (capacity, non-finite input) are sticky and are read
+ *     back by cas_kv_status.
+ */
+#ifndef CAS_H_
+#define CAS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CAS_OK = 0,
+  CAS_ERR_INVALID = -1,   /* bad argument (null pointer, range, alignment) */
+  CAS_ERR_SHAPE = -2,     /* K (or head_dim) not a multiple of 128          */
+  CAS_ERR_NONFINITE = -3, /* NaN or Inf in a tensor to encode               */
+  CAS_ERR_CAPACITY = -4,  /* KV cache full (tokens or code stream words)    */
+  CAS_ERR_CUDA = -5,      /* CUDA launch / runtime error                     */
+  CAS_ERR_BUFFER = -6,    /* buffer or workspace smaller than required       */
+  CAS_ERR_TIMEOUT = -8    /* a bounded device-side wait gave up              */
+} cas_status;
+
+/* Encoding parameters of one tensor.
+ *   variant        1 = Cassandra-1 (unary exponent codes), 2 = Cassandra-2
+ *                  (MX shared exponent per 32 positions) [B3.2]
+ *   keep_per_block k in [0,128]: values kept per 128-element block by magnitude
+ *                  [B3.1]; cas_keep_from_ratio(r) = floor(128 r + 0.5)
+ *   mant_bits      m in [0,7]: mantissa bits the draft keeps [B3.1]          */
+typedef struct {
+  int32_t variant;
+  int32_t keep_per_block;
+  int32_t mant_bits;
+} cas_params;
+
+/* Section indices of an encoded tensor (one buffer, each section 256-byte
+ * aligned, speculation sections first so the draft reads a compact prefix). */
+enum {
+  CAS_SEC_MASK = 0,        /* u32[nblk][4]: bit p set when position p is kept        */
+  CAS_SEC_SPEC_SM,         /* C-1: per block ceil(k(m+1)/32) words, field (s<<m)|f_hi */
+  CAS_SEC_SPEC_EXP,        /* C-1: unary codes of kept exponents, MSB-first words     */
+  CAS_SEC_SPEC_SBIDX,      /* C-1: u32[nsb+1] word offsets of superblocks             */
+  CAS_SEC_SPEC_MX,         /* C-2: u8[nblk][4] shared exponent per 32-position group  */
+  CAS_SEC_SPEC_Q,          /* C-2: per block ceil(k(m+2)/32) words, (s<<(m+1))|q      */
+  CAS_SEC_VER_LO,          /* C-1: per block ceil(k(7-m)/32) words, cut mantissa bits */
+  CAS_SEC_VER_D,           /* C-2: unary codes of exponent distance d, MSB-first      */
+  CAS_SEC_VER_D_SBIDX,     /* C-2: u32[nsb+1]                                         */
+  CAS_SEC_VER_RES,         /* C-2: residual significand bits, LSB-first               */
+  CAS_SEC_VER_RES_SBIDX,   /* C-2: u32[nsb+1]                                         */
+  CAS_SEC_VER_PR,          /* both: per block ceil((128-k)/4) words, bytes (s<<7)|f   */
+  CAS_SEC_VER_EXP,         /* both: unary codes of pruned exponents, MSB-first        */
+  CAS_SEC_VER_SBIDX,       /* both: u32[nsb+1]                                        */
+  CAS_NSECT
+};
+
+/* Descriptor of one encoded weight tensor W[N][K] (K % 128 == 0). Plain old
+ * data, owned by the caller, filled by cas_encode_weights_plan; `base` points
+ * into the caller's device buffer once cas_encode_weights has run. A block is
+ * 128 consecutive elements of a row; a superblock is 8 consecutive blocks of
+ * one row (the last one of a row may be shorter) [F11]. */
+typedef struct cas_weights {
+  int64_t N, K;
+  cas_params p;
+  int32_t reserved0;
+  uint8_t exp_of_rank[256]; /* rank table, exponents by (count desc, exp asc) */
+  uint8_t rank_of_exp[256];
+  void* base;               /* device buffer holding every section            */
+  uint64_t bytes;           /* bytes of the buffer the sections occupy        */
+  uint64_t off[CAS_NSECT];  /* section byte offsets from base                 */
+  uint64_t len[CAS_NSECT];  /* section byte lengths                           */
+} cas_weights;
+
+const char* cas_status_str(int status);
+
+/* Reads and clears the flags that bounded device-side waits set (a TMA
+ * staging copy that did not complete within its spin limit). Synchronises
+ * `stream`. Returns CAS_OK or CAS_ERR_TIMEOUT (CAS_ERR_CUDA on a runtime
+ * error). */
+int cas_device_status(void* stream);
+int32_t cas_keep_from_ratio(double ratio);
+/* Device-side scratch that cas_encode_weights_plan / cas_encode_weights need
+ * for a tensor of N x K (histogram, per-superblock lengths, scan). */
+uint64_t cas_encode_workspace_bytes(int64_t N, int64_t K);
+
+/* Plans the encoding of W [B3.1][B3.2]: counts the exponent histogram on the
+ * device, builds the rank table (count desc, exponent asc; unseen exponents
+ * last), selects the kept values of every block and sizes every section.
+ * Fills *desc (base = NULL) and *bytes_needed. Synchronises `stream`.
+ * Errors: CAS_ERR_SHAPE if K % 128, CAS_ERR_NONFINITE if W holds NaN/Inf,
+ * CAS_ERR_BUFFER if workspace_bytes < cas_encode_workspace_bytes(N, K). */
+int cas_encode_weights_plan(const uint16_t* W, int64_t N, int64_t K, cas_params p,
+                            cas_weights* desc, uint64_t* bytes_needed, void* workspace,
+                            uint64_t workspace_bytes, void* stream);
+
+/* Writes every section of W into buf (>= desc->bytes bytes, 256-byte aligned)
+ * with the rank table in *desc, sets desc->base = buf. Asynchronous. The same
+ * W and workspace as the plan must be passed. Output is byte-identical to the
+ * format definition (padding bits zero). */
+int cas_encode_weights(const uint16_t* W, cas_weights* desc, void* buf, uint64_t buf_bytes,
+                       void* workspace, uint64_t workspace_bytes, void* stream);
+
+/* Draft GEMV [B3.1]: y[v][n] = sum_k D(W)[n][k] * x[v][k] for v < nvec (1..4),
+ * where D(W) is the zero-filled speculation value (pruned -> 0, kept ->
+ * mantissa truncated, Cassandra-2 -> shared-exponent grid). Reads only the
+ * speculation sections. x: bf16 [nvec][K]; y: fp32 [nvec][N], overwritten.
+ * fp32 accumulation; summation order is unspecified. */
+int cas_draft_gemv(const cas_weights* W, const uint16_t* x, int nvec, float* y, void* stream);
+
+/* Verify GEMM [B3.1]: Y[t][n] = sum_k W[n][k] * X[t][k] for t < T (1..16)
+ * with W rebuilt bit-exactly from both streams, on tensor cores with fp32
+ * accumulation. X: bf16 [T][K]; Y: fp32 [T][N], overwritten. */
+int cas_verify_gemm(const cas_weights* W, const uint16_t* X, int T, float* Y, void* stream);
+
+/* Materialises the draft values D(W) as bf16 [N][K] (test path) [B3.1]. */
+int cas_decode_draft(const cas_weights* W, uint16_t* out, void* stream);
+/* Rebuilds the original bf16 bits of W [N][K] from both streams [B3.1]. */
+int cas_reconstruct(const cas_weights* W, uint16_t* out, void* stream);
+
+/* ------------------------------------------------------------------ KV cache
+ * One cas_kv holds the K and V cache of one (sequence, layer): n_kv_heads
+ * heads of head_dim 128, one 128-element block per token, head and K|V.
+ * Each (head, K|V) stream has its own rank table, counted over calibration
+ * tokens and then frozen [B3.3]. A KV superblock is 8 consecutive tokens of
+ * one stream. Only Cassandra-1 is supported for the KV cache.
+ * The device state (n_tokens, per-stream code tails, sticky status) lives in
+ * the caller's buffer, so appends, truncations and attention calls need no
+ * host round trip. */
+/* Sections of a KV buffer. Streams are numbered kv * n_kv_heads + head
+ * (kv 0 = K, 1 = V); section i of stream st starts at off[i] + st * stride[i].
+ * STATE holds the device state: int64 n_tokens, int32 sticky status, two
+ * internal counters, then u64 spec-code tails [S] and verification-code tails
+ * [S] (S = 2 * n_kv_heads). TABLES holds per stream exp_of_rank[256] then
+ * rank_of_exp[256]. The other sections are those of an encoded weight tensor
+ * with one row per stream and one block per token, sized for max_tokens. */
+enum {
+  CAS_KV_STATE = 0,
+  CAS_KV_TABLES,
+  CAS_KV_MASK,
+  CAS_KV_SPEC_SM,
+  CAS_KV_SPEC_EXP,
+  CAS_KV_SPEC_SBIDX,
+  CAS_KV_VER_LO,
+  CAS_KV_VER_PR,
+  CAS_KV_VER_EXP,
+  CAS_KV_VER_SBIDX,
+  CAS_KV_NSECT
+};
+
+typedef struct cas_kv {
+  int32_t n_kv_heads, head_dim;
+  cas_params p;
+  int64_t max_tokens;
+  uint64_t cap_spec_words;  /* code-stream capacity per stream, u32 words */
+  uint64_t cap_ver_words;
+  void* base;               /* device buffer */
+  uint64_t bytes;
+  uint64_t off[16];         /* section offsets (see cas_kv_plan)          */
+  uint64_t stride[16];      /* bytes between consecutive streams          */
+} cas_kv;
+
+/* Bytes of device buffer one cas_kv needs: est_bits_per_code is the planned
+ * mean unary code length of both code streams; each stream gets that many bits
+ * per code plus one word of alignment slack per superblock. Pruned (small)
+ * values have more spread exponents and longer codes than kept ones: on
+ * N(0,1) x LogNormal(0,0.5) K/V with k = 64 they average about 4 to 5 bits,
+ * so 6.0 leaves room; an append that would overflow sets CAS_ERR_CAPACITY. */
+int cas_kv_plan(int n_kv_heads, int64_t max_tokens, cas_params p, double est_bits_per_code,
+                uint64_t* bytes);
+
+/* Lays out *kv in buf and builds the rank table of each (head, K|V) stream from
+ * the n_calib calibration tokens calib_k / calib_v (bf16 [n_calib][H][128]).
+ * The cache starts empty (n_tokens = 0); calibration tokens are not appended.
+ * Synchronises `stream`. Errors: CAS_ERR_NONFINITE for NaN/Inf calibration. */
+int cas_kv_init(cas_kv* kv, void* buf, uint64_t bytes, int n_kv_heads, int64_t max_tokens,
+                cas_params p, double est_bits_per_code, const uint16_t* calib_k,
+                const uint16_t* calib_v, int64_t n_calib, void* stream);
+
+/* Online KV encoding [B3.3]: appends T tokens, k_new / v_new bf16 [T][H][128],
+ * in order. On the device: if the tokens or code words would exceed capacity,
+ * or a value is NaN/Inf, nothing is written and the sticky status is set. */
+int cas_encode_kv_append(cas_kv* kv, const uint16_t* k_new, const uint16_t* v_new, int T,
+                         void* stream);
+
+/* Rolls the cache back to its first n_tokens tokens (rejected draft tokens).
+ * n_tokens larger than the current count leaves the cache unchanged. */
+int cas_kv_truncate(cas_kv* kv, int64_t n_tokens, void* stream);
+
+/* Reads the device state. Synchronises `stream`. Returns the sticky device
+ * status (CAS_OK, CAS_ERR_CAPACITY or CAS_ERR_NONFINITE) and the token count. */
+int cas_kv_status(const cas_kv* kv, int64_t* n_tokens, void* stream);
+
+/* Clears the sticky device status. */
+int cas_kv_clear_status(cas_kv* kv, void* stream);
+
+/* Workspace bytes of cas_draft_attn_decode / cas_verify_attn for a batch. */
+uint64_t cas_attn_workspace_bytes(int batch, int n_q_heads, int T, int64_t max_tokens);
+
+/* Draft attention decode [B3.1][B3.3]: for each sequence b and query head h,
+ * o = softmax(q K~^T / sqrt(128)) V~ over the speculation KV of kv[b] (pruned
+ * entries zero, kept mantissas truncated) followed by n_tail exact bf16 tail
+ * tokens (the draft tokens of this step). GQA: head h reads kv head
+ * h / (n_q_heads / n_kv_heads). q: bf16 [batch][n_q_heads][128];
+ * tail_k, tail_v: bf16 [batch][n_tail][n_kv_heads][128] (NULL when n_tail = 0);
+ * o: fp32 [batch][n_q_heads][128]. Softmax in fp32. */
+int cas_draft_attn_decode(const cas_kv* const* kv, int batch, const uint16_t* q, int n_q_heads,
+                          const uint16_t* tail_k, const uint16_t* tail_v, int n_tail, float* o,
+                          void* workspace, uint64_t workspace_bytes, void* stream);
+
+/* Verify attention [B3.1]: T query tokens per sequence over the exact KV
+ * (both streams merged), the T queries being the last T tokens of the cache:
+ * query j sees every earlier token and the new tokens 0..j.
+ * q: bf16 [batch][T][n_q_heads][128]; o: fp32 [batch][T][n_q_heads][128]. */
+int cas_verify_attn(const cas_kv* const* kv, int batch, const uint16_t* q, int T, int n_q_heads,
+                    float* o, void* workspace, uint64_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CAS_H_ */

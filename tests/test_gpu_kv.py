@@ -1,0 +1,238 @@
+"""GPU parity of the compressed KV cache and the attention kernels.
+
+Online append: every stream byte-exact with the oracle's encoding of the same
+tokens (a stream = one row whose blocks are the tokens); chunked appends equal
+token-by-token appends; truncate + re-append equals a direct append; data
+faults set the sticky status and write nothing. Attention: within
+2e-3 * sum_t p_t |v_t| of the float64 oracle over the oracle's draft (resp.
+exact) K and V.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+D = 128
+
+
+@pytest.fixture(scope="module")
+def cas():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import bit_level_weight_gb300 as cas
+    from bit_level_weight_gb300 import build
+    build.build()
+    return cas
+
+
+def np16(t):
+    return t.cpu().numpy().view(np.uint16)
+
+
+def make_tokens(T, H, layer=0, seed=0):
+    K = synthetic.kv_tokens(T, H, seed=seed, scales=synthetic.kv_scales(layer, H, 0))
+    V = synthetic.kv_tokens(T, H, seed=seed + 1, scales=synthetic.kv_scales(layer, H, 1))
+    return K, V
+
+
+def new_cache(cas, H, Tm, K, V, k=64, m=3, calib=16, est=6.0):
+    return cas.KVCache(H, Tm, cas.params(1, k, m), K[:calib].cuda(), V[:calib].cuda(), est)
+
+
+def stream_sections(kv, st, n):
+    """Valid bytes of every section of stream st holding n tokens."""
+    k, m = kv.desc.p.keep_per_block, kv.desc.p.mant_bits
+    rec = lambda f, w: -(-(f * w) // 32)  # noqa: E731
+    nsb = -(-n // 8)
+    sidx = kv.section("spec_sbidx", st).cpu().numpy().view(np.uint32)[:nsb + 1]
+    vidx = kv.section("ver_sbidx", st).cpu().numpy().view(np.uint32)[:nsb + 1]
+    return {
+        "mask": kv.section("mask", st).cpu().numpy()[:n * 16],
+        "spec_sm": kv.section("spec_sm", st).cpu().numpy()[:n * rec(k, m + 1) * 4],
+        "spec_exp": kv.section("spec_exp", st).cpu().numpy()[:int(sidx[-1]) * 4],
+        "spec_sbidx": sidx.tobytes(),
+        "ver_lo": kv.section("ver_lo", st).cpu().numpy()[:n * rec(k, 7 - m) * 4],
+        "ver_pr": kv.section("ver_pr", st).cpu().numpy()[:n * rec(128 - k, 8) * 4],
+        "ver_exp": kv.section("ver_exp", st).cpu().numpy()[:int(vidx[-1]) * 4],
+        "ver_sbidx": vidx.tobytes(),
+    }
+
+
+def assert_streams_equal(a, b):
+    for key in a:
+        x, y = a[key], b[key]
+        x = x.tobytes() if hasattr(x, "tobytes") else x
+        y = y.tobytes() if hasattr(y, "tobytes") else y
+        assert x == y, key
+
+
+@pytest.mark.parametrize("T,k,m", [(37, 64, 3), (8, 64, 3), (64, 38, 3), (19, 128, 7), (11, 0, 2), (29, 77, 5)])
+def test_append_matches_oracle(cas, orc, T, k, m):
+    H = 3
+    K, V = make_tokens(T, H, seed=T)
+    kv = new_cache(cas, H, 100, K, V, k, m, calib=min(16, T))
+    kv.append(K.cuda(), V.cuda())
+    n, st = kv.status()
+    assert (n, st) == (T, 0)
+    for kvi, src in ((0, K), (1, V)):
+        calib = np16(src[:min(16, T)])
+        for h in range(H):
+            s = kvi * H + h
+            roe, eor = kv.tables(kvi, h)
+            c = orc.exp_hist(calib[:, h])
+            eor_ref, roe_ref = orc.rank_table(c)
+            assert np.array_equal(eor, eor_ref) and np.array_equal(roe, roe_ref)
+            ref = orc.kv_stream_encode(np16(src[:, h]), 1, k, m, roe, eor)
+            got = stream_sections(kv, s, T)
+            for name, val in got.items():
+                want = ref.section(name).tobytes()
+                val = val if isinstance(val, bytes) else val.tobytes()
+                assert val == want, (name, kvi, h)
+
+
+def test_chunked_equals_token_by_token(cas):
+    H, T = 2, 45
+    K, V = make_tokens(T, H, seed=5)
+    a = new_cache(cas, H, 64, K, V)
+    b = new_cache(cas, H, 64, K, V)
+    a.append(K.cuda(), V.cuda())
+    for t in range(T):
+        b.append(K[t:t + 1].cuda(), V[t:t + 1].cuda())
+    for chunks in ((3, 17, 25), ):
+        c = new_cache(cas, H, 64, K, V)
+        p = 0
+        for e in chunks + (T,):
+            c.append(K[p:e].cuda(), V[p:e].cuda())
+            p = e
+        for s in range(2 * H):
+            assert_streams_equal(stream_sections(a, s, T), stream_sections(c, s, T))
+    for s in range(2 * H):
+        assert_streams_equal(stream_sections(a, s, T), stream_sections(b, s, T))
+    assert torch.equal(a.section("state", 0)[:8 + 32 * H + 24], b.section("state", 0)[:8 + 32 * H + 24])
+
+
+@pytest.mark.parametrize("cut", [0, 1, 7, 8, 9, 30, 40])
+def test_truncate_then_append(cas, cut):
+    H, T = 2, 40
+    K, V = make_tokens(T, H, seed=9)
+    K2, V2 = make_tokens(T, H, seed=77)
+    ref = new_cache(cas, H, 96, K, V)
+    ref.append(K[:cut].cuda(), V[:cut].cuda())
+    ref.append(K2.cuda(), V2.cuda())
+    kv = new_cache(cas, H, 96, K, V)
+    kv.append(K.cuda(), V.cuda())
+    kv.truncate(cut)
+    assert kv.status() == (cut, 0)
+    kv.append(K2.cuda(), V2.cuda())
+    assert kv.status() == (cut + T, 0)
+    for s in range(2 * H):
+        assert_streams_equal(stream_sections(ref, s, cut + T), stream_sections(kv, s, cut + T))
+    kv.truncate(10**9)  # larger than the count: unchanged
+    assert kv.status() == (cut + T, 0)
+
+
+def test_capacity_and_nonfinite_write_nothing(cas):
+    H = 2
+    K, V = make_tokens(24, H, seed=3)
+    kv = new_cache(cas, H, 16, K, V)
+    kv.append(K[:10].cuda(), V[:10].cuda())
+    before = kv.buf.clone()
+    kv.append(K[10:24].cuda(), V[10:24].cuda())  # 24 > 16 tokens
+    n, st = kv.status()
+    assert (n, st) == (10, -4)
+    so = int(kv.desc.off[0])
+    assert torch.equal(kv.buf[:so + 8], before[:so + 8])
+    assert torch.equal(kv.buf[so + 12:], before[so + 12:])
+    kv.clear_status()
+    assert kv.status() == (10, 0)
+    Kb = K[10:12].clone()
+    Kb[1, 1, 5] = 0x7FC1  # NaN
+    kv.append(Kb.cuda(), V[10:12].cuda())
+    assert kv.status() == (10, -3)
+    assert torch.equal(kv.buf[so + 12:], before[so + 12:])
+    kv.clear_status()
+    kv.append(K[10:12].cuda(), V[10:12].cuda())
+    assert kv.status() == (12, 0)
+    # code-stream capacity: a tiny estimate of bits per code overflows the stream
+    small = new_cache(cas, H, 64, K, V, est=0.05)
+    small.append(K.cuda(), V.cuda())
+    assert small.status() == (0, -4)
+
+
+def oracle_draft_kv(orc, toks, k, m):
+    T, H, _ = toks.shape
+    a = np16(toks)
+    return np.stack([orc.draft_values(a[:, h].reshape(1, T * D), 1, k, m).reshape(T, D) for h in range(H)], 1)
+
+
+def check_attn(o, ref, nrm, what):
+    o = o.double().cpu().numpy()
+    bound = TOL * nrm + 1e-6
+    bad = np.abs(o - ref) > bound
+    assert not bad.any(), f"{what}: {bad.sum()} bad, worst {(np.abs(o - ref) / bound).max():.3g}"
+
+
+@pytest.mark.parametrize("lens,n_tail", [((300,), 0), ((1, ), 1), ((517, 64), 3), ((0,), 2), ((256, 1000), 4)])
+def test_draft_attention(cas, orc, lens, n_tail):
+    H, Hq, k, m = 8, 32, 64, 3
+    B = len(lens)
+    caches, Ks, Vs = [], [], []
+    for b, T in enumerate(lens):
+        K, V = make_tokens(max(T, 16), H, layer=b, seed=31 + b)
+        kv = new_cache(cas, H, 1100, K, V, k, m)
+        if T:
+            kv.append(K[:T].cuda(), V[:T].cuda())
+        assert kv.status() == (T, 0)
+        caches.append(kv)
+        Ks.append(K[:T])
+        Vs.append(V[:T])
+    q = synthetic.activations(B, Hq * D, seed=40).view(B, Hq, D)
+    tk = synthetic.activations(B * max(n_tail, 1), H * D, seed=41).view(B, max(n_tail, 1), H, D)[:, :n_tail]
+    tv = synthetic.activations(B * max(n_tail, 1), H * D, seed=42).view(B, max(n_tail, 1), H, D)[:, :n_tail]
+    o = cas.draft_attn_decode(caches, q.cuda(), tk.contiguous().cuda() if n_tail else None,
+                              tv.contiguous().cuda() if n_tail else None)
+    for b in range(B):
+        Kd = oracle_draft_kv(orc, Ks[b], k, m) if lens[b] else np.zeros((0, H, D), np.uint16)
+        Vd = oracle_draft_kv(orc, Vs[b], k, m) if lens[b] else np.zeros((0, H, D), np.uint16)
+        Kall = np.concatenate([Kd, np16(tk[b])], 0)
+        Vall = np.concatenate([Vd, np16(tv[b])], 0)
+        if Kall.shape[0] == 0:
+            assert torch.all(o[b] == 0)
+            continue
+        ref, nrm = orc.attention(np16(q[b:b + 1]), Kall, Vall)
+        check_attn(o[b:b + 1], ref, nrm, f"draft attention b={b}")
+
+
+@pytest.mark.parametrize("lens,T", [((300,), 5), ((5,), 5), ((517, 40), 7), ((1024,), 14), ((260,), 16), ((9,), 1)])
+def test_verify_attention(cas, orc, lens, T):
+    H, Hq = 8, 32
+    B = len(lens)
+    caches, Ks, Vs = [], [], []
+    for b, n in enumerate(lens):
+        K, V = make_tokens(max(n, 16), H, layer=b, seed=51 + b)
+        kv = new_cache(cas, H, 1100, K, V)
+        kv.append(K[:n].cuda(), V[:n].cuda())
+        assert kv.status() == (n, 0)
+        caches.append(kv)
+        Ks.append(K[:n])
+        Vs.append(V[:n])
+    q = synthetic.activations(B * T, Hq * D, seed=60).view(B, T, Hq, D)
+    o = cas.verify_attn(caches, q.cuda())
+    for b in range(B):
+        ref, nrm = orc.attention(np16(q[b]), np16(Ks[b]), np16(Vs[b]), causal_new=T)
+        check_attn(o[b], ref, nrm, f"verify attention b={b}")
+
+
+def test_attention_errors(cas):
+    H = 8
+    K, V = make_tokens(16, H, seed=1)
+    kv = new_cache(cas, H, 64, K, V)
+    q = torch.zeros(1, 30, D, dtype=torch.int16, device="cuda")  # 30 q heads not a multiple of 8
+    with pytest.raises(cas.CasError):
+        cas.draft_attn_decode([kv], q)
+    q = torch.zeros(1, 17, 32, D, dtype=torch.int16, device="cuda")  # T > 16
+    with pytest.raises(cas.CasError):
+        cas.verify_attn([kv], q)

@@ -1,0 +1,197 @@
+"""GPU parity of the weight path against the CPU oracle, through the C ABI.
+
+Encode / decode_draft / reconstruct: byte-exact. Draft GEMV and verify GEMM:
+|y - y_ref| <= 2e-3 * sum_k |w_k x_k| per output (y_ref in float64 over the
+oracle's draft values, resp. the original values).
+"""
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def cas():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import bit_level_weight_gb300 as cas
+    from bit_level_weight_gb300 import build
+    build.build()
+    return cas
+
+
+def np16(t):
+    return t.cpu().numpy().view(np.uint16)
+
+
+def check_close(y, ref, norm, what):
+    y = y.double().cpu().numpy()
+    err = np.abs(y - ref)
+    bound = TOL * norm + 1e-30
+    bad = err > bound
+    assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} outside 2e-3 bound; worst ratio {(err / bound).max():.3g}"
+
+
+CASES = [
+    # (N, K, variant, k, m)
+    (64, 1024, 1, 64, 3),
+    (37, 1152, 1, 38, 3),    # ragged superblock tail (9 blocks per row), odd N
+    (16, 384, 1, 0, 3),
+    (16, 256, 1, 128, 7),
+    (24, 640, 1, 77, 2),     # fields straddle words
+    (8, 128, 1, 1, 0),
+    (64, 1024, 2, 64, 3),
+    (37, 1152, 2, 38, 1),
+    (16, 256, 2, 128, 5),
+    (24, 640, 2, 90, 0),
+    (16, 384, 2, 0, 4),
+]
+
+
+@pytest.mark.parametrize("N,K,variant,k,m", CASES)
+def test_encode_decode_bit_exact(cas, orc, N, K, variant, k, m):
+    W = synthetic.normal_weight(N, K, seed=N * 1000 + K + variant, outlier_frac=0.01)
+    Wn = np16(W)
+    ref = orc.encode(Wn, variant, k, m)
+    enc = cas.encode_weights(W.cuda(), variant, k, m)
+    d = enc.desc
+    assert bytes(d.exp_of_rank) == ref.exp_of_rank.tobytes()
+    assert list(d.off) == list(ref.off) and list(d.len) == list(ref.len)
+    assert int(d.bytes) == ref.buf.size
+    got = enc.buf[: ref.buf.size].cpu().numpy()
+    for i, name in enumerate(orc.SECTIONS):
+        a, b = int(d.off[i]), int(d.off[i]) + int(d.len[i])
+        assert np.array_equal(got[a:b], ref.buf[a:b]), name
+    assert np.array_equal(got, ref.buf)  # padding bytes too
+    assert np.array_equal(np16(cas.decode_draft(enc)), orc.draft_values(Wn, variant, k, m))
+    assert np.array_equal(np16(cas.reconstruct(enc)), Wn)
+
+
+@pytest.mark.parametrize("N,K,variant,k,m", CASES)
+@pytest.mark.parametrize("nvec", [1, 2, 4])
+def test_draft_gemv(cas, orc, N, K, variant, k, m, nvec):
+    W = synthetic.normal_weight(N, K, seed=7 + N + K, outlier_frac=0.01)
+    x = synthetic.activations(nvec, K, seed=99 + nvec)
+    enc = cas.encode_weights(W.cuda(), variant, k, m)
+    y = cas.draft_gemv(enc, x.cuda())
+    ref, norm = orc.matvec(orc.draft_values(np16(W), variant, k, m), np16(x))
+    check_close(y, ref, norm, "draft_gemv")
+
+
+@pytest.mark.parametrize("N,K,variant,k,m", CASES)
+@pytest.mark.parametrize("T", [1, 5, 8, 9, 14, 16])
+def test_verify_gemm(cas, orc, N, K, variant, k, m, T):
+    W = synthetic.normal_weight(N, K, seed=11 + N + K, outlier_frac=0.01)
+    X = synthetic.activations(T, K, seed=123 + T)
+    enc = cas.encode_weights(W.cuda(), variant, k, m)
+    Y = cas.verify_gemm(enc, X.cuda())
+    ref, norm = orc.matvec(np16(W), np16(X))
+    check_close(Y, ref, norm, "verify_gemm")
+
+
+def test_all_finite_patterns_roundtrip(cas):
+    v = np.arange(65536, dtype=np.uint32)
+    v = v[((v >> 7) & 0xFF) != 255].astype(np.uint16)
+    rng = np.random.default_rng(4)
+    W = rng.permutation(np.concatenate([v, rng.choice(v, 65536 - v.size)])).reshape(64, 1024)
+    Wt = torch.from_numpy(W.view(np.int16)).cuda()
+    for variant in (1, 2):
+        for k, m in ((64, 3), (128, 0), (0, 7), (101, 1)):
+            enc = cas.encode_weights(Wt, variant, k, m)
+            assert np.array_equal(np16(cas.reconstruct(enc)), W)
+
+
+def test_errors(cas):
+    W = torch.zeros(4, 200, dtype=torch.int16, device="cuda")
+    with pytest.raises(cas.CasError) as e:
+        cas.encode_weights(W)
+    assert e.value.status == -2
+    W = torch.zeros(4, 256, dtype=torch.int16, device="cuda")
+    W[1, 3] = 0x7F80  # +inf
+    with pytest.raises(cas.CasError) as e:
+        cas.encode_weights(W)
+    assert e.value.status == -3
+    W = synthetic.normal_weight(8, 256, seed=1).cuda()
+    enc = cas.encode_weights(W)
+    x = torch.zeros(5, 256, dtype=torch.int16, device="cuda")
+    with pytest.raises(cas.CasError):
+        cas.draft_gemv(enc, x)  # nvec > 4
+    X = torch.zeros(17, 256, dtype=torch.int16, device="cuda")
+    with pytest.raises(cas.CasError):
+        cas.verify_gemm(enc, X)  # T > 16
+    assert cas.cas_device_status() == 0
+
+
+def test_empty_tensor(cas):
+    W = torch.zeros(0, 256, dtype=torch.int16, device="cuda")
+    enc = cas.encode_weights(W)
+    y = cas.draft_gemv(enc, torch.zeros(1, 256, dtype=torch.int16, device="cuda"))
+    assert y.shape == (1, 0)
+
+
+def test_cfg0_full_size(cas, orc):
+    """The 4096x4096 workload: encode byte-exact, GEMV and GEMM (T=5) in tolerance."""
+    W = synthetic.cfg0_weight()
+    Wn = np16(W)
+    ref = orc.encode(Wn, 1, 64, 3)
+    enc = cas.encode_weights(W.cuda(), 1, 64, 3)
+    assert np.array_equal(enc.buf[: ref.buf.size].cpu().numpy(), ref.buf)
+    x = synthetic.activations(1, 4096, seed=1)
+    y = cas.draft_gemv(enc, x.cuda())
+    yr, nr = orc.matvec(orc.decode(ref, False), np16(x))
+    check_close(y, yr, nr, "cfg0 draft gemv")
+    X = synthetic.activations(5, 4096, seed=2)
+    Y = cas.verify_gemm(enc, X.cuda())
+    Yr, Nr = orc.matvec(Wn, np16(X))
+    check_close(Y, Yr, Nr, "cfg0 verify gemm")
+
+
+@pytest.mark.parametrize("variant,k", [(1, 64), (1, 38), (2, 64)])
+def test_llama_ffn_full_size_sampled(cas, orc, variant, k):
+    """A 14336x4096 Student-t(4) FFN matrix: lossless reconstruct of the whole
+    tensor; sampled rows of the encoding byte-exact and of the GEMV / GEMM in
+    tolerance (rows are independent given the tensor's rank table)."""
+    N, K, m = 14336, 4096, 3
+    W = synthetic.t4_weight(N, K, seed=4)
+    Wd = W.cuda()
+    enc = cas.encode_weights(Wd, variant, k, m)
+    assert torch.equal(cas.reconstruct(enc), Wd)
+    Wn = np16(W)
+    eor, roe = orc.rank_table(orc.exp_hist(Wn))
+    assert bytes(enc.desc.exp_of_rank) == eor.tobytes()
+    rows = np.array([0, 1, 777, 8191, 14335])
+    sub = orc.encode(Wn[rows], variant, k, m, roe, eor)
+    nbr, nsr = K // 128, (K // 128 + 7) // 8
+    for name in ("mask", "spec_sm", "spec_q", "spec_mx", "ver_lo", "ver_pr"):
+        full, part = enc.section(name).cpu().numpy(), sub.section(name)
+        if part.size == 0:
+            continue
+        per_row = part.size // len(rows)
+        for i, r in enumerate(rows):
+            assert np.array_equal(full[r * per_row:(r + 1) * per_row], part[i * per_row:(i + 1) * per_row]), name
+    for sname, iname in (("spec_exp", "spec_sbidx"), ("ver_exp", "ver_sbidx"), ("ver_d", "ver_d_sbidx"),
+                         ("ver_res", "ver_res_sbidx")):
+        part_idx = sub.section(iname).view(np.uint32)
+        if part_idx.size == 0:
+            continue
+        full_idx = enc.section(iname).cpu().numpy().view(np.uint32)
+        full_w = enc.section(sname).cpu().numpy().view(np.uint32)
+        part_w = sub.section(sname).view(np.uint32)
+        for i, r in enumerate(rows):
+            for j in range(nsr):
+                s, ps = r * nsr + j, i * nsr + j
+                a = full_w[full_idx[s]:full_idx[s + 1]]
+                b = part_w[part_idx[ps]:part_idx[ps + 1]]
+                assert np.array_equal(a, b), (sname, r, j)
+    x = synthetic.activations(1, K, seed=5)
+    y = cas.draft_gemv(enc, x.cuda())[:, rows]
+    yr, nr = orc.matvec(orc.draft_values(Wn[rows], variant, k, m), np16(x))
+    check_close(y, yr, nr, "ffn draft gemv rows")
+    X = synthetic.activations(5, K, seed=6)
+    Y = cas.verify_gemm(enc, X.cuda())[:, rows]
+    Yr, Nr = orc.matvec(Wn[rows], np16(X))
+    check_close(Y, Yr, Nr, "ffn verify gemm rows")
