@@ -59,6 +59,15 @@ def parse():
     ap.add_argument("--no-attn", action="store_true", help="weights only (no KV cache)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--micro", default=None,
+                    choices=["draft_gemv", "verify_gemm", "draft_attn", "verify_attn", "kv_append", "encode"],
+                    help="time one kernel on one tensor (for profiling)")
+    ap.add_argument("--N", type=int, default=28672)
+    ap.add_argument("--K", type=int, default=4096)
+    ap.add_argument("--variant", type=int, default=1)
+    ap.add_argument("--nvec", type=int, default=1)
+    ap.add_argument("--T", type=int, default=5)
+    ap.add_argument("--reps", type=int, default=20)
     return ap.parse_args()
 
 
@@ -224,7 +233,7 @@ def run_cas(args):
     _b.build()
 
     stk = Stack(cas, args, dev)
-    st = torch.cuda.current_stream()
+    st = torch.cuda.Stream(device=dev)  # every call of the step is bound to this stream
     D, B = args.draft_len, args.batch
     nvec = B
     xs = {"qkv": synthetic.activations(nvec, stk.hidden, seed=1, device=dev),
@@ -243,15 +252,10 @@ def run_cas(args):
             for l in range(stk.L)]
     gemm = [{nm: cas.prepare("cas_verify_gemm", stk.mats[l][nm], Xs[nm], T, Ys[nm], st) for nm in Xs}
             for l in range(stk.L)]
-    draft_bytes_layer = {nm: stk.mats[0][nm].spec_bytes() + nvec * stk.mats[0][nm].K * 2 + nvec * stk.mats[0][nm].N * 4
-                         for nm in xs}
-    verify_bytes_layer = {nm: stk.mats[0][nm].all_bytes() + T * stk.mats[0][nm].K * 2 + T * stk.mats[0][nm].N * 4
-                          for nm in Xs}
     draft_bytes = {nm: sum(stk.mats[l][nm].spec_bytes() + nvec * stk.mats[l][nm].K * 2 + nvec * stk.mats[l][nm].N * 4
                            for l in range(stk.L)) for nm in xs}
     verify_bytes = {nm: sum(stk.mats[l][nm].all_bytes() + T * stk.mats[l][nm].K * 2 + T * stk.mats[l][nm].N * 4
                             for l in range(stk.L)) for nm in Xs}
-    del draft_bytes_layer, verify_bytes_layer
 
     attn = stk.kv is not None
     if attn:
@@ -264,63 +268,71 @@ def run_cas(args):
         ws = torch.empty(cas.cas_attn_workspace_bytes(B, stk.nq, D + 1, args.ctx + 64), dtype=torch.uint8, device=dev)
         o_d = torch.empty(B, stk.nq, stk.hd, dtype=torch.float32, device=dev)
         o_v = torch.empty(B, D + 1, stk.nq, stk.hd, dtype=torch.float32, device=dev)
-        dattn = [[cas.prepare_draft_attn(stk.kv[l], q_d, tail_k[:, :d + 1].contiguous(), tail_v[:, :d + 1].contiguous(),
-                                         o_d, ws, st) for d in range(D)] for l in range(stk.L)]
+        tails = [(tail_k[:, :d + 1].contiguous(), tail_v[:, :d + 1].contiguous()) for d in range(D)]
+        dattn = [[cas.prepare_draft_attn(stk.kv[l], q_d, tails[d][0], tails[d][1], o_d, ws, st) for d in range(D)]
+                 for l in range(stk.L)]
         vattn = [cas.prepare_verify_attn(stk.kv[l], q_v, o_v, ws, st) for l in range(stk.L)]
         appends = [[kv.prepare_append(newk, newv, st) for kv in stk.kv[l]] for l in range(stk.L)]
         truncs = [[kv.prepare_truncate(args.ctx, st) for kv in stk.kv[l]] for l in range(stk.L)]
 
-    n_ev = 4 * stk.L * D + 4 * stk.L
-    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
-    ev = evsets[0]
-
-    def step(record: bool, ev=ev):
-        """One speculative step; with record=True brackets the GEMV / GEMM runs
-        with events (pairs: draft GEMV runs first, then verify GEMM runs)."""
-        e = 0
-        for d in range(D):
-            for l in range(stk.L):
-                g = gemv[l]
-                if record:
-                    ev[e].record(st); e += 1
-                g["qkv"]()
-                if record:
-                    ev[e].record(st); e += 1
-                if attn:
-                    dattn[l][d]()
-                if record:
-                    ev[e].record(st); e += 1
-                g["o"](); g["gateup"](); g["down"]()
-                if record:
-                    ev[e].record(st); e += 1
+    # The step as an ordered list of segments; GEMV / GEMM segments are timed.
+    def seq(*fns):
+        def run():
+            for f in fns:
+                f()
+        return run
+    segs = []  # (kind, callable)
+    for d in range(D):
         for l in range(stk.L):
-            g = gemm[l]
-            if record:
-                ev[e].record(st); e += 1
-            g["qkv"]()
-            if record:
-                ev[e].record(st); e += 1
+            g = gemv[l]
+            segs.append(("gemv", g["qkv"]))
             if attn:
-                for a in appends[l]:
-                    a()
-                vattn[l]()
-            if record:
-                ev[e].record(st); e += 1
-            g["o"](); g["gateup"](); g["down"]()
-            if record:
-                ev[e].record(st); e += 1
+                segs.append(("attn", dattn[l][d]))
+            segs.append(("gemv", seq(g["o"], g["gateup"], g["down"])))
+    for l in range(stk.L):
+        g = gemm[l]
+        segs.append(("gemm", g["qkv"]))
         if attn:
-            for l in range(stk.L):
-                for t in truncs[l]:
-                    t()
-        return e
+            segs.append(("attn", seq(*appends[l], vattn[l])))
+        segs.append(("gemm", seq(g["o"], g["gateup"], g["down"])))
+    if attn:
+        segs.append(("attn", seq(*[t for l in range(stk.L) for t in truncs[l]])))
 
     launches_per_step = D * stk.L * 4 + stk.L * 4
     if attn:
         launches_per_step += D * stk.L * 2 + stk.L * (2 * B + 2) + stk.L * B
 
-    for _ in range(max(args.warmup, 3)):
-        step(False)
+    # eager warm-up (also caches every launch configuration), then one CUDA
+    # graph per segment so the timed region has no host gaps inside a segment
+    with torch.cuda.stream(st):
+        for _ in range(max(args.warmup, 3)):
+            for _, f in segs:
+                f()
+    torch.cuda.synchronize()
+    graphs = []
+    for kind, f in segs:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            f()
+        graphs.append((kind, g))
+    torch.cuda.synchronize()
+    n_timed = sum(1 for k, _ in graphs if k != "attn")
+    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * n_timed)] for _ in range(args.steps)]
+
+    def step(ev=None):
+        e = 0
+        for kind, g in graphs:
+            if ev is not None and kind != "attn":
+                ev[e].record(st)
+                g.replay()
+                ev[e + 1].record(st)
+                e += 2
+            else:
+                g.replay()
+
+    with torch.cuda.stream(st):
+        for _ in range(max(args.warmup, 3)):
+            step()
     torch.cuda.synchronize()
 
     # ---- timed region
@@ -330,21 +342,20 @@ def run_cas(args):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     gemv_ms, gemm_ms = 0.0, 0.0
-    with ClockSampler(local) as clk:
+    kinds = [k for k, _ in graphs if k != "attn"]
+    with ClockSampler(local) as clk, torch.cuda.stream(st):
         t_start.record(st)
         for i in range(args.steps):
-            step(True, evsets[i])
+            step(evsets[i])
         t_end.record(st)
         torch.cuda.synchronize()
-        for ev in evsets:
-            e = 0
-            for d in range(D):
-                for l in range(stk.L):
-                    gemv_ms += ev[e].elapsed_time(ev[e + 1]) + ev[e + 2].elapsed_time(ev[e + 3])
-                    e += 4
-            for l in range(stk.L):
-                gemm_ms += ev[e].elapsed_time(ev[e + 1]) + ev[e + 2].elapsed_time(ev[e + 3])
-                e += 4
+    for ev in evsets:
+        for i, kind in enumerate(kinds):
+            ms = ev[2 * i].elapsed_time(ev[2 * i + 1])
+            if kind == "gemv":
+                gemv_ms += ms
+            else:
+                gemm_ms += ms
     total_ms = t_start.elapsed_time(t_end)
     if world > 1:
         dist.barrier()
@@ -358,7 +369,8 @@ def run_cas(args):
 
     # ---- e2e: draft GEMV pass of the whole stack through the C ABI with the
     # activation in pinned host memory (H2D) and every output read back (D2H)
-    e2e = e2e_draft_pass(cas, stk, xs, ys, nvec, st, steps=max(3, steps))
+    with torch.cuda.stream(st):
+        e2e = e2e_draft_pass(cas, stk, xs, ys, nvec, st, steps=max(3, steps))
 
     vals = torch.tensor([gemv_gbs, gemm_gbs, ms_per_step], dtype=torch.float64, device=dev)
     if world > 1:
@@ -491,8 +503,107 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_micro(args):
+    """One kernel on one tensor: reps launches timed with CUDA events, bytes
+    per launch from the encoded section lengths."""
+    import torch
+
+    import bit_level_weight_gb300 as cas
+    import synthetic
+    from bit_level_weight_gb300 import build as _b
+    _b.build()
+    dev = torch.device("cuda", 0)
+    st = torch.cuda.Stream(device=dev)
+    out = {"micro": args.micro}
+    if args.micro in ("draft_gemv", "verify_gemm", "encode"):
+        W = synthetic.t4_weight(args.N, args.K, seed=1, device=dev)
+        enc = cas.encode_weights(W, args.variant, args.keep, args.mant)
+        if args.micro == "draft_gemv":
+            x = synthetic.activations(args.nvec, args.K, seed=2, device=dev)
+            y = torch.empty(args.nvec, args.N, dtype=torch.float32, device=dev)
+            call = cas.prepare("cas_draft_gemv", enc, x, args.nvec, y, st)
+            nbytes = enc.spec_bytes() + args.nvec * args.K * 2 + args.nvec * args.N * 4
+        elif args.micro == "verify_gemm":
+            X = synthetic.activations(args.T, args.K, seed=3, device=dev)
+            Y = torch.empty(args.T, args.N, dtype=torch.float32, device=dev)
+            call = cas.prepare("cas_verify_gemm", enc, X, args.T, Y, st)
+            nbytes = enc.all_bytes() + args.T * args.K * 2 + args.T * args.N * 4
+        else:
+            ws = torch.empty(cas.cas_encode_workspace_bytes(args.N, args.K), dtype=torch.uint8, device=dev)
+            buf = torch.empty_like(enc.buf)
+
+            def call():
+                cas.cas_encode_weights(W, enc.desc, buf, ws, st)
+            nbytes = args.N * args.K * 2 + enc.all_bytes()
+        out.update(N=args.N, K=args.K, variant=args.variant, keep=args.keep, mant=args.mant,
+                   spec_bits_per_elem=enc.spec_bytes() * 8 / (args.N * args.K),
+                   all_bits_per_elem=enc.all_bytes() * 8 / (args.N * args.K))
+    else:
+        H, Hq = 8, 32
+        sk, sv = synthetic.kv_scales(0, H, 0, device=dev), synthetic.kv_scales(0, H, 1, device=dev)
+        Kc = synthetic.kv_tokens(args.ctx, H, seed=5, scales=sk, device=dev)
+        Vc = synthetic.kv_tokens(args.ctx, H, seed=6, scales=sv, device=dev)
+        kv = cas.KVCache(H, args.ctx + 64, cas.params(1, args.keep, args.mant), Kc[:128], Vc[:128])
+        for t0 in range(0, args.ctx, 2048):
+            kv.append(Kc[t0:t0 + 2048], Vc[t0:t0 + 2048])
+        assert kv.status() == (args.ctx, 0)
+        k, m = args.keep, args.mant
+        words = lambda f, w: -(-(f * w) // 32) * 4  # noqa: E731
+        spec_tok = 16 + words(k, m + 1)
+        ver_tok = words(k, 7 - m) + words(128 - k, 8)
+        sidx = [kv.section("spec_sbidx", s_).cpu().numpy().view("uint32")[(args.ctx + 7) // 8] for s_ in range(2 * H)]
+        vidx = [kv.section("ver_sbidx", s_).cpu().numpy().view("uint32")[(args.ctx + 7) // 8] for s_ in range(2 * H)]
+        spec = 2 * H * args.ctx * spec_tok + 4 * int(sum(sidx)) + 2 * H * ((args.ctx + 7) // 8 + 1) * 4
+        full = spec + 2 * H * args.ctx * ver_tok + 4 * int(sum(vidx)) + 2 * H * ((args.ctx + 7) // 8 + 1) * 4
+        if args.micro == "draft_attn":
+            q = synthetic.activations(1, Hq * 128, seed=7, device=dev).view(1, Hq, 128)
+            tk = synthetic.activations(1, H * 128, seed=8, device=dev).view(1, 1, H, 128)
+            tv = synthetic.activations(1, H * 128, seed=9, device=dev).view(1, 1, H, 128)
+            o = torch.empty(1, Hq, 128, dtype=torch.float32, device=dev)
+            ws = torch.empty(cas.cas_attn_workspace_bytes(1, Hq, 1, args.ctx + 64), dtype=torch.uint8, device=dev)
+            call = cas.prepare_draft_attn([kv], q, tk, tv, o, ws, st)
+            nbytes = spec
+        elif args.micro == "verify_attn":
+            kv.truncate(args.ctx - args.T)
+            kv.append(Kc[-args.T:], Vc[-args.T:])
+            q = synthetic.activations(args.T, Hq * 128, seed=7, device=dev).view(1, args.T, Hq, 128)
+            o = torch.empty(1, args.T, Hq, 128, dtype=torch.float32, device=dev)
+            ws = torch.empty(cas.cas_attn_workspace_bytes(1, Hq, args.T, args.ctx + 64), dtype=torch.uint8, device=dev)
+            call = cas.prepare_verify_attn([kv], q, o, ws, st)
+            nbytes = full
+        else:
+            newk = Kc[-args.T:].contiguous()
+            newv = Vc[-args.T:].contiguous()
+            app = kv.prepare_append(newk, newv, st)
+            tr = kv.prepare_truncate(args.ctx, st)
+
+            def call():
+                app()
+                tr()
+            nbytes = 2 * args.T * H * 128 * 2
+        out.update(ctx=args.ctx, T=args.T, kv_spec_bytes=spec, kv_all_bytes=full)
+    with torch.cuda.stream(st):
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(args.reps):
+            call()
+        b.record(st)
+        torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.reps
+    peak, _ = peaks()
+    out.update(us_per_call=round(ms * 1e3, 2), bytes_per_call=int(nbytes),
+               gbs=round(nbytes / (ms * 1e-3) / 1e9, 1), frac_of_hbm=round(nbytes / (ms * 1e-3) / 1e9 / peak, 4))
+    print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse()
+    if args.micro:
+        run_micro(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

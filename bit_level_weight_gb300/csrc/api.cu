@@ -2,6 +2,8 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <mutex>
+#include <unordered_map>
 
 #include "common.cuh"
 
@@ -48,6 +50,34 @@ int sm_count() {
     cached = n > 0 ? n : 1;
   }
   return cached;
+}
+
+int occupancy(const void* func, int threads, size_t smem) {
+  struct Key {
+    const void* f;
+    int t;
+    size_t s;
+    bool operator==(const Key& o) const { return f == o.f && t == o.t && s == o.s; }
+  };
+  struct Hash {
+    size_t operator()(const Key& k) const { return (size_t)k.f ^ ((size_t)k.t << 20) ^ (k.s << 1); }
+  };
+  static std::mutex mu;
+  static std::unordered_map<Key, int, Hash> cache;
+  static std::unordered_map<const void*, size_t> smem_set;
+  std::lock_guard<std::mutex> g(mu);
+  Key k{func, threads, smem};
+  auto it = cache.find(k);
+  if (it != cache.end()) return it->second;
+  auto s = smem_set.find(func);
+  if (smem > 48 * 1024 && (s == smem_set.end() || s->second < smem)) {
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+    smem_set[func] = smem;
+  }
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, threads, smem) != cudaSuccess) n = 0;
+  cache[k] = n;
+  return n;
 }
 
 int launch_status() {

@@ -238,8 +238,7 @@ template <bool FULL, int QPW>
 int launch_chunk(const AttnArgs& a, int Hkv, cudaStream_t st) {
   size_t smem = chunk_smem();
   auto kern = attn_chunk_kernel<FULL, QPW>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return CAS_ERR_CUDA;
+  if (occupancy((const void*)kern, kThreads, smem) < 1) return CAS_ERR_CUDA;
   dim3 grid(a.nchunk, Hkv, a.B * a.ngroups);
   kern<<<grid, kThreads, smem, st>>>(a);
   return launch_status();

@@ -85,6 +85,35 @@ __device__ __forceinline__ uint32_t get_field(const uint32_t* w, int bit, int wi
   return v & ((1u << width) - 1u);
 }
 
+// Position (0..31, from the LSB) of the r-th set bit of m (r 0-based,
+// r < popc(m)): five popcount steps.
+__device__ __forceinline__ int nth_set_bit(uint32_t m, int r) {
+  int pos = 0;
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    int c = __popc(m & ((1u << w) - 1u));
+    if (r >= c) {
+      r -= c;
+      m >>= w;
+      pos += w;
+    }
+  }
+  return pos;
+}
+
+// Number of lanes whose non-decreasing value `v` is <= target (binary lifting
+// over the warp with shuffles); when v[31] > target this is the first lane
+// with v > target.
+__device__ __forceinline__ int warp_count_le(int v, int target) {
+  int lo = 0;
+#pragma unroll
+  for (int step = 16; step >= 1; step >>= 1) {
+    int u = __shfl_sync(CAS_FULL, v, lo + step - 1);
+    if (u <= target) lo += step;
+  }
+  return lo;
+}
+
 // ------------------------------------------------------------------ unary decoding
 // Warp-cooperative decode of the first `ncodes` unary codes of an MSB-first
 // stream of `nwords` words. Code i (rank r) is written as lut[r] to out[i].
@@ -97,6 +126,36 @@ __device__ __forceinline__ void warp_decode_unary(const uint32_t* __restrict__ w
                                                   uint8_t* __restrict__ out, int ncodes, int lane) {
   int done = 0;   // codes completed before this round
   int prev = -1;  // stream bit index of the last '1' before this round
+  for (int c0 = 0; c0 < nwords && done < ncodes; c0 += 32) {
+    int wi = c0 + lane;
+    uint32_t w = wi < nwords ? __ldg(words + wi) : 0u;
+    int ones = __popc(w);
+    int incl = warp_incl_add(ones, lane);
+    int ord = done + incl - ones;
+    int last = w ? (wi * 32 + 32 - __ffs(w)) : -1;
+    int mx = warp_incl_max(last, lane);
+    int pv = __shfl_up_sync(CAS_FULL, mx, 1);
+    if (lane == 0) pv = -1;
+    pv = max(pv, prev);
+    int base = wi * 32;
+    while (w) {
+      int i = __clz(w);
+      int pos = base + i;
+      if (ord < ncodes) out[ord] = lut[(pos - pv - 1) & 255];
+      pv = pos;
+      ++ord;
+      w &= 0x7FFFFFFFu >> i;
+    }
+    done += __shfl_sync(CAS_FULL, incl, 31);
+    prev = max(prev, __shfl_sync(CAS_FULL, mx, 31));
+  }
+}
+
+// Same decode, writing 32-bit table entries (e.g. exponent << 23).
+__device__ __forceinline__ void warp_decode_unary32(const uint32_t* __restrict__ words, int nwords,
+                                                    const uint32_t* __restrict__ lut,
+                                                    uint32_t* __restrict__ out, int ncodes, int lane) {
+  int done = 0, prev = -1;
   for (int c0 = 0; c0 < nwords && done < ncodes; c0 += 32) {
     int wi = c0 + lane;
     uint32_t w = wi < nwords ? __ldg(words + wi) : 0u;
@@ -259,4 +318,8 @@ bool aligned16(const void* p);
 int check_weights(const cas_weights* W);
 int sm_count();
 int launch_status();
+// Resident CTAs per SM of `func` with `threads` threads and `smem` dynamic
+// shared bytes; raises the kernel's dynamic shared-memory limit on first use.
+// Cached per (func, threads, smem), so repeated launches make no query.
+int occupancy(const void* func, int threads, size_t smem);
 }  // namespace cas

@@ -137,11 +137,8 @@ template <int VAR, int NT>
 int launch(const GemmArgs& a, cudaStream_t st) {
   size_t smem = (size_t)kRows * kTileStride * 2 + kWarps * 256 * 4 + 256 + kWarps * (2048 + kResWords * 4);
   auto kern = verify_gemm_kernel<VAR, NT>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return CAS_ERR_CUDA;
-  int per_sm = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
-  per_sm = std::max(per_sm, 1);
+  int per_sm = occupancy((const void*)kern, kThreads, smem);
+  if (per_sm < 1) return CAS_ERR_CUDA;
   int64_t ntasks = (a.w.N + kRows - 1) / kRows * a.w.nsr;
   int g = (int)std::max<int64_t>(1, std::min<int64_t>(ntasks, (int64_t)sm_count() * per_sm));
   kern<<<g, kThreads, smem, st>>>(a);

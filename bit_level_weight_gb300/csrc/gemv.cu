@@ -3,15 +3,22 @@
 // Reads only the speculation sections (mask, sign/mantissa records, unary
 // exponent stream and its superblock index; Cassandra-2: shared exponents and
 // q records). The draft does full-size FLOPs and saves bandwidth (Cassandra
-// blog review, section 3.1), so the kernel is bound by the HBM read of the
-// speculation stream and by the integer work of decoding it.
+// blog review, section 3.1), so the kernel moves only the speculation bytes
+// and its cost is the integer work of decoding them.
 //
-// Mapping: one warp per superblock (row n, 8 blocks); lane L owns mask word L,
-// i.e. 32 positions of block L>>2. The lane walks only its kept positions:
-// the sign/mantissa field comes from the block record, the exponent from the
-// superblock's unary codes decoded into shared memory, x from shared memory
-// (staged once per CTA by a TMA bulk copy). Partial sums go to y with one
-// fp32 atomic per (superblock, vector); y is cleared first.
+// Mapping: one warp per superblock (row n, up to 8 blocks). The superblock's
+// kept values are split into 32 runs of q consecutive ordinals, one per lane,
+// so all lanes do the same number of multiply-adds. A lane locates the start
+// of its run - the mask word and bit of its first kept position, and the bit
+// after the t0-th '1' of the unary exponent stream - with warp popcount
+// prefixes, shuffle binary searches and a popcount select within a word. It
+// then walks its run with two cursors over '1' bits held in two-word windows
+// (clz, then clear the bit; no 64-bit shifts): one over the bit-reversed mask
+// (next kept position), one over the unary stream (code end; rank = distance
+// from the previous end). The rank table gives exponent << 23, which is OR-ed
+// with the sign and mantissa field into an fp32 value and multiplied with x
+// from shared memory (staged once per CTA by a TMA bulk copy). Partial sums go
+// to y with one fp32 atomic per (superblock, vector); y is cleared first.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -30,23 +37,52 @@ struct GemvArgs {
   Lut lut;
   const uint16_t* x;
   float* y;
+  int sexp_words;  // words of the unary exponent section (read bound)
 };
 
 // Set when a bounded wait on the x staging copy gave up (read by
 // cas_device_status).
 __device__ int g_gemv_wait_status = 0;
 
-template <int VAR, int NV>
+constexpr int kRecWords = CAS_SB * 32 + 2;  // staged records of a superblock (+pad)
+constexpr int kMaskWords = 40;                 // bit-reversed mask words (+zero pad)
+constexpr int kWarpWords = kRecWords + kMaskWords;
+
+// Cursor over the '1' bits of an MSB-first bitstream held as a two-word
+// window (h: current word with consumed bits cleared, l: next word). `base`
+// is the stream bit index of h's MSB. Used for the mask (bit-reversed, a '1'
+// per kept position) and for the unary codes (a '1' ends each code).
+struct OnesCursor {
+  uint32_t h, l;
+  int base;
+  // bit index of the next '1', consuming it; `more` fetches the following
+  // word (stream bit index base + 64) when the window shifts.
+  template <class More>
+  __device__ __forceinline__ int next(More more) {
+    for (int guard = 0; h == 0 && guard < 64; ++guard) {  // window word exhausted
+      h = l;
+      l = more(base + 64);
+      base += 32;
+    }
+    int z = __clz(h);
+    h &= 0x7FFFFFFFu >> z;
+    return base + z;
+  }
+};
+
+template <int VAR, int NV, bool FAST>
 __global__ void __launch_bounds__(kThreads) draft_gemv_kernel(GemvArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const WView& w = a.w;
   const int K = (int)w.K;
   const int xbytes = NV * K * 2;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + xbytes);
-  uint8_t* s_lut = smem + xbytes + 16;
-  uint8_t* s_code = s_lut + 256 + (threadIdx.x >> 5) * 1024;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t* lut23 = reinterpret_cast<uint32_t*>(smem + xbytes + 16);  // exponent << 23 by rank
+  uint32_t* wbuf = lut23 + 256 + warp * kWarpWords;
+  uint32_t* s_rec = wbuf;                 // sign/mantissa records of the superblock
+  uint32_t* s_mw = wbuf + kRecWords;      // bit-reversed mask words
 
   if (threadIdx.x == 0) {
     mbar_init(bar, 1);
@@ -57,7 +93,8 @@ __global__ void __launch_bounds__(kThreads) draft_gemv_kernel(GemvArgs a) {
     mbar_arrive_tx(bar, (uint32_t)xbytes);
     bulk_g2s(xs, a.x, (uint32_t)xbytes, bar);
   }
-  for (int i = threadIdx.x; i < 256; i += kThreads) s_lut[i] = a.lut.v[i];
+  for (int i = threadIdx.x; i < 256; i += kThreads) lut23[i] = (uint32_t)a.lut.v[i] << 23;
+  if (lane < kMaskWords - 32) s_mw[32 + lane] = 0u;
   bool ok = mbar_wait_bounded(bar, 0);
   if (!__syncthreads_and(ok)) {
     if (threadIdx.x == 0) atomicExch(&g_gemv_wait_status, CAS_ERR_TIMEOUT);
@@ -65,55 +102,131 @@ __global__ void __launch_bounds__(kThreads) draft_gemv_kernel(GemvArgs a) {
     return;
   }
 
-  const int k = w.k, m = w.m;
-  for (int64_t s = blockIdx.x * (int64_t)kWarps + warp; s < w.nsb; s += (int64_t)gridDim.x * kWarps) {
-    int64_t n = s / w.nsr;
-    int j = (int)(s % w.nsr);
-    int nb = min(CAS_SB, w.nbr - CAS_SB * j);
-    int64_t gb0 = n * w.nbr + CAS_SB * j;
-    uint32_t mw = lane < 4 * nb ? __ldg(w.mask + gb0 * 4 + lane) : 0u;
-    int cnt = __popc(mw);
-    int o = warp_incl_add(cnt, lane) - cnt;
-    if (VAR == 1) {
-      uint32_t b0 = __ldg(w.sidx + s), b1 = __ldg(w.sidx + s + 1);
-      warp_decode_unary(w.sexp + b0, (int)(b1 - b0), s_lut, s_code, nb * k, lane);
-      __syncwarp();
+  const int k = w.k, m = w.m, nsr = w.nsr, nbr = w.nbr;
+  const int width = VAR == 1 ? m + 1 : m + 2;
+  const uint32_t fmask = (1u << width) - 1u;
+  const int rec = VAR == 1 ? w.rec_sm : w.rec_q;
+  const uint32_t* recs = VAR == 1 ? w.ssm : w.sq;
+  const int nsb = (int)w.nsb;
+  const int stride = gridDim.x * kWarps;
+  for (int s = blockIdx.x * kWarps + warp; s < nsb; s += stride) {
+    const int n = s / nsr;
+    const int j = s - n * nsr;
+    const int nb = min(CAS_SB, nbr - CAS_SB * j);
+    const int64_t gb0 = (int64_t)n * nbr + CAS_SB * j;
+    const uint32_t mw = lane < 4 * nb ? __ldg(w.mask + gb0 * 4 + lane) : 0u;
+    s_mw[lane] = __brev(mw);
+    if (!FAST) {
+      const uint32_t* rsrc = recs + gb0 * rec;
+      for (int i = lane; i < nb * rec; i += 32) s_rec[i] = __ldg(rsrc + i);
     }
+    const int cnt = __popc(mw);
+    const int incl = warp_incl_add(cnt, lane);
+    const int kt = nb * k;
+    const int q = FAST ? 16 : (kt + 31) >> 5;
+    const int t0 = min(lane * q, kt), t1 = min(t0 + q, kt);
+    // mask word and bit of the lane's first kept position
+    const int wi = min(warp_count_le(incl, t0), 31);
+    const int pre = __shfl_sync(CAS_FULL, incl - cnt, wi);
+    const uint32_t wsel = __shfl_sync(CAS_FULL, mw, wi);
+    const int bitpos = t0 < kt ? nth_set_bit(wsel, t0 - pre) : 0;
+    // unary stream: bit after the t0-th '1' (start of code t0)
+    const uint32_t* stream = nullptr;
+    int ebit = 0, slim = 0;  // slim: stream words readable from `stream`
+    if (VAR == 1) {
+      const uint32_t sb0 = __ldg(w.sidx + s), sb1 = __ldg(w.sidx + s + 1);
+      stream = w.sexp + sb0;
+      slim = (int)(a.sexp_words - sb0);
+      const int nwords = (int)(sb1 - sb0);
+      int before = 0;
+      bool done = t0 == 0 || t0 >= kt;
+      for (int c0 = 0; c0 < nwords; c0 += 32) {
+        if (!__any_sync(CAS_FULL, !done)) break;
+        uint32_t wv = c0 + lane < nwords ? __ldg(stream + c0 + lane) : 0u;
+        int ones = __popc(wv);
+        int oincl = warp_incl_add(ones, lane);
+        int total = __shfl_sync(CAS_FULL, oincl, 31);
+        int need = t0 - before;  // 1-based index of the '1' that ends code t0-1
+        int wk = min(warp_count_le(oincl, need - 1), 31);
+        int oexcl = __shfl_sync(CAS_FULL, oincl - ones, wk);
+        uint32_t word = __shfl_sync(CAS_FULL, wv, wk);
+        if (!done && need <= total) {
+          ebit = (c0 + wk) * 32 + nth_set_bit(__brev(word), need - oexcl - 1) + 1;
+          done = true;
+        }
+        before += total;
+      }
+    }
+    __syncwarp();
     float acc[NV];
 #pragma unroll
     for (int v = 0; v < NV; ++v) acc[v] = 0.f;
-    if (mw) {
-      int blk = lane >> 2, g = lane & 3;
-      int64_t gb = gb0 + blk;
-      int t = o - k * blk;
-      const uint16_t* xr = xs + CAS_BLK * CAS_SB * j + CAS_BLK * blk + 32 * g;
+    if (t0 < t1) {
+      const uint16_t* xrow = xs + CAS_BLK * CAS_SB * j;
+      // positions: cursor over the bit-reversed mask words from (wi, bitpos)
+      OnesCursor pc;
+      pc.h = s_mw[wi] & (0xFFFFFFFFu >> bitpos);
+      pc.l = s_mw[wi + 1];
+      pc.base = 32 * wi;
+      auto more_mask = [&](int bitidx) { return s_mw[min(bitidx >> 5, kMaskWords - 1)]; };
+      auto more_code = [&](int bitidx) { return (bitidx >> 5) < slim ? __ldg(stream + (bitidx >> 5)) : 0u; };
+      // codes: cursor over the unary stream from the word holding ebit
+      OnesCursor cc;
+      int prev = ebit;  // stream bit where the current code starts
       if (VAR == 1) {
-        const uint32_t* rs = w.ssm + gb * w.rec_sm;
-        const uint32_t fmask = (1u << m) - 1u;
-        while (mw) {
-          int p = __ffs(mw) - 1;
-          mw &= mw - 1;
-          uint32_t fld = get_field(rs, t * (m + 1), m + 1);
-          uint32_t bits = ((fld >> m) << 31) | ((uint32_t)s_code[o] << 23) | ((fld & fmask) << (23 - m));
-          float val = __uint_as_float(bits);
+        const int e0 = ebit & ~31;
+        cc.h = more_code(e0) & (0xFFFFFFFFu >> (ebit & 31));
+        cc.l = more_code(e0 + 32);
+        cc.base = e0;
+      }
+      float scale = 0.f;
+      int gcur = -1;
+      if (FAST) {
+        // k = 64, m = 3, full superblock: the lane's 16 fields are the 64
+        // bits at word 2*(lane%4) of record lane/4
+        const uint32_t* rb = recs + (gb0 + (lane >> 2)) * 8 + 2 * (lane & 3);
+        const uint32_t f0 = __ldg(rb), f1 = __ldg(rb + 1);
 #pragma unroll
-          for (int v = 0; v < NV; ++v) acc[v] = fmaf(val, bf2f(xr[v * K + p]), acc[v]);
-          ++t;
-          ++o;
+        for (int i = 0; i < 16; ++i) {
+          const int pos = pc.next(more_mask);
+          const int end = cc.next(more_code);
+          const uint32_t e23 = lut23[(end - prev) & 255];
+          prev = end + 1;
+          const uint32_t fld = ((i < 8 ? f0 : f1) >> (4 * (i & 7))) & 15u;
+          const float val = __uint_as_float(((fld >> 3) << 31) | e23 | ((fld & 7u) << 20));
+          const uint16_t* xp = xrow + (pos & 1023);
+#pragma unroll
+          for (int v = 0; v < NV; ++v) acc[v] = fmaf(val, bf2f(xp[v * K]), acc[v]);
         }
       } else {
-        const uint32_t* rs = w.sq + gb * w.rec_q;
-        float scale = pow2_biased(max((int)__ldg(w.smx + gb * 4 + g), 1) - m);
-        const uint32_t qmask = (1u << (m + 1)) - 1u;
-        while (mw) {
-          int p = __ffs(mw) - 1;
-          mw &= mw - 1;
-          uint32_t fld = get_field(rs, t * (m + 2), m + 2);
-          float val = (float)(fld & qmask) * scale;
-          val = (fld >> (m + 1)) & 1u ? -val : val;
+        int b = t0 / k, tl = t0 - b * k;  // block and block-local ordinal of t0
+        for (int t = t0; t < t1; ++t) {
+          const int pos = pc.next(more_mask);
+          if (tl == k) {
+            ++b;
+            tl = 0;
+          }
+          const int bit = b * rec * 32 + tl * width;
+          ++tl;
+          const uint32_t fld = __funnelshift_r(s_rec[bit >> 5], s_rec[(bit >> 5) + 1], bit & 31) & fmask;
+          float val;
+          if (VAR == 1) {
+            const int end = cc.next(more_code);
+            const uint32_t e23 = lut23[(end - prev) & 255];
+            prev = end + 1;
+            val = __uint_as_float(((fld >> m) << 31) | e23 | ((fld & (fmask >> 1)) << (23 - m)));
+          } else {
+            const int g = pos >> 5;
+            if (g != gcur) {
+              gcur = g;
+              scale = pow2_biased(max((int)__ldg(w.smx + gb0 * 4 + g), 1) - m);
+            }
+            val = (float)(fld & (fmask >> 1)) * scale;
+            val = (fld >> (m + 1)) ? -val : val;
+          }
+          const uint16_t* xp = xrow + (pos & 1023);
 #pragma unroll
-          for (int v = 0; v < NV; ++v) acc[v] = fmaf(val, bf2f(xr[v * K + p]), acc[v]);
-          ++t;
+          for (int v = 0; v < NV; ++v) acc[v] = fmaf(val, bf2f(xp[v * K]), acc[v]);
         }
       }
     }
@@ -126,28 +239,29 @@ __global__ void __launch_bounds__(kThreads) draft_gemv_kernel(GemvArgs a) {
   }
 }
 
-template <int VAR, int NV>
+template <int VAR, int NV, bool FAST>
 int launch(const GemvArgs& a, cudaStream_t st) {
-  size_t smem = (size_t)NV * a.w.K * 2 + 16 + 256 + kWarps * 1024;
-  auto kern = draft_gemv_kernel<VAR, NV>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return CAS_ERR_CUDA;
-  int per_sm = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
-  per_sm = std::max(per_sm, 1);
+  size_t smem = (size_t)NV * a.w.K * 2 + 16 + 1024 + kWarps * kWarpWords * 4;
+  auto kern = draft_gemv_kernel<VAR, NV, FAST>;
+  int per_sm = occupancy((const void*)kern, kThreads, smem);
+  if (per_sm < 1) return CAS_ERR_CUDA;
   int64_t need = (a.w.nsb + kWarps - 1) / kWarps;
   int g = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sm_count() * per_sm));
   kern<<<g, kThreads, smem, st>>>(a);
   return launch_status();
 }
 
+// The fast path covers Cassandra-1 with k = 64, m = 3 and rows that are whole
+// superblocks (K % 1024 == 0): every lane then owns exactly 16 ordinals that
+// sit in one 64-bit slice of one block record.
 template <int VAR>
 int dispatch(const GemvArgs& a, int nvec, cudaStream_t st) {
+  const bool fast = VAR == 1 && a.w.k == 64 && a.w.m == 3 && a.w.nbr % CAS_SB == 0;
   switch (nvec) {
-    case 1: return launch<VAR, 1>(a, st);
-    case 2: return launch<VAR, 2>(a, st);
-    case 3: return launch<VAR, 3>(a, st);
-    default: return launch<VAR, 4>(a, st);
+    case 1: return fast ? launch<VAR, 1, true>(a, st) : launch<VAR, 1, false>(a, st);
+    case 2: return fast ? launch<VAR, 2, true>(a, st) : launch<VAR, 2, false>(a, st);
+    case 3: return fast ? launch<VAR, 3, true>(a, st) : launch<VAR, 3, false>(a, st);
+    default: return fast ? launch<VAR, 4, true>(a, st) : launch<VAR, 4, false>(a, st);
   }
 }
 
@@ -177,10 +291,12 @@ extern "C" int cas_draft_gemv(const cas_weights* W, const uint16_t* x, int nvec,
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemsetAsync(y, 0, sizeof(float) * nvec * W->N, st) != cudaSuccess) return CAS_ERR_CUDA;
   if (W->K == 0) return CAS_OK;
+  if (W->N * ((W->K / CAS_BLK + CAS_SB - 1) / CAS_SB) >= (1ll << 31)) return CAS_ERR_INVALID;
   GemvArgs a;
   a.w = make_view(W);
   for (int i = 0; i < 256; ++i) a.lut.v[i] = W->exp_of_rank[i];
   a.x = x;
   a.y = y;
+  a.sexp_words = (int)(W->len[CAS_SEC_SPEC_EXP] / 4);
   return W->p.variant == 1 ? dispatch<1>(a, nvec, st) : dispatch<2>(a, nvec, st);
 }
