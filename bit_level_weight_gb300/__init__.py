@@ -90,6 +90,7 @@ def lib() -> ctypes.CDLL:
             "cas_draft_attn_decode": ([P, i32, P, i32, P, P, i32, P, P, u64, P], i32),
             "cas_verify_attn": ([P, i32, P, i32, i32, P, P, u64, P], i32),
             "cas_device_status": ([P], i32),
+            "cas_draft_attn_decode_noalloc": ([P, i32, P, i32, P, P, i32, P, P], i32),
         }
         for name, (args, res) in sig.items():
             if hasattr(L, name):
@@ -378,6 +379,23 @@ def draft_attn_decode(kvs, q: torch.Tensor, tail_k=None, tail_v=None, out=None, 
     arr = _kv_array(kvs)
     _check(lib().cas_draft_attn_decode(arr.ptr, B, _ptr(q), Hq, _ptr(tk), _ptr(tv), n_tail, _ptr(out), _ptr(workspace),
                                        workspace.numel(), _stream(stream)), "cas_draft_attn_decode")
+    return out
+
+
+def cas_draft_attn_decode_noalloc(kvs, q: torch.Tensor, tail_k=None, tail_v=None, out=None, stream=None):
+    """Draft attention without a workspace: for callers that cannot allocate
+    device memory when they decode. The library keeps the partials in one
+    fixed 8 MiB device array shared by every call (see include/cas.h)."""
+    q = _bits(q).contiguous()
+    B, Hq, _ = q.shape
+    n_tail = 0 if tail_k is None else tail_k.shape[1]
+    if out is None:
+        out = torch.empty(B, Hq, 128, dtype=torch.float32, device=q.device)
+    tk = None if tail_k is None else _bits(tail_k).contiguous()
+    tv = None if tail_v is None else _bits(tail_v).contiguous()
+    arr = _kv_array(kvs)
+    _check(lib().cas_draft_attn_decode_noalloc(arr.ptr, B, _ptr(q), Hq, _ptr(tk), _ptr(tv), n_tail, _ptr(out),
+                                               _stream(stream)), "cas_draft_attn_decode_noalloc")
     return out
 
 

@@ -18,6 +18,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 
 #include "kvview.cuh"
 #include "sbdecode.cuh"
@@ -328,5 +329,58 @@ extern "C" int cas_draft_attn_decode(const cas_kv* const* kv, int batch, const u
 extern "C" int cas_verify_attn(const cas_kv* const* kv, int batch, const uint16_t* q, int T, int n_q_heads, float* o,
                                void* workspace, uint64_t workspace_bytes, void* stream) {
   return run_attn(true, kv, batch, q, T, n_q_heads, nullptr, nullptr, 0, o, workspace, workspace_bytes,
+                  (cudaStream_t)stream);
+}
+
+// ------------------------------------------------------------------ no-allocation variant
+// Some callers cannot allocate device memory at the time they decode: a host
+// runtime whose memory plan is fixed at start-up and forbids later
+// allocation, or an embedding application that owns every allocation and
+// hands this library only its inputs and outputs. For them the draft
+// attention keeps its chunk partials in this fixed array instead of a
+// caller-provided workspace. It is part of the library's device image, so
+// every GPU that loads the library holds it until the process exits.
+namespace {
+
+constexpr uint64_t kStaticScratchBytes = 8ull << 20;  // 8 MiB
+static __device__ __align__(256) unsigned char g_attn_scratch[kStaticScratchBytes];
+
+// Device address of g_attn_scratch on the current device. The host symbol is
+// only a stand-in, so the address is looked up once per device (with that
+// device current) and cached.
+int static_scratch(void** out) {
+  static std::mutex mu;
+  static void* addr[128] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return CAS_ERR_CUDA;
+  std::lock_guard<std::mutex> g(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || !p) return CAS_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return CAS_OK;
+}
+
+}  // namespace
+
+extern "C" int cas_draft_attn_decode_noalloc(const cas_kv* const* kv, int batch, const uint16_t* q, int n_q_heads,
+                                             const uint16_t* tail_k, const uint16_t* tail_v, int n_tail, float* o,
+                                             void* stream) {
+  if (!kv || batch < 1 || batch > kMaxBatch || n_q_heads < 1) return CAS_ERR_INVALID;
+  int64_t Tm = 0;
+  for (int i = 0; i < batch; ++i) {
+    if (!kv[i]) return CAS_ERR_INVALID;
+    Tm = std::max(Tm, kv[i]->max_tokens);
+  }
+  uint64_t need = cas_attn_workspace_bytes(batch, n_q_heads, 1, Tm);
+  if (need == 0 || need > kStaticScratchBytes) return CAS_ERR_BUFFER;
+  void* ws = nullptr;
+  int s = static_scratch(&ws);
+  if (s) return s;
+  // every partial the combine step reads is written by the chunk step of this
+  // same call, so nothing in the array needs clearing between calls
+  return run_attn(false, kv, batch, q, 1, n_q_heads, tail_k, tail_v, n_tail, o, ws, kStaticScratchBytes,
                   (cudaStream_t)stream);
 }

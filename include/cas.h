@@ -238,6 +238,26 @@ int cas_draft_attn_decode(const cas_kv* const* kv, int batch, const uint16_t* q,
                           const uint16_t* tail_k, const uint16_t* tail_v, int n_tail, float* o,
                           void* workspace, uint64_t workspace_bytes, void* stream);
 
+/* Draft attention decode that allocates nothing and takes no workspace. The
+ * paper has no counterpart: this entry point is for callers that cannot
+ * allocate device memory when they decode (a runtime whose memory plan is
+ * fixed at start-up, or an application that owns every allocation and passes
+ * only inputs and outputs). Arguments and result are those of
+ * cas_draft_attn_decode. The chunk partials live in one fixed 8 MiB array in
+ * the library's device image (held by every GPU that loads the library until
+ * the process exits); the call returns CAS_ERR_BUFFER, without launching, when
+ * batch * n_q_heads * ceil(max_tokens / 256) * 520 bytes exceeds 8 MiB (e.g.
+ * batch 1 with 32 query heads reaches 128K tokens). The first call on a device
+ * looks up the array's device address with that device current; make that
+ * first call before any stream capture. Every call uses the same array, so
+ * calls that overlap on the GPU (on different streams, or on streams not
+ * ordered with each other) race; calls ordered on one stream do not. The
+ * array keeps the last call's partials; each call writes every partial it
+ * reads, so no clearing is needed. */
+int cas_draft_attn_decode_noalloc(const cas_kv* const* kv, int batch, const uint16_t* q, int n_q_heads,
+                                  const uint16_t* tail_k, const uint16_t* tail_v, int n_tail, float* o,
+                                  void* stream);
+
 /* Verify attention [B3.1]: T query tokens per sequence over the exact KV
  * (both streams merged), the T queries being the last T tokens of the cache:
  * query j sees every earlier token and the new tokens 0..j.
