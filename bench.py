@@ -418,7 +418,10 @@ def run_cas(args):
         "roofline": {"kernel": "draft_gemv_kernel<1,1>", "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
-                     "traffic": PROFILED_TRAFFIC,
+                     "traffic": (round(PROFILED_TRAFFIC_RATIO * per_launch_bytes) if PROFILED_TRAFFIC_RATIO
+                                 else None),
+                     "traffic_note": "per launch: ncu dram bytes / algorithmic bytes of a 28672x4096 launch "
+                                     "x algorithmic bytes per launch of this step",
                      "algorithmic_bytes_per_launch": int(per_launch_bytes)},
         "e2e": e2e,
         "gpu_launches": launches_per_step * steps,
@@ -432,8 +435,11 @@ def run_cas(args):
         dist.destroy_process_group()
 
 
-# traffic (dram bytes read + written) of one draft_gemv launch from ncu, or None
-PROFILED_TRAFFIC = None
+# DRAM traffic of the draft GEMV per algorithmic byte, from one ncu capture of
+# the current kernel on a 28672 x 4096 bench matrix (dram__bytes_read.sum +
+# dram__bytes_write.sum = 62.02 MB for 61.85 MB algorithmic; see
+# profiles/draft_gemv_28672x4096.md). Set to None when the kernel changes.
+PROFILED_TRAFFIC_RATIO = 62.02 / 61.85
 
 
 def e2e_draft_pass(cas, stk, xs, ys, nvec, st, steps):
