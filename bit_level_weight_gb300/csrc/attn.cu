@@ -36,6 +36,7 @@ constexpr int kMaxBatch = 8;
 constexpr int kMaxT = 16;
 
 constexpr int kQvPerCta = 32;  // query vectors per CTA (8 per warp)
+constexpr int kScratchWarp = (int)sizeof(FastScratch) > 2048 ? (int)sizeof(FastScratch) : 2048;
 
 struct AttnArgs {
   KvDev kv[kMaxBatch];
@@ -55,11 +56,26 @@ __device__ __forceinline__ float warp_maxf(float v) {
 // as fp32; rows of tokens that do not exist are zero.
 template <bool FULL>
 __device__ __forceinline__ void decode_sb_tile(const KvDev& d, int st, int64_t n, int64_t sb, float* tile, int row0,
-                                               const uint8_t* lut, SbScratch sc, int lane) {
+                                               const uint8_t* lut, uint8_t* scratch, int lane) {
   int64_t nsb = (n + CAS_SB - 1) / CAS_SB;
   uint32_t v[16];
   int nb = 0;
-  if (sb < nsb) {
+  if (sb < nsb && d.k == 64 && d.m == 3 && CAS_SB * (sb + 1) <= n) {
+    // whole superblock of 8 tokens: fast decoder
+    const uint32_t* sidx = (const uint32_t*)kv_sec(d, CAS_KV_SPEC_SBIDX, st);
+    const uint32_t* vidx = (const uint32_t*)kv_sec(d, CAS_KV_VER_SBIDX, st);
+    const uint32_t a0 = sidx[sb], a1 = sidx[sb + 1];
+    const uint32_t v0 = FULL ? vidx[sb] : 0u, v1 = FULL ? vidx[sb + 1] : 0u;
+    fast_sb_decode<FULL>((const uint32_t*)kv_sec(d, CAS_KV_MASK, st) + sb * 32,
+                         (const uint32_t*)kv_sec(d, CAS_KV_SPEC_SM, st) + sb * 64,
+                         (const uint32_t*)kv_sec(d, CAS_KV_VER_LO, st) + sb * 64,
+                         (const uint32_t*)kv_sec(d, CAS_KV_VER_PR, st) + sb * 128,
+                         (const uint32_t*)kv_sec(d, CAS_KV_SPEC_EXP, st) + a0, (int)(a1 - a0),
+                         (const uint32_t*)kv_sec(d, CAS_KV_VER_EXP, st) + v0, (int)(v1 - v0), lut,
+                         *reinterpret_cast<FastScratch*>(scratch), lane, v);
+    nb = CAS_SB;
+  } else if (sb < nsb) {
+    SbScratch sc{scratch, scratch + 1024, nullptr};
     WView w = kv_stream_view(d, st, n);
     SbInfo in = sb_prepare<1, FULL>(w, sb, lut, sc, lane);
     nb = in.nb;
@@ -90,7 +106,7 @@ __global__ void __launch_bounds__(kThreads) attn_chunk_kernel(AttnArgs a) {
   uint8_t* lutV = lutK + 256;
   uint8_t* scr = lutV + 256;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  SbScratch sc{scr + warp * 2048, scr + warp * 2048 + 1024, nullptr};
+  uint8_t* wscr = scr + warp * kScratchWarp;
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z / a.ngroups;
   const int qv0 = (blockIdx.z % a.ngroups) * kQvPerCta;
   const KvDev& d = a.kv[b];
@@ -121,8 +137,8 @@ __global__ void __launch_bounds__(kThreads) attn_chunk_kernel(AttnArgs a) {
   }
   for (int64_t t0 = t_begin; t0 < t_end; t0 += kStepTok) {
     int64_t sb = t0 / CAS_SB + warp;
-    decode_sb_tile<FULL>(d, h, n, sb, Kt, warp * CAS_SB, lutK, sc, lane);
-    decode_sb_tile<FULL>(d, H + h, n, sb, Vt, warp * CAS_SB, lutV, sc, lane);
+    decode_sb_tile<FULL>(d, h, n, sb, Kt, warp * CAS_SB, lutK, wscr, lane);
+    decode_sb_tile<FULL>(d, H + h, n, sb, Vt, warp * CAS_SB, lutV, wscr, lane);
     __syncthreads();
     const int64_t tok = t0 + lane;
     // scores: lane = token
@@ -233,7 +249,9 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(CombineArgs a) {
   a.o[(((int64_t)b * a.T + j) * a.Hq + hq) * CAS_BLK + dd] = L > 0.f ? O / L : 0.f;
 }
 
-size_t chunk_smem() { return (size_t)2 * kStepTok * kRow * 4 + (size_t)kQvPerCta * CAS_BLK * 4 + 512 + kWarps * 2048; }
+size_t chunk_smem() {
+  return (size_t)2 * kStepTok * kRow * 4 + (size_t)kQvPerCta * CAS_BLK * 4 + 512 + kWarps * kScratchWarp;
+}
 
 template <bool FULL, int QPW>
 int launch_chunk(const AttnArgs& a, int Hkv, cudaStream_t st) {

@@ -151,6 +151,36 @@ __device__ __forceinline__ void warp_decode_unary(const uint32_t* __restrict__ w
   }
 }
 
+// Decode of a stream known to hold at least `ncodes` codes with ncodes a
+// power of two: indices wrap with a mask instead of a bounds test.
+__device__ __forceinline__ void warp_decode_unary_pow2(const uint32_t* __restrict__ words, int nwords,
+                                                       const uint8_t* __restrict__ lut,
+                                                       uint8_t* __restrict__ out, int ncodes, int lane) {
+  const int wrap = ncodes - 1;
+  int done = 0, prev = -1;
+  for (int c0 = 0; c0 < nwords && done < ncodes; c0 += 32) {
+    const int wi = c0 + lane;
+    uint32_t w = wi < nwords ? __ldg(words + wi) : 0u;
+    const int ones = __popc(w);
+    const int incl = warp_incl_add(ones, lane);
+    int ord = done + incl - ones;
+    const int last = w ? (wi * 32 + 32 - __ffs(w)) : -1;
+    const int mx = warp_incl_max(last, lane);
+    int pv = __shfl_up_sync(CAS_FULL, mx, 1);
+    if (lane == 0) pv = -1;
+    pv = max(pv, prev) - wi * 32;  // relative to this word's MSB
+    while (w) {
+      const int i = __clz(w);
+      out[ord & wrap] = lut[(i - pv - 1) & 255];
+      pv = i;
+      ++ord;
+      w &= 0x7FFFFFFFu >> i;
+    }
+    done += __shfl_sync(CAS_FULL, incl, 31);
+    prev = max(prev, __shfl_sync(CAS_FULL, mx, 31));
+  }
+}
+
 // Same decode, writing 32-bit table entries (e.g. exponent << 23).
 __device__ __forceinline__ void warp_decode_unary32(const uint32_t* __restrict__ words, int nwords,
                                                     const uint32_t* __restrict__ lut,

@@ -45,7 +45,11 @@ __device__ __forceinline__ void mma_bf16(float c[4], const uint32_t a[4], uint32
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-template <int VAR, int NT>
+constexpr int kScratchGeneric = 2048 + kResWords * 4;
+constexpr int kScratchWarp = (int)sizeof(FastScratch) > kScratchGeneric ? (int)sizeof(FastScratch) : kScratchGeneric;
+
+// FAST: Cassandra-1, k = 64, m = 3, whole superblocks (see fast_sb_decode).
+template <int VAR, int NT, bool FAST>
 __global__ void __launch_bounds__(kThreads) verify_gemm_kernel(GemmArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const WView& w = a.w;
@@ -54,8 +58,9 @@ __global__ void __launch_bounds__(kThreads) verify_gemm_kernel(GemmArgs a) {
   uint8_t* s_lut = reinterpret_cast<uint8_t*>(red + kWarps * 256);
   uint8_t* scratch = s_lut + 256;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  SbScratch sc{scratch + warp * (2048 + kResWords * 4), scratch + warp * (2048 + kResWords * 4) + 1024,
-               reinterpret_cast<uint32_t*>(scratch + warp * (2048 + kResWords * 4) + 2048)};
+  uint8_t* wscr = scratch + warp * kScratchWarp;
+  SbScratch sc{wscr, wscr + 1024, reinterpret_cast<uint32_t*>(wscr + 2048)};
+  FastScratch& fs = *reinterpret_cast<FastScratch*>(wscr);
   for (int i = threadIdx.x; i < 256; i += kThreads) s_lut[i] = a.lut.v[i];
   __syncthreads();
 
@@ -71,7 +76,19 @@ __global__ void __launch_bounds__(kThreads) verify_gemm_kernel(GemmArgs a) {
     for (int r = warp; r < kRows; r += kWarps) {
       int64_t n = rt * kRows + r;
       uint4* dst = reinterpret_cast<uint4*>(tile + r * kTileStride + 32 * lane);
-      if (n < w.N) {
+      if (n < w.N && FAST) {
+        const int64_t s = n * w.nsr + j;
+        const int64_t gb0 = n * w.nbr + CAS_SB * j;
+        const uint32_t a0 = __ldg(w.sidx + s), a1 = __ldg(w.sidx + s + 1);
+        const uint32_t v0 = __ldg(w.vidx + s), v1 = __ldg(w.vidx + s + 1);
+        uint32_t v[16];
+        fast_sb_decode<true>(w.mask + gb0 * 4, w.ssm + gb0 * 8, w.vlo + gb0 * 8, w.vpr + gb0 * 16, w.sexp + a0,
+                             (int)(a1 - a0), w.vexp + v0, (int)(v1 - v0), s_lut, fs, lane, v);
+        dst[0] = make_uint4(v[0], v[1], v[2], v[3]);
+        dst[1] = make_uint4(v[4], v[5], v[6], v[7]);
+        dst[2] = make_uint4(v[8], v[9], v[10], v[11]);
+        dst[3] = make_uint4(v[12], v[13], v[14], v[15]);
+      } else if (n < w.N) {
         SbInfo in = sb_prepare<VAR, true>(w, n * w.nsr + j, s_lut, sc, lane);
         if (lane < 4 * nb) {
           uint32_t v[16];
@@ -133,10 +150,10 @@ __global__ void __launch_bounds__(kThreads) verify_gemm_kernel(GemmArgs a) {
   }
 }
 
-template <int VAR, int NT>
+template <int VAR, int NT, bool FAST>
 int launch(const GemmArgs& a, cudaStream_t st) {
-  size_t smem = (size_t)kRows * kTileStride * 2 + kWarps * 256 * 4 + 256 + kWarps * (2048 + kResWords * 4);
-  auto kern = verify_gemm_kernel<VAR, NT>;
+  size_t smem = (size_t)kRows * kTileStride * 2 + kWarps * 256 * 4 + 256 + kWarps * kScratchWarp;
+  auto kern = verify_gemm_kernel<VAR, NT, FAST>;
   int per_sm = occupancy((const void*)kern, kThreads, smem);
   if (per_sm < 1) return CAS_ERR_CUDA;
   int64_t ntasks = (a.w.N + kRows - 1) / kRows * a.w.nsr;
@@ -166,6 +183,7 @@ extern "C" int cas_verify_gemm(const cas_weights* W, const uint16_t* X, int T, f
   a.Y = Y;
   a.T = T;
   bool v1 = W->p.variant == 1;
-  if (T <= 8) return v1 ? launch<1, 1>(a, st) : launch<2, 1>(a, st);
-  return v1 ? launch<1, 2>(a, st) : launch<2, 2>(a, st);
+  bool fast = v1 && a.w.k == 64 && a.w.m == 3 && a.w.nbr % CAS_SB == 0;
+  if (T <= 8) return fast ? launch<1, 1, true>(a, st) : v1 ? launch<1, 1, false>(a, st) : launch<2, 1, false>(a, st);
+  return fast ? launch<1, 2, true>(a, st) : v1 ? launch<1, 2, false>(a, st) : launch<2, 2, false>(a, st);
 }

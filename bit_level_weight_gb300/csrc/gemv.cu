@@ -239,6 +239,127 @@ __global__ void __launch_bounds__(kThreads) draft_gemv_kernel(GemvArgs a) {
   }
 }
 
+// ------------------------------------------------------------------ fast path
+// Cassandra-1, k = 64, m = 3, rows made of whole superblocks (K % 1024 == 0).
+// Superblocks are visited column-major (s = j * N + n), so a warp keeps the
+// 1024 x values of its column superblock in registers (lane L: positions
+// 32L..32L+31) across rows. Per superblock, in three SIMD phases with no
+// per-lane branching:
+//   1. decode the unary stream cooperatively into exponents by kept ordinal;
+//   2. lane = ordinal (t = L + 32 i): build the fp32 draft value from its
+//      4-bit record field (offsets are compile-time: block i/2, field
+//      L + 32 (i%2)) and exponent, store it by ordinal;
+//   3. lane = mask word L: for each of its 32 positions, a kept bit selects
+//      the next value by ordinal and multiplies it with x (predicated).
+constexpr int kFastSkew = 512 + 16;  // values by ordinal, index t + t/32 (bank skew)
+struct FastWarp {
+  uint32_t rec[64];     // spec_sm records of the 8 blocks
+  uint8_t ek[512];      // exponent by kept ordinal
+  uint32_t val[kFastSkew];
+};
+
+template <int NV>
+__global__ void __launch_bounds__(kThreads) draft_gemv_fast_kernel(GemvArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const WView& w = a.w;
+  const int K = (int)w.K;
+  const int xbytes = NV * K * 2;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + xbytes);
+  uint8_t* lut8 = smem + xbytes + 16;
+  FastWarp& fw = reinterpret_cast<FastWarp*>(smem + xbytes + 16 + 256)[warp];
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_arrive_tx(bar, (uint32_t)xbytes);
+    bulk_g2s(xs, a.x, (uint32_t)xbytes, bar);
+  }
+  for (int i = threadIdx.x; i < 256; i += kThreads) lut8[i] = a.lut.v[i];
+  bool ok = mbar_wait_bounded(bar, 0);
+  if (!__syncthreads_and(ok)) {
+    if (threadIdx.x == 0) atomicExch(&g_gemv_wait_status, CAS_ERR_TIMEOUT);
+    mbar_wait_bounded(bar, 0);  // let an in-flight copy land before the CTA exits
+    return;
+  }
+
+  const int N = (int)w.N, nsr = w.nsr, nbr = w.nbr;
+  const int nsb = (int)w.nsb;
+  const int stride = gridDim.x * kWarps;
+  int jcur = -1;
+  float xr[NV][32];
+  for (int sc = blockIdx.x * kWarps + warp; sc < nsb; sc += stride) {
+    const int j = sc / N;
+    const int n = sc - j * N;
+    const int s = n * nsr + j;
+    if (j != jcur) {
+      jcur = j;
+      const uint16_t* xp = xs + CAS_BLK * CAS_SB * j + 32 * lane;
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int p = 0; p < 32; ++p) xr[v][p] = bf2f(xp[v * K + p]);
+    }
+    const int64_t gb0 = (int64_t)n * nbr + CAS_SB * j;
+    const uint32_t mw = __ldg(w.mask + gb0 * 4 + lane);
+    const int cnt = __popc(mw);
+    const int o = warp_incl_add(cnt, lane) - cnt;
+    {
+      const uint2 r = __ldg(reinterpret_cast<const uint2*>(w.ssm + gb0 * 8) + lane);
+      fw.rec[2 * lane] = r.x;
+      fw.rec[2 * lane + 1] = r.y;
+    }
+    const uint32_t b0 = __ldg(w.sidx + s), b1 = __ldg(w.sidx + s + 1);
+    warp_decode_unary_pow2(w.sexp + b0, (int)(b1 - b0), lut8, fw.ek, 512, lane);
+    __syncwarp();
+    // phase 2: values by ordinal
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int t = lane + 32 * i;
+      const int tl = lane + 32 * (i & 1);  // ordinal within block i/2
+      const uint32_t nib = (fw.rec[8 * (i >> 1) + (tl >> 3)] >> (4 * (tl & 7))) & 15u;
+      fw.val[t + (t >> 5)] = ((nib >> 3) << 31) | ((uint32_t)fw.ek[t] << 23) | ((nib & 7u) << 20);
+    }
+    __syncwarp();
+    // phase 3: positions of mask word `lane`
+    float acc[NV];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) acc[v] = 0.f;
+    int t = o;
+#pragma unroll
+    for (int p = 0; p < 32; ++p) {
+      if ((mw >> p) & 1u) {
+        const float val = __uint_as_float(fw.val[t + (t >> 5)]);
+#pragma unroll
+        for (int v = 0; v < NV; ++v) acc[v] = fmaf(val, xr[v][p], acc[v]);
+        ++t;
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      float r = warp_sumf(acc[v]);
+      if (lane == 0) atomicAdd(a.y + (int64_t)v * w.N + n, r);
+    }
+    __syncwarp();
+  }
+}
+
+template <int NV>
+int launch_fast(const GemvArgs& a, cudaStream_t st) {
+  size_t smem = (size_t)NV * a.w.K * 2 + 16 + 256 + kWarps * sizeof(FastWarp);
+  auto kern = draft_gemv_fast_kernel<NV>;
+  int per_sm = occupancy((const void*)kern, kThreads, smem);
+  if (per_sm < 1) return CAS_ERR_CUDA;
+  int64_t need = (a.w.nsb + kWarps - 1) / kWarps;
+  int g = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sm_count() * per_sm));
+  kern<<<g, kThreads, smem, st>>>(a);
+  return launch_status();
+}
+
 template <int VAR, int NV, bool FAST>
 int launch(const GemvArgs& a, cudaStream_t st) {
   size_t smem = (size_t)NV * a.w.K * 2 + 16 + 1024 + kWarps * kWarpWords * 4;
@@ -257,6 +378,7 @@ int launch(const GemvArgs& a, cudaStream_t st) {
 template <int VAR>
 int dispatch(const GemvArgs& a, int nvec, cudaStream_t st) {
   const bool fast = VAR == 1 && a.w.k == 64 && a.w.m == 3 && a.w.nbr % CAS_SB == 0;
+  if (fast && nvec <= 2) return nvec == 1 ? launch_fast<1>(a, st) : launch_fast<2>(a, st);
   switch (nvec) {
     case 1: return fast ? launch<VAR, 1, true>(a, st) : launch<VAR, 1, false>(a, st);
     case 2: return fast ? launch<VAR, 2, true>(a, st) : launch<VAR, 2, false>(a, st);
