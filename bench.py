@@ -41,7 +41,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "draft decode+GEMV GB/s (% of HBM peak); verify GEMM GB/s; µs per decode step"
-WORKLOAD = "llama3-8b-stack speculative decode step"
+WORKLOADS = {"llama3-8b": "llama3-8b-stack speculative decode step",
+             "qwen3-8b": "qwen3-8b full speculative decode step (with LM head)"}
 
 
 def parse():
@@ -50,12 +51,15 @@ def parse():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="cas", choices=["cas", "reference"])
-    ap.add_argument("--layers", type=int, default=32)
-    ap.add_argument("--ctx", type=int, default=32768)
+    ap.add_argument("--workload", default="llama3-8b", choices=["llama3-8b", "qwen3-8b"])
+    ap.add_argument("--layers", type=int, default=None)
+    ap.add_argument("--ctx", type=int, default=None)
     ap.add_argument("--keep", type=int, default=64)
     ap.add_argument("--mant", type=int, default=3)
-    ap.add_argument("--draft-len", type=int, default=4)
-    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--draft-len", type=int, default=None)
+    ap.add_argument("--batch", type=int, default=None)
+    ap.add_argument("--sweep", action="store_true",
+                    help="Cassandra-1 vs -2 over keep 20-60%% x mantissa 1-5 on the FFN matrices")
     ap.add_argument("--no-attn", action="store_true", help="weights only (no KV cache)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -68,7 +72,15 @@ def parse():
     ap.add_argument("--nvec", type=int, default=1)
     ap.add_argument("--T", type=int, default=5)
     ap.add_argument("--reps", type=int, default=20)
-    return ap.parse_args()
+    a = ap.parse_args()
+    # workload defaults: Llama-3-8B stack at batch 1, draft length 4, 32K
+    # context; Qwen3-8B step at batch 2, draft length 6, 16K context
+    dflt = {"llama3-8b": dict(layers=32, ctx=32768, draft_len=4, batch=1),
+            "qwen3-8b": dict(layers=36, ctx=16384, draft_len=6, batch=2)}[a.workload]
+    for key, val in dflt.items():
+        if getattr(a, key) is None:
+            setattr(a, key, val)
+    return a
 
 
 # ---------------------------------------------------------------------- helpers
@@ -159,8 +171,9 @@ class Stack:
 
         import synthetic
         self.cas, self.args, self.dev = cas, args, dev
-        shp = dict(synthetic.LLAMA3_8B)
+        shp = dict(synthetic.LLAMA3_8B if args.workload == "llama3-8b" else synthetic.QWEN3_8B)
         self.L = args.layers
+        self.vocab = shp.get("vocab", 0)
         h, f = shp["hidden"], shp["ffn"]
         self.hidden, self.ffn, self.nq, self.nkv, self.hd = h, f, shp["n_q"], shp["n_kv"], shp["head_dim"]
         self.mats = []  # per layer: dict name -> EncodedWeights
@@ -180,6 +193,11 @@ class Stack:
             enc = {nm: cas.encode_weights(W, 1, args.keep, args.mant) for nm, W in fused.items()}
             del fused
             self.mats.append(enc)
+        self.lm = None
+        if self.vocab:
+            Wl = synthetic.t4_weight(self.vocab, h, seed=999_983, device=dev)
+            self.lm = cas.encode_weights(Wl, 1, args.keep, args.mant)
+            del Wl
         torch.cuda.synchronize()
         self.encode_s = time.time() - t0
         self.kv = None
@@ -256,6 +274,14 @@ def run_cas(args):
                            for l in range(stk.L)) for nm in xs}
     verify_bytes = {nm: sum(stk.mats[l][nm].all_bytes() + T * stk.mats[l][nm].K * 2 + T * stk.mats[l][nm].N * 4
                             for l in range(stk.L)) for nm in Xs}
+    lm_gemv = lm_gemm = None
+    if stk.lm is not None:
+        y_lm = torch.empty(nvec, stk.vocab, dtype=torch.float32, device=dev)
+        Y_lm = torch.empty(T, stk.vocab, dtype=torch.float32, device=dev)
+        lm_gemv = cas.prepare("cas_draft_gemv", stk.lm, xs["qkv"], nvec, y_lm, st)
+        lm_gemm = cas.prepare("cas_verify_gemm", stk.lm, Xs["qkv"], T, Y_lm, st)
+        draft_bytes["lm_head"] = stk.lm.spec_bytes() + nvec * stk.hidden * 2 + nvec * stk.vocab * 4
+        verify_bytes["lm_head"] = stk.lm.all_bytes() + T * stk.hidden * 2 + T * stk.vocab * 4
 
     attn = stk.kv is not None
     if attn:
@@ -289,16 +315,20 @@ def run_cas(args):
             if attn:
                 segs.append(("attn", dattn[l][d]))
             segs.append(("gemv", seq(g["o"], g["gateup"], g["down"])))
+        if lm_gemv is not None:
+            segs.append(("gemv", lm_gemv))
     for l in range(stk.L):
         g = gemm[l]
         segs.append(("gemm", g["qkv"]))
         if attn:
             segs.append(("attn", seq(*appends[l], vattn[l])))
         segs.append(("gemm", seq(g["o"], g["gateup"], g["down"])))
+    if lm_gemm is not None:
+        segs.append(("gemm", lm_gemm))
     if attn:
         segs.append(("attn", seq(*[t for l in range(stk.L) for t in truncs[l]])))
 
-    launches_per_step = D * stk.L * 4 + stk.L * 4
+    launches_per_step = D * stk.L * 4 + stk.L * 4 + (D + 1 if lm_gemv is not None else 0)
     if attn:
         launches_per_step += D * stk.L * 2 + stk.L * (2 * B + 2) + stk.L * B
 
@@ -372,21 +402,17 @@ def run_cas(args):
     with torch.cuda.stream(st):
         e2e = e2e_draft_pass(cas, stk, xs, ys, nvec, st, steps=max(3, steps))
 
-    vals = torch.tensor([gemv_gbs, gemm_gbs, ms_per_step], dtype=torch.float64, device=dev)
     if world > 1:
-        # throughput aggregate over replicas; the slowest rank bounds the job
-        g = [torch.zeros_like(vals) for _ in range(world)]
-        dist.all_gather(g, vals)
-        gemv_gbs = min(float(t[0]) for t in g) * world
-        gemm_gbs = min(float(t[1]) for t in g) * world
-        ms_per_step = max(float(t[2]) for t in g)
+        agg = replica_aggregate(gather_stats((d_bytes, gemv_ms, v_bytes, gemm_ms, ms_per_step), world))
+        gemv_gbs, gemm_gbs, ms_per_step = agg["gemv_gbs"], agg["gemm_gbs"], agg["ms_per_step"]
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
     peak, peak_kind = peaks()
-    per_launch_bytes = sum(draft_bytes.values()) / (4 * stk.L)
-    per_launch_ms = gemv_ms / (steps * D * stk.L * 4)
+    n_gemv = 4 * stk.L + (1 if lm_gemv is not None else 0)
+    per_launch_bytes = sum(draft_bytes.values()) / n_gemv
+    per_launch_ms = gemv_ms / (steps * D * n_gemv)
     achieved = per_launch_bytes / (per_launch_ms * 1e-3) / 1e9
     out = {
         "metric": METRIC,
@@ -402,13 +428,13 @@ def run_cas(args):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {
-            "workload": WORKLOAD,
-            "layers": stk.L, "hidden": stk.hidden, "ffn": stk.ffn, "heads": f"{stk.nq}q/{stk.nkv}kv x {stk.hd}",
+            "workload": WORKLOADS[args.workload],
+            "layers": stk.L, "lm_head_rows": stk.vocab or None, "hidden": stk.hidden, "ffn": stk.ffn, "heads": f"{stk.nq}q/{stk.nkv}kv x {stk.hd}",
             "batch": B, "draft_len": D, "verify_tokens": T, "ctx": args.ctx if attn else 0,
             "keep_per_block": args.keep, "mant_bits": args.mant, "variant": "Cassandra-1",
             "weights": "Student-t(4) x 0.02/sqrt(2), fused qkv and gate|up",
             "parallelism": "replicas" if world > 1 else "single GPU",
-            "l2": "inputs larger than L2 (3.5 GB speculation stream per draft pass)",
+            "l2": f"inputs larger than L2 ({sum(draft_bytes.values()) / 1e9:.2f} GB speculation stream per draft pass)",
         },
         "verify_gemm_gbs": round(gemm_gbs, 1),
         "us_per_decode_step": round(ms_per_step * 1e3, 1),
@@ -420,8 +446,8 @@ def run_cas(args):
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
                      "traffic": (round(PROFILED_TRAFFIC_RATIO * per_launch_bytes) if PROFILED_TRAFFIC_RATIO
                                  else None),
-                     "traffic_note": "per launch: ncu dram bytes / algorithmic bytes of a 28672x4096 launch "
-                                     "x algorithmic bytes per launch of this step",
+                     "traffic_note": "per launch: (ncu dram bytes / algorithmic bytes of a 28672x4096 launch, "
+                                     "profiles/draft_gemv_28672x4096.md) x algorithmic bytes per launch of this step",
                      "algorithmic_bytes_per_launch": int(per_launch_bytes)},
         "e2e": e2e,
         "gpu_launches": launches_per_step * steps,
@@ -437,9 +463,28 @@ def run_cas(args):
 
 # DRAM traffic of the draft GEMV per algorithmic byte, from one ncu capture of
 # the current kernel on a 28672 x 4096 bench matrix (dram__bytes_read.sum +
-# dram__bytes_write.sum = 62.02 MB for 61.85 MB algorithmic; see
+# dram__bytes_write.sum = 62.20 MB for 61.85 MB algorithmic; see
 # profiles/draft_gemv_28672x4096.md). Set to None when the kernel changes.
-PROFILED_TRAFFIC_RATIO = None
+PROFILED_TRAFFIC_RATIO = 62.20 / 61.85
+
+
+def gather_stats(local: tuple, world: int) -> list:
+    """All ranks' (draft bytes, draft ms, verify bytes, verify ms, ms/step)."""
+    import torch.distributed as dist
+    out = [None] * world
+    dist.all_gather_object(out, tuple(float(v) for v in local))
+    return out
+
+
+def replica_aggregate(stats: list) -> dict:
+    """Whole-job numbers of N independent replicas (weak scaling): bytes all
+    ranks processed over the slowest rank's time; the step time is the max."""
+    d_bytes = sum(s[0] for s in stats)
+    v_bytes = sum(s[2] for s in stats)
+    gemv_ms = max(s[1] for s in stats)
+    gemm_ms = max(s[3] for s in stats)
+    return {"gemv_gbs": d_bytes / (gemv_ms * 1e-3) / 1e9, "gemm_gbs": v_bytes / (gemm_ms * 1e-3) / 1e9,
+            "ms_per_step": max(s[4] for s in stats)}
 
 
 def e2e_draft_pass(cas, stk, xs, ys, nvec, st, steps):
@@ -490,14 +535,14 @@ def run_reference(args):
     vals = [cpu_baseline(per, args.keep, args.mant) for _ in range(K)]
     v = statistics.median(x["value"] for x in vals)
     import synthetic
-    shp = synthetic.LLAMA3_8B
+    shp = synthetic.LLAMA3_8B if args.workload == "llama3-8b" else synthetic.QWEN3_8B
     spec_per_step = None
     out = {
         "impl": "reference",
         "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "layers": args.layers, "hidden": shp["hidden"], "ffn": shp["ffn"],
+        "config": {"workload": WORKLOADS[args.workload], "layers": args.layers, "hidden": shp["hidden"], "ffn": shp["ffn"],
                    "batch": args.batch, "draft_len": args.draft_len, "keep_per_block": args.keep,
                    "mant_bits": args.mant, "variant": "Cassandra-1"},
         "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
@@ -605,8 +650,55 @@ def run_micro(args):
     print(json.dumps(out), flush=True)
 
 
+def run_sweep(args):
+    """Cassandra-1 vs Cassandra-2 on the two FFN matrix shapes, keep 20..60 %
+    x mantissa 1..5: compression ratio CR = 1 - speculation bytes / bf16 bytes
+    (sections, index and padding included) and draft GEMV GB/s. One JSON line
+    per point; the points with CR in [40, 80] % are the pages' usable range."""
+    import torch
+
+    import bit_level_weight_gb300 as cas
+    import synthetic
+    from bit_level_weight_gb300 import build as _b
+    _b.build()
+    dev = torch.device("cuda", 0)
+    st = torch.cuda.Stream(device=dev)
+    for (N, K) in ((4096, 14336), (14336, 4096)):
+        W = synthetic.normal_weight(N, K, seed=N + K, std=0.02, device=dev)
+        x = synthetic.activations(1, K, seed=3, device=dev)
+        y = torch.empty(1, N, dtype=torch.float32, device=dev)
+        for keep in (0.2, 0.3, 0.4, 0.5, 0.6):
+            k = cas.cas_keep_from_ratio(keep)
+            for m in range(1, 6):
+                for variant in (1, 2):
+                    enc = cas.encode_weights(W, variant, k, m)
+                    call = cas.prepare("cas_draft_gemv", enc, x, 1, y, st)
+                    with torch.cuda.stream(st):
+                        for _ in range(3):
+                            call()
+                        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        a.record(st)
+                        for _ in range(10):
+                            call()
+                        b.record(st)
+                        torch.cuda.synchronize()
+                    ms = a.elapsed_time(b) / 10
+                    nbytes = enc.spec_bytes() + K * 2 + N * 4
+                    cr = 1.0 - enc.spec_bytes() / (2.0 * N * K)
+                    print(json.dumps({"sweep": "cassandra-1 vs -2", "N": N, "K": K, "keep": keep, "k": k, "m": m,
+                                      "variant": variant, "cr": round(cr, 4), "in_40_80": 0.4 <= cr <= 0.8,
+                                      "spec_bits_per_elem": round(enc.spec_bytes() * 8 / (N * K), 3),
+                                      "all_bits_per_elem": round(enc.all_bytes() * 8 / (N * K), 3),
+                                      "draft_gemv_us": round(ms * 1e3, 1),
+                                      "draft_gemv_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}), flush=True)
+                    del enc
+
+
 def main():
     args = parse()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.micro:
         run_micro(args)
         return
