@@ -30,7 +30,7 @@ constexpr int kThreads = 128;
 constexpr int kWarps = 4;
 constexpr int kChunk = 256;      // tokens per CTA
 constexpr int kStepTok = 32;     // tokens per step (4 superblocks)
-constexpr int kRow = CAS_BLK + 4;  // fp32 tile row stride
+constexpr int kRow = CAS_BLK + 8;  // bf16 tile row stride (272 B: conflict-free 16-byte rows)
 constexpr int kPart = CAS_BLK + 2; // floats per partial: o[128], m, l
 constexpr int kMaxBatch = 8;
 constexpr int kMaxT = 16;
@@ -42,7 +42,7 @@ struct AttnArgs {
   KvDev kv[kMaxBatch];
   const uint16_t* q;  // [B][T][Hq][128]
   float* part;        // [B][T][Hq][nchunk][kPart]
-  int B, T, Hq, G, nchunk, ngroups;
+  int B, T, Hq, G, nchunk, ngroups, qv_alloc;
   float scale;
 };
 
@@ -53,9 +53,9 @@ __device__ __forceinline__ float warp_maxf(float v) {
 }
 
 // Decodes superblock sb of stream st (n tokens) into tile rows [row0, row0+8)
-// as fp32; rows of tokens that do not exist are zero.
+// as bf16; rows of tokens that do not exist are zero.
 template <bool FULL>
-__device__ __forceinline__ void decode_sb_tile(const KvDev& d, int st, int64_t n, int64_t sb, float* tile, int row0,
+__device__ __forceinline__ void decode_sb_tile(const KvDev& d, int st, int64_t n, int64_t sb, uint16_t* tile, int row0,
                                                const uint8_t* lut, uint8_t* scratch, int lane) {
   int64_t nsb = (n + CAS_SB - 1) / CAS_SB;
   uint32_t v[16];
@@ -81,17 +81,18 @@ __device__ __forceinline__ void decode_sb_tile(const KvDev& d, int st, int64_t n
     nb = in.nb;
     if (lane < 4 * nb) sb_rebuild_word<1, FULL>(w, in, sc, lane, v);
   }
-  float* dst = tile + (row0 + (lane >> 2)) * kRow + 32 * (lane & 3);
+  uint4* dst = reinterpret_cast<uint4*>(tile + (row0 + (lane >> 2)) * kRow + 32 * (lane & 3));
   if (lane < 4 * nb) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float4 f = make_float4(__uint_as_float(v[2 * i] << 16), __uint_as_float(v[2 * i] & 0xFFFF0000u),
-                             __uint_as_float(v[2 * i + 1] << 16), __uint_as_float(v[2 * i + 1] & 0xFFFF0000u));
-      reinterpret_cast<float4*>(dst)[i] = f;
-    }
+    dst[0] = make_uint4(v[0], v[1], v[2], v[3]);
+    dst[1] = make_uint4(v[4], v[5], v[6], v[7]);
+    dst[2] = make_uint4(v[8], v[9], v[10], v[11]);
+    dst[3] = make_uint4(v[12], v[13], v[14], v[15]);
   } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) reinterpret_cast<float4*>(dst)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    dst[0] = z;
+    dst[1] = z;
+    dst[2] = z;
+    dst[3] = z;
   }
   __syncwarp();
 }
@@ -99,10 +100,10 @@ __device__ __forceinline__ void decode_sb_tile(const KvDev& d, int st, int64_t n
 template <bool FULL, int QPW>
 __global__ void __launch_bounds__(kThreads) attn_chunk_kernel(AttnArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
-  float* Kt = reinterpret_cast<float*>(smem);
-  float* Vt = Kt + kStepTok * kRow;
-  float* Qs = Vt + kStepTok * kRow;  // [kQvPerCta][128], pre-scaled
-  uint8_t* lutK = reinterpret_cast<uint8_t*>(Qs + kQvPerCta * CAS_BLK);
+  uint16_t* Kt = reinterpret_cast<uint16_t*>(smem);
+  uint16_t* Vt = Kt + kStepTok * kRow;
+  float* Qs = reinterpret_cast<float*>(Vt + kStepTok * kRow);  // [nq][128], pre-scaled
+  uint8_t* lutK = reinterpret_cast<uint8_t*>(Qs + a.qv_alloc * CAS_BLK);
   uint8_t* lutV = lutK + 256;
   uint8_t* scr = lutV + 256;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -145,15 +146,21 @@ __global__ void __launch_bounds__(kThreads) attn_chunk_kernel(AttnArgs a) {
     float s[QPW];
 #pragma unroll
     for (int i = 0; i < QPW; ++i) s[i] = 0.f;
-    const float4* krow = reinterpret_cast<const float4*>(Kt + lane * kRow);
-    for (int c = 0; c < CAS_BLK / 4; ++c) {
-      float4 k4 = krow[c];
+    const uint4* krow = reinterpret_cast<const uint4*>(Kt + lane * kRow);
+    for (int c = 0; c < CAS_BLK / 8; ++c) {
+      const uint4 k8 = krow[c];
+      const float k0 = __uint_as_float(k8.x << 16), k1 = __uint_as_float(k8.x & 0xFFFF0000u);
+      const float k2 = __uint_as_float(k8.y << 16), k3 = __uint_as_float(k8.y & 0xFFFF0000u);
+      const float k4 = __uint_as_float(k8.z << 16), k5 = __uint_as_float(k8.z & 0xFFFF0000u);
+      const float k6 = __uint_as_float(k8.w << 16), k7 = __uint_as_float(k8.w & 0xFFFF0000u);
 #pragma unroll
       for (int i = 0; i < QPW; ++i) {
         int qv = warp + kWarps * i;
         if (qv < nq) {
-          float4 q4 = reinterpret_cast<const float4*>(Qs + qv * CAS_BLK)[c];
-          s[i] = fmaf(q4.x, k4.x, fmaf(q4.y, k4.y, fmaf(q4.z, k4.z, fmaf(q4.w, k4.w, s[i]))));
+          const float4 qa = reinterpret_cast<const float4*>(Qs + qv * CAS_BLK)[2 * c];
+          const float4 qb = reinterpret_cast<const float4*>(Qs + qv * CAS_BLK)[2 * c + 1];
+          s[i] = fmaf(qa.x, k0, fmaf(qa.y, k1, fmaf(qa.z, k2, fmaf(qa.w, k3, s[i]))));
+          s[i] = fmaf(qb.x, k4, fmaf(qb.y, k5, fmaf(qb.z, k6, fmaf(qb.w, k7, s[i]))));
         }
       }
     }
@@ -173,11 +180,11 @@ __global__ void __launch_bounds__(kThreads) attn_chunk_kernel(AttnArgs a) {
       float acc0 = o_[i][0] * corr, acc1 = o_[i][1] * corr, acc2 = o_[i][2] * corr, acc3 = o_[i][3] * corr;
       for (int t = 0; t < kStepTok; ++t) {
         float pt = __shfl_sync(CAS_FULL, p, t);
-        float4 v4 = reinterpret_cast<const float4*>(Vt + t * kRow)[lane];
-        acc0 = fmaf(pt, v4.x, acc0);
-        acc1 = fmaf(pt, v4.y, acc1);
-        acc2 = fmaf(pt, v4.z, acc2);
-        acc3 = fmaf(pt, v4.w, acc3);
+        const uint2 v4 = reinterpret_cast<const uint2*>(Vt + t * kRow)[lane];
+        acc0 = fmaf(pt, __uint_as_float(v4.x << 16), acc0);
+        acc1 = fmaf(pt, __uint_as_float(v4.x & 0xFFFF0000u), acc1);
+        acc2 = fmaf(pt, __uint_as_float(v4.y << 16), acc2);
+        acc3 = fmaf(pt, __uint_as_float(v4.y & 0xFFFF0000u), acc3);
       }
       o_[i][0] = acc0; o_[i][1] = acc1; o_[i][2] = acc2; o_[i][3] = acc3;
     }
@@ -249,13 +256,13 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(CombineArgs a) {
   a.o[(((int64_t)b * a.T + j) * a.Hq + hq) * CAS_BLK + dd] = L > 0.f ? O / L : 0.f;
 }
 
-size_t chunk_smem() {
-  return (size_t)2 * kStepTok * kRow * 4 + (size_t)kQvPerCta * CAS_BLK * 4 + 512 + kWarps * kScratchWarp;
+size_t chunk_smem(int qv_alloc) {
+  return (size_t)2 * kStepTok * kRow * 2 + (size_t)qv_alloc * CAS_BLK * 4 + 512 + kWarps * kScratchWarp;
 }
 
 template <bool FULL, int QPW>
 int launch_chunk(const AttnArgs& a, int Hkv, cudaStream_t st) {
-  size_t smem = chunk_smem();
+  size_t smem = chunk_smem(a.qv_alloc);
   auto kern = attn_chunk_kernel<FULL, QPW>;
   if (occupancy((const void*)kern, kThreads, smem) < 1) return CAS_ERR_CUDA;
   dim3 grid(a.nchunk, Hkv, a.B * a.ngroups);
@@ -299,6 +306,7 @@ int run_attn(bool full, const cas_kv* const* kv, int B, const uint16_t* q, int T
   a.nchunk = nchunks(Tm);
   a.scale = 1.0f / std::sqrt((float)CAS_BLK);
   a.ngroups = (T * G + kQvPerCta - 1) / kQvPerCta;
+  a.qv_alloc = std::min(T * G, kQvPerCta);
   int qpw = (std::min(T * G, kQvPerCta) + kWarps - 1) / kWarps;
   int s;
   if (!full) {

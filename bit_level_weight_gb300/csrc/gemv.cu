@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kThreads) draft_gemv_kernel(GemvArgs a) {
 constexpr int kFastSkew = 512 + 16;  // values by ordinal, index t + t/32 (bank skew)
 struct FastWarp {
   uint32_t rec[64];     // spec_sm records of the 8 blocks
-  uint8_t ek[512];      // exponent by kept ordinal
+  alignas(16) uint8_t ek[512];  // exponent by kept ordinal
   uint32_t val[kFastSkew];
 };
 
@@ -314,7 +314,8 @@ __global__ void __launch_bounds__(kThreads) draft_gemv_fast_kernel(GemvArgs a) {
       fw.rec[2 * lane + 1] = r.y;
     }
     const uint32_t b0 = __ldg(w.sidx + s), b1 = __ldg(w.sidx + s + 1);
-    warp_decode_unary_pow2(w.sexp + b0, (int)(b1 - b0), lut8, fw.ek, 512, lane);
+    const int nw = (int)(b1 - b0);
+    warp_decode_unary_512(w.sexp + b0, nw, lut8, fw.ek, lane, stream_word(w.sexp + b0, nw, lane));
     __syncwarp();
     // phase 2: values by ordinal
 #pragma unroll

@@ -149,8 +149,8 @@ struct FastScratch {
   uint32_t sm[64];   // spec records (s<<3 | f_hi per kept value)
   uint32_t lo[64];   // cut mantissa bits per kept value
   uint32_t pr[128];  // pruned bytes (s<<7 | f)
-  uint8_t ek[512];   // exponent by kept ordinal
-  uint8_t ep[512];   // exponent by pruned ordinal
+  alignas(16) uint8_t ek[512];  // exponent by kept ordinal
+  alignas(16) uint8_t ep[512];  // exponent by pruned ordinal
   uint16_t kv[kFastSkew];
   uint16_t pv[kFastSkew];
 };
@@ -184,8 +184,10 @@ __device__ __forceinline__ void fast_sb_decode(const uint32_t* __restrict__ mask
     f.pr[4 * lane + 2] = q.z;
     f.pr[4 * lane + 3] = q.w;
   }
-  warp_decode_unary_pow2(sexp, snw, lut, f.ek, 512, lane);
-  if (FULL) warp_decode_unary_pow2(vexp, vnw, lut, f.ep, 512, lane);
+  const uint32_t sw0 = stream_word(sexp, snw, lane);
+  const uint32_t vw0 = FULL ? stream_word(vexp, vnw, lane) : 0u;
+  warp_decode_unary_512(sexp, snw, lut, f.ek, lane, sw0);
+  if (FULL) warp_decode_unary_512(vexp, vnw, lut, f.ep, lane, vw0);
   __syncwarp();
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
