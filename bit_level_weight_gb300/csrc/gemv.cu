@@ -349,6 +349,117 @@ __global__ void __launch_bounds__(kThreads) draft_gemv_fast_kernel(GemvArgs a) {
   }
 }
 
+// Cassandra-2 fast path (k = 64, m = 3, whole superblocks). The speculation
+// data has no unary stream: each kept value is a 5-bit field (sign, 4-bit q)
+// and each 32-position mask word is exactly one shared-exponent group. Phase
+// 2 stores the signed q by ordinal; phase 3 (lane = mask word = group)
+// accumulates q * x and multiplies the sum once by the group's scale
+// 2^(E' - 127 - m).
+struct Fast2Warp {
+  uint32_t rec[80 + 2];  // spec_q records of the 8 blocks (10 words each) + pad
+  float val[kFastSkew];
+};
+
+template <int NV>
+__global__ void __launch_bounds__(kThreads) draft_gemv_fast2_kernel(GemvArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const WView& w = a.w;
+  const int K = (int)w.K;
+  const int xbytes = NV * K * 2;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + xbytes);
+  Fast2Warp& fw = reinterpret_cast<Fast2Warp*>(smem + xbytes + 16)[warp];
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_arrive_tx(bar, (uint32_t)xbytes);
+    bulk_g2s(xs, a.x, (uint32_t)xbytes, bar);
+  }
+  bool ok = mbar_wait_bounded(bar, 0);
+  if (!__syncthreads_and(ok)) {
+    if (threadIdx.x == 0) atomicExch(&g_gemv_wait_status, CAS_ERR_TIMEOUT);
+    mbar_wait_bounded(bar, 0);  // let an in-flight copy land before the CTA exits
+    return;
+  }
+
+  const int N = (int)w.N, nbr = w.nbr;
+  const int nsb = (int)w.nsb;
+  const int stride = gridDim.x * kWarps;
+  int jcur = -1;
+  float xr[NV][32];
+  for (int sc = blockIdx.x * kWarps + warp; sc < nsb; sc += stride) {
+    const int j = sc / N;
+    const int n = sc - j * N;
+    if (j != jcur) {
+      jcur = j;
+      const uint16_t* xp = xs + CAS_BLK * CAS_SB * j + 32 * lane;
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int p = 0; p < 32; ++p) xr[v][p] = bf2f(xp[v * K + p]);
+    }
+    const int64_t gb0 = (int64_t)n * nbr + CAS_SB * j;
+    const uint32_t mw = __ldg(w.mask + gb0 * 4 + lane);
+    const int cnt = __popc(mw);
+    const int o = warp_incl_add(cnt, lane) - cnt;
+    const float scale = pow2_biased(max((int)__ldg(w.smx + gb0 * 4 + lane), 1) - 3);
+    const uint32_t* rsrc = w.sq + gb0 * 10;
+    fw.rec[lane] = __ldg(rsrc + lane);
+    fw.rec[32 + lane] = __ldg(rsrc + 32 + lane);
+    if (lane < 16) fw.rec[64 + lane] = __ldg(rsrc + 64 + lane);
+    __syncwarp();
+    // phase 2: signed q by ordinal
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int t = lane + 32 * i;
+      const int tl = lane + 32 * (i & 1);  // ordinal within block i/2
+      const int bit = 5 * tl;
+      const int wsel = 10 * (i >> 1) + (bit >> 5);
+      const uint32_t fld = __funnelshift_r(fw.rec[wsel], fw.rec[wsel + 1], bit & 31) & 31u;
+      const float q = (float)(fld & 15u);
+      fw.val[t + (t >> 5)] = (fld >> 4) ? -q : q;
+    }
+    __syncwarp();
+    // phase 3: positions of mask word `lane` (one shared-exponent group)
+    float acc[NV];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) acc[v] = 0.f;
+    int t = o;
+#pragma unroll
+    for (int p = 0; p < 32; ++p) {
+      if ((mw >> p) & 1u) {
+        const float val = fw.val[t + (t >> 5)];
+#pragma unroll
+        for (int v = 0; v < NV; ++v) acc[v] = fmaf(val, xr[v][p], acc[v]);
+        ++t;
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      float r = warp_sumf(acc[v] * scale);
+      if (lane == 0) atomicAdd(a.y + (int64_t)v * w.N + n, r);
+    }
+    __syncwarp();
+  }
+}
+
+template <int NV>
+int launch_fast2(const GemvArgs& a, cudaStream_t st) {
+  size_t smem = (size_t)NV * a.w.K * 2 + 16 + kWarps * sizeof(Fast2Warp);
+  auto kern = draft_gemv_fast2_kernel<NV>;
+  int per_sm = occupancy((const void*)kern, kThreads, smem);
+  if (per_sm < 1) return CAS_ERR_CUDA;
+  int64_t need = (a.w.nsb + kWarps - 1) / kWarps;
+  int g = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sm_count() * per_sm));
+  kern<<<g, kThreads, smem, st>>>(a);
+  return launch_status();
+}
+
 template <int NV>
 int launch_fast(const GemvArgs& a, cudaStream_t st) {
   size_t smem = (size_t)NV * a.w.K * 2 + 16 + 256 + kWarps * sizeof(FastWarp);
@@ -378,8 +489,9 @@ int launch(const GemvArgs& a, cudaStream_t st) {
 // sit in one 64-bit slice of one block record.
 template <int VAR>
 int dispatch(const GemvArgs& a, int nvec, cudaStream_t st) {
-  const bool fast = VAR == 1 && a.w.k == 64 && a.w.m == 3 && a.w.nbr % CAS_SB == 0;
-  if (fast && nvec <= 2) return nvec == 1 ? launch_fast<1>(a, st) : launch_fast<2>(a, st);
+  const bool fast = a.w.k == 64 && a.w.m == 3 && a.w.nbr % CAS_SB == 0 && nvec <= 2;
+  if (fast && VAR == 1) return nvec == 1 ? launch_fast<1>(a, st) : launch_fast<2>(a, st);
+  if (fast && VAR == 2) return nvec == 1 ? launch_fast2<1>(a, st) : launch_fast2<2>(a, st);
   switch (nvec) {
     case 1: return fast ? launch<VAR, 1, true>(a, st) : launch<VAR, 1, false>(a, st);
     case 2: return fast ? launch<VAR, 2, true>(a, st) : launch<VAR, 2, false>(a, st);
