@@ -58,6 +58,8 @@ def parse():
     ap.add_argument("--mant", type=int, default=3)
     ap.add_argument("--draft-len", type=int, default=None)
     ap.add_argument("--batch", type=int, default=None)
+    ap.add_argument("--capacity", action="store_true",
+                    help="max context at a fixed HBM budget from measured encoded sizes")
     ap.add_argument("--sweep", action="store_true",
                     help="Cassandra-1 vs -2 over keep 20-60%% x mantissa 1-5 on the FFN matrices")
     ap.add_argument("--no-attn", action="store_true", help="weights only (no KV cache)")
@@ -694,8 +696,77 @@ def run_sweep(args):
                     del enc
 
 
+def run_capacity(args):
+    """Memory-capacity model (the pages' 24 GB / Llama 3 8B comparison, Fig. 14):
+    model bytes and KV bytes per token measured from this library's encodings
+    (one decoder layer of weights, 4096 appended KV tokens), then the longest
+    context that fits a budget, bf16 vs Cassandra (both streams stored, as
+    the verification needs them). EAGLE-3 is modelled as bf16 plus one extra
+    bf16 decoder layer and its KV (a reading: the pages give no size)."""
+    import torch
+
+    import bit_level_weight_gb300 as cas
+    import synthetic
+    from bit_level_weight_gb300 import build as _b
+    _b.build()
+    dev = torch.device("cuda", 0)
+    shp = dict(synthetic.LLAMA3_8B)
+    L, h, nkv, hd = shp["layers"], shp["hidden"], shp["n_kv"], shp["head_dim"]
+    vocab = 128256  # Llama 3 embedding and LM head rows
+    layer_params, layer_bytes, layer_spec = 0, 0, 0
+    for idx, (nm, N, K) in enumerate(synthetic.layer_matrices(shp)):
+        W = synthetic.t4_weight(N, K, seed=idx, device=dev)
+        enc = cas.encode_weights(W, 1, args.keep, args.mant)
+        layer_params += N * K
+        layer_bytes += enc.all_bytes()
+        layer_spec += enc.spec_bytes()
+        del W, enc
+    bits_per_param = layer_bytes * 8 / layer_params
+    T = 4096
+    sk, sv = synthetic.kv_scales(0, nkv, 0, device=dev), synthetic.kv_scales(0, nkv, 1, device=dev)
+    Kc = synthetic.kv_tokens(T, nkv, seed=5, scales=sk, device=dev)
+    Vc = synthetic.kv_tokens(T, nkv, seed=6, scales=sv, device=dev)
+    kv = cas.KVCache(nkv, T, cas.params(1, args.keep, args.mant), Kc[:128], Vc[:128])
+    kv.append(Kc, Vc)
+    assert kv.status() == (T, 0)
+    k, m = args.keep, args.mant
+    rec = lambda f, w: -(-(f * w) // 32) * 4  # noqa: E731
+    per_tok_fixed = 16 + rec(k, m + 1) + rec(k, 7 - m) + rec(128 - k, 8)
+    nsb = (T + 7) // 8
+    code_bytes = 0
+    for st in range(2 * nkv):
+        code_bytes += 4 * int(kv.section("spec_sbidx", st).cpu().numpy().view("uint32")[nsb])
+        code_bytes += 4 * int(kv.section("ver_sbidx", st).cpu().numpy().view("uint32")[nsb])
+        code_bytes += 2 * 4 * (nsb + 1)
+    kv_layer_bytes = 2 * nkv * T * per_tok_fixed + code_bytes
+    kv_bits_per_elem = kv_layer_bytes * 8 / (T * 2 * nkv * hd)
+    params = L * layer_params + 2 * vocab * h
+    kv_bf16_tok = L * 2 * nkv * hd * 2
+    kv_cas_tok = kv_bf16_tok * kv_bits_per_elem / 16
+    embed_bytes = 2 * vocab * h * 2  # embedding and LM head kept bf16 in this model
+    schemes = {
+        "bf16": (params * 2, kv_bf16_tok),
+        "eagle3 (bf16 + one bf16 draft layer)": (params * 2 + layer_params * 2, kv_bf16_tok * (L + 1) / L),
+        "cassandra": (L * layer_params * bits_per_param / 8 + embed_bytes, kv_cas_tok),
+    }
+    for budget_name, budget in (("24 GB (RTX 4090 in the pages)", 24e9), ("GB300 HBM 284208 MiB", 284208 * 2**20)):
+        base = None
+        for name, (wbytes, tok) in schemes.items():
+            ctx = max(0.0, (budget - wbytes) / tok)
+            base = base or ctx
+            print(json.dumps({"capacity": budget_name, "scheme": name, "weights_gb": round(wbytes / 1e9, 3),
+                              "kv_bytes_per_token": round(tok), "max_context_tokens": int(ctx),
+                              "vs_bf16": round(ctx / base, 3) if base else None,
+                              "weight_bits_per_param": round(bits_per_param, 3) if name == "cassandra" else 16,
+                              "kv_bits_per_elem": round(kv_bits_per_elem, 3) if name == "cassandra" else 16}),
+                  flush=True)
+
+
 def main():
     args = parse()
+    if args.capacity:
+        run_capacity(args)
+        return
     if args.sweep:
         run_sweep(args)
         return

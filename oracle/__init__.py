@@ -258,3 +258,34 @@ def kv_stream_encode(tokens, variant: int, k: int, m: int, rank_of_exp, exp_of_r
     T, D = t.shape
     assert D == BLK
     return encode(t.reshape(1, T * D), variant, k, m, rank_of_exp, exp_of_rank)
+
+
+# ------------------------------------------------------------------ exponent code ablation
+def huffman_code_lengths(counts) -> np.ndarray:
+    """Huffman code length of every exponent with a nonzero count (0 for the
+    others): the optimal prefix code the blog review (section 3.2) weighs the
+    unary code against - shorter on average, but decoding needs a table over
+    2^N bit patterns or a serial parse."""
+    import heapq
+    c = np.asarray(counts, np.float64)
+    lens = np.zeros(c.size, np.int64)
+    syms = [i for i in range(c.size) if c[i] > 0]
+    if len(syms) == 1:
+        lens[syms[0]] = 1
+        return lens
+    heap = [(c[i], k, [i]) for k, i in enumerate(syms)]
+    heapq.heapify(heap)
+    tie = len(heap)
+    while len(heap) > 1:
+        a = heapq.heappop(heap)
+        b = heapq.heappop(heap)
+        for i in a[2] + b[2]:
+            lens[i] += 1
+        heapq.heappush(heap, (a[0] + b[0], tie, a[2] + b[2]))
+        tie += 1
+    return lens
+
+
+def huffman_mean_len(counts) -> float:
+    c = np.asarray(counts, np.float64)
+    return float((c * huffman_code_lengths(c)).sum() / c.sum())
