@@ -217,43 +217,76 @@ struct CombineArgs {
   float scale;
 };
 
-// One CTA of 128 threads per (sequence, query token, q head): thread = dim.
-__global__ void __launch_bounds__(128) attn_combine_kernel(CombineArgs a) {
-  __shared__ float red[4];
+// One CTA of 256 threads per (sequence, query token, q head). Warp w merges
+// chunks w, w+8, ... with lane L holding dims 4L..4L+3 (online max / sum);
+// the 8 warp results and the bf16 tail tokens are merged in shared memory.
+__global__ void __launch_bounds__(256) attn_combine_kernel(CombineArgs a) {
+  __shared__ float wm[8], wl[8];
+  __shared__ float4 wo[8][32];
   __shared__ float ts[kMaxT];
-  const int hq = blockIdx.x, j = blockIdx.y, b = blockIdx.z, dd = threadIdx.x;
-  const int lane = dd & 31, warp = dd >> 5;
+  const int hq = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t n = *(volatile const int64_t*)a.ntok[b];
   const int used = (int)min((int64_t)a.nchunk, (n + kChunk - 1) / kChunk);
   const float* P = a.part + (((int64_t)b * a.T + j) * a.Hq + hq) * a.nchunk * kPart;
   const int hk = hq / a.G;
-  // tail scores (exact bf16 tokens)
-  float qd = bf2f(a.q[(((int64_t)b * a.T + j) * a.Hq + hq) * CAS_BLK + dd]) * a.scale;
-  for (int t = 0; t < a.n_tail; ++t) {
-    float kd = bf2f(a.tail_k[(((int64_t)b * a.n_tail + t) * a.Hkv + hk) * CAS_BLK + dd]);
-    float s = warp_sumf(qd * kd);
-    if (lane == 0) red[warp] = s;
-    __syncthreads();
-    if (dd == 0) ts[t] = red[0] + red[1] + red[2] + red[3];
-    __syncthreads();
+  // tail scores (exact bf16 tokens), warp 0
+  if (warp == 0) {
+    const uint16_t* qp = a.q + (((int64_t)b * a.T + j) * a.Hq + hq) * CAS_BLK + 4 * lane;
+    for (int t = 0; t < a.n_tail; ++t) {
+      const uint16_t* kp = a.tail_k + (((int64_t)b * a.n_tail + t) * a.Hkv + hk) * CAS_BLK + 4 * lane;
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) s = fmaf(bf2f(qp[i]), bf2f(kp[i]), s);
+      s = warp_sumf(s) * a.scale;
+      if (lane == 0) ts[t] = s;
+    }
   }
-  float M = -INFINITY;
-  for (int c = 0; c < used; ++c) M = fmaxf(M, P[c * kPart + CAS_BLK]);
-  for (int t = 0; t < a.n_tail; ++t) M = fmaxf(M, ts[t]);
-  float L = 0.f, O = 0.f;
-  for (int c = 0; c < used; ++c) {
-    float mc = P[c * kPart + CAS_BLK];
+  float M = -INFINITY, L = 0.f;
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c = warp; c < used; c += 8) {
+    const float mc = P[c * kPart + CAS_BLK];
     if (mc == -INFINITY) continue;
-    float w = __expf(mc - M);
-    L += P[c * kPart + CAS_BLK + 1] * w;
-    O += P[c * kPart + dd] * w;
+    const float lc = P[c * kPart + CAS_BLK + 1];
+    // partials sit at a 130-float (520-byte) stride: 8-byte aligned, so two float2 loads
+    const float2 oa = reinterpret_cast<const float2*>(P + c * kPart)[2 * lane];
+    const float2 ob = reinterpret_cast<const float2*>(P + c * kPart)[2 * lane + 1];
+    const float4 oc = make_float4(oa.x, oa.y, ob.x, ob.y);
+    const float mn = fmaxf(M, mc);
+    const float fa = M == -INFINITY ? 0.f : __expf(M - mn), fb = __expf(mc - mn);
+    L = L * fa + lc * fb;
+    O = make_float4(O.x * fa + oc.x * fb, O.y * fa + oc.y * fb, O.z * fa + oc.z * fb, O.w * fa + oc.w * fb);
+    M = mn;
   }
-  for (int t = 0; t < a.n_tail; ++t) {
-    float w = __expf(ts[t] - M);
-    L += w;
-    O += w * bf2f(a.tail_v[(((int64_t)b * a.n_tail + t) * a.Hkv + hk) * CAS_BLK + dd]);
+  if (lane == 0) {
+    wm[warp] = M;
+    wl[warp] = L;
   }
-  a.o[(((int64_t)b * a.T + j) * a.Hq + hq) * CAS_BLK + dd] = L > 0.f ? O / L : 0.f;
+  wo[warp][lane] = O;
+  __syncthreads();
+  if (warp == 0) {
+    float Mt = -INFINITY;
+    for (int w = 0; w < 8; ++w) Mt = fmaxf(Mt, wm[w]);
+    for (int t = 0; t < a.n_tail; ++t) Mt = fmaxf(Mt, ts[t]);
+    float Lt = 0.f;
+    float4 Ot = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int w = 0; w < 8; ++w) {
+      if (wm[w] == -INFINITY) continue;
+      const float f = __expf(wm[w] - Mt);
+      Lt += wl[w] * f;
+      const float4 o = wo[w][lane];
+      Ot = make_float4(Ot.x + o.x * f, Ot.y + o.y * f, Ot.z + o.z * f, Ot.w + o.w * f);
+    }
+    for (int t = 0; t < a.n_tail; ++t) {
+      const float f = __expf(ts[t] - Mt);
+      Lt += f;
+      const uint16_t* vp = a.tail_v + (((int64_t)b * a.n_tail + t) * a.Hkv + hk) * CAS_BLK + 4 * lane;
+      Ot = make_float4(Ot.x + f * bf2f(vp[0]), Ot.y + f * bf2f(vp[1]), Ot.z + f * bf2f(vp[2]), Ot.w + f * bf2f(vp[3]));
+    }
+    const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
+    reinterpret_cast<float4*>(a.o + (((int64_t)b * a.T + j) * a.Hq + hq) * CAS_BLK)[lane] =
+        make_float4(Ot.x * inv, Ot.y * inv, Ot.z * inv, Ot.w * inv);
+  }
 }
 
 size_t chunk_smem(int qv_alloc) {
@@ -331,7 +364,7 @@ int run_attn(bool full, const cas_kv* const* kv, int B, const uint16_t* q, int T
   c.nchunk = a.nchunk;
   c.n_tail = full ? 0 : n_tail;
   c.scale = a.scale;
-  attn_combine_kernel<<<dim3(Hq, T, B), 128, 0, st>>>(c);
+  attn_combine_kernel<<<dim3(Hq, T, B), 256, 0, st>>>(c);
   return launch_status();
 }
 
