@@ -26,7 +26,7 @@ SECTIONS = (
 )
 SPEC_SECTIONS = ("mask", "spec_sm", "spec_exp", "spec_sbidx", "spec_mx", "spec_q")
 KV_SECTIONS = ("state", "tables", "mask", "spec_sm", "spec_exp", "spec_sbidx", "ver_lo", "ver_pr",
-               "ver_exp", "ver_sbidx")
+               "ver_exp", "ver_sbidx", "spec_mx", "spec_q", "ver_d", "ver_d_sbidx", "ver_res", "ver_res_sbidx")
 
 CAS_OK = 0
 

@@ -36,7 +36,10 @@ constexpr int kMaxBatch = 8;
 constexpr int kMaxT = 16;
 
 constexpr int kQvPerCta = 32;  // query vectors per CTA (8 per warp)
-constexpr int kScratchWarp = (int)sizeof(FastScratch) > 2048 ? (int)sizeof(FastScratch) : 2048;
+// per-warp decode scratch: the fast decoder's, or kept codes + pruned codes +
+// the Cassandra-2 residual words of one superblock
+constexpr int kScratchWarp =
+    (int)sizeof(FastScratch) > 2048 + 4 * kResWords ? (int)sizeof(FastScratch) : 2048 + 4 * kResWords;
 
 struct AttnArgs {
   KvDev kv[kMaxBatch];
@@ -60,7 +63,7 @@ __device__ __forceinline__ void decode_sb_tile(const KvDev& d, int st, int64_t n
   int64_t nsb = (n + CAS_SB - 1) / CAS_SB;
   uint32_t v[16];
   int nb = 0;
-  if (sb < nsb && d.k == 64 && d.m == 3 && CAS_SB * (sb + 1) <= n) {
+  if (sb < nsb && d.variant == 1 && d.k == 64 && d.m == 3 && CAS_SB * (sb + 1) <= n) {
     // whole superblock of 8 tokens: fast decoder
     const uint32_t* sidx = (const uint32_t*)kv_sec(d, CAS_KV_SPEC_SBIDX, st);
     const uint32_t* vidx = (const uint32_t*)kv_sec(d, CAS_KV_VER_SBIDX, st);
@@ -74,12 +77,18 @@ __device__ __forceinline__ void decode_sb_tile(const KvDev& d, int st, int64_t n
                          (const uint32_t*)kv_sec(d, CAS_KV_VER_EXP, st) + v0, (int)(v1 - v0), lut,
                          *reinterpret_cast<FastScratch*>(scratch), lane, v);
     nb = CAS_SB;
-  } else if (sb < nsb) {
+  } else if (sb < nsb && d.variant == 1) {
     SbScratch sc{scratch, scratch + 1024, nullptr};
     WView w = kv_stream_view(d, st, n);
     SbInfo in = sb_prepare<1, FULL>(w, sb, lut, sc, lane);
     nb = in.nb;
     if (lane < 4 * nb) sb_rebuild_word<1, FULL>(w, in, sc, lane, v);
+  } else if (sb < nsb) {
+    SbScratch sc{scratch, scratch + 1024, reinterpret_cast<uint32_t*>(scratch + 2048)};
+    WView w = kv_stream_view(d, st, n);
+    SbInfo in = sb_prepare<2, FULL>(w, sb, lut, sc, lane);
+    nb = in.nb;
+    if (lane < 4 * nb) sb_rebuild_word<2, FULL>(w, in, sc, lane, v);
   }
   uint4* dst = reinterpret_cast<uint4*>(tile + (row0 + (lane >> 2)) * kRow + 32 * (lane & 3));
   if (lane < 4 * nb) {

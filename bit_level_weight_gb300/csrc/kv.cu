@@ -1,14 +1,22 @@
 // kv.cu - compressed KV cache: layout, calibration (rank tables), online
 // append (Cassandra blog review, section 3.3: the KV cache is produced during
 // inference and encoded online), truncation (rejected draft tokens) and the
-// device status.
+// device status. Both variants: Cassandra-1 (unary exponent codes) and
+// Cassandra-2 (MX shared exponent per 32 positions).
 //
-// Append runs two kernels with one CTA per (head, K|V) stream: the first
-// computes every new token's code lengths and checks capacity and finiteness
-// (a failure sets a per-call flag and the sticky status); the second, unless
-// the flag is set, clears the stream words it will fill and encodes the tokens
-// (one warp per token). The CTA that finishes last advances n_tokens and
-// resets the per-call counters. No CTA waits on another.
+// Every (head, K|V) stream has up to three variable-length code streams:
+//   A: unary codes of kept values (C-1 exponent ranks, C-2 distances d);
+//   B: unary codes of pruned exponents (both variants);
+//   C: C-2 residual significand bits (fixed widths min(8, 7-m+d)).
+// Each is word-aligned per superblock (8 tokens) with a u32 index of word
+// offsets; the device state keeps the bit tail of every stream.
+//
+// Append runs two kernels with one CTA per stream: the first computes every
+// new token's code lengths and checks capacity and finiteness (a failure sets
+// a per-call flag and the sticky status); the second, unless the flag is set,
+// clears the stream words it will fill and encodes the tokens (one warp per
+// token). The CTA that finishes last advances n_tokens and resets the
+// per-call counters. No CTA waits on another.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -29,20 +37,24 @@ KvDev make_kv_dev(const cas_kv* kv) {
     d.stride[i] = kv->stride[i];
   }
   d.H = kv->n_kv_heads;
+  d.variant = kv->p.variant;
   d.k = kv->p.keep_per_block;
   d.m = kv->p.mant_bits;
   d.rec_sm = rec_words(d.k, d.m + 1);
+  d.rec_q = rec_words(d.k, d.m + 2);
   d.rec_lo = rec_words(d.k, 7 - d.m);
   d.rec_pr = rec_words(CAS_BLK - d.k, 8);
   d.max_tokens = kv->max_tokens;
-  d.cap_spec = kv->cap_spec_words;
-  d.cap_ver = kv->cap_ver_words;
+  d.cap_a = kv->cap_spec_words;
+  d.cap_b = kv->cap_ver_words;
+  d.cap_c = kv->stride[CAS_KV_VER_RES] / 4;
   return d;
 }
 
 int check_kv(const cas_kv* kv) {
-  if (!kv || !kv->base || kv->n_kv_heads < 1 || kv->head_dim != CAS_BLK || kv->p.variant != 1 ||
-      kv->p.keep_per_block < 0 || kv->p.keep_per_block > CAS_BLK || kv->p.mant_bits < 0 || kv->p.mant_bits > 7)
+  if (!kv || !kv->base || kv->n_kv_heads < 1 || kv->head_dim != CAS_BLK ||
+      (kv->p.variant != 1 && kv->p.variant != 2) || kv->p.keep_per_block < 0 || kv->p.keep_per_block > CAS_BLK ||
+      kv->p.mant_bits < 0 || kv->p.mant_bits > 7)
     return CAS_ERR_INVALID;
   return CAS_OK;
 }
@@ -56,29 +68,41 @@ constexpr int kChunk = 256;  // tokens whose starts are computed per round
 uint64_t a256(uint64_t x) { return (x + 255) & ~255ull; }
 
 struct KvLayout {
-  uint64_t off[16], stride[16], bytes, cap_spec, cap_ver;
+  uint64_t off[16], stride[16], bytes, cap_a, cap_b;
 };
 
 bool kv_layout(int H, int64_t Tm, cas_params p, double est, KvLayout* L) {
-  if (H < 1 || Tm < 1 || p.variant != 1 || p.keep_per_block < 0 || p.keep_per_block > CAS_BLK || p.mant_bits < 0 ||
-      p.mant_bits > 7 || !(est > 0.0) || est > 256.0)
+  if (H < 1 || Tm < 1 || (p.variant != 1 && p.variant != 2) || p.keep_per_block < 0 ||
+      p.keep_per_block > CAS_BLK || p.mant_bits < 0 || p.mant_bits > 7 || !(est > 0.0) || est > 256.0)
     return false;
-  int k = p.keep_per_block, m = p.mant_bits;
-  uint64_t S = 2ull * H, nsbm = (uint64_t)(Tm + 7) / 8;
-  L->cap_spec = (uint64_t)std::ceil((double)Tm * k * est / 32.0) + nsbm + 2;
-  L->cap_ver = (uint64_t)std::ceil((double)Tm * (CAS_BLK - k) * est / 32.0) + nsbm + 2;
+  const int k = p.keep_per_block, m = p.mant_bits;
+  const bool v1 = p.variant == 1;
+  const uint64_t S = 2ull * H, nsbm = (uint64_t)(Tm + 7) / 8, T = (uint64_t)Tm;
+  L->cap_a = (uint64_t)std::ceil((double)Tm * k * est / 32.0) + nsbm + 2;
+  L->cap_b = (uint64_t)std::ceil((double)Tm * (CAS_BLK - k) * est / 32.0) + nsbm + 2;
+  const uint64_t cap_c = v1 ? 0 : nsbm * (2ull * k + 1) + 2;  // 8 tokens x k x 8 bits per superblock
   std::memset(L->off, 0, sizeof(L->off));
   std::memset(L->stride, 0, sizeof(L->stride));
-  uint64_t state_bytes = 32 + 16 * S;
+  const uint64_t state_bytes = 32 + 24 * S;
+  const uint64_t idx = a256((nsbm + 1) * 4);
   L->stride[CAS_KV_TABLES] = 512;
-  L->stride[CAS_KV_MASK] = a256((uint64_t)Tm * 16);
-  L->stride[CAS_KV_SPEC_SM] = a256((uint64_t)Tm * rec_words(k, m + 1) * 4);
-  L->stride[CAS_KV_SPEC_EXP] = a256(L->cap_spec * 4);
-  L->stride[CAS_KV_SPEC_SBIDX] = a256((nsbm + 1) * 4);
-  L->stride[CAS_KV_VER_LO] = a256((uint64_t)Tm * rec_words(k, 7 - m) * 4);
-  L->stride[CAS_KV_VER_PR] = a256((uint64_t)Tm * rec_words(CAS_BLK - k, 8) * 4);
-  L->stride[CAS_KV_VER_EXP] = a256(L->cap_ver * 4);
-  L->stride[CAS_KV_VER_SBIDX] = a256((nsbm + 1) * 4);
+  L->stride[CAS_KV_MASK] = a256(T * 16);
+  L->stride[CAS_KV_VER_PR] = a256(T * rec_words(CAS_BLK - k, 8) * 4);
+  L->stride[CAS_KV_VER_EXP] = a256(L->cap_b * 4);
+  L->stride[CAS_KV_VER_SBIDX] = idx;
+  if (v1) {
+    L->stride[CAS_KV_SPEC_SM] = a256(T * rec_words(k, m + 1) * 4);
+    L->stride[CAS_KV_SPEC_EXP] = a256(L->cap_a * 4);
+    L->stride[CAS_KV_SPEC_SBIDX] = idx;
+    L->stride[CAS_KV_VER_LO] = a256(T * rec_words(k, 7 - m) * 4);
+  } else {
+    L->stride[CAS_KV_SPEC_MX] = a256(T * 4);
+    L->stride[CAS_KV_SPEC_Q] = a256(T * rec_words(k, m + 2) * 4);
+    L->stride[CAS_KV_VER_D] = a256(L->cap_a * 4);
+    L->stride[CAS_KV_VER_D_SBIDX] = idx;
+    L->stride[CAS_KV_VER_RES] = a256(cap_c * 4);
+    L->stride[CAS_KV_VER_RES_SBIDX] = idx;
+  }
   uint64_t run = 0;
   for (int i = 0; i < CAS_KV_NSECT; ++i) {
     L->off[i] = a256(run);
@@ -107,25 +131,23 @@ __global__ void kv_hist_kernel(const uint16_t* __restrict__ ck, const uint16_t* 
     if (h[i]) atomicAdd(hist + st * 256 + i, h[i]);
 }
 
-// Code bits of one token block (warp): spec = kept codes, ver = pruned codes.
-// Also reports whether any value is NaN/Inf.
-__device__ __forceinline__ void token_bits(const uint16_t* blk, int k, const uint8_t* roe, int lane, int* bs, int* bv,
-                                           bool* nonfinite) {
+// Code bits of one token block (warp) for streams A, B, C; also reports
+// whether any value is NaN/Inf.
+template <int VAR>
+__device__ __forceinline__ void token_bits(const uint16_t* blk, int k, int m, const uint8_t* roe, int lane,
+                                           int bits[3], bool* nonfinite) {
   uint32_t v[4];
   load_block4(blk, lane, v);
   uint32_t key[4] = {v[0] & 0x7FFFu, v[1] & 0x7FFFu, v[2] & 0x7FFFu, v[3] & 0x7FFFu};
   uint32_t kept = select_block4(key, k, lane);
-  int s = 0, u = 0;
   bool nf = false;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    int e = (v[j] >> 7) & 0xFF;
-    nf |= e == 255;
-    if ((kept >> j) & 1) s += roe[e] + 1;
-    else u += roe[e] + 1;
-  }
-  *bs = warp_sum(s);
-  *bv = warp_sum(u);
+  for (int j = 0; j < 4; ++j) nf |= ((v[j] >> 7) & 0xFF) == 255;
+  const int E = VAR == 2 ? group_shared_exp(v, kept) : 0;
+  const BlockBits b = block_lane_bits<VAR>(v, kept, E, m, roe);
+  bits[0] = warp_sum(VAR == 1 ? b.sexp : b.vd);
+  bits[1] = warp_sum(b.vexp);
+  bits[2] = warp_sum(b.vres);
   *nonfinite = __any_sync(CAS_FULL, nf);
 }
 
@@ -138,114 +160,116 @@ struct AppendArgs {
 
 // Shared per-round state of the append kernels.
 struct RoundSmem {
-  int bits_s[kChunk], bits_v[kChunk];
-  uint64_t start_s[kChunk], start_v[kChunk];
+  int bits[3][kChunk];
+  uint64_t start[3][kChunk];
   int nonfinite;
 };
 
-// Computes the starts of tokens [r0, r0+cnt) given the cursors before them;
-// returns updated cursors in cur_s / cur_v (thread 0 only). Token t starting
-// a superblock aligns its streams to a word and records the superblock index.
-__device__ void round_starts(RoundSmem& sm, int64_t t0, int cnt, uint64_t* cur_s, uint64_t* cur_v, uint32_t* sidx,
-                             uint32_t* vidx, bool write_idx) {
-  uint64_t cs = *cur_s, cv = *cur_v;
-  for (int i = 0; i < cnt; ++i) {
-    int64_t t = t0 + i;
-    if ((t & 7) == 0) {
-      cs = (cs + 31) & ~31ull;
-      cv = (cv + 31) & ~31ull;
-      if (write_idx) {
-        sidx[t >> 3] = (uint32_t)(cs >> 5);
-        vidx[t >> 3] = (uint32_t)(cv >> 5);
-      }
-    }
-    sm.start_s[i] = cs;
-    sm.start_v[i] = cv;
-    cs += sm.bits_s[i];
-    cv += sm.bits_v[i];
-  }
-  *cur_s = cs;
-  *cur_v = cv;
-}
-
-template <bool WRITE>
+template <int VAR, bool WRITE>
 __global__ void __launch_bounds__(kThreads) kv_append_kernel(AppendArgs a) {
   __shared__ RoundSmem sm;
   __shared__ uint8_t roe[256];
-  __shared__ uint64_t cur_s, cur_v;
+  __shared__ uint64_t cur[3];
   __shared__ int skip;
   const KvDev& d = a.d;
   const int st = blockIdx.x, H = d.H, head = st % H;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nstreams = VAR == 1 ? 2 : 3;
   KvState* S = kv_state(d);
   const uint16_t* src = st < H ? a.knew : a.vnew;
   for (int i = threadIdx.x; i < 256; i += kThreads) roe[i] = kv_rank_of_exp(d, st)[i];
   const int64_t n0 = *(volatile int64_t*)&S->n_tokens;
   if (threadIdx.x == 0) {
-    cur_s = kv_tail_spec(d)[st];
-    cur_v = kv_tail_ver(d)[st];
+    for (int q = 0; q < 3; ++q) cur[q] = q < nstreams ? kv_tail(d, q)[st] : 0ull;
     sm.nonfinite = 0;
     skip = WRITE ? *(volatile int32_t*)&S->call_fail : 0;
   }
   __syncthreads();
-  uint32_t* sidx = (uint32_t*)kv_sec(d, CAS_KV_SPEC_SBIDX, st);
-  uint32_t* vidx = (uint32_t*)kv_sec(d, CAS_KV_VER_SBIDX, st);
-  bool fail = !WRITE && n0 + a.T > d.max_tokens;
+  uint32_t* words[3];
+  uint32_t* idx[3];
+  uint64_t cap[3] = {d.cap_a, d.cap_b, d.cap_c};
+  for (int q = 0; q < 3; ++q) {
+    words[q] = (uint32_t*)kv_sec(d, kv_stream_sec(VAR, q), st);
+    idx[q] = (uint32_t*)kv_sec(d, kv_index_sec(VAR, q), st);
+  }
+  const bool fail = !WRITE && n0 + a.T > d.max_tokens;
   if (!skip && !fail) {
     for (int r0 = 0; r0 < a.T; r0 += kChunk) {
-      int cnt = min(kChunk, a.T - r0);
+      const int cnt = min(kChunk, a.T - r0);
       for (int i = warp; i < cnt; i += kWarps) {
-        int bs, bv;
+        int bits[3];
         bool nf;
-        token_bits(src + ((int64_t)(r0 + i) * H + head) * CAS_BLK, d.k, roe, lane, &bs, &bv, &nf);
+        token_bits<VAR>(src + ((int64_t)(r0 + i) * H + head) * CAS_BLK, d.k, d.m, roe, lane, bits, &nf);
         if (lane == 0) {
-          sm.bits_s[i] = bs;
-          sm.bits_v[i] = bv;
+          for (int q = 0; q < 3; ++q) sm.bits[q][i] = bits[q];
           if (nf) sm.nonfinite = 1;
         }
       }
       __syncthreads();
-      uint64_t before_s = cur_s, before_v = cur_v;
+      uint64_t before[3] = {cur[0], cur[1], cur[2]};
       __syncthreads();
       if (threadIdx.x == 0) {
-        uint64_t cs = cur_s, cv = cur_v;
-        round_starts(sm, n0 + r0, cnt, &cs, &cv, sidx, vidx, WRITE);
-        cur_s = cs;
-        cur_v = cv;
+        // token t starting a superblock aligns every stream to a word and
+        // records the superblock's word offsets
+        uint64_t c[3] = {cur[0], cur[1], cur[2]};
+        for (int i = 0; i < cnt; ++i) {
+          const int64_t t = n0 + r0 + i;
+          for (int q = 0; q < nstreams; ++q) {
+            if ((t & 7) == 0) {
+              c[q] = (c[q] + 31) & ~31ull;
+              if (WRITE) idx[q][t >> 3] = (uint32_t)(c[q] >> 5);
+            }
+            sm.start[q][i] = c[q];
+            c[q] += sm.bits[q][i];
+          }
+        }
+        for (int q = 0; q < 3; ++q) cur[q] = c[q];
       }
       __syncthreads();
       if (WRITE) {
-        // clear [before, end) of both streams: partial first word keeps its old bits
-        uint32_t* ws = (uint32_t*)kv_sec(d, CAS_KV_SPEC_EXP, st);
-        uint32_t* wv = (uint32_t*)kv_sec(d, CAS_KV_VER_EXP, st);
-        uint64_t e_s = (cur_s + 31) >> 5, e_v = (cur_v + 31) >> 5;
-        for (uint64_t i = (before_s >> 5) + threadIdx.x; i < e_s; i += kThreads) {
-          uint32_t keep = (i == (before_s >> 5) && (before_s & 31)) ? ~(0xFFFFFFFFu >> (before_s & 31)) : 0u;
-          if (i < d.cap_spec) ws[i] &= keep;
-        }
-        for (uint64_t i = (before_v >> 5) + threadIdx.x; i < e_v; i += kThreads) {
-          uint32_t keep = (i == (before_v >> 5) && (before_v & 31)) ? ~(0xFFFFFFFFu >> (before_v & 31)) : 0u;
-          if (i < d.cap_ver) wv[i] &= keep;
+        // clear [before, end) of every stream; a partial first word keeps its old bits
+        for (int q = 0; q < nstreams; ++q) {
+          const uint64_t b0 = before[q], e = (cur[q] + 31) >> 5;
+          for (uint64_t i = (b0 >> 5) + threadIdx.x; i < e; i += kThreads) {
+            uint32_t keep = 0u;
+            if (i == (b0 >> 5) && (b0 & 31)) keep = q == 2 ? (0xFFFFFFFFu >> (32 - (b0 & 31))) : ~(0xFFFFFFFFu >> (b0 & 31));
+            if (i < cap[q]) words[q][i] &= keep;
+          }
         }
         __syncthreads();
         for (int i = warp; i < cnt; i += kWarps) {
-          int64_t t = n0 + r0 + i;
+          const int64_t t = n0 + r0 + i;
           uint32_t* mask = (uint32_t*)kv_sec(d, CAS_KV_MASK, st) + t * 4;
-          uint32_t* rs = (uint32_t*)kv_sec(d, CAS_KV_SPEC_SM, st) + t * d.rec_sm;
-          uint32_t* rl = (uint32_t*)kv_sec(d, CAS_KV_VER_LO, st) + t * d.rec_lo;
           uint32_t* rp = (uint32_t*)kv_sec(d, CAS_KV_VER_PR, st) + t * d.rec_pr;
-          for (int q = lane; q < d.rec_sm; q += 32) rs[q] = 0u;
-          for (int q = lane; q < d.rec_lo; q += 32) rl[q] = 0u;
+          uint32_t* rs;
+          uint32_t* rl = nullptr;
+          uint8_t* mx = nullptr;
+          int rs_words, rl_words = 0;
+          if (VAR == 1) {
+            rs = (uint32_t*)kv_sec(d, CAS_KV_SPEC_SM, st) + t * d.rec_sm;
+            rs_words = d.rec_sm;
+            rl = (uint32_t*)kv_sec(d, CAS_KV_VER_LO, st) + t * d.rec_lo;
+            rl_words = d.rec_lo;
+          } else {
+            rs = (uint32_t*)kv_sec(d, CAS_KV_SPEC_Q, st) + t * d.rec_q;
+            rs_words = d.rec_q;
+            mx = kv_sec(d, CAS_KV_SPEC_MX, st) + t * 4;
+          }
+          for (int q = lane; q < rs_words; q += 32) rs[q] = 0u;
+          for (int q = lane; q < rl_words; q += 32) rl[q] = 0u;
           for (int q = lane; q < d.rec_pr; q += 32) rp[q] = 0u;
           __syncwarp();
           uint32_t v[4];
           load_block4(src + ((int64_t)(r0 + i) * H + head) * CAS_BLK, lane, v);
-          BlockDst dst{mask, rs, rl, rp, nullptr};
-          Stream ss{ws, sm.start_s[i], d.cap_spec};
-          Stream sv{wv, sm.start_v[i], d.cap_ver};
-          Stream dummy{nullptr, 0, 0};
-          Stream dummy2{nullptr, 0, 0};
-          encode_block<1>(v, d.k, d.m, roe, dst, ss, sv, dummy, dummy2, lane, ~0ull);
+          BlockDst dst{mask, rs, rl, rp, mx};
+          Stream sa{words[0], sm.start[0][i], cap[0]};
+          Stream sb{words[1], sm.start[1][i], cap[1]};
+          Stream sc{words[2], VAR == 2 ? sm.start[2][i] : 0ull, cap[2]};
+          Stream none{nullptr, 0, 0};
+          if (VAR == 1)
+            encode_block<1>(v, d.k, d.m, roe, dst, sa, sb, none, none, lane, ~0ull);
+          else
+            encode_block<2>(v, d.k, d.m, roe, dst, none, sb, sa, sc, lane, ~0ull);
         }
       }
       __syncthreads();
@@ -253,19 +277,20 @@ __global__ void __launch_bounds__(kThreads) kv_append_kernel(AppendArgs a) {
   }
   if (threadIdx.x == 0) {
     if (!WRITE) {
-      bool cap = fail || ((cur_s + 31) >> 5) > d.cap_spec || ((cur_v + 31) >> 5) > d.cap_ver;
-      int err = sm.nonfinite ? CAS_ERR_NONFINITE : (cap ? CAS_ERR_CAPACITY : CAS_OK);
+      bool over = fail;
+      for (int q = 0; q < nstreams; ++q) over |= ((cur[q] + 31) >> 5) > cap[q];
+      const int err = sm.nonfinite ? CAS_ERR_NONFINITE : (over ? CAS_ERR_CAPACITY : CAS_OK);
       if (err) {
         atomicExch(&S->call_fail, 1);
         atomicCAS(&S->status, 0, err);
       }
     } else {
       if (!skip) {
-        int64_t n1 = n0 + a.T;
-        kv_tail_spec(d)[st] = cur_s;
-        kv_tail_ver(d)[st] = cur_v;
-        sidx[(n1 + 7) >> 3] = (uint32_t)((cur_s + 31) >> 5);
-        vidx[(n1 + 7) >> 3] = (uint32_t)((cur_v + 31) >> 5);
+        const int64_t n1 = n0 + a.T;
+        for (int q = 0; q < nstreams; ++q) {
+          kv_tail(d, q)[st] = cur[q];
+          idx[q][(n1 + 7) >> 3] = (uint32_t)((cur[q] + 31) >> 5);
+        }
       }
       __threadfence();
       unsigned int prev = atomicAdd(&S->done, 1u);
@@ -312,29 +337,51 @@ __device__ uint64_t after_nth_one(const uint32_t* words, uint64_t w0, uint64_t w
   return wend * 32;
 }
 
+// Truncation: the new tail of each stream is found inside the superblock of
+// the last kept token - after its r*k kept codes (stream A), r*(128-k) pruned
+// codes (stream B) and, for Cassandra-2, after the residual widths of those r*k
+// kept values, which are read from their d codes (stream C).
+template <int VAR>
 __global__ void kv_truncate_kernel(KvDev d, int64_t n_req) {
+  __shared__ uint8_t s_d[CAS_SB * CAS_BLK];
   const int st = blockIdx.x, lane = threadIdx.x & 31;
   KvState* S = kv_state(d);
   const int64_t n0 = *(volatile int64_t*)&S->n_tokens;
   const int64_t n = n_req < n0 ? n_req : n0;
+  const int nstreams = VAR == 1 ? 2 : 3;
   if (n < n0) {
-    const uint32_t* ws = (const uint32_t*)kv_sec(d, CAS_KV_SPEC_EXP, st);
-    const uint32_t* wv = (const uint32_t*)kv_sec(d, CAS_KV_VER_EXP, st);
-    uint32_t* sidx = (uint32_t*)kv_sec(d, CAS_KV_SPEC_SBIDX, st);
-    uint32_t* vidx = (uint32_t*)kv_sec(d, CAS_KV_VER_SBIDX, st);
-    uint64_t ts = 0, tv = 0;
+    uint64_t tail[3] = {0, 0, 0};
+    const uint64_t cap[3] = {d.cap_a, d.cap_b, d.cap_c};
+    const int64_t sb = n > 0 ? (n - 1) >> 3 : 0;
     if (n > 0) {
-      int64_t sb = (n - 1) >> 3, r = n - 8 * sb;
-      uint64_t end_s = min((uint64_t)d.cap_spec, (kv_tail_spec(d)[st] + 31) >> 5);
-      uint64_t end_v = min((uint64_t)d.cap_ver, (kv_tail_ver(d)[st] + 31) >> 5);
-      ts = after_nth_one(ws, sidx[sb], end_s, r * d.k, lane);
-      tv = after_nth_one(wv, vidx[sb], end_v, r * (CAS_BLK - d.k), lane);
+      const int64_t r = n - 8 * sb;
+      const int64_t cnt[2] = {r * d.k, r * (CAS_BLK - d.k)};
+      for (int q = 0; q < 2; ++q) {
+        const uint32_t* w = (const uint32_t*)kv_sec(d, kv_stream_sec(VAR, q), st);
+        const uint32_t* ix = (const uint32_t*)kv_sec(d, kv_index_sec(VAR, q), st);
+        const uint64_t end = min(cap[q], (kv_tail(d, q)[st] + 31) >> 5);
+        tail[q] = after_nth_one(w, ix[sb], end, cnt[q], lane);
+      }
+      if (VAR == 2) {
+        const uint32_t* w = (const uint32_t*)kv_sec(d, CAS_KV_VER_D, st);
+        const uint32_t* ix = (const uint32_t*)kv_sec(d, CAS_KV_VER_D_SBIDX, st);
+        const uint32_t* rix = (const uint32_t*)kv_sec(d, CAS_KV_VER_RES_SBIDX, st);
+        const int ncodes = (int)cnt[0];
+        const int nw = (int)(min(cap[0], (kv_tail(d, 0)[st] + 31) >> 5) - ix[sb]);
+        warp_decode_unary_raw(w + ix[sb], nw, s_d, ncodes, lane);
+        __syncwarp();
+        int sum = 0;
+        for (int i = lane; i < ncodes; i += 32) sum += min(8, 7 - d.m + (int)s_d[i]);
+        sum = warp_sum(sum);
+        tail[2] = (uint64_t)rix[sb] * 32 + sum;
+      }
     }
     if (lane == 0) {
-      kv_tail_spec(d)[st] = ts;
-      kv_tail_ver(d)[st] = tv;
-      sidx[(n + 7) >> 3] = (uint32_t)((ts + 31) >> 5);
-      vidx[(n + 7) >> 3] = (uint32_t)((tv + 31) >> 5);
+      for (int q = 0; q < nstreams; ++q) {
+        kv_tail(d, q)[st] = tail[q];
+        uint32_t* ix = (uint32_t*)kv_sec(d, kv_index_sec(VAR, q), st);
+        ix[(n + 7) >> 3] = (uint32_t)((tail[q] + 31) >> 5);
+      }
     }
   }
   if (lane == 0) {
@@ -372,8 +419,8 @@ extern "C" int cas_kv_init(cas_kv* kv, void* buf, uint64_t bytes, int H, int64_t
   kv->head_dim = CAS_BLK;
   kv->p = p;
   kv->max_tokens = Tm;
-  kv->cap_spec_words = L.cap_spec;
-  kv->cap_ver_words = L.cap_ver;
+  kv->cap_spec_words = L.cap_a;
+  kv->cap_ver_words = L.cap_b;
   kv->base = buf;
   kv->bytes = L.bytes;
   for (int i = 0; i < CAS_KV_NSECT; ++i) {
@@ -422,8 +469,13 @@ extern "C" int cas_encode_kv_append(cas_kv* kv, const uint16_t* knew, const uint
   AppendArgs a{make_kv_dev(kv), knew, vnew, T};
   cudaStream_t st = (cudaStream_t)stream;
   int S = 2 * kv->n_kv_heads;
-  kv_append_kernel<false><<<S, kThreads, 0, st>>>(a);
-  kv_append_kernel<true><<<S, kThreads, 0, st>>>(a);
+  if (kv->p.variant == 1) {
+    kv_append_kernel<1, false><<<S, kThreads, 0, st>>>(a);
+    kv_append_kernel<1, true><<<S, kThreads, 0, st>>>(a);
+  } else {
+    kv_append_kernel<2, false><<<S, kThreads, 0, st>>>(a);
+    kv_append_kernel<2, true><<<S, kThreads, 0, st>>>(a);
+  }
   return launch_status();
 }
 
@@ -431,7 +483,10 @@ extern "C" int cas_kv_truncate(cas_kv* kv, int64_t n, void* stream) {
   int s = check_kv(kv);
   if (s) return s;
   if (n < 0) return CAS_ERR_INVALID;
-  kv_truncate_kernel<<<2 * kv->n_kv_heads, 32, 0, (cudaStream_t)stream>>>(make_kv_dev(kv), n);
+  if (kv->p.variant == 1)
+    kv_truncate_kernel<1><<<2 * kv->n_kv_heads, 32, 0, (cudaStream_t)stream>>>(make_kv_dev(kv), n);
+  else
+    kv_truncate_kernel<2><<<2 * kv->n_kv_heads, 32, 0, (cudaStream_t)stream>>>(make_kv_dev(kv), n);
   return launch_status();
 }
 

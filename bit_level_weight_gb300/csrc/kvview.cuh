@@ -12,10 +12,10 @@ struct KvDev {
   uint8_t* base;
   uint64_t off[CAS_KV_NSECT];
   uint64_t stride[CAS_KV_NSECT];
-  int H, k, m;
-  int rec_sm, rec_lo, rec_pr;
+  int H, variant, k, m;
+  int rec_sm, rec_q, rec_lo, rec_pr;
   int64_t max_tokens;
-  uint64_t cap_spec, cap_ver;
+  uint64_t cap_a, cap_b, cap_c;  // words of the three code streams (per stream)
 };
 
 // device state (STATE section)
@@ -25,15 +25,23 @@ struct KvState {
   int32_t call_fail;
   uint32_t done;
   uint32_t pad[3];
-  // followed by uint64 tail_spec[S], tail_ver[S]
+  // followed by uint64 tails[3][S]: kept-value unary stream (A), pruned
+  // exponents (B), Cassandra-2 residuals (C)
 };
 static_assert(sizeof(KvState) == 32, "state header");
 
 __host__ __device__ inline KvState* kv_state(const KvDev& d) { return (KvState*)(d.base + d.off[CAS_KV_STATE]); }
-__host__ __device__ inline uint64_t* kv_tail_spec(const KvDev& d) {
-  return (uint64_t*)(d.base + d.off[CAS_KV_STATE] + sizeof(KvState));
+__host__ __device__ inline uint64_t* kv_tail(const KvDev& d, int which) {
+  return (uint64_t*)(d.base + d.off[CAS_KV_STATE] + sizeof(KvState)) + which * 2 * d.H;
 }
-__host__ __device__ inline uint64_t* kv_tail_ver(const KvDev& d) { return kv_tail_spec(d) + 2 * d.H; }
+// sections of the three code streams and their superblock indices
+__host__ __device__ inline int kv_stream_sec(int variant, int which) {
+  return which == 0 ? (variant == 1 ? CAS_KV_SPEC_EXP : CAS_KV_VER_D) : which == 1 ? CAS_KV_VER_EXP : CAS_KV_VER_RES;
+}
+__host__ __device__ inline int kv_index_sec(int variant, int which) {
+  return which == 0 ? (variant == 1 ? CAS_KV_SPEC_SBIDX : CAS_KV_VER_D_SBIDX)
+                    : which == 1 ? CAS_KV_VER_SBIDX : CAS_KV_VER_RES_SBIDX;
+}
 __host__ __device__ inline uint8_t* kv_sec(const KvDev& d, int sec, int st) {
   return d.base + d.off[sec] + (uint64_t)st * d.stride[sec];
 }
@@ -53,15 +61,22 @@ __device__ inline WView kv_stream_view(const KvDev& d, int st, int64_t n) {
   w.vpr = (const uint32_t*)kv_sec(d, CAS_KV_VER_PR, st);
   w.vexp = (const uint32_t*)kv_sec(d, CAS_KV_VER_EXP, st);
   w.vidx = (const uint32_t*)kv_sec(d, CAS_KV_VER_SBIDX, st);
+  w.smx = kv_sec(d, CAS_KV_SPEC_MX, st);
+  w.sq = (const uint32_t*)kv_sec(d, CAS_KV_SPEC_Q, st);
+  w.vd = (const uint32_t*)kv_sec(d, CAS_KV_VER_D, st);
+  w.vdidx = (const uint32_t*)kv_sec(d, CAS_KV_VER_D_SBIDX, st);
+  w.vres = (const uint32_t*)kv_sec(d, CAS_KV_VER_RES, st);
+  w.vresidx = (const uint32_t*)kv_sec(d, CAS_KV_VER_RES_SBIDX, st);
   w.N = 1;
   w.K = n * CAS_BLK;
   w.nbr = (int)n;
   w.nsr = (int)((n + CAS_SB - 1) / CAS_SB);
   w.nsb = w.nsr;
-  w.variant = 1;
+  w.variant = d.variant;
   w.k = d.k;
   w.m = d.m;
   w.rec_sm = d.rec_sm;
+  w.rec_q = d.rec_q;
   w.rec_lo = d.rec_lo;
   w.rec_pr = d.rec_pr;
   return w;

@@ -160,10 +160,13 @@ int cas_reconstruct(const cas_weights* W, uint16_t* out, void* stream);
 /* Sections of a KV buffer. Streams are numbered kv * n_kv_heads + head
  * (kv 0 = K, 1 = V); section i of stream st starts at off[i] + st * stride[i].
  * STATE holds the device state: int64 n_tokens, int32 sticky status, two
- * internal counters, then u64 spec-code tails [S] and verification-code tails
- * [S] (S = 2 * n_kv_heads). TABLES holds per stream exp_of_rank[256] then
+ * internal counters, then three u64 code tails per stream, [3][S] with
+ * S = 2 * n_kv_heads: the kept-value unary stream (Cassandra-1 exponents,
+ * Cassandra-2 distances d), the pruned-exponent unary stream and the
+ * Cassandra-2 residual stream. TABLES holds per stream exp_of_rank[256] then
  * rank_of_exp[256]. The other sections are those of an encoded weight tensor
- * with one row per stream and one block per token, sized for max_tokens. */
+ * with one row per stream and one block per token, sized for max_tokens;
+ * sections the variant does not use have stride 0. */
 enum {
   CAS_KV_STATE = 0,
   CAS_KV_TABLES,
@@ -175,6 +178,12 @@ enum {
   CAS_KV_VER_PR,
   CAS_KV_VER_EXP,
   CAS_KV_VER_SBIDX,
+  CAS_KV_SPEC_MX,
+  CAS_KV_SPEC_Q,
+  CAS_KV_VER_D,
+  CAS_KV_VER_D_SBIDX,
+  CAS_KV_VER_RES,
+  CAS_KV_VER_RES_SBIDX,
   CAS_KV_NSECT
 };
 
@@ -182,8 +191,8 @@ typedef struct cas_kv {
   int32_t n_kv_heads, head_dim;
   cas_params p;
   int64_t max_tokens;
-  uint64_t cap_spec_words;  /* code-stream capacity per stream, u32 words */
-  uint64_t cap_ver_words;
+  uint64_t cap_spec_words;  /* kept-value unary stream capacity per stream, u32 words */
+  uint64_t cap_ver_words;   /* pruned-exponent unary stream capacity per stream */
   void* base;               /* device buffer */
   uint64_t bytes;
   uint64_t off[16];         /* section offsets (see cas_kv_plan)          */
@@ -191,8 +200,9 @@ typedef struct cas_kv {
 } cas_kv;
 
 /* Bytes of device buffer one cas_kv needs: est_bits_per_code is the planned
- * mean unary code length of both code streams; each stream gets that many bits
- * per code plus one word of alignment slack per superblock. Pruned (small)
+ * mean unary code length of the unary streams; each stream gets that many bits
+ * per code plus one word of alignment slack per superblock (the Cassandra-2
+ * residual stream is sized for its worst case, 8 bits per kept value). Pruned (small)
  * values have more spread exponents and longer codes than kept ones: on
  * N(0,1) x LogNormal(0,0.5) K/V with k = 64 they average about 4 to 5 bits,
  * so 6.0 leaves room; an append that would overflow sets CAS_ERR_CAPACITY. */

@@ -1,4 +1,5 @@
-"""GPU parity of the compressed KV cache and the attention kernels.
+"""GPU parity of the compressed KV cache and the attention kernels, both
+variants (Cassandra-1 unary exponent codes, Cassandra-2 shared exponents).
 
 Online append: every stream byte-exact with the oracle's encoding of the same
 tokens (a stream = one row whose blocks are the tokens); chunked appends equal
@@ -38,8 +39,8 @@ def make_tokens(T, H, layer=0, seed=0):
     return K, V
 
 
-def new_cache(cas, H, Tm, K, V, k=64, m=3, calib=16, est=6.0):
-    return cas.KVCache(H, Tm, cas.params(1, k, m), K[:calib].cuda(), V[:calib].cuda(), est)
+def new_cache(cas, H, Tm, K, V, k=64, m=3, calib=16, est=6.0, variant=1):
+    return cas.KVCache(H, Tm, cas.params(variant, k, m), K[:calib].cuda(), V[:calib].cuda(), est)
 
 
 def stream_sections(kv, st, n):
@@ -47,18 +48,30 @@ def stream_sections(kv, st, n):
     k, m = kv.desc.p.keep_per_block, kv.desc.p.mant_bits
     rec = lambda f, w: -(-(f * w) // 32)  # noqa: E731
     nsb = -(-n // 8)
-    sidx = kv.section("spec_sbidx", st).cpu().numpy().view(np.uint32)[:nsb + 1]
-    vidx = kv.section("ver_sbidx", st).cpu().numpy().view(np.uint32)[:nsb + 1]
-    return {
-        "mask": kv.section("mask", st).cpu().numpy()[:n * 16],
-        "spec_sm": kv.section("spec_sm", st).cpu().numpy()[:n * rec(k, m + 1) * 4],
-        "spec_exp": kv.section("spec_exp", st).cpu().numpy()[:int(sidx[-1]) * 4],
-        "spec_sbidx": sidx.tobytes(),
-        "ver_lo": kv.section("ver_lo", st).cpu().numpy()[:n * rec(k, 7 - m) * 4],
-        "ver_pr": kv.section("ver_pr", st).cpu().numpy()[:n * rec(128 - k, 8) * 4],
-        "ver_exp": kv.section("ver_exp", st).cpu().numpy()[:int(vidx[-1]) * 4],
-        "ver_sbidx": vidx.tobytes(),
-    }
+    sec = lambda name: kv.section(name, st).cpu().numpy()  # noqa: E731
+    out = {"mask": sec("mask")[:n * 16], "ver_pr": sec("ver_pr")[:n * rec(128 - k, 8) * 4]}
+
+    def stream(words, index):
+        ix = sec(index).view(np.uint32)[:nsb + 1]
+        out[index] = ix.tobytes()
+        out[words] = sec(words)[:int(ix[-1]) * 4]
+
+    stream("ver_exp", "ver_sbidx")
+    if kv.desc.p.variant == 1:
+        out["spec_sm"] = sec("spec_sm")[:n * rec(k, m + 1) * 4]
+        out["ver_lo"] = sec("ver_lo")[:n * rec(k, 7 - m) * 4]
+        stream("spec_exp", "spec_sbidx")
+    else:
+        out["spec_mx"] = sec("spec_mx")[:n * 4]
+        out["spec_q"] = sec("spec_q")[:n * rec(k, m + 2) * 4]
+        stream("ver_d", "ver_d_sbidx")
+        stream("ver_res", "ver_res_sbidx")
+    return out
+
+
+def state_bytes(kv):
+    o = int(kv.desc.off[0])
+    return kv.buf[o:o + 32 + 24 * 2 * kv.H].cpu()
 
 
 def assert_streams_equal(a, b):
@@ -69,11 +82,13 @@ def assert_streams_equal(a, b):
         assert x == y, key
 
 
-@pytest.mark.parametrize("T,k,m", [(37, 64, 3), (8, 64, 3), (64, 38, 3), (19, 128, 7), (11, 0, 2), (29, 77, 5)])
-def test_append_matches_oracle(cas, orc, T, k, m):
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("T,k,m", [(37, 64, 3), (8, 64, 3), (64, 38, 3), (19, 128, 7), (11, 0, 2), (29, 77, 5),
+                                   (21, 128, 0)])
+def test_append_matches_oracle(cas, orc, T, k, m, variant):
     H = 3
     K, V = make_tokens(T, H, seed=T)
-    kv = new_cache(cas, H, 100, K, V, k, m, calib=min(16, T))
+    kv = new_cache(cas, H, 100, K, V, k, m, calib=min(16, T), variant=variant)
     kv.append(K.cuda(), V.cuda())
     n, st = kv.status()
     assert (n, st) == (T, 0)
@@ -85,7 +100,7 @@ def test_append_matches_oracle(cas, orc, T, k, m):
             c = orc.exp_hist(calib[:, h])
             eor_ref, roe_ref = orc.rank_table(c)
             assert np.array_equal(eor, eor_ref) and np.array_equal(roe, roe_ref)
-            ref = orc.kv_stream_encode(np16(src[:, h]), 1, k, m, roe, eor)
+            ref = orc.kv_stream_encode(np16(src[:, h]), variant, k, m, roe, eor)
             got = stream_sections(kv, s, T)
             for name, val in got.items():
                 want = ref.section(name).tobytes()
@@ -93,16 +108,17 @@ def test_append_matches_oracle(cas, orc, T, k, m):
                 assert val == want, (name, kvi, h)
 
 
-def test_chunked_equals_token_by_token(cas):
+@pytest.mark.parametrize("variant", [1, 2])
+def test_chunked_equals_token_by_token(cas, variant):
     H, T = 2, 45
     K, V = make_tokens(T, H, seed=5)
-    a = new_cache(cas, H, 64, K, V)
-    b = new_cache(cas, H, 64, K, V)
+    a = new_cache(cas, H, 64, K, V, variant=variant)
+    b = new_cache(cas, H, 64, K, V, variant=variant)
     a.append(K.cuda(), V.cuda())
     for t in range(T):
         b.append(K[t:t + 1].cuda(), V[t:t + 1].cuda())
     for chunks in ((3, 17, 25), ):
-        c = new_cache(cas, H, 64, K, V)
+        c = new_cache(cas, H, 64, K, V, variant=variant)
         p = 0
         for e in chunks + (T,):
             c.append(K[p:e].cuda(), V[p:e].cuda())
@@ -111,18 +127,19 @@ def test_chunked_equals_token_by_token(cas):
             assert_streams_equal(stream_sections(a, s, T), stream_sections(c, s, T))
     for s in range(2 * H):
         assert_streams_equal(stream_sections(a, s, T), stream_sections(b, s, T))
-    assert torch.equal(a.section("state", 0)[:8 + 32 * H + 24], b.section("state", 0)[:8 + 32 * H + 24])
+    assert torch.equal(state_bytes(a), state_bytes(b))
 
 
+@pytest.mark.parametrize("variant", [1, 2])
 @pytest.mark.parametrize("cut", [0, 1, 7, 8, 9, 30, 40])
-def test_truncate_then_append(cas, cut):
+def test_truncate_then_append(cas, cut, variant):
     H, T = 2, 40
     K, V = make_tokens(T, H, seed=9)
     K2, V2 = make_tokens(T, H, seed=77)
-    ref = new_cache(cas, H, 96, K, V)
+    ref = new_cache(cas, H, 96, K, V, variant=variant)
     ref.append(K[:cut].cuda(), V[:cut].cuda())
     ref.append(K2.cuda(), V2.cuda())
-    kv = new_cache(cas, H, 96, K, V)
+    kv = new_cache(cas, H, 96, K, V, variant=variant)
     kv.append(K.cuda(), V.cuda())
     kv.truncate(cut)
     assert kv.status() == (cut, 0)
@@ -130,14 +147,16 @@ def test_truncate_then_append(cas, cut):
     assert kv.status() == (cut + T, 0)
     for s in range(2 * H):
         assert_streams_equal(stream_sections(ref, s, cut + T), stream_sections(kv, s, cut + T))
+    assert torch.equal(state_bytes(ref), state_bytes(kv))
     kv.truncate(10**9)  # larger than the count: unchanged
     assert kv.status() == (cut + T, 0)
 
 
-def test_capacity_and_nonfinite_write_nothing(cas):
+@pytest.mark.parametrize("variant", [1, 2])
+def test_capacity_and_nonfinite_write_nothing(cas, variant):
     H = 2
     K, V = make_tokens(24, H, seed=3)
-    kv = new_cache(cas, H, 16, K, V)
+    kv = new_cache(cas, H, 16, K, V, variant=variant)
     kv.append(K[:10].cuda(), V[:10].cuda())
     before = kv.buf.clone()
     kv.append(K[10:24].cuda(), V[10:24].cuda())  # 24 > 16 tokens
@@ -157,15 +176,15 @@ def test_capacity_and_nonfinite_write_nothing(cas):
     kv.append(K[10:12].cuda(), V[10:12].cuda())
     assert kv.status() == (12, 0)
     # code-stream capacity: a tiny estimate of bits per code overflows the stream
-    small = new_cache(cas, H, 64, K, V, est=0.05)
+    small = new_cache(cas, H, 64, K, V, est=0.05, variant=variant)
     small.append(K.cuda(), V.cuda())
     assert small.status() == (0, -4)
 
 
-def oracle_draft_kv(orc, toks, k, m):
+def oracle_draft_kv(orc, toks, k, m, variant=1):
     T, H, _ = toks.shape
     a = np16(toks)
-    return np.stack([orc.draft_values(a[:, h].reshape(1, T * D), 1, k, m).reshape(T, D) for h in range(H)], 1)
+    return np.stack([orc.draft_values(a[:, h].reshape(1, T * D), variant, k, m).reshape(T, D) for h in range(H)], 1)
 
 
 def check_attn(o, ref, nrm, what):
@@ -175,14 +194,17 @@ def check_attn(o, ref, nrm, what):
     assert not bad.any(), f"{what}: {bad.sum()} bad, worst {(np.abs(o - ref) / bound).max():.3g}"
 
 
-@pytest.mark.parametrize("lens,n_tail", [((300,), 0), ((1, ), 1), ((517, 64), 3), ((0,), 2), ((256, 1000), 4)])
-def test_draft_attention(cas, orc, lens, n_tail):
-    H, Hq, k, m = 8, 32, 64, 3
+@pytest.mark.parametrize("lens,n_tail,variant,k,m", [
+    ((300,), 0, 1, 64, 3), ((1, ), 1, 1, 64, 3), ((517, 64), 3, 1, 64, 3), ((0,), 2, 1, 64, 3),
+    ((256, 1000), 4, 1, 64, 3), ((300,), 0, 2, 64, 3), ((517, 64), 3, 2, 64, 3), ((777,), 1, 2, 48, 4),
+    ((99,), 2, 1, 40, 2)])
+def test_draft_attention(cas, orc, lens, n_tail, variant, k, m):
+    H, Hq = 8, 32
     B = len(lens)
     caches, Ks, Vs = [], [], []
     for b, T in enumerate(lens):
         K, V = make_tokens(max(T, 16), H, layer=b, seed=31 + b)
-        kv = new_cache(cas, H, 1100, K, V, k, m)
+        kv = new_cache(cas, H, 1100, K, V, k, m, variant=variant)
         if T:
             kv.append(K[:T].cuda(), V[:T].cuda())
         assert kv.status() == (T, 0)
@@ -195,8 +217,8 @@ def test_draft_attention(cas, orc, lens, n_tail):
     o = cas.draft_attn_decode(caches, q.cuda(), tk.contiguous().cuda() if n_tail else None,
                               tv.contiguous().cuda() if n_tail else None)
     for b in range(B):
-        Kd = oracle_draft_kv(orc, Ks[b], k, m) if lens[b] else np.zeros((0, H, D), np.uint16)
-        Vd = oracle_draft_kv(orc, Vs[b], k, m) if lens[b] else np.zeros((0, H, D), np.uint16)
+        Kd = oracle_draft_kv(orc, Ks[b], k, m, variant) if lens[b] else np.zeros((0, H, D), np.uint16)
+        Vd = oracle_draft_kv(orc, Vs[b], k, m, variant) if lens[b] else np.zeros((0, H, D), np.uint16)
         Kall = np.concatenate([Kd, np16(tk[b])], 0)
         Vall = np.concatenate([Vd, np16(tv[b])], 0)
         if Kall.shape[0] == 0:
@@ -206,14 +228,16 @@ def test_draft_attention(cas, orc, lens, n_tail):
         check_attn(o[b:b + 1], ref, nrm, f"draft attention b={b}")
 
 
-@pytest.mark.parametrize("lens,T", [((300,), 5), ((5,), 5), ((517, 40), 7), ((1024,), 14), ((260,), 16), ((9,), 1)])
-def test_verify_attention(cas, orc, lens, T):
+@pytest.mark.parametrize("lens,T,variant", [((300,), 5, 1), ((5,), 5, 1), ((517, 40), 7, 1), ((1024,), 14, 1),
+                                            ((260,), 16, 1), ((9,), 1, 1), ((517, 40), 7, 2), ((1024,), 14, 2),
+                                            ((9,), 1, 2)])
+def test_verify_attention(cas, orc, lens, T, variant):
     H, Hq = 8, 32
     B = len(lens)
     caches, Ks, Vs = [], [], []
     for b, n in enumerate(lens):
         K, V = make_tokens(max(n, 16), H, layer=b, seed=51 + b)
-        kv = new_cache(cas, H, 1100, K, V)
+        kv = new_cache(cas, H, 1100, K, V, variant=variant)
         kv.append(K[:n].cuda(), V[:n].cuda())
         assert kv.status() == (n, 0)
         caches.append(kv)
