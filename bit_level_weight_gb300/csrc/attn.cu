@@ -7,7 +7,9 @@
 // causal among the last T tokens.
 //
 // Split over tokens (flash decoding): a CTA takes one (sequence, kv head,
-// 256-token chunk). Per 32-token step its 4 warps each decode one superblock
+// token chunk). The number of chunks is fixed at launch so that the grid is
+// one wave of resident CTAs; each CTA derives its range of 32-token steps
+// from the sequence length held on the device. Per 32-token step its 4 warps each decode one superblock
 // of K and of V into shared-memory tiles (fp32); then warp w runs the query
 // vectors w, w+4, ... of that kv head (GQA: the q heads h*G .. h*G+G-1, times
 // the T query tokens): scores with lane = token, online softmax, and the
@@ -28,7 +30,7 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kWarps = 4;
-constexpr int kChunk = 256;      // tokens per CTA
+constexpr int kChunk = 256;      // smallest chunk the workspace is sized for
 constexpr int kStepTok = 32;     // tokens per step (4 superblocks)
 constexpr int kRow = CAS_BLK + 8;  // bf16 tile row stride (272 B: conflict-free 16-byte rows)
 constexpr int kPart = CAS_BLK + 2; // floats per partial: o[128], m, l
@@ -122,8 +124,9 @@ __global__ void __launch_bounds__(kThreads) attn_chunk_kernel(AttnArgs a) {
   const KvDev& d = a.kv[b];
   const int H = d.H, T = a.T, G = a.G, nq = min(T * G - qv0, kQvPerCta);
   const int64_t n = *(volatile const int64_t*)&kv_state(d)->n_tokens;
-  const int64_t t_begin = (int64_t)chunk * kChunk;
-  const int64_t t_end = min(n, t_begin + kChunk);
+  const int64_t steps = (n + kStepTok - 1) / kStepTok;
+  const int64_t t_begin = steps * chunk / a.nchunk * kStepTok;
+  const int64_t t_end = min(n, steps * (chunk + 1) / a.nchunk * kStepTok);
 
   // query vectors qv = j * G + g (query token j, head h*G+g), scaled; this
   // CTA takes qv0 .. qv0 + nq - 1 (local index qv - qv0)
@@ -236,7 +239,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(CombineArgs a) {
   const int hq = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t n = *(volatile const int64_t*)a.ntok[b];
-  const int used = (int)min((int64_t)a.nchunk, (n + kChunk - 1) / kChunk);
+  const int used = n > 0 ? a.nchunk : 0;
   const float* P = a.part + (((int64_t)b * a.T + j) * a.Hq + hq) * a.nchunk * kPart;
   const int hk = hq / a.G;
   // tail scores (exact bf16 tokens), warp 0
@@ -302,17 +305,22 @@ size_t chunk_smem(int qv_alloc) {
   return (size_t)2 * kStepTok * kRow * 2 + (size_t)qv_alloc * CAS_BLK * 4 + 512 + kWarps * kScratchWarp;
 }
 
+int nchunks(int64_t max_tokens) { return (int)((max_tokens + kChunk - 1) / kChunk); }
+
+// a.nchunk on entry: the most chunks the workspace holds; on return: the
+// chunks launched (one wave of resident CTAs, at most that many).
 template <bool FULL, int QPW>
-int launch_chunk(const AttnArgs& a, int Hkv, cudaStream_t st) {
+int launch_chunk(AttnArgs& a, int Hkv, cudaStream_t st) {
   size_t smem = chunk_smem(a.qv_alloc);
   auto kern = attn_chunk_kernel<FULL, QPW>;
-  if (occupancy((const void*)kern, kThreads, smem) < 1) return CAS_ERR_CUDA;
+  const int per_sm = occupancy((const void*)kern, kThreads, smem);
+  if (per_sm < 1) return CAS_ERR_CUDA;
+  const int64_t slots = (int64_t)per_sm * sm_count();
+  a.nchunk = (int)std::max<int64_t>(1, std::min<int64_t>(a.nchunk, slots / ((int64_t)Hkv * a.B * a.ngroups)));
   dim3 grid(a.nchunk, Hkv, a.B * a.ngroups);
   kern<<<grid, kThreads, smem, st>>>(a);
   return launch_status();
 }
-
-int nchunks(int64_t max_tokens) { return (int)((max_tokens + kChunk - 1) / kChunk); }
 
 int run_attn(bool full, const cas_kv* const* kv, int B, const uint16_t* q, int T, int Hq, const uint16_t* tail_k,
              const uint16_t* tail_v, int n_tail, float* o, void* ws, uint64_t ws_bytes, cudaStream_t st) {

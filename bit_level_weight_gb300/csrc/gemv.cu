@@ -24,6 +24,8 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "lanedec.cuh"
+#include "sbdecode.cuh"
 
 namespace cas {
 namespace {
@@ -70,7 +72,7 @@ struct OnesCursor {
   }
 };
 
-template <int VAR, int NV, bool FAST>
+template <int VAR, int NV>
 __global__ void __launch_bounds__(kThreads) draft_gemv_kernel(GemvArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const WView& w = a.w;
@@ -116,14 +118,14 @@ __global__ void __launch_bounds__(kThreads) draft_gemv_kernel(GemvArgs a) {
     const int64_t gb0 = (int64_t)n * nbr + CAS_SB * j;
     const uint32_t mw = lane < 4 * nb ? __ldg(w.mask + gb0 * 4 + lane) : 0u;
     s_mw[lane] = __brev(mw);
-    if (!FAST) {
+    {
       const uint32_t* rsrc = recs + gb0 * rec;
       for (int i = lane; i < nb * rec; i += 32) s_rec[i] = __ldg(rsrc + i);
     }
     const int cnt = __popc(mw);
     const int incl = warp_incl_add(cnt, lane);
     const int kt = nb * k;
-    const int q = FAST ? 16 : (kt + 31) >> 5;
+    const int q = (kt + 31) >> 5;
     const int t0 = min(lane * q, kt), t1 = min(t0 + q, kt);
     // mask word and bit of the lane's first kept position
     const int wi = min(warp_count_le(incl, t0), 31);
@@ -181,24 +183,7 @@ __global__ void __launch_bounds__(kThreads) draft_gemv_kernel(GemvArgs a) {
       }
       float scale = 0.f;
       int gcur = -1;
-      if (FAST) {
-        // k = 64, m = 3, full superblock: the lane's 16 fields are the 64
-        // bits at word 2*(lane%4) of record lane/4
-        const uint32_t* rb = recs + (gb0 + (lane >> 2)) * 8 + 2 * (lane & 3);
-        const uint32_t f0 = __ldg(rb), f1 = __ldg(rb + 1);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int pos = pc.next(more_mask);
-          const int end = cc.next(more_code);
-          const uint32_t e23 = lut23[(end - prev) & 255];
-          prev = end + 1;
-          const uint32_t fld = ((i < 8 ? f0 : f1) >> (4 * (i & 7))) & 15u;
-          const float val = __uint_as_float(((fld >> 3) << 31) | e23 | ((fld & 7u) << 20));
-          const uint16_t* xp = xrow + (pos & 1023);
-#pragma unroll
-          for (int v = 0; v < NV; ++v) acc[v] = fmaf(val, bf2f(xp[v * K]), acc[v]);
-        }
-      } else {
+      {
         int b = t0 / k, tl = t0 - b * k;  // block and block-local ordinal of t0
         for (int t = t0; t < t1; ++t) {
           const int pos = pc.next(more_mask);
@@ -241,22 +226,41 @@ __global__ void __launch_bounds__(kThreads) draft_gemv_kernel(GemvArgs a) {
 
 // ------------------------------------------------------------------ fast path
 // Cassandra-1, k = 64, m = 3, rows made of whole superblocks (K % 1024 == 0).
-// Superblocks are visited column-major (s = j * N + n), so a warp keeps the
-// 1024 x values of its column superblock in registers (lane L: positions
-// 32L..32L+31) across rows. Per superblock, in three SIMD phases with no
-// per-lane branching:
-//   1. decode the unary stream cooperatively into exponents by kept ordinal;
-//   2. lane = ordinal (t = L + 32 i): build the fp32 draft value from its
-//      4-bit record field (offsets are compile-time: block i/2, field
-//      L + 32 (i%2)) and exponent, store it by ordinal;
-//   3. lane = mask word L: for each of its 32 positions, a kept bit selects
-//      the next value by ordinal and multiplies it with x (predicated).
-constexpr int kFastSkew = 512 + 16;  // values by ordinal, index t + t/32 (bank skew)
-struct FastWarp {
-  uint32_t rec[64];     // spec_sm records of the 8 blocks
-  alignas(16) uint8_t ek[512];  // exponent by kept ordinal
-  uint32_t val[kFastSkew];
+// One warp per superblock, visited in row-major order; lane L owns kept
+// ordinals 16L..16L+15 (block L/4). The warp stages the superblock's unary
+// exponent stream in shared memory with its popcount prefixes; each lane finds
+// where its first code starts (a lower bound over the prefixes and a popcount
+// select) and where its first kept position is (popcounts of the block's four
+// mask words), then walks 16 steps: next code -> rank -> exponent, next set
+// mask bit -> position, 4-bit record field -> sign and mantissa, fp32 value
+// times x (bf16 in shared memory, staged once per CTA by a TMA bulk copy).
+// Lanes whose codes run past the cursor's one-word refill (longer than 32
+// bits) are detected afterwards and the superblock is recomputed by the
+// generic superblock decoder.
+union LaneWarp {
+  UnaryStage us;
+  uint8_t code[1024];  // generic decoder scratch (exponents by kept ordinal)
 };
+
+template <int NV>
+__device__ __forceinline__ void gemv_superblock_generic(const WView& w, int64_t s, const uint8_t* lut8,
+                                                        uint8_t* scratch, const uint16_t* xsb, int K, int lane,
+                                                        float acc[NV]) {
+  SbScratch sc{scratch, nullptr, nullptr};
+  const SbInfo in = sb_prepare<1, false>(w, s, lut8, sc, lane);
+  uint32_t v[16];
+  sb_rebuild_word<1, false>(w, in, sc, lane, v);
+  const uint16_t* xp = xsb + 32 * lane;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+#pragma unroll
+    for (int q = 0; q < NV; ++q) {
+      acc[q] = fmaf(bf2f(v[i] & 0xFFFFu), bf2f(xp[q * K + 2 * i]), acc[q]);
+      acc[q] = fmaf(bf2f(v[i] >> 16), bf2f(xp[q * K + 2 * i + 1]), acc[q]);
+    }
+  }
+  __syncwarp();
+}
 
 template <int NV>
 __global__ void __launch_bounds__(kThreads) draft_gemv_fast_kernel(GemvArgs a) {
@@ -268,7 +272,7 @@ __global__ void __launch_bounds__(kThreads) draft_gemv_fast_kernel(GemvArgs a) {
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + xbytes);
   uint8_t* lut8 = smem + xbytes + 16;
-  FastWarp& fw = reinterpret_cast<FastWarp*>(smem + xbytes + 16 + 256)[warp];
+  LaneWarp& lw = reinterpret_cast<LaneWarp*>(smem + xbytes + 16 + 256)[warp];
 
   if (threadIdx.x == 0) {
     mbar_init(bar, 1);
@@ -287,65 +291,55 @@ __global__ void __launch_bounds__(kThreads) draft_gemv_fast_kernel(GemvArgs a) {
     return;
   }
 
-  const int N = (int)w.N, nsr = w.nsr, nbr = w.nbr;
+  const int nsr = w.nsr, nbr = w.nbr;
   const int nsb = (int)w.nsb;
   const int stride = gridDim.x * kWarps;
-  int jcur = -1;
-  float xr[NV][32];
-  for (int sc = blockIdx.x * kWarps + warp; sc < nsb; sc += stride) {
-    const int j = sc / N;
-    const int n = sc - j * N;
-    const int s = n * nsr + j;
-    if (j != jcur) {
-      jcur = j;
-      const uint16_t* xp = xs + CAS_BLK * CAS_SB * j + 32 * lane;
-#pragma unroll
-      for (int v = 0; v < NV; ++v)
-#pragma unroll
-        for (int p = 0; p < 32; ++p) xr[v][p] = bf2f(xp[v * K + p]);
-    }
+  const uint32_t lim = (uint32_t)a.sexp_words;
+  for (int s = blockIdx.x * kWarps + warp; s < nsb; s += stride) {
+    const int n = s / nsr;
+    const int j = s - n * nsr;
     const int64_t gb0 = (int64_t)n * nbr + CAS_SB * j;
-    const uint32_t mw = __ldg(w.mask + gb0 * 4 + lane);
-    const int cnt = __popc(mw);
-    const int o = warp_incl_add(cnt, lane) - cnt;
-    {
-      const uint2 r = __ldg(reinterpret_cast<const uint2*>(w.ssm + gb0 * 8) + lane);
-      fw.rec[2 * lane] = r.x;
-      fw.rec[2 * lane + 1] = r.y;
-    }
-    const uint32_t b0 = __ldg(w.sidx + s), b1 = __ldg(w.sidx + s + 1);
-    const int nw = (int)(b1 - b0);
-    warp_decode_unary_512(w.sexp + b0, nw, lut8, fw.ek, lane, stream_word(w.sexp + b0, nw, lane));
-    __syncwarp();
-    // phase 2: values by ordinal
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int t = lane + 32 * i;
-      const int tl = lane + 32 * (i & 1);  // ordinal within block i/2
-      const uint32_t nib = (fw.rec[8 * (i >> 1) + (tl >> 3)] >> (4 * (tl & 7))) & 15u;
-      fw.val[t + (t >> 5)] = ((nib >> 3) << 31) | ((uint32_t)fw.ek[t] << 23) | ((nib & 7u) << 20);
-    }
-    __syncwarp();
-    // phase 3: positions of mask word `lane`
+    const uint4 mm = __ldg(reinterpret_cast<const uint4*>(w.mask) + gb0 + (lane >> 2));
+    const uint2 rr = __ldg(reinterpret_cast<const uint2*>(w.ssm + gb0 * 8) + lane);
+    const uint32_t sb1 = min(__ldg(w.sidx + s + 1), lim), sb0 = min(__ldg(w.sidx + s), sb1);
+    const int nw = (int)(sb1 - sb0);
+    const uint16_t* xsb = xs + CAS_BLK * CAS_SB * j;
     float acc[NV];
 #pragma unroll
-    for (int v = 0; v < NV; ++v) acc[v] = 0.f;
-    int t = o;
-#pragma unroll
-    for (int p = 0; p < 32; ++p) {
-      if ((mw >> p) & 1u) {
-        const float val = __uint_as_float(fw.val[t + (t >> 5)]);
-#pragma unroll
-        for (int v = 0; v < NV; ++v) acc[v] = fmaf(val, xr[v][p], acc[v]);
-        ++t;
-      }
-    }
-#pragma unroll
-    for (int v = 0; v < NV; ++v) {
-      float r = warp_sumf(acc[v]);
-      if (lane == 0) atomicAdd(a.y + (int64_t)v * w.N + n, r);
-    }
+    for (int q = 0; q < NV; ++q) acc[q] = 0.f;
+    bool fast = nw <= kStageWords;
+    if (fast) fast = stage_unary(w.sexp + sb0, nw, lw.us, lane) >= 16 * 32;
     __syncwarp();
+    if (fast) {
+      UnaryCursor uc;
+      uc.init(lw.us, unary_code_start(lw.us, nw, 16 * lane));
+      MaskCursor mc;
+      mc.init(mm.x, mm.y, mm.z, mm.w, 16 * (lane & 3));
+      const uint16_t* xl = xsb + CAS_BLK * (lane >> 2);
+      int z = 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int pos = mc.next();
+        const int rank = uc.next(&z);
+        const uint32_t e = lut8[rank & 255];
+        const uint32_t f = (i < 8 ? rr.x : rr.y) >> (4 * (i & 7));
+        const float val = __uint_as_float(((f & 8u) << 28) | (e << 23) | ((f & 7u) << 20));
+#pragma unroll
+        for (int q = 0; q < NV; ++q) acc[q] = fmaf(val, bf2f(xl[q * K + pos]), acc[q]);
+      }
+      fast = __all_sync(CAS_FULL, unary_lane_ok(lw.us, nw, uc.hw, z, 16 * (lane + 1)));
+      __syncwarp();
+    }
+    if (!fast) {
+#pragma unroll
+      for (int q = 0; q < NV; ++q) acc[q] = 0.f;
+      gemv_superblock_generic<NV>(w, s, lut8, lw.code, xsb, K, lane, acc);
+    }
+#pragma unroll
+    for (int q = 0; q < NV; ++q) {
+      const float r = warp_sumf(acc[q]);
+      if (lane == 0) atomicAdd(a.y + (int64_t)q * w.N + n, r);
+    }
   }
 }
 
@@ -462,7 +456,7 @@ int launch_fast2(const GemvArgs& a, cudaStream_t st) {
 
 template <int NV>
 int launch_fast(const GemvArgs& a, cudaStream_t st) {
-  size_t smem = (size_t)NV * a.w.K * 2 + 16 + 256 + kWarps * sizeof(FastWarp);
+  size_t smem = (size_t)NV * a.w.K * 2 + 16 + 256 + kWarps * sizeof(LaneWarp);
   auto kern = draft_gemv_fast_kernel<NV>;
   int per_sm = occupancy((const void*)kern, kThreads, smem);
   if (per_sm < 1) return CAS_ERR_CUDA;
@@ -472,10 +466,10 @@ int launch_fast(const GemvArgs& a, cudaStream_t st) {
   return launch_status();
 }
 
-template <int VAR, int NV, bool FAST>
+template <int VAR, int NV>
 int launch(const GemvArgs& a, cudaStream_t st) {
   size_t smem = (size_t)NV * a.w.K * 2 + 16 + 1024 + kWarps * kWarpWords * 4;
-  auto kern = draft_gemv_kernel<VAR, NV, FAST>;
+  auto kern = draft_gemv_kernel<VAR, NV>;
   int per_sm = occupancy((const void*)kern, kThreads, smem);
   if (per_sm < 1) return CAS_ERR_CUDA;
   int64_t need = (a.w.nsb + kWarps - 1) / kWarps;
@@ -489,14 +483,21 @@ int launch(const GemvArgs& a, cudaStream_t st) {
 // sit in one 64-bit slice of one block record.
 template <int VAR>
 int dispatch(const GemvArgs& a, int nvec, cudaStream_t st) {
-  const bool fast = a.w.k == 64 && a.w.m == 3 && a.w.nbr % CAS_SB == 0 && nvec <= 2;
-  if (fast && VAR == 1) return nvec == 1 ? launch_fast<1>(a, st) : launch_fast<2>(a, st);
-  if (fast && VAR == 2) return nvec == 1 ? launch_fast2<1>(a, st) : launch_fast2<2>(a, st);
+  const bool fast = a.w.k == 64 && a.w.m == 3 && a.w.nbr % CAS_SB == 0;
+  if (fast && VAR == 1) {
+    switch (nvec) {
+      case 1: return launch_fast<1>(a, st);
+      case 2: return launch_fast<2>(a, st);
+      case 3: return launch_fast<3>(a, st);
+      default: return launch_fast<4>(a, st);
+    }
+  }
+  if (fast && VAR == 2 && nvec <= 2) return nvec == 1 ? launch_fast2<1>(a, st) : launch_fast2<2>(a, st);
   switch (nvec) {
-    case 1: return fast ? launch<VAR, 1, true>(a, st) : launch<VAR, 1, false>(a, st);
-    case 2: return fast ? launch<VAR, 2, true>(a, st) : launch<VAR, 2, false>(a, st);
-    case 3: return fast ? launch<VAR, 3, true>(a, st) : launch<VAR, 3, false>(a, st);
-    default: return fast ? launch<VAR, 4, true>(a, st) : launch<VAR, 4, false>(a, st);
+    case 1: return launch<VAR, 1>(a, st);
+    case 2: return launch<VAR, 2>(a, st);
+    case 3: return launch<VAR, 3>(a, st);
+    default: return launch<VAR, 4>(a, st);
   }
 }
 

@@ -82,6 +82,33 @@ def test_draft_gemv(cas, orc, N, K, variant, k, m, nvec):
     check_close(y, ref, norm, "draft_gemv")
 
 
+def wide_exponent_rows(N, K, n_wide, seed):
+    """Normal rows, then n_wide rows whose exponents spread over ~200 values:
+    their unary codes are long (tens to hundreds of bits) and their
+    superblock streams exceed a few hundred words. Row 0 gets a few long codes
+    inside otherwise short streams."""
+    Wn = np16(synthetic.normal_weight(N, K, seed=seed)).copy()
+    rng = np.random.default_rng(seed)
+    e = rng.integers(-100, 100, size=(n_wide, K)).astype(np.float64)
+    v = rng.choice([-1.0, 1.0], size=(n_wide, K)) * rng.uniform(1.0, 2.0, size=(n_wide, K)) * 2.0 ** e
+    Wn[N - n_wide:] = np16(synthetic.to_bits(torch.from_numpy(v.astype(np.float32))))
+    spikes = 2.0 ** rng.integers(-60, 60, size=Wn[0, ::97].size)
+    Wn[0, ::97] = np16(synthetic.to_bits(torch.from_numpy(spikes.astype(np.float32))))
+    return torch.from_numpy(Wn.view(np.int16))
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("nvec", [1, 3])
+def test_draft_gemv_long_codes(cas, orc, variant, nvec):
+    N, K = 48, 2048
+    W = wide_exponent_rows(N, K, 8, seed=5)
+    x = synthetic.activations(nvec, K, seed=17)
+    enc = cas.encode_weights(W.cuda(), variant, 64, 3)
+    y = cas.draft_gemv(enc, x.cuda())
+    ref, norm = orc.matvec(orc.draft_values(np16(W), variant, 64, 3), np16(x))
+    check_close(y, ref, norm, "draft_gemv long codes")
+
+
 @pytest.mark.parametrize("N,K,variant,k,m", CASES)
 @pytest.mark.parametrize("T", [1, 5, 8, 9, 14, 16])
 def test_verify_gemm(cas, orc, N, K, variant, k, m, T):
