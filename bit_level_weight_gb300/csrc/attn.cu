@@ -23,6 +23,7 @@
 #include <mutex>
 
 #include "kvview.cuh"
+#include "lanedec.cuh"
 #include "sbdecode.cuh"
 
 namespace cas {
@@ -38,10 +39,10 @@ constexpr int kMaxBatch = 8;
 constexpr int kMaxT = 16;
 
 constexpr int kQvPerCta = 32;  // query vectors per CTA (8 per warp)
-// per-warp decode scratch: the fast decoder's, or kept codes + pruned codes +
-// the Cassandra-2 residual words of one superblock
+// per-warp decode scratch: the cursor decoder's staged stream, or kept codes +
+// pruned codes + the Cassandra-2 residual words of one superblock
 constexpr int kScratchWarp =
-    (int)sizeof(FastScratch) > 2048 + 4 * kResWords ? (int)sizeof(FastScratch) : 2048 + 4 * kResWords;
+    (int)sizeof(UnaryStage) > 2048 + 4 * kResWords ? (int)sizeof(UnaryStage) : 2048 + 4 * kResWords;
 
 struct AttnArgs {
   KvDev kv[kMaxBatch];
@@ -62,24 +63,25 @@ __device__ __forceinline__ float warp_maxf(float v) {
 template <bool FULL>
 __device__ __forceinline__ void decode_sb_tile(const KvDev& d, int st, int64_t n, int64_t sb, uint16_t* tile, int row0,
                                                const uint8_t* lut, uint8_t* scratch, int lane) {
-  int64_t nsb = (n + CAS_SB - 1) / CAS_SB;
-  uint32_t v[16];
-  int nb = 0;
+  const int64_t nsb = (n + CAS_SB - 1) / CAS_SB;
   if (sb < nsb && d.variant == 1 && d.k == 64 && d.m == 3 && CAS_SB * (sb + 1) <= n) {
-    // whole superblock of 8 tokens: fast decoder
+    // whole superblock of 8 tokens: per-lane cursors
     const uint32_t* sidx = (const uint32_t*)kv_sec(d, CAS_KV_SPEC_SBIDX, st);
     const uint32_t* vidx = (const uint32_t*)kv_sec(d, CAS_KV_VER_SBIDX, st);
     const uint32_t a0 = sidx[sb], a1 = sidx[sb + 1];
     const uint32_t v0 = FULL ? vidx[sb] : 0u, v1 = FULL ? vidx[sb + 1] : 0u;
-    fast_sb_decode<FULL>((const uint32_t*)kv_sec(d, CAS_KV_MASK, st) + sb * 32,
-                         (const uint32_t*)kv_sec(d, CAS_KV_SPEC_SM, st) + sb * 64,
-                         (const uint32_t*)kv_sec(d, CAS_KV_VER_LO, st) + sb * 64,
-                         (const uint32_t*)kv_sec(d, CAS_KV_VER_PR, st) + sb * 128,
-                         (const uint32_t*)kv_sec(d, CAS_KV_SPEC_EXP, st) + a0, (int)(a1 - a0),
-                         (const uint32_t*)kv_sec(d, CAS_KV_VER_EXP, st) + v0, (int)(v1 - v0), lut,
-                         *reinterpret_cast<FastScratch*>(scratch), lane, v);
-    nb = CAS_SB;
-  } else if (sb < nsb && d.variant == 1) {
+    if (lane_sb_tile<FULL>((const uint32_t*)kv_sec(d, CAS_KV_MASK, st) + sb * 32,
+                           (const uint32_t*)kv_sec(d, CAS_KV_SPEC_SM, st) + sb * 64,
+                           (const uint32_t*)kv_sec(d, CAS_KV_VER_LO, st) + sb * 64,
+                           (const uint32_t*)kv_sec(d, CAS_KV_VER_PR, st) + sb * 128,
+                           (const uint32_t*)kv_sec(d, CAS_KV_SPEC_EXP, st) + a0, (int)(a1 - a0),
+                           (const uint32_t*)kv_sec(d, CAS_KV_VER_EXP, st) + v0, (int)(v1 - v0), lut,
+                           *reinterpret_cast<UnaryStage*>(scratch), tile + row0 * kRow, kRow, lane))
+      return;
+  }
+  uint32_t v[16];
+  int nb = 0;
+  if (sb < nsb && d.variant == 1) {
     SbScratch sc{scratch, scratch + 1024, nullptr};
     WView w = kv_stream_view(d, st, n);
     SbInfo in = sb_prepare<1, FULL>(w, sb, lut, sc, lane);

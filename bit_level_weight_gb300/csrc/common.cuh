@@ -151,126 +151,6 @@ __device__ __forceinline__ void warp_decode_unary(const uint32_t* __restrict__ w
   }
 }
 
-// Decode of a stream known to hold at least `ncodes` codes with ncodes a
-// power of two: indices wrap with a mask instead of a bounds test.
-__device__ __forceinline__ void warp_decode_unary_pow2(const uint32_t* __restrict__ words, int nwords,
-                                                       const uint8_t* __restrict__ lut,
-                                                       uint8_t* __restrict__ out, int ncodes, int lane) {
-  const int wrap = ncodes - 1;
-  int done = 0, prev = -1;
-  for (int c0 = 0; c0 < nwords && done < ncodes; c0 += 32) {
-    const int wi = c0 + lane;
-    uint32_t w = wi < nwords ? __ldg(words + wi) : 0u;
-    const int ones = __popc(w);
-    const int incl = warp_incl_add(ones, lane);
-    int ord = done + incl - ones;
-    const int last = w ? (wi * 32 + 32 - __ffs(w)) : -1;
-    const int mx = warp_incl_max(last, lane);
-    int pv = __shfl_up_sync(CAS_FULL, mx, 1);
-    if (lane == 0) pv = -1;
-    pv = max(pv, prev) - wi * 32;  // relative to this word's MSB
-    while (w) {
-      const int i = __clz(w);
-      out[ord & wrap] = lut[(i - pv - 1) & 255];
-      pv = i;
-      ++ord;
-      w &= 0x7FFFFFFFu >> i;
-    }
-    done += __shfl_sync(CAS_FULL, incl, 31);
-    prev = max(prev, __shfl_sync(CAS_FULL, mx, 31));
-  }
-}
-
-// Word `lane` of a stream of nwords words (zero past the end).
-__device__ __forceinline__ uint32_t stream_word(const uint32_t* words, int nwords, int lane) {
-  return lane < nwords ? __ldg(words + lane) : 0u;
-}
-
-// Decode of exactly 512 codes with a fixed run of 16 consecutive codes per
-// lane (no per-lane trip-count divergence). Lane L finds the start of code
-// 16 L - the bit after the (16 L)-th '1' - from warp popcount prefixes over
-// the stream words (a shuffle binary search for the word, a popcount select
-// inside it), then reads its 16 codes with clz over a two-word window and
-// writes their table values as four 32-bit words (out must be 4-byte
-// aligned). Stream words are read through the read-only path; reads stop at
-// nwords (missing words read as zero).
-// first_word: word `lane` of the stream when already loaded by the caller
-// (0 if lane >= nwords); later rounds load their own words.
-__device__ __forceinline__ void warp_decode_unary_512(const uint32_t* __restrict__ words, int nwords,
-                                                      const uint8_t* __restrict__ lut,
-                                                      uint8_t* __restrict__ out, int lane, uint32_t first_word) {
-  const int target = 16 * lane;  // codes before this lane's run
-  int start = 0, before = 0;
-  bool done = lane == 0;
-  for (int c0 = 0; c0 < nwords; c0 += 32) {
-    if (!__any_sync(CAS_FULL, !done)) break;
-    const uint32_t wv = c0 == 0 ? first_word : (c0 + lane < nwords ? __ldg(words + c0 + lane) : 0u);
-    const int ones = __popc(wv);
-    const int incl = warp_incl_add(ones, lane);
-    const int total = __shfl_sync(CAS_FULL, incl, 31);
-    const int need = target - before;  // 1-based index of the '1' ending code target-1
-    const int wk = min(warp_count_le(incl, need - 1), 31);
-    const int excl = __shfl_sync(CAS_FULL, incl - ones, wk);
-    const uint32_t word = __shfl_sync(CAS_FULL, wv, wk);
-    if (!done && need <= total) {
-      start = (c0 + wk) * 32 + nth_set_bit(__brev(word), need - excl - 1) + 1;
-      done = true;
-    }
-    before += total;
-  }
-  int wi = start >> 5;
-  uint32_t h = (wi < nwords ? __ldg(words + wi) : 0u) & (0xFFFFFFFFu >> (start & 31));
-  uint32_t l = wi + 1 < nwords ? __ldg(words + wi + 1) : 0u;
-  int base = wi * 32;
-  uint32_t packed[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-  for (int c = 0; c < 16; ++c) {
-    for (int guard = 0; h == 0 && guard < 16; ++guard) {  // window word used up
-      h = l;
-      wi += 1;
-      l = wi + 1 < nwords ? __ldg(words + wi + 1) : 0u;
-      base += 32;
-    }
-    const int z = __clz(h);
-    h &= 0x7FFFFFFFu >> z;
-    const int end = base + z;
-    packed[c >> 2] |= (uint32_t)lut[(end - start) & 255] << (8 * (c & 3));
-    start = end + 1;
-  }
-  uint4* o4 = reinterpret_cast<uint4*>(out) + lane;
-  *o4 = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-}
-
-// Same decode, writing 32-bit table entries (e.g. exponent << 23).
-__device__ __forceinline__ void warp_decode_unary32(const uint32_t* __restrict__ words, int nwords,
-                                                    const uint32_t* __restrict__ lut,
-                                                    uint32_t* __restrict__ out, int ncodes, int lane) {
-  int done = 0, prev = -1;
-  for (int c0 = 0; c0 < nwords && done < ncodes; c0 += 32) {
-    int wi = c0 + lane;
-    uint32_t w = wi < nwords ? __ldg(words + wi) : 0u;
-    int ones = __popc(w);
-    int incl = warp_incl_add(ones, lane);
-    int ord = done + incl - ones;
-    int last = w ? (wi * 32 + 32 - __ffs(w)) : -1;
-    int mx = warp_incl_max(last, lane);
-    int pv = __shfl_up_sync(CAS_FULL, mx, 1);
-    if (lane == 0) pv = -1;
-    pv = max(pv, prev);
-    int base = wi * 32;
-    while (w) {
-      int i = __clz(w);
-      int pos = base + i;
-      if (ord < ncodes) out[ord] = lut[(pos - pv - 1) & 255];
-      pv = pos;
-      ++ord;
-      w &= 0x7FFFFFFFu >> i;
-    }
-    done += __shfl_sync(CAS_FULL, incl, 31);
-    prev = max(prev, __shfl_sync(CAS_FULL, mx, 31));
-  }
-}
-
 // Same, but writes the raw code value (the unary count) instead of a table
 // lookup; used for the Cassandra-2 exponent distances.
 __device__ __forceinline__ void warp_decode_unary_raw(const uint32_t* __restrict__ words, int nwords,

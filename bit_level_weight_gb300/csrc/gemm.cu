@@ -13,6 +13,7 @@
 
 #include <algorithm>
 
+#include "lanedec.cuh"
 #include "sbdecode.cuh"
 
 namespace cas {
@@ -46,9 +47,9 @@ __device__ __forceinline__ void mma_bf16(float c[4], const uint32_t a[4], uint32
 }
 
 constexpr int kScratchGeneric = 2048 + kResWords * 4;
-constexpr int kScratchWarp = (int)sizeof(FastScratch) > kScratchGeneric ? (int)sizeof(FastScratch) : kScratchGeneric;
+constexpr int kScratchWarp = (int)sizeof(UnaryStage) > kScratchGeneric ? (int)sizeof(UnaryStage) : kScratchGeneric;
 
-// FAST: Cassandra-1, k = 64, m = 3, whole superblocks (see fast_sb_decode).
+// FAST: Cassandra-1, k = 64, m = 3, whole superblocks (per-lane cursors, lane_sb_tile).
 template <int VAR, int NT, bool FAST>
 __global__ void __launch_bounds__(kThreads) verify_gemm_kernel(GemmArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -60,7 +61,7 @@ __global__ void __launch_bounds__(kThreads) verify_gemm_kernel(GemmArgs a) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint8_t* wscr = scratch + warp * kScratchWarp;
   SbScratch sc{wscr, wscr + 1024, reinterpret_cast<uint32_t*>(wscr + 2048)};
-  FastScratch& fs = *reinterpret_cast<FastScratch*>(wscr);
+  UnaryStage& us = *reinterpret_cast<UnaryStage*>(wscr);
   for (int i = threadIdx.x; i < 256; i += kThreads) s_lut[i] = a.lut.v[i];
   __syncthreads();
 
@@ -76,18 +77,17 @@ __global__ void __launch_bounds__(kThreads) verify_gemm_kernel(GemmArgs a) {
     for (int r = warp; r < kRows; r += kWarps) {
       int64_t n = rt * kRows + r;
       uint4* dst = reinterpret_cast<uint4*>(tile + r * kTileStride + 32 * lane);
+      bool done = false;
       if (n < w.N && FAST) {
         const int64_t s = n * w.nsr + j;
         const int64_t gb0 = n * w.nbr + CAS_SB * j;
         const uint32_t a0 = __ldg(w.sidx + s), a1 = __ldg(w.sidx + s + 1);
         const uint32_t v0 = __ldg(w.vidx + s), v1 = __ldg(w.vidx + s + 1);
-        uint32_t v[16];
-        fast_sb_decode<true>(w.mask + gb0 * 4, w.ssm + gb0 * 8, w.vlo + gb0 * 8, w.vpr + gb0 * 16, w.sexp + a0,
-                             (int)(a1 - a0), w.vexp + v0, (int)(v1 - v0), s_lut, fs, lane, v);
-        dst[0] = make_uint4(v[0], v[1], v[2], v[3]);
-        dst[1] = make_uint4(v[4], v[5], v[6], v[7]);
-        dst[2] = make_uint4(v[8], v[9], v[10], v[11]);
-        dst[3] = make_uint4(v[12], v[13], v[14], v[15]);
+        done = lane_sb_tile<true>(w.mask + gb0 * 4, w.ssm + gb0 * 8, w.vlo + gb0 * 8, w.vpr + gb0 * 16,
+                                  w.sexp + a0, (int)(a1 - a0), w.vexp + v0, (int)(v1 - v0), s_lut, us,
+                                  tile + r * kTileStride, CAS_BLK, lane);
+      }
+      if (done) {
       } else if (n < w.N) {
         SbInfo in = sb_prepare<VAR, true>(w, n * w.nsr + j, s_lut, sc, lane);
         if (lane < 4 * nb) {

@@ -234,9 +234,8 @@ __global__ void __launch_bounds__(kThreads) draft_gemv_kernel(GemvArgs a) {
 // mask words), then walks 16 steps: next code -> rank -> exponent, next set
 // mask bit -> position, 4-bit record field -> sign and mantissa, fp32 value
 // times x (bf16 in shared memory, staged once per CTA by a TMA bulk copy).
-// Lanes whose codes run past the cursor's one-word refill (longer than 32
-// bits) are detected afterwards and the superblock is recomputed by the
-// generic superblock decoder.
+// Superblocks whose stream exceeds the stage (or holds fewer than 512 codes)
+// go through the generic superblock decoder.
 union LaneWarp {
   UnaryStage us;
   uint8_t code[1024];  // generic decoder scratch (exponents by kept ordinal)
@@ -260,6 +259,22 @@ __device__ __forceinline__ void gemv_superblock_generic(const WView& w, int64_t 
     }
   }
   __syncwarp();
+}
+
+// The lane's 16 kept values times x: value = sign, exponent (rank table) and
+// the 3 high mantissa bits of the record field; x is bf16 in shared memory.
+template <int NV, bool LONG>
+__device__ __forceinline__ void lane_kept_dot(UnaryCursor& uc, MaskCursor& mc, uint2 rr, const uint8_t* lut8,
+                                              const uint16_t* xl, int K, float acc[NV]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int pos = mc.next();
+    const uint32_t e = lut8[uc.next<LONG>() & 255];
+    const uint32_t f = (i < 8 ? rr.x : rr.y) >> (4 * (i & 7));
+    const float val = __uint_as_float(((f & 8u) << 28) | (e << 23) | ((f & 7u) << 20));
+#pragma unroll
+    for (int q = 0; q < NV; ++q) acc[q] = fmaf(val, bf2f(xl[q * K + pos]), acc[q]);
+  }
 }
 
 template <int NV>
@@ -307,8 +322,8 @@ __global__ void __launch_bounds__(kThreads) draft_gemv_fast_kernel(GemvArgs a) {
     float acc[NV];
 #pragma unroll
     for (int q = 0; q < NV; ++q) acc[q] = 0.f;
-    bool fast = nw <= kStageWords;
-    if (fast) fast = stage_unary(w.sexp + sb0, nw, lw.us, lane) >= 16 * 32;
+    bool fast = nw <= kStageWords, long_codes = false;
+    if (fast) fast = stage_unary(w.sexp + sb0, nw, lw.us, lane, &long_codes) >= 16 * 32;
     __syncwarp();
     if (fast) {
       UnaryCursor uc;
@@ -316,18 +331,10 @@ __global__ void __launch_bounds__(kThreads) draft_gemv_fast_kernel(GemvArgs a) {
       MaskCursor mc;
       mc.init(mm.x, mm.y, mm.z, mm.w, 16 * (lane & 3));
       const uint16_t* xl = xsb + CAS_BLK * (lane >> 2);
-      int z = 0;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int pos = mc.next();
-        const int rank = uc.next(&z);
-        const uint32_t e = lut8[rank & 255];
-        const uint32_t f = (i < 8 ? rr.x : rr.y) >> (4 * (i & 7));
-        const float val = __uint_as_float(((f & 8u) << 28) | (e << 23) | ((f & 7u) << 20));
-#pragma unroll
-        for (int q = 0; q < NV; ++q) acc[q] = fmaf(val, bf2f(xl[q * K + pos]), acc[q]);
-      }
-      fast = __all_sync(CAS_FULL, unary_lane_ok(lw.us, nw, uc.hw, z, 16 * (lane + 1)));
+      if (long_codes)
+        lane_kept_dot<NV, true>(uc, mc, rr, lut8, xl, K, acc);
+      else
+        lane_kept_dot<NV, false>(uc, mc, rr, lut8, xl, K, acc);
       __syncwarp();
     }
     if (!fast) {
@@ -349,6 +356,7 @@ __global__ void __launch_bounds__(kThreads) draft_gemv_fast_kernel(GemvArgs a) {
 // 2 stores the signed q by ordinal; phase 3 (lane = mask word = group)
 // accumulates q * x and multiplies the sum once by the group's scale
 // 2^(E' - 127 - m).
+constexpr int kFastSkew = 512 + 16;  // values by ordinal, index t + t/32 (bank skew)
 struct Fast2Warp {
   uint32_t rec[80 + 2];  // spec_q records of the 8 blocks (10 words each) + pad
   float val[kFastSkew];

@@ -10,10 +10,8 @@
 //     (Cassandra blog review, section 3.2: a code is `rank` zeros and a one);
 //   - a mask cursor over the block's four mask words: each step returns the
 //     position of the next kept (or, on the inverted mask, pruned) value.
-// Both refill from the next word with predicated moves (no divergent branch,
-// no global load in the loop). A code longer than the 32 bits of one refill
-// is not decoded correctly; `unary_lane_ok` detects that afterwards (the lane
-// then takes the generic path).
+// Both refill from the next word with predicated moves (no global load in the
+// loop); a code that spans more than one further word takes a rare loop.
 #pragma once
 #include "common.cuh"
 
@@ -28,17 +26,24 @@ struct UnaryStage {
 };
 
 // Stages words [0, nw) of a unary stream (nw <= kStageWords) with their
-// popcount prefixes; returns the number of ones (warp-uniform).
-__device__ __forceinline__ int stage_unary(const uint32_t* __restrict__ g, int nw, UnaryStage& s, int lane) {
+// popcount prefixes; returns the number of ones (warp-uniform). *long_codes
+// (warp-uniform) tells whether a staged word is all zeros: only then can a
+// code outlast one refill of the cursor.
+__device__ __forceinline__ int stage_unary(const uint32_t* __restrict__ g, int nw, UnaryStage& s, int lane,
+                                           bool* long_codes) {
   int before = 0;
+  bool zero = false;
   for (int c0 = 0; c0 < nw; c0 += 32) {
-    const uint32_t wv = c0 + lane < nw ? __ldg(g + c0 + lane) : 0u;
+    const bool in = c0 + lane < nw;
+    const uint32_t wv = in ? __ldg(g + c0 + lane) : 0u;
     s.st[c0 + lane] = wv;
+    zero |= in && wv == 0u;
     const int incl = warp_incl_add(__popc(wv), lane) + before;
     s.pc[c0 + lane] = (uint16_t)incl;
     before = __shfl_sync(CAS_FULL, incl, 31);
   }
   if (lane < kStagePad) s.st[nw + lane] = 0u;
+  *long_codes = __any_sync(CAS_FULL, zero);
   return before;
 }
 
@@ -64,45 +69,41 @@ struct UnaryCursor {
   uint32_t h, l;        // current word (consumed bits cleared), next word
   const uint32_t* np;   // word after l
   int sr;               // start of the current code relative to h's MSB
-  int hw;               // index of h's word
+  const uint32_t* end;  // the rare loop reads no further (the 16 plain
+                        // refills after it stay inside the stage pad)
 
   __device__ __forceinline__ void init(const UnaryStage& s, int start) {
-    hw = start >> 5;
+    const int hw = start >> 5;
+    end = s.st + kStageWords + 2;
     sr = start & 31;
     h = s.st[hw] & (0xFFFFFFFFu >> sr);
     l = s.st[hw + 1];
     np = s.st + hw + 2;
   }
-  // Rank of the next code (garbage, but harmless, for an over-long code);
-  // *z_out gets its last bit relative to word hw.
-  __device__ __forceinline__ int next(int* z_out) {
+  // Rank of the next code. LONG: the stream has an all-zero word, so a code
+  // may need more than one refill. A stream with fewer codes than asked for
+  // yields garbage ranks, never a read outside the stage.
+  template <bool LONG>
+  __device__ __forceinline__ int next() {
     if (h == 0u) {  // the code continues in the next word
       h = l;
       l = *np++;
       sr -= 32;
-      ++hw;
     }
-    const int z = __clz(h);  // 32 when the code runs past this word too
+    if (LONG) {
+      while (h == 0u && np < end) {
+        h = l;
+        l = *np++;
+        sr -= 32;
+      }
+    }
+    const int z = __clz(h);  // 32 only when the staged words ran out
     h ^= __funnelshift_rc(0x80000000u, 0u, z);
     const int rank = z - sr;
     sr = z + 1;
-    *z_out = z;
     return rank;
   }
 };
-
-// True when the lane's last code (last bit hw*32 + z) is the `ones`-th '1'
-// of the stream: every code of the lane was short enough for the cursor.
-__device__ __forceinline__ bool unary_lane_ok(const UnaryStage& s, int nw, int hw, int z, int ones) {
-  const int end = hw * 32 + z;
-  const int wi = end >> 5;
-  if (wi >= nw) return false;
-  const uint32_t word = s.st[wi];
-  const int b = end & 31;
-  const uint32_t upto = word >> (31 - b);  // bits 0..b of the word, MSB-first
-  const int cnt = (wi > 0 ? (int)s.pc[wi - 1] : 0) + __popc(upto);
-  return (upto & 1u) && cnt == ones;
-}
 
 // Cursor over the set bits of a block's 128-bit mask (LSB-first positions),
 // starting at the r-th set bit (0-based). Words are held bit-reversed so the
@@ -140,5 +141,115 @@ struct MaskCursor {
     return (base + p) & 127;
   }
 };
+
+}  // namespace cas
+
+namespace cas {
+
+// Rebuilds one whole superblock (Cassandra-1, k = 64, m = 3, 8 blocks) as bf16
+// bit patterns: the value at position p of block i goes to dst[i * bstride + p].
+// FULL merges speculation and verification data (lossless); otherwise the
+// draft value is written and pruned positions are zero. Lane L rebuilds kept
+// ordinals 16L..16L+15 (and, FULL, pruned ordinals 16L..16L+15) with the
+// cursors above; the unary streams are staged one after the other in `us`.
+// mask: 32 words, sm / lo: 64 words, pr: 128 words of the superblock (16-byte
+// aligned); sexp / vexp: its code streams. Returns false (warp-uniform) when a
+// stream is longer than the stage or holds fewer than 512 codes: dst is then
+// partly written and the caller rebuilds the superblock with the generic
+// decoder. dst + i * bstride must be 16-byte aligned.
+// Kept values of lane L (ordinals 16L..16L+15): position from the mask
+// cursor, exponent from the unary cursor, sign and mantissa fields from the
+// lane's slices of the speculation (rs) and cut-mantissa (rl) records.
+template <bool FULL, bool LONG>
+__device__ __forceinline__ void lane_kept_to_row(UnaryCursor& uc, MaskCursor& mc, uint2 rs, uint2 rl,
+                                                 const uint8_t* __restrict__ lut, uint16_t* row) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int pos = mc.next();
+    const uint32_t e = lut[uc.next<LONG>() & 255];
+    const int sh = 4 * (i & 7);
+    const uint32_t f = (i < 8 ? rs.x : rs.y) >> sh;
+    uint32_t bits = ((f & 8u) << 12) | (e << 7) | ((f & 7u) << 4);
+    if (FULL) bits |= ((i < 8 ? rl.x : rl.y) >> sh) & 15u;
+    row[pos] = (uint16_t)bits;
+  }
+}
+
+// Pruned values of lane L (pruned ordinals 16L..16L+15) from the inverted
+// mask, the pruned exponent stream and the lane's 16 verification bytes.
+template <bool LONG>
+__device__ __forceinline__ void lane_pruned_to_row(UnaryCursor& uc, MaskCursor& mc, uint4 pb,
+                                                   const uint8_t* __restrict__ lut, uint16_t* row) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int pos = mc.next();
+    const uint32_t e = lut[uc.next<LONG>() & 255];
+    const uint32_t wsel = (i >> 2) == 0 ? pb.x : (i >> 2) == 1 ? pb.y : (i >> 2) == 2 ? pb.z : pb.w;
+    const uint32_t byte = (wsel >> (8 * (i & 3))) & 0xFFu;
+    row[pos] = (uint16_t)(((byte & 0x80u) << 8) | (e << 7) | (byte & 0x7Fu));
+  }
+}
+
+// Rebuilds one whole superblock (Cassandra-1, k = 64, m = 3, 8 blocks) as bf16
+// bit patterns: the value at position p of block i goes to dst[i * bstride + p].
+// FULL merges speculation and verification data (lossless); otherwise the
+// draft value is written and pruned positions are zero. Lane L rebuilds kept
+// ordinals 16L..16L+15 (and, FULL, pruned ordinals 16L..16L+15) with the
+// cursors above; the unary streams are staged one after the other in `us`.
+// mask: 32 words, sm / lo: 64 words, pr: 128 words of the superblock (16-byte
+// aligned); sexp / vexp: its code streams. Returns false (warp-uniform) when a
+// stream is longer than the stage or holds fewer than 512 codes: dst is then
+// partly written and the caller rebuilds the superblock with the generic
+// decoder. dst + i * bstride must be 16-byte aligned.
+template <bool FULL>
+__device__ __forceinline__ bool lane_sb_tile(const uint32_t* __restrict__ mask, const uint32_t* __restrict__ sm,
+                                             const uint32_t* __restrict__ lo, const uint32_t* __restrict__ pr,
+                                             const uint32_t* __restrict__ sexp, int snw,
+                                             const uint32_t* __restrict__ vexp, int vnw,
+                                             const uint8_t* __restrict__ lut, UnaryStage& us, uint16_t* dst,
+                                             int bstride, int lane) {
+  if (snw > kStageWords || (FULL && vnw > kStageWords)) return false;
+  const int q = lane & 3;
+  uint16_t* row = dst + (lane >> 2) * bstride;
+  const uint4 mm = __ldg(reinterpret_cast<const uint4*>(mask) + (lane >> 2));
+  const uint2 rs = __ldg(reinterpret_cast<const uint2*>(sm) + lane);
+  uint2 rl = make_uint2(0u, 0u);
+  if (FULL) rl = __ldg(reinterpret_cast<const uint2*>(lo) + lane);
+  if (!FULL) {
+    uint4* z = reinterpret_cast<uint4*>(row + 32 * q);
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    z[0] = zero;
+    z[1] = zero;
+    z[2] = zero;
+    z[3] = zero;
+  }
+  bool long_codes;
+  const bool enough = stage_unary(sexp, snw, us, lane, &long_codes) >= 16 * 32;
+  __syncwarp();
+  if (!enough) return false;
+  UnaryCursor uc;
+  MaskCursor mc;
+  uc.init(us, unary_code_start(us, snw, 16 * lane));
+  mc.init(mm.x, mm.y, mm.z, mm.w, 16 * q);
+  if (long_codes)
+    lane_kept_to_row<FULL, true>(uc, mc, rs, rl, lut, row);
+  else
+    lane_kept_to_row<FULL, false>(uc, mc, rs, rl, lut, row);
+  if (FULL) {
+    const uint4 pb = __ldg(reinterpret_cast<const uint4*>(pr) + lane);
+    __syncwarp();  // every lane is done with the kept stream
+    const bool enough_v = stage_unary(vexp, vnw, us, lane, &long_codes) >= 16 * 32;
+    __syncwarp();
+    if (!enough_v) return false;
+    uc.init(us, unary_code_start(us, vnw, 16 * lane));
+    mc.init(~mm.x, ~mm.y, ~mm.z, ~mm.w, 16 * q);
+    if (long_codes)
+      lane_pruned_to_row<true>(uc, mc, pb, lut, row);
+    else
+      lane_pruned_to_row<false>(uc, mc, pb, lut, row);
+  }
+  __syncwarp();
+  return true;
+}
 
 }  // namespace cas

@@ -132,95 +132,3 @@ __device__ __forceinline__ void sb_rebuild_word(const WView& w, const SbInfo& in
 }
 
 }  // namespace cas
-
-namespace cas {
-
-// ------------------------------------------------------------------ fast path
-// Cassandra-1 with k = 64, m = 3 and a superblock of 8 full blocks: 512 kept
-// and 512 pruned values, every record exactly 8 (spec), 8 (cut mantissa) and
-// 16 (pruned bytes) words, so each lane's field offsets are compile-time.
-// Three SIMD phases with no per-lane branching:
-//   1. decode the unary streams cooperatively into exponents by ordinal;
-//   2. lane = ordinal: build every kept (and, FULL, pruned) value by ordinal;
-//   3. lane = mask word: each position takes the next kept or pruned value.
-constexpr int kFastSkew = 512 + 16;  // values by ordinal at index t + t/32 (bank skew)
-
-struct FastScratch {
-  uint32_t sm[64];   // spec records (s<<3 | f_hi per kept value)
-  uint32_t lo[64];   // cut mantissa bits per kept value
-  uint32_t pr[128];  // pruned bytes (s<<7 | f)
-  alignas(16) uint8_t ek[512];  // exponent by kept ordinal
-  alignas(16) uint8_t ep[512];  // exponent by pruned ordinal
-  uint16_t kv[kFastSkew];
-  uint16_t pv[kFastSkew];
-};
-
-// Decodes one superblock into 32 bf16 values per lane (positions 32 lane ..
-// 32 lane + 31, packed in pairs). mask: 32 words; sm, lo: 64 words; pr: 128
-// words (all consecutive over the 8 blocks); sexp/vexp: the superblock's
-// code streams. Ends with the lane's values in out; scratch is reused.
-template <bool FULL>
-__device__ __forceinline__ void fast_sb_decode(const uint32_t* __restrict__ mask, const uint32_t* __restrict__ sm,
-                                               const uint32_t* __restrict__ lo, const uint32_t* __restrict__ pr,
-                                               const uint32_t* __restrict__ sexp, int snw,
-                                               const uint32_t* __restrict__ vexp, int vnw,
-                                               const uint8_t* __restrict__ lut, FastScratch& f, int lane,
-                                               uint32_t out[16]) {
-  const uint32_t mw = __ldg(mask + lane);
-  const int cnt = __popc(mw);
-  const int o = warp_incl_add(cnt, lane) - cnt;
-  {
-    const uint2 r = __ldg(reinterpret_cast<const uint2*>(sm) + lane);
-    f.sm[2 * lane] = r.x;
-    f.sm[2 * lane + 1] = r.y;
-  }
-  if (FULL) {
-    const uint2 r = __ldg(reinterpret_cast<const uint2*>(lo) + lane);
-    f.lo[2 * lane] = r.x;
-    f.lo[2 * lane + 1] = r.y;
-    const uint4 q = __ldg(reinterpret_cast<const uint4*>(pr) + lane);
-    f.pr[4 * lane] = q.x;
-    f.pr[4 * lane + 1] = q.y;
-    f.pr[4 * lane + 2] = q.z;
-    f.pr[4 * lane + 3] = q.w;
-  }
-  const uint32_t sw0 = stream_word(sexp, snw, lane);
-  const uint32_t vw0 = FULL ? stream_word(vexp, vnw, lane) : 0u;
-  warp_decode_unary_512(sexp, snw, lut, f.ek, lane, sw0);
-  if (FULL) warp_decode_unary_512(vexp, vnw, lut, f.ep, lane, vw0);
-  __syncwarp();
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int t = lane + 32 * i;
-    const int tl = lane + 32 * (i & 1);  // ordinal within block i/2
-    const int wsel = 8 * (i >> 1) + (tl >> 3), sh = 4 * (tl & 7);
-    const uint32_t nib = (f.sm[wsel] >> sh) & 15u;
-    uint32_t v = ((nib >> 3) << 15) | ((uint32_t)f.ek[t] << 7) | ((nib & 7u) << 4);
-    if (FULL) v |= (f.lo[wsel] >> sh) & 15u;
-    f.kv[t + (t >> 5)] = (uint16_t)v;
-    if (FULL) {
-      const uint32_t byte = (f.pr[16 * (i >> 1) + (tl >> 2)] >> (8 * (tl & 3))) & 0xFFu;
-      f.pv[t + (t >> 5)] = (uint16_t)(((byte >> 7) << 15) | ((uint32_t)f.ep[t] << 7) | (byte & 0x7Fu));
-    }
-  }
-  __syncwarp();
-  int t = o, u = 32 * lane - o;
-#pragma unroll
-  for (int p = 0; p < 32; ++p) {
-    uint32_t v;
-    if ((mw >> p) & 1u) {
-      v = f.kv[t + (t >> 5)];
-      ++t;
-    } else {
-      v = FULL ? f.pv[u + (u >> 5)] : 0u;
-      ++u;
-    }
-    if (p & 1)
-      out[p >> 1] |= v << 16;
-    else
-      out[p >> 1] = v;
-  }
-  __syncwarp();
-}
-
-}  // namespace cas
