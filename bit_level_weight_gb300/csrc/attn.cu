@@ -24,6 +24,7 @@
 
 #include "kvview.cuh"
 #include "lanedec.cuh"
+#include "mma.cuh"
 #include "sbdecode.cuh"
 
 namespace cas {
@@ -79,33 +80,30 @@ __device__ __forceinline__ void decode_sb_tile(const KvDev& d, int st, int64_t n
                            *reinterpret_cast<UnaryStage*>(scratch), tile + row0 * kRow, kRow, lane))
       return;
   }
-  uint32_t v[16];
+  // generic decoder (other k, m, Cassandra-2, partial superblocks, fallback):
+  // lane L writes mask word L, zeros past the stream's tokens
+  uint16_t* dst = tile + (row0 + (lane >> 2)) * kRow + 32 * (lane & 3);
   int nb = 0;
   if (sb < nsb && d.variant == 1) {
     SbScratch sc{scratch, scratch + 1024, nullptr};
     WView w = kv_stream_view(d, st, n);
     SbInfo in = sb_prepare<1, FULL>(w, sb, lut, sc, lane);
     nb = in.nb;
-    if (lane < 4 * nb) sb_rebuild_word<1, FULL>(w, in, sc, lane, v);
+    if (lane < 4 * nb) sb_rebuild_store<1, FULL>(w, in, sc, lane, dst);
   } else if (sb < nsb) {
     SbScratch sc{scratch, scratch + 1024, reinterpret_cast<uint32_t*>(scratch + 2048)};
     WView w = kv_stream_view(d, st, n);
     SbInfo in = sb_prepare<2, FULL>(w, sb, lut, sc, lane);
     nb = in.nb;
-    if (lane < 4 * nb) sb_rebuild_word<2, FULL>(w, in, sc, lane, v);
+    if (lane < 4 * nb) sb_rebuild_store<2, FULL>(w, in, sc, lane, dst);
   }
-  uint4* dst = reinterpret_cast<uint4*>(tile + (row0 + (lane >> 2)) * kRow + 32 * (lane & 3));
-  if (lane < 4 * nb) {
-    dst[0] = make_uint4(v[0], v[1], v[2], v[3]);
-    dst[1] = make_uint4(v[4], v[5], v[6], v[7]);
-    dst[2] = make_uint4(v[8], v[9], v[10], v[11]);
-    dst[3] = make_uint4(v[12], v[13], v[14], v[15]);
-  } else {
-    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-    dst[0] = z;
-    dst[1] = z;
-    dst[2] = z;
-    dst[3] = z;
+  if (lane >= 4 * nb) {
+    uint4* z = reinterpret_cast<uint4*>(dst);
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    z[0] = zero;
+    z[1] = zero;
+    z[2] = zero;
+    z[3] = zero;
   }
   __syncwarp();
 }
@@ -220,6 +218,187 @@ __global__ void __launch_bounds__(kThreads) attn_chunk_kernel(AttnArgs a) {
   }
 }
 
+// Tensor-core variant of the chunk kernel (up to 32 query vectors per CTA in
+// MT m16 tiles): per 32-token step, after the K and V superblocks are
+// decoded into the tiles, S = Q K^T (mma m16n8k16, bf16 inputs, fp32
+// accumulators; Q is the unscaled bf16 query, the 1/sqrt(128) scale is applied
+// to S in fp32), the online softmax runs on the S fragments (rows shared by
+// the 4 lanes of a quad), and O += P V with P split into two bf16 terms
+// (p = hi + lo, |p - hi - lo| <= 2^-17 p) so the product keeps fp32-like
+// precision. With MT = 2, warps 2i and 2i+1 take m-tile i and split the 128
+// output dimensions; with MT = 1 the 4 warps split them four ways (each
+// warp recomputes the m-tile's S, which is cheap next to the decode).
+template <bool FULL, int MT>
+__global__ void __launch_bounds__(kThreads) attn_mma_kernel(AttnArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint16_t* Kt = reinterpret_cast<uint16_t*>(smem);
+  uint16_t* Vt = Kt + kStepTok * kRow;
+  uint16_t* Qt = Vt + kStepTok * kRow;  // [16 MT][kRow], rows >= nq zero
+  uint8_t* lutK = reinterpret_cast<uint8_t*>(Qt + 16 * MT * kRow);
+  uint8_t* lutV = lutK + 256;
+  uint8_t* scr = lutV + 256;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint8_t* wscr = scr + warp * kScratchWarp;
+  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z / a.ngroups;
+  const int qv0 = (blockIdx.z % a.ngroups) * kQvPerCta;
+  const KvDev& d = a.kv[b];
+  const int H = d.H, T = a.T, G = a.G, nq = min(T * G - qv0, kQvPerCta);
+  const int64_t n = *(volatile const int64_t*)&kv_state(d)->n_tokens;
+  const int64_t steps = (n + kStepTok - 1) / kStepTok;
+  const int64_t t_begin = steps * chunk / a.nchunk * kStepTok;
+  const int64_t t_end = min(n, steps * (chunk + 1) / a.nchunk * kStepTok);
+
+  for (int i = threadIdx.x; i < 16 * MT * CAS_BLK; i += kThreads) {
+    const int r = i / CAS_BLK, dd = i % CAS_BLK;
+    uint16_t v = 0;
+    if (r < nq) {
+      const int qv = qv0 + r, j = qv / G, g = qv % G;
+      v = a.q[(((int64_t)b * T + j) * a.Hq + h * G + g) * CAS_BLK + dd];
+    }
+    Qt[r * kRow + dd] = v;
+  }
+  for (int i = threadIdx.x; i < 256; i += kThreads) {
+    lutK[i] = kv_exp_of_rank(d, h)[i];
+    lutV[i] = kv_exp_of_rank(d, H + h)[i];
+  }
+  __syncthreads();
+
+  constexpr int WPM = 4 / MT;       // warps per m-tile
+  constexpr int NT = 16 / WPM;      // 8-dim output tiles per warp
+  const int mt = MT == 1 ? 0 : warp / WPM;
+  const int dbase = (warp % WPM) * NT * 8;
+  const int g = lane >> 2, tq = lane & 3;
+  const int r0 = mt * 16 + g, r1 = r0 + 8;  // local query rows of this lane
+  // last token each row may attend to (causal among the last T tokens for verify); -1: no row
+  const int64_t last0 = r0 < nq ? (FULL ? n - T + (qv0 + r0) / G : n - 1) : -1;
+  const int64_t last1 = r1 < nq ? (FULL ? n - T + (qv0 + r1) / G : n - 1) : -1;
+  float o[NT][4];
+#pragma unroll
+  for (int i = 0; i < NT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  const bool active = mt * 16 < nq;
+
+  for (int64_t t0 = t_begin; t0 < t_end; t0 += kStepTok) {
+    const int64_t sb = t0 / CAS_SB + warp;
+    decode_sb_tile<FULL>(d, h, n, sb, Kt, warp * CAS_SB, lutK, wscr, lane);
+    decode_sb_tile<FULL>(d, H + h, n, sb, Vt, warp * CAS_SB, lutV, wscr, lane);
+    __syncthreads();
+    if (active) {
+      // S = Q K^T: 16 rows x 32 tokens
+      float s[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < CAS_BLK / 16; ++ks) {
+        uint32_t af[4];
+        ldmatrix_x4(af, Qt + (mt * 16 + (lane & 15)) * kRow + ks * 16 + (lane >> 4) * 8);
+#pragma unroll
+        for (int nt2 = 0; nt2 < 2; ++nt2) {
+          uint32_t bf[4];
+          const int mi = lane >> 3;
+          ldmatrix_x4(bf, Kt + (nt2 * 16 + (mi >> 1) * 8 + (lane & 7)) * kRow + ks * 16 + (mi & 1) * 8);
+          mma_bf16(s[2 * nt2], af, bf[0], bf[1]);
+          mma_bf16(s[2 * nt2 + 1], af, bf[2], bf[3]);
+        }
+      }
+      // online softmax on the fragments
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int64_t tok = t0 + nt * 8 + 2 * tq + (e & 1);
+          const bool ok = tok < t_end && tok <= (e < 2 ? last0 : last1);
+          s[nt][e] = ok ? s[nt][e] * a.scale : -INFINITY;
+        }
+        mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+        mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+      }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(CAS_FULL, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(CAS_FULL, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(CAS_FULL, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(CAS_FULL, mx1, 2));
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float c0 = mn0 == -INFINITY ? 1.f : (m0 == -INFINITY ? 0.f : __expf(m0 - mn0));
+      const float c1 = mn1 == -INFINITY ? 1.f : (m1 == -INFINITY ? 0.f : __expf(m1 - mn1));
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float mref = e < 2 ? mn0 : mn1;
+          const float p = s[nt][e] == -INFINITY ? 0.f : __expf(s[nt][e] - mref);
+          s[nt][e] = p;
+        }
+        sum0 += s[nt][0] + s[nt][1];
+        sum1 += s[nt][2] + s[nt][3];
+      }
+      sum0 += __shfl_xor_sync(CAS_FULL, sum0, 1);
+      sum0 += __shfl_xor_sync(CAS_FULL, sum0, 2);
+      sum1 += __shfl_xor_sync(CAS_FULL, sum1, 1);
+      sum1 += __shfl_xor_sync(CAS_FULL, sum1, 2);
+      l0 = l0 * c0 + sum0;
+      l1 = l1 * c1 + sum1;
+      m0 = mn0;
+      m1 = mn1;
+#pragma unroll
+      for (int i = 0; i < NT; ++i) {
+        o[i][0] *= c0;
+        o[i][1] *= c0;
+        o[i][2] *= c1;
+        o[i][3] *= c1;
+      }
+      // O += P V over two 16-token k-steps; P = hi + lo in bf16
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        uint32_t ph[4], pl[4];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const float* sp = s[2 * kk + half];
+          const uint32_t h01 = pack_bf16x2(sp[0], sp[1]), h23 = pack_bf16x2(sp[2], sp[3]);
+          const float e0 = sp[0] - __uint_as_float(h01 << 16), e1 = sp[1] - __uint_as_float(h01 & 0xFFFF0000u);
+          const float e2 = sp[2] - __uint_as_float(h23 << 16), e3 = sp[3] - __uint_as_float(h23 & 0xFFFF0000u);
+          ph[2 * half] = h01;
+          ph[2 * half + 1] = h23;
+          pl[2 * half] = pack_bf16x2(e0, e1);
+          pl[2 * half + 1] = pack_bf16x2(e2, e3);
+        }
+        // A fragment order: (row g, k lo), (row g+8, k lo), (row g, k hi), (row g+8, k hi)
+        const uint32_t ah[4] = {ph[0], ph[1], ph[2], ph[3]};
+        const uint32_t al[4] = {pl[0], pl[1], pl[2], pl[3]};
+#pragma unroll
+        for (int i = 0; i < NT; i += 2) {
+          uint32_t bv[4];
+          const int mi = lane >> 3;
+          ldmatrix_x4_trans(bv, Vt + (kk * 16 + (mi & 1) * 8 + (lane & 7)) * kRow + dbase + i * 8 + (mi >> 1) * 8);
+          mma_bf16(o[i], ah, bv[0], bv[1]);
+          mma_bf16(o[i], al, bv[0], bv[1]);
+          mma_bf16(o[i + 1], ah, bv[2], bv[3]);
+          mma_bf16(o[i + 1], al, bv[2], bv[3]);
+        }
+      }
+    }
+    __syncthreads();
+  }
+  // partials: O (unnormalised), max and sum of every query row
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    const int r = rr ? r1 : r0;
+    if (!active || r >= nq) continue;
+    const int qv = qv0 + r, j = qv / G, gg = qv % G;
+    float* dst = a.part + ((((int64_t)b * T + j) * a.Hq + h * G + gg) * a.nchunk + chunk) * kPart;
+#pragma unroll
+    for (int i = 0; i < NT; ++i)
+      *reinterpret_cast<float2*>(dst + dbase + i * 8 + 2 * tq) = make_float2(o[i][2 * rr], o[i][2 * rr + 1]);
+    if (warp % WPM == 0 && tq == 0) {
+      dst[CAS_BLK] = rr ? m1 : m0;
+      dst[CAS_BLK + 1] = rr ? l1 : l0;
+    }
+  }
+}
+
+constexpr int kCombineWarps = 32;  // warps of a combine CTA (each merges every 32nd chunk)
+
 struct CombineArgs {
   const float* part;
   const uint16_t* q;       // [B][T][Hq][128]
@@ -231,12 +410,12 @@ struct CombineArgs {
   float scale;
 };
 
-// One CTA of 256 threads per (sequence, query token, q head). Warp w merges
-// chunks w, w+8, ... with lane L holding dims 4L..4L+3 (online max / sum);
-// the 8 warp results and the bf16 tail tokens are merged in shared memory.
-__global__ void __launch_bounds__(256) attn_combine_kernel(CombineArgs a) {
-  __shared__ float wm[8], wl[8];
-  __shared__ float4 wo[8][32];
+// One CTA of 32 warps per (sequence, query token, q head). Warp w merges
+// chunks w, w+32, ... with lane L holding dims 4L..4L+3 (online max / sum);
+// the warp results and the bf16 tail tokens are merged in shared memory.
+__global__ void __launch_bounds__(kCombineWarps * 32) attn_combine_kernel(CombineArgs a) {
+  __shared__ float wm[kCombineWarps], wl[kCombineWarps];
+  __shared__ float4 wo[kCombineWarps][32];
   __shared__ float ts[kMaxT];
   const int hq = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -258,7 +437,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(CombineArgs a) {
   }
   float M = -INFINITY, L = 0.f;
   float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c = warp; c < used; c += 8) {
+  for (int c = warp; c < used; c += kCombineWarps) {
     const float mc = P[c * kPart + CAS_BLK];
     if (mc == -INFINITY) continue;
     const float lc = P[c * kPart + CAS_BLK + 1];
@@ -280,11 +459,11 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(CombineArgs a) {
   __syncthreads();
   if (warp == 0) {
     float Mt = -INFINITY;
-    for (int w = 0; w < 8; ++w) Mt = fmaxf(Mt, wm[w]);
+    for (int w = 0; w < kCombineWarps; ++w) Mt = fmaxf(Mt, wm[w]);
     for (int t = 0; t < a.n_tail; ++t) Mt = fmaxf(Mt, ts[t]);
     float Lt = 0.f;
     float4 Ot = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int w = 0; w < 8; ++w) {
+    for (int w = 0; w < kCombineWarps; ++w) {
       if (wm[w] == -INFINITY) continue;
       const float f = __expf(wm[w] - Mt);
       Lt += wl[w] * f;
@@ -309,16 +488,35 @@ size_t chunk_smem(int qv_alloc) {
 
 int nchunks(int64_t max_tokens) { return (int)((max_tokens + kChunk - 1) / kChunk); }
 
+size_t mma_smem(int mt) { return (size_t)2 * kStepTok * kRow * 2 + (size_t)16 * mt * kRow * 2 + 512 + kWarps * kScratchWarp; }
+
+// Sets a.nchunk to one wave of resident CTAs (at most the workspace's count).
+int one_wave(AttnArgs& a, int Hkv, const void* kern, size_t smem) {
+  const int per_sm = occupancy(kern, kThreads, smem);
+  if (per_sm < 1) return CAS_ERR_CUDA;
+  const int64_t slots = (int64_t)per_sm * sm_count();
+  a.nchunk = (int)std::max<int64_t>(1, std::min<int64_t>(a.nchunk, slots / ((int64_t)Hkv * a.B * a.ngroups)));
+  return CAS_OK;
+}
+
+template <bool FULL, int MT>
+int launch_mma(AttnArgs& a, int Hkv, cudaStream_t st) {
+  const size_t smem = mma_smem(MT);
+  auto kern = attn_mma_kernel<FULL, MT>;
+  const int s = one_wave(a, Hkv, (const void*)kern, smem);
+  if (s) return s;
+  kern<<<dim3(a.nchunk, Hkv, a.B * a.ngroups), kThreads, smem, st>>>(a);
+  return launch_status();
+}
+
 // a.nchunk on entry: the most chunks the workspace holds; on return: the
 // chunks launched (one wave of resident CTAs, at most that many).
 template <bool FULL, int QPW>
 int launch_chunk(AttnArgs& a, int Hkv, cudaStream_t st) {
   size_t smem = chunk_smem(a.qv_alloc);
   auto kern = attn_chunk_kernel<FULL, QPW>;
-  const int per_sm = occupancy((const void*)kern, kThreads, smem);
-  if (per_sm < 1) return CAS_ERR_CUDA;
-  const int64_t slots = (int64_t)per_sm * sm_count();
-  a.nchunk = (int)std::max<int64_t>(1, std::min<int64_t>(a.nchunk, slots / ((int64_t)Hkv * a.B * a.ngroups)));
+  const int s = one_wave(a, Hkv, (const void*)kern, smem);
+  if (s) return s;
   dim3 grid(a.nchunk, Hkv, a.B * a.ngroups);
   kern<<<grid, kThreads, smem, st>>>(a);
   return launch_status();
@@ -366,9 +564,7 @@ int run_attn(bool full, const cas_kv* const* kv, int B, const uint16_t* q, int T
     else if (qpw <= 4) s = launch_chunk<false, 4>(a, Hkv, st);
     else s = launch_chunk<false, 8>(a, Hkv, st);
   } else {
-    if (qpw <= 1) s = launch_chunk<true, 1>(a, Hkv, st);
-    else if (qpw <= 4) s = launch_chunk<true, 4>(a, Hkv, st);
-    else s = launch_chunk<true, 8>(a, Hkv, st);
+    s = a.qv_alloc > 16 ? launch_mma<true, 2>(a, Hkv, st) : launch_mma<true, 1>(a, Hkv, st);
   }
   if (s) return s;
   c.part = a.part;
@@ -383,7 +579,7 @@ int run_attn(bool full, const cas_kv* const* kv, int B, const uint16_t* q, int T
   c.nchunk = a.nchunk;
   c.n_tail = full ? 0 : n_tail;
   c.scale = a.scale;
-  attn_combine_kernel<<<dim3(Hq, T, B), 256, 0, st>>>(c);
+  attn_combine_kernel<<<dim3(Hq, T, B), kCombineWarps * 32, 0, st>>>(c);
   return launch_status();
 }
 

@@ -14,6 +14,7 @@
 #include <algorithm>
 
 #include "lanedec.cuh"
+#include "mma.cuh"
 #include "sbdecode.cuh"
 
 namespace cas {
@@ -31,20 +32,6 @@ struct GemmArgs {
   float* Y;
   int T;
 };
-
-__device__ __forceinline__ void ldmatrix_x4(uint32_t r[4], const void* p) {
-  uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(a));
-}
-__device__ __forceinline__ void mma_bf16(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 
 constexpr int kScratchGeneric = 2048 + kResWords * 4;
 constexpr int kScratchWarp = (int)sizeof(UnaryStage) > kScratchGeneric ? (int)sizeof(UnaryStage) : kScratchGeneric;

@@ -73,43 +73,57 @@ __device__ __forceinline__ SbInfo sb_prepare(const WView& w, int64_t s, const ui
   return in;
 }
 
-// Rebuilds the 32 values of this lane's mask word as bf16 bit patterns,
-// packed in pairs (out[i] = value 2i | value 2i+1 << 16).
+// Walks the 32 positions of this lane's mask word in order; at(p) returns
+// the bf16 bit pattern of position p (draft or, FULL, exact value).
 template <int VAR, bool FULL>
-__device__ __forceinline__ void sb_rebuild_word(const WView& w, const SbInfo& in, SbScratch sc, int lane,
-                                                uint32_t out[16]) {
-  const int k = w.k, m = w.m;
-  int blk = lane >> 2, g = lane & 3;
-  int64_t gb = in.gb0 + blk;
-  int o = in.o, uo = in.uo;
-  int t = o - k * blk, u = uo - (CAS_BLK - k) * blk;
-  const uint32_t* rs = VAR == 1 ? w.ssm + gb * w.rec_sm : w.sq + gb * w.rec_q;
-  const uint32_t* rl = w.vlo + gb * w.rec_lo;
-  const uint32_t* rp = w.vpr + gb * w.rec_pr;
-  int Ep = VAR == 2 ? max((int)__ldg(w.smx + gb * 4 + g), 1) : 1;
-  float scale = VAR == 2 ? pow2_biased(Ep - m) : 0.f;
-  int rb = in.rbit;
-  uint32_t mw = in.mw;
-#pragma unroll
-  for (int p = 0; p < 32; ++p) {
+struct SbRebuilder {
+  const uint32_t *rs, *rl, *rp;
+  const uint8_t *code, *vcode;
+  const uint32_t* res;
+  int m, o, uo, t, u, Ep, rb;
+  float scale;
+  uint32_t mw;
+
+  __device__ __forceinline__ SbRebuilder(const WView& w, const SbInfo& in, SbScratch sc, int lane) {
+    const int k = w.k;
+    m = w.m;
+    const int blk = lane >> 2, g = lane & 3;
+    const int64_t gb = in.gb0 + blk;
+    o = in.o;
+    uo = in.uo;
+    t = o - k * blk;
+    u = uo - (CAS_BLK - k) * blk;
+    rs = VAR == 1 ? w.ssm + gb * w.rec_sm : w.sq + gb * w.rec_q;
+    rl = w.vlo + gb * w.rec_lo;
+    rp = w.vpr + gb * w.rec_pr;
+    code = sc.code;
+    vcode = sc.vcode;
+    res = sc.res;
+    Ep = VAR == 2 ? max((int)__ldg(w.smx + gb * 4 + g), 1) : 1;
+    scale = VAR == 2 ? pow2_biased(Ep - m) : 0.f;
+    rb = in.rbit;
+    mw = in.mw;
+  }
+
+  __device__ __forceinline__ uint32_t at(int p) {
     uint32_t bits = 0;
     if ((mw >> p) & 1u) {
       if (VAR == 1) {
         uint32_t fld = get_field(rs, t * (m + 1), m + 1);
         uint32_t f = (fld & ((1u << m) - 1u)) << (7 - m);
         if (FULL && m < 7) f |= get_field(rl, t * (7 - m), 7 - m);
-        bits = ((fld >> m) << 15) | ((uint32_t)sc.code[o] << 7) | f;
+        bits = ((fld >> m) << 15) | ((uint32_t)code[o] << 7) | f;
       } else {
         uint32_t fld = get_field(rs, t * (m + 2), m + 2);
         uint32_t s = (fld >> (m + 1)) & 1u, q = fld & ((1u << (m + 1)) - 1u);
         if (!FULL) {
           bits = (__float_as_uint((float)q * scale) >> 16) | (s << 15);
         } else {
-          int d = sc.code[o];
+          int d = code[o];
           int wd = min(7 - m + d, 8);
-          uint32_t res = get_field(sc.res, rb, wd);
+          uint32_t r = get_field(res, rb, wd);
           rb += wd;
-          uint32_t sig = ((q << wd) | res) & 0xFFu;
+          uint32_t sig = ((q << wd) | r) & 0xFFu;
           uint32_t e = (sig & 0x80u) ? (uint32_t)(Ep - d) : 0u;
           bits = (s << 15) | (e << 7) | (sig & 0x7Fu);
         }
@@ -119,16 +133,39 @@ __device__ __forceinline__ void sb_rebuild_word(const WView& w, const SbInfo& in
     } else {
       if (FULL) {
         uint32_t byte = (__ldg(rp + (u >> 2)) >> ((u & 3) * 8)) & 0xFFu;
-        bits = ((byte >> 7) << 15) | ((uint32_t)sc.vcode[uo] << 7) | (byte & 0x7Fu);
+        bits = ((byte >> 7) << 15) | ((uint32_t)vcode[uo] << 7) | (byte & 0x7Fu);
       }
       ++u;
       ++uo;
     }
+    return bits;
+  }
+};
+
+// Rebuilds the 32 values of this lane's mask word as bf16 bit patterns,
+// packed in pairs (out[i] = value 2i | value 2i+1 << 16).
+template <int VAR, bool FULL>
+__device__ __forceinline__ void sb_rebuild_word(const WView& w, const SbInfo& in, SbScratch sc, int lane,
+                                                uint32_t out[16]) {
+  SbRebuilder<VAR, FULL> rb(w, in, sc, lane);
+#pragma unroll
+  for (int p = 0; p < 32; ++p) {
+    const uint32_t bits = rb.at(p);
     if (p & 1)
       out[p >> 1] |= bits << 16;
     else
       out[p >> 1] = bits;
   }
+}
+
+// Same values stored one by one to dst[0..31] (a rolled loop: little register
+// pressure, for fallback paths inside register-heavy kernels).
+template <int VAR, bool FULL>
+__device__ __forceinline__ void sb_rebuild_store(const WView& w, const SbInfo& in, SbScratch sc, int lane,
+                                                 uint16_t* dst) {
+  SbRebuilder<VAR, FULL> rb(w, in, sc, lane);
+#pragma unroll 1
+  for (int p = 0; p < 32; ++p) dst[p] = (uint16_t)rb.at(p);
 }
 
 }  // namespace cas
