@@ -236,10 +236,32 @@ __global__ void __launch_bounds__(kThreads) draft_gemv_kernel(GemvArgs a) {
 // times x (bf16 in shared memory, staged once per CTA by a TMA bulk copy).
 // Superblocks whose stream exceeds the stage (or holds fewer than 512 codes)
 // go through the generic superblock decoder.
-union LaneWarp {
+struct LaneStage {
   UnaryStage us;
+  alignas(16) uint8_t pos[CAS_SB * 64];  // block position of every kept ordinal
+};
+union LaneWarp {
+  LaneStage ls;
   uint8_t code[1024];  // generic decoder scratch (exponents by kept ordinal)
 };
+
+// Lane L = mask word L of the superblock (block L/4, positions 32(L%4)..+31)
+// writes the block position of each of its kept values at their superblock
+// ordinal. Positions of a corrupt mask (a block without exactly 64 kept
+// values) land at wrong ordinals but never outside the array.
+__device__ __forceinline__ void expand_mask_positions(uint32_t mw, uint8_t* pos, int lane) {
+  const int cnt = __popc(mw);
+  int idx = warp_incl_add(cnt, lane) - cnt;
+  uint32_t pv = 32u * (lane & 3);
+#pragma unroll
+  for (int p = 0; p < 32; ++p) {
+    if ((mw >> p) & 1u) {
+      pos[idx & (CAS_SB * 64 - 1)] = (uint8_t)pv;
+      ++idx;
+    }
+    ++pv;
+  }
+}
 
 template <int NV>
 __device__ __forceinline__ void gemv_superblock_generic(const WView& w, int64_t s, const uint8_t* lut8,
@@ -264,11 +286,12 @@ __device__ __forceinline__ void gemv_superblock_generic(const WView& w, int64_t 
 // The lane's 16 kept values times x: value = sign, exponent (rank table) and
 // the 3 high mantissa bits of the record field; x is bf16 in shared memory.
 template <int NV, bool LONG>
-__device__ __forceinline__ void lane_kept_dot(UnaryCursor& uc, MaskCursor& mc, uint2 rr, const uint8_t* lut8,
+__device__ __forceinline__ void lane_kept_dot(UnaryCursor& uc, uint4 pq, uint2 rr, const uint8_t* lut8,
                                               const uint16_t* xl, int K, float acc[NV]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const int pos = mc.next();
+    const uint32_t pw = (i >> 2) == 0 ? pq.x : (i >> 2) == 1 ? pq.y : (i >> 2) == 2 ? pq.z : pq.w;
+    const int pos = (pw >> (8 * (i & 3))) & 127u;
     const uint32_t e = lut8[uc.next<LONG>() & 255];
     const uint32_t f = (i < 8 ? rr.x : rr.y) >> (4 * (i & 7));
     const float val = __uint_as_float(((f & 8u) << 28) | (e << 23) | ((f & 7u) << 20));
@@ -306,15 +329,17 @@ __global__ void __launch_bounds__(kThreads, NV <= 2 ? 5 : 4) draft_gemv_fast_ker
     return;
   }
 
-  const int nsr = w.nsr, nbr = w.nbr;
+  const int nsr = w.nsr;
   const int nsb = (int)w.nsb;
   const int stride = gridDim.x * kWarps;
+  const int dn = stride / nsr, dj = stride - dn * nsr;  // (row, column) step of the superblock loop
   const uint32_t lim = (uint32_t)a.sexp_words;
-  for (int s = blockIdx.x * kWarps + warp; s < nsb; s += stride) {
-    const int n = s / nsr;
-    const int j = s - n * nsr;
-    const int64_t gb0 = (int64_t)n * nbr + CAS_SB * j;
-    const uint4 mm = __ldg(reinterpret_cast<const uint4*>(w.mask) + gb0 + (lane >> 2));
+  int s = blockIdx.x * kWarps + warp;
+  int n = s / nsr, j = s - n * nsr;
+  for (; s < nsb; s += stride) {
+    // superblock s = n * nsr + j is blocks gb0 .. gb0 + 7 (rows are whole superblocks)
+    const int64_t gb0 = (int64_t)s * CAS_SB;
+    const uint32_t mw = __ldg(w.mask + gb0 * 4 + lane);
     const uint2 rr = __ldg(reinterpret_cast<const uint2*>(w.ssm + gb0 * 8) + lane);
     const uint32_t sb1 = min(__ldg(w.sidx + s + 1), lim), sb0 = min(__ldg(w.sidx + s), sb1);
     const int nw = (int)(sb1 - sb0);
@@ -323,20 +348,22 @@ __global__ void __launch_bounds__(kThreads, NV <= 2 ? 5 : 4) draft_gemv_fast_ker
 #pragma unroll
     for (int q = 0; q < NV; ++q) acc[q] = 0.f;
     bool fast = nw <= kStageWords, long_codes = false;
-    if (fast) fast = stage_unary(w.sexp + sb0, nw, lw.us, lane, &long_codes) >= 16 * 32;
+    if (fast) {
+      fast = stage_unary(w.sexp + sb0, nw, lw.ls.us, lane, &long_codes) >= 16 * 32;
+      expand_mask_positions(mw, lw.ls.pos, lane);
+    }
     __syncwarp();
     if (fast) {
       UnaryCursor uc;
-      uc.init(lw.us, unary_code_start(lw.us, nw, 16 * lane));
-      MaskCursor mc;
-      mc.init(mm.x, mm.y, mm.z, mm.w, 16 * (lane & 3));
+      uc.init(lw.ls.us, unary_code_start(lw.ls.us, nw, 16 * lane));
+      const uint4 pq = reinterpret_cast<const uint4*>(lw.ls.pos)[lane];
       const uint16_t* xl = xsb + CAS_BLK * (lane >> 2);
       if (long_codes)
-        lane_kept_dot<NV, true>(uc, mc, rr, lut8, xl, K, acc);
+        lane_kept_dot<NV, true>(uc, pq, rr, lut8, xl, K, acc);
       else
-        lane_kept_dot<NV, false>(uc, mc, rr, lut8, xl, K, acc);
-      __syncwarp();
+        lane_kept_dot<NV, false>(uc, pq, rr, lut8, xl, K, acc);
     }
+    __syncwarp();
     if (!fast) {
 #pragma unroll
       for (int q = 0; q < NV; ++q) acc[q] = 0.f;
@@ -346,6 +373,12 @@ __global__ void __launch_bounds__(kThreads, NV <= 2 ? 5 : 4) draft_gemv_fast_ker
     for (int q = 0; q < NV; ++q) {
       const float r = warp_sumf(acc[q]);
       if (lane == 0) atomicAdd(a.y + (int64_t)q * w.N + n, r);
+    }
+    n += dn;
+    j += dj;
+    if (j >= nsr) {
+      j -= nsr;
+      ++n;
     }
   }
 }
