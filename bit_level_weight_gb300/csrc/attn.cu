@@ -42,8 +42,10 @@ constexpr int kMaxT = 16;
 constexpr int kQvPerCta = 32;  // query vectors per CTA (8 per warp)
 // per-warp decode scratch: the cursor decoder's staged stream, or kept codes +
 // pruned codes + the Cassandra-2 residual words of one superblock
+// (a multiple of 16 bytes: the tile decoder reads its position arrays as uint4)
 constexpr int kScratchWarp =
-    (int)sizeof(UnaryStage) > 2048 + 4 * kResWords ? (int)sizeof(UnaryStage) : 2048 + 4 * kResWords;
+    (((int)sizeof(TileStage) > 2048 + 4 * kResWords ? (int)sizeof(TileStage) : 2048 + 4 * kResWords) + 15) & ~15;
+static_assert(kScratchWarp % 16 == 0 && alignof(TileStage) <= 16, "per-warp scratch alignment");
 
 struct AttnArgs {
   KvDev kv[kMaxBatch];
@@ -77,7 +79,7 @@ __device__ __forceinline__ void decode_sb_tile(const KvDev& d, int st, int64_t n
                            (const uint32_t*)kv_sec(d, CAS_KV_VER_PR, st) + sb * 128,
                            (const uint32_t*)kv_sec(d, CAS_KV_SPEC_EXP, st) + a0, (int)(a1 - a0),
                            (const uint32_t*)kv_sec(d, CAS_KV_VER_EXP, st) + v0, (int)(v1 - v0), lut,
-                           *reinterpret_cast<UnaryStage*>(scratch), tile + row0 * kRow, kRow, lane))
+                           *reinterpret_cast<TileStage*>(scratch), tile + row0 * kRow, kRow, lane))
       return;
   }
   // generic decoder (other k, m, Cassandra-2, partial superblocks, fallback):

@@ -34,7 +34,10 @@ struct GemmArgs {
 };
 
 constexpr int kScratchGeneric = 2048 + kResWords * 4;
-constexpr int kScratchWarp = (int)sizeof(UnaryStage) > kScratchGeneric ? (int)sizeof(UnaryStage) : kScratchGeneric;
+// a multiple of 16 bytes: the tile decoder reads its position arrays as uint4
+constexpr int kScratchWarp =
+    (((int)sizeof(TileStage) > kScratchGeneric ? (int)sizeof(TileStage) : kScratchGeneric) + 15) & ~15;
+static_assert(kScratchWarp % 16 == 0 && alignof(TileStage) <= 16, "per-warp scratch alignment");
 
 // FAST: Cassandra-1, k = 64, m = 3, whole superblocks (per-lane cursors, lane_sb_tile).
 template <int VAR, int NT, bool FAST>
@@ -48,7 +51,7 @@ __global__ void __launch_bounds__(kThreads) verify_gemm_kernel(GemmArgs a) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint8_t* wscr = scratch + warp * kScratchWarp;
   SbScratch sc{wscr, wscr + 1024, reinterpret_cast<uint32_t*>(wscr + 2048)};
-  UnaryStage& us = *reinterpret_cast<UnaryStage*>(wscr);
+  TileStage& ts = *reinterpret_cast<TileStage*>(wscr);
   for (int i = threadIdx.x; i < 256; i += kThreads) s_lut[i] = a.lut.v[i];
   __syncthreads();
 
@@ -71,7 +74,7 @@ __global__ void __launch_bounds__(kThreads) verify_gemm_kernel(GemmArgs a) {
         const uint32_t a0 = __ldg(w.sidx + s), a1 = __ldg(w.sidx + s + 1);
         const uint32_t v0 = __ldg(w.vidx + s), v1 = __ldg(w.vidx + s + 1);
         done = lane_sb_tile<true>(w.mask + gb0 * 4, w.ssm + gb0 * 8, w.vlo + gb0 * 8, w.vpr + gb0 * 16,
-                                  w.sexp + a0, (int)(a1 - a0), w.vexp + v0, (int)(v1 - v0), s_lut, us,
+                                  w.sexp + a0, (int)(a1 - a0), w.vexp + v0, (int)(v1 - v0), s_lut, ts,
                                   tile + r * kTileStride, CAS_BLK, lane);
       }
       if (done) {

@@ -245,23 +245,6 @@ union LaneWarp {
   uint8_t code[1024];  // generic decoder scratch (exponents by kept ordinal)
 };
 
-// Lane L = mask word L of the superblock (block L/4, positions 32(L%4)..+31)
-// writes the block position of each of its kept values at their superblock
-// ordinal. Positions of a corrupt mask (a block without exactly 64 kept
-// values) land at wrong ordinals but never outside the array.
-__device__ __forceinline__ void expand_mask_positions(uint32_t mw, uint8_t* pos, int lane) {
-  const int cnt = __popc(mw);
-  int idx = warp_incl_add(cnt, lane) - cnt;
-  uint32_t pv = 32u * (lane & 3);
-#pragma unroll
-  for (int p = 0; p < 32; ++p) {
-    if ((mw >> p) & 1u) {
-      pos[idx & (CAS_SB * 64 - 1)] = (uint8_t)pv;
-      ++idx;
-    }
-    ++pv;
-  }
-}
 
 template <int NV>
 __device__ __forceinline__ void gemv_superblock_generic(const WView& w, int64_t s, const uint8_t* lut8,

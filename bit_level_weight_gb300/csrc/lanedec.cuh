@@ -1,17 +1,17 @@
-// lanedec.cuh - per-lane cursors for superblocks with k = 64: 512 kept (and
+// lanedec.cuh - per-lane decoding of superblocks with k = 64: 512 kept (and
 // 512 pruned) values, 16 consecutive ordinals per lane.
 //
 // Lane L owns kept ordinals 16L..16L+15 of the superblock: they are the
 // ordinals 16(L%4)..16(L%4)+15 of block L/4, so their sign/mantissa fields are
-// one 64-bit slice of that block's record and their positions follow one
-// another in that block's mask. A lane walks two cursors:
-//   - a unary cursor over the superblock's exponent code stream (MSB-first,
-//     staged in shared memory): each step returns the rank of the next code
-//     (Cassandra blog review, section 3.2: a code is `rank` zeros and a one);
-//   - a mask cursor over the block's four mask words: each step returns the
-//     position of the next kept (or, on the inverted mask, pruned) value.
-// Both refill from the next word with predicated moves (no global load in the
-// loop); a code that spans more than one further word takes a rare loop.
+// one 64-bit slice of that block's record. The warp first stages the
+// superblock's unary exponent stream in shared memory (with popcount prefixes)
+// and expands the mask into the block position of every ordinal (lane = mask
+// word). Each lane then finds where its first code starts and walks a unary
+// cursor (Cassandra blog review, section 3.2: a code is `rank` zeros and a
+// one): each step returns the rank of the next code. The cursor refills from
+// the next staged word with predicated moves; a code that spans more than one
+// further word (possible only when a staged word is all zeros) takes a rare
+// loop, compiled in only for such streams.
 #pragma once
 #include "common.cuh"
 
@@ -105,67 +105,43 @@ struct UnaryCursor {
   }
 };
 
-// Cursor over the set bits of a block's 128-bit mask (LSB-first positions),
-// starting at the r-th set bit (0-based). Words are held bit-reversed so the
-// next position is a clz.
-struct MaskCursor {
-  uint32_t cur, n1, n2, n3;
-  int base;
-
-  __device__ __forceinline__ void init(uint32_t m0, uint32_t m1, uint32_t m2, uint32_t m3, int r) {
-    const int c0 = __popc(m0), c01 = c0 + __popc(m1), c012 = c01 + __popc(m2);
-    const int w0 = (r >= c0) + (r >= c01) + (r >= c012);
-    const int excl = w0 == 0 ? 0 : w0 == 1 ? c0 : w0 == 2 ? c01 : c012;
-    const uint32_t a0 = w0 == 0 ? m0 : w0 == 1 ? m1 : w0 == 2 ? m2 : m3;
-    const uint32_t a1 = w0 == 0 ? m1 : w0 == 1 ? m2 : w0 == 2 ? m3 : 0u;
-    const uint32_t a2 = w0 == 0 ? m2 : w0 == 1 ? m3 : 0u;
-    const uint32_t a3 = w0 == 0 ? m3 : 0u;
-    const int bit = nth_set_bit(a0, min(max(r - excl, 0), 31));
-    cur = __brev(a0 & (0xFFFFFFFFu << bit));
-    n1 = __brev(a1);
-    n2 = __brev(a2);
-    n3 = __brev(a3);
-    base = 32 * w0;
-  }
-  // Position (0..127) of the next set bit.
-  __device__ __forceinline__ int next() {
-    if (cur == 0u) {
-      cur = n1;
-      n1 = n2;
-      n2 = n3;
-      n3 = 0u;
-      base += 32;
+// Lane L = mask word L of the superblock (block L/4, positions 32(L%4)..+31)
+// writes the block position of each of its kept values at their superblock
+// ordinal. Positions of a corrupt mask (a block without exactly 64 kept
+// values) land at wrong ordinals but never outside the array.
+__device__ __forceinline__ void expand_mask_positions(uint32_t mw, uint8_t* pos, int lane) {
+  const int cnt = __popc(mw);
+  int idx = warp_incl_add(cnt, lane) - cnt;
+  uint32_t pv = 32u * (lane & 3);
+#pragma unroll
+  for (int p = 0; p < 32; ++p) {
+    if ((mw >> p) & 1u) {
+      pos[idx & (CAS_SB * 64 - 1)] = (uint8_t)pv;
+      ++idx;
     }
-    const int p = __clz(cur);
-    cur ^= __funnelshift_rc(0x80000000u, 0u, p);
-    return (base + p) & 127;
+    ++pv;
   }
-};
+}
 
 }  // namespace cas
 
 namespace cas {
 
-// Rebuilds one whole superblock (Cassandra-1, k = 64, m = 3, 8 blocks) as bf16
-// bit patterns: the value at position p of block i goes to dst[i * bstride + p].
-// FULL merges speculation and verification data (lossless); otherwise the
-// draft value is written and pruned positions are zero. Lane L rebuilds kept
-// ordinals 16L..16L+15 (and, FULL, pruned ordinals 16L..16L+15) with the
-// cursors above; the unary streams are staged one after the other in `us`.
-// mask: 32 words, sm / lo: 64 words, pr: 128 words of the superblock (16-byte
-// aligned); sexp / vexp: its code streams. Returns false (warp-uniform) when a
-// stream is longer than the stage or holds fewer than 512 codes: dst is then
-// partly written and the caller rebuilds the superblock with the generic
-// decoder. dst + i * bstride must be 16-byte aligned.
-// Kept values of lane L (ordinals 16L..16L+15): position from the mask
-// cursor, exponent from the unary cursor, sign and mantissa fields from the
+// Kept values of lane L (ordinals 16L..16L+15): positions from the expanded
+// mask, exponent from the unary cursor, sign and mantissa fields from the
 // lane's slices of the speculation (rs) and cut-mantissa (rl) records.
+// Byte i of a 16-byte group of positions.
+__device__ __forceinline__ int pos_byte(uint4 pq, int i) {
+  const uint32_t pw = (i >> 2) == 0 ? pq.x : (i >> 2) == 1 ? pq.y : (i >> 2) == 2 ? pq.z : pq.w;
+  return (pw >> (8 * (i & 3))) & 127u;
+}
+
 template <bool FULL, bool LONG>
-__device__ __forceinline__ void lane_kept_to_row(UnaryCursor& uc, MaskCursor& mc, uint2 rs, uint2 rl,
+__device__ __forceinline__ void lane_kept_to_row(UnaryCursor& uc, uint4 pq, uint2 rs, uint2 rl,
                                                  const uint8_t* __restrict__ lut, uint16_t* row) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const int pos = mc.next();
+    const int pos = pos_byte(pq, i);
     const uint32_t e = lut[uc.next<LONG>() & 255];
     const int sh = 4 * (i & 7);
     const uint32_t f = (i < 8 ? rs.x : rs.y) >> sh;
@@ -175,14 +151,14 @@ __device__ __forceinline__ void lane_kept_to_row(UnaryCursor& uc, MaskCursor& mc
   }
 }
 
-// Pruned values of lane L (pruned ordinals 16L..16L+15) from the inverted
-// mask, the pruned exponent stream and the lane's 16 verification bytes.
+// Pruned values of lane L (pruned ordinals 16L..16L+15) from their positions,
+// the pruned exponent stream and the lane's 16 verification bytes.
 template <bool LONG>
-__device__ __forceinline__ void lane_pruned_to_row(UnaryCursor& uc, MaskCursor& mc, uint4 pb,
+__device__ __forceinline__ void lane_pruned_to_row(UnaryCursor& uc, uint4 pq, uint4 pb,
                                                    const uint8_t* __restrict__ lut, uint16_t* row) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const int pos = mc.next();
+    const int pos = pos_byte(pq, i);
     const uint32_t e = lut[uc.next<LONG>() & 255];
     const uint32_t wsel = (i >> 2) == 0 ? pb.x : (i >> 2) == 1 ? pb.y : (i >> 2) == 2 ? pb.z : pb.w;
     const uint32_t byte = (wsel >> (8 * (i & 3))) & 0xFFu;
@@ -190,14 +166,21 @@ __device__ __forceinline__ void lane_pruned_to_row(UnaryCursor& uc, MaskCursor& 
   }
 }
 
+// Per-warp shared scratch of the tile decoder.
+struct TileStage {
+  UnaryStage us;
+  alignas(16) uint8_t kpos[CAS_SB * 64];  // block position of every kept ordinal
+  alignas(16) uint8_t ppos[CAS_SB * 64];  // block position of every pruned ordinal
+};
+
 // Rebuilds one whole superblock (Cassandra-1, k = 64, m = 3, 8 blocks) as bf16
 // bit patterns: the value at position p of block i goes to dst[i * bstride + p].
 // FULL merges speculation and verification data (lossless); otherwise the
 // draft value is written and pruned positions are zero. Lane L rebuilds kept
 // ordinals 16L..16L+15 (and, FULL, pruned ordinals 16L..16L+15) with the
-// cursors above; the unary streams are staged one after the other in `us`.
-// mask: 32 words, sm / lo: 64 words, pr: 128 words of the superblock (16-byte
-// aligned); sexp / vexp: its code streams. Returns false (warp-uniform) when a
+// unary cursor and the expanded mask; the unary streams are staged one after
+// the other. mask: 32 words, sm / lo: 64 words, pr: 128 words of the
+// superblock (16-byte aligned); sexp / vexp: its code streams. Returns false (warp-uniform) when a
 // stream is longer than the stage or holds fewer than 512 codes: dst is then
 // partly written and the caller rebuilds the superblock with the generic
 // decoder. dst + i * bstride must be 16-byte aligned.
@@ -206,17 +189,16 @@ __device__ __forceinline__ bool lane_sb_tile(const uint32_t* __restrict__ mask, 
                                              const uint32_t* __restrict__ lo, const uint32_t* __restrict__ pr,
                                              const uint32_t* __restrict__ sexp, int snw,
                                              const uint32_t* __restrict__ vexp, int vnw,
-                                             const uint8_t* __restrict__ lut, UnaryStage& us, uint16_t* dst,
+                                             const uint8_t* __restrict__ lut, TileStage& ts, uint16_t* dst,
                                              int bstride, int lane) {
   if (snw > kStageWords || (FULL && vnw > kStageWords)) return false;
-  const int q = lane & 3;
   uint16_t* row = dst + (lane >> 2) * bstride;
-  const uint4 mm = __ldg(reinterpret_cast<const uint4*>(mask) + (lane >> 2));
+  const uint32_t mw = __ldg(mask + lane);
   const uint2 rs = __ldg(reinterpret_cast<const uint2*>(sm) + lane);
   uint2 rl = make_uint2(0u, 0u);
   if (FULL) rl = __ldg(reinterpret_cast<const uint2*>(lo) + lane);
   if (!FULL) {
-    uint4* z = reinterpret_cast<uint4*>(row + 32 * q);
+    uint4* z = reinterpret_cast<uint4*>(row + 32 * (lane & 3));
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
     z[0] = zero;
     z[1] = zero;
@@ -224,29 +206,30 @@ __device__ __forceinline__ bool lane_sb_tile(const uint32_t* __restrict__ mask, 
     z[3] = zero;
   }
   bool long_codes;
-  const bool enough = stage_unary(sexp, snw, us, lane, &long_codes) >= 16 * 32;
+  const bool enough = stage_unary(sexp, snw, ts.us, lane, &long_codes) >= 16 * 32;
+  expand_mask_positions(mw, ts.kpos, lane);
+  if (FULL) expand_mask_positions(~mw, ts.ppos, lane);
   __syncwarp();
   if (!enough) return false;
   UnaryCursor uc;
-  MaskCursor mc;
-  uc.init(us, unary_code_start(us, snw, 16 * lane));
-  mc.init(mm.x, mm.y, mm.z, mm.w, 16 * q);
+  uc.init(ts.us, unary_code_start(ts.us, snw, 16 * lane));
+  const uint4 kq = reinterpret_cast<const uint4*>(ts.kpos)[lane];
   if (long_codes)
-    lane_kept_to_row<FULL, true>(uc, mc, rs, rl, lut, row);
+    lane_kept_to_row<FULL, true>(uc, kq, rs, rl, lut, row);
   else
-    lane_kept_to_row<FULL, false>(uc, mc, rs, rl, lut, row);
+    lane_kept_to_row<FULL, false>(uc, kq, rs, rl, lut, row);
   if (FULL) {
     const uint4 pb = __ldg(reinterpret_cast<const uint4*>(pr) + lane);
     __syncwarp();  // every lane is done with the kept stream
-    const bool enough_v = stage_unary(vexp, vnw, us, lane, &long_codes) >= 16 * 32;
+    const bool enough_v = stage_unary(vexp, vnw, ts.us, lane, &long_codes) >= 16 * 32;
     __syncwarp();
     if (!enough_v) return false;
-    uc.init(us, unary_code_start(us, vnw, 16 * lane));
-    mc.init(~mm.x, ~mm.y, ~mm.z, ~mm.w, 16 * q);
+    uc.init(ts.us, unary_code_start(ts.us, vnw, 16 * lane));
+    const uint4 pq = reinterpret_cast<const uint4*>(ts.ppos)[lane];
     if (long_codes)
-      lane_pruned_to_row<true>(uc, mc, pb, lut, row);
+      lane_pruned_to_row<true>(uc, pq, pb, lut, row);
     else
-      lane_pruned_to_row<false>(uc, mc, pb, lut, row);
+      lane_pruned_to_row<false>(uc, pq, pb, lut, row);
   }
   __syncwarp();
   return true;
