@@ -469,7 +469,10 @@ def run_cas(args):
 # the current kernel on a 28672 x 4096 bench matrix (dram__bytes_read.sum +
 # dram__bytes_write.sum = 62.20 MB for 61.85 MB algorithmic; see
 # profiles/draft_gemv_28672x4096.md). Set to None when the kernel changes.
-PROFILED_TRAFFIC_RATIO = 62.20 / 61.85
+# dram bytes read + written / algorithmic bytes of one draft_gemv_fast_kernel<1>
+# launch on the 28672 x 4096 matrix (ncu, profiles/draft_gemv_28672x4096.md);
+# set to None whenever that kernel changes until it is captured again
+PROFILED_TRAFFIC_RATIO = (61.904896 + 0.104192) / 61.85268
 
 
 def gather_stats(local: tuple, world: int) -> list:
