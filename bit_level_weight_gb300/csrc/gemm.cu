@@ -33,23 +33,29 @@ struct GemmArgs {
   int T;
 };
 
-constexpr int kScratchGeneric = 2048 + kResWords * 4;
-// a multiple of 16 bytes: the tile decoder reads its position arrays as uint4
-constexpr int kScratchWarp =
-    (((int)sizeof(TileStage) > kScratchGeneric ? (int)sizeof(TileStage) : kScratchGeneric) + 15) & ~15;
-static_assert(kScratchWarp % 16 == 0 && alignof(TileStage) <= 16, "per-warp scratch alignment");
+// Per-warp decode scratch: the cursor decoder's stage, or the generic
+// decoder's kept + pruned codes (+ Cassandra-2 residual words); a multiple of
+// 16 bytes (the cursor decoder reads its position arrays as uint4). The warp
+// partials of the product reuse this region after the decode.
+template <int VAR>
+__host__ __device__ constexpr int scratch_warp() {
+  constexpr int generic = 2048 + (VAR == 2 ? kResWords * 4 : 0);
+  return (((int)sizeof(TileStage) > generic ? (int)sizeof(TileStage) : generic) + 15) & ~15;
+}
+static_assert(scratch_warp<1>() % 16 == 0 && alignof(TileStage) <= 16, "per-warp scratch alignment");
+static_assert(kWarps * scratch_warp<1>() >= kWarps * 256 * 4, "warp partials fit in the scratch");
 
 // FAST: Cassandra-1, k = 64, m = 3, whole superblocks (per-lane cursors, lane_sb_tile).
 template <int VAR, int NT, bool FAST>
 __global__ void __launch_bounds__(kThreads) verify_gemm_kernel(GemmArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const WView& w = a.w;
-  uint16_t* tile = reinterpret_cast<uint16_t*>(smem);                       // [16][kTileStride]
-  float* red = reinterpret_cast<float*>(smem + kRows * kTileStride * 2);    // [8][16][16]
-  uint8_t* s_lut = reinterpret_cast<uint8_t*>(red + kWarps * 256);
+  uint16_t* tile = reinterpret_cast<uint16_t*>(smem);  // [16][kTileStride]
+  uint8_t* s_lut = smem + kRows * kTileStride * 2;
   uint8_t* scratch = s_lut + 256;
+  float* red = reinterpret_cast<float*>(scratch);  // [8][16][16], after the decode
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint8_t* wscr = scratch + warp * kScratchWarp;
+  uint8_t* wscr = scratch + warp * scratch_warp<VAR>();
   SbScratch sc{wscr, wscr + 1024, reinterpret_cast<uint32_t*>(wscr + 2048)};
   TileStage& ts = *reinterpret_cast<TileStage*>(wscr);
   for (int i = threadIdx.x; i < 256; i += kThreads) s_lut[i] = a.lut.v[i];
@@ -142,7 +148,7 @@ __global__ void __launch_bounds__(kThreads) verify_gemm_kernel(GemmArgs a) {
 
 template <int VAR, int NT, bool FAST>
 int launch(const GemmArgs& a, cudaStream_t st) {
-  size_t smem = (size_t)kRows * kTileStride * 2 + kWarps * 256 * 4 + 256 + kWarps * kScratchWarp;
+  size_t smem = (size_t)kRows * kTileStride * 2 + 256 + kWarps * scratch_warp<VAR>();
   auto kern = verify_gemm_kernel<VAR, NT, FAST>;
   int per_sm = occupancy((const void*)kern, kThreads, smem);
   if (per_sm < 1) return CAS_ERR_CUDA;
