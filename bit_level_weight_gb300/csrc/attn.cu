@@ -43,15 +43,19 @@ constexpr int kQvPerCta = 32;  // query vectors per CTA (8 per warp)
 // per-warp decode scratch: the cursor decoder's staged stream, or kept codes +
 // pruned codes + the Cassandra-2 residual words of one superblock
 // (a multiple of 16 bytes: the tile decoder reads its position arrays as uint4)
-constexpr int kScratchWarp =
+// Cassandra-1 caches need the stage or 2 x 1024 code bytes, Cassandra-2 caches
+// also the residual words of a superblock.
+constexpr int kScratchC1 = (((int)sizeof(TileStage) > 2048 ? (int)sizeof(TileStage) : 2048) + 15) & ~15;
+constexpr int kScratchC2 =
     (((int)sizeof(TileStage) > 2048 + 4 * kResWords ? (int)sizeof(TileStage) : 2048 + 4 * kResWords) + 15) & ~15;
-static_assert(kScratchWarp % 16 == 0 && alignof(TileStage) <= 16, "per-warp scratch alignment");
+static_assert(kScratchC1 % 16 == 0 && kScratchC2 % 16 == 0 && alignof(TileStage) <= 16, "per-warp scratch alignment");
 
 struct AttnArgs {
   KvDev kv[kMaxBatch];
   const uint16_t* q;  // [B][T][Hq][128]
   float* part;        // [B][T][Hq][nchunk][kPart]
   int B, T, Hq, G, nchunk, ngroups, qv_alloc;
+  int scr_warp;       // per-warp decode scratch bytes (kScratchC1 or kScratchC2)
   float scale;
 };
 
@@ -120,7 +124,7 @@ __global__ void __launch_bounds__(kThreads) attn_chunk_kernel(AttnArgs a) {
   uint8_t* lutV = lutK + 256;
   uint8_t* scr = lutV + 256;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint8_t* wscr = scr + warp * kScratchWarp;
+  uint8_t* wscr = scr + warp * a.scr_warp;
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z / a.ngroups;
   const int qv0 = (blockIdx.z % a.ngroups) * kQvPerCta;
   const KvDev& d = a.kv[b];
@@ -231,7 +235,7 @@ __global__ void __launch_bounds__(kThreads) attn_chunk_kernel(AttnArgs a) {
 // output dimensions; with MT = 1 the 4 warps split them four ways (each
 // warp recomputes the m-tile's S, which is cheap next to the decode).
 template <bool FULL, int MT>
-__global__ void __launch_bounds__(kThreads) attn_mma_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, MT == 2 ? 4 : 5) attn_mma_kernel(AttnArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint16_t* Kt = reinterpret_cast<uint16_t*>(smem);
   uint16_t* Vt = Kt + kStepTok * kRow;
@@ -240,7 +244,7 @@ __global__ void __launch_bounds__(kThreads) attn_mma_kernel(AttnArgs a) {
   uint8_t* lutV = lutK + 256;
   uint8_t* scr = lutV + 256;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint8_t* wscr = scr + warp * kScratchWarp;
+  uint8_t* wscr = scr + warp * a.scr_warp;
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z / a.ngroups;
   const int qv0 = (blockIdx.z % a.ngroups) * kQvPerCta;
   const KvDev& d = a.kv[b];
@@ -484,13 +488,15 @@ __global__ void __launch_bounds__(kCombineWarps * 32) attn_combine_kernel(Combin
   }
 }
 
-size_t chunk_smem(int qv_alloc) {
-  return (size_t)2 * kStepTok * kRow * 2 + (size_t)qv_alloc * CAS_BLK * 4 + 512 + kWarps * kScratchWarp;
+size_t chunk_smem(int qv_alloc, int scr_warp) {
+  return (size_t)2 * kStepTok * kRow * 2 + (size_t)qv_alloc * CAS_BLK * 4 + 512 + (size_t)kWarps * scr_warp;
 }
 
 int nchunks(int64_t max_tokens) { return (int)((max_tokens + kChunk - 1) / kChunk); }
 
-size_t mma_smem(int mt) { return (size_t)2 * kStepTok * kRow * 2 + (size_t)16 * mt * kRow * 2 + 512 + kWarps * kScratchWarp; }
+size_t mma_smem(int mt, int scr_warp) {
+  return (size_t)2 * kStepTok * kRow * 2 + (size_t)16 * mt * kRow * 2 + 512 + (size_t)kWarps * scr_warp;
+}
 
 // Sets a.nchunk to one wave of resident CTAs (at most the workspace's count).
 int one_wave(AttnArgs& a, int Hkv, const void* kern, size_t smem) {
@@ -503,7 +509,7 @@ int one_wave(AttnArgs& a, int Hkv, const void* kern, size_t smem) {
 
 template <bool FULL, int MT>
 int launch_mma(AttnArgs& a, int Hkv, cudaStream_t st) {
-  const size_t smem = mma_smem(MT);
+  const size_t smem = mma_smem(MT, a.scr_warp);
   auto kern = attn_mma_kernel<FULL, MT>;
   const int s = one_wave(a, Hkv, (const void*)kern, smem);
   if (s) return s;
@@ -515,7 +521,7 @@ int launch_mma(AttnArgs& a, int Hkv, cudaStream_t st) {
 // chunks launched (one wave of resident CTAs, at most that many).
 template <bool FULL, int QPW>
 int launch_chunk(AttnArgs& a, int Hkv, cudaStream_t st) {
-  size_t smem = chunk_smem(a.qv_alloc);
+  size_t smem = chunk_smem(a.qv_alloc, a.scr_warp);
   auto kern = attn_chunk_kernel<FULL, QPW>;
   const int s = one_wave(a, Hkv, (const void*)kern, smem);
   if (s) return s;
@@ -542,6 +548,7 @@ int run_attn(bool full, const cas_kv* const* kv, int B, const uint16_t* q, int T
       return CAS_ERR_INVALID;
     Tm = std::max(Tm, kv[i]->max_tokens);
     a.kv[i] = make_kv_dev(kv[i]);
+    a.scr_warp = std::max(a.scr_warp, kv[i]->p.variant == 1 ? kScratchC1 : kScratchC2);
     c.ntok[i] = (const int64_t*)((uint8_t*)kv[i]->base + kv[i]->off[CAS_KV_STATE]);
   }
   if (Hq % Hkv) return CAS_ERR_INVALID;
