@@ -50,18 +50,21 @@ __device__ __forceinline__ int stage_unary(const uint32_t* __restrict__ g, int n
 // Stream bit just after the T-th '1' (T >= 1; total ones >= T), i.e. where
 // code T starts; 0 for T = 0. Branch-free lower bound over the prefixes (the
 // trip count depends only on nw) and a popcount select inside the word.
-__device__ __forceinline__ int unary_code_start(const UnaryStage& s, int nw, int T) {
+__device__ __forceinline__ int unary_code_start(const uint32_t* st, const uint16_t* pc, int nw, int T) {
   int base = 0, n = nw;
   while (n > 1) {
     const int half = n >> 1;
-    base = (int)s.pc[base + half - 1] < T ? base + half : base;
+    base = (int)pc[base + half - 1] < T ? base + half : base;
     n -= half;
   }
   const int wsel = base;  // first word whose inclusive prefix reaches T
-  const int excl = wsel > 0 ? (int)s.pc[wsel - 1] : 0;
+  const int excl = wsel > 0 ? (int)pc[wsel - 1] : 0;
   const int r = T - excl;  // the r-th '1' of word wsel (1-based)
-  const int pos = nth_set_bit(__brev(s.st[wsel]), max(r - 1, 0));
+  const int pos = nth_set_bit(__brev(st[wsel]), max(r - 1, 0));
   return T > 0 ? wsel * 32 + pos + 1 : 0;
+}
+__device__ __forceinline__ int unary_code_start(const UnaryStage& s, int nw, int T) {
+  return unary_code_start(s.st, s.pc, nw, T);
 }
 
 // Cursor over the codes of a staged stream, from bit `start`.
@@ -72,14 +75,16 @@ struct UnaryCursor {
   const uint32_t* end;  // the rare loop reads no further (the 16 plain
                         // refills after it stay inside the stage pad)
 
-  __device__ __forceinline__ void init(const UnaryStage& s, int start) {
+  // st holds cap + kStagePad readable words (cap >= the stream's words).
+  __device__ __forceinline__ void init(const uint32_t* st, int cap, int start) {
     const int hw = start >> 5;
-    end = s.st + kStageWords + 2;
+    end = st + cap + 2;
     sr = start & 31;
-    h = s.st[hw] & (0xFFFFFFFFu >> sr);
-    l = s.st[hw + 1];
-    np = s.st + hw + 2;
+    h = st[hw] & (0xFFFFFFFFu >> sr);
+    l = st[hw + 1];
+    np = st + hw + 2;
   }
+  __device__ __forceinline__ void init(const UnaryStage& s, int start) { init(s.st, kStageWords, start); }
   // Rank of the next code. LONG: the stream has an all-zero word, so a code
   // may need more than one refill. A stream with fewer codes than asked for
   // yields garbage ranks, never a read outside the stage.
