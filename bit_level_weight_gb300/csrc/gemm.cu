@@ -23,7 +23,14 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRows = 16;
-constexpr int kTileStride = CAS_BLK * CAS_SB + 8;  // bf16 per tile row (+8: conflict-free ldmatrix)
+// Tile row: the 8 blocks of a row-superblock, each followed by 8 bf16 of
+// padding (blocks start in different banks, so the decoder's scattered
+// stores spread), then 8 more (rows start 4 banks apart: conflict-free
+// ldmatrix).
+constexpr int kBlkStride = CAS_BLK + 8;
+constexpr int kTileStride = kBlkStride * CAS_SB + 8;
+// tile column of k-step ks (16 columns)
+__device__ __forceinline__ int tile_col(int ks) { return kBlkStride * (ks >> 3) + 16 * (ks & 7); }
 
 struct GemmArgs {
   WView w;
@@ -72,7 +79,7 @@ __global__ void __launch_bounds__(kThreads) verify_gemm_kernel(GemmArgs a) {
     // 1) rebuild rows rt*16 + {warp, warp + 8}
     for (int r = warp; r < kRows; r += kWarps) {
       int64_t n = rt * kRows + r;
-      uint4* dst = reinterpret_cast<uint4*>(tile + r * kTileStride + 32 * lane);
+      uint4* dst = reinterpret_cast<uint4*>(tile + r * kTileStride + kBlkStride * (lane >> 2) + 32 * (lane & 3));
       bool done = false;
       if (n < w.N && FAST) {
         const int64_t s = n * w.nsr + j;
@@ -81,7 +88,7 @@ __global__ void __launch_bounds__(kThreads) verify_gemm_kernel(GemmArgs a) {
         const uint32_t v0 = __ldg(w.vidx + s), v1 = __ldg(w.vidx + s + 1);
         done = lane_sb_tile<true>(w.mask + gb0 * 4, w.ssm + gb0 * 8, w.vlo + gb0 * 8, w.vpr + gb0 * 16,
                                   w.sexp + a0, (int)(a1 - a0), w.vexp + v0, (int)(v1 - v0), s_lut, ts,
-                                  tile + r * kTileStride, CAS_BLK, lane);
+                                  tile + r * kTileStride, kBlkStride, lane);
       }
       if (done) {
       } else if (n < w.N) {
@@ -109,7 +116,7 @@ __global__ void __launch_bounds__(kThreads) verify_gemm_kernel(GemmArgs a) {
     const int ksteps = nb * (CAS_BLK / 16);
     for (int ks = warp; ks < ksteps; ks += kWarps) {
       uint32_t af[4];
-      ldmatrix_x4(af, tile + (lane & 15) * kTileStride + ks * 16 + (lane >> 4) * 8);
+      ldmatrix_x4(af, tile + (lane & 15) * kTileStride + tile_col(ks) + (lane >> 4) * 8);
       int col = CAS_BLK * CAS_SB * j + ks * 16 + 2 * tq;
 #pragma unroll
       for (int q = 0; q < NT; ++q) {

@@ -128,6 +128,27 @@ __device__ __forceinline__ void expand_mask_positions(uint32_t mw, uint8_t* pos,
   }
 }
 
+// Same for both the kept (set) and the pruned (clear) bits of the word in one
+// pass: kpos gets the kept positions by kept ordinal, ppos the pruned ones by
+// pruned ordinal.
+__device__ __forceinline__ void expand_mask_both(uint32_t mw, uint8_t* kpos, uint8_t* ppos, int lane) {
+  const int cnt = __popc(mw);
+  const int kbefore = warp_incl_add(cnt, lane) - cnt;
+  int ki = kbefore, pi = 32 * lane - kbefore;
+  uint32_t pv = 32u * (lane & 3);
+#pragma unroll
+  for (int p = 0; p < 32; ++p) {
+    if ((mw >> p) & 1u) {
+      kpos[ki & (CAS_SB * 64 - 1)] = (uint8_t)pv;
+      ++ki;
+    } else {
+      ppos[pi & (CAS_SB * 64 - 1)] = (uint8_t)pv;
+      ++pi;
+    }
+    ++pv;
+  }
+}
+
 }  // namespace cas
 
 namespace cas {
@@ -212,8 +233,10 @@ __device__ __forceinline__ bool lane_sb_tile(const uint32_t* __restrict__ mask, 
   }
   bool long_codes;
   const bool enough = stage_unary(sexp, snw, ts.us, lane, &long_codes) >= 16 * 32;
-  expand_mask_positions(mw, ts.kpos, lane);
-  if (FULL) expand_mask_positions(~mw, ts.ppos, lane);
+  if (FULL)
+    expand_mask_both(mw, ts.kpos, ts.ppos, lane);
+  else
+    expand_mask_positions(mw, ts.kpos, lane);
   __syncwarp();
   if (!enough) return false;
   UnaryCursor uc;

@@ -109,6 +109,19 @@ def test_draft_gemv_long_codes(cas, orc, variant, nvec):
     check_close(y, ref, norm, "draft_gemv long codes")
 
 
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("T", [5, 14])
+def test_verify_gemm_long_codes(cas, orc, variant, T):
+    N, K = 48, 2048
+    W = wide_exponent_rows(N, K, 8, seed=6)
+    X = synthetic.activations(T, K, seed=18)
+    enc = cas.encode_weights(W.cuda(), variant, 64, 3)
+    Y = cas.verify_gemm(enc, X.cuda())
+    ref, norm = orc.matvec(np16(W), np16(X))
+    check_close(Y, ref, norm, "verify_gemm long codes")
+    assert np.array_equal(np16(cas.reconstruct(enc)), np16(W))
+
+
 @pytest.mark.parametrize("N,K,variant,k,m", CASES)
 @pytest.mark.parametrize("T", [1, 5, 8, 9, 14, 16])
 def test_verify_gemm(cas, orc, N, K, variant, k, m, T):
