@@ -526,7 +526,7 @@ def e2e_draft_pass(cas, stk, xs, ys, nvec, st, steps):
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
     return {"value": round(spec / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "what": "one draft GEMV pass over all 32 layers' matrices via "
+            "d2h_bytes_per_step": d2h, "what": f"one draft GEMV pass over all {stk.L} layers' matrices via "
             "cas_draft_gemv, x copied in from pinned host memory and all outputs copied out, per step"}
 
 
