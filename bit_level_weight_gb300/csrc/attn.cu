@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kThreads) attn_chunk_kernel(AttnArgs a) {
 // output dimensions; with MT = 1 the 4 warps split them four ways (each
 // warp recomputes the m-tile's S, which is cheap next to the decode).
 template <bool FULL, int MT>
-__global__ void __launch_bounds__(kThreads, MT == 2 ? 4 : 5) attn_mma_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, MT == 2 ? 5 : 6) attn_mma_kernel(AttnArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint16_t* Kt = reinterpret_cast<uint16_t*>(smem);
   uint16_t* Vt = Kt + kStepTok * kRow;
