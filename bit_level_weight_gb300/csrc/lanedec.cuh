@@ -153,14 +153,15 @@ __device__ __forceinline__ void expand_mask_both(uint32_t mw, uint8_t* kpos, uin
 
 namespace cas {
 
-// Kept values of lane L (ordinals 16L..16L+15): positions from the expanded
-// mask, exponent from the unary cursor, sign and mantissa fields from the
-// lane's slices of the speculation (rs) and cut-mantissa (rl) records.
 // Byte i of a 16-byte group of positions.
 __device__ __forceinline__ int pos_byte(uint4 pq, int i) {
   const uint32_t pw = (i >> 2) == 0 ? pq.x : (i >> 2) == 1 ? pq.y : (i >> 2) == 2 ? pq.z : pq.w;
   return (pw >> (8 * (i & 3))) & 127u;
 }
+
+// Kept values of lane L (ordinals 16L..16L+15): positions from the expanded
+// mask, exponent from the unary cursor, sign and mantissa fields from the
+// lane's slices of the speculation (rs) and cut-mantissa (rl) records.
 
 template <bool FULL, bool LONG>
 __device__ __forceinline__ void lane_kept_to_row(UnaryCursor& uc, uint4 pq, uint2 rs, uint2 rl,
