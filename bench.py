@@ -453,6 +453,7 @@ def run_cas(args):
                      "traffic_note": "per launch: (ncu dram bytes / algorithmic bytes of a 28672x4096 launch, "
                                      "profiles/draft_gemv_28672x4096.md) x algorithmic bytes per launch of this step",
                      "algorithmic_bytes_per_launch": int(per_launch_bytes)},
+        "alu_roof": alu_roof(achieved, clk) if args.keep == 64 and args.mant == 3 and B == 1 else None,
         "e2e": e2e,
         "gpu_launches": launches_per_step * steps,
         "encode_s": round(stk.encode_s, 2),
@@ -473,6 +474,33 @@ def run_cas(args):
 # launch on the 28672 x 4096 matrix (ncu, profiles/draft_gemv_28672x4096.md);
 # set to None whenever that kernel changes until it is captured again
 PROFILED_TRAFFIC_RATIO = (61.904896 + 0.104192) / 61.85268
+
+
+# warp instructions x 32 / elements of one draft_gemv_fast_kernel<1> launch on
+# the 28672 x 4096 matrix (ncu smsp__inst_executed.sum,
+# profiles/draft_gemv_28672x4096.md); None whenever that kernel changes
+PROFILED_LANE_INSTR_PER_ELEM = 109543024 * 32 / (28672 * 4096)
+SMS, LANES_PER_SM_CLK = 152, 128  # 4 schedulers x 32 lanes issue per SM clock
+
+
+def alu_roof(achieved_gbs: float, clk) -> dict:
+    """The draft GEMV is bound by instruction issue (integer decode), so its
+    second roof is the lane-instruction issue peak: SMs x 128 x SM clock.
+    achieved = profiled lane instructions per element x elements per second."""
+    if PROFILED_LANE_INSTR_PER_ELEM is None:
+        return None
+    mhz = (clk.summary() or {}).get("sm_mhz") or 2070.0
+    peak = SMS * LANES_PER_SM_CLK * mhz * 1e6
+    bytes_per_elem = 4.205 / 8  # speculation bits per element of the Student-t matrices (k = 64, m = 3)
+    elems = achieved_gbs * 1e9 / bytes_per_elem
+    achieved = PROFILED_LANE_INSTR_PER_ELEM * elems
+    budget = peak / (0.75 * peaks()[0] * 1e9 / bytes_per_elem)
+    return {"bound": "alu", "achieved": round(achieved / 1e12, 2), "peak": round(peak / 1e12, 2),
+            "unit": "T lane-instr/s", "frac": round(achieved / peak, 4),
+            "lane_instr_per_elem": round(PROFILED_LANE_INSTR_PER_ELEM, 2),
+            "budget_at_75pct_hbm": round(budget, 2),
+            "note": "lane instructions per element from ncu (profiles/draft_gemv_28672x4096.md); "
+                    "peak = 152 SMs x 128 lanes x median SM clock"}
 
 
 def gather_stats(local: tuple, world: int) -> list:
