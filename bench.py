@@ -705,6 +705,7 @@ def run_sweep(args):
         for keep in (0.2, 0.3, 0.4, 0.5, 0.6):
             k = cas.cas_keep_from_ratio(keep)
             for m in range(1, 6):
+                chosen, _ = cas.cas_choose_variant(W, k, m)  # per-tensor choice: fewer speculation bytes
                 for variant in (1, 2):
                     enc = cas.encode_weights(W, variant, k, m)
                     call = cas.prepare("cas_draft_gemv", enc, x, 1, y, st)
@@ -721,7 +722,8 @@ def run_sweep(args):
                     nbytes = enc.spec_bytes() + K * 2 + N * 4
                     cr = 1.0 - enc.spec_bytes() / (2.0 * N * K)
                     print(json.dumps({"sweep": "cassandra-1 vs -2", "N": N, "K": K, "keep": keep, "k": k, "m": m,
-                                      "variant": variant, "cr": round(cr, 4), "in_40_80": 0.4 <= cr <= 0.8,
+                                      "variant": variant, "chosen": variant == chosen,
+                                      "cr": round(cr, 4), "in_40_80": 0.4 <= cr <= 0.8,
                                       "spec_bits_per_elem": round(enc.spec_bytes() * 8 / (N * K), 3),
                                       "all_bits_per_elem": round(enc.all_bytes() * 8 / (N * K), 3),
                                       "draft_gemv_us": round(ms * 1e3, 1),

@@ -76,6 +76,7 @@ def lib() -> ctypes.CDLL:
             "cas_encode_workspace_bytes": ([i64, i64], u64),
             "cas_encode_weights_plan": ([P, i64, i64, cas_params, P, P, P, u64, P], i32),
             "cas_encode_weights": ([P, P, P, u64, P, u64, P], i32),
+            "cas_choose_variant": ([P, i64, i64, i32, i32, P, u64, P, P, P], i32),
             "cas_draft_gemv": ([P, P, i32, P, P], i32),
             "cas_verify_gemm": ([P, P, i32, P, P], i32),
             "cas_decode_draft": ([P, P, P], i32),
@@ -196,6 +197,18 @@ def cas_encode_weights(W: torch.Tensor, desc: cas_weights, buf: torch.Tensor, wo
     _check(lib().cas_encode_weights(_ptr(W), ctypes.byref(desc), _ptr(buf), buf.numel() * buf.element_size(),
                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
                                     _stream(stream)), "cas_encode_weights")
+
+
+def cas_choose_variant(W: torch.Tensor, keep_per_block: int = 64, mant_bits: int = 3, stream=None):
+    """(variant, (cassandra1_spec_bytes, cassandra2_spec_bytes)) for W [N][K]."""
+    W = _bits(W).contiguous()
+    N, K = W.shape
+    ws = torch.empty(max(cas_encode_workspace_bytes(N, K), 256), dtype=torch.uint8, device=W.device)
+    v = ctypes.c_int(0)
+    sb = (ctypes.c_uint64 * 2)()
+    _check(lib().cas_choose_variant(_ptr(W), N, K, keep_per_block, mant_bits, _ptr(ws), ws.numel(),
+                                    ctypes.byref(v), sb, _stream(stream)), "cas_choose_variant")
+    return int(v.value), (int(sb[0]), int(sb[1]))
 
 
 def encode_weights(W: torch.Tensor, variant: int = 1, keep_per_block: int = 64, mant_bits: int = 3,

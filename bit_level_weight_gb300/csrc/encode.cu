@@ -383,3 +383,26 @@ extern "C" int cas_encode_weights(const uint16_t* W, cas_weights* d, void* buf, 
     write_kernel<2><<<g, kThreads, 0, st>>>(a);
   return launch_status();
 }
+
+extern "C" int cas_choose_variant(const uint16_t* W, int64_t N, int64_t K, int keep_per_block, int mant_bits,
+                                  void* workspace, uint64_t workspace_bytes, int* variant, uint64_t* spec_bytes,
+                                  void* stream) {
+  if (!variant) return CAS_ERR_INVALID;
+  uint64_t sb[2] = {0, 0};
+  for (int v = 1; v <= 2; ++v) {
+    cas_weights d;
+    uint64_t need = 0;
+    const cas_params p{v, keep_per_block, mant_bits};
+    const int s = cas_encode_weights_plan(W, N, K, p, &d, &need, workspace, workspace_bytes, stream);
+    if (s) return s;
+    for (int sec : {CAS_SEC_MASK, CAS_SEC_SPEC_SM, CAS_SEC_SPEC_EXP, CAS_SEC_SPEC_SBIDX, CAS_SEC_SPEC_MX,
+                    CAS_SEC_SPEC_Q})
+      sb[v - 1] += d.len[sec];
+  }
+  *variant = sb[1] < sb[0] ? 2 : 1;
+  if (spec_bytes) {
+    spec_bytes[0] = sb[0];
+    spec_bytes[1] = sb[1];
+  }
+  return CAS_OK;
+}

@@ -131,6 +131,18 @@ int cas_encode_weights_plan(const uint16_t* W, int64_t N, int64_t K, cas_params 
 int cas_encode_weights(const uint16_t* W, cas_weights* desc, void* buf, uint64_t buf_bytes,
                        void* workspace, uint64_t workspace_bytes, void* stream);
 
+/* Per-tensor choice between Cassandra-1 and Cassandra-2 [B3.2]: plans W under
+ * both variants with the same k and m (as cas_encode_weights_plan, which it
+ * calls twice; synchronises `stream`) and sets *variant to the one whose
+ * speculation sections (mask, records, exponent codes or shared exponents,
+ * index) are smaller; ties go to Cassandra-1, whose draft keeps every kept
+ * value's own exponent. spec_bytes (NULL or 2 entries) receives both sizes,
+ * Cassandra-1 first. Errors: those of cas_encode_weights_plan;
+ * CAS_ERR_INVALID if variant is NULL. */
+int cas_choose_variant(const uint16_t* W, int64_t N, int64_t K, int keep_per_block, int mant_bits,
+                       void* workspace, uint64_t workspace_bytes, int* variant, uint64_t* spec_bytes,
+                       void* stream);
+
 /* Draft GEMV [B3.1]: y[v][n] = sum_k D(W)[n][k] * x[v][k] for v < nvec (1..4),
  * where D(W) is the zero-filled speculation value (pruned -> 0, kept ->
  * mantissa truncated, Cassandra-2 -> shared-exponent grid). Reads only the

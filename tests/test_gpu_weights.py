@@ -82,6 +82,16 @@ def test_draft_gemv(cas, orc, N, K, variant, k, m, nvec):
     check_close(y, ref, norm, "draft_gemv")
 
 
+@pytest.mark.parametrize("k,m", [(64, 3), (26, 1), (102, 5), (38, 3)])
+def test_choose_variant_matches_oracle_sizes(cas, orc, k, m):
+    W = synthetic.normal_weight(48, 2048, seed=k + m, outlier_frac=0.001)
+    v, (b1, b2) = cas.cas_choose_variant(W.cuda(), k, m)
+    r1 = orc.encode(np16(W), 1, k, m).spec_bytes()
+    r2 = orc.encode(np16(W), 2, k, m).spec_bytes()
+    assert (b1, b2) == (r1, r2)
+    assert v == (2 if r2 < r1 else 1)
+
+
 def wide_exponent_rows(N, K, n_wide, seed):
     """Normal rows, then n_wide rows whose exponents spread over ~200 values:
     their unary codes are long (tens to hundreds of bits) and their
