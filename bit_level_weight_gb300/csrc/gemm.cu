@@ -54,7 +54,7 @@ static_assert(kWarps * scratch_warp<1>() >= kWarps * 256 * 4, "warp partials fit
 
 // FAST: Cassandra-1, k = 64, m = 3, whole superblocks (per-lane cursors, lane_sb_tile).
 template <int VAR, int NT, bool FAST>
-__global__ void __launch_bounds__(kThreads) verify_gemm_kernel(GemmArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) verify_gemm_kernel(GemmArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const WView& w = a.w;
   uint16_t* tile = reinterpret_cast<uint16_t*>(smem);  // [16][kTileStride]
@@ -107,26 +107,39 @@ __global__ void __launch_bounds__(kThreads) verify_gemm_kernel(GemmArgs a) {
         dst[0] = z; dst[1] = z; dst[2] = z; dst[3] = z;
       }
     }
+    // 2) tensor-core product of the tile with X[:, tile columns]. This warp's X
+    // fragments (k-steps warp, warp + 8, ...) are loaded before the barrier so
+    // their latency overlaps the other warps' decode.
+    const int g = lane >> 2, tq = lane & 3;
+    const int ksteps = nb * (CAS_BLK / 16);
+    constexpr int kKsPerWarp = CAS_BLK * CAS_SB / 16 / kWarps;
+    uint32_t xb[kKsPerWarp][NT][2];
+#pragma unroll
+    for (int i = 0; i < kKsPerWarp; ++i) {
+      const int ks = warp + kWarps * i;
+      const int col = CAS_BLK * CAS_SB * j + ks * 16 + 2 * tq;
+#pragma unroll
+      for (int q = 0; q < NT; ++q) {
+        const int tok = q * 8 + g;
+        xb[i][q][0] = xb[i][q][1] = 0u;
+        if (ks < ksteps && tok < T) {
+          xb[i][q][0] = __ldg(X32 + ((int64_t)tok * K + col) / 2);
+          xb[i][q][1] = __ldg(X32 + ((int64_t)tok * K + col + 8) / 2);
+        }
+      }
+    }
     __syncthreads();
-    // 2) tensor-core product of the tile with X[:, tile columns]
     float c[NT][4];
 #pragma unroll
     for (int q = 0; q < NT; ++q) c[q][0] = c[q][1] = c[q][2] = c[q][3] = 0.f;
-    const int g = lane >> 2, tq = lane & 3;
-    const int ksteps = nb * (CAS_BLK / 16);
-    for (int ks = warp; ks < ksteps; ks += kWarps) {
-      uint32_t af[4];
-      ldmatrix_x4(af, tile + (lane & 15) * kTileStride + tile_col(ks) + (lane >> 4) * 8);
-      int col = CAS_BLK * CAS_SB * j + ks * 16 + 2 * tq;
 #pragma unroll
-      for (int q = 0; q < NT; ++q) {
-        int tok = q * 8 + g;
-        uint32_t b0 = 0, b1 = 0;
-        if (tok < T) {
-          b0 = __ldg(X32 + ((int64_t)tok * K + col) / 2);
-          b1 = __ldg(X32 + ((int64_t)tok * K + col + 8) / 2);
-        }
-        mma_bf16(c[q], af, b0, b1);
+    for (int i = 0; i < kKsPerWarp; ++i) {
+      const int ks = warp + kWarps * i;
+      if (ks < ksteps) {
+        uint32_t af[4];
+        ldmatrix_x4(af, tile + (lane & 15) * kTileStride + tile_col(ks) + (lane >> 4) * 8);
+#pragma unroll
+        for (int q = 0; q < NT; ++q) mma_bf16(c[q], af, xb[i][q][0], xb[i][q][1]);
       }
     }
     // 3) reduce warp partials: red[warp][row][token]
