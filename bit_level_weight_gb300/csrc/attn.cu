@@ -403,6 +403,164 @@ __global__ void __launch_bounds__(kThreads, MT == 2 ? 5 : 6) attn_mma_kernel(Att
   }
 }
 
+// ---------------------------------------------------------------- fused draft
+// Draft attention with at most 4 query vectors per kv head (T = 1, GQA up to
+// 4:1). The K side needs no tile: lane L decodes its 16 kept K values of
+// token L/4 (per-lane cursors, as for the tiles) and multiplies each with the
+// 4 query vectors at its position (q4: dims x 4, pre-scaled, one 16-byte load
+// per value); the 4 lanes of a token add their partial scores.
+
+template <bool LONG>
+__device__ __forceinline__ float4 lane_kept_qdot(UnaryCursor& uc, uint4 kq, uint2 rs, const uint8_t* __restrict__ lut,
+                                                 const float4* q4) {
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int pos = pos_byte(kq, i);
+    const uint32_t e = lut[uc.next<LONG>() & 255];
+    const uint32_t f = (i < 8 ? rs.x : rs.y) >> (4 * (i & 7));
+    const float val = __uint_as_float(((f & 8u) << 28) | (e << 23) | ((f & 7u) << 20));
+    const float4 q = q4[pos];
+    acc.x = fmaf(val, q.x, acc.x);
+    acc.y = fmaf(val, q.y, acc.y);
+    acc.z = fmaf(val, q.z, acc.z);
+    acc.w = fmaf(val, q.w, acc.w);
+  }
+  return acc;
+}
+
+// Scores of the 8 tokens of superblock sb of K stream st against the 4 query
+// vectors into out[8][4] (float4 per token). Only for whole Cassandra-1
+// superblocks with k = 64, m = 3 and a stream that fits the stage; returns
+// false otherwise (nothing written, warp-uniform).
+__device__ __forceinline__ bool lane_sb_scores(const KvDev& d, int st, int64_t n, int64_t sb, const uint8_t* lut,
+                                               uint8_t* scratch, const float4* q4, float4* out, int lane) {
+  const int64_t nsb = (n + CAS_SB - 1) / CAS_SB;
+  if (!(sb < nsb && d.variant == 1 && d.k == 64 && d.m == 3 && CAS_SB * (sb + 1) <= n)) return false;
+  const uint32_t* sidx = (const uint32_t*)kv_sec(d, CAS_KV_SPEC_SBIDX, st);
+  const uint32_t a0 = sidx[sb], a1 = sidx[sb + 1];
+  const int snw = (int)(a1 - a0);
+  if (snw > kStageWords) return false;
+  TileStage& ts = *reinterpret_cast<TileStage*>(scratch);
+  const uint32_t mw = __ldg((const uint32_t*)kv_sec(d, CAS_KV_MASK, st) + sb * 32 + lane);
+  const uint2 rs = __ldg(reinterpret_cast<const uint2*>((const uint32_t*)kv_sec(d, CAS_KV_SPEC_SM, st) + sb * 64) + lane);
+  bool long_codes;
+  const bool enough =
+      stage_unary((const uint32_t*)kv_sec(d, CAS_KV_SPEC_EXP, st) + a0, snw, ts.us, lane, &long_codes) >= 16 * 32;
+  expand_mask_positions(mw, ts.kpos, lane);
+  __syncwarp();
+  if (!enough) return false;
+  UnaryCursor uc;
+  uc.init(ts.us, unary_code_start(ts.us, snw, 16 * lane));
+  const uint4 kq = reinterpret_cast<const uint4*>(ts.kpos)[lane];
+  float4 acc = long_codes ? lane_kept_qdot<true>(uc, kq, rs, lut, q4) : lane_kept_qdot<false>(uc, kq, rs, lut, q4);
+#pragma unroll
+  for (int x = 1; x <= 2; x <<= 1) {
+    acc.x += __shfl_xor_sync(CAS_FULL, acc.x, x);
+    acc.y += __shfl_xor_sync(CAS_FULL, acc.y, x);
+    acc.z += __shfl_xor_sync(CAS_FULL, acc.z, x);
+    acc.w += __shfl_xor_sync(CAS_FULL, acc.w, x);
+  }
+  if ((lane & 3) == 0) out[lane >> 2] = acc;
+  __syncwarp();
+  return true;
+}
+
+// Per 32-token step warp w scores its K superblock (tokens 8w..8w+7 of the
+// step) into sc, decodes its V superblock into the V tile, and after the
+// barrier runs query vector w over the 32 tokens (online softmax, P.V with
+// lane = 4 dims) exactly as the chunk kernel. Superblocks the cursors do not
+// cover (partial, Cassandra-2, other k or m, long streams) are decoded into a
+// K tile and scored from it.
+__global__ void __launch_bounds__(kThreads) attn_draft_fused_kernel(AttnArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint16_t* Kt = reinterpret_cast<uint16_t*>(smem);  // fallback K tile
+  uint16_t* Vt = Kt + kStepTok * kRow;
+  float4* q4 = reinterpret_cast<float4*>(Vt + kStepTok * kRow);  // [128] dims x 4 query vectors
+  float4* sc = q4 + CAS_BLK;                                      // [32] tokens x 4 query vectors
+  uint8_t* lutK = reinterpret_cast<uint8_t*>(sc + kStepTok);
+  uint8_t* lutV = lutK + 256;
+  uint8_t* scr = lutV + 256;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint8_t* wscr = scr + warp * a.scr_warp;
+  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const KvDev& d = a.kv[b];
+  const int H = d.H, G = a.G, nq = min(a.T * G, 4);
+  const int64_t n = *(volatile const int64_t*)&kv_state(d)->n_tokens;
+  const int64_t steps = (n + kStepTok - 1) / kStepTok;
+  const int64_t t_begin = steps * chunk / a.nchunk * kStepTok;
+  const int64_t t_end = min(n, steps * (chunk + 1) / a.nchunk * kStepTok);
+
+  // q4[dd] = the 4 query vectors (q heads h*G .. h*G+3 of token 0) at dimension dd, scaled
+  for (int i = threadIdx.x; i < 4 * CAS_BLK; i += kThreads) {
+    const int r = i & 3, dd = i >> 2;
+    float v = 0.f;
+    if (r < nq) v = bf2f(a.q[((int64_t)b * a.Hq + h * G + r) * CAS_BLK + dd]) * a.scale;
+    reinterpret_cast<float*>(q4)[i] = v;
+  }
+  for (int i = threadIdx.x; i < 256; i += kThreads) {
+    lutK[i] = kv_exp_of_rank(d, h)[i];
+    lutV[i] = kv_exp_of_rank(d, H + h)[i];
+  }
+  __syncthreads();
+
+  const int qv = warp;  // query vector run by this warp (if < nq)
+  float m = -INFINITY, l = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+  for (int64_t t0 = t_begin; t0 < t_end; t0 += kStepTok) {
+    const int64_t sb = t0 / CAS_SB + warp;
+    if (!lane_sb_scores(d, h, n, sb, lutK, wscr, q4, sc + warp * CAS_SB, lane)) {
+      decode_sb_tile<false>(d, h, n, sb, Kt, warp * CAS_SB, lutK, wscr, lane);
+      // lane = (token lane / 4 of this superblock, query vector lane % 4)
+      const uint32_t* kr = reinterpret_cast<const uint32_t*>(Kt + (warp * CAS_SB + (lane >> 2)) * kRow);
+      const float* qf = reinterpret_cast<const float*>(q4) + (lane & 3);
+      float acc = 0.f;
+      for (int dd = 0; dd < CAS_BLK; dd += 2) {
+        const uint32_t k2 = kr[dd >> 1];
+        acc = fmaf(bf2f(k2 & 0xFFFFu), qf[4 * dd], acc);
+        acc = fmaf(bf2f(k2 >> 16), qf[4 * dd + 4], acc);
+      }
+      reinterpret_cast<float*>(sc + warp * CAS_SB + (lane >> 2))[lane & 3] = acc;
+      __syncwarp();
+    }
+    decode_sb_tile<false>(d, H + h, n, sb, Vt, warp * CAS_SB, lutV, wscr, lane);
+    __syncthreads();
+    if (qv < nq) {
+      const int64_t tok = t0 + lane;
+      const float si = tok < t_end ? reinterpret_cast<const float*>(sc + lane)[qv] : -INFINITY;
+      const float mx = warp_maxf(si);
+      const float mnew = fmaxf(m, mx);
+      const float p = (si == -INFINITY) ? 0.f : __expf(si - mnew);
+      float corr = (m == -INFINITY) ? 0.f : __expf(m - mnew);
+      if (mnew == -INFINITY) corr = 1.f;
+      l = l * corr + warp_sumf(p);
+      m = mnew;
+      float acc0 = o0 * corr, acc1 = o1 * corr, acc2 = o2 * corr, acc3 = o3 * corr;
+      for (int t = 0; t < kStepTok; ++t) {
+        const float pt = __shfl_sync(CAS_FULL, p, t);
+        const uint2 v4 = reinterpret_cast<const uint2*>(Vt + t * kRow)[lane];
+        acc0 = fmaf(pt, __uint_as_float(v4.x << 16), acc0);
+        acc1 = fmaf(pt, __uint_as_float(v4.x & 0xFFFF0000u), acc1);
+        acc2 = fmaf(pt, __uint_as_float(v4.y << 16), acc2);
+        acc3 = fmaf(pt, __uint_as_float(v4.y & 0xFFFF0000u), acc3);
+      }
+      o0 = acc0;
+      o1 = acc1;
+      o2 = acc2;
+      o3 = acc3;
+    }
+    __syncthreads();
+  }
+  if (qv < nq) {
+    float* dst = a.part + (((int64_t)b * a.Hq + h * G + qv) * a.nchunk + chunk) * kPart;
+    reinterpret_cast<float2*>(dst)[2 * lane] = make_float2(o0, o1);
+    reinterpret_cast<float2*>(dst)[2 * lane + 1] = make_float2(o2, o3);
+    if (lane == 0) {
+      dst[CAS_BLK] = m;
+      dst[CAS_BLK + 1] = l;
+    }
+  }
+}
+
 constexpr int kCombineWarps = 32;  // warps of a combine CTA (each merges every 32nd chunk)
 
 struct CombineArgs {
@@ -507,6 +665,15 @@ int one_wave(AttnArgs& a, int Hkv, const void* kern, size_t smem) {
   return CAS_OK;
 }
 
+int launch_fused(AttnArgs& a, int Hkv, cudaStream_t st) {
+  const size_t smem = (size_t)2 * kStepTok * kRow * 2 + (size_t)CAS_BLK * 16 + (size_t)kStepTok * 16 + 512 +
+                      (size_t)kWarps * a.scr_warp;
+  const int s = one_wave(a, Hkv, (const void*)attn_draft_fused_kernel, smem);
+  if (s) return s;
+  attn_draft_fused_kernel<<<dim3(a.nchunk, Hkv, a.B), kThreads, smem, st>>>(a);
+  return launch_status();
+}
+
 template <bool FULL, int MT>
 int launch_mma(AttnArgs& a, int Hkv, cudaStream_t st) {
   const size_t smem = mma_smem(MT, a.scr_warp);
@@ -568,7 +735,9 @@ int run_attn(bool full, const cas_kv* const* kv, int B, const uint16_t* q, int T
   a.qv_alloc = std::min(T * G, kQvPerCta);
   int qpw = (std::min(T * G, kQvPerCta) + kWarps - 1) / kWarps;
   int s;
-  if (!full) {
+  if (!full && T == 1 && a.qv_alloc <= 4) {
+    s = launch_fused(a, Hkv, st);
+  } else if (!full) {
     if (qpw <= 1) s = launch_chunk<false, 1>(a, Hkv, st);
     else if (qpw <= 4) s = launch_chunk<false, 4>(a, Hkv, st);
     else s = launch_chunk<false, 8>(a, Hkv, st);
