@@ -228,6 +228,25 @@ def test_draft_attention(cas, orc, lens, n_tail, variant, k, m):
         check_attn(o[b:b + 1], ref, nrm, f"draft attention b={b}")
 
 
+@pytest.mark.parametrize("Hq", [8, 16, 64])
+def test_draft_attention_gqa_ratios(cas, orc, Hq):
+    """1, 2 and 8 query heads per kv head (the fused kernel takes up to 4 query
+    vectors per kv head, the chunk kernel more)."""
+    H, T = 8, 600
+    K, V = make_tokens(T, H, layer=2, seed=71)
+    kv = new_cache(cas, H, 700, K, V)
+    kv.append(K.cuda(), V.cuda())
+    assert kv.status() == (T, 0)
+    q = synthetic.activations(1, Hq * D, seed=72).view(1, Hq, D)
+    tk = synthetic.activations(2, H * D, seed=73).view(1, 2, H, D)
+    tv = synthetic.activations(2, H * D, seed=74).view(1, 2, H, D)
+    o = cas.draft_attn_decode([kv], q.cuda(), tk.contiguous().cuda(), tv.contiguous().cuda())
+    Kall = np.concatenate([oracle_draft_kv(orc, K, 64, 3), np16(tk[0])], 0)
+    Vall = np.concatenate([oracle_draft_kv(orc, V, 64, 3), np16(tv[0])], 0)
+    ref, nrm = orc.attention(np16(q), Kall, Vall)
+    check_attn(o, ref, nrm, f"draft attention Hq={Hq}")
+
+
 @pytest.mark.parametrize("lens,T,variant", [((300,), 5, 1), ((5,), 5, 1), ((517, 40), 7, 1), ((1024,), 14, 1),
                                             ((260,), 16, 1), ((9,), 1, 1), ((517, 40), 7, 2), ((1024,), 14, 2),
                                             ((9,), 1, 2)])
