@@ -366,6 +366,154 @@ __global__ void __launch_bounds__(kThreads, NV <= 2 ? 5 : 4) draft_gemv_fast_ker
   }
 }
 
+// ------------------------------------------------------------------ any k, m
+// Rows made of whole superblocks, any k and m, both variants. Lane L takes
+// the run of kept ordinals [L q, L q + q) of the superblock (q = ceil(8k/32),
+// runs may cross blocks). The warp stages the superblock's records (and, for
+// Cassandra-1, its unary stream; for Cassandra-2, its shared exponents) in
+// shared memory and expands the mask into the block position of every kept
+// ordinal; each lane then walks its run: block position, record field at a
+// run-time bit offset, exponent (unary cursor, or the group's shared exponent
+// for Cassandra-2), times x. Superblocks whose unary stream exceeds the stage
+// take the generic decoder.
+struct RunsWarp {
+  UnaryStage us;                               // Cassandra-1 codes
+  uint32_t rec[CAS_SB * 36 + 2];               // records of the 8 blocks (<= 36 words each) + pad
+  alignas(16) uint8_t pos[CAS_SB * CAS_BLK];   // block position of every kept ordinal
+  uint8_t mx[CAS_SB * 4];                      // Cassandra-2 shared exponents
+};
+union RunsScratch {
+  RunsWarp r;
+  uint8_t code[CAS_SB * CAS_BLK];  // generic decoder: exponents by kept ordinal
+};
+
+template <int VAR, int NV, bool LONG>
+__device__ __forceinline__ void run_dot(const RunsWarp& rw, UnaryCursor& uc, const uint8_t* lut8, int k, int m,
+                                        int rec, int t0, int t1, const uint16_t* xsb, int K, float acc[NV]) {
+  const int width = VAR == 1 ? m + 1 : m + 2;
+  const uint32_t fmask = (1u << width) - 1u;
+  int b = k > 0 ? t0 / k : 0;
+  int tl = t0 - b * k;
+  for (int t = t0; t < t1; ++t) {
+    if (tl == k) {
+      ++b;
+      tl = 0;
+    }
+    const int p = rw.pos[t];
+    const uint32_t fld = get_field(rw.rec + b * rec, tl * width, width) & fmask;
+    ++tl;
+    float val;
+    if (VAR == 1) {
+      const uint32_t e = lut8[uc.next<LONG>() & 255];
+      val = __uint_as_float(((fld >> m) << 31) | (e << 23) | ((fld & (fmask >> 1)) << (23 - m)));
+    } else {
+      const float scale = pow2_biased(max((int)rw.mx[b * 4 + (p >> 5)], 1) - m);
+      const float qv = (float)(fld & (fmask >> 1)) * scale;
+      val = (fld >> (m + 1)) ? -qv : qv;
+    }
+    const uint16_t* xp = xsb + CAS_BLK * b + p;
+#pragma unroll
+    for (int q = 0; q < NV; ++q) acc[q] = fmaf(val, bf2f(xp[q * K]), acc[q]);
+  }
+}
+
+template <int VAR, int NV>
+__global__ void __launch_bounds__(kThreads) draft_gemv_runs_kernel(GemvArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const WView& w = a.w;
+  const int K = (int)w.K;
+  const int xbytes = NV * K * 2;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + xbytes);
+  uint8_t* lut8 = smem + xbytes + 16;
+  RunsScratch& rs = reinterpret_cast<RunsScratch*>(smem + xbytes + 16 + 256)[warp];
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_arrive_tx(bar, (uint32_t)xbytes);
+    bulk_g2s(xs, a.x, (uint32_t)xbytes, bar);
+  }
+  for (int i = threadIdx.x; i < 256; i += kThreads) lut8[i] = a.lut.v[i];
+  bool ok = mbar_wait_bounded(bar, 0);
+  if (!__syncthreads_and(ok)) {
+    if (threadIdx.x == 0) atomicExch(&g_gemv_wait_status, CAS_ERR_TIMEOUT);
+    mbar_wait_bounded(bar, 0);  // let an in-flight copy land before the CTA exits
+    return;
+  }
+
+  const int k = w.k, m = w.m, nsr = w.nsr;
+  const int rec = VAR == 1 ? w.rec_sm : w.rec_q;
+  const uint32_t* recs = VAR == 1 ? w.ssm : w.sq;
+  const int nsb = (int)w.nsb;
+  const int kt = CAS_SB * k, q = (kt + 31) >> 5;
+  const int t0 = min(lane * q, kt), t1 = min(t0 + q, kt);
+  const int stride = gridDim.x * kWarps;
+  const uint32_t lim = (uint32_t)a.sexp_words;
+  for (int s = blockIdx.x * kWarps + warp; s < nsb; s += stride) {
+    const int n = s / nsr;
+    const int j = s - n * nsr;
+    const int64_t gb0 = (int64_t)s * CAS_SB;  // rows are whole superblocks
+    const uint16_t* xsb = xs + CAS_BLK * CAS_SB * j;
+    float acc[NV];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) acc[v] = 0.f;
+    int nw = 0;
+    uint32_t sb0 = 0;
+    if (VAR == 1) {
+      const uint32_t sb1 = min(__ldg(w.sidx + s + 1), lim);
+      sb0 = min(__ldg(w.sidx + s), sb1);
+      nw = (int)(sb1 - sb0);
+    }
+    bool fast = VAR == 2 || nw <= kStageWords, long_codes = false;
+    if (fast) {
+      const uint32_t* rsrc = recs + gb0 * rec;
+      for (int i = lane; i < CAS_SB * rec; i += 32) rs.r.rec[i] = __ldg(rsrc + i);
+      if (lane < 2) rs.r.rec[CAS_SB * rec + lane] = 0u;
+      if (VAR == 2) rs.r.mx[lane] = __ldg(w.smx + gb0 * 4 + lane);
+      if (VAR == 1) fast = stage_unary(w.sexp + sb0, nw, rs.r.us, lane, &long_codes) >= kt;
+      expand_mask_positions<CAS_SB * CAS_BLK>(__ldg(w.mask + gb0 * 4 + lane), rs.r.pos, lane);
+    }
+    __syncwarp();
+    if (fast) {
+      UnaryCursor uc;
+      if (VAR == 1) uc.init(rs.r.us, unary_code_start(rs.r.us, nw, t0));
+      if (long_codes)
+        run_dot<VAR, NV, true>(rs.r, uc, lut8, k, m, rec, t0, t1, xsb, K, acc);
+      else
+        run_dot<VAR, NV, false>(rs.r, uc, lut8, k, m, rec, t0, t1, xsb, K, acc);
+    }
+    __syncwarp();
+    if (!fast) {  // Cassandra-1 stream longer than the stage
+#pragma unroll
+      for (int v = 0; v < NV; ++v) acc[v] = 0.f;
+      SbScratch sc{rs.code, nullptr, nullptr};
+      const SbInfo in = sb_prepare<1, false>(w, s, lut8, sc, lane);
+      uint32_t v[16];
+      sb_rebuild_word<1, false>(w, in, sc, lane, v);
+      const uint16_t* xp = xsb + 32 * lane;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+#pragma unroll
+        for (int qq = 0; qq < NV; ++qq) {
+          acc[qq] = fmaf(bf2f(v[i] & 0xFFFFu), bf2f(xp[qq * K + 2 * i]), acc[qq]);
+          acc[qq] = fmaf(bf2f(v[i] >> 16), bf2f(xp[qq * K + 2 * i + 1]), acc[qq]);
+        }
+      }
+      __syncwarp();
+    }
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const float r = warp_sumf(acc[v]);
+      if (lane == 0) atomicAdd(a.y + (int64_t)v * w.N + n, r);
+    }
+  }
+}
+
 // Cassandra-2 fast path (k = 64, m = 3, whole superblocks). The speculation
 // data has no unary stream: each kept value is a 5-bit field (sign, 4-bit q)
 // and each 32-position mask word is exactly one shared-exponent group. Phase
@@ -491,6 +639,18 @@ int launch_fast(const GemvArgs& a, cudaStream_t st) {
 }
 
 template <int VAR, int NV>
+int launch_runs(const GemvArgs& a, cudaStream_t st) {
+  size_t smem = (size_t)NV * a.w.K * 2 + 16 + 256 + kWarps * sizeof(RunsScratch);
+  auto kern = draft_gemv_runs_kernel<VAR, NV>;
+  int per_sm = occupancy((const void*)kern, kThreads, smem);
+  if (per_sm < 1) return CAS_ERR_CUDA;
+  int64_t need = (a.w.nsb + kWarps - 1) / kWarps;
+  int g = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sm_count() * per_sm));
+  kern<<<g, kThreads, smem, st>>>(a);
+  return launch_status();
+}
+
+template <int VAR, int NV>
 int launch(const GemvArgs& a, cudaStream_t st) {
   size_t smem = (size_t)NV * a.w.K * 2 + 16 + 1024 + kWarps * kWarpWords * 4;
   auto kern = draft_gemv_kernel<VAR, NV>;
@@ -517,6 +677,14 @@ int dispatch(const GemvArgs& a, int nvec, cudaStream_t st) {
     }
   }
   if (fast && VAR == 2 && nvec <= 2) return nvec == 1 ? launch_fast2<1>(a, st) : launch_fast2<2>(a, st);
+  if (a.w.nbr % CAS_SB == 0) {
+    switch (nvec) {
+      case 1: return launch_runs<VAR, 1>(a, st);
+      case 2: return launch_runs<VAR, 2>(a, st);
+      case 3: return launch_runs<VAR, 3>(a, st);
+      default: return launch_runs<VAR, 4>(a, st);
+    }
+  }
   switch (nvec) {
     case 1: return launch<VAR, 1>(a, st);
     case 2: return launch<VAR, 2>(a, st);

@@ -114,6 +114,8 @@ struct UnaryCursor {
 // writes the block position of each of its kept values at their superblock
 // ordinal. Positions of a corrupt mask (a block without exactly 64 kept
 // values) land at wrong ordinals but never outside the array.
+// CAP: entries of pos (a power of two; 512 for k = 64, 1024 for any k).
+template <int CAP = CAS_SB * 64>
 __device__ __forceinline__ void expand_mask_positions(uint32_t mw, uint8_t* pos, int lane) {
   const int cnt = __popc(mw);
   int idx = warp_incl_add(cnt, lane) - cnt;
@@ -121,7 +123,7 @@ __device__ __forceinline__ void expand_mask_positions(uint32_t mw, uint8_t* pos,
 #pragma unroll
   for (int p = 0; p < 32; ++p) {
     if ((mw >> p) & 1u) {
-      pos[idx & (CAS_SB * 64 - 1)] = (uint8_t)pv;
+      pos[idx & (CAP - 1)] = (uint8_t)pv;
       ++idx;
     }
     ++pv;

@@ -107,6 +107,36 @@ def wide_exponent_rows(N, K, n_wide, seed):
     return torch.from_numpy(Wn.view(np.int16))
 
 
+RUN_CASES = [
+    # rows of whole superblocks (K % 1024 == 0) with k, m off the k = 64, m = 3 path
+    (32, 2048, 1, 38, 3), (16, 1024, 1, 0, 3), (16, 2048, 1, 128, 7), (24, 1024, 1, 77, 2),
+    (8, 1024, 1, 1, 0), (16, 1024, 1, 26, 5), (32, 2048, 2, 38, 1), (16, 1024, 2, 128, 7),
+    (24, 2048, 2, 90, 0), (16, 1024, 2, 0, 4), (16, 1024, 2, 51, 3),
+]
+
+
+@pytest.mark.parametrize("N,K,variant,k,m", RUN_CASES)
+@pytest.mark.parametrize("nvec", [1, 2, 3, 4])
+def test_draft_gemv_any_k_m(cas, orc, N, K, variant, k, m, nvec):
+    W = synthetic.normal_weight(N, K, seed=3 * N + K + k, outlier_frac=0.01)
+    x = synthetic.activations(nvec, K, seed=7 + nvec)
+    enc = cas.encode_weights(W.cuda(), variant, k, m)
+    y = cas.draft_gemv(enc, x.cuda())
+    ref, norm = orc.matvec(orc.draft_values(np16(W), variant, k, m), np16(x))
+    check_close(y, ref, norm, "draft_gemv any k, m")
+
+
+@pytest.mark.parametrize("variant,k,m", [(1, 38, 3), (1, 90, 5), (2, 38, 3)])
+def test_draft_gemv_any_k_m_long_codes(cas, orc, variant, k, m):
+    N, K = 48, 2048
+    W = wide_exponent_rows(N, K, 8, seed=9)
+    x = synthetic.activations(2, K, seed=19)
+    enc = cas.encode_weights(W.cuda(), variant, k, m)
+    y = cas.draft_gemv(enc, x.cuda())
+    ref, norm = orc.matvec(orc.draft_values(np16(W), variant, k, m), np16(x))
+    check_close(y, ref, norm, "draft_gemv any k, m, long codes")
+
+
 @pytest.mark.parametrize("variant", [1, 2])
 @pytest.mark.parametrize("nvec", [1, 3])
 def test_draft_gemv_long_codes(cas, orc, variant, nvec):
