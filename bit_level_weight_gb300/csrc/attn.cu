@@ -86,6 +86,22 @@ __device__ __forceinline__ void decode_sb_tile(const KvDev& d, int st, int64_t n
                            *reinterpret_cast<TileStage*>(scratch), tile + row0 * kRow, kRow, lane))
       return;
   }
+  if (sb < nsb && d.variant == 1 && CAS_SB * (sb + 1) <= n && !(d.k == 64 && d.m == 3)) {
+    // whole superblock, other k or m: per-lane runs
+    const uint32_t* sidx = (const uint32_t*)kv_sec(d, CAS_KV_SPEC_SBIDX, st);
+    const uint32_t* vidx = (const uint32_t*)kv_sec(d, CAS_KV_VER_SBIDX, st);
+    const uint32_t a0 = sidx[sb], a1 = sidx[sb + 1];
+    const uint32_t v0 = FULL ? vidx[sb] : 0u, v1 = FULL ? vidx[sb + 1] : 0u;
+    TileStage& ts = *reinterpret_cast<TileStage*>(scratch);
+    if (runs_sb_tile<FULL>((const uint32_t*)kv_sec(d, CAS_KV_MASK, st) + sb * 32,
+                           (const uint32_t*)kv_sec(d, CAS_KV_SPEC_SM, st) + sb * CAS_SB * d.rec_sm, d.rec_sm,
+                           (const uint32_t*)kv_sec(d, CAS_KV_VER_LO, st) + sb * CAS_SB * d.rec_lo, d.rec_lo,
+                           (const uint32_t*)kv_sec(d, CAS_KV_VER_PR, st) + sb * CAS_SB * d.rec_pr, d.rec_pr,
+                           (const uint32_t*)kv_sec(d, CAS_KV_SPEC_EXP, st) + a0, (int)(a1 - a0),
+                           (const uint32_t*)kv_sec(d, CAS_KV_VER_EXP, st) + v0, (int)(v1 - v0), d.k, d.m, lut,
+                           ts.us, ts.kpos, tile + row0 * kRow, kRow, lane))
+      return;
+  }
   // generic decoder (other k, m, Cassandra-2, partial superblocks, fallback):
   // lane L writes mask word L, zeros past the stream's tokens
   uint16_t* dst = tile + (row0 + (lane >> 2)) * kRow + 32 * (lane & 3);

@@ -53,7 +53,9 @@ static_assert(scratch_warp<1>() % 16 == 0 && alignof(TileStage) <= 16, "per-warp
 static_assert(kWarps * scratch_warp<1>() >= kWarps * 256 * 4, "warp partials fit in the scratch");
 
 // FAST: Cassandra-1, k = 64, m = 3, whole superblocks (per-lane cursors, lane_sb_tile).
-template <int VAR, int NT, bool FAST>
+// MODE 1: Cassandra-1, k = 64, m = 3 (lane_sb_tile); MODE 2: Cassandra-1,
+// any k, m, rows of whole superblocks (runs_sb_tile); MODE 0: generic.
+template <int VAR, int NT, int MODE>
 __global__ void __launch_bounds__(kThreads, 4) verify_gemm_kernel(GemmArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const WView& w = a.w;
@@ -81,14 +83,20 @@ __global__ void __launch_bounds__(kThreads, 4) verify_gemm_kernel(GemmArgs a) {
       int64_t n = rt * kRows + r;
       uint4* dst = reinterpret_cast<uint4*>(tile + r * kTileStride + kBlkStride * (lane >> 2) + 32 * (lane & 3));
       bool done = false;
-      if (n < w.N && FAST) {
+      if (n < w.N && MODE != 0) {
         const int64_t s = n * w.nsr + j;
         const int64_t gb0 = n * w.nbr + CAS_SB * j;
         const uint32_t a0 = __ldg(w.sidx + s), a1 = __ldg(w.sidx + s + 1);
         const uint32_t v0 = __ldg(w.vidx + s), v1 = __ldg(w.vidx + s + 1);
-        done = lane_sb_tile<true>(w.mask + gb0 * 4, w.ssm + gb0 * 8, w.vlo + gb0 * 8, w.vpr + gb0 * 16,
-                                  w.sexp + a0, (int)(a1 - a0), w.vexp + v0, (int)(v1 - v0), s_lut, ts,
-                                  tile + r * kTileStride, kBlkStride, lane);
+        if (MODE == 1)
+          done = lane_sb_tile<true>(w.mask + gb0 * 4, w.ssm + gb0 * 8, w.vlo + gb0 * 8, w.vpr + gb0 * 16,
+                                    w.sexp + a0, (int)(a1 - a0), w.vexp + v0, (int)(v1 - v0), s_lut, ts,
+                                    tile + r * kTileStride, kBlkStride, lane);
+        else
+          done = runs_sb_tile<true>(w.mask + gb0 * 4, w.ssm + gb0 * w.rec_sm, w.rec_sm, w.vlo + gb0 * w.rec_lo,
+                                    w.rec_lo, w.vpr + gb0 * w.rec_pr, w.rec_pr, w.sexp + a0, (int)(a1 - a0),
+                                    w.vexp + v0, (int)(v1 - v0), w.k, w.m, s_lut, ts.us, ts.kpos,
+                                    tile + r * kTileStride, kBlkStride, lane);
       }
       if (done) {
       } else if (n < w.N) {
@@ -166,10 +174,10 @@ __global__ void __launch_bounds__(kThreads, 4) verify_gemm_kernel(GemmArgs a) {
   }
 }
 
-template <int VAR, int NT, bool FAST>
+template <int VAR, int NT, int MODE>
 int launch(const GemmArgs& a, cudaStream_t st) {
   size_t smem = (size_t)kRows * kTileStride * 2 + 256 + kWarps * scratch_warp<VAR>();
-  auto kern = verify_gemm_kernel<VAR, NT, FAST>;
+  auto kern = verify_gemm_kernel<VAR, NT, MODE>;
   int per_sm = occupancy((const void*)kern, kThreads, smem);
   if (per_sm < 1) return CAS_ERR_CUDA;
   int64_t ntasks = (a.w.N + kRows - 1) / kRows * a.w.nsr;
@@ -199,7 +207,14 @@ extern "C" int cas_verify_gemm(const cas_weights* W, const uint16_t* X, int T, f
   a.Y = Y;
   a.T = T;
   bool v1 = W->p.variant == 1;
-  bool fast = v1 && a.w.k == 64 && a.w.m == 3 && a.w.nbr % CAS_SB == 0;
-  if (T <= 8) return fast ? launch<1, 1, true>(a, st) : v1 ? launch<1, 1, false>(a, st) : launch<2, 1, false>(a, st);
-  return fast ? launch<1, 2, true>(a, st) : v1 ? launch<1, 2, false>(a, st) : launch<2, 2, false>(a, st);
+  const bool whole = a.w.nbr % CAS_SB == 0;
+  const bool fast = v1 && a.w.k == 64 && a.w.m == 3 && whole;
+  if (T <= 8) {
+    if (fast) return launch<1, 1, 1>(a, st);
+    if (v1 && whole) return launch<1, 1, 2>(a, st);
+    return v1 ? launch<1, 1, 0>(a, st) : launch<2, 1, 0>(a, st);
+  }
+  if (fast) return launch<1, 2, 1>(a, st);
+  if (v1 && whole) return launch<1, 2, 2>(a, st);
+  return v1 ? launch<1, 2, 0>(a, st) : launch<2, 2, 0>(a, st);
 }

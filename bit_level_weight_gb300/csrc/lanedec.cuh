@@ -266,4 +266,103 @@ __device__ __forceinline__ bool lane_sb_tile(const uint32_t* __restrict__ mask, 
   return true;
 }
 
+// Any k and m (Cassandra-1, one whole superblock): lane L rebuilds the run of
+// kept ordinals [L q, L q + q), q = ceil(8k / 32), and (FULL) the run of
+// pruned ordinals [L q', L q' + q'), q' = ceil(8(128-k) / 32); runs may cross
+// blocks. Positions come from the mask expanded into `pos` (1024 bytes; kept,
+// then pruned), exponents from the unary cursor, record fields from global
+// memory at run-time bit offsets (rec_*: words per block record). Same
+// contract as lane_sb_tile; scratch: `us` and `pos` (1888 bytes).
+__device__ __forceinline__ uint32_t field_g(const uint32_t* __restrict__ w, int bit, int width) {
+  const int i = bit >> 5;
+  return __funnelshift_r(__ldg(w + i), __ldg(w + i + 1), bit & 31) & ((1u << width) - 1u);
+}
+
+template <bool FULL, bool LONG>
+__device__ __forceinline__ void runs_kept_to_tile(UnaryCursor& uc, const uint8_t* pos, const uint32_t* sm, int rec_sm,
+                                                  const uint32_t* lo, int rec_lo, int k, int m, int t0, int t1,
+                                                  const uint8_t* __restrict__ lut, uint16_t* dst, int bstride) {
+  int b = k > 0 ? t0 / k : 0;
+  int tl = t0 - b * k;
+  for (int t = t0; t < t1; ++t) {
+    if (tl == k) {
+      ++b;
+      tl = 0;
+    }
+    const uint32_t fld = field_g(sm + b * rec_sm, tl * (m + 1), m + 1);
+    const uint32_t e = lut[uc.next<LONG>() & 255];
+    uint32_t bits = ((fld >> m) << 15) | (e << 7) | ((fld & ((1u << m) - 1u)) << (7 - m));
+    if (FULL && m < 7) bits |= field_g(lo + b * rec_lo, tl * (7 - m), 7 - m);
+    ++tl;
+    dst[b * bstride + pos[t]] = (uint16_t)bits;
+  }
+}
+
+template <bool LONG>
+__device__ __forceinline__ void runs_pruned_to_tile(UnaryCursor& uc, const uint8_t* pos, const uint32_t* pr, int rec_pr,
+                                                    int kp, int u0, int u1, const uint8_t* __restrict__ lut,
+                                                    uint16_t* dst, int bstride) {
+  int b = kp > 0 ? u0 / kp : 0;
+  int ul = u0 - b * kp;
+  for (int u = u0; u < u1; ++u) {
+    if (ul == kp) {
+      ++b;
+      ul = 0;
+    }
+    const uint32_t byte = (__ldg(pr + b * rec_pr + (ul >> 2)) >> (8 * (ul & 3))) & 0xFFu;
+    const uint32_t e = lut[uc.next<LONG>() & 255];
+    ++ul;
+    dst[b * bstride + pos[u]] = (uint16_t)(((byte & 0x80u) << 8) | (e << 7) | (byte & 0x7Fu));
+  }
+}
+
+template <bool FULL>
+__device__ __forceinline__ bool runs_sb_tile(const uint32_t* __restrict__ mask, const uint32_t* __restrict__ sm,
+                                             int rec_sm, const uint32_t* __restrict__ lo, int rec_lo,
+                                             const uint32_t* __restrict__ pr, int rec_pr,
+                                             const uint32_t* __restrict__ sexp, int snw,
+                                             const uint32_t* __restrict__ vexp, int vnw, int k, int m,
+                                             const uint8_t* __restrict__ lut, UnaryStage& us, uint8_t* pos,
+                                             uint16_t* dst, int bstride, int lane) {
+  if (snw > kStageWords || (FULL && vnw > kStageWords)) return false;
+  const uint32_t mw = __ldg(mask + lane);
+  if (!FULL) {
+    uint4* z = reinterpret_cast<uint4*>(dst + (lane >> 2) * bstride + 32 * (lane & 3));
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    z[0] = zero;
+    z[1] = zero;
+    z[2] = zero;
+    z[3] = zero;
+  }
+  const int kt = CAS_SB * k, q = (kt + 31) >> 5;
+  const int t0 = min(lane * q, kt), t1 = min(t0 + q, kt);
+  bool long_codes;
+  const bool enough = stage_unary(sexp, snw, us, lane, &long_codes) >= kt;
+  expand_mask_positions<CAS_SB * CAS_BLK>(mw, pos, lane);
+  __syncwarp();
+  if (!enough) return false;
+  UnaryCursor uc;
+  uc.init(us, unary_code_start(us, snw, t0));
+  if (long_codes)
+    runs_kept_to_tile<FULL, true>(uc, pos, sm, rec_sm, lo, rec_lo, k, m, t0, t1, lut, dst, bstride);
+  else
+    runs_kept_to_tile<FULL, false>(uc, pos, sm, rec_sm, lo, rec_lo, k, m, t0, t1, lut, dst, bstride);
+  if (FULL) {
+    const int kp = CAS_BLK - k, pt = CAS_SB * kp, q2 = (pt + 31) >> 5;
+    const int u0 = min(lane * q2, pt), u1 = min(u0 + q2, pt);
+    __syncwarp();  // every lane is done with the kept stream and positions
+    const bool enough_v = stage_unary(vexp, vnw, us, lane, &long_codes) >= pt;
+    expand_mask_positions<CAS_SB * CAS_BLK>(~mw, pos, lane);
+    __syncwarp();
+    if (!enough_v) return false;
+    uc.init(us, unary_code_start(us, vnw, u0));
+    if (long_codes)
+      runs_pruned_to_tile<true>(uc, pos, pr, rec_pr, kp, u0, u1, lut, dst, bstride);
+    else
+      runs_pruned_to_tile<false>(uc, pos, pr, rec_pr, kp, u0, u1, lut, dst, bstride);
+  }
+  __syncwarp();
+  return true;
+}
+
 }  // namespace cas
