@@ -445,7 +445,8 @@ def run_cas(args):
         "draft_gemv_frac_of_hbm": round(gemv_gbs / world / peak, 4),
         "draft_gemv_frac_of_8tbs_nominal": round(gemv_gbs / world / 8000.0, 4),
         "verify_gemm_frac_of_hbm": round(gemm_gbs / world / peak, 4),
-        "roofline": {"kernel": "draft_gemv_fast_kernel<1>" if args.keep == 64 and args.mant == 3 and B == 1 else "draft_gemv_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+        "roofline": {"kernel": ("draft_gemv_fast_kernel<1>" if args.keep == 64 and args.mant == 3 and B == 1
+                                else f"draft_gemv_runs_kernel<1,{B}>"), "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
                      "traffic": (round(PROFILED_TRAFFIC_RATIO * per_launch_bytes) if PROFILED_TRAFFIC_RATIO
