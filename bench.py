@@ -139,7 +139,7 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------- CPU oracle baseline
-def cpu_baseline(seconds: float, keep: int, mant: int):
+def cpu_baseline(seconds: float, keep: int, mant: int, variant: int = 1):
     """Oracle draft decode + GEMV (plain C, one thread) on a bounded sample: one
     1024x4096 Student-t(4) matrix of the same stack, repeated for ~`seconds`."""
     import numpy as np
@@ -149,7 +149,7 @@ def cpu_baseline(seconds: float, keep: int, mant: int):
     N, K = 1024, 4096
     W = synthetic.t4_weight(N, K, seed=0).numpy().view(np.uint16)
     x = synthetic.activations(1, K, seed=1).numpy().view(np.uint16)
-    enc = oracle.encode(W, 1, keep, mant)
+    enc = oracle.encode(W, variant, keep, mant)
     spec = enc.spec_bytes() + K * 2 + N * 4
     reps, t0 = 0, time.perf_counter()
     while True:
@@ -161,7 +161,7 @@ def cpu_baseline(seconds: float, keep: int, mant: int):
     dt = time.perf_counter() - t0
     return {"value": spec * reps / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{reps} x oracle draft decode + float64 GEMV of one 1024x4096 t4 matrix "
-                      f"(keep {keep}/128, m={mant}, Cassandra-1), {dt:.1f} s"}
+                      f"(keep {keep}/128, m={mant}, Cassandra-{variant}), {dt:.1f} s"}
 
 
 # ---------------------------------------------------------------------- workload
@@ -192,13 +192,13 @@ class Stack:
                 "down": raw["wdown"],
             }
             del raw
-            enc = {nm: cas.encode_weights(W, 1, args.keep, args.mant) for nm, W in fused.items()}
+            enc = {nm: cas.encode_weights(W, args.variant, args.keep, args.mant) for nm, W in fused.items()}
             del fused
             self.mats.append(enc)
         self.lm = None
         if self.vocab:
             Wl = synthetic.t4_weight(self.vocab, h, seed=999_983, device=dev)
-            self.lm = cas.encode_weights(Wl, 1, args.keep, args.mant)
+            self.lm = cas.encode_weights(Wl, args.variant, args.keep, args.mant)
             del Wl
         torch.cuda.synchronize()
         self.encode_s = time.time() - t0
@@ -213,7 +213,7 @@ class Stack:
         cas, args, dev = self.cas, self.args, self.dev
         T = args.ctx
         self.kv = []
-        p = cas.params(1, args.keep, args.mant)
+        p = cas.params(args.variant, args.keep, args.mant)
         chunk = 2048
         for layer in range(self.L):
             layer_kv = []
@@ -435,7 +435,7 @@ def run_cas(args):
             "workload": WORKLOADS[args.workload],
             "layers": stk.L, "lm_head_rows": stk.vocab or None, "hidden": stk.hidden, "ffn": stk.ffn, "heads": f"{stk.nq}q/{stk.nkv}kv x {stk.hd}",
             "batch": B, "draft_len": D, "verify_tokens": T, "ctx": args.ctx if attn else 0,
-            "keep_per_block": args.keep, "mant_bits": args.mant, "variant": "Cassandra-1",
+            "keep_per_block": args.keep, "mant_bits": args.mant, "variant": f"Cassandra-{args.variant}",
             "weights": "Student-t(4) x 0.02/sqrt(2), fused qkv and gate|up",
             "parallelism": "replicas" if world > 1 else "single GPU",
             "l2": f"inputs larger than L2 ({sum(draft_bytes.values()) / 1e9:.2f} GB speculation stream per draft pass)",
@@ -445,8 +445,7 @@ def run_cas(args):
         "draft_gemv_frac_of_hbm": round(gemv_gbs / world / peak, 4),
         "draft_gemv_frac_of_8tbs_nominal": round(gemv_gbs / world / 8000.0, 4),
         "verify_gemm_frac_of_hbm": round(gemm_gbs / world / peak, 4),
-        "roofline": {"kernel": ("draft_gemv_fast_kernel<1>" if args.keep == 64 and args.mant == 3 and B == 1
-                                else f"draft_gemv_runs_kernel<1,{B}>"), "bound": "hbm", "achieved": round(achieved, 1),
+        "roofline": {"kernel": gemv_kernel_name(args, B), "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
                      "traffic": (round(PROFILED_TRAFFIC_RATIO * per_launch_bytes) if PROFILED_TRAFFIC_RATIO
@@ -454,14 +453,15 @@ def run_cas(args):
                      "traffic_note": "per launch: (ncu dram bytes / algorithmic bytes of a 28672x4096 launch, "
                                      "profiles/draft_gemv_28672x4096.md) x algorithmic bytes per launch of this step",
                      "algorithmic_bytes_per_launch": int(per_launch_bytes)},
-        "alu_roof": alu_roof(achieved, clk) if args.keep == 64 and args.mant == 3 and B == 1 else None,
+        "alu_roof": (alu_roof(achieved, clk) if args.variant == 1 and args.keep == 64 and args.mant == 3 and B == 1
+                     else None),
         "e2e": e2e,
         "gpu_launches": launches_per_step * steps,
         "encode_s": round(stk.encode_s, 2),
     }
     out["clocks"] = clk.summary()
     if not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(args.cpu_seconds, args.keep, args.mant)
+        out["cpu_baseline"] = cpu_baseline(args.cpu_seconds, args.keep, args.mant, args.variant)
     print(json.dumps(out), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -482,6 +482,16 @@ PROFILED_TRAFFIC_RATIO = (61.904896 + 0.104192) / 61.85268
 # profiles/draft_gemv_28672x4096.md); None whenever that kernel changes
 PROFILED_LANE_INSTR_PER_ELEM = 109543024 * 32 / (28672 * 4096)
 SMS, LANES_PER_SM_CLK = 152, 128  # 4 schedulers x 32 lanes issue per SM clock
+
+
+def gemv_kernel_name(args, nvec: int) -> str:
+    """The draft GEMV kernel the stack's matrices (rows of whole superblocks) run."""
+    if args.keep == 64 and args.mant == 3:
+        if args.variant == 1:
+            return f"draft_gemv_fast_kernel<{nvec}>"
+        if nvec <= 2:
+            return f"draft_gemv_fast2_kernel<{nvec}>"
+    return f"draft_gemv_runs_kernel<{args.variant},{nvec}>"
 
 
 def alu_roof(achieved_gbs: float, clk) -> dict:
@@ -567,8 +577,8 @@ def run_reference(args):
     K, W = args.steps, max(args.warmup, 3)
     per = max(1.0, min(args.cpu_seconds, 90.0 / (K + W)))
     for _ in range(W):
-        cpu_baseline(per / 4, args.keep, args.mant)
-    vals = [cpu_baseline(per, args.keep, args.mant) for _ in range(K)]
+        cpu_baseline(per / 4, args.keep, args.mant, args.variant)
+    vals = [cpu_baseline(per, args.keep, args.mant, args.variant) for _ in range(K)]
     v = statistics.median(x["value"] for x in vals)
     import synthetic
     shp = synthetic.LLAMA3_8B if args.workload == "llama3-8b" else synthetic.QWEN3_8B
@@ -580,7 +590,7 @@ def run_reference(args):
         "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOADS[args.workload], "layers": args.layers, "hidden": shp["hidden"], "ffn": shp["ffn"],
                    "batch": args.batch, "draft_len": args.draft_len, "keep_per_block": args.keep,
-                   "mant_bits": args.mant, "variant": "Cassandra-1"},
+                   "mant_bits": args.mant, "variant": f"Cassandra-{args.variant}"},
         "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": vals[0]["sample"]},
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -630,18 +640,11 @@ def run_micro(args):
         sk, sv = synthetic.kv_scales(0, H, 0, device=dev), synthetic.kv_scales(0, H, 1, device=dev)
         Kc = synthetic.kv_tokens(args.ctx, H, seed=5, scales=sk, device=dev)
         Vc = synthetic.kv_tokens(args.ctx, H, seed=6, scales=sv, device=dev)
-        kv = cas.KVCache(H, args.ctx + 64, cas.params(1, args.keep, args.mant), Kc[:128], Vc[:128])
+        kv = cas.KVCache(H, args.ctx + 64, cas.params(args.variant, args.keep, args.mant), Kc[:128], Vc[:128])
         for t0 in range(0, args.ctx, 2048):
             kv.append(Kc[t0:t0 + 2048], Vc[t0:t0 + 2048])
         assert kv.status() == (args.ctx, 0)
-        k, m = args.keep, args.mant
-        words = lambda f, w: -(-(f * w) // 32) * 4  # noqa: E731
-        spec_tok = 16 + words(k, m + 1)
-        ver_tok = words(k, 7 - m) + words(128 - k, 8)
-        sidx = [kv.section("spec_sbidx", s_).cpu().numpy().view("uint32")[(args.ctx + 7) // 8] for s_ in range(2 * H)]
-        vidx = [kv.section("ver_sbidx", s_).cpu().numpy().view("uint32")[(args.ctx + 7) // 8] for s_ in range(2 * H)]
-        spec = 2 * H * args.ctx * spec_tok + 4 * int(sum(sidx)) + 2 * H * ((args.ctx + 7) // 8 + 1) * 4
-        full = spec + 2 * H * args.ctx * ver_tok + 4 * int(sum(vidx)) + 2 * H * ((args.ctx + 7) // 8 + 1) * 4
+        spec, full = kv_section_bytes(kv, args.ctx, args.variant, args.keep, args.mant)
         if args.micro == "draft_attn":
             q = synthetic.activations(1, Hq * 128, seed=7, device=dev).view(1, Hq, 128)
             tk = synthetic.activations(1, H * 128, seed=8, device=dev).view(1, 1, H, 128)
@@ -684,6 +687,30 @@ def run_micro(args):
     out.update(us_per_call=round(ms * 1e3, 2), bytes_per_call=int(nbytes),
                gbs=round(nbytes / (ms * 1e-3) / 1e9, 1), frac_of_hbm=round(nbytes / (ms * 1e-3) / 1e9 / peak, 4))
     print(json.dumps(out), flush=True)
+
+
+def kv_section_bytes(kv, n: int, variant: int, k: int, m: int) -> tuple:
+    """(speculation bytes, all bytes) of the KV cache's 2H streams holding n
+    tokens: fixed per-token records plus the words of every variable-length
+    stream and its superblock index."""
+    words = lambda f, w: -(-(f * w) // 32) * 4  # noqa: E731
+    nsb = (n + 7) // 8
+    idx = (nsb + 1) * 4
+
+    def stream(name, s_):
+        return 4 * int(kv.section(name, s_).cpu().numpy().view("uint32")[nsb]) + idx
+    spec = full = 0
+    for s_ in range(2 * kv.H):
+        if variant == 1:
+            sp = n * (16 + words(k, m + 1)) + stream("spec_sbidx", s_)
+            vr = n * (words(k, 7 - m) + words(128 - k, 8)) + stream("ver_sbidx", s_)
+        else:
+            sp = n * (16 + 4 + words(k, m + 2))
+            vr = (n * words(128 - k, 8) + stream("ver_sbidx", s_) + stream("ver_d_sbidx", s_)
+                  + stream("ver_res_sbidx", s_))
+        spec += sp
+        full += sp + vr
+    return spec, full
 
 
 def run_sweep(args):

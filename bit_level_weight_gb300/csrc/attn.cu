@@ -49,6 +49,7 @@ constexpr int kScratchC1 = (((int)sizeof(TileStage) > 2048 ? (int)sizeof(TileSta
 constexpr int kScratchC2 =
     (((int)sizeof(TileStage) > 2048 + 4 * kResWords ? (int)sizeof(TileStage) : 2048 + 4 * kResWords) + 15) & ~15;
 static_assert(kScratchC1 % 16 == 0 && kScratchC2 % 16 == 0 && alignof(TileStage) <= 16, "per-warp scratch alignment");
+static_assert(kScratchC2 >= (int)sizeof(TileStage2) && alignof(TileStage2) <= 16, "Cassandra-2 stage fits");
 
 struct AttnArgs {
   KvDev kv[kMaxBatch];
@@ -100,6 +101,24 @@ __device__ __forceinline__ void decode_sb_tile(const KvDev& d, int st, int64_t n
                            (const uint32_t*)kv_sec(d, CAS_KV_SPEC_EXP, st) + a0, (int)(a1 - a0),
                            (const uint32_t*)kv_sec(d, CAS_KV_VER_EXP, st) + v0, (int)(v1 - v0), d.k, d.m, lut,
                            ts.us, ts.kpos, tile + row0 * kRow, kRow, lane))
+      return;
+  }
+  if (sb < nsb && d.variant == 2 && CAS_SB * (sb + 1) <= n) {
+    // whole Cassandra-2 superblock: per-lane runs
+    const uint32_t* didx = (const uint32_t*)kv_sec(d, CAS_KV_VER_D_SBIDX, st);
+    const uint32_t* ridx = (const uint32_t*)kv_sec(d, CAS_KV_VER_RES_SBIDX, st);
+    const uint32_t* vidx = (const uint32_t*)kv_sec(d, CAS_KV_VER_SBIDX, st);
+    const uint32_t d0 = FULL ? didx[sb] : 0u, d1 = FULL ? didx[sb + 1] : 0u;
+    const uint32_t v0 = FULL ? vidx[sb] : 0u, v1 = FULL ? vidx[sb + 1] : 0u;
+    const uint32_t r0 = FULL ? ridx[sb] : 0u;
+    if (runs_sb_tile_c2<FULL>((const uint32_t*)kv_sec(d, CAS_KV_MASK, st) + sb * 32,
+                              (const uint32_t*)kv_sec(d, CAS_KV_SPEC_Q, st) + sb * CAS_SB * d.rec_q, d.rec_q,
+                              kv_sec(d, CAS_KV_SPEC_MX, st) + sb * 32,
+                              (const uint32_t*)kv_sec(d, CAS_KV_VER_D, st) + d0, (int)(d1 - d0),
+                              (const uint32_t*)kv_sec(d, CAS_KV_VER_RES, st) + r0,
+                              (const uint32_t*)kv_sec(d, CAS_KV_VER_PR, st) + sb * CAS_SB * d.rec_pr, d.rec_pr,
+                              (const uint32_t*)kv_sec(d, CAS_KV_VER_EXP, st) + v0, (int)(v1 - v0), d.k, d.m, lut,
+                              *reinterpret_cast<TileStage2*>(scratch), tile + row0 * kRow, kRow, lane))
       return;
   }
   // generic decoder (other k, m, Cassandra-2, partial superblocks, fallback):

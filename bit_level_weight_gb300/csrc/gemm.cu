@@ -50,11 +50,13 @@ __host__ __device__ constexpr int scratch_warp() {
   return (((int)sizeof(TileStage) > generic ? (int)sizeof(TileStage) : generic) + 15) & ~15;
 }
 static_assert(scratch_warp<1>() % 16 == 0 && alignof(TileStage) <= 16, "per-warp scratch alignment");
+static_assert(scratch_warp<2>() >= (int)sizeof(TileStage2) && alignof(TileStage2) <= 16, "Cassandra-2 stage fits");
 static_assert(kWarps * scratch_warp<1>() >= kWarps * 256 * 4, "warp partials fit in the scratch");
 
 // FAST: Cassandra-1, k = 64, m = 3, whole superblocks (per-lane cursors, lane_sb_tile).
-// MODE 1: Cassandra-1, k = 64, m = 3 (lane_sb_tile); MODE 2: Cassandra-1,
-// any k, m, rows of whole superblocks (runs_sb_tile); MODE 0: generic.
+// MODE 1: Cassandra-1, k = 64, m = 3 (lane_sb_tile); MODE 2: rows of whole
+// superblocks, any k, m (runs_sb_tile, Cassandra-2: runs_sb_tile_c2);
+// MODE 0: generic.
 template <int VAR, int NT, int MODE>
 __global__ void __launch_bounds__(kThreads, 4) verify_gemm_kernel(GemmArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -86,17 +88,26 @@ __global__ void __launch_bounds__(kThreads, 4) verify_gemm_kernel(GemmArgs a) {
       if (n < w.N && MODE != 0) {
         const int64_t s = n * w.nsr + j;
         const int64_t gb0 = n * w.nbr + CAS_SB * j;
-        const uint32_t a0 = __ldg(w.sidx + s), a1 = __ldg(w.sidx + s + 1);
         const uint32_t v0 = __ldg(w.vidx + s), v1 = __ldg(w.vidx + s + 1);
-        if (MODE == 1)
+        if (VAR == 2) {
+          const uint32_t d0 = __ldg(w.vdidx + s), d1 = __ldg(w.vdidx + s + 1);
+          done = runs_sb_tile_c2<true>(w.mask + gb0 * 4, w.sq + gb0 * w.rec_q, w.rec_q, w.smx + gb0 * 4,
+                                       w.vd + d0, (int)(d1 - d0), w.vres + __ldg(w.vresidx + s),
+                                       w.vpr + gb0 * w.rec_pr, w.rec_pr, w.vexp + v0, (int)(v1 - v0), w.k, w.m,
+                                       s_lut, *reinterpret_cast<TileStage2*>(wscr), tile + r * kTileStride,
+                                       kBlkStride, lane);
+        } else if (MODE == 1) {
+          const uint32_t a0 = __ldg(w.sidx + s), a1 = __ldg(w.sidx + s + 1);
           done = lane_sb_tile<true>(w.mask + gb0 * 4, w.ssm + gb0 * 8, w.vlo + gb0 * 8, w.vpr + gb0 * 16,
                                     w.sexp + a0, (int)(a1 - a0), w.vexp + v0, (int)(v1 - v0), s_lut, ts,
                                     tile + r * kTileStride, kBlkStride, lane);
-        else
+        } else {
+          const uint32_t a0 = __ldg(w.sidx + s), a1 = __ldg(w.sidx + s + 1);
           done = runs_sb_tile<true>(w.mask + gb0 * 4, w.ssm + gb0 * w.rec_sm, w.rec_sm, w.vlo + gb0 * w.rec_lo,
                                     w.rec_lo, w.vpr + gb0 * w.rec_pr, w.rec_pr, w.sexp + a0, (int)(a1 - a0),
                                     w.vexp + v0, (int)(v1 - v0), w.k, w.m, s_lut, ts.us, ts.kpos,
                                     tile + r * kTileStride, kBlkStride, lane);
+        }
       }
       if (done) {
       } else if (n < w.N) {
@@ -211,10 +222,10 @@ extern "C" int cas_verify_gemm(const cas_weights* W, const uint16_t* X, int T, f
   const bool fast = v1 && a.w.k == 64 && a.w.m == 3 && whole;
   if (T <= 8) {
     if (fast) return launch<1, 1, 1>(a, st);
-    if (v1 && whole) return launch<1, 1, 2>(a, st);
+    if (whole) return v1 ? launch<1, 1, 2>(a, st) : launch<2, 1, 2>(a, st);
     return v1 ? launch<1, 1, 0>(a, st) : launch<2, 1, 0>(a, st);
   }
   if (fast) return launch<1, 2, 1>(a, st);
-  if (v1 && whole) return launch<1, 2, 2>(a, st);
+  if (whole) return v1 ? launch<1, 2, 2>(a, st) : launch<2, 2, 2>(a, st);
   return v1 ? launch<1, 2, 0>(a, st) : launch<2, 2, 0>(a, st);
 }

@@ -365,4 +365,110 @@ __device__ __forceinline__ bool runs_sb_tile(const uint32_t* __restrict__ mask, 
   return true;
 }
 
+// Cassandra-2, any k and m, one whole superblock (same contract as
+// runs_sb_tile). Kept value t: sign and q from its spec_q field, E' = max(E, 1)
+// of its 32-position group; the draft value is q * 2^(E'-127-m). FULL adds
+// the distance d (unary code of the ver_d stream, read with the cursor) and
+// the min(8, 7-m+d) residual bits: sig = (q << w) | residual, exponent E' - d
+// when sig's leading bit is set (else 0). A lane's residual bits start at the
+// exclusive warp sum of the widths of the runs before it, so the lane first
+// decodes its d codes into `dbuf`. Pruned values as for Cassandra-1.
+struct TileStage2 {
+  UnaryStage us;
+  alignas(16) uint8_t pos[CAS_SB * CAS_BLK];
+  uint8_t dbuf[CAS_SB * CAS_BLK];  // distance d of every kept ordinal
+  uint8_t mx[CAS_SB * 4];          // shared exponents of the superblock
+};
+
+template <bool LONG>
+__device__ __forceinline__ int runs_read_d(UnaryCursor& uc, uint8_t* dbuf, int m, int t0, int t1) {
+  int wsum = 0;
+  for (int t = t0; t < t1; ++t) {
+    const int dd = uc.next<LONG>() & 255;
+    dbuf[t] = (uint8_t)dd;
+    wsum += min(8, 7 - m + dd);
+  }
+  return wsum;
+}
+
+template <bool FULL>
+__device__ __forceinline__ bool runs_sb_tile_c2(const uint32_t* __restrict__ mask, const uint32_t* __restrict__ sq,
+                                                int rec_q, const uint8_t* __restrict__ smx,
+                                                const uint32_t* __restrict__ vd, int dnw,
+                                                const uint32_t* __restrict__ vres,
+                                                const uint32_t* __restrict__ pr, int rec_pr,
+                                                const uint32_t* __restrict__ vexp, int vnw, int k, int m,
+                                                const uint8_t* __restrict__ lut, TileStage2& ts, uint16_t* dst,
+                                                int bstride, int lane) {
+  if (FULL && (dnw > kStageWords || vnw > kStageWords)) return false;
+  const uint32_t mw = __ldg(mask + lane);
+  if (!FULL) {
+    uint4* z = reinterpret_cast<uint4*>(dst + (lane >> 2) * bstride + 32 * (lane & 3));
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    z[0] = zero;
+    z[1] = zero;
+    z[2] = zero;
+    z[3] = zero;
+  }
+  const int kt = CAS_SB * k, q = (kt + 31) >> 5;
+  const int t0 = min(lane * q, kt), t1 = min(t0 + q, kt);
+  ts.mx[lane] = __ldg(smx + lane);
+  bool long_codes = false, enough = true;
+  if (FULL) enough = stage_unary(vd, dnw, ts.us, lane, &long_codes) >= kt;
+  expand_mask_positions<CAS_SB * CAS_BLK>(mw, ts.pos, lane);
+  __syncwarp();
+  if (!enough) return false;
+  int rbit = 0;
+  if (FULL) {
+    UnaryCursor uc;
+    uc.init(ts.us, unary_code_start(ts.us, dnw, t0));
+    const int wsum = long_codes ? runs_read_d<true>(uc, ts.dbuf, m, t0, t1) : runs_read_d<false>(uc, ts.dbuf, m, t0, t1);
+    rbit = warp_incl_add(wsum, lane) - wsum;
+  }
+  const int width = m + 2;
+  int b = k > 0 ? t0 / k : 0;
+  int tl = t0 - b * k;
+  for (int t = t0; t < t1; ++t) {
+    if (tl == k) {
+      ++b;
+      tl = 0;
+    }
+    const int p = ts.pos[t];
+    const uint32_t fld = field_g(sq + b * rec_q, tl * width, width);
+    ++tl;
+    const uint32_t sgn = fld >> (m + 1), qv = fld & ((1u << (m + 1)) - 1u);
+    const int ep = max((int)ts.mx[b * 4 + (p >> 5)], 1);
+    uint32_t bits;
+    if (FULL) {
+      const int dd = ts.dbuf[t];
+      const int w = min(8, 7 - m + dd);
+      const uint32_t res = field_g(vres, rbit, w);
+      rbit += w;
+      const uint32_t sig = ((qv << w) | res) & 0xFFu;
+      const uint32_t e = (sig & 0x80u) ? (uint32_t)(ep - dd) : 0u;
+      bits = (sgn << 15) | (e << 7) | (sig & 0x7Fu);
+    } else {
+      bits = (__float_as_uint((float)qv * pow2_biased(ep - m)) >> 16) | (sgn << 15);
+    }
+    dst[b * bstride + p] = (uint16_t)bits;
+  }
+  if (FULL) {
+    const int kp = CAS_BLK - k, pt = CAS_SB * kp, q2 = (pt + 31) >> 5;
+    const int u0 = min(lane * q2, pt), u1 = min(u0 + q2, pt);
+    __syncwarp();  // every lane is done with the distance stream and positions
+    const bool enough_v = stage_unary(vexp, vnw, ts.us, lane, &long_codes) >= pt;
+    expand_mask_positions<CAS_SB * CAS_BLK>(~mw, ts.pos, lane);
+    __syncwarp();
+    if (!enough_v) return false;
+    UnaryCursor uc;
+    uc.init(ts.us, unary_code_start(ts.us, vnw, u0));
+    if (long_codes)
+      runs_pruned_to_tile<true>(uc, ts.pos, pr, rec_pr, kp, u0, u1, lut, dst, bstride);
+    else
+      runs_pruned_to_tile<false>(uc, ts.pos, pr, rec_pr, kp, u0, u1, lut, dst, bstride);
+  }
+  __syncwarp();
+  return true;
+}
+
 }  // namespace cas

@@ -269,6 +269,24 @@ def test_verify_attention(cas, orc, lens, T, variant):
         check_attn(o[b], ref, nrm, f"verify attention b={b}")
 
 
+@pytest.mark.parametrize("variant,k,m", [(1, 38, 3), (2, 38, 2), (1, 100, 6), (2, 77, 5)])
+def test_attention_any_k_m(cas, orc, variant, k, m):
+    """Draft and verify attention over caches with k, m off the 64 / 3 path."""
+    H, Hq, n, T = 8, 32, 523, 5
+    K, V = make_tokens(n, H, layer=3, seed=91)
+    kv = new_cache(cas, H, 600, K, V, k, m, variant=variant)
+    kv.append(K.cuda(), V.cuda())
+    assert kv.status() == (n, 0)
+    q = synthetic.activations(1, Hq * D, seed=92).view(1, Hq, D)
+    o = cas.draft_attn_decode([kv], q.cuda())
+    ref, nrm = orc.attention(np16(q), oracle_draft_kv(orc, K, k, m, variant), oracle_draft_kv(orc, V, k, m, variant))
+    check_attn(o, ref, nrm, f"draft attention k={k} m={m} v={variant}")
+    qv = synthetic.activations(T, Hq * D, seed=93).view(1, T, Hq, D)
+    ov = cas.verify_attn([kv], qv.cuda())
+    ref, nrm = orc.attention(np16(qv[0]), np16(K), np16(V), causal_new=T)
+    check_attn(ov[0], ref, nrm, f"verify attention k={k} m={m} v={variant}")
+
+
 def test_attention_errors(cas):
     H = 8
     K, V = make_tokens(16, H, seed=1)

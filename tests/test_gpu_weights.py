@@ -126,6 +126,17 @@ def test_draft_gemv_any_k_m(cas, orc, N, K, variant, k, m, nvec):
     check_close(y, ref, norm, "draft_gemv any k, m")
 
 
+@pytest.mark.parametrize("N,K,variant,k,m", RUN_CASES)
+@pytest.mark.parametrize("T", [5, 14])
+def test_verify_gemm_any_k_m(cas, orc, N, K, variant, k, m, T):
+    W = synthetic.normal_weight(N, K, seed=5 * N + K + k + m, outlier_frac=0.01)
+    X = synthetic.activations(T, K, seed=31 + T)
+    enc = cas.encode_weights(W.cuda(), variant, k, m)
+    Y = cas.verify_gemm(enc, X.cuda())
+    ref, norm = orc.matvec(np16(W), np16(X))
+    check_close(Y, ref, norm, "verify_gemm any k, m")
+
+
 @pytest.mark.parametrize("variant,k,m", [(1, 38, 3), (1, 90, 5), (2, 38, 3)])
 def test_draft_gemv_any_k_m_long_codes(cas, orc, variant, k, m):
     N, K = 48, 2048
@@ -135,6 +146,10 @@ def test_draft_gemv_any_k_m_long_codes(cas, orc, variant, k, m):
     y = cas.draft_gemv(enc, x.cuda())
     ref, norm = orc.matvec(orc.draft_values(np16(W), variant, k, m), np16(x))
     check_close(y, ref, norm, "draft_gemv any k, m, long codes")
+    X = synthetic.activations(5, K, seed=20)
+    Y = cas.verify_gemm(enc, X.cuda())
+    ref, norm = orc.matvec(np16(W), np16(X))
+    check_close(Y, ref, norm, "verify_gemm any k, m, long codes")
 
 
 @pytest.mark.parametrize("variant", [1, 2])
