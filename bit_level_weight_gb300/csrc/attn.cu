@@ -501,13 +501,91 @@ __device__ __forceinline__ bool lane_sb_scores(const KvDev& d, int st, int64_t n
   return true;
 }
 
+// Any k, m, both variants, one whole superblock: lane L takes the kept
+// ordinals [ceil(k q / 4), ceil(k (q+1) / 4)) of block b = L / 4 (q = L % 4), so
+// the 4 lanes of a token still add their partial scores; record fields are
+// read at run-time offsets, exponents from the unary cursor (Cassandra-1) or
+// the group's shared exponent (Cassandra-2). Scratch: TileStage (C-1) or
+// TileStage2 (C-2); same contract as lane_sb_scores.
+template <int VAR, bool LONG>
+__device__ __forceinline__ float4 quarter_qdot(UnaryCursor& uc, const uint8_t* pos, const uint32_t* rec, const uint8_t* mx,
+                                               int m, int b, int o0, int o1, int k, const uint8_t* __restrict__ lut,
+                                               const float4* q4) {
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int width = VAR == 1 ? m + 1 : m + 2;
+  for (int o = o0; o < o1; ++o) {
+    const int p = pos[b * k + o];
+    const uint32_t fld = field_g(rec, o * width, width);
+    float val;
+    if (VAR == 1) {
+      const uint32_t e = lut[uc.next<LONG>() & 255];
+      val = __uint_as_float(((fld >> m) << 31) | (e << 23) | ((fld & ((1u << m) - 1u)) << (23 - m)));
+    } else {
+      const float qv = (float)(fld & ((1u << (m + 1)) - 1u)) * pow2_biased(max((int)mx[b * 4 + (p >> 5)], 1) - m);
+      val = (fld >> (m + 1)) ? -qv : qv;
+    }
+    const float4 q = q4[p];
+    acc.x = fmaf(val, q.x, acc.x);
+    acc.y = fmaf(val, q.y, acc.y);
+    acc.z = fmaf(val, q.z, acc.z);
+    acc.w = fmaf(val, q.w, acc.w);
+  }
+  return acc;
+}
+
+__device__ __forceinline__ bool quarter_sb_scores(const KvDev& d, int st, int64_t n, int64_t sb, const uint8_t* lut,
+                                                  uint8_t* scratch, const float4* q4, float4* out, int lane) {
+  const int64_t nsb = (n + CAS_SB - 1) / CAS_SB;
+  if (!(sb < nsb && CAS_SB * (sb + 1) <= n)) return false;
+  const int k = d.k, m = d.m, b = lane >> 2, q = lane & 3;
+  const int o0 = (k * q + 3) >> 2, o1 = (k * (q + 1) + 3) >> 2;
+  const uint32_t mw = __ldg((const uint32_t*)kv_sec(d, CAS_KV_MASK, st) + sb * 32 + lane);
+  float4 acc;
+  if (d.variant == 1) {
+    const uint32_t* sidx = (const uint32_t*)kv_sec(d, CAS_KV_SPEC_SBIDX, st);
+    const uint32_t a0 = sidx[sb], a1 = sidx[sb + 1];
+    const int snw = (int)(a1 - a0);
+    if (snw > kStageWords) return false;
+    TileStage& ts = *reinterpret_cast<TileStage*>(scratch);
+    bool long_codes;
+    const bool enough =
+        stage_unary((const uint32_t*)kv_sec(d, CAS_KV_SPEC_EXP, st) + a0, snw, ts.us, lane, &long_codes) >= CAS_SB * k;
+    expand_mask_positions<CAS_SB * CAS_BLK>(mw, ts.kpos, lane);
+    __syncwarp();
+    if (!enough) return false;
+    UnaryCursor uc;
+    uc.init(ts.us, unary_code_start(ts.us, snw, b * k + o0));
+    const uint32_t* rec = (const uint32_t*)kv_sec(d, CAS_KV_SPEC_SM, st) + (sb * CAS_SB + b) * d.rec_sm;
+    acc = long_codes ? quarter_qdot<1, true>(uc, ts.kpos, rec, nullptr, m, b, o0, o1, k, lut, q4)
+                     : quarter_qdot<1, false>(uc, ts.kpos, rec, nullptr, m, b, o0, o1, k, lut, q4);
+  } else {
+    TileStage2& ts = *reinterpret_cast<TileStage2*>(scratch);
+    ts.mx[lane] = __ldg(kv_sec(d, CAS_KV_SPEC_MX, st) + sb * 32 + lane);
+    expand_mask_positions<CAS_SB * CAS_BLK>(mw, ts.pos, lane);
+    __syncwarp();
+    UnaryCursor uc;  // unused for Cassandra-2
+    const uint32_t* rec = (const uint32_t*)kv_sec(d, CAS_KV_SPEC_Q, st) + (sb * CAS_SB + b) * d.rec_q;
+    acc = quarter_qdot<2, false>(uc, ts.pos, rec, ts.mx, m, b, o0, o1, k, lut, q4);
+  }
+#pragma unroll
+  for (int x = 1; x <= 2; x <<= 1) {
+    acc.x += __shfl_xor_sync(CAS_FULL, acc.x, x);
+    acc.y += __shfl_xor_sync(CAS_FULL, acc.y, x);
+    acc.z += __shfl_xor_sync(CAS_FULL, acc.z, x);
+    acc.w += __shfl_xor_sync(CAS_FULL, acc.w, x);
+  }
+  if (q == 0) out[b] = acc;
+  __syncwarp();
+  return true;
+}
+
 // Per 32-token step warp w scores its K superblock (tokens 8w..8w+7 of the
 // step) into sc, decodes its V superblock into the V tile, and after the
 // barrier runs query vector w over the 32 tokens (online softmax, P.V with
 // lane = 4 dims) exactly as the chunk kernel. Superblocks the cursors do not
 // cover (partial, Cassandra-2, other k or m, long streams) are decoded into a
 // K tile and scored from it.
-__global__ void __launch_bounds__(kThreads) attn_draft_fused_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, 7) attn_draft_fused_kernel(AttnArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint16_t* Kt = reinterpret_cast<uint16_t*>(smem);  // fallback K tile
   uint16_t* Vt = Kt + kStepTok * kRow;
@@ -543,7 +621,10 @@ __global__ void __launch_bounds__(kThreads) attn_draft_fused_kernel(AttnArgs a) 
   float m = -INFINITY, l = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
   for (int64_t t0 = t_begin; t0 < t_end; t0 += kStepTok) {
     const int64_t sb = t0 / CAS_SB + warp;
-    if (!lane_sb_scores(d, h, n, sb, lutK, wscr, q4, sc + warp * CAS_SB, lane)) {
+    const bool scored = (d.variant == 1 && d.k == 64 && d.m == 3)
+                            ? lane_sb_scores(d, h, n, sb, lutK, wscr, q4, sc + warp * CAS_SB, lane)
+                            : quarter_sb_scores(d, h, n, sb, lutK, wscr, q4, sc + warp * CAS_SB, lane);
+    if (!scored) {
       decode_sb_tile<false>(d, h, n, sb, Kt, warp * CAS_SB, lutK, wscr, lane);
       // lane = (token lane / 4 of this superblock, query vector lane % 4)
       const uint32_t* kr = reinterpret_cast<const uint32_t*>(Kt + (warp * CAS_SB + (lane >> 2)) * kRow);
