@@ -269,7 +269,8 @@ def test_verify_attention(cas, orc, lens, T, variant):
         check_attn(o[b], ref, nrm, f"verify attention b={b}")
 
 
-@pytest.mark.parametrize("variant,k,m", [(1, 38, 3), (2, 38, 2), (1, 100, 6), (2, 77, 5)])
+@pytest.mark.parametrize("variant,k,m", [(1, 38, 3), (2, 38, 2), (1, 100, 6), (2, 77, 5), (1, 128, 7), (2, 0, 3),
+                                         (1, 0, 0), (2, 128, 7)])
 def test_attention_any_k_m(cas, orc, variant, k, m):
     """Draft and verify attention over caches with k, m off the 64 / 3 path."""
     H, Hq, n, T = 8, 32, 523, 5
