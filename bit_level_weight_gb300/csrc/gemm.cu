@@ -8,7 +8,10 @@
 // split the k16 steps of the tile among themselves on the tensor cores
 // (mma m16n8k16, bf16 inputs, fp32 accumulation; T <= 8 uses one n8 tile, T <= 16
 // two). Warp partials are summed in shared memory and added to Y with fp32
-// atomics; Y is cleared first.
+// atomics; Y is cleared first. The row-superblocks are rebuilt by the
+// per-lane decoders of lanedec.cuh (k = 64, m = 3; any k, m on rows of whole
+// superblocks, both variants) or, for rows ending in a partial superblock, by
+// the generic warp decoder of sbdecode.cuh.
 #include <cuda_runtime.h>
 
 #include <algorithm>

@@ -6,19 +6,26 @@
 // blog review, section 3.1), so the kernel moves only the speculation bytes
 // and its cost is the integer work of decoding them.
 //
-// Mapping: one warp per superblock (row n, up to 8 blocks). The superblock's
-// kept values are split into 32 runs of q consecutive ordinals, one per lane,
-// so all lanes do the same number of multiply-adds. A lane locates the start
-// of its run - the mask word and bit of its first kept position, and the bit
-// after the t0-th '1' of the unary exponent stream - with warp popcount
-// prefixes, shuffle binary searches and a popcount select within a word. It
-// then walks its run with two cursors over '1' bits held in two-word windows
-// (clz, then clear the bit; no 64-bit shifts): one over the bit-reversed mask
-// (next kept position), one over the unary stream (code end; rank = distance
-// from the previous end). The rank table gives exponent << 23, which is OR-ed
-// with the sign and mantissa field into an fp32 value and multiplied with x
-// from shared memory (staged once per CTA by a TMA bulk copy). Partial sums go
-// to y with one fp32 atomic per (superblock, vector); y is cleared first.
+// Every kernel maps one warp to one superblock (row n, up to 8 blocks), stages
+// x once per CTA by a TMA bulk copy, and adds its partial sums to y with one
+// fp32 atomic per (superblock, vector); y is cleared first. Kernels:
+//   draft_gemv_fast_kernel   Cassandra-1, k = 64, m = 3, whole superblocks:
+//                            16 ordinals per lane, unary cursor over the
+//                            stream staged in shared memory (lanedec.cuh);
+//   draft_gemv_fast2_kernel  Cassandra-2, k = 64, m = 3, up to 2 vectors;
+//   draft_gemv_runs_kernel   any k, m, both variants, whole superblocks: runs
+//                            of ordinals across blocks;
+//   draft_gemv_kernel        rows ending in a partial superblock: per-lane
+//                            runs with cursors over '1' bits of the mask and
+//                            of the stream read from global memory (below).
+// draft_gemv_kernel: a lane locates the start of its run - the mask word and
+// bit of its first kept position, and the bit after the t0-th '1' of the unary
+// exponent stream - with warp popcount prefixes, shuffle binary searches and
+// a popcount select within a word, then walks it with two cursors over '1'
+// bits held in two-word windows: one over the bit-reversed mask (next kept
+// position), one over the unary stream (code end; rank = distance from the
+// previous end). The rank table gives exponent << 23, OR-ed with the sign and
+// mantissa field into an fp32 value multiplied with x.
 #include <cuda_runtime.h>
 
 #include <algorithm>
