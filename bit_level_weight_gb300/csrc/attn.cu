@@ -9,13 +9,18 @@
 // Split over tokens (flash decoding): a CTA takes one (sequence, kv head,
 // token chunk). The number of chunks is fixed at launch so that the grid is
 // one wave of resident CTAs; each CTA derives its range of 32-token steps
-// from the sequence length held on the device. Per 32-token step its 4 warps each decode one superblock
-// of K and of V into shared-memory tiles (fp32); then warp w runs the query
-// vectors w, w+4, ... of that kv head (GQA: the q heads h*G .. h*G+G-1, times
-// the T query tokens): scores with lane = token, online softmax, and the
-// P.V update with lane = 4 head dimensions. Chunk partials (max, sum,
-// unnormalised output) go to the workspace; a combine kernel merges them,
-// adds the tail tokens and normalises.
+// from the sequence length held on the device. Per 32-token step its 4 warps
+// each decode one superblock (8 tokens) of K and of V. Kernels:
+//   attn_draft_fused_kernel  draft, up to 4 query vectors per kv head: K
+//                            scores computed in the per-lane decode, V into a
+//                            bf16 tile, CUDA-core P.V (lane = 4 dimensions);
+//   attn_chunk_kernel        draft with more query vectors: K and V tiles,
+//                            scores with lane = token, CUDA-core P.V;
+//   attn_mma_kernel          verify: K and V tiles, S = Q K^T, online softmax
+//                            and P.V on tensor cores.
+// GQA: the q heads h*G .. h*G+G-1 (times the T query tokens) share kv head h.
+// Chunk partials (max, sum, unnormalised output) go to the workspace; a
+// combine kernel merges them, adds the tail tokens and normalises.
 #include <cuda_runtime.h>
 
 #include <algorithm>
