@@ -859,9 +859,7 @@ int run_attn(bool full, const cas_kv* const* kv, int B, const uint16_t* q, int T
   if (!full && T == 1 && a.qv_alloc <= 4) {
     s = launch_fused(a, Hkv, st);
   } else if (!full) {
-    if (qpw <= 1) s = launch_chunk<false, 1>(a, Hkv, st);
-    else if (qpw <= 4) s = launch_chunk<false, 4>(a, Hkv, st);
-    else s = launch_chunk<false, 8>(a, Hkv, st);
+    s = qpw <= 4 ? launch_chunk<false, 4>(a, Hkv, st) : launch_chunk<false, 8>(a, Hkv, st);
   } else {
     s = a.qv_alloc > 16 ? launch_mma<true, 2>(a, Hkv, st) : launch_mma<true, 1>(a, Hkv, st);
   }
