@@ -582,7 +582,6 @@ def run_reference(args):
     v = statistics.median(x["value"] for x in vals)
     import synthetic
     shp = synthetic.LLAMA3_8B if args.workload == "llama3-8b" else synthetic.QWEN3_8B
-    spec_per_step = None
     out = {
         "impl": "reference",
         "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
@@ -594,8 +593,8 @@ def run_reference(args):
         "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": vals[0]["sample"]},
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "note": "CPU oracle (plain C, one thread) on a bounded sample of the draft GEMV; spec_per_step "
-                f"{spec_per_step}",
+        "note": "CPU oracle (plain C, one thread) timed on a bounded sample of the draft GEMV workload; "
+                "value = speculation bytes decoded per second",
     }
     print(json.dumps(out), flush=True)
 
