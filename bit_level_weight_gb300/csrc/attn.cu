@@ -55,6 +55,11 @@ constexpr int kScratchC2 =
     (((int)sizeof(TileStage) > 2048 + 4 * kResWords ? (int)sizeof(TileStage) : 2048 + 4 * kResWords) + 15) & ~15;
 static_assert(kScratchC1 % 16 == 0 && kScratchC2 % 16 == 0 && alignof(TileStage) <= 16, "per-warp scratch alignment");
 static_assert(kScratchC2 >= (int)sizeof(TileStage2) && alignof(TileStage2) <= 16, "Cassandra-2 stage fits");
+// The draft decodes no pruned codes: its generic decoder needs 1024 code bytes,
+// so a Cassandra-1 draft takes just the cursor stage (8 resident CTAs of the
+// fused kernel fit in shared memory).
+constexpr int kScratchDraftC1 = (((int)sizeof(TileStage) > 1024 ? (int)sizeof(TileStage) : 1024) + 15) & ~15;
+static_assert(kScratchDraftC1 <= kScratchC1 && kScratchDraftC1 % 16 == 0, "draft scratch");
 
 struct AttnArgs {
   KvDev kv[kMaxBatch];
@@ -590,7 +595,7 @@ __device__ __forceinline__ bool quarter_sb_scores(const KvDev& d, int st, int64_
 // lane = 4 dims) exactly as the chunk kernel. Superblocks the cursors do not
 // cover (partial, Cassandra-2, other k or m, long streams) are decoded into a
 // K tile and scored from it.
-__global__ void __launch_bounds__(kThreads, 7) attn_draft_fused_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, 8) attn_draft_fused_kernel(AttnArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint16_t* Kt = reinterpret_cast<uint16_t*>(smem);  // fallback K tile
   uint16_t* Vt = Kt + kStepTok * kRow;
@@ -787,6 +792,7 @@ int one_wave(AttnArgs& a, int Hkv, const void* kern, size_t smem) {
 }
 
 int launch_fused(AttnArgs& a, int Hkv, cudaStream_t st) {
+  if (a.scr_warp == kScratchC1) a.scr_warp = kScratchDraftC1;  // every cache is Cassandra-1
   const size_t smem = (size_t)2 * kStepTok * kRow * 2 + (size_t)CAS_BLK * 16 + (size_t)kStepTok * 16 + 512 +
                       (size_t)kWarps * a.scr_warp;
   const int s = one_wave(a, Hkv, (const void*)attn_draft_fused_kernel, smem);
