@@ -467,20 +467,17 @@ def run_cas(args):
         dist.destroy_process_group()
 
 
-# DRAM traffic of the draft GEMV per algorithmic byte, from one ncu capture of
-# the current kernel on a 28672 x 4096 bench matrix (dram__bytes_read.sum +
-# dram__bytes_write.sum = 62.20 MB for 61.85 MB algorithmic; see
-# profiles/draft_gemv_28672x4096.md). Set to None when the kernel changes.
 # dram bytes read + written / algorithmic bytes of one draft_gemv_fast_kernel<1>
-# launch on the 28672 x 4096 matrix (ncu, profiles/draft_gemv_28672x4096.md);
-# set to None whenever that kernel changes until it is captured again
-PROFILED_TRAFFIC_RATIO = (61.904896 + 0.104192) / 61.85268
+# launch on the 28672 x 4096 matrix (ncu: 62.04 MB for 61.85 MB algorithmic,
+# profiles/draft_gemv_28672x4096.md); set to None whenever that kernel changes
+# until it is captured again
+PROFILED_TRAFFIC_RATIO = (61.904384 + 0.135168) / 61.85268
 
 
 # warp instructions x 32 / elements of one draft_gemv_fast_kernel<1> launch on
 # the 28672 x 4096 matrix (ncu smsp__inst_executed.sum,
 # profiles/draft_gemv_28672x4096.md); None whenever that kernel changes
-PROFILED_LANE_INSTR_PER_ELEM = 109543024 * 32 / (28672 * 4096)
+PROFILED_LANE_INSTR_PER_ELEM = 107314082 * 32 / (28672 * 4096)
 SMS, LANES_PER_SM_CLK = 152, 128  # 4 schedulers x 32 lanes issue per SM clock
 
 

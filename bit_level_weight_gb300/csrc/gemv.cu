@@ -291,7 +291,7 @@ __device__ __forceinline__ void lane_kept_dot(UnaryCursor& uc, uint4 pq, uint2 r
 }
 
 template <int NV>
-__global__ void __launch_bounds__(kThreads, NV <= 2 ? 5 : 4) draft_gemv_fast_kernel(GemvArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) draft_gemv_fast_kernel(GemvArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const WView& w = a.w;
   const int K = (int)w.K;
