@@ -726,7 +726,8 @@ extern "C" int cas_draft_gemv(const cas_weights* W, const uint16_t* x, int nvec,
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemsetAsync(y, 0, sizeof(float) * nvec * W->N, st) != cudaSuccess) return CAS_ERR_CUDA;
   if (W->K == 0) return CAS_OK;
-  if (W->N * ((W->K / CAS_BLK + CAS_SB - 1) / CAS_SB) >= (1ll << 31)) return CAS_ERR_INVALID;
+  // superblock indices stay 32-bit, with room for the grid stride
+  if (W->N * ((W->K / CAS_BLK + CAS_SB - 1) / CAS_SB) >= (1ll << 30)) return CAS_ERR_INVALID;
   GemvArgs a;
   a.w = make_view(W);
   for (int i = 0; i < 256; ++i) a.lut.v[i] = W->exp_of_rank[i];

@@ -147,12 +147,19 @@ int cas_choose_variant(const uint16_t* W, int64_t N, int64_t K, int keep_per_blo
  * where D(W) is the zero-filled speculation value (pruned -> 0, kept ->
  * mantissa truncated, Cassandra-2 -> shared-exponent grid). Reads only the
  * speculation sections. x: bf16 [nvec][K]; y: fp32 [nvec][N], overwritten.
- * fp32 accumulation; summation order is unspecified. */
+ * fp32 accumulation; summation order is unspecified. Errors: those of the
+ * descriptor check (CAS_ERR_INVALID, CAS_ERR_SHAPE); CAS_ERR_INVALID if nvec
+ * is outside 1..4, x or y is null or not 16-byte aligned, nvec * K * 2 bytes
+ * exceed 200 KiB (x is staged whole in shared memory) or the tensor has 2^30
+ * superblocks or more; CAS_ERR_CUDA on a launch error. N = 0 writes nothing. */
 int cas_draft_gemv(const cas_weights* W, const uint16_t* x, int nvec, float* y, void* stream);
 
 /* Verify GEMM [B3.1]: Y[t][n] = sum_k W[n][k] * X[t][k] for t < T (1..16)
  * with W rebuilt bit-exactly from both streams, on tensor cores with fp32
- * accumulation. X: bf16 [T][K]; Y: fp32 [T][N], overwritten. */
+ * accumulation. X: bf16 [T][K]; Y: fp32 [T][N], overwritten. Errors: those
+ * of the descriptor check (CAS_ERR_INVALID, CAS_ERR_SHAPE); CAS_ERR_INVALID if
+ * T is outside 1..16 or X or Y is null or not 16-byte aligned; CAS_ERR_CUDA on
+ * a launch error. N = 0 writes nothing. */
 int cas_verify_gemm(const cas_weights* W, const uint16_t* X, int T, float* Y, void* stream);
 
 /* Materialises the draft values D(W) as bf16 [N][K] (test path) [B3.1]. */
