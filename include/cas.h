@@ -162,9 +162,12 @@ int cas_draft_gemv(const cas_weights* W, const uint16_t* x, int nvec, float* y, 
  * a launch error. N = 0 writes nothing. */
 int cas_verify_gemm(const cas_weights* W, const uint16_t* X, int T, float* Y, void* stream);
 
-/* Materialises the draft values D(W) as bf16 [N][K] (test path) [B3.1]. */
+/* Materialises the draft values D(W) as bf16 [N][K] (test path) [B3.1].
+ * Errors: those of the descriptor check; CAS_ERR_INVALID if out is null or
+ * not 16-byte aligned (an empty tensor writes nothing); CAS_ERR_CUDA. */
 int cas_decode_draft(const cas_weights* W, uint16_t* out, void* stream);
-/* Rebuilds the original bf16 bits of W [N][K] from both streams [B3.1]. */
+/* Rebuilds the original bf16 bits of W [N][K] from both streams [B3.1].
+ * Errors as cas_decode_draft. */
 int cas_reconstruct(const cas_weights* W, uint16_t* out, void* stream);
 
 /* ------------------------------------------------------------------ KV cache
@@ -172,7 +175,11 @@ int cas_reconstruct(const cas_weights* W, uint16_t* out, void* stream);
  * heads of head_dim 128, one 128-element block per token, head and K|V.
  * Each (head, K|V) stream has its own rank table, counted over calibration
  * tokens and then frozen [B3.3]. A KV superblock is 8 consecutive tokens of
- * one stream. Only Cassandra-1 is supported for the KV cache.
+ * one stream. Either variant: Cassandra-1 (unary exponent codes) or
+ * Cassandra-2 (shared exponent per 32 dimensions of a token).
+ * Every KV entry point first checks the descriptor: CAS_ERR_INVALID for a
+ * null kv or base, n_kv_heads < 1, head_dim != 128 or parameters out of
+ * range.
  * The device state (n_tokens, per-stream code tails, sticky status) lives in
  * the caller's buffer, so appends, truncations and attention calls need no
  * host round trip. */
@@ -224,33 +231,41 @@ typedef struct cas_kv {
  * residual stream is sized for its worst case, 8 bits per kept value). Pruned (small)
  * values have more spread exponents and longer codes than kept ones: on
  * N(0,1) x LogNormal(0,0.5) K/V with k = 64 they average about 4 to 5 bits,
- * so 6.0 leaves room; an append that would overflow sets CAS_ERR_CAPACITY. */
+ * so 6.0 leaves room; an append that would overflow sets CAS_ERR_CAPACITY.
+ * Errors: CAS_ERR_INVALID for a null bytes, n_kv_heads < 1, max_tokens < 1,
+ * parameters out of range or an estimate outside (0, 256] bits. */
 int cas_kv_plan(int n_kv_heads, int64_t max_tokens, cas_params p, double est_bits_per_code,
                 uint64_t* bytes);
 
 /* Lays out *kv in buf and builds the rank table of each (head, K|V) stream from
  * the n_calib calibration tokens calib_k / calib_v (bf16 [n_calib][H][128]).
  * The cache starts empty (n_tokens = 0); calibration tokens are not appended.
- * Synchronises `stream`. Errors: CAS_ERR_NONFINITE for NaN/Inf calibration. */
+ * Synchronises `stream`. Errors: CAS_ERR_INVALID for bad layout arguments (as
+ * cas_kv_plan), a buf not 256-byte aligned, n_calib < 0 or null / misaligned
+ * calibration tokens; CAS_ERR_BUFFER if bytes is below the plan;
+ * CAS_ERR_NONFINITE for NaN/Inf calibration; CAS_ERR_CUDA. */
 int cas_kv_init(cas_kv* kv, void* buf, uint64_t bytes, int n_kv_heads, int64_t max_tokens,
                 cas_params p, double est_bits_per_code, const uint16_t* calib_k,
                 const uint16_t* calib_v, int64_t n_calib, void* stream);
 
 /* Online KV encoding [B3.3]: appends T tokens, k_new / v_new bf16 [T][H][128],
  * in order. On the device: if the tokens or code words would exceed capacity,
- * or a value is NaN/Inf, nothing is written and the sticky status is set. */
+ * or a value is NaN/Inf, nothing is written and the sticky status is set.
+ * Errors at the call: CAS_ERR_INVALID for T < 0 or null / misaligned tokens
+ * (T = 0 does nothing); CAS_ERR_CUDA. */
 int cas_encode_kv_append(cas_kv* kv, const uint16_t* k_new, const uint16_t* v_new, int T,
                          void* stream);
 
 /* Rolls the cache back to its first n_tokens tokens (rejected draft tokens).
- * n_tokens larger than the current count leaves the cache unchanged. */
+ * n_tokens larger than the current count leaves the cache unchanged.
+ * Errors: CAS_ERR_INVALID for n_tokens < 0; CAS_ERR_CUDA. */
 int cas_kv_truncate(cas_kv* kv, int64_t n_tokens, void* stream);
 
 /* Reads the device state. Synchronises `stream`. Returns the sticky device
  * status (CAS_OK, CAS_ERR_CAPACITY or CAS_ERR_NONFINITE) and the token count. */
 int cas_kv_status(const cas_kv* kv, int64_t* n_tokens, void* stream);
 
-/* Clears the sticky device status. */
+/* Clears the sticky device status. Errors: CAS_ERR_CUDA. */
 int cas_kv_clear_status(cas_kv* kv, void* stream);
 
 /* Workspace bytes of cas_draft_attn_decode / cas_verify_attn for a batch. */
@@ -262,7 +277,12 @@ uint64_t cas_attn_workspace_bytes(int batch, int n_q_heads, int T, int64_t max_t
  * tokens (the draft tokens of this step). GQA: head h reads kv head
  * h / (n_q_heads / n_kv_heads). q: bf16 [batch][n_q_heads][128];
  * tail_k, tail_v: bf16 [batch][n_tail][n_kv_heads][128] (NULL when n_tail = 0);
- * o: fp32 [batch][n_q_heads][128]. Softmax in fp32. */
+ * o: fp32 [batch][n_q_heads][128]. Softmax in fp32. Errors: CAS_ERR_INVALID
+ * for batch outside 1..8, null or misaligned q / o, n_tail outside 0..16 (or
+ * null tails with n_tail > 0), caches that differ in n_kv_heads, k or m, or
+ * n_q_heads not a multiple of n_kv_heads with at most 64 query vectors per kv
+ * head; CAS_ERR_BUFFER if the workspace is null, misaligned or smaller than
+ * cas_attn_workspace_bytes; CAS_ERR_CUDA. */
 int cas_draft_attn_decode(const cas_kv* const* kv, int batch, const uint16_t* q, int n_q_heads,
                           const uint16_t* tail_k, const uint16_t* tail_v, int n_tail, float* o,
                           void* workspace, uint64_t workspace_bytes, void* stream);
@@ -290,7 +310,9 @@ int cas_draft_attn_decode_noalloc(const cas_kv* const* kv, int batch, const uint
 /* Verify attention [B3.1]: T query tokens per sequence over the exact KV
  * (both streams merged), the T queries being the last T tokens of the cache:
  * query j sees every earlier token and the new tokens 0..j.
- * q: bf16 [batch][T][n_q_heads][128]; o: fp32 [batch][T][n_q_heads][128]. */
+ * q: bf16 [batch][T][n_q_heads][128]; o: fp32 [batch][T][n_q_heads][128].
+ * Errors as cas_draft_attn_decode, with T outside 1..16 also CAS_ERR_INVALID
+ * and T * n_q_heads / n_kv_heads at most 64. */
 int cas_verify_attn(const cas_kv* const* kv, int batch, const uint16_t* q, int T, int n_q_heads,
                     float* o, void* workspace, uint64_t workspace_bytes, void* stream);
 
