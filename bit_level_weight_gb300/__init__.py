@@ -138,6 +138,20 @@ def _bits(t: torch.Tensor) -> torch.Tensor:
     return t
 
 
+def _shape(t: torch.Tensor, shape: tuple, what: str):
+    """Raises unless t has exactly `shape` (the C ABI takes sizes on trust)."""
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{what}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _out(t: torch.Tensor, n: int, dtypes: tuple, what: str):
+    """Raises unless the output t holds exactly n elements of one of dtypes."""
+    if t.dtype not in dtypes:
+        raise ValueError(f"{what}: dtype {t.dtype}, expected one of {dtypes}")
+    if t.numel() != n:
+        raise ValueError(f"{what}: {t.numel()} elements, expected {n}")
+
+
 def params(variant: int = 1, keep_per_block: int = 64, mant_bits: int = 3) -> cas_params:
     return cas_params(variant, keep_per_block, mant_bits)
 
@@ -226,6 +240,8 @@ def encode_weights(W: torch.Tensor, variant: int = 1, keep_per_block: int = 64, 
 def cas_draft_gemv(W: EncodedWeights, x: torch.Tensor, y: torch.Tensor, stream=None):
     x = _bits(x)
     nvec = 1 if x.dim() == 1 else x.shape[0]
+    _shape(x, (W.K,) if x.dim() == 1 else (nvec, W.K), "x")
+    _out(y, nvec * W.N, (torch.float32,), "y")
     _check(lib().cas_draft_gemv(ctypes.byref(W.desc), _ptr(x), nvec, _ptr(y), _stream(stream)), "cas_draft_gemv")
     return y
 
@@ -233,16 +249,20 @@ def cas_draft_gemv(W: EncodedWeights, x: torch.Tensor, y: torch.Tensor, stream=N
 def cas_verify_gemm(W: EncodedWeights, X: torch.Tensor, Y: torch.Tensor, stream=None):
     X = _bits(X)
     T = 1 if X.dim() == 1 else X.shape[0]
+    _shape(X, (W.K,) if X.dim() == 1 else (T, W.K), "X")
+    _out(Y, T * W.N, (torch.float32,), "Y")
     _check(lib().cas_verify_gemm(ctypes.byref(W.desc), _ptr(X), T, _ptr(Y), _stream(stream)), "cas_verify_gemm")
     return Y
 
 
 def cas_decode_draft(W: EncodedWeights, out: torch.Tensor, stream=None):
+    _out(out, W.N * W.K, (torch.int16, torch.uint16, torch.bfloat16), "out")
     _check(lib().cas_decode_draft(ctypes.byref(W.desc), _ptr(out), _stream(stream)), "cas_decode_draft")
     return out
 
 
 def cas_reconstruct(W: EncodedWeights, out: torch.Tensor, stream=None):
+    _out(out, W.N * W.K, (torch.int16, torch.uint16, torch.bfloat16), "out")
     _check(lib().cas_reconstruct(ctypes.byref(W.desc), _ptr(out), _stream(stream)), "cas_reconstruct")
     return out
 
@@ -313,6 +333,8 @@ class KVCache:
     def __init__(self, n_kv_heads: int, max_tokens: int, p: cas_params, calib_k: torch.Tensor,
                  calib_v: torch.Tensor, est_bits_per_code: float = 6.0, stream=None):
         calib_k, calib_v = _bits(calib_k).contiguous(), _bits(calib_v).contiguous()
+        _shape(calib_k, (calib_k.shape[0], n_kv_heads, 128), "calib_k")
+        _shape(calib_v, tuple(calib_k.shape), "calib_v")
         dev = calib_k.device
         self.buf = torch.empty(cas_kv_plan(n_kv_heads, max_tokens, p, est_bits_per_code), dtype=torch.uint8,
                                device=dev)
@@ -327,6 +349,8 @@ class KVCache:
 
     def append(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
         k_new, v_new = _bits(k_new).contiguous(), _bits(v_new).contiguous()
+        _shape(k_new, (k_new.shape[0], self.H, 128), "k_new")
+        _shape(v_new, tuple(k_new.shape), "v_new")
         _check(lib().cas_encode_kv_append(ctypes.byref(self.desc), _ptr(k_new), _ptr(v_new), k_new.shape[0],
                                           _stream(stream)), "cas_encode_kv_append")
 
@@ -377,13 +401,26 @@ def cas_attn_workspace_bytes(batch: int, n_q_heads: int, T: int, max_tokens: int
     return int(lib().cas_attn_workspace_bytes(batch, n_q_heads, T, max_tokens))
 
 
+def _check_draft_args(kvs, q, tail_k, tail_v) -> int:
+    """Shape checks of a draft attention call; returns n_tail."""
+    _shape(q, (len(kvs), q.shape[1], 128), "q")
+    if (tail_k is None) != (tail_v is None):
+        raise ValueError("tail_k and tail_v: both or neither")
+    if tail_k is None:
+        return 0
+    _shape(tail_k, (len(kvs), tail_k.shape[1], kvs[0].H, 128), "tail_k")
+    _shape(tail_v, tuple(tail_k.shape), "tail_v")
+    return int(tail_k.shape[1])
+
+
 def draft_attn_decode(kvs, q: torch.Tensor, tail_k=None, tail_v=None, out=None, workspace=None, stream=None):
     """q [B][Hq][128] -> o [B][Hq][128] fp32 over the speculation KV plus bf16 tail tokens."""
     q = _bits(q).contiguous()
     B, Hq, _ = q.shape
-    n_tail = 0 if tail_k is None else tail_k.shape[1]
+    n_tail = _check_draft_args(kvs, q, tail_k, tail_v)
     if out is None:
         out = torch.empty(B, Hq, 128, dtype=torch.float32, device=q.device)
+    _out(out, B * Hq * 128, (torch.float32,), "out")
     if workspace is None:
         workspace = torch.empty(cas_attn_workspace_bytes(B, Hq, 1, max(k.desc.max_tokens for k in kvs)),
                                 dtype=torch.uint8, device=q.device)
@@ -401,9 +438,10 @@ def cas_draft_attn_decode_noalloc(kvs, q: torch.Tensor, tail_k=None, tail_v=None
     fixed 8 MiB device array shared by every call (see include/cas.h)."""
     q = _bits(q).contiguous()
     B, Hq, _ = q.shape
-    n_tail = 0 if tail_k is None else tail_k.shape[1]
+    n_tail = _check_draft_args(kvs, q, tail_k, tail_v)
     if out is None:
         out = torch.empty(B, Hq, 128, dtype=torch.float32, device=q.device)
+    _out(out, B * Hq * 128, (torch.float32,), "out")
     tk = None if tail_k is None else _bits(tail_k).contiguous()
     tv = None if tail_v is None else _bits(tail_v).contiguous()
     arr = _kv_array(kvs)
@@ -416,8 +454,10 @@ def verify_attn(kvs, q: torch.Tensor, out=None, workspace=None, stream=None):
     """q [B][T][Hq][128] -> o [B][T][Hq][128] fp32 over the exact KV (causal in the last T)."""
     q = _bits(q).contiguous()
     B, T, Hq, _ = q.shape
+    _shape(q, (len(kvs), T, Hq, 128), "q")
     if out is None:
         out = torch.empty(B, T, Hq, 128, dtype=torch.float32, device=q.device)
+    _out(out, B * T * Hq * 128, (torch.float32,), "out")
     if workspace is None:
         workspace = torch.empty(cas_attn_workspace_bytes(B, Hq, T, max(k.desc.max_tokens for k in kvs)),
                                 dtype=torch.uint8, device=q.device)
