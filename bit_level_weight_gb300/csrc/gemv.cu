@@ -669,12 +669,317 @@ int launch(const GemvArgs& a, cudaStream_t st) {
   return launch_status();
 }
 
+// ------------------------------------------------------------------ word path
+// Cassandra-1, k = 64, m = 3, rows made of whole superblocks, 1 or 2 vectors.
+// Lane L owns mask word L of the superblock (block L/4, positions
+// 32(L%4)..+31). Its kept values are consecutive ordinals, so their 4-bit
+// sign/mantissa fields are one bit range of the block record and their
+// exponent codes one bit range of the superblock's unary stream: each lane
+// walks three cursors of its own, with no cross-lane traffic per value.
+//   position: count of leading zeros of the bit-reversed mask word, the found
+//             bit cleared; once the word is exhausted the count is 32, which
+//             points at a zero pad float of x;
+//   exponent: count of leading zeros of a 64-bit window of the code stream
+//             aligned at the lane's first code (rank -> exponent by a table),
+//             re-aligned after every 8 codes;
+//   field:    nibble i of the lane's field window, moved into the sign and
+//             mantissa bits of an fp32 by one byte permute.
+// x is staged per CTA as fp32 with one zero pad float after every 32
+// positions, so lane L's 32 positions start on bank L and the lanes' gathers
+// of one step spread over the banks. Each warp takes a contiguous run of
+// superblocks and adds its sum to y once per row. Superblocks the fast walk
+// cannot take (a run of 31 or more zeros in the code stream, a lane's codes
+// wider than its windows, a stream longer than 64 words) go through the
+// generic superblock decoder.
+constexpr int kXGroup = 33;   // staged floats per 32 positions (32 + a zero pad)
+constexpr int kWordLut = 64;  // exponent by rank, ranks 0..63
+
+struct WordStage {
+  uint32_t st[64 + 32];  // stream words of the superblock, then zeros / read-ahead
+  uint32_t rec[64 + 8];  // sign/mantissa records of the 8 blocks, then pad
+};
+union WordScratch {
+  WordStage ws;
+  uint8_t code[CAS_SB * CAS_BLK];  // generic decoder: exponents by kept ordinal
+};
+
+__host__ __device__ constexpr int word_x_floats(int K) { return ((K / 32) * kXGroup + 3) & ~3; }
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+  float v;
+  asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t mad_u32(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+// trailing zeros (32 for 0)
+__device__ __forceinline__ int tzcnt(uint32_t w) { return w ? 31 - __clz(w & (0u - w)) : 32; }
+
+// sel8[b*8 + i] = MSB-first bit index of the (i+1)-th '1' of byte b (0 when
+// b has fewer ones), built at compile time.
+struct Sel8Table {
+  uint8_t v[2048];
+};
+constexpr Sel8Table make_sel8() {
+  Sel8Table t{};
+  for (int b = 0; b < 256; ++b) {
+    int seen = 0;
+    for (int q = 7; q >= 0; --q)
+      if ((b >> q) & 1) t.v[b * 8 + seen++] = (uint8_t)(7 - q);
+  }
+  return t;
+}
+__device__ const Sel8Table g_sel8 = make_sel8();
+
+// Bit index, counted from the MSB, of the r-th '1' (1-based) of w: two
+// popcount halvings, then the byte-select table.
+__device__ __forceinline__ int select_msb(uint32_t w, int r, const uint8_t* sel8) {
+  const uint32_t hi = w >> 16;
+  const int c1 = __popc(hi);
+  const bool h = r <= c1;
+  const uint32_t w16 = h ? hi : (w & 0xFFFFu);
+  r = h ? r : r - c1;
+  const uint32_t hb = w16 >> 8;
+  const int c2 = __popc(hb);
+  const bool hh = r <= c2;
+  const uint32_t b = hh ? hb : (w16 & 0xFFu);
+  r = hh ? r : r - c2;
+  const int base = (h ? 0 : 16) + (hh ? 0 : 8);
+  return base + __ldg(sel8 + b * 8 + ((r - 1) & 7));
+}
+
+// The generic superblock decoder for what the word walk cannot take. Kept out
+// of line so that its registers do not count against the fast path.
+template <int NV>
+__device__ __noinline__ void word_fallback(WView w, int64_t s, const uint8_t* lut8, uint8_t* code, const float* xb,
+                                           int xfl, float* part) {
+  const int lane = threadIdx.x & 31;
+  SbScratch ss{code, nullptr, nullptr};
+  const SbInfo in = sb_prepare<1, false>(w, s, lut8, ss, lane);
+  uint32_t v[16];
+  sb_rebuild_word<1, false>(w, in, ss, lane, v);
+#pragma unroll
+  for (int q = 0; q < NV; ++q) part[q] = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+#pragma unroll
+    for (int q = 0; q < NV; ++q) {
+      part[q] = fmaf(bf2f(v[i] & 0xFFFFu), xb[q * xfl + 2 * i], part[q]);
+      part[q] = fmaf(bf2f(v[i] >> 16), xb[q * xfl + 2 * i + 1], part[q]);
+    }
+  }
+  __syncwarp();
+}
+
+// 32 registers per thread (8 CTAs of 256 per SM).
+template <int NV>
+__global__ void __launch_bounds__(kThreads, 8) draft_gemv_word_kernel(GemvArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint8_t lut8[256];  // exponent by rank
+  const uint8_t* sel8 = g_sel8.v;
+  const WView& w = a.w;
+  const int K = (int)w.K;
+  const int xfl = word_x_floats(K);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float* xs = reinterpret_cast<float*>(smem);
+  WordScratch& sc = reinterpret_cast<WordScratch*>(smem + (size_t)NV * xfl * 4)[warp];
+
+  // x -> fp32, position p of vector v at v*xfl + (p/32)*33 + p%32; pads zero
+  for (int v = 0; v < NV; ++v) {
+    const uint4* xv = reinterpret_cast<const uint4*>(a.x + (size_t)v * K);
+    for (int i = threadIdx.x; i < K / 8; i += kThreads) {
+      const uint4 pr = __ldg(xv + i);
+      const int p = 8 * i;
+      float* d = xs + v * xfl + (p >> 5) * kXGroup + (p & 31);
+      d[0] = bf2f(pr.x & 0xFFFFu);
+      d[1] = bf2f(pr.x >> 16);
+      d[2] = bf2f(pr.y & 0xFFFFu);
+      d[3] = bf2f(pr.y >> 16);
+      d[4] = bf2f(pr.z & 0xFFFFu);
+      d[5] = bf2f(pr.z >> 16);
+      d[6] = bf2f(pr.w & 0xFFFFu);
+      d[7] = bf2f(pr.w >> 16);
+    }
+    for (int g = threadIdx.x; g < K / 32; g += kThreads) xs[v * xfl + g * kXGroup + 32] = 0.f;
+  }
+  for (int i = threadIdx.x; i < 256; i += kThreads) lut8[i] = a.lut.v[i];
+  if (lane < 8) sc.ws.rec[64 + lane] = 0u;
+  __syncthreads();
+
+  const int nsr = w.nsr;
+  const int nsb = (int)w.nsb;
+  const int nwarps = gridDim.x * kWarps;
+  const int gw = blockIdx.x * kWarps + warp;
+  const int per = (nsb + nwarps - 1) / nwarps;
+  const int s0 = min(gw * per, nsb), s1 = min(s0 + per, nsb);
+  const uint32_t lim = (uint32_t)a.sexp_words;
+  const int blk = lane >> 2;
+  const uint32_t x_a = smem_addr(xs) + 4u * (uint32_t)(lane * kXGroup);
+  int n = s0 / nsr, j = s0 - n * nsr;
+  float acc[NV];
+#pragma unroll
+  for (int q = 0; q < NV; ++q) acc[q] = 0.f;
+  for (int s = s0; s < s1; ++s) {
+    const int64_t gb0 = (int64_t)s * CAS_SB;
+    const uint32_t mw = __ldg(w.mask + gb0 * 4 + lane);
+    const uint2 rr = __ldg(reinterpret_cast<const uint2*>(w.ssm + gb0 * 8) + lane);
+    const uint32_t sb1 = min(__ldg(w.sidx + s + 1), lim), sb0 = min(__ldg(w.sidx + s), sb1);
+    const int nw = (int)(sb1 - sb0);
+    float part[NV];
+#pragma unroll
+    for (int q = 0; q < NV; ++q) part[q] = 0.f;
+    bool fast = nw <= 64;
+    if (fast) {
+      WordStage& ws = sc.ws;
+      ws.rec[2 * lane] = rr.x;
+      ws.rec[2 * lane + 1] = rr.y;
+      // stream words 2l, 2l+1 in lane l, with popcount prefixes
+      const uint32_t* gs = w.sexp + sb0;
+      const uint32_t w0 = 2 * lane < nw ? __ldg(gs + 2 * lane) : 0u;
+      const uint32_t w1 = 2 * lane + 1 < nw ? __ldg(gs + 2 * lane + 1) : 0u;
+      ws.st[2 * lane] = w0;
+      ws.st[2 * lane + 1] = w1;
+      ws.st[64 + lane] = 0u;
+      const int b1 = __popc(w1);
+      const int S = warp_incl_add(__popc(w0) + b1, lane);  // ones through word 2l+1
+      const int ncodes = __shfl_sync(CAS_FULL, S, 31);
+      // runs of 31+ zeros (a code of rank >= 31) across word boundaries
+      const int tz0 = tzcnt(w0), tz1 = tzcnt(w1);
+      const int lz1 = __clz(w1), lzn = __shfl_down_sync(CAS_FULL, __clz(w0), 1);
+      const bool run = (2 * lane + 1 < nw && tz0 + lz1 >= 31) || (2 * lane + 2 < nw && tz1 + lzn >= 31) ||
+                       (lane == 0 && nw > 0 && __clz(w0) >= 31);
+      const bool lng = __any_sync(CAS_FULL, run);
+      const int lw = nw - 1;  // the stream ends inside word nw-1
+      const int tzl = __shfl_sync(CAS_FULL, (lw & 1) ? tz1 : tz0, (lw >> 1) & 31);
+      const int endbit = nw > 0 ? 32 * lw + 32 - tzl : 0;
+      // block-local ordinal of the lane's first kept value
+      const int c = __popc(mw);
+      int inc = c;
+      const int u1 = __shfl_up_sync(CAS_FULL, inc, 1, 4);
+      if ((lane & 3) >= 1) inc += u1;
+      const int u2 = __shfl_up_sync(CAS_FULL, inc, 2, 4);
+      if ((lane & 3) >= 2) inc += u2;
+      const int o = min(inc - c, 64);
+      // start of the lane's first code: just after the T-th '1'
+      const int T = 64 * blk + o;
+      const int l = min(warp_count_le(S, T - 1), 31);  // first lane whose prefix reaches T
+      const int Sl = __shfl_sync(CAS_FULL, S, l), bl = __shfl_sync(CAS_FULL, b1, l);
+      const uint32_t x0 = __shfl_sync(CAS_FULL, w0, l), x1 = __shfl_sync(CAS_FULL, w1, l);
+      const int q0 = Sl - bl;  // ones through word 2l
+      const bool in0 = T <= q0;
+      const uint32_t wsel = in0 ? x0 : x1;
+      const int rr1 = T - (in0 ? q0 - __popc(x0) : q0);
+      const int start = T > 0 ? 32 * (2 * l + (in0 ? 0 : 1)) + select_msb(wsel, max(rr1, 1), sel8) + 1 : 0;
+      int nxt = __shfl_down_sync(CAS_FULL, start, 1);
+      if (lane == 31) nxt = endbit;
+      const int span = nxt - start;
+      __syncwarp();
+      // field window: fields o..o+31 of block blk's record, nibble i = field i
+      const uint32_t* rp = ws.rec + 8 * blk + (o >> 3);
+      const int fs = 4 * (o & 7);
+      uint32_t fo[4], fe[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        fo[q] = __funnelshift_r(rp[q], rp[q + 1], fs);  // odd fields in high nibbles
+        fe[q] = fo[q] << 4;                              // even fields moved up
+      }
+      // code window: 64 bits from `start`
+      int hw = start >> 5, sh = start & 31;
+      uint32_t H = __funnelshift_l(ws.st[hw + 1], ws.st[hw], sh);
+      uint32_t Lw = __funnelshift_l(ws.st[hw + 2], ws.st[hw + 1], sh);
+      uint32_t M = __brev(mw);
+      const uint32_t xa = x_a + 4u * (uint32_t)(j * (32 * kXGroup));
+      const int maxc = __reduce_max_sync(CAS_FULL, c);
+      int used = 0, u8 = 0, u16 = 0, u24 = 0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if ((i & 3) == 0 && i >= maxc) break;
+        if ((i & 7) == 0 && i > 0) {  // re-align the code window every 8 codes
+          if (i == 8) u8 = used;
+          if (i == 16) u16 = used;
+          if (i == 24) u24 = used;
+          const int pos = start + used;
+          hw = min(pos >> 5, 93);
+          sh = pos & 31;
+          H = __funnelshift_l(ws.st[hw + 1], ws.st[hw], sh);
+          Lw = __funnelshift_l(ws.st[hw + 2], ws.st[hw + 1], sh);
+        }
+        const int p = __clz(M);  // 32 once the word is exhausted: zero pad
+        M &= ~(0x80000000u >> (p & 31));
+        const int r = __clz(H);  // <= 30 for every code of a checked stream
+        const uint32_t e = lut8[r];
+        const int nb = r + 1;
+        H = __funnelshift_l(Lw, H, nb);
+        Lw = Lw << (nb & 31);
+        used += nb;
+        const uint32_t src = (i & 1) ? fo[i >> 3] : fe[i >> 3];
+        const int by = (i & 7) >> 1;
+        const uint32_t A = __byte_perm(src, 0u, (by << 12) | (by << 8) | 0x44);
+        const float val = __uint_as_float(mad_u32(e, 0x800000u, A & 0x80700000u));
+        const uint32_t xp = mad_u32((uint32_t)p, 4u, xa);
+#pragma unroll
+        for (int q = 0; q < NV; ++q) part[q] = fmaf(val, lds_f32(xp + 4u * (uint32_t)(q * xfl)), part[q]);
+      }
+      // every group of 8 codes must have fit its 64-bit window: full groups by
+      // the bits they consumed, the lane's last group by its true end
+      const int last = (c - 1) >> 3;  // -1 when the lane has no values
+      const bool bad = (last > 0 && u8 > 64) || (last > 1 && u16 - u8 > 64) || (last > 2 && u24 - u16 > 64) ||
+                       (last >= 0 && span - (last == 0 ? 0 : last == 1 ? u8 : last == 2 ? u16 : u24) > 64);
+      fast = !lng && ncodes >= 512 && !__any_sync(CAS_FULL, bad);
+    }
+    __syncwarp();
+    if (!fast) {
+      word_fallback<NV>(w, s, lut8, sc.code, xs + j * (32 * kXGroup) + lane * kXGroup, xfl, part);
+      if (lane < 8) sc.ws.rec[64 + lane] = 0u;  // the generic decoder used the scratch
+    }
+#pragma unroll
+    for (int q = 0; q < NV; ++q) acc[q] += part[q];
+    // next superblock; the row's sum goes to y when the row ends
+    if (++j == nsr || s + 1 == s1) {
+#pragma unroll
+      for (int q = 0; q < NV; ++q) {
+        const float r = warp_sumf(acc[q]);
+        if (lane == 0) atomicAdd(a.y + (int64_t)q * w.N + n, r);
+        acc[q] = 0.f;
+      }
+      if (j == nsr) {
+        j = 0;
+        ++n;
+      }
+    }
+  }
+}
+
+template <int NV>
+size_t word_smem(int64_t K) {
+  return (size_t)NV * word_x_floats((int)K) * 4 + kWarps * sizeof(WordScratch);
+}
+
+template <int NV>
+int launch_word(const GemvArgs& a, cudaStream_t st) {
+  const size_t smem = word_smem<NV>(a.w.K);
+  auto kern = draft_gemv_word_kernel<NV>;
+  int per_sm = occupancy((const void*)kern, kThreads, smem);
+  if (per_sm < 1) return CAS_ERR_CUDA;
+  // at least 4 superblocks per warp: each CTA stages x once
+  int64_t need = (a.w.nsb + 4 * kWarps - 1) / (4 * kWarps);
+  int g = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sm_count() * per_sm));
+  kern<<<g, kThreads, smem, st>>>(a);
+  return launch_status();
+}
+
 // The fast path covers Cassandra-1 with k = 64, m = 3 and rows that are whole
 // superblocks (K % 1024 == 0): every lane then owns exactly 16 ordinals that
 // sit in one 64-bit slice of one block record.
 template <int VAR>
 int dispatch(const GemvArgs& a, int nvec, cudaStream_t st) {
   const bool fast = a.w.k == 64 && a.w.m == 3 && a.w.nbr % CAS_SB == 0;
+  if (fast && VAR == 1 && nvec <= 2 && word_smem<2>(a.w.K) <= 200 * 1024)
+    return nvec == 1 ? launch_word<1>(a, st) : launch_word<2>(a, st);
   if (fast && VAR == 1) {
     switch (nvec) {
       case 1: return launch_fast<1>(a, st);

@@ -290,3 +290,41 @@ def test_llama_ffn_full_size_sampled(cas, orc, variant, k):
     Y = cas.verify_gemm(enc, X.cuda())[:, rows]
     Yr, Nr = orc.matvec(Wn[rows], np16(X))
     check_close(Y, Yr, Nr, "ffn verify gemm rows")
+
+
+def clustered_rows(N, K, seed):
+    """Rows whose kept values sit in chosen mask words of every block, so the
+    per-word counts of one superblock range from 0 to 32: row r of a group of
+    four keeps positions [0, 64), [64, 128), [32, 96) or every other position
+    of each block; the magnitudes of kept values are spread over many
+    exponents in the last rows, which makes their code runs long."""
+    rng = np.random.default_rng(seed)
+    base = rng.standard_normal((N, K)) * 0.02
+    big = rng.standard_normal((N, K)) * 0.5 + np.sign(rng.standard_normal((N, K))) * 0.6
+    keep = np.zeros((N, K // 128, 128), dtype=bool)
+    for r in range(N):
+        kind = r % 4
+        if kind == 0:
+            keep[r, :, :64] = True
+        elif kind == 1:
+            keep[r, :, 64:] = True
+        elif kind == 2:
+            keep[r, :, 32:96] = True
+        else:
+            keep[r, :, ::2] = True
+    v = np.where(keep.reshape(N, K), big, base)
+    wide = max(1, N // 8)
+    v[-wide:] = np.where(keep.reshape(N, K)[-wide:], v[-wide:] * 2.0 ** rng.integers(-40, 40, size=(wide, K)),
+                         v[-wide:])
+    return synthetic.to_bits(torch.from_numpy(v.astype(np.float32)))
+
+
+@pytest.mark.parametrize("nvec", [1, 2])
+@pytest.mark.parametrize("N,K", [(32, 2048), (24, 4096)])
+def test_draft_gemv_clustered_masks(cas, orc, N, K, nvec):
+    W = clustered_rows(N, K, seed=N + K)
+    x = synthetic.activations(nvec, K, seed=41 + nvec)
+    enc = cas.encode_weights(W.cuda(), 1, 64, 3)
+    y = cas.draft_gemv(enc, x.cuda())
+    ref, norm = orc.matvec(orc.draft_values(np16(W), 1, 64, 3), np16(x))
+    check_close(y, ref, norm, "draft_gemv clustered masks")
