@@ -91,6 +91,7 @@ def lib() -> ctypes.CDLL:
             "cas_draft_attn_decode": ([P, i32, P, i32, P, P, i32, P, P, u64, P], i32),
             "cas_verify_attn": ([P, i32, P, i32, i32, P, P, u64, P], i32),
             "cas_device_status": ([P], i32),
+            "cas_test_first_wait_spins": ([ctypes.c_uint32], i32),
             "cas_draft_attn_decode_noalloc": ([P, i32, P, i32, P, P, i32, P, P], i32),
         }
         for name, (args, res) in sig.items():

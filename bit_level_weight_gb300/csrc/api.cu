@@ -29,7 +29,13 @@ extern "C" int32_t cas_keep_from_ratio(double r) {
 
 namespace cas {
 int gemv_wait_status(bool clear);
+int set_first_wait_spins(uint32_t spins);
 }  // namespace cas
+
+extern "C" int cas_test_first_wait_spins(uint32_t spins) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return CAS_ERR_CUDA;
+  return cas::set_first_wait_spins(spins == 0xFFFFFFFFu ? cas::kSpinLimit : spins);
+}
 
 extern "C" int cas_device_status(void* stream) {
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return CAS_ERR_CUDA;

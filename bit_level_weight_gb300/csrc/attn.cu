@@ -25,7 +25,6 @@
 
 #include <algorithm>
 #include <cmath>
-#include <mutex>
 
 #include "kvview.cuh"
 #include "lanedec.cuh"
@@ -922,21 +921,14 @@ namespace {
 constexpr uint64_t kStaticScratchBytes = 8ull << 20;  // 8 MiB
 static __device__ __align__(256) unsigned char g_attn_scratch[kStaticScratchBytes];
 
-// Device address of g_attn_scratch on the current device. The host symbol is
-// only a stand-in, so the address is looked up once per device (with that
-// device current) and cached.
+// Device address of g_attn_scratch in the current context. The host symbol is
+// only a stand-in, so the address is looked up on every call: a context that
+// was rebuilt (cudaDeviceReset) or another context on the same device holds
+// the array at another address.
 int static_scratch(void** out) {
-  static std::mutex mu;
-  static void* addr[128] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return CAS_ERR_CUDA;
-  std::lock_guard<std::mutex> g(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || !p) return CAS_ERR_CUDA;
-    addr[dev] = p;
-  }
-  *out = addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || !p) return CAS_ERR_CUDA;
+  *out = p;
   return CAS_OK;
 }
 
@@ -948,11 +940,12 @@ extern "C" int cas_draft_attn_decode_noalloc(const cas_kv* const* kv, int batch,
   if (!kv || batch < 1 || batch > kMaxBatch || n_q_heads < 1) return CAS_ERR_INVALID;
   int64_t Tm = 0;
   for (int i = 0; i < batch; ++i) {
-    if (!kv[i]) return CAS_ERR_INVALID;
+    const int s = check_kv(kv[i]);  // the same descriptor errors as the workspace version
+    if (s) return s;
     Tm = std::max(Tm, kv[i]->max_tokens);
   }
-  uint64_t need = cas_attn_workspace_bytes(batch, n_q_heads, 1, Tm);
-  if (need == 0 || need > kStaticScratchBytes) return CAS_ERR_BUFFER;
+  const uint64_t need = cas_attn_workspace_bytes(batch, n_q_heads, 1, Tm);
+  if (need > kStaticScratchBytes) return CAS_ERR_BUFFER;
   void* ws = nullptr;
   int s = static_scratch(&ws);
   if (s) return s;

@@ -52,6 +52,9 @@ struct GemvArgs {
 // Set when a bounded wait on the x staging copy gave up (read by
 // cas_device_status).
 __device__ int g_gemv_wait_status = 0;
+// Spin limit of the first wait on the x staging copy (the wait after it keeps
+// the full limit); lowered only by the failure-detection test hook.
+__device__ uint32_t g_first_wait_spins = kSpinLimit;
 
 constexpr int kRecWords = CAS_SB * 32 + 2;  // staged records of a superblock (+pad)
 constexpr int kMaskWords = 40;                 // bit-reversed mask words (+zero pad)
@@ -104,7 +107,7 @@ __global__ void __launch_bounds__(kThreads) draft_gemv_kernel(GemvArgs a) {
   }
   for (int i = threadIdx.x; i < 256; i += kThreads) lut23[i] = (uint32_t)a.lut.v[i] << 23;
   if (lane < kMaskWords - 32) s_mw[32 + lane] = 0u;
-  bool ok = mbar_wait_bounded(bar, 0);
+  bool ok = mbar_wait_bounded(bar, 0, g_first_wait_spins);
   if (!__syncthreads_and(ok)) {
     if (threadIdx.x == 0) atomicExch(&g_gemv_wait_status, CAS_ERR_TIMEOUT);
     mbar_wait_bounded(bar, 0);  // let an in-flight copy land before the CTA exits
@@ -312,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 4) draft_gemv_fast_kernel(GemvArgs a
     bulk_g2s(xs, a.x, (uint32_t)xbytes, bar);
   }
   for (int i = threadIdx.x; i < 256; i += kThreads) lut8[i] = a.lut.v[i];
-  bool ok = mbar_wait_bounded(bar, 0);
+  bool ok = mbar_wait_bounded(bar, 0, g_first_wait_spins);
   if (!__syncthreads_and(ok)) {
     if (threadIdx.x == 0) atomicExch(&g_gemv_wait_status, CAS_ERR_TIMEOUT);
     mbar_wait_bounded(bar, 0);  // let an in-flight copy land before the CTA exits
@@ -446,7 +449,7 @@ __global__ void __launch_bounds__(kThreads) draft_gemv_runs_kernel(GemvArgs a) {
     bulk_g2s(xs, a.x, (uint32_t)xbytes, bar);
   }
   for (int i = threadIdx.x; i < 256; i += kThreads) lut8[i] = a.lut.v[i];
-  bool ok = mbar_wait_bounded(bar, 0);
+  bool ok = mbar_wait_bounded(bar, 0, g_first_wait_spins);
   if (!__syncthreads_and(ok)) {
     if (threadIdx.x == 0) atomicExch(&g_gemv_wait_status, CAS_ERR_TIMEOUT);
     mbar_wait_bounded(bar, 0);  // let an in-flight copy land before the CTA exits
@@ -553,7 +556,7 @@ __global__ void __launch_bounds__(kThreads) draft_gemv_fast2_kernel(GemvArgs a) 
     mbar_arrive_tx(bar, (uint32_t)xbytes);
     bulk_g2s(xs, a.x, (uint32_t)xbytes, bar);
   }
-  bool ok = mbar_wait_bounded(bar, 0);
+  bool ok = mbar_wait_bounded(bar, 0, g_first_wait_spins);
   if (!__syncthreads_and(ok)) {
     if (threadIdx.x == 0) atomicExch(&g_gemv_wait_status, CAS_ERR_TIMEOUT);
     mbar_wait_bounded(bar, 0);  // let an in-flight copy land before the CTA exits
@@ -1006,6 +1009,10 @@ int dispatch(const GemvArgs& a, int nvec, cudaStream_t st) {
 }
 
 }  // namespace
+
+int set_first_wait_spins(uint32_t spins) {
+  return cudaMemcpyToSymbol(g_first_wait_spins, &spins, sizeof(spins)) == cudaSuccess ? CAS_OK : CAS_ERR_CUDA;
+}
 
 int gemv_wait_status(bool clear) {
   int v = 0;

@@ -52,7 +52,7 @@ KvDev make_kv_dev(const cas_kv* kv) {
 }
 
 int check_kv(const cas_kv* kv) {
-  if (!kv || !kv->base || kv->n_kv_heads < 1 || kv->head_dim != CAS_BLK ||
+  if (!kv || !kv->base || kv->n_kv_heads < 1 || kv->head_dim != CAS_BLK || kv->max_tokens < 1 ||
       (kv->p.variant != 1 && kv->p.variant != 2) || kv->p.keep_per_block < 0 || kv->p.keep_per_block > CAS_BLK ||
       kv->p.mant_bits < 0 || kv->p.mant_bits > 7)
     return CAS_ERR_INVALID;

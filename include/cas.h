@@ -109,6 +109,15 @@ const char* cas_status_str(int status);
  * `stream`. Returns CAS_OK or CAS_ERR_TIMEOUT (CAS_ERR_CUDA on a runtime
  * error). */
 int cas_device_status(void* stream);
+/* Failure-detection test hook, not for production use. The draft GEMV
+ * kernels that stage x in shared memory by a bulk copy wait for that copy
+ * with a spin limit; on expiry they record CAS_ERR_TIMEOUT (read by
+ * cas_device_status), wait once more with the normal limit so the copy lands
+ * before the block exits, and write no output. This sets the limit of that
+ * first wait for later launches: 0 makes it give up at once, 0xFFFFFFFF
+ * restores the normal limit. Synchronises the device; returns CAS_OK or
+ * CAS_ERR_CUDA. */
+int cas_test_first_wait_spins(uint32_t spins);
 int32_t cas_keep_from_ratio(double ratio);
 /* Device-side scratch that cas_encode_weights_plan / cas_encode_weights need
  * for a tensor of N x K (histogram, per-superblock lengths, scan). */
@@ -296,9 +305,11 @@ int cas_draft_attn_decode(const cas_kv* const* kv, int batch, const uint16_t* q,
  * the library's device image (held by every GPU that loads the library until
  * the process exits); the call returns CAS_ERR_BUFFER, without launching, when
  * batch * n_q_heads * ceil(max_tokens / 256) * 520 bytes exceeds 8 MiB (e.g.
- * batch 1 with 32 query heads reaches 128K tokens). The first call on a device
- * looks up the array's device address with that device current; make that
- * first call before any stream capture. Every call uses the same array, so
+ * batch 1 with 32 query heads reaches 128K tokens). Every call looks up the
+ * array's device address in the calling thread's current context (the device
+ * and context the caller has made current), so a rebuilt context is
+ * followed; the first call in a context may load the library's device code,
+ * so make it before any stream capture. Every call uses the same array, so
  * calls that overlap on the GPU (on different streams, or on streams not
  * ordered with each other) race; calls ordered on one stream do not. The
  * array keeps the last call's partials; each call writes every partial it

@@ -298,3 +298,70 @@ def test_attention_errors(cas):
     q = torch.zeros(1, 17, 32, D, dtype=torch.int16, device="cuda")  # T > 16
     with pytest.raises(cas.CasError):
         cas.verify_attn([kv], q)
+
+
+# Caches sized for 20000 tokens hold ceil(20000 / 256) = 79 token chunks; with
+# 2 kv heads and one sequence every resident-CTA budget keeps at least 76 of
+# them, so each of the combine kernel's 32 warps merges two or more chunks
+# (the rescale of its running maximum is exercised). Live lengths leave many
+# chunks empty.
+MULTI_CHUNK_CAP = 20000
+
+
+def _long_cache(cas, H, n, variant, seed):
+    K, V = make_tokens(n, H, layer=4, seed=seed)
+    kv = new_cache(cas, H, MULTI_CHUNK_CAP, K, V, variant=variant)
+    for t0 in range(0, n, 2048):
+        kv.append(K[t0:t0 + 2048].cuda(), V[t0:t0 + 2048].cuda())
+    assert kv.status() == (n, 0)
+    return kv, K, V
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("Hq,n,n_tail", [(8, 4000, 3), (16, 1600, 0), (8, 9000, 1)])
+def test_draft_attention_multi_chunk_combine(cas, orc, variant, Hq, n, n_tail):
+    H = 2
+    kv, K, V = _long_cache(cas, H, n, variant, seed=200 + n)
+    q = synthetic.activations(1, Hq * D, seed=201).view(1, Hq, D)
+    tk = synthetic.activations(max(n_tail, 1), H * D, seed=202).view(1, max(n_tail, 1), H, D)[:, :n_tail]
+    tv = synthetic.activations(max(n_tail, 1), H * D, seed=203).view(1, max(n_tail, 1), H, D)[:, :n_tail]
+    o = cas.draft_attn_decode([kv], q.cuda(), tk.contiguous().cuda() if n_tail else None,
+                              tv.contiguous().cuda() if n_tail else None)
+    Kall = np.concatenate([oracle_draft_kv(orc, K, 64, 3, variant), np16(tk[0])], 0)
+    Vall = np.concatenate([oracle_draft_kv(orc, V, 64, 3, variant), np16(tv[0])], 0)
+    ref, nrm = orc.attention(np16(q), Kall, Vall)
+    check_attn(o, ref, nrm, f"draft attention, {n} tokens in a {MULTI_CHUNK_CAP}-token cache, v={variant}")
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+def test_draft_attention_tail_holds_the_maximum(cas, orc, variant):
+    """The bf16 draft tail scores far above every cached token, so the running
+    maximum comes from the tail and every chunk partial is rescaled by it."""
+    H, Hq, n = 2, 8, 3000
+    kv, K, V = _long_cache(cas, H, n, variant, seed=300)
+    q = synthetic.activations(1, Hq * D, seed=301).view(1, Hq, D)
+    qf = q.view(torch.int16).to(torch.int32).__lshift__(16).view(torch.float32)  # bf16 -> fp32
+    G = Hq // H
+    tail = torch.stack([qf[0, h * G:(h + 1) * G].sum(0) for h in range(H)])  # [H][D]
+    tk = synthetic.to_bits((2.0 * tail)[None, None])                       # [1][1][H][D]
+    tv = synthetic.activations(H, D, seed=302).view(1, 1, H, D)
+    o = cas.draft_attn_decode([kv], q.cuda(), tk.contiguous().cuda(), tv.contiguous().cuda())
+    Kall = np.concatenate([oracle_draft_kv(orc, K, 64, 3, variant), np16(tk[0])], 0)
+    Vall = np.concatenate([oracle_draft_kv(orc, V, 64, 3, variant), np16(tv[0])], 0)
+    ref, nrm = orc.attention(np16(q), Kall, Vall)
+    s_tail = (np.asarray(orc.bf16_to_f64(np16(q)))[0].reshape(H, G, D) *
+              np.asarray(orc.bf16_to_f64(np16(tk)))[0, 0][:, None, :]).sum(-1)
+    s_cache = np.einsum("thd,hgd->thg", orc.bf16_to_f64(Kall[:-1]), orc.bf16_to_f64(np16(q))[0].reshape(H, G, D))
+    assert (s_tail > s_cache.max(0)).all()  # the tail really holds the maximum
+    check_attn(o, ref, nrm, f"draft attention with a dominant tail, v={variant}")
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("n,T", [(5000, 5), (2100, 14)])
+def test_verify_attention_multi_chunk_combine(cas, orc, variant, n, T):
+    H, Hq = 2, 8
+    kv, K, V = _long_cache(cas, H, n, variant, seed=400 + n)
+    q = synthetic.activations(T, Hq * D, seed=401).view(1, T, Hq, D)
+    o = cas.verify_attn([kv], q.cuda())
+    ref, nrm = orc.attention(np16(q[0]), np16(K), np16(V), causal_new=T)
+    check_attn(o[0], ref, nrm, f"verify attention, {n} tokens in a {MULTI_CHUNK_CAP}-token cache, v={variant}")

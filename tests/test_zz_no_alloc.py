@@ -34,17 +34,36 @@ def cas():
     return cas
 
 
-def _caches(cas, lens, H, seed):
+def _caches(cas, lens, H, seed, max_tokens=None):
+    """One cache per entry of lens holding that many tokens (0 allowed),
+    sized for max_tokens (default: its length + 64)."""
     caches = []
     for b, T in enumerate(lens):
         sk, sv = synthetic.kv_scales(b, H, 0), synthetic.kv_scales(b, H, 1)
-        K = synthetic.kv_tokens(T, H, seed=seed + 2 * b, scales=sk).cuda()
-        V = synthetic.kv_tokens(T, H, seed=seed + 2 * b + 1, scales=sv).cuda()
-        kv = cas.KVCache(H, T + 64, cas.params(1, 64, 3), K[:16].contiguous(), V[:16].contiguous())
-        kv.append(K, V)
+        K = synthetic.kv_tokens(max(T, 16), H, seed=seed + 2 * b, scales=sk).cuda()
+        V = synthetic.kv_tokens(max(T, 16), H, seed=seed + 2 * b + 1, scales=sv).cuda()
+        cap = max_tokens if max_tokens is not None else T + 64
+        kv = cas.KVCache(H, cap, cas.params(1, 64, 3), K[:16].contiguous(), V[:16].contiguous())
+        if T:
+            kv.append(K[:T].contiguous(), V[:T].contiguous())
         assert kv.status() == (T, 0)
         caches.append(kv)
     return caches
+
+
+def _check_against_workspace_version(cas, caches, Hq, H, seed, what):
+    B = len(caches)
+    q = synthetic.activations(B, Hq * D, seed=seed).view(B, Hq, D).cuda()
+    tk = synthetic.activations(B * 3, H * D, seed=seed + 10).view(B, 3, H, D).cuda()
+    tv = synthetic.activations(B * 3, H * D, seed=seed + 20).view(B, 3, H, D).cuda()
+    ref = cas.draft_attn_decode(caches, q, tk, tv)
+    out = torch.full_like(ref, float("nan"))
+    assert _noalloc_abi(cas, caches, q, tk, tv, out) == 0
+    torch.cuda.synchronize()
+    r, o = ref.double().cpu().numpy(), out.double().cpu().numpy()
+    assert np.isfinite(o).all(), what
+    err = np.abs(o - r)
+    assert (err <= TOL * np.abs(r) + 1e-6).all(), f"{what}: worst {err.max():.3g}"
 
 
 def _noalloc_abi(cas, caches, q, tk, tv, out):
@@ -76,6 +95,42 @@ def test_noalloc_matches_workspace_version_two_calls(cas):
         assert np.isfinite(o).all(), f"call {call}"
         err = np.abs(o - r)
         assert (err <= TOL * np.abs(r) + 1e-6).all(), f"call {call}: worst {err.max():.3g}"
+
+
+def test_noalloc_large_call_then_smaller_layout(cas):
+    """A call that fills much of the array (batch 2, 24 chunks per head) and
+    then one with another chunk count and stride, one of whose sequences has
+    no cached tokens: the second call must read none of the first call's
+    partials."""
+    H, Hq = 8, 32
+    big = _caches(cas, (5000, 4100), H, seed=70, max_tokens=6000)
+    _check_against_workspace_version(cas, big, Hq, H, seed=11, what="large call")
+    small = _caches(cas, (0, 200), H, seed=80, max_tokens=300)
+    _check_against_workspace_version(cas, small, Hq, H, seed=12, what="smaller call after it")
+    one = _caches(cas, (130,), H, seed=85)
+    _check_against_workspace_version(cas, one, 16, H, seed=13, what="batch 1, 16 query heads")
+
+
+def test_noalloc_rejects_invalid_descriptor_like_workspace_version(cas):
+    H = 8
+    good = _caches(cas, (40,), H, seed=3)[0]
+    bad = cas.cas_kv.from_buffer_copy(bytes(good.desc))
+    bad.max_tokens = 0
+    q = torch.zeros(1, 32, D, dtype=torch.int16, device="cuda")
+    out = torch.zeros(1, 32, D, dtype=torch.float32, device="cuda")
+    f = cas.lib().cas_draft_attn_decode_noalloc
+    P = ctypes.c_void_p
+    f.argtypes = [P, ctypes.c_int, P, ctypes.c_int, P, P, ctypes.c_int, P, P]
+    f.restype = ctypes.c_int
+    arr = (ctypes.POINTER(cas.cas_kv) * 1)(ctypes.pointer(bad))
+    st = torch.cuda.current_stream().cuda_stream
+    got = f(ctypes.addressof(arr), 1, q.data_ptr(), 32, None, None, 0, out.data_ptr(), st)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    g = cas.lib().cas_draft_attn_decode
+    g.argtypes = [P, ctypes.c_int, P, ctypes.c_int, P, P, ctypes.c_int, P, P, ctypes.c_uint64, P]
+    g.restype = ctypes.c_int
+    want = g(ctypes.addressof(arr), 1, q.data_ptr(), 32, None, None, 0, out.data_ptr(), ws.data_ptr(), ws.numel(), st)
+    assert got == want == -1  # CAS_ERR_INVALID
 
 
 def test_noalloc_rejects_oversized_request(cas):
