@@ -19,6 +19,7 @@
 #include "lanedec.cuh"
 #include "mma.cuh"
 #include "sbdecode.cuh"
+#include "wordlane.cuh"
 
 namespace cas {
 namespace {
@@ -53,6 +54,7 @@ __host__ __device__ constexpr int scratch_warp() {
   return (((int)sizeof(TileStage) > generic ? (int)sizeof(TileStage) : generic) + 15) & ~15;
 }
 static_assert(scratch_warp<1>() % 16 == 0 && alignof(TileStage) <= 16, "per-warp scratch alignment");
+static_assert(scratch_warp<1>() >= (int)sizeof(WordTileStage), "word decoder stage fits");
 static_assert(scratch_warp<2>() >= (int)sizeof(TileStage2) && alignof(TileStage2) <= 16, "Cassandra-2 stage fits");
 static_assert(kWarps * scratch_warp<1>() >= kWarps * 256 * 4, "warp partials fit in the scratch");
 
@@ -101,9 +103,9 @@ __global__ void __launch_bounds__(kThreads, 4) verify_gemm_kernel(GemmArgs a) {
                                        kBlkStride, lane);
         } else if (MODE == 1) {
           const uint32_t a0 = __ldg(w.sidx + s), a1 = __ldg(w.sidx + s + 1);
-          done = lane_sb_tile<true>(w.mask + gb0 * 4, w.ssm + gb0 * 8, w.vlo + gb0 * 8, w.vpr + gb0 * 16,
-                                    w.sexp + a0, (int)(a1 - a0), w.vexp + v0, (int)(v1 - v0), s_lut, ts,
-                                    tile + r * kTileStride, kBlkStride, lane);
+          done = word_tile<true>(w.mask + gb0 * 4, w.ssm + gb0 * 8, w.vlo + gb0 * 8, w.vpr + gb0 * 16,
+                                 w.sexp + a0, (int)(a1 - a0), w.vexp + v0, (int)(v1 - v0), s_lut,
+                                 *reinterpret_cast<WordTileStage*>(wscr), tile + r * kTileStride, kBlkStride, lane);
         } else {
           const uint32_t a0 = __ldg(w.sidx + s), a1 = __ldg(w.sidx + s + 1);
           done = runs_sb_tile<true>(w.mask + gb0 * 4, w.ssm + gb0 * w.rec_sm, w.rec_sm, w.vlo + gb0 * w.rec_lo,

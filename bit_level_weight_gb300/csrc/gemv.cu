@@ -33,6 +33,7 @@
 #include "common.cuh"
 #include "lanedec.cuh"
 #include "sbdecode.cuh"
+#include "wordlane.cuh"
 
 namespace cas {
 namespace {
@@ -714,46 +715,6 @@ __device__ __forceinline__ float lds_f32(uint32_t a) {
   asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
   return v;
 }
-__device__ __forceinline__ uint32_t mad_u32(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-// trailing zeros (32 for 0)
-__device__ __forceinline__ int tzcnt(uint32_t w) { return w ? 31 - __clz(w & (0u - w)) : 32; }
-
-// sel8[b*8 + i] = MSB-first bit index of the (i+1)-th '1' of byte b (0 when
-// b has fewer ones), built at compile time.
-struct Sel8Table {
-  uint8_t v[2048];
-};
-constexpr Sel8Table make_sel8() {
-  Sel8Table t{};
-  for (int b = 0; b < 256; ++b) {
-    int seen = 0;
-    for (int q = 7; q >= 0; --q)
-      if ((b >> q) & 1) t.v[b * 8 + seen++] = (uint8_t)(7 - q);
-  }
-  return t;
-}
-__device__ const Sel8Table g_sel8 = make_sel8();
-
-// Bit index, counted from the MSB, of the r-th '1' (1-based) of w: two
-// popcount halvings, then the byte-select table.
-__device__ __forceinline__ int select_msb(uint32_t w, int r, const uint8_t* sel8) {
-  const uint32_t hi = w >> 16;
-  const int c1 = __popc(hi);
-  const bool h = r <= c1;
-  const uint32_t w16 = h ? hi : (w & 0xFFFFu);
-  r = h ? r : r - c1;
-  const uint32_t hb = w16 >> 8;
-  const int c2 = __popc(hb);
-  const bool hh = r <= c2;
-  const uint32_t b = hh ? hb : (w16 & 0xFFu);
-  r = hh ? r : r - c2;
-  const int base = (h ? 0 : 16) + (hh ? 0 : 8);
-  return base + __ldg(sel8 + b * 8 + ((r - 1) & 7));
-}
 
 // The generic superblock decoder for what the word walk cannot take. Kept out
 // of line so that its registers do not count against the fast path.
@@ -783,7 +744,6 @@ template <int NV>
 __global__ void __launch_bounds__(kThreads, 8) draft_gemv_word_kernel(GemvArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint8_t lut8[256];  // exponent by rank
-  const uint8_t* sel8 = g_sel8.v;
   const WView& w = a.w;
   const int K = (int)w.K;
   const int xfl = word_x_floats(K);
@@ -876,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 8) draft_gemv_word_kernel(GemvArgs a
       const bool in0 = T <= q0;
       const uint32_t wsel = in0 ? x0 : x1;
       const int rr1 = T - (in0 ? q0 - __popc(x0) : q0);
-      const int start = T > 0 ? 32 * (2 * l + (in0 ? 0 : 1)) + select_msb(wsel, max(rr1, 1), sel8) + 1 : 0;
+      const int start = T > 0 ? 32 * (2 * l + (in0 ? 0 : 1)) + select_msb(wsel, max(rr1, 1)) + 1 : 0;
       int nxt = __shfl_down_sync(CAS_FULL, start, 1);
       if (lane == 31) nxt = endbit;
       const int span = nxt - start;
@@ -911,19 +871,19 @@ __global__ void __launch_bounds__(kThreads, 8) draft_gemv_word_kernel(GemvArgs a
           H = __funnelshift_l(ws.st[hw + 1], ws.st[hw], sh);
           Lw = __funnelshift_l(ws.st[hw + 2], ws.st[hw + 1], sh);
         }
-        const int p = __clz(M);  // 32 once the word is exhausted: zero pad
-        M &= ~(0x80000000u >> (p & 31));
-        const int r = __clz(H);  // <= 30 for every code of a checked stream
+        const uint32_t p = __clz(M);  // 32 once the word is exhausted: zero pad
+        M &= ~shr32(0x80000000u, p);  // p = 32 clears nothing
+        const uint32_t r = __clz(H);  // <= 30 for every code of a checked stream
         const uint32_t e = lut8[r];
-        const int nb = r + 1;
-        H = __funnelshift_l(Lw, H, nb);
-        Lw = Lw << (nb & 31);
-        used += nb;
+        const uint32_t nb = r + 1u;
+        H = shfl_wrap(Lw, H, nb);
+        Lw = shl32(Lw, nb);
+        used += (int)nb;
         const uint32_t src = (i & 1) ? fo[i >> 3] : fe[i >> 3];
         const int by = (i & 7) >> 1;
         const uint32_t A = __byte_perm(src, 0u, (by << 12) | (by << 8) | 0x44);
-        const float val = __uint_as_float(mad_u32(e, 0x800000u, A & 0x80700000u));
-        const uint32_t xp = mad_u32((uint32_t)p, 4u, xa);
+        const float val = __uint_as_float(mad32(e, 0x800000u, A & 0x80700000u));
+        const uint32_t xp = mad32((uint32_t)p, 4u, xa);
 #pragma unroll
         for (int q = 0; q < NV; ++q) part[q] = fmaf(val, lds_f32(xp + 4u * (uint32_t)(q * xfl)), part[q]);
       }
