@@ -92,6 +92,12 @@ def lib() -> ctypes.CDLL:
             "cas_verify_attn": ([P, i32, P, i32, i32, P, P, u64, P], i32),
             "cas_device_status": ([P], i32),
             "cas_test_first_wait_spins": ([ctypes.c_uint32], i32),
+            "cas_add_rmsnorm": ([P, P, i32, i32, P, ctypes.c_float, P, P], i32),
+            "cas_rope_split": ([P, i32, i32, i32, i64, i32, ctypes.c_double, P, P, i64, P, i64, P], i32),
+            "cas_silu_mul": ([P, i32, i32, P, P], i32),
+            "cas_f32_to_bf16": ([P, i64, P, P], i32),
+            "cas_argmax": ([P, i32, i64, P, P], i32),
+            "cas_embed": ([P, i32, P, i64, i32, P, P], i32),
             "cas_draft_attn_decode_noalloc": ([P, i32, P, i32, P, P, i32, P, P], i32),
         }
         for name, (args, res) in sig.items():
@@ -485,3 +491,73 @@ def prepare_verify_attn(kvs, q, out, workspace, stream=None):
                    stream or torch.cuda.current_stream())
     call.keep = (arr, kvs, q, out, workspace)
     return call
+
+
+# ------------------------------------------------------------------ forward-pass glue
+def add_rmsnorm(x: torch.Tensor, y: torch.Tensor | None, gamma: torch.Tensor, eps: float = 1e-5,
+                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """x += y (if given), returns bf16 rmsnorm(x) * gamma. x, y: fp32 [rows][dim]."""
+    rows, dim = x.shape
+    if x.dtype != torch.float32 or (y is not None and (y.dtype != torch.float32 or tuple(y.shape) != (rows, dim))):
+        raise ValueError("add_rmsnorm: x and y must be fp32 of one shape")
+    gamma = _bits(gamma)
+    _shape(gamma, (dim,), "gamma")
+    if out is None:
+        out = torch.empty(rows, dim, dtype=torch.int16, device=x.device)
+    _out(out, rows * dim, (torch.int16, torch.bfloat16), "out")
+    _check(lib().cas_add_rmsnorm(_ptr(x), _ptr(y), rows, dim, _ptr(gamma), float(eps), _ptr(out), _stream(stream)),
+           "cas_add_rmsnorm")
+    return out
+
+
+def rope_split(qkv: torch.Tensor, n_q_heads: int, n_kv_heads: int, pos0: int, rows_per_seq: int | None = None,
+               theta: float = 500000.0, stream=None):
+    """Returns (q, k, v) bf16 bit patterns [rows][H][128] from fp32 qkv [rows][(Hq+2Hkv)*128]."""
+    rows = qkv.shape[0]
+    _shape(qkv, (rows, (n_q_heads + 2 * n_kv_heads) * 128), "qkv")
+    if qkv.dtype != torch.float32:
+        raise ValueError("rope_split: qkv must be fp32")
+    dev = qkv.device
+    q = torch.empty(rows, n_q_heads, 128, dtype=torch.int16, device=dev)
+    k = torch.empty(rows, n_kv_heads, 128, dtype=torch.int16, device=dev)
+    v = torch.empty(rows, n_kv_heads, 128, dtype=torch.int16, device=dev)
+    _check(lib().cas_rope_split(_ptr(qkv), rows, n_q_heads, n_kv_heads, pos0, rows_per_seq or rows, float(theta),
+                                _ptr(q), _ptr(k), n_kv_heads * 128, _ptr(v), n_kv_heads * 128, _stream(stream)),
+           "cas_rope_split")
+    return q, k, v
+
+
+def silu_mul(gate_up: torch.Tensor, stream=None) -> torch.Tensor:
+    rows, two_f = gate_up.shape
+    if gate_up.dtype != torch.float32 or two_f % 2:
+        raise ValueError("silu_mul: fp32 [rows][2 ffn] expected")
+    out = torch.empty(rows, two_f // 2, dtype=torch.int16, device=gate_up.device)
+    _check(lib().cas_silu_mul(_ptr(gate_up), rows, two_f // 2, _ptr(out), _stream(stream)), "cas_silu_mul")
+    return out
+
+
+def f32_to_bf16(x: torch.Tensor, stream=None) -> torch.Tensor:
+    if x.dtype != torch.float32:
+        raise ValueError("f32_to_bf16: fp32 input expected")
+    out = torch.empty(x.shape, dtype=torch.int16, device=x.device)
+    _check(lib().cas_f32_to_bf16(_ptr(x), x.numel(), _ptr(out), _stream(stream)), "cas_f32_to_bf16")
+    return out
+
+
+def argmax(logits: torch.Tensor, stream=None) -> torch.Tensor:
+    rows, V = logits.shape
+    if logits.dtype != torch.float32:
+        raise ValueError("argmax: fp32 logits expected")
+    out = torch.empty(rows, dtype=torch.int32, device=logits.device)
+    _check(lib().cas_argmax(_ptr(logits), rows, V, _ptr(out), _stream(stream)), "cas_argmax")
+    return out
+
+
+def embed(tokens: torch.Tensor, table: torch.Tensor, stream=None) -> torch.Tensor:
+    if tokens.dtype != torch.int32:
+        raise ValueError("embed: int32 token ids expected")
+    table = _bits(table)
+    V, dim = table.shape
+    x = torch.empty(tokens.numel(), dim, dtype=torch.float32, device=table.device)
+    _check(lib().cas_embed(_ptr(tokens), tokens.numel(), _ptr(table), V, dim, _ptr(x), _stream(stream)), "cas_embed")
+    return x

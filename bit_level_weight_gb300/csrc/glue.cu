@@ -1,0 +1,216 @@
+// glue.cu - the transformer operations between the split's matrix products in
+// one decode step of the evaluated models (Llama-3-8B, Qwen3-8B: Cassandra
+// paper, evaluation; Cassandra blog review, section 4): residual add fused with
+// RMSNorm, the split of the fused QKV product with rotary position embedding,
+// SiLU(gate) * up, fp32 -> bf16, greedy argmax and the embedding lookup.
+// They turn the per-matrix entry points into a data-dependent forward: every
+// kernel reads what the previous one wrote.
+//
+// Numerics: fp32 arithmetic, bf16 outputs rounded to nearest even; the rotary
+// angle p * theta^(-2i/D) is formed and reduced in double precision and its
+// sine and cosine taken in double, so long contexts lose no accuracy there.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "common.cuh"
+
+namespace cas {
+namespace {
+
+__device__ __forceinline__ uint16_t to_bf16(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+
+// ---------------------------------------------------------------- add + RMSNorm
+// x[r] += y[r] (when y is given), then out[r] = bf16(x[r] / sqrt(mean(x[r]^2) + eps) * gamma).
+constexpr int kNormThreads = 256;
+__global__ void __launch_bounds__(kNormThreads) add_rmsnorm_kernel(float* __restrict__ x, const float* __restrict__ y,
+                                                                   int dim, const uint16_t* __restrict__ gamma,
+                                                                   float eps, uint16_t* __restrict__ out) {
+  __shared__ float red[kNormThreads / 32];
+  const int64_t r = blockIdx.x;
+  float* xr = x + r * dim;
+  const float* yr = y ? y + r * dim : nullptr;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < dim; i += kNormThreads) {
+    float v = xr[i];
+    if (yr) {
+      v += yr[i];
+      xr[i] = v;
+    }
+    ss = fmaf(v, v, ss);
+  }
+  ss = warp_sumf(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kNormThreads / 32; ++w) tot += red[w];
+  const float inv = rsqrtf(tot / (float)dim + eps);
+  for (int i = threadIdx.x; i < dim; i += kNormThreads) out[r * dim + i] = to_bf16(xr[i] * inv * bf2f(gamma[i]));
+}
+
+// ---------------------------------------------------------------- QKV split + rotary embedding
+// qkv: fp32 [rows][(Hq + 2 Hkv) * 128] (q heads, then k heads, then v heads).
+// Pairs (i, i + 64) of a q or k head rotate by angle p * theta^(-i/64):
+// (a, b) -> (a cos - b sin, b cos + a sin); p = pos0 + row % rows_per_seq.
+__global__ void rope_split_kernel(const float* __restrict__ qkv, int Hq, int Hkv, int64_t pos0, int rows_per_seq,
+                                  double log_theta, uint16_t* __restrict__ q, uint16_t* __restrict__ k,
+                                  int64_t k_stride, uint16_t* __restrict__ v, int64_t v_stride) {
+  const int r = blockIdx.y;
+  const int H = Hq + 2 * Hkv;
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;  // (head, pair)
+  if (t >= H * 64) return;
+  const int h = t >> 6, i = t & 63;
+  const float* src = qkv + ((int64_t)r * H + h) * CAS_BLK;
+  const float a = src[i], b = src[i + 64];
+  if (h >= Hq + Hkv) {  // v: no rotation
+    uint16_t* d = v + (int64_t)r * v_stride + (int64_t)(h - Hq - Hkv) * CAS_BLK;
+    d[i] = to_bf16(a);
+    d[i + 64] = to_bf16(b);
+    return;
+  }
+  const double p = (double)(pos0 + r % rows_per_seq);
+  const double ang = p * exp(-log_theta * (double)i / 64.0);
+  double sd, cd;
+  sincos(fmod(ang, 6.283185307179586476925286766559), &sd, &cd);
+  const float s = (float)sd, c = (float)cd;
+  uint16_t* d = h < Hq ? q + ((int64_t)r * Hq + h) * CAS_BLK : k + (int64_t)r * k_stride + (int64_t)(h - Hq) * CAS_BLK;
+  d[i] = to_bf16(fmaf(a, c, -b * s));
+  d[i + 64] = to_bf16(fmaf(b, c, a * s));
+}
+
+// ---------------------------------------------------------------- SiLU(gate) * up
+__global__ void silu_mul_kernel(const float* __restrict__ gu, int F, int64_t n, uint16_t* __restrict__ out) {
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = t / F;
+    const int j = (int)(t - r * F);
+    const float g = gu[r * 2 * F + j], u = gu[r * 2 * F + F + j];
+    out[t] = to_bf16(g / (1.f + expf(-g)) * u);
+  }
+}
+
+__global__ void to_bf16_kernel(const float* __restrict__ in, int64_t n, uint16_t* __restrict__ out) {
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x)
+    out[t] = to_bf16(in[t]);
+}
+
+// ---------------------------------------------------------------- greedy argmax (ties to the lower index)
+constexpr int kArgThreads = 1024;
+__global__ void __launch_bounds__(kArgThreads) argmax_kernel(const float* __restrict__ logits, int64_t V,
+                                                             int32_t* __restrict__ out) {
+  __shared__ float bv[kArgThreads / 32];
+  __shared__ int64_t bi[kArgThreads / 32];
+  const float* lr = logits + (int64_t)blockIdx.x * V;
+  float best = -INFINITY;
+  int64_t idx = V;  // none yet
+  for (int64_t i = threadIdx.x; i < V; i += kArgThreads) {
+    const float v = lr[i];
+    if (v > best) {  // strictly greater: the first (lowest) index of a tie stays
+      best = v;
+      idx = i;
+    }
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) {
+    const float ov = __shfl_xor_sync(CAS_FULL, best, d);
+    const int64_t oi = __shfl_xor_sync(CAS_FULL, idx, d);
+    if (ov > best || (ov == best && oi < idx)) {
+      best = ov;
+      idx = oi;
+    }
+  }
+  if ((threadIdx.x & 31) == 0) {
+    bv[threadIdx.x >> 5] = best;
+    bi[threadIdx.x >> 5] = idx;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kArgThreads / 32; ++w)
+      if (bv[w] > best || (bv[w] == best && bi[w] < idx)) {
+        best = bv[w];
+        idx = bi[w];
+      }
+    out[blockIdx.x] = (int32_t)(idx < V ? idx : 0);
+  }
+}
+
+// ---------------------------------------------------------------- embedding lookup
+__global__ void embed_kernel(const int32_t* __restrict__ tok, const uint16_t* __restrict__ table, int64_t V, int dim,
+                             float* __restrict__ x) {
+  const int r = blockIdx.y;
+  const int64_t id = tok[r];
+  const int64_t row = id < 0 ? 0 : (id >= V ? V - 1 : id);  // an invalid id reads a valid row
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < dim; i += gridDim.x * blockDim.x)
+    x[(int64_t)r * dim + i] = bf2f(table[row * dim + i]);
+}
+
+int grid1d(int64_t n, int threads) {
+  const int64_t g = (n + threads - 1) / threads;
+  return (int)std::min<int64_t>(std::max<int64_t>(g, 1), (int64_t)sm_count() * 8);
+}
+
+}  // namespace
+}  // namespace cas
+
+using namespace cas;
+
+extern "C" int cas_add_rmsnorm(float* x, const float* y, int rows, int dim, const uint16_t* gamma, float eps,
+                               uint16_t* out, void* stream) {
+  if (rows < 0 || dim < 1 || !(eps >= 0.f)) return CAS_ERR_INVALID;
+  if (rows == 0) return CAS_OK;
+  if (!x || !gamma || !out) return CAS_ERR_INVALID;
+  add_rmsnorm_kernel<<<rows, kNormThreads, 0, (cudaStream_t)stream>>>(x, y, dim, gamma, eps, out);
+  return launch_status();
+}
+
+extern "C" int cas_rope_split(const float* qkv, int rows, int n_q_heads, int n_kv_heads, int64_t pos0,
+                              int rows_per_seq, double theta, uint16_t* q, uint16_t* k, int64_t k_row_stride,
+                              uint16_t* v, int64_t v_row_stride, void* stream) {
+  if (rows < 0 || n_q_heads < 1 || n_kv_heads < 1 || pos0 < 0 || rows_per_seq < 1 || !(theta > 1.0))
+    return CAS_ERR_INVALID;
+  if (rows == 0) return CAS_OK;
+  if (!qkv || !q || !k || !v || k_row_stride < (int64_t)n_kv_heads * CAS_BLK ||
+      v_row_stride < (int64_t)n_kv_heads * CAS_BLK)
+    return CAS_ERR_INVALID;
+  const int pairs = (n_q_heads + 2 * n_kv_heads) * 64;
+  dim3 g((pairs + 255) / 256, rows);
+  rope_split_kernel<<<g, 256, 0, (cudaStream_t)stream>>>(qkv, n_q_heads, n_kv_heads, pos0, rows_per_seq,
+                                                         std::log(theta), q, k, k_row_stride, v, v_row_stride);
+  return launch_status();
+}
+
+extern "C" int cas_silu_mul(const float* gate_up, int rows, int ffn, uint16_t* out, void* stream) {
+  if (rows < 0 || ffn < 1) return CAS_ERR_INVALID;
+  if (rows == 0) return CAS_OK;
+  if (!gate_up || !out) return CAS_ERR_INVALID;
+  const int64_t n = (int64_t)rows * ffn;
+  silu_mul_kernel<<<grid1d(n, 256), 256, 0, (cudaStream_t)stream>>>(gate_up, ffn, n, out);
+  return launch_status();
+}
+
+extern "C" int cas_f32_to_bf16(const float* in, int64_t n, uint16_t* out, void* stream) {
+  if (n < 0) return CAS_ERR_INVALID;
+  if (n == 0) return CAS_OK;
+  if (!in || !out) return CAS_ERR_INVALID;
+  to_bf16_kernel<<<grid1d(n, 256), 256, 0, (cudaStream_t)stream>>>(in, n, out);
+  return launch_status();
+}
+
+extern "C" int cas_argmax(const float* logits, int rows, int64_t vocab, int32_t* out, void* stream) {
+  if (rows < 0 || vocab < 1 || vocab > 0x7FFFFFFF) return CAS_ERR_INVALID;
+  if (rows == 0) return CAS_OK;
+  if (!logits || !out) return CAS_ERR_INVALID;
+  argmax_kernel<<<rows, kArgThreads, 0, (cudaStream_t)stream>>>(logits, vocab, out);
+  return launch_status();
+}
+
+extern "C" int cas_embed(const int32_t* tokens, int rows, const uint16_t* table, int64_t vocab, int dim, float* x,
+                         void* stream) {
+  if (rows < 0 || vocab < 1 || dim < 1) return CAS_ERR_INVALID;
+  if (rows == 0) return CAS_OK;
+  if (!tokens || !table || !x) return CAS_ERR_INVALID;
+  dim3 g((dim + 255) / 256, rows);
+  embed_kernel<<<g, 256, 0, (cudaStream_t)stream>>>(tokens, table, vocab, dim, x);
+  return launch_status();
+}

@@ -327,6 +327,55 @@ int cas_draft_attn_decode_noalloc(const cas_kv* const* kv, int batch, const uint
 int cas_verify_attn(const cas_kv* const* kv, int batch, const uint16_t* q, int T, int n_q_heads,
                     float* o, void* workspace, uint64_t workspace_bytes, void* stream);
 
+/* ---- Forward-pass glue. The operations between the matrix products of one
+ * decode step of the models the method is evaluated on (Llama-3-8B,
+ * Qwen3-8B: Cassandra paper, evaluation; Cassandra blog review, section 4),
+ * so that a step runs as a data-dependent forward through this library. All
+ * asynchronous on `stream`; fp32 arithmetic; bf16 outputs rounded to nearest
+ * even; CAS_ERR_INVALID for a null pointer or a size out of range (nothing
+ * launched), CAS_ERR_CUDA for a launch error; rows == 0 does nothing. */
+
+/* Residual add fused with RMSNorm: for each of `rows` rows of dim fp32,
+ * x += y (skipped when y is NULL), then
+ * out = bf16(x / sqrt(mean(x^2) + eps) * gamma). x: fp32 [rows][dim], updated
+ * in place; y: fp32 [rows][dim] or NULL; gamma: bf16 [dim]; out: bf16
+ * [rows][dim]. */
+int cas_add_rmsnorm(float* x, const float* y, int rows, int dim, const uint16_t* gamma, float eps,
+                    uint16_t* out, void* stream);
+
+/* Split of a fused QKV product with rotary position embedding (head_dim
+ * 128). qkv: fp32 [rows][(n_q_heads + 2 n_kv_heads) * 128], q heads then k
+ * heads then v heads. Row r has position p = pos0 + r % rows_per_seq; in
+ * every q and k head the pair (i, i + 64), i < 64, turns by the angle
+ * p * theta^(-i/64): (a, b) -> (a cos - b sin, b cos + a sin), the angle
+ * formed in double precision. Outputs bf16: q [rows][n_q_heads][128]; k and v
+ * rows of n_kv_heads * 128 values at strides k_row_stride / v_row_stride
+ * elements (at least n_kv_heads * 128), so rows can land in a KV tail buffer.
+ * theta must exceed 1. */
+int cas_rope_split(const float* qkv, int rows, int n_q_heads, int n_kv_heads, int64_t pos0, int rows_per_seq,
+                   double theta, uint16_t* q, uint16_t* k, int64_t k_row_stride, uint16_t* v,
+                   int64_t v_row_stride, void* stream);
+
+/* out = bf16(silu(gate) * up) with silu(g) = g / (1 + exp(-g)); gate_up:
+ * fp32 [rows][2 ffn] (gate then up, the fused gate|up product); out: bf16
+ * [rows][ffn]. */
+int cas_silu_mul(const float* gate_up, int rows, int ffn, uint16_t* out, void* stream);
+
+/* out = bf16(in) for n values (e.g. an attention output before the output
+ * projection). */
+int cas_f32_to_bf16(const float* in, int64_t n, uint16_t* out, void* stream);
+
+/* Greedy decoding: out[r] = the lowest index of the largest of the `vocab`
+ * fp32 logits of row r (NaN never wins). logits: [rows][vocab]; out: int32
+ * [rows]. vocab at most 2^31 - 1. */
+int cas_argmax(const float* logits, int rows, int64_t vocab, int32_t* out, void* stream);
+
+/* Embedding lookup: x[r] = fp32(table[tokens[r]]); table: bf16 [vocab][dim];
+ * x: fp32 [rows][dim]. A token id outside [0, vocab) reads the nearest valid
+ * row (the device cannot report it). */
+int cas_embed(const int32_t* tokens, int rows, const uint16_t* table, int64_t vocab, int dim, float* x,
+              void* stream);
+
 #ifdef __cplusplus
 }
 #endif
