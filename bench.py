@@ -1,19 +1,22 @@
 #!/usr/bin/env python
 """Benchmark of the Cassandra bit-split hot path on GB300.
 
-One step = one self-speculative decode step of a Llama-3-8B-shaped decoder
-stack (32 layers, hidden 4096, FFN 14336, GQA 32q/8kv, head_dim 128) with
-random-init Student-t(4) bf16 weights split at keep 50% / 3 mantissa bits
+One step = one self-speculative decode step of a Llama-3-8B-shaped model (32
+layers, hidden 4096, FFN 14336, GQA 32q/8kv, head_dim 128, 128256-row LM head)
+with random-init Student-t(4) bf16 weights split at keep 50% / 3 mantissa bits
 (Cassandra-1), batch 1, draft length 4, and a compressed KV cache of 32K tokens
-(bf16 K/V ~ N(0,1) x LogNormal(0,0.5) channel scales):
-  4 draft forwards  : per layer draft GEMV (Wqkv), draft attention over the
-                      speculation KV + bf16 tail, draft GEMV (Wo, Wgate|up, Wdown);
-  1 verify forward  : per layer verify GEMM (T=5), online KV append of the 5
-                      tokens, verify attention, verify GEMMs;
-  then the 5 tokens are rolled back (fixed schedule: acceptance has no meaning
-  on random weights).
-Activations fed to each kernel are synthetic device vectors (the norm / RoPE /
-activation glue between kernels is not part of the measured path).
+(bf16 K/V ~ N(0,1) x LogNormal(0,0.5) channel scales), run as a data-dependent
+forward through the library's C ABI:
+  4 draft forwards : embedding of the previous token; per layer RMSNorm, draft
+                     GEMV Wqkv, RoPE into the bf16 draft tail, draft attention
+                     over the speculation KV + tail, draft GEMVs Wo, Wgate|up,
+                     Wdown with residual adds, RMSNorm and SiLU*mul between;
+                     final RMSNorm, draft LM head, argmax = the next token;
+  1 verify forward : the same over the exact weights for the 5 tokens (verify
+                     GEMMs, online KV append of the 5 tokens, verify attention);
+  then the caches are rolled back to the context (fixed schedule: acceptance
+  has no meaning on random weights); the verify's last token starts the next
+  step.
 
 Headline value: draft decode+GEMV GB/s over the algorithmic bytes of the
 speculation streams read (plus x read and y written), timed with CUDA events on
@@ -63,6 +66,8 @@ def parse():
     ap.add_argument("--sweep", action="store_true",
                     help="Cassandra-1 vs -2 over keep 20-60%% x mantissa 1-5 on the FFN matrices")
     ap.add_argument("--no-attn", action="store_true", help="weights only (no KV cache)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the other configurations (keep 30%%, Qwen3-8B step, 128K attention)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--micro", default=None,
@@ -140,99 +145,341 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------- CPU oracle baseline
 def cpu_baseline(seconds: float, keep: int, mant: int, variant: int = 1):
-    """Oracle draft decode + GEMV (plain C, one thread) on a bounded sample: one
-    1024x4096 Student-t(4) matrix of the same stack, repeated for ~`seconds`."""
+    """The oracle's draft decode + float64 GEMV (plain C) timed on the host
+    cores on a bounded sample of the same workload: a 1024x4096 Student-t(4)
+    matrix of the stack, split into one 1024/n-row slice per thread (each
+    slice encoded as its own tensor), repeated for about `seconds` - half the
+    time on one thread, half on every host core. value = speculation bytes
+    decoded per second with all cores; the one-thread figure is reported too."""
+    import concurrent.futures as cf
+
     import numpy as np
 
     import oracle
     import synthetic
+    oracle.build()
     N, K = 1024, 4096
     W = synthetic.t4_weight(N, K, seed=0).numpy().view(np.uint16)
     x = synthetic.activations(1, K, seed=1).numpy().view(np.uint16)
-    enc = oracle.encode(W, variant, keep, mant)
-    spec = enc.spec_bytes() + K * 2 + N * 4
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        d = oracle.decode(enc, False)
-        oracle.matvec(d, x)
-        reps += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": spec * reps / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{reps} x oracle draft decode + float64 GEMV of one 1024x4096 t4 matrix "
-                      f"(keep {keep}/128, m={mant}, Cassandra-{variant}), {dt:.1f} s"}
+    host = os.cpu_count() or 1
+
+    def timed(nthreads, budget):
+        rows = N // nthreads
+        parts = [oracle.encode(np.ascontiguousarray(W[i * rows:(i + 1) * rows]), variant, keep, mant)
+                 for i in range(nthreads)]
+        spec = sum(p.spec_bytes() + K * 2 + rows * 4 for p in parts)
+
+        def work(p):
+            oracle.matvec(oracle.decode(p, False), x)
+
+        reps, t0 = 0, time.perf_counter()
+        with cf.ThreadPoolExecutor(nthreads) as ex:
+            while True:
+                list(ex.map(work, parts))
+                reps += 1
+                if time.perf_counter() - t0 >= budget:
+                    break
+        dt = time.perf_counter() - t0
+        return spec * reps / dt / 1e9, reps, dt
+
+    one, r1, t1 = timed(1, seconds / 2)
+    nt = max(1, min(host, 64))
+    while N % nt:
+        nt -= 1
+    allc, rn, tn = timed(nt, seconds / 2)
+    return {"value": allc, "unit": "GB/s", "cores": nt, "host_cores": host, "kind": "oracle",
+            "single_thread_value": one,
+            "sample": f"oracle draft decode + float64 GEMV of one 1024x4096 t4 matrix (keep {keep}/128, m={mant}, "
+                      f"Cassandra-{variant}): {r1} passes on 1 thread in {t1:.1f} s, {rn} passes with the rows "
+                      f"split over {nt} threads in {tn:.1f} s"}
 
 
 # ---------------------------------------------------------------------- workload
 class Stack:
-    """Encoded Llama-3-8B-shaped stack plus its compressed KV caches."""
+    """Encoded decoder stack of one model shape (Student-t(4) bf16 weights,
+    Wq|Wk|Wv and Wgate|Wup fused), its RMSNorm weights, LM head, embedding
+    table and compressed KV caches filled to `ctx` tokens per sequence."""
 
-    def __init__(self, cas, args, dev):
+    def __init__(self, cas, dev, workload, layers, variant, keep, mant, ctx, batch, attn=True):
         import torch
 
         import synthetic
-        self.cas, self.args, self.dev = cas, args, dev
-        shp = dict(synthetic.LLAMA3_8B if args.workload == "llama3-8b" else synthetic.QWEN3_8B)
-        self.L = args.layers
-        self.vocab = shp.get("vocab", 0)
+        self.cas, self.dev = cas, dev
+        shp = dict(synthetic.LLAMA3_8B if workload == "llama3-8b" else synthetic.QWEN3_8B)
+        self.L, self.ctx, self.B = layers, ctx, batch
+        self.variant, self.keep, self.mant = variant, keep, mant
         h, f = shp["hidden"], shp["ffn"]
         self.hidden, self.ffn, self.nq, self.nkv, self.hd = h, f, shp["n_q"], shp["n_kv"], shp["head_dim"]
-        self.mats = []  # per layer: dict name -> EncodedWeights
+        self.vocab, self.theta = shp["vocab"], shp["rope_theta"]
+        self.mats, self.g1, self.g2 = [], [], []
         t0 = time.time()
         for layer in range(self.L):
-            names = synthetic.layer_matrices(shp)
-            raw = {}
-            for idx, (nm, N, K) in enumerate(names):
-                raw[nm] = synthetic.t4_weight(N, K, seed=layer * 16 + idx, device=dev)
-            fused = {
-                "qkv": torch.cat([raw["wq"], raw["wk"], raw["wv"]], 0),
-                "o": raw["wo"],
-                "gateup": torch.cat([raw["wgate"], raw["wup"]], 0),
-                "down": raw["wdown"],
-            }
+            raw = {nm: synthetic.t4_weight(N, K, seed=layer * 16 + idx, device=dev)
+                   for idx, (nm, N, K) in enumerate(synthetic.layer_matrices(shp))}
+            fused = {"qkv": torch.cat([raw["wq"], raw["wk"], raw["wv"]], 0), "o": raw["wo"],
+                     "gateup": torch.cat([raw["wgate"], raw["wup"]], 0), "down": raw["wdown"]}
             del raw
-            enc = {nm: cas.encode_weights(W, args.variant, args.keep, args.mant) for nm, W in fused.items()}
+            self.mats.append({nm: cas.encode_weights(W, variant, keep, mant) for nm, W in fused.items()})
             del fused
-            self.mats.append(enc)
-        self.lm = None
-        if self.vocab:
-            Wl = synthetic.t4_weight(self.vocab, h, seed=999_983, device=dev)
-            self.lm = cas.encode_weights(Wl, args.variant, args.keep, args.mant)
-            del Wl
+            self.g1.append(synthetic.norm_weight(h, seed=layer * 16 + 8, device=dev))
+            self.g2.append(synthetic.norm_weight(h, seed=layer * 16 + 9, device=dev))
+        self.gf = synthetic.norm_weight(h, seed=999_981, device=dev)
+        Wl = synthetic.t4_weight(self.vocab, h, seed=999_983, device=dev)
+        self.lm = cas.encode_weights(Wl, variant, keep, mant)
+        del Wl
+        self.emb = synthetic.normal_weight(self.vocab, h, seed=999_979, device=dev)
         torch.cuda.synchronize()
         self.encode_s = time.time() - t0
-        self.kv = None
-        if not args.no_attn and hasattr(cas, "KVCache"):
-            self._fill_kv()
+        self.kv = self._fill_kv() if attn else None
 
     def _fill_kv(self):
         import torch
 
         import synthetic
-        cas, args, dev = self.cas, self.args, self.dev
-        T = args.ctx
-        self.kv = []
-        p = cas.params(args.variant, args.keep, args.mant)
-        chunk = 2048
+        cas, dev, T = self.cas, self.dev, self.ctx
+        p = cas.params(self.variant, self.keep, self.mant)
+        kvs = []
         for layer in range(self.L):
             layer_kv = []
-            for b in range(args.batch):
+            for b in range(self.B):
                 sk = synthetic.kv_scales(layer, self.nkv, 0, device=dev)
                 sv = synthetic.kv_scales(layer, self.nkv, 1, device=dev)
                 Kc = synthetic.kv_tokens(T, self.nkv, seed=100 * layer + 2 * b, scales=sk, device=dev)
                 Vc = synthetic.kv_tokens(T, self.nkv, seed=100 * layer + 2 * b + 1, scales=sv, device=dev)
                 kv = cas.KVCache(self.nkv, T + 64, p, Kc[:128], Vc[:128])
-                for t0 in range(0, T, chunk):
-                    kv.append(Kc[t0:t0 + chunk], Vc[t0:t0 + chunk])
+                for t0 in range(0, T, 2048):
+                    kv.append(Kc[t0:t0 + 2048], Vc[t0:t0 + 2048])
                 layer_kv.append(kv)
                 del Kc, Vc
-            self.kv.append(layer_kv)
+            kvs.append(layer_kv)
         torch.cuda.synchronize()
-        for layer_kv in self.kv:
+        for layer_kv in kvs:
             for kv in layer_kv:
-                n, st = kv.status()
-                assert st == 0 and n == T, (n, st)
+                n, s = kv.status()
+                assert s == 0 and n == T, (n, s)
+        return kvs
+
+
+# kernels of ours each call launches (the y / Y clear of the matrix products
+# is a memset node, not a kernel)
+KERNELS_PER_CALL = {"gemv": 1, "gemm": 1, "draft_attn": 2, "verify_attn": 2, "append": 2, "truncate": 1, "glue": 1}
+
+
+class Step:
+    """One self-speculative decode step as a data-dependent forward through
+    the C ABI: D draft tokens, each a forward of every layer over the
+    speculation data (embedding, RMSNorm, draft GEMV Wqkv, RoPE into a bf16
+    draft tail, draft attention over the compressed KV + tail, Wo, residual +
+    RMSNorm, Wgate|up, SiLU*mul, Wdown, ..., final RMSNorm, LM head, argmax
+    -> next draft token), then one verify forward of the T = D + 1 tokens over
+    the exact weights (verify GEMMs, online KV append, verify attention, LM
+    head, argmax), then a rollback of the KV caches to the context (fixed
+    schedule: acceptance has no meaning on random weights). The verify's last
+    token is the next step's first token, so successive steps chain."""
+
+    def __init__(self, cas, stk, st, D):
+        import torch
+        self.cas, self.stk, self.st, self.D = cas, stk, st, D
+        B, T, dev = stk.B, D + 1, stk.dev
+        self.T = T
+        h, F, Hq, Hkv, hd, V = stk.hidden, stk.ffn, stk.nq, stk.nkv, stk.hd, stk.vocab
+        f32, i16 = torch.float32, torch.int16
+        E = lambda *s, dt=f32: torch.empty(*s, dtype=dt, device=dev)  # noqa: E731
+        self.vtok = torch.zeros(B * T, dtype=torch.int32, device=dev)  # per sequence: [t_last, d_1 .. d_D]
+        x, xn, qkv, q = E(B, h), E(B, h, dt=i16), E(B, (Hq + 2 * Hkv) * hd), E(B, Hq, hd, dt=i16)
+        tk, tv, o, ob = E(B, D, Hkv, hd, dt=i16), E(B, D, Hkv, hd, dt=i16), E(B, Hq, hd), E(B, Hq * hd, dt=i16)
+        yo, gu, hh, yd, lg = E(B, h), E(B, 2 * F), E(B, F, dt=i16), E(B, h), E(B, V)
+        tk.zero_()
+        tv.zero_()
+        X, Xn, QKV = E(B * T, h), E(B * T, h, dt=i16), E(B * T, (Hq + 2 * Hkv) * hd)
+        Q, Kn, Vn = E(B * T, Hq, hd, dt=i16), E(B * T, Hkv, hd, dt=i16), E(B * T, Hkv, hd, dt=i16)
+        O, Ob, Yo = E(B, T, Hq, hd), E(B * T, Hq * hd, dt=i16), E(B * T, h)
+        GU, HH, YD, LG = E(B * T, 2 * F), E(B * T, F, dt=i16), E(B * T, h), E(B * T, V)
+        self.vout = torch.zeros(B * T, dtype=torch.int32, device=dev)
+        attn = stk.kv is not None
+        ws = E(cas.cas_attn_workspace_bytes(B, Hq, T, stk.ctx + 64), dt=torch.uint8) if attn else None
+        self.keep = [x, xn, qkv, q, tk, tv, o, ob, yo, gu, hh, yd, lg, X, Xn, QKV, Q, Kn, Vn, O, Ob, Yo, GU, HH, YD,
+                     LG, ws]
+        P, eps = cas.prepare, 1e-5
+        segs, self.kernels = [], {"gemv": 0, "gemm": 0, "other": 0}
+        self.draft_bytes, self.verify_bytes = 0, 0
+
+        def add(kind, fns, what):
+            segs.append((kind, fns))
+            self.kernels["other" if kind == "other" else kind] += sum(KERNELS_PER_CALL[w] for w in what)
+
+        def gemv(W, xin, y):
+            self.draft_bytes += W.spec_bytes() + B * W.K * 2 + B * W.N * 4
+            add("gemv", [P("cas_draft_gemv", W, xin, B, y, st)], ["gemv"])
+
+        def gemm(W, Xin, Y):
+            self.verify_bytes += W.all_bytes() + B * T * W.K * 2 + B * T * W.N * 4
+            add("gemm", [P("cas_verify_gemm", W, Xin, B * T, Y, st)], ["gemm"])
+
+        for d in range(D):
+            add("other", [P("cas_embed", self.vtok[b * T + d:b * T + d + 1], 1, stk.emb, V, h, x[b:b + 1], st)
+                          for b in range(B)], ["glue"] * B)
+            for layer in range(stk.L):
+                M = stk.mats[layer]
+                add("other", [P("cas_add_rmsnorm", x, yd if layer else None, B, h, stk.g1[layer], eps, xn, st)],
+                    ["glue"])
+                gemv(M["qkv"], xn, qkv)
+                fns = [P("cas_rope_split", qkv, B, Hq, Hkv, stk.ctx + d, 1, stk.theta, q, tk[0, d], D * Hkv * hd,
+                         tv[0, d], D * Hkv * hd, st)]
+                what = ["glue"]
+                if attn:
+                    for b in range(B):
+                        fns.append(cas.prepare_draft_attn([stk.kv[layer][b]], q[b:b + 1], tk[b:b + 1, :d + 1],
+                                                          tv[b:b + 1, :d + 1], o[b:b + 1], ws, st))
+                        what.append("draft_attn")
+                fns.append(P("cas_f32_to_bf16", o, B * Hq * hd, ob, st))
+                what.append("glue")
+                add("other", fns, what)
+                gemv(M["o"], ob, yo)
+                add("other", [P("cas_add_rmsnorm", x, yo, B, h, stk.g2[layer], eps, xn, st)], ["glue"])
+                gemv(M["gateup"], xn, gu)
+                add("other", [P("cas_silu_mul", gu, B, F, hh, st)], ["glue"])
+                gemv(M["down"], hh, yd)
+            add("other", [P("cas_add_rmsnorm", x, yd, B, h, stk.gf, eps, xn, st)], ["glue"])
+            gemv(stk.lm, xn, lg)
+            add("other", [P("cas_argmax", lg[b:b + 1], 1, V, self.vtok[b * T + 1 + d:b * T + 2 + d], st)
+                          for b in range(B)], ["glue"] * B)
+        # verify forward of the T tokens of every sequence
+        add("other", [P("cas_embed", self.vtok, B * T, stk.emb, V, h, X, st)], ["glue"])
+        for layer in range(stk.L):
+            M = stk.mats[layer]
+            add("other", [P("cas_add_rmsnorm", X, YD if layer else None, B * T, h, stk.g1[layer], eps, Xn, st)],
+                ["glue"])
+            gemm(M["qkv"], Xn, QKV)
+            fns = [P("cas_rope_split", QKV, B * T, Hq, Hkv, stk.ctx, T, stk.theta, Q, Kn, Hkv * hd, Vn, Hkv * hd, st)]
+            what = ["glue"]
+            if attn:
+                for b in range(B):
+                    fns.append(stk.kv[layer][b].prepare_append(Kn[b * T:(b + 1) * T], Vn[b * T:(b + 1) * T], st))
+                    what.append("append")
+                fns.append(cas.prepare_verify_attn(stk.kv[layer], Q.view(B, T, Hq, hd), O, ws, st))
+                what.append("verify_attn")
+            fns.append(P("cas_f32_to_bf16", O, B * T * Hq * hd, Ob, st))
+            what.append("glue")
+            add("other", fns, what)
+            gemm(M["o"], Ob, Yo)
+            add("other", [P("cas_add_rmsnorm", X, Yo, B * T, h, stk.g2[layer], eps, Xn, st)], ["glue"])
+            gemm(M["gateup"], Xn, GU)
+            add("other", [P("cas_silu_mul", GU, B * T, F, HH, st)], ["glue"])
+            gemm(M["down"], HH, YD)
+        add("other", [P("cas_add_rmsnorm", X, YD, B * T, h, stk.gf, eps, Xn, st)], ["glue"])
+        gemm(stk.lm, Xn, LG)
+        fns = [P("cas_argmax", LG, B * T, V, self.vout, st)]
+        fns += [P("cas_argmax", LG[b * T + T - 1:b * T + T], 1, V, self.vtok[b * T:b * T + 1], st) for b in range(B)]
+        what = ["glue"] * (1 + B)
+        if attn:  # rollback: every cache back to the context
+            fns += [kv.prepare_truncate(stk.ctx, st) for layer_kv in stk.kv for kv in layer_kv]
+            what += ["truncate"] * (stk.L * B)
+        add("other", fns, what)
+        self.segs = segs
+        self.launches = sum(self.kernels.values())
+
+    def eager(self):
+        for _, fns in self.segs:
+            for f in fns:
+                f()
+
+    def capture(self):
+        """One CUDA graph per segment (the timed launches stay separately timable)."""
+        import torch
+        self.graphs = []
+        for kind, fns in self.segs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.st):
+                for f in fns:
+                    f()
+            self.graphs.append((kind, g))
+
+    def replay(self, ev=None):
+        """One step from the graphs; with `ev`, events around every matrix-product segment."""
+        e = 0
+        for kind, g in self.graphs:
+            if ev is not None and kind != "other":
+                ev[e].record(self.st)
+                g.replay()
+                ev[e + 1].record(self.st)
+                e += 2
+            else:
+                g.replay()
+
+
+def time_step(step, steps, warmup, clocks=None):
+    """Graph-replayed steps timed with CUDA events on the step's stream:
+    (total ms, draft GEMV ms, verify GEMM ms) over `steps` steps."""
+    import torch
+    st = step.st
+    with torch.cuda.stream(st):
+        for _ in range(max(warmup, 3)):
+            step.eager()
+    torch.cuda.synchronize()
+    step.capture()
+    torch.cuda.synchronize()
+    kinds = [k for k, _ in step.graphs if k != "other"]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(kinds))] for _ in range(steps)]
+    with torch.cuda.stream(st):
+        for _ in range(max(warmup, 3)):
+            step.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ctx = clocks if clocks is not None else _Null()
+    with ctx, torch.cuda.stream(st):
+        torch.cuda.nvtx.range_push("timed")  # lets a profiler select the timed launches
+        a.record(st)
+        for i in range(steps):
+            step.replay(evs[i])
+        b.record(st)
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
+    gemv_ms = gemm_ms = 0.0
+    for ev in evs:
+        for i, kind in enumerate(kinds):
+            ms = ev[2 * i].elapsed_time(ev[2 * i + 1])
+            if kind == "gemv":
+                gemv_ms += ms
+            else:
+                gemm_ms += ms
+    return a.elapsed_time(b), gemv_ms, gemm_ms
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def e2e_step(step, steps):
+    """The whole step through the C ABI, launched call by call as a user would
+    (no graphs), with each step's first token copied in from pinned host
+    memory and its verified tokens copied back and read on the host."""
+    import torch
+    st, B, T = step.st, step.stk.B, step.T
+    host_in = step.vtok.view(B, T)[:, 0].cpu().pin_memory()
+    host_out = torch.empty(B * T, dtype=torch.int32).pin_memory()
+    first = [step.vtok[b * T:b * T + 1] for b in range(B)]
+
+    def one():
+        for b in range(B):
+            first[b].copy_(host_in[b:b + 1], non_blocking=True)
+        step.eager()
+        host_out.copy_(step.vout, non_blocking=True)
+        st.synchronize()
+        host_in.copy_(host_out.view(B, T)[:, -1])
+
+    with torch.cuda.stream(st):
+        for _ in range(2):
+            one()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            one()
+        dt = (time.perf_counter() - t0) / steps
+    return dt * 1e3, B * 4, B * T * 4
 
 
 def run_cas(args):
@@ -240,7 +487,6 @@ def run_cas(args):
     import torch.distributed as dist
 
     import bit_level_weight_gb300 as cas
-    import synthetic
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -252,172 +498,48 @@ def run_cas(args):
     from bit_level_weight_gb300 import build as _b
     _b.build()
 
-    stk = Stack(cas, args, dev)
+    stk = Stack(cas, dev, args.workload, args.layers, args.variant, args.keep, args.mant, args.ctx, args.batch,
+                attn=not args.no_attn)
     st = torch.cuda.Stream(device=dev)  # every call of the step is bound to this stream
-    D, B = args.draft_len, args.batch
-    nvec = B
-    xs = {"qkv": synthetic.activations(nvec, stk.hidden, seed=1, device=dev),
-          "o": synthetic.activations(nvec, stk.hidden, seed=2, device=dev),
-          "gateup": synthetic.activations(nvec, stk.hidden, seed=3, device=dev),
-          "down": synthetic.activations(nvec, stk.ffn, seed=4, device=dev)}
-    T = B * (D + 1)
-    Xs = {"qkv": synthetic.activations(T, stk.hidden, seed=5, device=dev),
-          "o": synthetic.activations(T, stk.hidden, seed=6, device=dev),
-          "gateup": synthetic.activations(T, stk.hidden, seed=7, device=dev),
-          "down": synthetic.activations(T, stk.ffn, seed=8, device=dev)}
-    ys = {nm: torch.empty(nvec, stk.mats[0][nm].N, dtype=torch.float32, device=dev) for nm in xs}
-    Ys = {nm: torch.empty(T, stk.mats[0][nm].N, dtype=torch.float32, device=dev) for nm in Xs}
-
-    gemv = [{nm: cas.prepare("cas_draft_gemv", stk.mats[l][nm], xs[nm], nvec, ys[nm], st) for nm in xs}
-            for l in range(stk.L)]
-    gemm = [{nm: cas.prepare("cas_verify_gemm", stk.mats[l][nm], Xs[nm], T, Ys[nm], st) for nm in Xs}
-            for l in range(stk.L)]
-    draft_bytes = {nm: sum(stk.mats[l][nm].spec_bytes() + nvec * stk.mats[l][nm].K * 2 + nvec * stk.mats[l][nm].N * 4
-                           for l in range(stk.L)) for nm in xs}
-    verify_bytes = {nm: sum(stk.mats[l][nm].all_bytes() + T * stk.mats[l][nm].K * 2 + T * stk.mats[l][nm].N * 4
-                            for l in range(stk.L)) for nm in Xs}
-    lm_gemv = lm_gemm = None
-    if stk.lm is not None:
-        y_lm = torch.empty(nvec, stk.vocab, dtype=torch.float32, device=dev)
-        Y_lm = torch.empty(T, stk.vocab, dtype=torch.float32, device=dev)
-        lm_gemv = cas.prepare("cas_draft_gemv", stk.lm, xs["qkv"], nvec, y_lm, st)
-        lm_gemm = cas.prepare("cas_verify_gemm", stk.lm, Xs["qkv"], T, Y_lm, st)
-        draft_bytes["lm_head"] = stk.lm.spec_bytes() + nvec * stk.hidden * 2 + nvec * stk.vocab * 4
-        verify_bytes["lm_head"] = stk.lm.all_bytes() + T * stk.hidden * 2 + T * stk.vocab * 4
-
-    attn = stk.kv is not None
-    if attn:
-        q_d = synthetic.activations(B, stk.nq * stk.hd, seed=20, device=dev).view(B, stk.nq, stk.hd)
-        tail_k = synthetic.activations(B * D, stk.nkv * stk.hd, seed=21, device=dev).view(B, D, stk.nkv, stk.hd)
-        tail_v = synthetic.activations(B * D, stk.nkv * stk.hd, seed=22, device=dev).view(B, D, stk.nkv, stk.hd)
-        q_v = synthetic.activations(B * (D + 1), stk.nq * stk.hd, seed=23, device=dev).view(B, D + 1, stk.nq, stk.hd)
-        newk = synthetic.activations(D + 1, stk.nkv * stk.hd, seed=24, device=dev).view(D + 1, stk.nkv, stk.hd)
-        newv = synthetic.activations(D + 1, stk.nkv * stk.hd, seed=25, device=dev).view(D + 1, stk.nkv, stk.hd)
-        ws = torch.empty(cas.cas_attn_workspace_bytes(B, stk.nq, D + 1, args.ctx + 64), dtype=torch.uint8, device=dev)
-        o_d = torch.empty(B, stk.nq, stk.hd, dtype=torch.float32, device=dev)
-        o_v = torch.empty(B, D + 1, stk.nq, stk.hd, dtype=torch.float32, device=dev)
-        tails = [(tail_k[:, :d + 1].contiguous(), tail_v[:, :d + 1].contiguous()) for d in range(D)]
-        dattn = [[cas.prepare_draft_attn(stk.kv[l], q_d, tails[d][0], tails[d][1], o_d, ws, st) for d in range(D)]
-                 for l in range(stk.L)]
-        vattn = [cas.prepare_verify_attn(stk.kv[l], q_v, o_v, ws, st) for l in range(stk.L)]
-        appends = [[kv.prepare_append(newk, newv, st) for kv in stk.kv[l]] for l in range(stk.L)]
-        truncs = [[kv.prepare_truncate(args.ctx, st) for kv in stk.kv[l]] for l in range(stk.L)]
-
-    # The step as an ordered list of segments; GEMV / GEMM segments are timed.
-    def seq(*fns):
-        def run():
-            for f in fns:
-                f()
-        return run
-    segs = []  # (kind, callable)
-    for d in range(D):
-        for l in range(stk.L):
-            g = gemv[l]
-            segs.append(("gemv", g["qkv"]))
-            if attn:
-                segs.append(("attn", dattn[l][d]))
-            segs.append(("gemv", seq(g["o"], g["gateup"], g["down"])))
-        if lm_gemv is not None:
-            segs.append(("gemv", lm_gemv))
-    for l in range(stk.L):
-        g = gemm[l]
-        segs.append(("gemm", g["qkv"]))
-        if attn:
-            segs.append(("attn", seq(*appends[l], vattn[l])))
-        segs.append(("gemm", seq(g["o"], g["gateup"], g["down"])))
-    if lm_gemm is not None:
-        segs.append(("gemm", lm_gemm))
-    if attn:
-        segs.append(("attn", seq(*[t for l in range(stk.L) for t in truncs[l]])))
-
-    launches_per_step = D * stk.L * 4 + stk.L * 4 + (D + 1 if lm_gemv is not None else 0)
-    if attn:
-        launches_per_step += D * stk.L * 2 + stk.L * (2 * B + 2) + stk.L * B
-
-    # eager warm-up (also caches every launch configuration), then one CUDA
-    # graph per segment so the timed region has no host gaps inside a segment
-    with torch.cuda.stream(st):
-        for _ in range(max(args.warmup, 3)):
-            for _, f in segs:
-                f()
-    torch.cuda.synchronize()
-    graphs = []
-    for kind, f in segs:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=st):
-            f()
-        graphs.append((kind, g))
-    torch.cuda.synchronize()
-    n_timed = sum(1 for k, _ in graphs if k != "attn")
-    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * n_timed)] for _ in range(args.steps)]
-
-    def step(ev=None):
-        e = 0
-        for kind, g in graphs:
-            if ev is not None and kind != "attn":
-                ev[e].record(st)
-                g.replay()
-                ev[e + 1].record(st)
-                e += 2
-            else:
-                g.replay()
-
-    with torch.cuda.stream(st):
-        for _ in range(max(args.warmup, 3)):
-            step()
-    torch.cuda.synchronize()
-
-    # ---- timed region
+    step = Step(cas, stk, st, args.draft_len)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    gemv_ms, gemm_ms = 0.0, 0.0
-    kinds = [k for k, _ in graphs if k != "attn"]
-    with ClockSampler(local) as clk, torch.cuda.stream(st):
-        torch.cuda.nvtx.range_push("timed")  # lets a profiler select the timed launches
-        t_start.record(st)
-        for i in range(args.steps):
-            step(evsets[i])
-        t_end.record(st)
-        torch.cuda.synchronize()
-        torch.cuda.nvtx.range_pop()
-    for ev in evsets:
-        for i, kind in enumerate(kinds):
-            ms = ev[2 * i].elapsed_time(ev[2 * i + 1])
-            if kind == "gemv":
-                gemv_ms += ms
-            else:
-                gemm_ms += ms
-    total_ms = t_start.elapsed_time(t_end)
+    with ClockSampler(local) as clk:
+        total_ms, gemv_ms, gemm_ms = time_step(step, args.steps, args.warmup)
     if world > 1:
         dist.barrier()
-
-    steps = args.steps
-    d_bytes = sum(draft_bytes.values()) * D * steps
-    v_bytes = sum(verify_bytes.values()) * steps
+    steps, D = args.steps, args.draft_len
+    d_bytes = step.draft_bytes * steps
+    v_bytes = step.verify_bytes * steps
     gemv_gbs = d_bytes / (gemv_ms * 1e-3) / 1e9
     gemm_gbs = v_bytes / (gemm_ms * 1e-3) / 1e9
     ms_per_step = total_ms / steps
-
-    # ---- e2e: draft GEMV pass of the whole stack through the C ABI with the
-    # activation in pinned host memory (H2D) and every output read back (D2H)
-    with torch.cuda.stream(st):
-        e2e = e2e_draft_pass(cas, stk, xs, ys, nvec, st, steps=max(3, steps))
+    e2e_ms, h2d, d2h = e2e_step(step, max(3, steps // 2))
+    status = cas.cas_device_status(st)
+    assert status == 0, f"device status {status}"
 
     if world > 1:
-        agg = replica_aggregate(gather_stats((d_bytes, gemv_ms, v_bytes, gemm_ms, ms_per_step), world))
-        gemv_gbs, gemm_gbs, ms_per_step = agg["gemv_gbs"], agg["gemm_gbs"], agg["ms_per_step"]
+        agg = replica_aggregate(gather_stats((d_bytes, gemv_ms, v_bytes, gemm_ms, ms_per_step, e2e_ms), world))
+        gemv_gbs, gemm_gbs, ms_per_step, e2e_ms = agg["gemv_gbs"], agg["gemm_gbs"], agg["ms_per_step"], agg["e2e_ms"]
+    launches = step.launches
+    ctx_used = args.ctx if stk.kv is not None else 0
+    extra = {}
+    if rank == 0 and not args.no_extra and world == 1:
+        del step
+        extra = extra_configs(cas, args, dev, stk)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
     peak, peak_kind = peaks()
-    n_gemv = 4 * stk.L + (1 if lm_gemv is not None else 0)
-    per_launch_bytes = sum(draft_bytes.values()) / n_gemv
+    n_gemv = 4 * stk.L + 1  # per draft token
+    per_launch_bytes = step_draft_bytes = d_bytes / steps
+    per_launch_bytes = step_draft_bytes / (D * n_gemv)
     per_launch_ms = gemv_ms / (steps * D * n_gemv)
     achieved = per_launch_bytes / (per_launch_ms * 1e-3) / 1e9
+    kern = gemv_kernel_name(args, args.batch)
+    rec = profiled_record(kern)
     out = {
         "metric": METRIC,
         "value": round(gemv_gbs, 1),
@@ -433,32 +555,42 @@ def run_cas(args):
         "data": "synthetic",
         "config": {
             "workload": WORKLOADS[args.workload],
-            "layers": stk.L, "lm_head_rows": stk.vocab or None, "hidden": stk.hidden, "ffn": stk.ffn, "heads": f"{stk.nq}q/{stk.nkv}kv x {stk.hd}",
-            "batch": B, "draft_len": D, "verify_tokens": T, "ctx": args.ctx if attn else 0,
+            "layers": stk.L, "lm_head_rows": stk.vocab, "hidden": stk.hidden, "ffn": stk.ffn,
+            "heads": f"{stk.nq}q/{stk.nkv}kv x {stk.hd}", "batch": args.batch, "draft_len": D,
+            "verify_tokens": args.batch * (D + 1), "ctx": ctx_used,
             "keep_per_block": args.keep, "mant_bits": args.mant, "variant": f"Cassandra-{args.variant}",
-            "weights": "Student-t(4) x 0.02/sqrt(2), fused qkv and gate|up",
+            "weights": "Student-t(4) x 0.02/sqrt(2), fused qkv and gate|up; embedding N(0, 0.02)",
+            "forward": "data-dependent: embedding, RMSNorm, RoPE, SiLU*mul, residual adds, LM head, argmax chain",
             "parallelism": "replicas" if world > 1 else "single GPU",
-            "l2": f"inputs larger than L2 ({sum(draft_bytes.values()) / 1e9:.2f} GB speculation stream per draft pass)",
+            "l2": f"inputs larger than L2 ({step_draft_bytes / D / 1e9:.2f} GB speculation stream per draft pass)",
         },
         "verify_gemm_gbs": round(gemm_gbs, 1),
         "us_per_decode_step": round(ms_per_step * 1e3, 1),
         "draft_gemv_frac_of_hbm": round(gemv_gbs / world / peak, 4),
         "draft_gemv_frac_of_8tbs_nominal": round(gemv_gbs / world / 8000.0, 4),
         "verify_gemm_frac_of_hbm": round(gemm_gbs / world / peak, 4),
-        "roofline": {"kernel": gemv_kernel_name(args, B), "bound": "hbm", "achieved": round(achieved, 1),
+        "draft_gemv_ms_per_step": round(gemv_ms / steps, 3),
+        "verify_gemm_ms_per_step": round(gemm_ms / steps, 3),
+        "roofline": {"kernel": kern, "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
-                     "traffic": (round(PROFILED_TRAFFIC_RATIO * per_launch_bytes) if PROFILED_TRAFFIC_RATIO
-                                 else None),
-                     "traffic_note": "per launch: (ncu dram bytes / algorithmic bytes of a 28672x4096 launch, "
-                                     "profiles/draft_gemv_28672x4096.md) x algorithmic bytes per launch of this step",
+                     "traffic": (round(rec["traffic_ratio"] * per_launch_bytes) if rec else None),
+                     "traffic_note": ("per launch: ncu dram bytes / algorithmic bytes of one profiled launch of "
+                                      f"this kernel ({rec['shape']}) x algorithmic bytes per launch of this step"
+                                      if rec else "null: the kernel's source changed since its counters were taken"),
                      "algorithmic_bytes_per_launch": int(per_launch_bytes)},
-        "alu_roof": (alu_roof(achieved, clk) if args.variant == 1 and args.keep == 64 and args.mant == 3 and B == 1
-                     else None),
-        "e2e": e2e,
-        "gpu_launches": launches_per_step * steps,
+        "alu_roof": (alu_roof(achieved, clk, rec) if args.variant == 1 and args.keep == 64 and args.mant == 3
+                     and args.batch <= 2 else None),
+        "e2e": {"value": round(step_draft_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "us_per_step": round(e2e_ms * 1e3, 1),
+                "what": "the whole step (draft forwards, verify forward, KV append and rollback) called entry point "
+                        "by entry point through the C ABI without graphs, the first token copied in from pinned host "
+                        "memory and the verified tokens copied out and read each step; value = the step's "
+                        "speculation bytes over its end-to-end time"},
+        "gpu_launches": launches * steps,
         "encode_s": round(stk.encode_s, 2),
     }
+    out.update(extra)
     out["clocks"] = clk.summary()
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.cpu_seconds, args.keep, args.mant, args.variant)
@@ -467,52 +599,154 @@ def run_cas(args):
         dist.destroy_process_group()
 
 
-# dram bytes read + written / algorithmic bytes of one draft_gemv_fast_kernel<1>
-# launch on the 28672 x 4096 matrix (ncu: 62.04 MB for 61.85 MB algorithmic,
-# profiles/draft_gemv_28672x4096.md); set to None whenever that kernel changes
-# until it is captured again
-PROFILED_TRAFFIC_RATIO = (61.904384 + 0.135168) / 61.85268
+def extra_configs(cas, args, dev, main_stk):
+    """The other configurations of the workload table, each timed on this
+    GPU after the main line: the 30%-keep stack (k = 38), the Qwen3-8B-shaped
+    full step (36 layers + 151936-row LM head, batch 2, 16K, draft 6) and the
+    attention of a 128K-token cache (batch 1 and 2)."""
+    import gc
+
+    import torch
+    out = {}
+    for kv in (main_stk.kv or []):
+        del kv
+    main_stk.kv = None
+    gc.collect()
+    torch.cuda.empty_cache()
+
+    def step_ms(workload, layers, keep, ctx, batch, D):
+        stk = Stack(cas, dev, workload, layers, args.variant, keep, args.mant, ctx, batch)
+        st = torch.cuda.Stream(device=dev)
+        s = Step(cas, stk, st, D)
+        total, gv, gm = time_step(s, 3, 3)
+        r = {"ms_per_step": round(total / 3, 3), "draft_gemv_gbs": round(s.draft_bytes * 3 / (gv * 1e-3) / 1e9, 1),
+             "verify_gemm_gbs": round(s.verify_bytes * 3 / (gm * 1e-3) / 1e9, 1)}
+        del s, stk
+        gc.collect()
+        torch.cuda.empty_cache()
+        return r
+
+    if args.workload == "llama3-8b":
+        out["keep30"] = dict(step_ms("llama3-8b", 32, cas.cas_keep_from_ratio(0.3), 32768, 1, 4),
+                             config="llama3-8b stack, keep 38/128, m = 3, batch 1, draft 4, 32K")
+        out["qwen3_step"] = dict(step_ms("qwen3-8b", 36, args.keep, 16384, 2, 6),
+                                 config="qwen3-8b full step, 36 layers + 151936-row LM head, batch 2, 16K, draft 6")
+        out["keep30_step_ms"] = out["keep30"]["ms_per_step"]
+        out["qwen3_step_ms"] = out["qwen3_step"]["ms_per_step"]
+    out.update(attn_128k(cas, args, dev))
+    return out
 
 
-# warp instructions x 32 / elements of one draft_gemv_fast_kernel<1> launch on
-# the 28672 x 4096 matrix (ncu smsp__inst_executed.sum,
-# profiles/draft_gemv_28672x4096.md); None whenever that kernel changes
-PROFILED_LANE_INSTR_PER_ELEM = 107314082 * 32 / (28672 * 4096)
+def attn_128k(cas, args, dev):
+    """Draft and verify attention of one layer over 128K-token compressed
+    caches (8 kv heads, 32 query heads), batch 1 and 2: CUDA-event time of 10
+    calls each; the 32-layer figure is 32 x this."""
+    import torch
+
+    import synthetic
+    H, Hq, T, n = 8, 32, 5, 131072
+    p = cas.params(args.variant, args.keep, args.mant)
+    res = {}
+    caches = []
+    for b in range(2):
+        sk, sv = synthetic.kv_scales(0, H, 0, device=dev), synthetic.kv_scales(0, H, 1, device=dev)
+        kv = cas.KVCache(H, n + 64, p, synthetic.kv_tokens(128, H, seed=7 + b, scales=sk, device=dev),
+                         synthetic.kv_tokens(128, H, seed=9 + b, scales=sv, device=dev))
+        for t0 in range(0, n, 4096):
+            Kc = synthetic.kv_tokens(4096, H, seed=1000 + 2 * t0 + b, scales=sk, device=dev)
+            Vc = synthetic.kv_tokens(4096, H, seed=1001 + 2 * t0 + b, scales=sv, device=dev)
+            kv.append(Kc, Vc)
+        caches.append(kv)
+    st = torch.cuda.Stream(device=dev)
+    for B in (1, 2):
+        kvs = caches[:B]
+        ws = torch.empty(cas.cas_attn_workspace_bytes(B, Hq, T, n + 64), dtype=torch.uint8, device=dev)
+        q = synthetic.activations(B, Hq * 128, seed=3, device=dev).view(B, Hq, 128)
+        tk = synthetic.activations(B * 4, H * 128, seed=4, device=dev).view(B, 4, H, 128)
+        tv = synthetic.activations(B * 4, H * 128, seed=5, device=dev).view(B, 4, H, 128)
+        o = torch.empty(B, Hq, 128, dtype=torch.float32, device=dev)
+        d = cas.prepare_draft_attn(kvs, q, tk, tv, o, ws, st)
+        for kv in kvs:
+            kv.truncate(n - T)
+        newk = synthetic.activations(T, H * 128, seed=6, device=dev).view(T, H, 128)
+        newv = synthetic.activations(T, H * 128, seed=8, device=dev).view(T, H, 128)
+        for kv in kvs:
+            kv.append(newk, newv)
+        qv = synthetic.activations(B * T, Hq * 128, seed=7, device=dev).view(B, T, Hq, 128)
+        ov = torch.empty(B, T, Hq, 128, dtype=torch.float32, device=dev)
+        v = cas.prepare_verify_attn(kvs, qv, ov, ws, st)
+        for name, f in (("draft", d), ("verify", v)):
+            with torch.cuda.stream(st):
+                for _ in range(3):
+                    f()
+                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(st)
+                for _ in range(10):
+                    f()
+                b_.record(st)
+                torch.cuda.synchronize()
+            res[f"{name}_attn_128k_b{B}_us"] = round(a.elapsed_time(b_) / 10 * 1e3, 1)
+    res["draft_attn_128k_us"] = res["draft_attn_128k_b1_us"]
+    res["verify_attn_128k_us"] = res["verify_attn_128k_b1_us"]
+    res["attn_128k_note"] = "one layer (8 kv heads, 32 query heads) over a 131072-token cache; x 32 for a stack"
+    return res
+
+
+# ncu counters of one profiled launch of each draft GEMV kernel, stored with a
+# hash of the sources the kernel is built from; a record whose hash no longer
+# matches the tree is not used (the kernel changed since it was profiled).
+PROFILED = {}
+PROFILED_SOURCES = ("bit_level_weight_gb300/csrc/gemv.cu", "bit_level_weight_gb300/csrc/wordlane.cuh",
+                    "bit_level_weight_gb300/csrc/common.cuh", "bit_level_weight_gb300/csrc/sbdecode.cuh")
 SMS, LANES_PER_SM_CLK = 152, 128  # 4 schedulers x 32 lanes issue per SM clock
+
+
+def source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in PROFILED_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_record(kernel: str):
+    rec = PROFILED.get(kernel)
+    return rec if rec and rec["source_sha16"] == source_hash() else None
 
 
 def gemv_kernel_name(args, nvec: int) -> str:
     """The draft GEMV kernel the stack's matrices (rows of whole superblocks) run."""
     if args.keep == 64 and args.mant == 3:
         if args.variant == 1:
-            return f"draft_gemv_fast_kernel<{nvec}>"
+            return f"draft_gemv_word_kernel<{nvec}>" if nvec <= 2 else f"draft_gemv_fast_kernel<{nvec}>"
         if nvec <= 2:
             return f"draft_gemv_fast2_kernel<{nvec}>"
     return f"draft_gemv_runs_kernel<{args.variant},{nvec}>"
 
 
-def alu_roof(achieved_gbs: float, clk) -> dict:
+def alu_roof(achieved_gbs: float, clk, rec) -> dict:
     """The draft GEMV is bound by instruction issue (integer decode), so its
     second roof is the lane-instruction issue peak: SMs x 128 x SM clock.
     achieved = profiled lane instructions per element x elements per second."""
-    if PROFILED_LANE_INSTR_PER_ELEM is None:
+    if not rec:
         return None
     mhz = (clk.summary() or {}).get("sm_mhz") or 2070.0
     peak = SMS * LANES_PER_SM_CLK * mhz * 1e6
-    bytes_per_elem = 4.205 / 8  # speculation bits per element of the Student-t matrices (k = 64, m = 3)
+    bytes_per_elem = rec["spec_bits_per_elem"] / 8
     elems = achieved_gbs * 1e9 / bytes_per_elem
-    achieved = PROFILED_LANE_INSTR_PER_ELEM * elems
+    achieved = rec["lane_instr_per_elem"] * elems
     budget = peak / (0.75 * peaks()[0] * 1e9 / bytes_per_elem)
     return {"bound": "alu", "achieved": round(achieved / 1e12, 2), "peak": round(peak / 1e12, 2),
             "unit": "T lane-instr/s", "frac": round(achieved / peak, 4),
-            "lane_instr_per_elem": round(PROFILED_LANE_INSTR_PER_ELEM, 2),
+            "lane_instr_per_elem": round(rec["lane_instr_per_elem"], 2),
             "budget_at_75pct_hbm": round(budget, 2),
-            "note": "lane instructions per element from ncu (profiles/draft_gemv_28672x4096.md); "
+            "note": f"lane instructions per element from ncu smsp__inst_executed.sum on {rec['shape']}; "
                     "peak = 152 SMs x 128 lanes x median SM clock"}
 
 
 def gather_stats(local: tuple, world: int) -> list:
-    """All ranks' (draft bytes, draft ms, verify bytes, verify ms, ms/step)."""
+    """All ranks' (draft bytes, draft ms, verify bytes, verify ms, ms/step, e2e ms)."""
     import torch.distributed as dist
     out = [None] * world
     dist.all_gather_object(out, tuple(float(v) for v in local))
@@ -527,43 +761,7 @@ def replica_aggregate(stats: list) -> dict:
     gemv_ms = max(s[1] for s in stats)
     gemm_ms = max(s[3] for s in stats)
     return {"gemv_gbs": d_bytes / (gemv_ms * 1e-3) / 1e9, "gemm_gbs": v_bytes / (gemm_ms * 1e-3) / 1e9,
-            "ms_per_step": max(s[4] for s in stats)}
-
-
-def e2e_draft_pass(cas, stk, xs, ys, nvec, st, steps):
-    import torch
-    host_x = {nm: x.cpu().pin_memory() for nm, x in xs.items()}
-    host_y = {nm: torch.empty(stk.L, *y.shape, dtype=torch.float32).pin_memory() for nm, y in ys.items()}
-    dev_y = {nm: torch.empty(stk.L, *y.shape, dtype=torch.float32, device=y.device) for nm, y in ys.items()}
-    calls = [{nm: cas.prepare("cas_draft_gemv", stk.mats[l][nm], xs[nm], nvec, dev_y[nm][l], st) for nm in xs}
-             for l in range(stk.L)]
-    h2d = sum(t.numel() * t.element_size() for t in host_x.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_y.values())
-    spec = sum(stk.mats[l][nm].spec_bytes() + nvec * stk.mats[l][nm].K * 2 + nvec * stk.mats[l][nm].N * 4
-               for l in range(stk.L) for nm in xs)
-
-    def one():
-        for nm in xs:
-            xs[nm].copy_(host_x[nm], non_blocking=True)
-        for l in range(stk.L):
-            c = calls[l]
-            c["qkv"](); c["o"](); c["gateup"](); c["down"]()
-        for nm in ys:
-            host_y[nm].copy_(dev_y[nm], non_blocking=True)
-
-    for _ in range(3):
-        one()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(st)
-    for _ in range(steps):
-        one()
-    b.record(st)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / steps
-    return {"value": round(spec / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "what": f"one draft GEMV pass over all {stk.L} layers' matrices via "
-            "cas_draft_gemv, x copied in from pinned host memory and all outputs copied out, per step"}
+            "ms_per_step": max(s[4] for s in stats), "e2e_ms": max(s[5] for s in stats) if len(stats[0]) > 5 else 0.0}
 
 
 def run_reference(args):
@@ -587,11 +785,13 @@ def run_reference(args):
         "config": {"workload": WORKLOADS[args.workload], "layers": args.layers, "hidden": shp["hidden"], "ffn": shp["ffn"],
                    "batch": args.batch, "draft_len": args.draft_len, "keep_per_block": args.keep,
                    "mant_bits": args.mant, "variant": f"Cassandra-{args.variant}"},
-        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": vals[0]["cores"],
+                         "host_cores": vals[0]["host_cores"], "kind": "oracle",
+                         "single_thread_value": round(statistics.median(x["single_thread_value"] for x in vals), 4),
                          "sample": vals[0]["sample"]},
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "note": "CPU oracle (plain C, one thread) timed on a bounded sample of the draft GEMV workload; "
-                "value = speculation bytes decoded per second",
+        "note": "CPU oracle (plain C) timed on the host cores on a bounded sample of the draft GEMV workload; "
+                "value = speculation bytes decoded per second with every core",
     }
     print(json.dumps(out), flush=True)
 

@@ -86,10 +86,20 @@ def cfg0_weight(device="cpu") -> torch.Tensor:
     return normal_weight(4096, 4096, seed=0, std=0.02, outlier_frac=0.001, outlier_mul=20.0, device=device)
 
 
-# Llama-3-8B decoder layer: hidden 4096, FFN 14336, 32 q heads / 8 kv heads of 128.
-LLAMA3_8B = dict(layers=32, hidden=4096, ffn=14336, n_q=32, n_kv=8, head_dim=128)
-# Qwen3-8B decoder layer: 36 layers, hidden 4096, FFN 12288, 32/8 heads, vocab 151936.
-QWEN3_8B = dict(layers=36, hidden=4096, ffn=12288, n_q=32, n_kv=8, head_dim=128, vocab=151936)
+# Llama-3-8B: 32 layers, hidden 4096, FFN 14336, 32 q heads / 8 kv heads of 128,
+# vocabulary 128256, rotary base 500000.
+LLAMA3_8B = dict(layers=32, hidden=4096, ffn=14336, n_q=32, n_kv=8, head_dim=128, vocab=128256,
+                 rope_theta=500000.0)
+# Qwen3-8B: 36 layers, hidden 4096, FFN 12288, 32/8 heads, vocabulary 151936,
+# rotary base 1000000.
+QWEN3_8B = dict(layers=36, hidden=4096, ffn=12288, n_q=32, n_kv=8, head_dim=128, vocab=151936,
+                rope_theta=1000000.0)
+
+
+def norm_weight(dim: int, seed: int, device="cpu") -> torch.Tensor:
+    """RMSNorm weight: 1 + N(0, 0.05), as bf16 bits."""
+    g = _gen(seed, device)
+    return to_bits(1.0 + 0.05 * torch.randn(dim, generator=g, device=device, dtype=torch.float32))
 
 
 def layer_matrices(shape: dict) -> list[tuple[str, int, int]]:

@@ -14,7 +14,8 @@ def args(variant=1, keep=64, mant=3):
 
 
 @pytest.mark.parametrize("a,nvec,name", [
-    (args(), 1, "draft_gemv_fast_kernel<1>"), (args(), 2, "draft_gemv_fast_kernel<2>"),
+    (args(), 1, "draft_gemv_word_kernel<1>"), (args(), 2, "draft_gemv_word_kernel<2>"),
+    (args(), 3, "draft_gemv_fast_kernel<3>"),
     (args(2), 2, "draft_gemv_fast2_kernel<2>"), (args(2), 3, "draft_gemv_runs_kernel<2,3>"),
     (args(1, 38), 1, "draft_gemv_runs_kernel<1,1>"), (args(2, 64, 4), 1, "draft_gemv_runs_kernel<2,1>"),
 ])
@@ -24,15 +25,28 @@ def test_gemv_kernel_name(a, nvec, name):
 
 def test_alu_roof_arithmetic():
     clk = types.SimpleNamespace(summary=lambda: {"sm_mhz": 2000.0})
-    r = bench.alu_roof(500.0, clk)
+    rec = {"lane_instr_per_elem": 23.0, "spec_bits_per_elem": 4.205, "shape": "28672 x 4096"}
+    r = bench.alu_roof(500.0, clk, rec)
     peak = 152 * 128 * 2000e6
     elems = 500e9 / (4.205 / 8)
     assert r["bound"] == "alu"
     assert r["peak"] == pytest.approx(peak / 1e12, abs=0.01)
-    assert r["achieved"] == pytest.approx(bench.PROFILED_LANE_INSTR_PER_ELEM * elems / 1e12, abs=0.01)
+    assert r["achieved"] == pytest.approx(23.0 * elems / 1e12, abs=0.01)
     assert r["frac"] == pytest.approx(r["achieved"] / r["peak"], abs=1e-3)
     budget = peak / (0.75 * bench.peaks()[0] * 1e9 / (4.205 / 8))
     assert r["budget_at_75pct_hbm"] == pytest.approx(budget, abs=0.01)
+    assert bench.alu_roof(500.0, clk, None) is None
+
+
+def test_profiled_record_needs_matching_source_hash(monkeypatch):
+    h = bench.source_hash()
+    rec = {"source_sha16": h, "traffic_ratio": 1.0, "lane_instr_per_elem": 1.0, "spec_bits_per_elem": 4.2,
+           "shape": "x"}
+    monkeypatch.setitem(bench.PROFILED, "k<1>", rec)
+    assert bench.profiled_record("k<1>") is rec
+    monkeypatch.setitem(bench.PROFILED, "k<1>", dict(rec, source_sha16="0" * 16))
+    assert bench.profiled_record("k<1>") is None
+    assert bench.profiled_record("absent<1>") is None
 
 
 class FakeKV:
