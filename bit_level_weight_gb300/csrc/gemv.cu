@@ -739,7 +739,9 @@ __device__ __noinline__ void word_fallback(WView w, int64_t s, const uint8_t* lu
   __syncwarp();
 }
 
-// 32 registers per thread (8 CTAs of 256 per SM).
+// 32 registers per thread (8 CTAs of 256 per SM); superblocks for the generic
+// decoder wait in a per-warp list in shared memory until the warp's run is
+// done, so nothing of that decoder is live in the hot loop.
 template <int NV>
 __global__ void __launch_bounds__(kThreads, 8) draft_gemv_word_kernel(GemvArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -782,6 +784,9 @@ __global__ void __launch_bounds__(kThreads, 8) draft_gemv_word_kernel(GemvArgs a
   const uint32_t lim = (uint32_t)a.sexp_words;
   const int blk = lane >> 2;
   const uint32_t x_a = smem_addr(xs) + 4u * (uint32_t)(lane * kXGroup);
+  int* fb = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(&sc) + sizeof(WordScratch) * (kWarps - warp)) +
+            warp * per;  // this warp's list of superblocks for the generic decoder
+  int nfb = 0;
   int n = s0 / nsr, j = s0 - n * nsr;
   float acc[NV];
 #pragma unroll
@@ -895,9 +900,11 @@ __global__ void __launch_bounds__(kThreads, 8) draft_gemv_word_kernel(GemvArgs a
       fast = !lng && ncodes >= 512 && !__any_sync(CAS_FULL, bad);
     }
     __syncwarp();
-    if (!fast) {
-      word_fallback<NV>(w, s, lut8, sc.code, xs + j * (32 * kXGroup) + lane * kXGroup, xfl, part);
-      if (lane < 8) sc.ws.rec[64 + lane] = 0u;  // the generic decoder used the scratch
+    if (!fast) {  // decoded after the run; nothing of it is added now
+      if (lane == 0) fb[nfb] = s;
+      ++nfb;
+#pragma unroll
+      for (int q = 0; q < NV; ++q) part[q] = 0.f;
     }
 #pragma unroll
     for (int q = 0; q < NV; ++q) acc[q] += part[q];
@@ -915,22 +922,46 @@ __global__ void __launch_bounds__(kThreads, 8) draft_gemv_word_kernel(GemvArgs a
       }
     }
   }
+  // superblocks the word walk did not take: the generic decoder, one row
+  // segment each
+  __syncwarp();
+  for (int i = 0; i < nfb; ++i) {
+    const int sf = fb[i];
+    const int nf = sf / nsr, jf = sf - nf * nsr;
+    float part[NV];
+    word_fallback<NV>(w, sf, lut8, sc.code, xs + jf * (32 * kXGroup) + lane * kXGroup, xfl, part);
+#pragma unroll
+    for (int q = 0; q < NV; ++q) {
+      const float r = warp_sumf(part[q]);
+      if (lane == 0) atomicAdd(a.y + (int64_t)q * w.N + nf, r);
+    }
+  }
 }
 
 template <int NV>
 size_t word_smem(int64_t K) {
   return (size_t)NV * word_x_floats((int)K) * 4 + kWarps * sizeof(WordScratch);
 }
+// superblocks per warp of a launch with g CTAs
+inline int word_per(int64_t nsb, int g) { return (int)((nsb + (int64_t)g * kWarps - 1) / ((int64_t)g * kWarps)); }
 
 template <int NV>
 int launch_word(const GemvArgs& a, cudaStream_t st) {
-  const size_t smem = word_smem<NV>(a.w.K);
   auto kern = draft_gemv_word_kernel<NV>;
-  int per_sm = occupancy((const void*)kern, kThreads, smem);
-  if (per_sm < 1) return CAS_ERR_CUDA;
+  // the smem of the fallback lists depends on the grid, the grid on the
+  // occupancy: size the lists for the largest grid that can be resident
+  const int max_per_sm = occupancy((const void*)kern, kThreads, word_smem<NV>(a.w.K));
+  if (max_per_sm < 1) return CAS_ERR_CUDA;
   // at least 4 superblocks per warp: each CTA stages x once
-  int64_t need = (a.w.nsb + 4 * kWarps - 1) / (4 * kWarps);
-  int g = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sm_count() * per_sm));
+  const int64_t need = (a.w.nsb + 4 * kWarps - 1) / (4 * kWarps);
+  int g = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sm_count() * max_per_sm));
+  size_t smem = word_smem<NV>(a.w.K) + (size_t)kWarps * word_per(a.w.nsb, g) * sizeof(int);
+  const int per_sm = occupancy((const void*)kern, kThreads, smem);
+  if (per_sm < 1) return CAS_ERR_CUDA;
+  if ((int64_t)g > (int64_t)sm_count() * per_sm) {  // the lists cost a resident CTA per SM
+    g = sm_count() * per_sm;
+    smem = word_smem<NV>(a.w.K) + (size_t)kWarps * word_per(a.w.nsb, g) * sizeof(int);
+  }
   kern<<<g, kThreads, smem, st>>>(a);
   return launch_status();
 }
