@@ -16,6 +16,11 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libcas.so")
+# The CAS_DEBUG variant: device code also records inconsistent encoded data
+# (superblock indices that decrease or run past their section) in a flag read
+# by cas_device_status. Same C ABI; built on request only.
+OUT_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(HERE, "libcas_debug.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -30,15 +35,15 @@ def _inputs() -> list[str]:
     return sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + [os.path.join(ROOT, "include", "cas.h")]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
-def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(OUT, os.path.basename(src) + ".o")
+def _compile(src: str, extra: list[str], out: str = OUT) -> str:
+    obj = os.path.join(out, os.path.basename(src) + ".o")
     cmd = [NVCC, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -46,24 +51,26 @@ def _compile(src: str, extra: list[str]) -> str:
     return obj
 
 
-def build(force: bool = False, extra: list[str] | None = None, verbose: bool = False) -> str:
-    """Compile every kernel for sm_103a and link libcas.so; returns its path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(OUT, exist_ok=True)
-    extra = list(extra or [])
+def build(force: bool = False, extra: list[str] | None = None, verbose: bool = False, debug: bool = False) -> str:
+    """Compile every kernel for sm_103a and link libcas.so (debug: the
+    CAS_DEBUG variant libcas_debug.so); returns its path."""
+    lib, out = (LIB_DEBUG, OUT_DEBUG) if debug else (LIB, OUT)
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(out, exist_ok=True)
+    extra = list(extra or []) + (["-DCAS_DEBUG"] if debug else [])
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), srcs))
-    tmp = LIB + f".{os.getpid()}.tmp"
+        objs = list(ex.map(lambda s: _compile(s, extra, out), srcs))
+    tmp = lib + f".{os.getpid()}.tmp"
     cmd = [NVCC, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     if verbose:
-        print(f"built {LIB}")
-    return LIB
+        print(f"built {lib}")
+    return lib
 
 
 if __name__ == "__main__":

@@ -1,6 +1,7 @@
 // api.cu - status strings, argument checks and descriptor views of libcas.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 #include <unordered_map>
@@ -16,6 +17,7 @@ extern "C" const char* cas_status_str(int s) {
     case CAS_ERR_CAPACITY: return "KV cache capacity exhausted";
     case CAS_ERR_CUDA: return "CUDA error";
     case CAS_ERR_BUFFER: return "buffer or workspace too small";
+    case CAS_ERR_CORRUPT: return "encoded data inconsistent";
     case CAS_ERR_TIMEOUT: return "bounded device wait gave up";
     default: return "unknown status";
   }
@@ -40,6 +42,9 @@ extern "C" int cas_test_first_wait_spins(uint32_t spins) {
 extern "C" int cas_device_status(void* stream) {
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return CAS_ERR_CUDA;
   int s = cas::gemv_wait_status(true);
+  const int c[3] = {cas::corrupt_status_gemv(true), cas::corrupt_status_gemm(true), cas::corrupt_status_decode(true)};
+  for (int v : c)
+    if (!s) s = v;
   return s;
 }
 
@@ -130,6 +135,11 @@ WView make_view(const cas_weights* W) {
   v.rec_q = rec_words(v.k, v.m + 2);
   v.rec_lo = rec_words(v.k, 7 - v.m);
   v.rec_pr = rec_words(CAS_BLK - v.k, 8);
+  auto words = [&](int sec) { return (uint32_t)std::min<uint64_t>(W->len[sec] / 4, 0xFFFFFFFFull); };
+  v.lim_sexp = words(CAS_SEC_SPEC_EXP);
+  v.lim_vexp = words(CAS_SEC_VER_EXP);
+  v.lim_vd = words(CAS_SEC_VER_D);
+  v.lim_vres = words(CAS_SEC_VER_RES);
   return v;
 }
 

@@ -39,6 +39,8 @@ struct WView {
   int nbr, nsr;
   int variant, k, m;
   int rec_sm, rec_q, rec_lo, rec_pr;
+  // words of each variable-length stream section (reads stay below these)
+  uint32_t lim_sexp, lim_vexp, lim_vd, lim_vres;
 };
 
 struct Lut {
@@ -230,6 +232,26 @@ __device__ __forceinline__ uint32_t gather_mask_word(uint32_t nib, int lane) {
   return word;
 }
 
+// ------------------------------------------------------------------ stream indices
+#ifdef CAS_DEBUG
+// Debug builds: set when a superblock index is not non-decreasing or points
+// past its section (one flag per translation unit, read by cas_device_status).
+static __device__ int g_corrupt_status = 0;
+#endif
+
+// Word range [a, b) of superblock s of a variable-length stream whose index
+// is idx and whose section holds lim words. A corrupted index cannot move a
+// read outside the section: b is clamped to lim and a to b.
+__device__ __forceinline__ void stream_range(const uint32_t* __restrict__ idx, int64_t s, uint32_t lim, uint32_t& a,
+                                             uint32_t& b) {
+  const uint32_t a0 = __ldg(idx + s), b0 = __ldg(idx + s + 1);
+  b = min(b0, lim);
+  a = min(a0, b);
+#ifdef CAS_DEBUG
+  if (a0 > b0 || b0 > lim) atomicExch(&g_corrupt_status, CAS_ERR_CORRUPT);
+#endif
+}
+
 // ------------------------------------------------------------------ bounded waits
 // Spin limits: a wait that runs out returns false; the caller records a status
 // and leaves the kernel instead of hanging the GPU.
@@ -286,6 +308,11 @@ namespace cas {
 WView make_view(const cas_weights* W);
 bool aligned16(const void* p);
 int check_weights(const cas_weights* W);
+// Reads (and with clear, resets) the debug build's corrupt-index flag of the
+// translation unit that defines it; 0 in other builds.
+int corrupt_status_gemv(bool clear);
+int corrupt_status_gemm(bool clear);
+int corrupt_status_decode(bool clear);
 int sm_count();
 int launch_status();
 // Resident CTAs per SM of `func` with `threads` threads and `smem` dynamic

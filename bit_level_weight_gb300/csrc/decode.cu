@@ -56,6 +56,22 @@ int run_decode(const cas_weights* W, uint16_t* out, void* stream) {
 }
 
 }  // namespace
+
+int corrupt_status_decode(bool clear) {
+#ifdef CAS_DEBUG
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_corrupt_status, sizeof(int)) != cudaSuccess) return CAS_ERR_CUDA;
+  if (clear && v) {
+    const int z = 0;
+    cudaMemcpyToSymbol(g_corrupt_status, &z, sizeof(int));
+  }
+  return v;
+#else
+  (void)clear;
+  return 0;
+#endif
+}
+
 }  // namespace cas
 
 extern "C" int cas_decode_draft(const cas_weights* W, uint16_t* out, void* stream) {

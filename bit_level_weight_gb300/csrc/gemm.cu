@@ -93,21 +93,26 @@ __global__ void __launch_bounds__(kThreads, 4) verify_gemm_kernel(GemmArgs a) {
       if (n < w.N && MODE != 0) {
         const int64_t s = n * w.nsr + j;
         const int64_t gb0 = n * w.nbr + CAS_SB * j;
-        const uint32_t v0 = __ldg(w.vidx + s), v1 = __ldg(w.vidx + s + 1);
+        uint32_t v0, v1;
+        stream_range(w.vidx, s, w.lim_vexp, v0, v1);
         if (VAR == 2) {
-          const uint32_t d0 = __ldg(w.vdidx + s), d1 = __ldg(w.vdidx + s + 1);
+          uint32_t d0, d1, r0, r1;
+          stream_range(w.vdidx, s, w.lim_vd, d0, d1);
+          stream_range(w.vresidx, s, w.lim_vres, r0, r1);
           done = runs_sb_tile_c2<true>(w.mask + gb0 * 4, w.sq + gb0 * w.rec_q, w.rec_q, w.smx + gb0 * 4,
-                                       w.vd + d0, (int)(d1 - d0), w.vres + __ldg(w.vresidx + s),
+                                       w.vd + d0, (int)(d1 - d0), w.vres + r0,
                                        w.vpr + gb0 * w.rec_pr, w.rec_pr, w.vexp + v0, (int)(v1 - v0), w.k, w.m,
                                        s_lut, *reinterpret_cast<TileStage2*>(wscr), tile + r * kTileStride,
                                        kBlkStride, lane);
         } else if (MODE == 1) {
-          const uint32_t a0 = __ldg(w.sidx + s), a1 = __ldg(w.sidx + s + 1);
+          uint32_t a0, a1;
+          stream_range(w.sidx, s, w.lim_sexp, a0, a1);
           done = word_tile<true>(w.mask + gb0 * 4, w.ssm + gb0 * 8, w.vlo + gb0 * 8, w.vpr + gb0 * 16,
                                  w.sexp + a0, (int)(a1 - a0), w.vexp + v0, (int)(v1 - v0), s_lut,
                                  *reinterpret_cast<WordTileStage*>(wscr), tile + r * kTileStride, kBlkStride, lane);
         } else {
-          const uint32_t a0 = __ldg(w.sidx + s), a1 = __ldg(w.sidx + s + 1);
+          uint32_t a0, a1;
+          stream_range(w.sidx, s, w.lim_sexp, a0, a1);
           done = runs_sb_tile<true>(w.mask + gb0 * 4, w.ssm + gb0 * w.rec_sm, w.rec_sm, w.vlo + gb0 * w.rec_lo,
                                     w.rec_lo, w.vpr + gb0 * w.rec_pr, w.rec_pr, w.sexp + a0, (int)(a1 - a0),
                                     w.vexp + v0, (int)(v1 - v0), w.k, w.m, s_lut, ts.us, ts.kpos,
@@ -203,6 +208,21 @@ int launch(const GemmArgs& a, cudaStream_t st) {
 }
 
 }  // namespace
+
+int corrupt_status_gemm(bool clear) {
+#ifdef CAS_DEBUG
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_corrupt_status, sizeof(int)) != cudaSuccess) return CAS_ERR_CUDA;
+  if (clear && v) {
+    const int z = 0;
+    cudaMemcpyToSymbol(g_corrupt_status, &z, sizeof(int));
+  }
+  return v;
+#else
+  (void)clear;
+  return 0;
+#endif
+}
 }  // namespace cas
 
 using namespace cas;

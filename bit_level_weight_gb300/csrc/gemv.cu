@@ -795,7 +795,8 @@ __global__ void __launch_bounds__(kThreads, 8) draft_gemv_word_kernel(GemvArgs a
     const int64_t gb0 = (int64_t)s * CAS_SB;
     const uint32_t mw = __ldg(w.mask + gb0 * 4 + lane);
     const uint2 rr = __ldg(reinterpret_cast<const uint2*>(w.ssm + gb0 * 8) + lane);
-    const uint32_t sb1 = min(__ldg(w.sidx + s + 1), lim), sb0 = min(__ldg(w.sidx + s), sb1);
+    uint32_t sb0, sb1;
+    stream_range(w.sidx, s, lim, sb0, sb1);
     const int nw = (int)(sb1 - sb0);
     float part[NV];
 #pragma unroll
@@ -1003,6 +1004,21 @@ int dispatch(const GemvArgs& a, int nvec, cudaStream_t st) {
 
 int set_first_wait_spins(uint32_t spins) {
   return cudaMemcpyToSymbol(g_first_wait_spins, &spins, sizeof(spins)) == cudaSuccess ? CAS_OK : CAS_ERR_CUDA;
+}
+
+int corrupt_status_gemv(bool clear) {
+#ifdef CAS_DEBUG
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_corrupt_status, sizeof(int)) != cudaSuccess) return CAS_ERR_CUDA;
+  if (clear && v) {
+    const int z = 0;
+    cudaMemcpyToSymbol(g_corrupt_status, &z, sizeof(int));
+  }
+  return v;
+#else
+  (void)clear;
+  return 0;
+#endif
 }
 
 int gemv_wait_status(bool clear) {

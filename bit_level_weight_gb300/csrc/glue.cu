@@ -23,7 +23,10 @@ __device__ __forceinline__ uint16_t to_bf16(float f) { return __bfloat16_as_usho
 
 // ---------------------------------------------------------------- add + RMSNorm
 // x[r] += y[r] (when y is given), then out[r] = bf16(x[r] / sqrt(mean(x[r]^2) + eps) * gamma).
-constexpr int kNormThreads = 256;
+// One CTA of 1024 threads per row; a thread keeps its <= kNormVpt values in
+// registers, so the row is read and written once.
+constexpr int kNormThreads = 1024;
+constexpr int kNormVpt = 16;  // dim <= 16384
 __global__ void __launch_bounds__(kNormThreads) add_rmsnorm_kernel(float* __restrict__ x, const float* __restrict__ y,
                                                                    int dim, const uint16_t* __restrict__ gamma,
                                                                    float eps, uint16_t* __restrict__ out) {
@@ -31,33 +34,53 @@ __global__ void __launch_bounds__(kNormThreads) add_rmsnorm_kernel(float* __rest
   const int64_t r = blockIdx.x;
   float* xr = x + r * dim;
   const float* yr = y ? y + r * dim : nullptr;
+  float v[kNormVpt];
   float ss = 0.f;
-  for (int i = threadIdx.x; i < dim; i += kNormThreads) {
-    float v = xr[i];
-    if (yr) {
-      v += yr[i];
-      xr[i] = v;
+#pragma unroll
+  for (int k = 0; k < kNormVpt; ++k) {
+    const int i = threadIdx.x + k * kNormThreads;
+    v[k] = 0.f;
+    if (i < dim) {
+      v[k] = xr[i];
+      if (yr) {
+        v[k] += yr[i];
+        xr[i] = v[k];
+      }
     }
-    ss = fmaf(v, v, ss);
+    ss = fmaf(v[k], v[k], ss);
   }
   ss = warp_sumf(ss);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   __syncthreads();
-  float tot = 0.f;
-#pragma unroll
-  for (int w = 0; w < kNormThreads / 32; ++w) tot += red[w];
+  float tot = (threadIdx.x & 31) < kNormThreads / 32 ? red[threadIdx.x & 31] : 0.f;
+  tot = warp_sumf(tot);
   const float inv = rsqrtf(tot / (float)dim + eps);
-  for (int i = threadIdx.x; i < dim; i += kNormThreads) out[r * dim + i] = to_bf16(xr[i] * inv * bf2f(gamma[i]));
+#pragma unroll
+  for (int k = 0; k < kNormVpt; ++k) {
+    const int i = threadIdx.x + k * kNormThreads;
+    if (i < dim) out[r * dim + i] = to_bf16(v[k] * inv * bf2f(gamma[i]));
+  }
 }
 
 // ---------------------------------------------------------------- QKV split + rotary embedding
 // qkv: fp32 [rows][(Hq + 2 Hkv) * 128] (q heads, then k heads, then v heads).
 // Pairs (i, i + 64) of a q or k head rotate by angle p * theta^(-i/64):
 // (a, b) -> (a cos - b sin, b cos + a sin); p = pos0 + row % rows_per_seq.
+// The 64 sines and cosines of the row's position are taken once per block.
 __global__ void rope_split_kernel(const float* __restrict__ qkv, int Hq, int Hkv, int64_t pos0, int rows_per_seq,
                                   double log_theta, uint16_t* __restrict__ q, uint16_t* __restrict__ k,
                                   int64_t k_stride, uint16_t* __restrict__ v, int64_t v_stride) {
+  __shared__ float cs[64], sn[64];
   const int r = blockIdx.y;
+  if (threadIdx.x < 64) {
+    const double p = (double)(pos0 + r % rows_per_seq);
+    const double ang = p * exp(-log_theta * (double)threadIdx.x / 64.0);
+    double sd, cd;
+    sincos(fmod(ang, 6.283185307179586476925286766559), &sd, &cd);
+    cs[threadIdx.x] = (float)cd;
+    sn[threadIdx.x] = (float)sd;
+  }
+  __syncthreads();
   const int H = Hq + 2 * Hkv;
   const int t = blockIdx.x * blockDim.x + threadIdx.x;  // (head, pair)
   if (t >= H * 64) return;
@@ -70,11 +93,7 @@ __global__ void rope_split_kernel(const float* __restrict__ qkv, int Hq, int Hkv
     d[i + 64] = to_bf16(b);
     return;
   }
-  const double p = (double)(pos0 + r % rows_per_seq);
-  const double ang = p * exp(-log_theta * (double)i / 64.0);
-  double sd, cd;
-  sincos(fmod(ang, 6.283185307179586476925286766559), &sd, &cd);
-  const float s = (float)sd, c = (float)cd;
+  const float s = sn[i], c = cs[i];
   uint16_t* d = h < Hq ? q + ((int64_t)r * Hq + h) * CAS_BLK : k + (int64_t)r * k_stride + (int64_t)(h - Hq) * CAS_BLK;
   d[i] = to_bf16(fmaf(a, c, -b * s));
   d[i + 64] = to_bf16(fmaf(b, c, a * s));
@@ -157,7 +176,7 @@ using namespace cas;
 
 extern "C" int cas_add_rmsnorm(float* x, const float* y, int rows, int dim, const uint16_t* gamma, float eps,
                                uint16_t* out, void* stream) {
-  if (rows < 0 || dim < 1 || !(eps >= 0.f)) return CAS_ERR_INVALID;
+  if (rows < 0 || dim < 1 || dim > kNormThreads * kNormVpt || !(eps >= 0.f)) return CAS_ERR_INVALID;
   if (rows == 0) return CAS_OK;
   if (!x || !gamma || !out) return CAS_ERR_INVALID;
   add_rmsnorm_kernel<<<rows, kNormThreads, 0, (cudaStream_t)stream>>>(x, y, dim, gamma, eps, out);

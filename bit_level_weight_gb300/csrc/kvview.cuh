@@ -79,6 +79,10 @@ __device__ inline WView kv_stream_view(const KvDev& d, int st, int64_t n) {
   w.rec_q = d.rec_q;
   w.rec_lo = d.rec_lo;
   w.rec_pr = d.rec_pr;
+  w.lim_sexp = (uint32_t)(d.variant == 1 ? d.cap_a : 0);
+  w.lim_vd = (uint32_t)(d.variant == 2 ? d.cap_a : 0);
+  w.lim_vexp = (uint32_t)d.cap_b;
+  w.lim_vres = (uint32_t)d.cap_c;
   return w;
 }
 

@@ -50,18 +50,22 @@ __device__ __forceinline__ SbInfo sb_prepare(const WView& w, int64_t s, const ui
   in.uo = warp_incl_add(pc, lane) - pc;
   in.rbit = 0;
   if (VAR == 1) {
-    uint32_t a = __ldg(w.sidx + s), b = __ldg(w.sidx + s + 1);
+    uint32_t a, b;
+    stream_range(w.sidx, s, w.lim_sexp, a, b);
     warp_decode_unary(w.sexp + a, (int)(b - a), lut, sc.code, in.nb * w.k, lane);
   } else if (FULL) {
-    uint32_t a = __ldg(w.vdidx + s), b = __ldg(w.vdidx + s + 1);
+    uint32_t a, b;
+    stream_range(w.vdidx, s, w.lim_vd, a, b);
     warp_decode_unary_raw(w.vd + a, (int)(b - a), sc.code, in.nb * w.k, lane);
-    uint32_t ra = __ldg(w.vresidx + s), rb = __ldg(w.vresidx + s + 1);
+    uint32_t ra, rb;
+    stream_range(w.vresidx, s, w.lim_vres, ra, rb);
     int nres = min((int)(rb - ra), kResWords - 2);
     for (int i = lane; i < nres; i += 32) sc.res[i] = __ldg(w.vres + ra + i);
     if (lane < 2) sc.res[nres + lane] = 0u;
   }
   if (FULL) {
-    uint32_t a = __ldg(w.vidx + s), b = __ldg(w.vidx + s + 1);
+    uint32_t a, b;
+    stream_range(w.vidx, s, w.lim_vexp, a, b);
     warp_decode_unary(w.vexp + a, (int)(b - a), lut, sc.vcode, in.nb * (CAS_BLK - w.k), lane);
   }
   __syncwarp();

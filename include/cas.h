@@ -50,6 +50,7 @@ typedef enum {
   CAS_ERR_CAPACITY = -4,  /* KV cache full (tokens or code stream words)    */
   CAS_ERR_CUDA = -5,      /* CUDA launch / runtime error                     */
   CAS_ERR_BUFFER = -6,    /* buffer or workspace smaller than required       */
+  CAS_ERR_CORRUPT = -7,   /* encoded data inconsistent (debug builds)        */
   CAS_ERR_TIMEOUT = -8    /* a bounded device-side wait gave up              */
 } cas_status;
 
@@ -104,10 +105,14 @@ typedef struct cas_weights {
 
 const char* cas_status_str(int status);
 
-/* Reads and clears the flags that bounded device-side waits set (a TMA
- * staging copy that did not complete within its spin limit). Synchronises
- * `stream`. Returns CAS_OK or CAS_ERR_TIMEOUT (CAS_ERR_CUDA on a runtime
- * error). */
+/* Reads and clears the flags that device code sets: a bounded wait that gave
+ * up (a TMA staging copy that did not complete within its spin limit:
+ * CAS_ERR_TIMEOUT) and, in a library built with CAS_DEBUG, a superblock index
+ * of an encoded tensor that decreases or points past its section
+ * (CAS_ERR_CORRUPT; every build clamps such reads to the section, so corrupt
+ * data gives wrong values but no read outside the buffer). Synchronises
+ * `stream`. Returns CAS_OK, the first flag set, or CAS_ERR_CUDA on a runtime
+ * error. */
 int cas_device_status(void* stream);
 /* Failure-detection test hook, not for production use. The draft GEMV
  * kernels that stage x in shared memory by a bulk copy wait for that copy
@@ -339,7 +344,7 @@ int cas_verify_attn(const cas_kv* const* kv, int batch, const uint16_t* q, int T
  * x += y (skipped when y is NULL), then
  * out = bf16(x / sqrt(mean(x^2) + eps) * gamma). x: fp32 [rows][dim], updated
  * in place; y: fp32 [rows][dim] or NULL; gamma: bf16 [dim]; out: bf16
- * [rows][dim]. */
+ * [rows][dim]; dim at most 16384. */
 int cas_add_rmsnorm(float* x, const float* y, int rows, int dim, const uint16_t* gamma, float eps,
                     uint16_t* out, void* stream);
 
