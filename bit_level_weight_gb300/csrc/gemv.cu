@@ -946,6 +946,370 @@ size_t word_smem(int64_t K) {
 // superblocks per warp of a launch with g CTAs
 inline int word_per(int64_t nsb, int g) { return (int)((nsb + (int64_t)g * kWarps - 1) / ((int64_t)g * kWarps)); }
 
+// ------------------------------------------------------------------ block path
+// Cassandra-1, k = 64, m = 3, rows of whole superblocks with at least 32
+// blocks (K >= 4096), 1 or 2 vectors. A warp takes a chunk of 32 consecutive
+// blocks (4 superblocks) and lane L owns block L of it: 128 positions with
+// exactly 64 kept values, so every lane decodes the same number of values.
+// Per chunk the warp stages the 4 superblocks' code streams and its blocks'
+// bit-reversed mask words in shared memory; each lane finds where its block's
+// codes start (the bit after the (64 j)-th '1' of its superblock's stream, j
+// the block's place in it) by a warp popcount scan and a shuffle search, and
+// then walks two cursors of its own, re-aligned every 8 values:
+//   position: a 64-bit window of the mask at the last found position, whose
+//             bit (the top bit) is cleared; the count of leading zeros is the
+//             distance to the next kept position, the window shifts by it;
+//   exponent: the same over the code stream at the last code's terminating
+//             '1': the count of leading zeros is rank + 1.
+// A window that runs dry (the next '1' outside it, a gap of 32 or more
+// positions, a code of rank 31 or more) yields a count of 32 - the only
+// count with bit 5 set - so OR-ing every count finds all of them at once; the
+// chunk's sums are then dropped and its superblocks go to the generic decoder
+// after the warp's run. x is staged per CTA as fp32 with 129 floats per block,
+// so position p of block b sits on bank (b + p) % 32 and the 32 lanes, which
+// advance through their blocks at about the same pace, spread over the banks.
+constexpr int kBThreads = 512;
+constexpr int kBWarps = kBThreads / 32;
+constexpr int kBXRow = CAS_BLK + 1;   // staged floats per block
+constexpr int kBXPad = 2048;          // bytes after x: reads of a failed walk stay inside
+constexpr int kBStreamWords = 2 + 64 + 4;  // 2 zero words, up to 64 stream words, 4 zero words
+constexpr int kBMaskRows = 7;         // zero row, 4 mask words, 2 zero rows
+
+struct BlockStage {
+  uint32_t st[4][kBStreamWords];  // the chunk's code streams
+  uint32_t ms[kBMaskRows][32];    // row 1 + i, column l: bit-reversed mask word i of lane l's block
+  uint32_t fs[8][32];             // row i, column l: word i of the sign/mantissa record of lane l's block
+};
+static_assert(sizeof(BlockStage) >= CAS_SB * CAS_BLK, "the generic decoder's scratch overlays the stage");
+static_assert(sizeof(BlockStage) % 16 == 0, "stage alignment");
+
+__host__ __device__ constexpr int block_x_floats(int nbr) { return (nbr * kBXRow + 3) & ~3; }
+
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+  uint32_t v;
+  asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+
+// 64-bit window (H, L) of a staged MSB-first bitstream at bit q: the word
+// rows are `stride` bytes apart starting at address `base`; H's top bit (the
+// last consumed '1') is cleared.
+__device__ __forceinline__ void bwindow(uint32_t base, uint32_t stride, int q, int maxw, uint32_t& H, uint32_t& L) {
+  const int hw = min(q >> 5, maxw), sh = q & 31;
+  const uint32_t a = base + stride * (uint32_t)hw;
+  const uint32_t w0 = lds_u32(a), w1 = lds_u32(a + stride), w2 = lds_u32(a + 2u * stride);
+  H = __funnelshift_l(w1, w0, sh) & 0x7FFFFFFFu;
+  L = __funnelshift_l(w2, w1, sh);
+}
+
+// Index of the first '1' at or after bit b of a staged MSB-first bitstream
+// (word rows `stride` bytes apart, rows 0..maxw), or -1.
+__device__ __forceinline__ int bnext_one(uint32_t base, uint32_t stride, int b, int maxw) {
+  int wi = b >> 5;
+  if (wi > maxw) return -1;
+  uint32_t h = lds_u32(base + stride * (uint32_t)wi) << (b & 31);
+  int pos = b;
+  while (h == 0u) {
+    if (++wi > maxw) return -1;
+    h = lds_u32(base + stride * (uint32_t)wi);
+    pos = 32 * wi;
+  }
+  return pos + (int)__clz(h);
+}
+
+// The block walk without windows: every position and code found by a scan
+// of the staged words, so gaps and codes of any length are taken. For a lane
+// whose windowed walk ran dry; false when the staged data runs out (the
+// encoding is inconsistent).
+template <int NV>
+struct ScanSum {
+  float part[NV];
+  bool ok;
+};
+template <int NV>
+__device__ __noinline__ ScanSum<NV> block_walk_scan(uint32_t ms_a, uint32_t st_a, uint32_t fs_a, uint32_t lut_a,
+                                                    uint32_t xbase, int xfl, int cq0) {
+  ScanSum<NV> r;
+  int cur = -1, qc = cq0;
+#pragma unroll
+  for (int q = 0; q < NV; ++q) r.part[q] = 0.f;
+  r.ok = false;
+  for (int i = 0; i < 64; ++i) {
+    const int pb = bnext_one(ms_a, 128u, 32 + cur + 1, kBMaskRows - 1);
+    const int tb = bnext_one(st_a, 4u, qc + 1, kBStreamWords - 1);
+    if (pb < 0 || pb >= 32 + CAS_BLK || tb < 0) return r;
+    cur = pb - 32;
+    const uint32_t E = lds_u32(lut_a + 4u * (uint32_t)min(tb - qc, 256));  // rank tb - qc - 1
+    qc = tb;
+    const uint32_t f = (lds_u32(fs_a + 128u * (uint32_t)(i >> 3)) >> (4 * (i & 7))) & 15u;
+    const float val = __uint_as_float(((f & 8u) << 28) | E | ((f & 7u) << 20));
+#pragma unroll
+    for (int q = 0; q < NV; ++q) r.part[q] = fmaf(val, lds_f32(xbase + 4u * (uint32_t)(cur + q * xfl)), r.part[q]);
+  }
+  r.ok = true;
+  return r;
+}
+
+template <int NV>
+__global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint32_t lut32[256];  // exponent << 23 by rank
+  __shared__ uint8_t lut8[256];    // exponent by rank (generic decoder)
+  const WView& w = a.w;
+  const int K = (int)w.K;
+  const int nbr = w.nbr;
+  const int xfl = block_x_floats(nbr);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float* xs = reinterpret_cast<float*>(smem);
+  BlockStage& bs = reinterpret_cast<BlockStage*>(smem + (size_t)NV * xfl * 4 + kBXPad)[warp];
+
+  // x -> fp32, position p of vector v at v*xfl + (p/128)*129 + p%128
+  for (int v = 0; v < NV; ++v) {
+    const uint4* xv = reinterpret_cast<const uint4*>(a.x + (size_t)v * K);
+    for (int i = threadIdx.x; i < K / 8; i += kBThreads) {
+      const uint4 pr = __ldg(xv + i);
+      const int p = 8 * i;
+      float* d = xs + v * xfl + (p >> 7) * kBXRow + (p & 127);
+      d[0] = bf2f(pr.x & 0xFFFFu);
+      d[1] = bf2f(pr.x >> 16);
+      d[2] = bf2f(pr.y & 0xFFFFu);
+      d[3] = bf2f(pr.y >> 16);
+      d[4] = bf2f(pr.z & 0xFFFFu);
+      d[5] = bf2f(pr.z >> 16);
+      d[6] = bf2f(pr.w & 0xFFFFu);
+      d[7] = bf2f(pr.w >> 16);
+    }
+  }
+  for (int i = threadIdx.x; i < kBXPad / 4; i += kBThreads) xs[NV * xfl + i] = 0.f;
+  for (int i = threadIdx.x; i < 256; i += kBThreads) {
+    lut32[i] = (uint32_t)a.lut.v[i] << 23;
+    lut8[i] = a.lut.v[i];
+  }
+  __syncthreads();
+
+  const int64_t nsb = w.nsb;
+  const int nch = (int)((nsb + 3) / 4);
+  const int nwarps = gridDim.x * kBWarps;
+  const int gw = blockIdx.x * kBWarps + warp;
+  const int per = (nch + nwarps - 1) / nwarps;
+  const int c0 = min(gw * per, nch), c1 = min(c0 + per, nch);
+  const uint32_t lim = (uint32_t)a.sexp_words;
+  const int t = lane >> 3, j = lane & 7;
+  const uint32_t ms_a = smem_addr(&bs.ms[0][lane]);
+  const uint32_t fs_a = smem_addr(&bs.fs[0][lane]);
+  const uint32_t st_a = smem_addr(&bs.st[t][0]);
+  const uint32_t lut_a = smem_addr(lut32) - 4u;  // rank c - 1 at lut_a + 4c
+  const uint32_t xs_a = smem_addr(xs);
+  int* fb = reinterpret_cast<int*>(smem + (size_t)NV * xfl * 4 + kBXPad + kBWarps * sizeof(BlockStage)) + warp * per;
+  int nfb = 0;
+  // zero rows and words of the stage, written once
+  if (lane < 4) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) bs.st[lane][i] = 0u;
+#pragma unroll
+    for (int i = 66; i < kBStreamWords; ++i) bs.st[lane][i] = 0u;
+  }
+  bs.ms[0][lane] = 0u;
+  bs.ms[5][lane] = 0u;
+  bs.ms[6][lane] = 0u;
+
+  for (int c = c0; c < c1; ++c) {
+    // the chunk's streams; a stream longer than the stage sends the chunk to
+    // the generic decoder
+    uint32_t sa[4];
+    int nw[4];
+    bool fast = true;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t su = (int64_t)c * 4 + u;
+      uint32_t a0 = 0u, b0 = 0u;
+      if (su < nsb) stream_range(w.sidx, su, lim, a0, b0);
+      sa[u] = a0;
+      nw[u] = (int)(b0 - a0);
+      fast = fast && nw[u] <= 64;
+    }
+    const int64_t g = (int64_t)c * 32 + lane;  // this lane's block
+    const bool valid = (int64_t)c * 4 + t < nsb;
+    const int64_t gl = valid ? g : (int64_t)c * 32;
+    if (fast) {
+      const uint4 mk = __ldg(reinterpret_cast<const uint4*>(w.mask) + gl);
+      const uint4 fA = __ldg(reinterpret_cast<const uint4*>(w.ssm + gl * 8));
+      const uint4 fB = __ldg(reinterpret_cast<const uint4*>(w.ssm + gl * 8) + 1);
+      int pc[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t* gs = w.sexp + sa[u];
+        const uint32_t s0 = 2 * lane < nw[u] ? __ldg(gs + 2 * lane) : 0u;
+        const uint32_t s1 = 2 * lane + 1 < nw[u] ? __ldg(gs + 2 * lane + 1) : 0u;
+        *reinterpret_cast<uint2*>(&bs.st[u][2 + 2 * lane]) = make_uint2(s0, s1);
+        pc[u] = __popc(s0) + __popc(s1);
+      }
+      bs.ms[1][lane] = valid ? __brev(mk.x) : 0u;
+      bs.ms[2][lane] = valid ? __brev(mk.y) : 0u;
+      bs.ms[3][lane] = valid ? __brev(mk.z) : 0u;
+      bs.ms[4][lane] = valid ? __brev(mk.w) : 0u;
+      bs.fs[0][lane] = fA.x;
+      bs.fs[1][lane] = fA.y;
+      bs.fs[2][lane] = fA.z;
+      bs.fs[3][lane] = fA.w;
+      bs.fs[4][lane] = fB.x;
+      bs.fs[5][lane] = fB.y;
+      bs.fs[6][lane] = fB.z;
+      bs.fs[7][lane] = fB.w;
+      // popcount prefixes of the 4 streams over word pairs, 16 bits each
+      const int S01 = warp_incl_add(pc[0] | (pc[1] << 16), lane);
+      const int S23 = warp_incl_add(pc[2] | (pc[3] << 16), lane);
+      const int T01 = __shfl_sync(CAS_FULL, S01, 31), T23 = __shfl_sync(CAS_FULL, S23, 31);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int ones = ((u < 2 ? T01 : T23) >> (16 * (u & 1))) & 0xFFFF;
+        if ((int64_t)c * 4 + u < nsb && ones < CAS_SB * 64) fast = false;
+      }
+      // pair holding the (64 j)-th '1' of stream t: pairs whose prefix, in
+      // units of 64, is below j
+      const int B01 = min((S01 & 0xFFFF) >> 6, 15) | (min((S01 >> 16) >> 6, 15) << 4);
+      const int B23 = min((S23 & 0xFFFF) >> 6, 15) | (min((S23 >> 16) >> 6, 15) << 4);
+      const int KB = B01 | (B23 << 8);
+      int lo = 0;
+#pragma unroll
+      for (int step = 16; step >= 1; step >>= 1) {
+        const int kb = __shfl_sync(CAS_FULL, KB, lo + step - 1);
+        if (((kb >> (4 * t)) & 15) < j) lo += step;
+      }
+      const int lp = min(lo, 31);
+      const int Sa = __shfl_sync(CAS_FULL, S01, lp), Sb = __shfl_sync(CAS_FULL, S23, lp);
+      const int Sp = ((t < 2 ? Sa : Sb) >> (16 * (t & 1))) & 0xFFFF;  // ones through pair lp
+      __syncwarp();
+      const uint32_t w0 = lds_u32(st_a + 4u * (uint32_t)(2 + 2 * lp)), w1 = lds_u32(st_a + 4u * (uint32_t)(3 + 2 * lp));
+      const int n0 = __popc(w0);
+      const int r = 64 * j - (Sp - n0 - __popc(w1));  // the one's rank inside the pair (1-based)
+      const bool in0 = r <= n0;
+      const int term = j == 0 ? -1 : 32 * (2 * lp + (in0 ? 0 : 1)) + select_msb(in0 ? w0 : w1, max(in0 ? r : r - n0, 1));
+      // cursors
+      const uint32_t gl32 = (uint32_t)gl, nr = gl32 / (uint32_t)nbr;  // row, and block gl32 - nr * nbr in it
+      const uint32_t xbase = xs_a + 4u * (gl32 - nr * (uint32_t)nbr) * kBXRow;
+      uint32_t xa = xbase - 4u;  // position -1
+      uint32_t Hp, Lp, Hc, Lc;
+      bwindow(ms_a, 128u, 31, kBMaskRows - 3, Hp, Lp);
+      const int cq0 = 64 + term;
+      bwindow(st_a, 4u, cq0, kBStreamWords - 3, Hc, Lc);
+      uint32_t used = 0u, cor = 0u;
+      float part[NV];
+#pragma unroll
+      for (int q = 0; q < NV; ++q) part[q] = 0.f;
+#pragma unroll
+      for (int gi = 0; gi < 8; ++gi) {
+        if (gi > 0) {
+          const int cur = min((int)(xa - xbase) >> 2, CAS_BLK - 1);
+          xa = xbase + 4u * (uint32_t)cur;
+          bwindow(ms_a, 128u, 32 + cur, kBMaskRows - 3, Hp, Lp);
+          bwindow(st_a, 4u, cq0 + (int)used, kBStreamWords - 3, Hc, Lc);
+        }
+        const uint32_t fo = lds_u32(fs_a + 128u * gi), fe = fo << 4;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t cp = __clz(Hp);  // distance to the next kept position
+          xa = mad32(cp, 4u, xa);
+          Hp = shfl_wrap(Lp, Hp, cp) & 0x7FFFFFFFu;
+          Lp = shfl_wrap(0u, Lp, cp);
+          const uint32_t cc = __clz(Hc);  // rank + 1
+          const uint32_t E = lds_u32(lut_a + 4u * cc);
+          Hc = shfl_wrap(Lc, Hc, cc) & 0x7FFFFFFFu;
+          Lc = shfl_wrap(0u, Lc, cc);
+          used += cc;
+          cor |= cp | cc;
+          const int by = i >> 1;
+          const uint32_t A = __byte_perm((i & 1) ? fo : fe, 0u, (by << 12) | (by << 8) | 0x44);
+          const float val = __uint_as_float((A & 0x80700000u) | E);
+#pragma unroll
+          for (int q = 0; q < NV; ++q) part[q] = fmaf(val, lds_f32(xa + 4u * (uint32_t)(q * xfl)), part[q]);
+        }
+      }
+      // a lane whose windows ran dry scans its block again (divergent, rare)
+      bool bad = false;
+      if (valid && (cor & 32u)) {
+        const ScanSum<NV> r = block_walk_scan<NV>(ms_a, st_a, fs_a, lut_a, xbase, xfl, cq0);
+#pragma unroll
+        for (int q = 0; q < NV; ++q) part[q] = r.part[q];
+        bad = !r.ok;
+      }
+      fast = fast && !__any_sync(CAS_FULL, bad);
+      if (fast) {
+        const uint32_t nA = __shfl_sync(CAS_FULL, nr, 0);
+        const uint32_t nB = __reduce_max_sync(CAS_FULL, valid ? nr : nA);  // rows of a chunk: nA and maybe nA + 1
+#pragma unroll
+        for (int q = 0; q < NV; ++q) {
+          const float v = valid ? part[q] : 0.f;
+          if (nA == nB) {
+            const float sA = warp_sumf(v);
+            if (lane == 0) atomicAdd(a.y + (int64_t)q * w.N + nA, sA);
+          } else {
+            const float sA = warp_sumf(nr == nA ? v : 0.f), sB = warp_sumf(nr == nA ? 0.f : v);
+            if (lane == 0) {
+              atomicAdd(a.y + (int64_t)q * w.N + nA, sA);
+              atomicAdd(a.y + (int64_t)q * w.N + nB, sB);
+            }
+          }
+        }
+      }
+      __syncwarp();
+    }
+    if (!fast) {  // decoded after the run; nothing of it was added
+      if (lane == 0) fb[nfb] = c;
+      ++nfb;
+    }
+  }
+  // chunks the block walk did not take: the generic decoder, one superblock
+  // at a time
+  __syncwarp();
+  uint8_t* code = reinterpret_cast<uint8_t*>(&bs);
+  for (int i = 0; i < nfb; ++i) {
+    const int cf = fb[i];
+    for (int u = 0; u < 4; ++u) {
+      const int64_t sf = (int64_t)cf * 4 + u;
+      if (sf >= nsb) break;
+      const int64_t nf = sf / w.nsr;
+      const int jf = (int)(sf - nf * w.nsr);
+      float part[NV];
+      word_fallback<NV>(w, sf, lut8, code, xs + (jf * CAS_SB + (lane >> 2)) * kBXRow + 32 * (lane & 3), xfl, part);
+#pragma unroll
+      for (int q = 0; q < NV; ++q) {
+        const float r = warp_sumf(part[q]);
+        if (lane == 0) atomicAdd(a.y + (int64_t)q * w.N + nf, r);
+      }
+    }
+  }
+}
+
+template <int NV>
+size_t block_smem(int64_t nbr) {
+  return (size_t)NV * block_x_floats((int)nbr) * 4 + kBXPad + kBWarps * sizeof(BlockStage);
+}
+// chunks per warp of a launch with g CTAs
+inline int block_per(int64_t nsb, int g) {
+  const int64_t nch = (nsb + 3) / 4;
+  return (int)((nch + (int64_t)g * kBWarps - 1) / ((int64_t)g * kBWarps));
+}
+
+template <int NV>
+int launch_block(const GemvArgs& a, cudaStream_t st) {
+  auto kern = draft_gemv_block_kernel<NV>;
+  const int max_per_sm = occupancy((const void*)kern, kBThreads, block_smem<NV>(a.w.nbr));
+  if (max_per_sm < 1) return CAS_ERR_CUDA;
+  const int64_t nch = (a.w.nsb + 3) / 4;
+  const int64_t need = (nch + kBWarps - 1) / kBWarps;
+  int g = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sm_count() * max_per_sm));
+  size_t smem = block_smem<NV>(a.w.nbr) + (size_t)kBWarps * block_per(a.w.nsb, g) * sizeof(int);
+  const int per_sm = occupancy((const void*)kern, kBThreads, smem);
+  if (per_sm < 1) return CAS_ERR_CUDA;
+  if ((int64_t)g > (int64_t)sm_count() * per_sm) {
+    g = sm_count() * per_sm;
+    smem = block_smem<NV>(a.w.nbr) + (size_t)kBWarps * block_per(a.w.nsb, g) * sizeof(int);
+  }
+  kern<<<g, kBThreads, smem, st>>>(a);
+  return launch_status();
+}
+
 template <int NV>
 int launch_word(const GemvArgs& a, cudaStream_t st) {
   auto kern = draft_gemv_word_kernel<NV>;
@@ -973,6 +1337,8 @@ int launch_word(const GemvArgs& a, cudaStream_t st) {
 template <int VAR>
 int dispatch(const GemvArgs& a, int nvec, cudaStream_t st) {
   const bool fast = a.w.k == 64 && a.w.m == 3 && a.w.nbr % CAS_SB == 0;
+  if (fast && VAR == 1 && nvec <= 2 && a.w.nbr >= 32 && block_smem<2>(a.w.nbr) <= 200 * 1024)
+    return nvec == 1 ? launch_block<1>(a, st) : launch_block<2>(a, st);
   if (fast && VAR == 1 && nvec <= 2 && word_smem<2>(a.w.K) <= 200 * 1024)
     return nvec == 1 ? launch_word<1>(a, st) : launch_word<2>(a, st);
   if (fast && VAR == 1) {
