@@ -727,7 +727,7 @@ def gemv_kernel_name(args, nvec: int) -> str:
     """The draft GEMV kernel the stack's matrices (rows of whole superblocks) run."""
     if args.keep == 64 and args.mant == 3:
         if args.variant == 1:
-            return f"draft_gemv_word_kernel<{nvec}>" if nvec <= 2 else f"draft_gemv_fast_kernel<{nvec}>"
+            return f"draft_gemv_block_kernel<{nvec}>" if nvec <= 2 else f"draft_gemv_fast_kernel<{nvec}>"
         if nvec <= 2:
             return f"draft_gemv_fast2_kernel<{nvec}>"
     return f"draft_gemv_runs_kernel<{args.variant},{nvec}>"

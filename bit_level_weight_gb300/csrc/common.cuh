@@ -242,14 +242,16 @@ static __device__ int g_corrupt_status = 0;
 // Word range [a, b) of superblock s of a variable-length stream whose index
 // is idx and whose section holds lim words. A corrupted index cannot move a
 // read outside the section: b is clamped to lim and a to b.
-__device__ __forceinline__ void stream_range(const uint32_t* __restrict__ idx, int64_t s, uint32_t lim, uint32_t& a,
-                                             uint32_t& b) {
-  const uint32_t a0 = __ldg(idx + s), b0 = __ldg(idx + s + 1);
+__device__ __forceinline__ void stream_clamp(uint32_t a0, uint32_t b0, uint32_t lim, uint32_t& a, uint32_t& b) {
   b = min(b0, lim);
   a = min(a0, b);
 #ifdef CAS_DEBUG
   if (a0 > b0 || b0 > lim) atomicExch(&g_corrupt_status, CAS_ERR_CORRUPT);
 #endif
+}
+__device__ __forceinline__ void stream_range(const uint32_t* __restrict__ idx, int64_t s, uint32_t lim, uint32_t& a,
+                                             uint32_t& b) {
+  stream_clamp(__ldg(idx + s), __ldg(idx + s + 1), lim, a, b);
 }
 
 // ------------------------------------------------------------------ bounded waits

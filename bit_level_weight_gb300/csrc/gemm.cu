@@ -20,6 +20,7 @@
 #include "mma.cuh"
 #include "sbdecode.cuh"
 #include "wordlane.cuh"
+#include "blockwalk.cuh"
 
 namespace cas {
 namespace {
@@ -207,6 +208,307 @@ int launch(const GemmArgs& a, cudaStream_t st) {
   return launch_status();
 }
 
+
+// ------------------------------------------------------------------ block path
+// Cassandra-1, k = 64, m = 3, rows of whole superblocks. A CTA of 8 warps
+// takes 16 rows by one superblock column; warp w rebuilds rows 2w and 2w + 1.
+// Each block is walked by two lanes (blockwalk.cuh): lane 8t + j takes block j
+// of row 2w + (t >> 1), its 64 kept values for even t and its 64 pruned
+// values for odd t, so the warp's four staged code streams are row 0 kept, row
+// 0 pruned, row 1 kept, row 1 pruned and every lane walks 64 values:
+// positions from a window over the bit-reversed mask (or its complement),
+// exponents from a window over its stream. A kept value joins its sign and 3
+// high mantissa bits with the 4 cut bits of the verification record, a pruned
+// value is its byte of the pruned record; both are laid out as even and odd
+// bytes per group of 8, so the per-value code is the same for both kinds. Each
+// bf16 goes to its position in the tile. When a lane meets a step of 32 or more
+// (a long gap or code), the stores of its failed walk may land up to 782
+// bytes past its block's start - in the warp's own rows, the next warp's first
+// row, or the slack after the tile - so that warp and the next one rebuild
+// their rows by scanning the staged words instead; streams longer than the
+// stage go to the generic decoder. Then the product runs as in
+// verify_gemm_kernel.
+constexpr int kVThreads = 256;
+constexpr int kVWarps = kVThreads / 32;
+constexpr int kVRows = 2 * kVWarps;
+constexpr int kVPad = 512;                                  // bytes of slack after the tile
+constexpr int kVTile = kVRows * kTileStride + kVPad / 2;     // elements
+__device__ __forceinline__ int vrow(int r) { return r * kTileStride; }
+
+using VerifyStreams = BlockStreams<3, 80>;
+struct VerifyStage {
+  VerifyStreams st;    // codes: row 0 kept, row 0 pruned, row 1 kept, row 1 pruned (up to 80 words each)
+  uint32_t ms[7][32];  // row i, column l: bit-reversed word i of lane l's positions; rows 4-6 zero
+};
+static_assert(sizeof(VerifyStage) % 16 == 0, "stage alignment");
+static_assert(sizeof(VerifyStage) >= 2048, "the generic decoder's codes fit in the stage");
+static_assert(kVWarps * sizeof(VerifyStage) >= kVWarps * 256 * 4, "warp partials fit over the stages");
+
+// Zero rows and words of a warp's stage.
+__device__ __forceinline__ void verify_stage_init(VerifyStage& vs, int lane) {
+  block_streams_init(vs.st, lane);
+#pragma unroll
+  for (int r = 4; r < 7; ++r) vs.ms[r][lane] = 0u;
+}
+
+// The walk of one lane's 64 values without windows: every position and code
+// found by a scan of the staged words (any gap, any code length), the record
+// read again through the cache. For a warp whose windowed walk stepped 32 or
+// more; false when the staged data runs out (the encoding is inconsistent).
+__device__ __noinline__ bool verify_lane_scan(uint32_t ms_a, uint32_t st_a, int q0, uint32_t lut_a, bool pruned,
+                                              const uint32_t* __restrict__ ra, const uint32_t* __restrict__ rb,
+                                              uint32_t tb) {
+  int cur = -1, q = q0;
+  for (int i = 0; i < 64; ++i) {
+    const int p = bnext_one(ms_a, 128u, cur + 1, 6);
+    const int e = bnext_one(st_a, 4u, q + 1, VerifyStreams::kRow - 1);
+    if (p < 0 || p >= CAS_BLK || e < 0) return false;
+    cur = p;
+    const uint32_t E = lds_u32(lut_a + 4u * (uint32_t)min(e - q, 256));  // rank e - q - 1
+    q = e;
+    uint32_t b;
+    if (pruned) {
+      b = (__ldg(ra + (i >> 2)) >> (8 * (i & 3))) & 255u;
+    } else {
+      const int sh = 4 * (i & 7);
+      b = (((__ldg(ra + (i >> 3)) >> sh) & 15u) << 4) | ((__ldg(rb + (i >> 3)) >> sh) & 15u);
+    }
+    sts_u16(tb + 2u * (uint32_t)cur, ((b & 0x80u) << 8) | E | (b & 0x7Fu));
+  }
+  return true;
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kVThreads, 4) verify_gemm_block_kernel(GemmArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint32_t lut7[256];  // exponent << 7 by rank
+  __shared__ uint8_t lut8[256];   // exponent by rank (generic decoder)
+  __shared__ uint32_t s_bad;      // bit w: warp w's walk stepped 32 or more in this task
+  const WView& w = a.w;
+  uint16_t* tile = reinterpret_cast<uint16_t*>(smem);
+  VerifyStage& vs = reinterpret_cast<VerifyStage*>(smem + kVTile * 2)[threadIdx.x >> 5];
+  float* red = reinterpret_cast<float*>(smem + kVTile * 2);  // [warps][16][16], over the stages after the decode
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < 256; i += kVThreads) {
+    lut7[i] = (uint32_t)a.lut.v[i] << 7;
+    lut8[i] = a.lut.v[i];
+  }
+  if (threadIdx.x == 0) s_bad = 0u;
+  __syncthreads();
+
+  const int64_t ntile = (w.N + kVRows - 1) / kVRows;
+  const int64_t ntasks = ntile * w.nsr;
+  const int K = (int)w.K, T = a.T;
+  const uint32_t* X32 = reinterpret_cast<const uint32_t*>(a.X);
+  const int t = lane >> 3, j = lane & 7;
+  const bool pruned = t & 1;
+  const uint32_t ms_a0 = smem_addr(&vs.ms[0][lane]), st_a0 = smem_addr(&vs.st.w[t][0]);
+  const uint32_t lut_a = smem_addr(lut7) - 4u;  // rank c - 1 at lut_a + 4c
+  const uint32_t tile_a = smem_addr(tile);
+  for (int64_t task = blockIdx.x; task < ntasks; task += gridDim.x) {
+    const int64_t rt = task / w.nsr;
+    const int col = (int)(task % w.nsr);
+    const int64_t r0 = rt * kVRows + 2 * warp;  // the warp's first row
+    const int64_t n = r0 + (t >> 1);            // this lane's row
+    const bool valid = n < w.N;
+    // the next task's index words, mask and records, into L1 while this one
+    // decodes (its stream words follow halfway through the walk)
+    const int64_t nxt = task + gridDim.x;
+    const int64_t nn = (nxt / w.nsr) * kVRows + 2 * warp + (t >> 1);
+    const int ncol = (int)(nxt % w.nsr);
+    const bool pf = nxt < ntasks && nn < w.N;
+    if (pf) {
+      const int64_t ngb = nn * w.nbr + CAS_SB * ncol + j;
+      prefetch_l1(w.mask + ngb * 4);
+      prefetch_l1(pruned ? w.vpr + ngb * 16 : w.ssm + ngb * 8);
+      prefetch_l1(pruned ? w.vpr + ngb * 16 + 8 : w.vlo + ngb * 8);
+      if (j == 0) prefetch_l1((pruned ? w.vidx : w.sidx) + nn * w.nsr + ncol);
+    }
+    // 1) rebuild rows r0, r0 + 1 of the tile (the stage's zero words first: the
+    // previous task's partials and the generic decoder write over them)
+    verify_stage_init(vs, lane);
+    const uint32_t* gs[4];
+    int nw[4];
+    int present = 0;
+    bool fast = true;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      uint32_t a0 = 0u, b0 = 0u;
+      const int64_t ru = r0 + (u >> 1);
+      if (ru < w.N) {
+        const int64_t s = ru * w.nsr + col;
+        if (u & 1)
+          stream_range(w.vidx, s, w.lim_vexp, a0, b0);
+        else
+          stream_range(w.sidx, s, w.lim_sexp, a0, b0);
+        present = u + 1;
+      }
+      gs[u] = ((u & 1) ? w.vexp : w.sexp) + a0;
+      nw[u] = (int)(b0 - a0);
+      fast = fast && nw[u] <= VerifyStreams::kWords;
+    }
+    const int64_t gb = (valid ? n : r0) * w.nbr + CAS_SB * col + j;  // this lane's block
+    const uint32_t tb = tile_a + 2u * (uint32_t)(vrow(2 * warp + (t >> 1)) + kBlkStride * j);
+    int q0s = 0;
+    if (fast) {
+      const uint4 mk = __ldg(reinterpret_cast<const uint4*>(w.mask) + gb);
+      // the lane's records: kept, spec_sm and ver_lo words (one each per group
+      // of 8); pruned, ver_pr words (two per group)
+      const uint32_t* ra = pruned ? w.vpr + gb * 16 : w.ssm + gb * 8;
+      const uint32_t* rb = pruned ? w.vpr + gb * 16 + 1 : w.vlo + gb * 8;
+      const int rs = pruned ? 2 : 1;
+      const uint32_t inv = pruned ? 0xFFFFFFFFu : 0u;
+      vs.ms[0][lane] = valid ? __brev(mk.x ^ inv) : 0u;
+      vs.ms[1][lane] = valid ? __brev(mk.y ^ inv) : 0u;
+      vs.ms[2][lane] = valid ? __brev(mk.z ^ inv) : 0u;
+      vs.ms[3][lane] = valid ? __brev(mk.w ^ inv) : 0u;
+      const int q0 = block_code_term<3, 64>(gs, nw, present, vs.st, lane, fast);
+      const uint32_t ms_a = fenced(ms_a0), st_a = fenced(st_a0);
+      uint32_t ta = tb - 2u;  // tile address of the last found position (-1 at first)
+      uint32_t Hp, Lp, Hc, Lc;
+      bwindow(ms_a, 128u, 0, 4, Hp, Lp);
+      bwindow(st_a, 4u, q0 + 1, VerifyStreams::kRow - 3, Hc, Lc);
+      uint32_t used = 0u, cor = 0u;
+      uint32_t an = __ldg(ra), bn = __ldg(rb);  // the next group's record words
+#pragma unroll 1
+      for (int gi = 0; gi < 8; ++gi) {
+        const uint32_t aw = an, bw = bn;
+        if (gi < 7) {
+          an = __ldg(ra + rs * (gi + 1));
+          bn = __ldg(rb + rs * (gi + 1));
+        }
+        if (gi == 4 && pf && j == 0) {  // the next task's stream words (lanes 0, 8, 16, 24)
+          uint32_t a0, b0;
+          if (pruned)
+            stream_range(w.vidx, nn * w.nsr + ncol, w.lim_vexp, a0, b0);
+          else
+            stream_range(w.sidx, nn * w.nsr + ncol, w.lim_sexp, a0, b0);
+          const uint32_t* s0 = (pruned ? w.vexp : w.sexp) + a0;
+          for (uint32_t q = 0; q < b0 - a0 && q < 96u; q += 32u) prefetch_l1(s0 + q);
+        }
+        if (gi > 0) {
+          const int cur = min((int)(ta - tb) >> 1, CAS_BLK - 1);
+          ta = tb + 2u * (uint32_t)cur;
+          bwindow(ms_a, 128u, cur + 1, 4, Hp, Lp);  // rows <= 6 since cur <= 127
+          bwindow(st_a, 4u, q0 + 1 + (int)used, VerifyStreams::kRow - 3, Hc, Lc);
+        }
+        // bytes [s f6 .. f0] of the group's values 0, 2, 4, 6 (ev) and 1, 3, 5, 7 (od)
+        const uint32_t ev = pruned ? __byte_perm(aw, bw, 0x6420)
+                                   : ((aw << 4) & 0xF0F0F0F0u) | (bw & 0x0F0F0F0Fu);
+        const uint32_t od = pruned ? __byte_perm(aw, bw, 0x7531)
+                                   : (aw & 0xF0F0F0F0u) | ((bw >> 4) & 0x0F0F0F0Fu);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t np = __clz(Hp) + 1u;  // distance to the next position
+          ta = mad32(np, 2u, ta);
+          Hp = shfl_wrap(Lp, Hp, np);
+          Lp = shfl_wrap(0u, Lp, np);
+          const uint32_t nc = __clz(Hc) + 1u;  // rank + 1
+          const uint32_t E = lds_u32(lut_a + 4u * nc);
+          Hc = shfl_wrap(Lc, Hc, nc);
+          Lc = shfl_wrap(0u, Lc, nc);
+          used += nc;
+          cor |= np | nc;
+          const uint32_t A = __byte_perm((i & 1) ? od : ev, 0u, (uint32_t)(i >> 1) * 0x11u | 0x4400u);
+          sts_u16(ta, (A & 0x807Fu) | E);
+        }
+      }
+      if (__any_sync(CAS_FULL, valid && (cor & 32u)) && lane == 0) atomicOr(&s_bad, 1u << warp);
+      q0s = q0;
+    }
+    // a step of 32 or more in this warp or the one before: rebuild by the scan
+    // walk (a failed walk may have stored into the blocks after it)
+    __syncthreads();
+    const uint32_t bad = s_bad;
+    if (((bad >> warp) & 1u || (warp > 0 && ((bad >> (warp - 1)) & 1u))) && fast) {
+      const uint32_t* ra = pruned ? w.vpr + gb * 16 : w.ssm + gb * 8;
+      const uint32_t* rb = pruned ? w.vpr + gb * 16 + 1 : w.vlo + gb * 8;
+      const bool ok = !valid || verify_lane_scan(fenced(ms_a0), fenced(st_a0), q0s, lut_a, pruned, ra, rb, tb);
+      fast = __all_sync(CAS_FULL, ok);
+    }
+    __syncwarp();
+    if (!fast) {  // the generic decoder, one row-superblock at a time
+      SbScratch sc{reinterpret_cast<uint8_t*>(&vs), reinterpret_cast<uint8_t*>(&vs) + 1024, nullptr};
+      for (int u = 0; u < 2; ++u) {
+        if (r0 + u >= w.N) break;
+        const SbInfo in = sb_prepare<1, true>(w, (r0 + u) * w.nsr + col, lut8, sc, lane);
+        uint32_t v[16];
+        sb_rebuild_word<1, true>(w, in, sc, lane, v);
+        uint4* dst = reinterpret_cast<uint4*>(tile + vrow(2 * warp + u) + kBlkStride * (lane >> 2) + 32 * (lane & 3));
+        dst[0] = make_uint4(v[0], v[1], v[2], v[3]);
+        dst[1] = make_uint4(v[4], v[5], v[6], v[7]);
+        dst[2] = make_uint4(v[8], v[9], v[10], v[11]);
+        dst[3] = make_uint4(v[12], v[13], v[14], v[15]);
+        __syncwarp();
+      }
+    }
+    // 2) tensor-core product of the tile with X[:, tile columns]
+    const int gq = lane >> 2, tq = lane & 3;
+    constexpr int kKs = CAS_BLK * CAS_SB / 16 / kVWarps;
+    uint32_t xb[kKs][NT][2];
+#pragma unroll
+    for (int i = 0; i < kKs; ++i) {
+      const int ks = warp + kVWarps * i;
+      const int c = CAS_BLK * CAS_SB * col + ks * 16 + 2 * tq;
+#pragma unroll
+      for (int q = 0; q < NT; ++q) {
+        const int tok = q * 8 + gq;
+        xb[i][q][0] = xb[i][q][1] = 0u;
+        if (tok < T) {
+          xb[i][q][0] = __ldg(X32 + ((int64_t)tok * K + c) / 2);
+          xb[i][q][1] = __ldg(X32 + ((int64_t)tok * K + c + 8) / 2);
+        }
+      }
+    }
+    __syncthreads();
+    float acc[NT][4];
+#pragma unroll
+    for (int q = 0; q < NT; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
+#pragma unroll
+    for (int i = 0; i < kKs; ++i) {
+      const int ks = warp + kVWarps * i;
+      uint32_t af[4];
+      ldmatrix_x4(af, tile + vrow(lane & 15) + tile_col(ks) + (lane >> 4) * 8);
+#pragma unroll
+      for (int q = 0; q < NT; ++q) mma_bf16(acc[q], af, xb[i][q][0], xb[i][q][1]);
+    }
+    // 3) reduce warp partials: red[warp][row][token]
+    float* rw = red + warp * 256;
+#pragma unroll
+    for (int q = 0; q < NT; ++q) {
+      rw[gq * 16 + q * 8 + 2 * tq] = acc[q][0];
+      rw[gq * 16 + q * 8 + 2 * tq + 1] = acc[q][1];
+      rw[(gq + 8) * 16 + q * 8 + 2 * tq] = acc[q][2];
+      rw[(gq + 8) * 16 + q * 8 + 2 * tq + 1] = acc[q][3];
+    }
+    __syncthreads();
+    {
+      const int r = threadIdx.x >> 4, tt = threadIdx.x & 15;
+      const int64_t nn2 = rt * kVRows + r;
+      if (tt < T && tt < NT * 8 && nn2 < w.N) {
+        float sum = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < kVWarps; ++ww) sum += red[ww * 256 + r * 16 + tt];
+        atomicAdd(a.Y + (int64_t)tt * w.N + nn2, sum);
+      }
+      if (threadIdx.x == 0) s_bad = 0u;
+    }
+    __syncthreads();
+  }
+}
+
+template <int NT>
+int launch_block(const GemmArgs& a, cudaStream_t st) {
+  const size_t smem = (size_t)kVTile * 2 + kVWarps * sizeof(VerifyStage);
+  auto kern = verify_gemm_block_kernel<NT>;
+  const int per_sm = occupancy((const void*)kern, kVThreads, smem);
+  if (per_sm < 1) return CAS_ERR_CUDA;
+  const int64_t ntasks = (a.w.N + kVRows - 1) / kVRows * a.w.nsr;
+  const int g = (int)std::max<int64_t>(1, std::min<int64_t>(ntasks, (int64_t)sm_count() * per_sm));
+  kern<<<g, kVThreads, smem, st>>>(a);
+  return launch_status();
+}
+
 }  // namespace
 
 int corrupt_status_gemm(bool clear) {
@@ -246,11 +548,11 @@ extern "C" int cas_verify_gemm(const cas_weights* W, const uint16_t* X, int T, f
   const bool whole = a.w.nbr % CAS_SB == 0;
   const bool fast = v1 && a.w.k == 64 && a.w.m == 3 && whole;
   if (T <= 8) {
-    if (fast) return launch<1, 1, 1>(a, st);
+    if (fast) return launch_block<1>(a, st);
     if (whole) return v1 ? launch<1, 1, 2>(a, st) : launch<2, 1, 2>(a, st);
     return v1 ? launch<1, 1, 0>(a, st) : launch<2, 1, 0>(a, st);
   }
-  if (fast) return launch<1, 2, 1>(a, st);
+  if (fast) return launch_block<2>(a, st);
   if (whole) return v1 ? launch<1, 2, 2>(a, st) : launch<2, 2, 2>(a, st);
   return v1 ? launch<1, 2, 0>(a, st) : launch<2, 2, 0>(a, st);
 }

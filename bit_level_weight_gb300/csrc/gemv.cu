@@ -34,6 +34,7 @@
 #include "lanedec.cuh"
 #include "sbdecode.cuh"
 #include "wordlane.cuh"
+#include "blockwalk.cuh"
 
 namespace cas {
 namespace {
@@ -709,12 +710,6 @@ union WordScratch {
 
 __host__ __device__ constexpr int word_x_floats(int K) { return ((K / 32) * kXGroup + 3) & ~3; }
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ float lds_f32(uint32_t a) {
-  float v;
-  asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
-  return v;
-}
 
 // The generic superblock decoder for what the word walk cannot take. Kept out
 // of line so that its registers do not count against the fast path.
@@ -956,27 +951,30 @@ inline int word_per(int64_t nsb, int g) { return (int)((nsb + (int64_t)g * kWarp
 // codes start (the bit after the (64 j)-th '1' of its superblock's stream, j
 // the block's place in it) by a warp popcount scan and a shuffle search, and
 // then walks two cursors of its own, re-aligned every 8 values:
-//   position: a 64-bit window of the mask at the last found position, whose
-//             bit (the top bit) is cleared; the count of leading zeros is the
-//             distance to the next kept position, the window shifts by it;
-//   exponent: the same over the code stream at the last code's terminating
-//             '1': the count of leading zeros is rank + 1.
-// A window that runs dry (the next '1' outside it, a gap of 32 or more
-// positions, a code of rank 31 or more) yields a count of 32 - the only
-// count with bit 5 set - so OR-ing every count finds all of them at once; the
-// chunk's sums are then dropped and its superblocks go to the generic decoder
-// after the warp's run. x is staged per CTA as fp32 with 129 floats per block,
-// so position p of block b sits on bank (b + p) % 32 and the 32 lanes, which
-// advance through their blocks at about the same pace, spread over the banks.
+//   position: a 64-bit window of the bit-reversed mask starting just after the
+//             last found position; one more than its count of leading zeros
+//             is the distance n to the next kept position, and the window
+//             shifts by n (a funnel shift of the two words);
+//   exponent: the same over the code stream starting at the next code: the
+//             count of leading zeros is the rank.
+// Every shift must be below 32. A larger one - a gap of 32 or more positions,
+// a code of rank 31 or more, a window that runs dry (count 32) - is the only
+// case with bit 5 set, so OR-ing every shift finds all of them at once; a
+// lane that met one walks its block again by scanning the staged words
+// (block_walk_scan), which takes any gap and any code. Chunks whose streams
+// do not fit the stage go to the generic decoder after the warp's run. x is
+// staged per CTA as fp32 with 129 floats per block, so position p of block b
+// sits on bank (b + p) % 32 and the 32 lanes, which advance through their
+// blocks at about the same pace, spread over the banks.
 constexpr int kBThreads = 512;
 constexpr int kBWarps = kBThreads / 32;
 constexpr int kBXRow = CAS_BLK + 1;   // staged floats per block
 constexpr int kBXPad = 2048;          // bytes after x: reads of a failed walk stay inside
-constexpr int kBStreamWords = 2 + 64 + 4;  // 2 zero words, up to 64 stream words, 4 zero words
-constexpr int kBMaskRows = 7;         // zero row, 4 mask words, 2 zero rows
+constexpr int kBMaskRows = 8;         // zero row, 4 mask words, 3 zero rows
 
+constexpr int kBStreamWords = BlockStreams<2>::kRow;
 struct BlockStage {
-  uint32_t st[4][kBStreamWords];  // the chunk's code streams
+  BlockStreams<2> st;             // the chunk's code streams
   uint32_t ms[kBMaskRows][32];    // row 1 + i, column l: bit-reversed mask word i of lane l's block
   uint32_t fs[8][32];             // row i, column l: word i of the sign/mantissa record of lane l's block
 };
@@ -984,38 +982,6 @@ static_assert(sizeof(BlockStage) >= CAS_SB * CAS_BLK, "the generic decoder's scr
 static_assert(sizeof(BlockStage) % 16 == 0, "stage alignment");
 
 __host__ __device__ constexpr int block_x_floats(int nbr) { return (nbr * kBXRow + 3) & ~3; }
-
-__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
-  uint32_t v;
-  asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
-  return v;
-}
-
-// 64-bit window (H, L) of a staged MSB-first bitstream at bit q: the word
-// rows are `stride` bytes apart starting at address `base`; H's top bit (the
-// last consumed '1') is cleared.
-__device__ __forceinline__ void bwindow(uint32_t base, uint32_t stride, int q, int maxw, uint32_t& H, uint32_t& L) {
-  const int hw = min(q >> 5, maxw), sh = q & 31;
-  const uint32_t a = base + stride * (uint32_t)hw;
-  const uint32_t w0 = lds_u32(a), w1 = lds_u32(a + stride), w2 = lds_u32(a + 2u * stride);
-  H = __funnelshift_l(w1, w0, sh) & 0x7FFFFFFFu;
-  L = __funnelshift_l(w2, w1, sh);
-}
-
-// Index of the first '1' at or after bit b of a staged MSB-first bitstream
-// (word rows `stride` bytes apart, rows 0..maxw), or -1.
-__device__ __forceinline__ int bnext_one(uint32_t base, uint32_t stride, int b, int maxw) {
-  int wi = b >> 5;
-  if (wi > maxw) return -1;
-  uint32_t h = lds_u32(base + stride * (uint32_t)wi) << (b & 31);
-  int pos = b;
-  while (h == 0u) {
-    if (++wi > maxw) return -1;
-    h = lds_u32(base + stride * (uint32_t)wi);
-    pos = 32 * wi;
-  }
-  return pos + (int)__clz(h);
-}
 
 // The block walk without windows: every position and code found by a scan
 // of the staged words, so gaps and codes of any length are taken. For a lane
@@ -1039,7 +1005,7 @@ __device__ __noinline__ ScanSum<NV> block_walk_scan(uint32_t ms_a, uint32_t st_a
     const int tb = bnext_one(st_a, 4u, qc + 1, kBStreamWords - 1);
     if (pb < 0 || pb >= 32 + CAS_BLK || tb < 0) return r;
     cur = pb - 32;
-    const uint32_t E = lds_u32(lut_a + 4u * (uint32_t)min(tb - qc, 256));  // rank tb - qc - 1
+    const uint32_t E = lds_u32(lut_a + 4u * (uint32_t)min(tb - qc - 1, 255));  // rank tb - qc - 1
     qc = tb;
     const uint32_t f = (lds_u32(fs_a + 128u * (uint32_t)(i >> 3)) >> (4 * (i & 7))) & 15u;
     const float val = __uint_as_float(((f & 8u) << 28) | E | ((f & 7u) << 20));
@@ -1095,35 +1061,36 @@ __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs
   const int c0 = min(gw * per, nch), c1 = min(c0 + per, nch);
   const uint32_t lim = (uint32_t)a.sexp_words;
   const int t = lane >> 3, j = lane & 7;
-  const uint32_t ms_a = smem_addr(&bs.ms[0][lane]);
-  const uint32_t fs_a = smem_addr(&bs.fs[0][lane]);
-  const uint32_t st_a = smem_addr(&bs.st[t][0]);
-  const uint32_t lut_a = smem_addr(lut32) - 4u;  // rank c - 1 at lut_a + 4c
+  const uint32_t ms_a0 = smem_addr(&bs.ms[0][lane]);
+  const uint32_t fs_a0 = smem_addr(&bs.fs[0][lane]);
+  const uint32_t st_a0 = smem_addr(&bs.st.w[t][0]);
+  const uint32_t lut_a = smem_addr(lut32);  // rank r at lut_a + 4r
   const uint32_t xs_a = smem_addr(xs);
   int* fb = reinterpret_cast<int*>(smem + (size_t)NV * xfl * 4 + kBXPad + kBWarps * sizeof(BlockStage)) + warp * per;
   int nfb = 0;
   // zero rows and words of the stage, written once
-  if (lane < 4) {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) bs.st[lane][i] = 0u;
-#pragma unroll
-    for (int i = 66; i < kBStreamWords; ++i) bs.st[lane][i] = 0u;
-  }
+  block_streams_init(bs.st, lane);
   bs.ms[0][lane] = 0u;
   bs.ms[5][lane] = 0u;
   bs.ms[6][lane] = 0u;
+  bs.ms[7][lane] = 0u;
 
+  // row and block in the row of the chunk's first block
+  uint32_t row0 = (uint32_t)(((int64_t)c0 * 32) / nbr);
+  uint32_t jb0 = (uint32_t)((int64_t)c0 * 32 - (int64_t)row0 * nbr);
   for (int c = c0; c < c1; ++c) {
     // the chunk's streams; a stream longer than the stage sends the chunk to
     // the generic decoder
     uint32_t sa[4];
     int nw[4];
     bool fast = true;
+    const int64_t s0 = (int64_t)c * 4;
+    const uint32_t ix = lane <= 4 && s0 + lane <= nsb ? __ldg(w.sidx + s0 + lane) : 0u;  // index words s0 .. s0+4
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int64_t su = (int64_t)c * 4 + u;
+      const uint32_t i0 = __shfl_sync(CAS_FULL, ix, u), i1 = __shfl_sync(CAS_FULL, ix, u + 1);
       uint32_t a0 = 0u, b0 = 0u;
-      if (su < nsb) stream_range(w.sidx, su, lim, a0, b0);
+      if (s0 + u < nsb) stream_clamp(i0, i1, lim, a0, b0);
       sa[u] = a0;
       nw[u] = (int)(b0 - a0);
       fast = fast && nw[u] <= 64;
@@ -1135,15 +1102,6 @@ __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs
       const uint4 mk = __ldg(reinterpret_cast<const uint4*>(w.mask) + gl);
       const uint4 fA = __ldg(reinterpret_cast<const uint4*>(w.ssm + gl * 8));
       const uint4 fB = __ldg(reinterpret_cast<const uint4*>(w.ssm + gl * 8) + 1);
-      int pc[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const uint32_t* gs = w.sexp + sa[u];
-        const uint32_t s0 = 2 * lane < nw[u] ? __ldg(gs + 2 * lane) : 0u;
-        const uint32_t s1 = 2 * lane + 1 < nw[u] ? __ldg(gs + 2 * lane + 1) : 0u;
-        *reinterpret_cast<uint2*>(&bs.st[u][2 + 2 * lane]) = make_uint2(s0, s1);
-        pc[u] = __popc(s0) + __popc(s1);
-      }
       bs.ms[1][lane] = valid ? __brev(mk.x) : 0u;
       bs.ms[2][lane] = valid ? __brev(mk.y) : 0u;
       bs.ms[3][lane] = valid ? __brev(mk.z) : 0u;
@@ -1156,43 +1114,21 @@ __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs
       bs.fs[5][lane] = fB.y;
       bs.fs[6][lane] = fB.z;
       bs.fs[7][lane] = fB.w;
-      // popcount prefixes of the 4 streams over word pairs, 16 bits each
-      const int S01 = warp_incl_add(pc[0] | (pc[1] << 16), lane);
-      const int S23 = warp_incl_add(pc[2] | (pc[3] << 16), lane);
-      const int T01 = __shfl_sync(CAS_FULL, S01, 31), T23 = __shfl_sync(CAS_FULL, S23, 31);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int ones = ((u < 2 ? T01 : T23) >> (16 * (u & 1))) & 0xFFFF;
-        if ((int64_t)c * 4 + u < nsb && ones < CAS_SB * 64) fast = false;
-      }
-      // pair holding the (64 j)-th '1' of stream t: pairs whose prefix, in
-      // units of 64, is below j
-      const int B01 = min((S01 & 0xFFFF) >> 6, 15) | (min((S01 >> 16) >> 6, 15) << 4);
-      const int B23 = min((S23 & 0xFFFF) >> 6, 15) | (min((S23 >> 16) >> 6, 15) << 4);
-      const int KB = B01 | (B23 << 8);
-      int lo = 0;
-#pragma unroll
-      for (int step = 16; step >= 1; step >>= 1) {
-        const int kb = __shfl_sync(CAS_FULL, KB, lo + step - 1);
-        if (((kb >> (4 * t)) & 15) < j) lo += step;
-      }
-      const int lp = min(lo, 31);
-      const int Sa = __shfl_sync(CAS_FULL, S01, lp), Sb = __shfl_sync(CAS_FULL, S23, lp);
-      const int Sp = ((t < 2 ? Sa : Sb) >> (16 * (t & 1))) & 0xFFFF;  // ones through pair lp
-      __syncwarp();
-      const uint32_t w0 = lds_u32(st_a + 4u * (uint32_t)(2 + 2 * lp)), w1 = lds_u32(st_a + 4u * (uint32_t)(3 + 2 * lp));
-      const int n0 = __popc(w0);
-      const int r = 64 * j - (Sp - n0 - __popc(w1));  // the one's rank inside the pair (1-based)
-      const bool in0 = r <= n0;
-      const int term = j == 0 ? -1 : 32 * (2 * lp + (in0 ? 0 : 1)) + select_msb(in0 ? w0 : w1, max(in0 ? r : r - n0, 1));
+      const uint32_t* gsx[4] = {w.sexp + sa[0], w.sexp + sa[1], w.sexp + sa[2], w.sexp + sa[3]};
+      const int present = nsb - (int64_t)c * 4 < 4 ? (int)(nsb - (int64_t)c * 4) : 4;
+      // staged bit of the '1' before the block's first code
+      const int cq0 = block_code_term<2, 64>(gsx, nw, present, bs.st, lane, fast);
+      const uint32_t ms_a = fenced(ms_a0), fs_a = fenced(fs_a0), st_a = fenced(st_a0);
       // cursors
-      const uint32_t gl32 = (uint32_t)gl, nr = gl32 / (uint32_t)nbr;  // row, and block gl32 - nr * nbr in it
-      const uint32_t xbase = xs_a + 4u * (gl32 - nr * (uint32_t)nbr) * kBXRow;
-      uint32_t xa = xbase - 4u;  // position -1
+      // row and block in the row (nbr >= 32: the chunk wraps at most once)
+      uint32_t jb = valid ? jb0 + (uint32_t)lane : jb0;
+      const uint32_t nr = row0 + (jb >= (uint32_t)nbr ? 1u : 0u);
+      jb = jb >= (uint32_t)nbr ? jb - (uint32_t)nbr : jb;
+      const uint32_t xbase = xs_a + 4u * jb * kBXRow;
+      uint32_t xa = xbase - 4u;  // x address of the last found position (-1 at first)
       uint32_t Hp, Lp, Hc, Lc;
-      bwindow(ms_a, 128u, 31, kBMaskRows - 3, Hp, Lp);
-      const int cq0 = 64 + term;
-      bwindow(st_a, 4u, cq0, kBStreamWords - 3, Hc, Lc);
+      bwindow(ms_a, 128u, 32, kBMaskRows - 3, Hp, Lp);
+      bwindow(st_a, 4u, cq0 + 1, kBStreamWords - 3, Hc, Lc);
       uint32_t used = 0u, cor = 0u;
       float part[NV];
 #pragma unroll
@@ -1202,22 +1138,22 @@ __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs
         if (gi > 0) {
           const int cur = min((int)(xa - xbase) >> 2, CAS_BLK - 1);
           xa = xbase + 4u * (uint32_t)cur;
-          bwindow(ms_a, 128u, 32 + cur, kBMaskRows - 3, Hp, Lp);
-          bwindow(st_a, 4u, cq0 + (int)used, kBStreamWords - 3, Hc, Lc);
+          bwindow(ms_a, 128u, 33 + cur, kBMaskRows - 3, Hp, Lp);  // rows <= 7 since cur <= 127
+          bwindow(st_a, 4u, cq0 + 1 + (int)used, kBStreamWords - 3, Hc, Lc);
         }
         const uint32_t fo = lds_u32(fs_a + 128u * gi), fe = fo << 4;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const uint32_t cp = __clz(Hp);  // distance to the next kept position
-          xa = mad32(cp, 4u, xa);
-          Hp = shfl_wrap(Lp, Hp, cp) & 0x7FFFFFFFu;
-          Lp = shfl_wrap(0u, Lp, cp);
-          const uint32_t cc = __clz(Hc);  // rank + 1
-          const uint32_t E = lds_u32(lut_a + 4u * cc);
-          Hc = shfl_wrap(Lc, Hc, cc) & 0x7FFFFFFFu;
-          Lc = shfl_wrap(0u, Lc, cc);
-          used += cc;
-          cor |= cp | cc;
+          const uint32_t np = __clz(Hp) + 1u;  // distance to the next kept position
+          xa = mad32(np, 4u, xa);
+          Hp = shfl_wrap(Lp, Hp, np);
+          Lp = shfl_wrap(0u, Lp, np);
+          const uint32_t nc = __clz(Hc) + 1u;  // rank + 1
+          const uint32_t E = lds_u32(lut_a - 4u + 4u * nc);
+          Hc = shfl_wrap(Lc, Hc, nc);
+          Lc = shfl_wrap(0u, Lc, nc);
+          used += nc;
+          cor |= np | nc;
           const int by = i >> 1;
           const uint32_t A = __byte_perm((i & 1) ? fo : fe, 0u, (by << 12) | (by << 8) | 0x44);
           const float val = __uint_as_float((A & 0x80700000u) | E);
@@ -1257,6 +1193,11 @@ __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs
     if (!fast) {  // decoded after the run; nothing of it was added
       if (lane == 0) fb[nfb] = c;
       ++nfb;
+    }
+    jb0 += 32u;
+    if (jb0 >= (uint32_t)nbr) {
+      jb0 -= (uint32_t)nbr;
+      ++row0;
     }
   }
   // chunks the block walk did not take: the generic decoder, one superblock

@@ -14,7 +14,7 @@ def args(variant=1, keep=64, mant=3):
 
 
 @pytest.mark.parametrize("a,nvec,name", [
-    (args(), 1, "draft_gemv_word_kernel<1>"), (args(), 2, "draft_gemv_word_kernel<2>"),
+    (args(), 1, "draft_gemv_block_kernel<1>"), (args(), 2, "draft_gemv_block_kernel<2>"),
     (args(), 3, "draft_gemv_fast_kernel<3>"),
     (args(2), 2, "draft_gemv_fast2_kernel<2>"), (args(2), 3, "draft_gemv_runs_kernel<2,3>"),
     (args(1, 38), 1, "draft_gemv_runs_kernel<1,1>"), (args(2, 64, 4), 1, "draft_gemv_runs_kernel<2,1>"),

@@ -345,3 +345,24 @@ def test_draft_gemv_block_chunks(cas, orc, N, K, kind, nvec):
     y = cas.draft_gemv(enc, x.cuda())
     ref, norm = orc.matvec(orc.draft_values(np16(W), 1, 64, 3), np16(x))
     check_close(y, ref, norm, "draft_gemv block chunks")
+
+
+@pytest.mark.parametrize("T", [1, 5, 13])
+@pytest.mark.parametrize("N,K,kind", [(3, 1024, "t4"), (21, 4096, "t4"), (35, 5120, "t4"), (18, 2048, "clustered"),
+                                       (40, 1024, "wide")])
+def test_verify_gemm_block_tiles(cas, orc, N, K, kind, T):
+    """The verify GEMM rebuilds 16-row tiles with one lane per block: row
+    counts that leave the last tile partly empty, clustered masks whose long
+    runs of kept or pruned positions and rows whose long codes send a warp's
+    row-superblocks to the generic decoder, against the exact product."""
+    if kind == "t4":
+        W = synthetic.t4_weight(N, K, seed=N + K + T)
+    elif kind == "clustered":
+        W = clustered_rows(N, K, seed=N + K)
+    else:
+        W = wide_exponent_rows(N, K, 6, seed=N + T)
+    X = synthetic.activations(T, K, seed=23 + T)
+    enc = cas.encode_weights(W.cuda(), 1, 64, 3)
+    Y = cas.verify_gemm(enc, X.cuda())
+    ref, norm = orc.matvec(np16(W), np16(X))
+    check_close(Y, ref, norm, "verify_gemm block tiles")
