@@ -27,6 +27,7 @@
 #include <cmath>
 
 #include "kvview.cuh"
+#include "blockwalk.cuh"
 #include "lanedec.cuh"
 #include "mma.cuh"
 #include "sbdecode.cuh"
@@ -800,6 +801,467 @@ int launch_fused(AttnArgs& a, int Hkv, cudaStream_t st) {
   return launch_status();
 }
 
+
+// ---------------------------------------------------------------- block draft
+// Draft attention for Cassandra-1 caches with k = 64, m = 3 and at most 4
+// query vectors per kv head (blockwalk.cuh). A warp takes 32 tokens at a time
+// (4 superblocks of a stream) with lane = token: it walks the token's 64 kept
+// K values and multiplies each with the 4 query vectors at its position (one
+// 16-byte load of a dims x 4 query table), runs the online softmax per query
+// vector over its 32 scores, walks the 64 kept V values of the same tokens
+// into a zero-filled bf16 tile, and adds P V on tensor cores as O^T += V^T P^T
+// (mma m16n8k16: A = the tile, transposed by ldmatrix; B = P in bf16 as hi +
+// lo, |p - hi - lo| <= 2^-17 p; C = 128 dims x 8 query columns, 4 used). Each
+// warp keeps its own softmax state over every 4th step of the CTA's chunk;
+// the 4 warps merge at the end. A lane whose windows ran dry rescans its
+// token (K) or makes the whole warp rebuild its V rows by scanning (its
+// stores may have run into the next rows); superblocks whose streams do not
+// fit the stage are decoded by decode_sb_tile and scored from the tile.
+constexpr int kDRow = CAS_BLK + 8;     // V tile row (272 B)
+constexpr int kDPRow = 40;             // P^T stage row: 32 tokens + pad (conflict-free ldmatrix)
+constexpr int kDWarpPad = 512;         // bytes after a warp's V tile: stores of a failed walk stay inside
+struct DraftStage {
+  union {
+    struct {
+      BlockStreams<2> st;  // codes of the step's 4 superblocks (K, then V)
+      uint32_t ms[7][32];  // row i, column l: bit-reversed mask word i of token l; rows 4-6 zero
+    } w;
+    uint8_t tile_scratch[kScratchDraftC1];  // decode_sb_tile's stage
+  } u;
+  uint16_t ph[8][kDPRow], pl[8][kDPRow];  // P^T hi / lo: query vector x token (rows 4-7 zero)
+  uint16_t vt[kStepTok * kDRow + kDWarpPad / 2];  // V tile: token x dim (+ slack)
+};
+static_assert(sizeof(DraftStage) % 16 == 0, "draft stage alignment");
+
+// The K walk of one token without windows (any gap, any code length): the
+// scores against the 4 query vectors, or ok = false when the staged data runs
+// out (the encoding is inconsistent).
+__device__ __noinline__ float4 draft_k_scan(uint32_t ms_a, uint32_t st_a, int q0, uint32_t lutk_a,
+                                            const uint32_t* __restrict__ rec, uint32_t q4_a, bool& ok) {
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  int cur = -1, q = q0;
+  ok = false;
+  for (int i = 0; i < 64; ++i) {
+    const int p = bnext_one(ms_a, 128u, cur + 1, 6);
+    const int e = bnext_one(st_a, 4u, q + 1, BlockStreams<2>::kRow - 1);
+    if (p < 0 || p >= CAS_BLK || e < 0) return acc;
+    cur = p;
+    const uint32_t E = lds_u32(lutk_a + 4u * (uint32_t)min(e - q - 1, 255));
+    q = e;
+    const uint32_t f = (__ldg(rec + (i >> 3)) >> (4 * (i & 7))) & 15u;
+    const float v = __uint_as_float(((f & 8u) << 28) | E | ((f & 7u) << 20));
+    const float4 qq = *reinterpret_cast<const float4*>(__cvta_shared_to_generic(q4_a + 16u * (uint32_t)p));
+    acc.x = fmaf(v, qq.x, acc.x);
+    acc.y = fmaf(v, qq.y, acc.y);
+    acc.z = fmaf(v, qq.z, acc.z);
+    acc.w = fmaf(v, qq.w, acc.w);
+  }
+  ok = true;
+  return acc;
+}
+
+// The V walk of one token without windows into its tile row; false when the
+// staged data runs out.
+__device__ __noinline__ bool draft_v_scan(uint32_t ms_a, uint32_t st_a, int q0, uint32_t lutv_a,
+                                          const uint32_t* __restrict__ rec, uint32_t row_a) {
+  int cur = -1, q = q0;
+  for (int i = 0; i < 64; ++i) {
+    const int p = bnext_one(ms_a, 128u, cur + 1, 6);
+    const int e = bnext_one(st_a, 4u, q + 1, BlockStreams<2>::kRow - 1);
+    if (p < 0 || p >= CAS_BLK || e < 0) return false;
+    cur = p;
+    const uint32_t E = lds_u32(lutv_a + 4u * (uint32_t)min(e - q - 1, 255));
+    q = e;
+    const uint32_t f = (__ldg(rec + (i >> 3)) >> (4 * (i & 7))) & 15u;
+    sts_u16(row_a + 2u * (uint32_t)p, ((f & 8u) << 12) | E | ((f & 7u) << 4));
+  }
+  return true;
+}
+
+__global__ void __launch_bounds__(kThreads, 4) attn_draft_block_kernel(AttnArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  float4* q4 = reinterpret_cast<float4*>(smem);  // [128] dims x 4 query vectors, scaled
+  uint32_t* lutk = reinterpret_cast<uint32_t*>(q4 + CAS_BLK);  // exponent << 23 by rank (K)
+  uint32_t* lutv = lutk + 256;                                  // exponent << 7 by rank (V)
+  uint8_t* lut8k = reinterpret_cast<uint8_t*>(lutv + 256);      // exponent by rank (generic decoder)
+  uint8_t* lut8v = lut8k + 256;
+  DraftStage* stages = reinterpret_cast<DraftStage*>(lut8v + 256);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  DraftStage& ds = stages[warp];
+  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const KvDev& d = a.kv[b];
+  const int H = d.H, G = a.G, nq = min(a.T * G, 4);
+  const int64_t n = *(volatile const int64_t*)&kv_state(d)->n_tokens;
+  const int64_t nsb = (n + CAS_SB - 1) / CAS_SB;
+  const int64_t steps = (n + kStepTok - 1) / kStepTok;
+  const int64_t s_begin = steps * chunk / a.nchunk, s_end = steps * (chunk + 1) / a.nchunk;
+
+  for (int i = threadIdx.x; i < 4 * CAS_BLK; i += kThreads) {
+    const int r = i & 3, dd = i >> 2;
+    float v = 0.f;
+    if (r < nq) v = bf2f(a.q[((int64_t)b * a.Hq + h * G + r) * CAS_BLK + dd]) * a.scale;
+    reinterpret_cast<float*>(q4)[i] = v;
+  }
+  for (int i = threadIdx.x; i < 256; i += kThreads) {
+    const uint8_t ek = kv_exp_of_rank(d, h)[i], ev = kv_exp_of_rank(d, H + h)[i];
+    lutk[i] = (uint32_t)ek << 23;
+    lutv[i] = (uint32_t)ev << 7;
+    lut8k[i] = ek;
+    lut8v[i] = ev;
+  }
+  block_streams_init(ds.u.w.st, lane);
+#pragma unroll
+  for (int r = 4; r < 7; ++r) ds.u.w.ms[r][lane] = 0u;
+  for (int i = lane; i < 8 * kDPRow; i += 32) {
+    (&ds.ph[0][0])[i] = 0;
+    (&ds.pl[0][0])[i] = 0;
+  }
+  __syncthreads();
+
+  const uint32_t q4_a = smem_addr(q4), lutk_a = smem_addr(lutk), lutv_a = smem_addr(lutv);
+  const uint32_t ms_a0 = smem_addr(&ds.u.w.ms[0][lane]), st_a0 = smem_addr(&ds.u.w.st.w[lane >> 3][0]);
+  const uint32_t vt_a = smem_addr(ds.vt), row_a = vt_a + 2u * (uint32_t)(lane * kDRow);
+  const uint32_t* sidxK = (const uint32_t*)kv_sec(d, CAS_KV_SPEC_SBIDX, h);
+  const uint32_t* sidxV = (const uint32_t*)kv_sec(d, CAS_KV_SPEC_SBIDX, H + h);
+  const uint32_t lim = (uint32_t)d.cap_a;
+  const int gq = lane >> 2, tq = lane & 3;
+  float mst[4], lst[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    mst[q] = -INFINITY;
+    lst[q] = 0.f;
+  }
+  float c[8][4];
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) c[mt][0] = c[mt][1] = c[mt][2] = c[mt][3] = 0.f;
+
+  for (int64_t s = s_begin + warp; s < s_end; s += kWarps) {
+    const int64_t t0 = s * kStepTok, tok = t0 + lane, sb0 = t0 / CAS_SB;
+    const bool valid = tok < n;
+    const int64_t tk = valid ? tok : t0;
+    // superblocks of the step with all 8 tokens (their streams hold 512 codes)
+    int whole = 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) whole += CAS_SB * (sb0 + u + 1) <= n ? 1 : 0;
+    float sc[4];
+    // ---- K: scores of token tok against the query vectors
+    {
+      const uint32_t* g4[4];
+      int nw[4];
+      bool fast = true;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        uint32_t a0 = 0u, b0 = 0u;
+        if (sb0 + u < nsb) stream_range(sidxK, sb0 + u, lim, a0, b0);
+        g4[u] = (const uint32_t*)kv_sec(d, CAS_KV_SPEC_EXP, h) + a0;
+        nw[u] = (int)(b0 - a0);
+        fast = fast && nw[u] <= 64;
+      }
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (fast) {
+        const uint4 mk = __ldg(reinterpret_cast<const uint4*>(kv_sec(d, CAS_KV_MASK, h)) + tk);
+        const uint32_t* rec = (const uint32_t*)kv_sec(d, CAS_KV_SPEC_SM, h) + tk * 8;
+        ds.u.w.ms[0][lane] = valid ? __brev(mk.x) : 0u;
+        ds.u.w.ms[1][lane] = valid ? __brev(mk.y) : 0u;
+        ds.u.w.ms[2][lane] = valid ? __brev(mk.z) : 0u;
+        ds.u.w.ms[3][lane] = valid ? __brev(mk.w) : 0u;
+        uint32_t fn = __ldg(rec);  // the next group's record word
+        const int q0 = block_code_term<2, 64>(g4, nw, whole, ds.u.w.st, lane, fast);
+        const uint32_t ms_a = fenced(ms_a0), st_a = fenced(st_a0);
+        uint32_t xa = q4_a - 16u;  // query table address of the last found position (-1 at first)
+        uint32_t Hp, Lp, Hc, Lc;
+        bwindow(ms_a, 128u, 0, 4, Hp, Lp);
+        bwindow(st_a, 4u, q0 + 1, BlockStreams<2>::kRow - 3, Hc, Lc);
+        uint32_t used = 0u, cor = 0u;
+#pragma unroll 1
+        for (int gi = 0; gi < 8; ++gi) {
+          const uint32_t fo = fn, fe = fn << 4;
+          if (gi < 7) fn = __ldg(rec + gi + 1);
+          if (gi > 0) {
+            const int cur = min((int)(xa - q4_a) >> 4, CAS_BLK - 1);
+            xa = q4_a + 16u * (uint32_t)cur;
+            bwindow(ms_a, 128u, cur + 1, 4, Hp, Lp);
+            bwindow(st_a, 4u, q0 + 1 + (int)used, BlockStreams<2>::kRow - 3, Hc, Lc);
+          }
+          // a group whose 8 positions or codes do not all end in the windows
+          // (a code longer than the window: an exponent the tables rank far
+          // down) is taken by scanning; the walk goes on after it
+          if (__popc(Hp) + __popc(Lp) < 8 || __popc(Hc) + __popc(Lc) < 8) {
+            int cur = (int)(xa - q4_a) >> 4, qt = q0 + (int)used;
+            for (int i = 0; i < 8; ++i) {
+              const int pb = bnext_one(ms_a, 128u, cur + 1, 6);
+              const int eb = bnext_one(st_a, 4u, qt + 1, BlockStreams<2>::kRow - 1);
+              if (pb < 0 || pb >= CAS_BLK || eb < 0) {
+                cor |= 32u;
+                break;
+              }
+              const uint32_t E = lds_u32(lutk_a + 4u * (uint32_t)min(eb - qt - 1, 255));
+              used += (uint32_t)(eb - qt);
+              qt = eb;
+              cur = pb;
+              const uint32_t f = (fo >> (4 * i)) & 15u;
+              const float v = __uint_as_float(((f & 8u) << 28) | E | ((f & 7u) << 20));
+              float4 qq;
+              asm("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                  : "=f"(qq.x), "=f"(qq.y), "=f"(qq.z), "=f"(qq.w)
+                  : "r"(q4_a + 16u * (uint32_t)cur));
+              acc.x = fmaf(v, qq.x, acc.x);
+              acc.y = fmaf(v, qq.y, acc.y);
+              acc.z = fmaf(v, qq.z, acc.z);
+              acc.w = fmaf(v, qq.w, acc.w);
+            }
+            xa = q4_a + 16u * (uint32_t)max(cur, -1);
+            continue;
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t np = __clz(Hp) + 1u;
+            xa = mad32(np, 16u, xa);
+            Hp = shfl_wrap(Lp, Hp, np);
+            Lp = shfl_wrap(0u, Lp, np);
+            const uint32_t nc = __clz(Hc) + 1u;
+            const uint32_t E = lds_u32(lutk_a - 4u + 4u * nc);
+            Hc = shfl_wrap(Lc, Hc, nc);
+            Lc = shfl_wrap(0u, Lc, nc);
+            used += nc;
+            cor |= np | nc;
+            const int by = i >> 1;
+            const uint32_t A = __byte_perm((i & 1) ? fo : fe, 0u, (by << 12) | (by << 8) | 0x44);
+            const float v = __uint_as_float((A & 0x80700000u) | E);
+            float4 qq;
+            asm("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(qq.x), "=f"(qq.y), "=f"(qq.z), "=f"(qq.w) : "r"(xa));
+            acc.x = fmaf(v, qq.x, acc.x);
+            acc.y = fmaf(v, qq.y, acc.y);
+            acc.z = fmaf(v, qq.z, acc.z);
+            acc.w = fmaf(v, qq.w, acc.w);
+          }
+        }
+        if (valid && (cor & 32u)) {  // rescan this token (divergent, rare)
+          bool ok;
+          acc = draft_k_scan(ms_a, st_a, q0, lutk_a, rec, q4_a, ok);
+          if (!ok) acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        __syncwarp();
+      }
+      if (!fast) {  // a stream longer than the stage: K tile, then scores from it
+        for (int u = 0; u < 4; ++u)
+          decode_sb_tile<false>(d, h, n, sb0 + u, ds.vt, CAS_SB * u, lut8k, ds.u.tile_scratch, lane);
+        const uint32_t* kr = reinterpret_cast<const uint32_t*>(ds.vt + lane * kDRow);
+        for (int dd = 0; dd < CAS_BLK; dd += 2) {
+          const uint32_t k2 = kr[dd >> 1];
+          const float4 qa = q4[dd], qb = q4[dd + 1];
+          const float k0 = bf2f(k2 & 0xFFFFu), k1 = bf2f(k2 >> 16);
+          acc.x = fmaf(k0, qa.x, fmaf(k1, qb.x, acc.x));
+          acc.y = fmaf(k0, qa.y, fmaf(k1, qb.y, acc.y));
+          acc.z = fmaf(k0, qa.z, fmaf(k1, qb.z, acc.z));
+          acc.w = fmaf(k0, qa.w, fmaf(k1, qb.w, acc.w));
+        }
+        block_streams_init(ds.u.w.st, lane);
+#pragma unroll
+        for (int r = 4; r < 7; ++r) ds.u.w.ms[r][lane] = 0u;
+        __syncwarp();
+      }
+      sc[0] = valid ? acc.x : -INFINITY;
+      sc[1] = valid ? acc.y : -INFINITY;
+      sc[2] = valid ? acc.z : -INFINITY;
+      sc[3] = valid ? acc.w : -INFINITY;
+    }
+    // ---- online softmax per query vector; P^T (hi, lo) to the stage
+    float corr[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float mnew = fmaxf(mst[q], warp_maxf(sc[q]));
+      const float p = sc[q] == -INFINITY ? 0.f : __expf(sc[q] - mnew);
+      corr[q] = mst[q] == -INFINITY ? (mnew == -INFINITY ? 1.f : 0.f) : __expf(mst[q] - mnew);
+      lst[q] = lst[q] * corr[q] + warp_sumf(p);
+      mst[q] = mnew;
+      const uint32_t hi = pack_bf16x2(p, 0.f) & 0xFFFFu;
+      const float lo = p - __uint_as_float(hi << 16);
+      ds.ph[q][lane] = (uint16_t)hi;
+      ds.pl[q][lane] = (uint16_t)(pack_bf16x2(lo, 0.f) & 0xFFFFu);
+    }
+    // ---- V: draft values of the 32 tokens into the tile
+    {
+      const uint32_t* g4[4];
+      int nw[4];
+      bool fast = true;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        uint32_t a0 = 0u, b0 = 0u;
+        if (sb0 + u < nsb) stream_range(sidxV, sb0 + u, lim, a0, b0);
+        g4[u] = (const uint32_t*)kv_sec(d, CAS_KV_SPEC_EXP, H + h) + a0;
+        nw[u] = (int)(b0 - a0);
+        fast = fast && nw[u] <= 64;
+      }
+      if (fast) {
+        const uint4 mk = __ldg(reinterpret_cast<const uint4*>(kv_sec(d, CAS_KV_MASK, H + h)) + tk);
+        const uint32_t* rec = (const uint32_t*)kv_sec(d, CAS_KV_SPEC_SM, H + h) + tk * 8;
+        uint32_t fn = __ldg(rec);  // the next group's record word
+        // zero the token's row (pruned dims, tokens past the cache)
+        uint4* zr = reinterpret_cast<uint4*>(ds.vt + lane * kDRow);
+#pragma unroll
+        for (int i = 0; i < CAS_BLK / 8; ++i) zr[i] = make_uint4(0u, 0u, 0u, 0u);
+        ds.u.w.ms[0][lane] = valid ? __brev(mk.x) : 0u;
+        ds.u.w.ms[1][lane] = valid ? __brev(mk.y) : 0u;
+        ds.u.w.ms[2][lane] = valid ? __brev(mk.z) : 0u;
+        ds.u.w.ms[3][lane] = valid ? __brev(mk.w) : 0u;
+        const int q0 = block_code_term<2, 64>(g4, nw, whole, ds.u.w.st, lane, fast);
+        const uint32_t ms_a = fenced(ms_a0), st_a = fenced(st_a0);
+        uint32_t ta = row_a - 2u;
+        uint32_t Hp, Lp, Hc, Lc;
+        bwindow(ms_a, 128u, 0, 4, Hp, Lp);
+        bwindow(st_a, 4u, q0 + 1, BlockStreams<2>::kRow - 3, Hc, Lc);
+        uint32_t used = 0u, cor = 0u;
+        if (valid) {
+#pragma unroll 1
+          for (int gi = 0; gi < 8; ++gi) {
+            const uint32_t fo = fn, fe = fn << 4;
+            if (gi < 7) fn = __ldg(rec + gi + 1);
+            if (gi > 0) {
+              const int cur = min((int)(ta - row_a) >> 1, CAS_BLK - 1);
+              ta = row_a + 2u * (uint32_t)cur;
+              bwindow(ms_a, 128u, cur + 1, 4, Hp, Lp);
+              bwindow(st_a, 4u, q0 + 1 + (int)used, BlockStreams<2>::kRow - 3, Hc, Lc);
+            }
+            if (__popc(Hp) + __popc(Lp) < 8 || __popc(Hc) + __popc(Lc) < 8) {  // as for K
+              int cur = (int)(ta - row_a) >> 1, qt = q0 + (int)used;
+              for (int i = 0; i < 8; ++i) {
+                const int pb = bnext_one(ms_a, 128u, cur + 1, 6);
+                const int eb = bnext_one(st_a, 4u, qt + 1, BlockStreams<2>::kRow - 1);
+                if (pb < 0 || pb >= CAS_BLK || eb < 0) {
+                  cor |= 32u;
+                  break;
+                }
+                const uint32_t E = lds_u32(lutv_a + 4u * (uint32_t)min(eb - qt - 1, 255));
+                used += (uint32_t)(eb - qt);
+                qt = eb;
+                cur = pb;
+                const uint32_t f = (fo >> (4 * i)) & 15u;
+                sts_u16(row_a + 2u * (uint32_t)cur, ((f & 8u) << 12) | E | ((f & 7u) << 4));
+              }
+              ta = row_a + 2u * (uint32_t)max(cur, -1);
+              continue;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint32_t np = __clz(Hp) + 1u;
+              ta = mad32(np, 2u, ta);
+              Hp = shfl_wrap(Lp, Hp, np);
+              Lp = shfl_wrap(0u, Lp, np);
+              const uint32_t nc = __clz(Hc) + 1u;
+              const uint32_t E = lds_u32(lutv_a - 4u + 4u * nc);
+              Hc = shfl_wrap(Lc, Hc, nc);
+              Lc = shfl_wrap(0u, Lc, nc);
+              used += nc;
+              cor |= np | nc;
+              const int by = i >> 1;
+              const uint32_t A = __byte_perm((i & 1) ? fo : fe, 0u, by * 0x11 | 0x4400);
+              sts_u16(ta, (A & 0x8070u) | E);
+            }
+          }
+        }
+        // a walk that ran dry may have stored into the next rows: every lane
+        // rebuilds its row by scanning
+        if (__any_sync(CAS_FULL, valid && (cor & 32u))) {
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < CAS_BLK / 8; ++i) zr[i] = make_uint4(0u, 0u, 0u, 0u);
+          bool ok = !valid || draft_v_scan(ms_a, st_a, q0, lutv_a, rec, row_a);
+          if (!ok)
+            for (int i = 0; i < CAS_BLK / 8; ++i) zr[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncwarp();
+      }
+      if (!fast) {
+        for (int u = 0; u < 4; ++u)
+          decode_sb_tile<false>(d, H + h, n, sb0 + u, ds.vt, CAS_SB * u, lut8v, ds.u.tile_scratch, lane);
+        block_streams_init(ds.u.w.st, lane);
+#pragma unroll
+        for (int r = 4; r < 7; ++r) ds.u.w.ms[r][lane] = 0u;
+        __syncwarp();
+      }
+    }
+    // ---- O^T += V^T P^T: rescale, then 2 k-steps x 8 m-tiles x (hi, lo)
+    const float ca = tq == 0 ? corr[0] : corr[2], cb = tq == 0 ? corr[1] : corr[3];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      c[mt][0] *= ca;
+      c[mt][1] *= cb;
+      c[mt][2] *= ca;
+      c[mt][3] *= cb;
+    }
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+      uint32_t bh[2], bl[2];
+      {
+        const int r = lane & 7, kh = (lane >> 3) & 1;
+        const uint32_t ah = smem_addr(&ds.ph[r][16 * ks + 8 * kh]), al = smem_addr(&ds.pl[r][16 * ks + 8 * kh]);
+        asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(bh[0]), "=r"(bh[1]) : "r"(ah));
+        asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(bl[0]), "=r"(bl[1]) : "r"(al));
+      }
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        uint32_t av[4];
+        const int tr = 16 * ks + (lane & 7) + ((lane >> 4) & 1) * 8, dc = 16 * mt + ((lane >> 3) & 1) * 8;
+        ldmatrix_x4_trans(av, ds.vt + tr * kDRow + dc);
+        mma_bf16(c[mt], av, bh[0], bh[1]);
+        mma_bf16(c[mt], av, bl[0], bl[1]);
+      }
+    }
+    __syncwarp();
+  }
+  // merge the 4 warps' states: o[w][q][dim] over the V tiles
+  __syncthreads();
+  float* ow = reinterpret_cast<float*>(stages);  // [4][4][128]
+  __shared__ float wm[kWarps][4], wl[kWarps][4];
+  if (lane < 4) {
+    wm[warp][lane] = lane == 0 ? mst[0] : lane == 1 ? mst[1] : lane == 2 ? mst[2] : mst[3];
+    wl[warp][lane] = lane == 0 ? lst[0] : lane == 1 ? lst[1] : lane == 2 ? lst[2] : lst[3];
+  }
+  if (tq < 2) {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const int d0 = 16 * mt + gq;
+      ow[(warp * 4 + 2 * tq) * CAS_BLK + d0] = c[mt][0];
+      ow[(warp * 4 + 2 * tq + 1) * CAS_BLK + d0] = c[mt][1];
+      ow[(warp * 4 + 2 * tq) * CAS_BLK + d0 + 8] = c[mt][2];
+      ow[(warp * 4 + 2 * tq + 1) * CAS_BLK + d0 + 8] = c[mt][3];
+    }
+  }
+  __syncthreads();
+  // warp q writes query vector q's partial
+  if (warp < nq) {
+    const int q = warp;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w2 = 0; w2 < kWarps; ++w2) M = fmaxf(M, wm[w2][q]);
+    float L = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int w2 = 0; w2 < kWarps; ++w2) {
+      if (wm[w2][q] == -INFINITY) continue;
+      const float f = __expf(wm[w2][q] - M);
+      L += wl[w2][q] * f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] += f * ow[(w2 * 4 + q) * CAS_BLK + 4 * lane + i];
+    }
+    float* dst = a.part + (((int64_t)b * a.Hq + h * G + q) * a.nchunk + chunk) * kPart;
+    reinterpret_cast<float2*>(dst)[2 * lane] = make_float2(o[0], o[1]);
+    reinterpret_cast<float2*>(dst)[2 * lane + 1] = make_float2(o[2], o[3]);
+    if (lane == 0) {
+      dst[CAS_BLK] = M;
+      dst[CAS_BLK + 1] = L;
+    }
+  }
+}
+
+int launch_draft_block(AttnArgs& a, int Hkv, cudaStream_t st) {
+  const size_t smem = (size_t)CAS_BLK * 16 + 2 * 256 * 4 + 2 * 256 + (size_t)kWarps * sizeof(DraftStage);
+  const int s = one_wave(a, Hkv, (const void*)attn_draft_block_kernel, smem);
+  if (s) return s;
+  attn_draft_block_kernel<<<dim3(a.nchunk, Hkv, a.B), kThreads, smem, st>>>(a);
+  return launch_status();
+}
+
 template <bool FULL, int MT>
 int launch_mma(AttnArgs& a, int Hkv, cudaStream_t st) {
   const size_t smem = mma_smem(MT, a.scr_warp);
@@ -861,7 +1323,12 @@ int run_attn(bool full, const cas_kv* const* kv, int B, const uint16_t* q, int T
   a.qv_alloc = std::min(T * G, kQvPerCta);
   int qpw = (std::min(T * G, kQvPerCta) + kWarps - 1) / kWarps;
   int s;
-  if (!full && T == 1 && a.qv_alloc <= 4) {
+  bool block_ok = true;  // every cache Cassandra-1 with k = 64, m = 3
+  for (int i = 0; i < B; ++i)
+    block_ok = block_ok && kv[i]->p.variant == 1 && kv[i]->p.keep_per_block == 64 && kv[i]->p.mant_bits == 3;
+  if (!full && T == 1 && a.qv_alloc <= 4 && block_ok) {
+    s = launch_draft_block(a, Hkv, st);
+  } else if (!full && T == 1 && a.qv_alloc <= 4) {
     s = launch_fused(a, Hkv, st);
   } else if (!full) {
     s = qpw <= 4 ? launch_chunk<false, 4>(a, Hkv, st) : launch_chunk<false, 8>(a, Hkv, st);
