@@ -41,6 +41,7 @@ constexpr int kChunk = 256;      // smallest chunk the workspace is sized for
 constexpr int kStepTok = 32;     // tokens per step (4 superblocks)
 constexpr int kRow = CAS_BLK + 8;  // bf16 tile row stride (272 B: conflict-free 16-byte rows)
 constexpr int kPart = CAS_BLK + 2; // floats per partial: o[128], m, l
+constexpr int kTileSlack = 1024;   // bytes after the verify V tile: stores of a failed walk stay inside
 constexpr int kMaxBatch = 8;
 constexpr int kMaxT = 16;
 
@@ -269,6 +270,147 @@ __global__ void __launch_bounds__(kThreads) attn_chunk_kernel(AttnArgs a) {
   }
 }
 
+// ---------------------------------------------------------------- exact tiles by block walks
+// Cassandra-1 caches with k = 64, m = 3: superblock sb (8 tokens) of the K and
+// V streams of head h rebuilt exactly into tile rows row0 .. row0+7 of Kt and
+// Vt by one warp (blockwalk.cuh). Lane 8t + j walks token j of stream K (t <
+// 2) or V (t >= 2): its 64 kept values for even t (sign and 3 high mantissa
+// bits joined with the 4 cut bits), its 64 pruned values for odd t (the pruned
+// byte), so the four staged code streams are K kept, K pruned, V kept, V
+// pruned. A group of 8 values whose positions or codes do not all end in the
+// 64-bit windows (a code longer than the window: an exponent the calibrated
+// table ranks far down) is taken by scanning. Streams longer than the stage go
+// to decode_sb_tile. Returns false when a walk stepped 32 or more anyway (a
+// gap of 32 or more, a code of 31 to 63 bits inside a full window): its rows
+// are then wrong and its stores may have run up to 782 bytes past its row.
+struct KvBlockStage {
+  BlockStreams<3, 80> st;  // codes: K kept, K pruned, V kept, V pruned
+  uint32_t ms[7][32];      // row i, column l: bit-reversed word i of lane l's positions; rows 4-6 zero
+};
+static_assert(sizeof(KvBlockStage) % 16 == 0, "stage alignment");
+
+__device__ __forceinline__ bool kv_block_tiles(const KvDev& d, int h, int64_t n, int64_t sb, uint16_t* Kt, uint16_t* Vt,
+                                            int row0, const uint32_t* lut7k, const uint32_t* lut7v,
+                                            const uint8_t* lutK, const uint8_t* lutV, uint8_t* scratch, int lane) {
+  KvBlockStage& vs = *reinterpret_cast<KvBlockStage*>(scratch);
+  const int H = d.H, t = lane >> 3, j = lane & 7;
+  const bool pruned = t & 1;
+  const int st = t < 2 ? h : H + h;
+  const int64_t nsb = (n + CAS_SB - 1) / CAS_SB, tok = sb * CAS_SB + j;
+  const bool valid = sb < nsb && tok < n;
+  uint16_t* row = (t < 2 ? Kt : Vt) + (row0 + j) * kRow;
+  if (!valid) {  // a token past the cache: a zero row
+    uint4* z = reinterpret_cast<uint4*>(row);
+    for (int i = (int)pruned; i < CAS_BLK / 8; i += 2) z[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (sb >= nsb) {
+    __syncwarp();
+    return true;
+  }
+  const uint32_t* gs[4];
+  int nw[4];
+  bool fast = true;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int su = u < 2 ? h : H + h;
+    uint32_t a0, b0;
+    if (u & 1)
+      stream_range((const uint32_t*)kv_sec(d, CAS_KV_VER_SBIDX, su), sb, (uint32_t)d.cap_b, a0, b0);
+    else
+      stream_range((const uint32_t*)kv_sec(d, CAS_KV_SPEC_SBIDX, su), sb, (uint32_t)d.cap_a, a0, b0);
+    gs[u] = (const uint32_t*)kv_sec(d, (u & 1) ? CAS_KV_VER_EXP : CAS_KV_SPEC_EXP, su) + a0;
+    nw[u] = (int)(b0 - a0);
+    fast = fast && nw[u] <= BlockStreams<3, 80>::kWords;
+  }
+  int q0 = 0;
+  if (fast) {
+    block_streams_init(vs.st, lane);
+#pragma unroll
+    for (int r = 4; r < 7; ++r) vs.ms[r][lane] = 0u;
+    const uint4 mk = __ldg(reinterpret_cast<const uint4*>(kv_sec(d, CAS_KV_MASK, st)) + (valid ? tok : 0));
+    const uint32_t inv = pruned ? 0xFFFFFFFFu : 0u;
+    vs.ms[0][lane] = valid ? __brev(mk.x ^ inv) : 0u;
+    vs.ms[1][lane] = valid ? __brev(mk.y ^ inv) : 0u;
+    vs.ms[2][lane] = valid ? __brev(mk.z ^ inv) : 0u;
+    vs.ms[3][lane] = valid ? __brev(mk.w ^ inv) : 0u;
+    q0 = block_code_term<3, 64>(gs, nw, CAS_SB * (sb + 1) <= n ? 4 : 0, vs.st, lane, fast);
+  }
+  if (!fast) {  // streams longer than the stage, or too few codes: the tile decoder
+    __syncwarp();
+    decode_sb_tile<true>(d, h, n, sb, Kt, row0, lutK, scratch, lane);
+    decode_sb_tile<true>(d, H + h, n, sb, Vt, row0, lutV, scratch, lane);
+    return true;
+  }
+  const uint32_t ms_a = fenced(smem_addr(&vs.ms[0][lane])), st_a = fenced(smem_addr(&vs.st.w[t][0]));
+  const uint32_t lut_a = smem_addr(t < 2 ? lut7k : lut7v);
+  const uint32_t* ra = pruned ? (const uint32_t*)kv_sec(d, CAS_KV_VER_PR, st) + tok * 16
+                              : (const uint32_t*)kv_sec(d, CAS_KV_SPEC_SM, st) + tok * 8;
+  const uint32_t* rb = pruned ? ra + 1 : (const uint32_t*)kv_sec(d, CAS_KV_VER_LO, st) + tok * 8;
+  const int rs = pruned ? 2 : 1;
+  const uint32_t tb = smem_addr(row);
+  uint32_t ta = tb - 2u;
+  uint32_t cor = 0u;
+  if (valid) {
+    uint32_t Hp, Lp, Hc, Lc;
+    bwindow(ms_a, 128u, 0, 4, Hp, Lp);
+    bwindow(st_a, 4u, q0 + 1, BlockStreams<3, 80>::kRow - 3, Hc, Lc);
+    uint32_t used = 0u;
+    uint32_t an = __ldg(ra), bn = __ldg(rb);
+#pragma unroll 1
+    for (int gi = 0; gi < 8; ++gi) {
+      const uint32_t aw = an, bw = bn;
+      if (gi < 7) {
+        an = __ldg(ra + rs * (gi + 1));
+        bn = __ldg(rb + rs * (gi + 1));
+      }
+      if (gi > 0) {
+        const int cur = min((int)(ta - tb) >> 1, CAS_BLK - 1);
+        ta = tb + 2u * (uint32_t)cur;
+        bwindow(ms_a, 128u, cur + 1, 4, Hp, Lp);
+        bwindow(st_a, 4u, q0 + 1 + (int)used, BlockStreams<3, 80>::kRow - 3, Hc, Lc);
+      }
+      // bytes [s f6 .. f0] of the group's values 0, 2, 4, 6 (ev) and 1, 3, 5, 7 (od)
+      const uint32_t ev = pruned ? __byte_perm(aw, bw, 0x6420) : ((aw << 4) & 0xF0F0F0F0u) | (bw & 0x0F0F0F0Fu);
+      const uint32_t od = pruned ? __byte_perm(aw, bw, 0x7531) : (aw & 0xF0F0F0F0u) | ((bw >> 4) & 0x0F0F0F0Fu);
+      if (__popc(Hp) + __popc(Lp) < 8 || __popc(Hc) + __popc(Lc) < 8) {  // this group by scanning
+        int cur = (int)(ta - tb) >> 1, qt = q0 + (int)used;
+        for (int i = 0; i < 8; ++i) {
+          const int pb = bnext_one(ms_a, 128u, cur + 1, 6);
+          const int eb = bnext_one(st_a, 4u, qt + 1, BlockStreams<3, 80>::kRow - 1);
+          if (pb < 0 || pb >= CAS_BLK || eb < 0) {
+            cor |= 32u;
+            break;
+          }
+          const uint32_t E = lds_u32(lut_a + 4u * (uint32_t)min(eb - qt - 1, 255));
+          used += (uint32_t)(eb - qt);
+          qt = eb;
+          cur = pb;
+          const uint32_t by = (((i & 1) ? od : ev) >> (8 * (i >> 1))) & 0xFFu;
+          sts_u16(tb + 2u * (uint32_t)cur, ((by & 0x80u) << 8) | E | (by & 0x7Fu));
+        }
+        ta = tb + 2u * (uint32_t)max(cur, -1);
+        continue;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t np = __clz(Hp) + 1u;
+        ta = mad32(np, 2u, ta);
+        Hp = shfl_wrap(Lp, Hp, np);
+        Lp = shfl_wrap(0u, Lp, np);
+        const uint32_t nc = __clz(Hc) + 1u;  // rank + 1
+        const uint32_t E = lds_u32(lut_a - 4u + 4u * nc);
+        Hc = shfl_wrap(Lc, Hc, nc);
+        Lc = shfl_wrap(0u, Lc, nc);
+        used += nc;
+        cor |= np | nc;
+        const uint32_t A = __byte_perm((i & 1) ? od : ev, 0u, (uint32_t)(i >> 1) * 0x11u | 0x4400u);
+        sts_u16(ta, (A & 0x807Fu) | E);
+      }
+    }
+  }
+  return !__any_sync(CAS_FULL, valid && (cor & 32u));
+}
+
 // Tensor-core variant of the chunk kernel (up to 32 query vectors per CTA in
 // MT m16 tiles): per 32-token step, after the K and V superblocks are
 // decoded into the tiles, S = Q K^T (mma m16n8k16, bf16 inputs, fp32
@@ -280,14 +422,16 @@ __global__ void __launch_bounds__(kThreads) attn_chunk_kernel(AttnArgs a) {
 // output dimensions; with MT = 1 the 4 warps split them four ways (each
 // warp recomputes the m-tile's S, which is cheap next to the decode).
 template <bool FULL, int MT>
-__global__ void __launch_bounds__(kThreads, MT == 2 ? 5 : 6) attn_mma_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, MT == 2 ? 4 : 5) attn_mma_kernel(AttnArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint16_t* Kt = reinterpret_cast<uint16_t*>(smem);
   uint16_t* Vt = Kt + kStepTok * kRow;
-  uint16_t* Qt = Vt + kStepTok * kRow;  // [16 MT][kRow], rows >= nq zero
+  uint16_t* Qt = Vt + kStepTok * kRow + kTileSlack / 2;  // [16 MT][kRow], rows >= nq zero
   uint8_t* lutK = reinterpret_cast<uint8_t*>(Qt + 16 * MT * kRow);
   uint8_t* lutV = lutK + 256;
-  uint8_t* scr = lutV + 256;
+  uint32_t* lut7K = reinterpret_cast<uint32_t*>(lutV + 256);  // exponent << 7 by rank
+  uint32_t* lut7V = lut7K + 256;
+  uint8_t* scr = reinterpret_cast<uint8_t*>(lut7V + 256);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint8_t* wscr = scr + warp * a.scr_warp;
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z / a.ngroups;
@@ -311,8 +455,11 @@ __global__ void __launch_bounds__(kThreads, MT == 2 ? 5 : 6) attn_mma_kernel(Att
   for (int i = threadIdx.x; i < 256; i += kThreads) {
     lutK[i] = kv_exp_of_rank(d, h)[i];
     lutV[i] = kv_exp_of_rank(d, H + h)[i];
+    lut7K[i] = (uint32_t)lutK[i] << 7;
+    lut7V[i] = (uint32_t)lutV[i] << 7;
   }
   __syncthreads();
+  const bool walk = FULL && d.variant == 1 && d.k == 64 && d.m == 3;
 
   constexpr int WPM = 4 / MT;       // warps per m-tile
   constexpr int NT = 16 / WPM;      // 8-dim output tiles per warp
@@ -331,9 +478,18 @@ __global__ void __launch_bounds__(kThreads, MT == 2 ? 5 : 6) attn_mma_kernel(Att
 
   for (int64_t t0 = t_begin; t0 < t_end; t0 += kStepTok) {
     const int64_t sb = t0 / CAS_SB + warp;
-    decode_sb_tile<FULL>(d, h, n, sb, Kt, warp * CAS_SB, lutK, wscr, lane);
-    decode_sb_tile<FULL>(d, H + h, n, sb, Vt, warp * CAS_SB, lutV, wscr, lane);
-    __syncthreads();
+    bool bad = false;
+    if (walk) {
+      bad = !kv_block_tiles(d, h, n, sb, Kt, Vt, warp * CAS_SB, lut7K, lut7V, lutK, lutV, wscr, lane);
+    } else {
+      decode_sb_tile<FULL>(d, h, n, sb, Kt, warp * CAS_SB, lutK, wscr, lane);
+      decode_sb_tile<FULL>(d, H + h, n, sb, Vt, warp * CAS_SB, lutV, wscr, lane);
+    }
+    if (__syncthreads_or(bad)) {  // a failed walk may have stored into other warps' rows: rebuild all
+      decode_sb_tile<FULL>(d, h, n, sb, Kt, warp * CAS_SB, lutK, wscr, lane);
+      decode_sb_tile<FULL>(d, H + h, n, sb, Vt, warp * CAS_SB, lutV, wscr, lane);
+      __syncthreads();
+    }
     if (active) {
       // S = Q K^T: 16 rows x 32 tokens
       float s[4][4];
@@ -473,6 +629,7 @@ __device__ __forceinline__ float4 lane_kept_qdot(UnaryCursor& uc, uint4 kq, uint
   }
   return acc;
 }
+
 
 // Scores of the 8 tokens of superblock sb of K stream st against the 4 query
 // vectors into out[8][4] (float4 per token). Only for whole Cassandra-1
@@ -779,7 +936,8 @@ size_t chunk_smem(int qv_alloc, int scr_warp) {
 int nchunks(int64_t max_tokens) { return (int)((max_tokens + kChunk - 1) / kChunk); }
 
 size_t mma_smem(int mt, int scr_warp) {
-  return (size_t)2 * kStepTok * kRow * 2 + (size_t)16 * mt * kRow * 2 + 512 + (size_t)kWarps * scr_warp;
+  return (size_t)2 * kStepTok * kRow * 2 + kTileSlack + (size_t)16 * mt * kRow * 2 + 512 + 2048 +
+         (size_t)kWarps * scr_warp;
 }
 
 // Sets a.nchunk to one wave of resident CTAs (at most the workspace's count).
@@ -1264,6 +1422,8 @@ int launch_draft_block(AttnArgs& a, int Hkv, cudaStream_t st) {
 
 template <bool FULL, int MT>
 int launch_mma(AttnArgs& a, int Hkv, cudaStream_t st) {
+  // the block walks' stage (every Cassandra-1 cache uses a C-1 scratch)
+  if (a.scr_warp == kScratchC1) a.scr_warp = std::max<int>(kScratchC1, (int)sizeof(KvBlockStage));
   const size_t smem = mma_smem(MT, a.scr_warp);
   auto kern = attn_mma_kernel<FULL, MT>;
   const int s = one_wave(a, Hkv, (const void*)kern, smem);
