@@ -8,10 +8,11 @@
 // split the k16 steps of the tile among themselves on the tensor cores
 // (mma m16n8k16, bf16 inputs, fp32 accumulation; T <= 8 uses one n8 tile, T <= 16
 // two). Warp partials are summed in shared memory and added to Y with fp32
-// atomics; Y is cleared first. The row-superblocks are rebuilt by the
-// per-lane decoders of lanedec.cuh (k = 64, m = 3; any k, m on rows of whole
-// superblocks, both variants) or, for rows ending in a partial superblock, by
-// the generic warp decoder of sbdecode.cuh.
+// atomics; Y is cleared first. Cassandra-1 with k = 64, m = 3 on rows of whole
+// superblocks rebuilds the tile by block walks (verify_gemm_block_kernel,
+// blockwalk.cuh); other k, m and Cassandra-2 by the per-lane run decoders of
+// lanedec.cuh; rows ending in a partial superblock by the generic warp
+// decoder of sbdecode.cuh.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -55,14 +56,12 @@ __host__ __device__ constexpr int scratch_warp() {
   return (((int)sizeof(TileStage) > generic ? (int)sizeof(TileStage) : generic) + 15) & ~15;
 }
 static_assert(scratch_warp<1>() % 16 == 0 && alignof(TileStage) <= 16, "per-warp scratch alignment");
-static_assert(scratch_warp<1>() >= (int)sizeof(WordTileStage), "word decoder stage fits");
 static_assert(scratch_warp<2>() >= (int)sizeof(TileStage2) && alignof(TileStage2) <= 16, "Cassandra-2 stage fits");
 static_assert(kWarps * scratch_warp<1>() >= kWarps * 256 * 4, "warp partials fit in the scratch");
 
-// FAST: Cassandra-1, k = 64, m = 3, whole superblocks (per-lane cursors, lane_sb_tile).
-// MODE 1: Cassandra-1, k = 64, m = 3 (lane_sb_tile); MODE 2: rows of whole
-// superblocks, any k, m (runs_sb_tile, Cassandra-2: runs_sb_tile_c2);
-// MODE 0: generic.
+// MODE 2: rows of whole superblocks, any k, m (runs_sb_tile, Cassandra-2:
+// runs_sb_tile_c2); MODE 0: generic. (Cassandra-1 with k = 64, m = 3 runs
+// verify_gemm_block_kernel below.)
 template <int VAR, int NT, int MODE>
 __global__ void __launch_bounds__(kThreads, 4) verify_gemm_kernel(GemmArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -105,12 +104,6 @@ __global__ void __launch_bounds__(kThreads, 4) verify_gemm_kernel(GemmArgs a) {
                                        w.vpr + gb0 * w.rec_pr, w.rec_pr, w.vexp + v0, (int)(v1 - v0), w.k, w.m,
                                        s_lut, *reinterpret_cast<TileStage2*>(wscr), tile + r * kTileStride,
                                        kBlkStride, lane);
-        } else if (MODE == 1) {
-          uint32_t a0, a1;
-          stream_range(w.sidx, s, w.lim_sexp, a0, a1);
-          done = word_tile<true>(w.mask + gb0 * 4, w.ssm + gb0 * 8, w.vlo + gb0 * 8, w.vpr + gb0 * 16,
-                                 w.sexp + a0, (int)(a1 - a0), w.vexp + v0, (int)(v1 - v0), s_lut,
-                                 *reinterpret_cast<WordTileStage*>(wscr), tile + r * kTileStride, kBlkStride, lane);
         } else {
           uint32_t a0, a1;
           stream_range(w.sidx, s, w.lim_sexp, a0, a1);
