@@ -942,13 +942,14 @@ size_t word_smem(int64_t K) {
 inline int word_per(int64_t nsb, int g) { return (int)((nsb + (int64_t)g * kWarps - 1) / ((int64_t)g * kWarps)); }
 
 // ------------------------------------------------------------------ block path
-// Cassandra-1, k = 64, m = 3, rows of whole superblocks with at least 32
-// blocks (K >= 4096), 1 or 2 vectors. A warp takes a chunk of 32 consecutive
-// blocks (4 superblocks) and lane L owns block L of it: 128 positions with
-// exactly 64 kept values, so every lane decodes the same number of values.
+// Cassandra-1, m = 3, k = 64 or 38 (keep 50 % or 30 %), rows of whole
+// superblocks with at least 32 blocks (K >= 4096), 1 or 2 vectors. A warp
+// takes a chunk of 32 consecutive blocks (4 superblocks) and lane L owns block
+// L of it: 128 positions with exactly k kept values, so every lane decodes the
+// same number of values.
 // Per chunk the warp stages the 4 superblocks' code streams and its blocks'
 // bit-reversed mask words in shared memory; each lane finds where its block's
-// codes start (the bit after the (64 j)-th '1' of its superblock's stream, j
+// codes start (the bit after the (k j)-th '1' of its superblock's stream, j
 // the block's place in it) by a warp popcount scan and a shuffle search, and
 // then walks two cursors of its own, re-aligned every 8 values:
 //   position: a 64-bit window of the bit-reversed mask starting just after the
@@ -994,13 +995,13 @@ struct ScanSum {
 };
 template <int NV>
 __device__ __noinline__ ScanSum<NV> block_walk_scan(uint32_t ms_a, uint32_t st_a, uint32_t fs_a, uint32_t lut_a,
-                                                    uint32_t xbase, int xfl, int cq0) {
+                                                    uint32_t xbase, int xfl, int cq0, int keep) {
   ScanSum<NV> r;
   int cur = -1, qc = cq0;
 #pragma unroll
   for (int q = 0; q < NV; ++q) r.part[q] = 0.f;
   r.ok = false;
-  for (int i = 0; i < 64; ++i) {
+  for (int i = 0; i < keep; ++i) {
     const int pb = bnext_one(ms_a, 128u, 32 + cur + 1, kBMaskRows - 1);
     const int tb = bnext_one(st_a, 4u, qc + 1, kBStreamWords - 1);
     if (pb < 0 || pb >= 32 + CAS_BLK || tb < 0) return r;
@@ -1016,8 +1017,10 @@ __device__ __noinline__ ScanSum<NV> block_walk_scan(uint32_t ms_a, uint32_t st_a
   return r;
 }
 
-template <int NV>
+template <int NV, int KEEP>
 __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs a) {
+  constexpr int kRec = (KEEP * 4 + 31) / 32;  // sign/mantissa record words per block
+  constexpr int kGroups = (KEEP + 7) / 8;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint32_t lut32[256];  // exponent << 23 by rank
   __shared__ uint8_t lut8[256];    // exponent by rank (generic decoder)
@@ -1100,24 +1103,32 @@ __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs
     const int64_t gl = valid ? g : (int64_t)c * 32;
     if (fast) {
       const uint4 mk = __ldg(reinterpret_cast<const uint4*>(w.mask) + gl);
-      const uint4 fA = __ldg(reinterpret_cast<const uint4*>(w.ssm + gl * 8));
-      const uint4 fB = __ldg(reinterpret_cast<const uint4*>(w.ssm + gl * 8) + 1);
+      uint32_t fw[kRec];
+      if (KEEP == 64) {
+        const uint4 fA = __ldg(reinterpret_cast<const uint4*>(w.ssm + gl * 8));
+        const uint4 fB = __ldg(reinterpret_cast<const uint4*>(w.ssm + gl * 8) + 1);
+        fw[0] = fA.x;
+        fw[1] = fA.y;
+        fw[2] = fA.z;
+        fw[3] = fA.w;
+        fw[kRec > 4 ? 4 : 0] = fB.x;
+        fw[kRec > 5 ? 5 : 0] = fB.y;
+        fw[kRec > 6 ? 6 : 0] = fB.z;
+        fw[kRec > 7 ? 7 : 0] = fB.w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < kRec; ++i) fw[i] = __ldg(w.ssm + gl * kRec + i);
+      }
       bs.ms[1][lane] = valid ? __brev(mk.x) : 0u;
       bs.ms[2][lane] = valid ? __brev(mk.y) : 0u;
       bs.ms[3][lane] = valid ? __brev(mk.z) : 0u;
       bs.ms[4][lane] = valid ? __brev(mk.w) : 0u;
-      bs.fs[0][lane] = fA.x;
-      bs.fs[1][lane] = fA.y;
-      bs.fs[2][lane] = fA.z;
-      bs.fs[3][lane] = fA.w;
-      bs.fs[4][lane] = fB.x;
-      bs.fs[5][lane] = fB.y;
-      bs.fs[6][lane] = fB.z;
-      bs.fs[7][lane] = fB.w;
+#pragma unroll
+      for (int i = 0; i < kRec; ++i) bs.fs[i][lane] = fw[i];
       const uint32_t* gsx[4] = {w.sexp + sa[0], w.sexp + sa[1], w.sexp + sa[2], w.sexp + sa[3]};
       const int present = nsb - (int64_t)c * 4 < 4 ? (int)(nsb - (int64_t)c * 4) : 4;
       // staged bit of the '1' before the block's first code
-      const int cq0 = block_code_term<2, 64>(gsx, nw, present, bs.st, lane, fast);
+      const int cq0 = block_code_term<2, KEEP>(gsx, nw, present, bs.st, lane, fast);
       const uint32_t ms_a = fenced(ms_a0), fs_a = fenced(fs_a0), st_a = fenced(st_a0);
       // cursors
       // row and block in the row (nbr >= 32: the chunk wraps at most once)
@@ -1134,7 +1145,7 @@ __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs
 #pragma unroll
       for (int q = 0; q < NV; ++q) part[q] = 0.f;
 #pragma unroll
-      for (int gi = 0; gi < 8; ++gi) {
+      for (int gi = 0; gi < kGroups; ++gi) {
         if (gi > 0) {
           const int cur = min((int)(xa - xbase) >> 2, CAS_BLK - 1);
           xa = xbase + 4u * (uint32_t)cur;
@@ -1144,6 +1155,7 @@ __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs
         const uint32_t fo = lds_u32(fs_a + 128u * gi), fe = fo << 4;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
+          if (8 * gi + i >= KEEP) break;
           const uint32_t np = __clz(Hp) + 1u;  // distance to the next kept position
           xa = mad32(np, 4u, xa);
           Hp = shfl_wrap(Lp, Hp, np);
@@ -1164,7 +1176,7 @@ __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs
       // a lane whose windows ran dry scans its block again (divergent, rare)
       bool bad = false;
       if (valid && (cor & 32u)) {
-        const ScanSum<NV> r = block_walk_scan<NV>(ms_a, st_a, fs_a, lut_a, xbase, xfl, cq0);
+        const ScanSum<NV> r = block_walk_scan<NV>(ms_a, st_a, fs_a, lut_a, xbase, xfl, cq0, KEEP);
 #pragma unroll
         for (int q = 0; q < NV; ++q) part[q] = r.part[q];
         bad = !r.ok;
@@ -1232,9 +1244,9 @@ inline int block_per(int64_t nsb, int g) {
   return (int)((nch + (int64_t)g * kBWarps - 1) / ((int64_t)g * kBWarps));
 }
 
-template <int NV>
+template <int NV, int KEEP>
 int launch_block(const GemvArgs& a, cudaStream_t st) {
-  auto kern = draft_gemv_block_kernel<NV>;
+  auto kern = draft_gemv_block_kernel<NV, KEEP>;
   const int max_per_sm = occupancy((const void*)kern, kBThreads, block_smem<NV>(a.w.nbr));
   if (max_per_sm < 1) return CAS_ERR_CUDA;
   const int64_t nch = (a.w.nsb + 3) / 4;
@@ -1278,8 +1290,10 @@ int launch_word(const GemvArgs& a, cudaStream_t st) {
 template <int VAR>
 int dispatch(const GemvArgs& a, int nvec, cudaStream_t st) {
   const bool fast = a.w.k == 64 && a.w.m == 3 && a.w.nbr % CAS_SB == 0;
-  if (fast && VAR == 1 && nvec <= 2 && a.w.nbr >= 32 && block_smem<2>(a.w.nbr) <= 200 * 1024)
-    return nvec == 1 ? launch_block<1>(a, st) : launch_block<2>(a, st);
+  const bool block = VAR == 1 && nvec <= 2 && a.w.m == 3 && a.w.nbr % CAS_SB == 0 && a.w.nbr >= 32 &&
+                     block_smem<2>(a.w.nbr) <= 200 * 1024;
+  if (block && a.w.k == 64) return nvec == 1 ? launch_block<1, 64>(a, st) : launch_block<2, 64>(a, st);
+  if (block && a.w.k == 38) return nvec == 1 ? launch_block<1, 38>(a, st) : launch_block<2, 38>(a, st);
   if (fast && VAR == 1 && nvec <= 2 && word_smem<2>(a.w.K) <= 200 * 1024)
     return nvec == 1 ? launch_word<1>(a, st) : launch_word<2>(a, st);
   if (fast && VAR == 1) {

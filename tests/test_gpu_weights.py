@@ -330,20 +330,22 @@ def test_draft_gemv_clustered_masks(cas, orc, N, K, nvec):
     check_close(y, ref, norm, "draft_gemv clustered masks")
 
 
+@pytest.mark.parametrize("keep", [64, 38])
 @pytest.mark.parametrize("nvec", [1, 2])
 @pytest.mark.parametrize("N,K,kind", [(3, 4096, "t4"), (5, 14336, "t4"), (7, 5120, "t4"), (9, 8192, "t4"),
                                        (6, 5120, "clustered"), (11, 14336, "clustered")])
-def test_draft_gemv_block_chunks(cas, orc, N, K, kind, nvec):
+def test_draft_gemv_block_chunks(cas, orc, N, K, kind, nvec, keep):
     """Rows of 32 or more blocks: a warp decodes 32 consecutive blocks (four
-    superblocks) at once, so chunks span two rows (K = 5120, 14336), the last
+    superblocks) at once, for keep 64 and 38 of 128, so chunks span two rows
+    (K = 5120, 14336), the last
     chunk of a matrix can hold fewer than four superblocks (N * K / 1024 not a
     multiple of 4), and chunks with long codes or long runs of pruned
     positions (clustered rows) go to the generic decoder."""
     W = synthetic.t4_weight(N, K, seed=N + K) if kind == "t4" else clustered_rows(N, K, seed=2 * N + K)
     x = synthetic.activations(nvec, K, seed=17 + nvec)
-    enc = cas.encode_weights(W.cuda(), 1, 64, 3)
+    enc = cas.encode_weights(W.cuda(), 1, keep, 3)
     y = cas.draft_gemv(enc, x.cuda())
-    ref, norm = orc.matvec(orc.draft_values(np16(W), 1, 64, 3), np16(x))
+    ref, norm = orc.matvec(orc.draft_values(np16(W), 1, keep, 3), np16(x))
     check_close(y, ref, norm, "draft_gemv block chunks")
 
 
