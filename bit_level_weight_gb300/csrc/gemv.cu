@@ -1059,9 +1059,10 @@ __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs
   const int64_t nsb = w.nsb;
   const int nch = (int)((nsb + 3) / 4);
   const int nwarps = gridDim.x * kBWarps;
-  const int gw = blockIdx.x * kBWarps + warp;
+  // chunks dealt round-robin over the CTAs (chunk c to CTA c % gridDim.x), so
+  // a small matrix spreads evenly over the CTAs of the wave, and so over the SMs
+  const int gw = warp * gridDim.x + blockIdx.x;
   const int per = (nch + nwarps - 1) / nwarps;
-  const int c0 = min(gw * per, nch), c1 = min(c0 + per, nch);
   const uint32_t lim = (uint32_t)a.sexp_words;
   const int t = lane >> 3, j = lane & 7;
   const uint32_t ms_a0 = smem_addr(&bs.ms[0][lane]);
@@ -1078,10 +1079,10 @@ __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs
   bs.ms[6][lane] = 0u;
   bs.ms[7][lane] = 0u;
 
-  // row and block in the row of the chunk's first block
-  uint32_t row0 = (uint32_t)(((int64_t)c0 * 32) / nbr);
-  uint32_t jb0 = (uint32_t)((int64_t)c0 * 32 - (int64_t)row0 * nbr);
-  for (int c = c0; c < c1; ++c) {
+  for (int c = gw; c < nch; c += nwarps) {
+    // row and block in the row of the chunk's first block
+    const uint32_t row0 = (uint32_t)(((int64_t)c * 32) / nbr);
+    const uint32_t jb0 = (uint32_t)((int64_t)c * 32 - (int64_t)row0 * nbr);
     // the chunk's streams; a stream longer than the stage sends the chunk to
     // the generic decoder
     uint32_t sa[4];
@@ -1206,11 +1207,6 @@ __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs
       if (lane == 0) fb[nfb] = c;
       ++nfb;
     }
-    jb0 += 32u;
-    if (jb0 >= (uint32_t)nbr) {
-      jb0 -= (uint32_t)nbr;
-      ++row0;
-    }
   }
   // chunks the block walk did not take: the generic decoder, one superblock
   // at a time
@@ -1249,9 +1245,9 @@ int launch_block(const GemvArgs& a, cudaStream_t st) {
   auto kern = draft_gemv_block_kernel<NV, KEEP>;
   const int max_per_sm = occupancy((const void*)kern, kBThreads, block_smem<NV>(a.w.nbr));
   if (max_per_sm < 1) return CAS_ERR_CUDA;
+  // one full wave (chunks are dealt round-robin over the CTAs), at most a CTA per chunk
   const int64_t nch = (a.w.nsb + 3) / 4;
-  const int64_t need = (nch + kBWarps - 1) / kBWarps;
-  int g = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sm_count() * max_per_sm));
+  int g = (int)std::max<int64_t>(1, std::min<int64_t>(nch, (int64_t)sm_count() * max_per_sm));
   size_t smem = block_smem<NV>(a.w.nbr) + (size_t)kBWarps * block_per(a.w.nsb, g) * sizeof(int);
   const int per_sm = occupancy((const void*)kern, kBThreads, smem);
   if (per_sm < 1) return CAS_ERR_CUDA;
