@@ -41,9 +41,8 @@ __device__ __forceinline__ uint32_t fenced(uint32_t a) {
   return r;
 }
 __device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
-__device__ __forceinline__ void sts_u16(uint32_t a, uint32_t v) {
-  asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"((uint16_t)v));
-}
+// Stores the low 16 bits of v (the instruction truncates the 32-bit register).
+__device__ __forceinline__ void sts_u16(uint32_t a, uint32_t v) { asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "r"(v)); }
 
 // 64-bit window (H, L) of a staged MSB-first bitstream at bit q: word rows
 // `stride` bytes apart starting at address `base`, rows 0 .. maxw + 2.

@@ -299,16 +299,20 @@ __global__ void __launch_bounds__(kVThreads, 4) verify_gemm_block_kernel(GemmArg
   const uint32_t lut_a = smem_addr(lut7) - 4u;  // rank c - 1 at lut_a + 4c
   const uint32_t tile_a = smem_addr(tile);
   for (int64_t task = blockIdx.x; task < ntasks; task += gridDim.x) {
-    const int64_t rt = task / w.nsr;
-    const int col = (int)(task % w.nsr);
+    // task indices fit 32 bits (launch checks): 32-bit division
+    const uint32_t nsr32 = (uint32_t)w.nsr;
+    const uint32_t rt32 = (uint32_t)task / nsr32;
+    const int64_t rt = rt32;
+    const int col = (int)((uint32_t)task - rt32 * nsr32);
     const int64_t r0 = rt * kVRows + 2 * warp;  // the warp's first row
     const int64_t n = r0 + (t >> 1);            // this lane's row
     const bool valid = n < w.N;
     // the next task's index words, mask and records, into L1 while this one
-    // decodes (its stream words follow halfway through the walk)
+    // decodes (its stream words follow before the walk)
     const int64_t nxt = task + gridDim.x;
-    const int64_t nn = (nxt / w.nsr) * kVRows + 2 * warp + (t >> 1);
-    const int ncol = (int)(nxt % w.nsr);
+    const uint32_t nrt32 = (uint32_t)nxt / nsr32;
+    const int64_t nn = (int64_t)nrt32 * kVRows + 2 * warp + (t >> 1);
+    const int ncol = (int)((uint32_t)nxt - nrt32 * nsr32);
     const bool pf = nxt < ntasks && nn < w.N;
     if (pf) {
       const int64_t ngb = nn * w.nbr + CAS_SB * ncol + j;
@@ -362,6 +366,15 @@ __global__ void __launch_bounds__(kVThreads, 4) verify_gemm_block_kernel(GemmArg
       bwindow(ms_a, 128u, 0, 4, Hp, Lp);
       bwindow(st_a, 4u, q0 + 1, VerifyStreams::kRow - 3, Hc, Lc);
       uint32_t used = 0u, cor = 0u;
+      if (pf && j == 0) {  // the next task's stream words (lanes 0, 8, 16, 24), into L1
+        uint32_t a0, b0;
+        if (pruned)
+          stream_range(w.vidx, nn * w.nsr + ncol, w.lim_vexp, a0, b0);
+        else
+          stream_range(w.sidx, nn * w.nsr + ncol, w.lim_sexp, a0, b0);
+        const uint32_t* s0 = (pruned ? w.vexp : w.sexp) + a0;
+        for (uint32_t q = 0; q < b0 - a0 && q < 96u; q += 32u) prefetch_l1(s0 + q);
+      }
       uint32_t an = __ldg(ra), bn = __ldg(rb);  // the next group's record words
 #pragma unroll 1
       for (int gi = 0; gi < 8; ++gi) {
@@ -369,15 +382,6 @@ __global__ void __launch_bounds__(kVThreads, 4) verify_gemm_block_kernel(GemmArg
         if (gi < 7) {
           an = __ldg(ra + rs * (gi + 1));
           bn = __ldg(rb + rs * (gi + 1));
-        }
-        if (gi == 4 && pf && j == 0) {  // the next task's stream words (lanes 0, 8, 16, 24)
-          uint32_t a0, b0;
-          if (pruned)
-            stream_range(w.vidx, nn * w.nsr + ncol, w.lim_vexp, a0, b0);
-          else
-            stream_range(w.sidx, nn * w.nsr + ncol, w.lim_sexp, a0, b0);
-          const uint32_t* s0 = (pruned ? w.vexp : w.sexp) + a0;
-          for (uint32_t q = 0; q < b0 - a0 && q < 96u; q += 32u) prefetch_l1(s0 + q);
         }
         if (gi > 0) {
           const int cur = min((int)(ta - tb) >> 1, CAS_BLK - 1);
@@ -497,6 +501,7 @@ int launch_block(const GemmArgs& a, cudaStream_t st) {
   const int per_sm = occupancy((const void*)kern, kVThreads, smem);
   if (per_sm < 1) return CAS_ERR_CUDA;
   const int64_t ntasks = (a.w.N + kVRows - 1) / kVRows * a.w.nsr;
+  if (ntasks + (int64_t)sm_count() * per_sm >= (int64_t)1 << 32) return CAS_ERR_INVALID;  // 32-bit task indices
   const int g = (int)std::max<int64_t>(1, std::min<int64_t>(ntasks, (int64_t)sm_count() * per_sm));
   kern<<<g, kVThreads, smem, st>>>(a);
   return launch_status();

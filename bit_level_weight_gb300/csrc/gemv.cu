@@ -1081,8 +1081,8 @@ __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs
 
   for (int c = gw; c < nch; c += nwarps) {
     // row and block in the row of the chunk's first block
-    const uint32_t row0 = (uint32_t)(((int64_t)c * 32) / nbr);
-    const uint32_t jb0 = (uint32_t)((int64_t)c * 32 - (int64_t)row0 * nbr);
+    const uint32_t row0 = (uint32_t)c * 32u / (uint32_t)nbr;  // block indices fit 32 bits (launch checks)
+    const uint32_t jb0 = (uint32_t)c * 32u - row0 * (uint32_t)nbr;
     // the chunk's streams; a stream longer than the stage sends the chunk to
     // the generic decoder
     uint32_t sa[4];
@@ -1247,6 +1247,7 @@ int launch_block(const GemvArgs& a, cudaStream_t st) {
   if (max_per_sm < 1) return CAS_ERR_CUDA;
   // one full wave (chunks are dealt round-robin over the CTAs), at most a CTA per chunk
   const int64_t nch = (a.w.nsb + 3) / 4;
+  if (nch * 32 >= (int64_t)1 << 32) return CAS_ERR_INVALID;  // 32-bit block indices
   int g = (int)std::max<int64_t>(1, std::min<int64_t>(nch, (int64_t)sm_count() * max_per_sm));
   size_t smem = block_smem<NV>(a.w.nbr) + (size_t)kBWarps * block_per(a.w.nsb, g) * sizeof(int);
   const int per_sm = occupancy((const void*)kern, kBThreads, smem);
