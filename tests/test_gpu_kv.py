@@ -365,3 +365,52 @@ def test_verify_attention_multi_chunk_combine(cas, orc, variant, n, T):
     o = cas.verify_attn([kv], q.cuda())
     ref, nrm = orc.attention(np16(q[0]), np16(K), np16(V), causal_new=T)
     check_attn(o[0], ref, nrm, f"verify attention, {n} tokens in a {MULTI_CHUNK_CAP}-token cache, v={variant}")
+
+
+def _wild_tokens(n, H, seed):
+    """Tokens the calibrated tables rank badly: in a third of them 6 dims hold
+    values of 2^-20 .. 2^7 (exponents unseen in calibration, so codes of rank
+    31 and more, longer than a window), a third whose large values fill dims
+    32 .. 95 only (kept positions start after a gap of 32, pruned ones have a
+    gap of 64), the rest ordinary."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((n, H, D))
+    kind = np.arange(n) % 3
+    spread = rng.choice([-1.0, 1.0], size=(n, H, D)) * 2.0 ** rng.uniform(-20, 7, size=(n, H, D))
+    pick = np.zeros((n, H, D), dtype=bool)
+    for t in range(n):
+        for h in range(H):
+            pick[t, h, rng.choice(D, 6, replace=False)] = True
+    x = np.where((kind == 0)[:, None, None] & pick, spread, x)
+    band = np.zeros(D, dtype=bool)
+    band[32:96] = True
+    sign = rng.choice([-1.0, 1.0], size=(n, H, D))
+    banded = sign * np.where(band, rng.uniform(1.0, 2.0, size=(n, H, D)), rng.uniform(0.125, 0.25, size=(n, H, D)))
+    x = np.where((kind == 1)[:, None, None], banded, x)
+    return synthetic.to_bits(torch.from_numpy(x.astype(np.float32)))
+
+
+def test_attention_long_codes_and_gaps(cas, orc):
+    """Draft and verify attention over a cache whose tokens defeat the 64-bit
+    windows of the block walk (codes longer than a window, gaps of 32 or more
+    positions), so the per-group scans and the whole-token rescans run."""
+    H, Hq, n, T = 2, 8, 700, 5
+    K0, V0 = make_tokens(16, H, seed=500)
+    K = torch.cat([K0, _wild_tokens(n - 16, H, seed=501)])
+    V = torch.cat([V0, _wild_tokens(n - 16, H, seed=502)])
+    kv = new_cache(cas, H, n + 64, K, V, est=16.0)  # long codes: room for ~16 bits per code
+    kv.append(K[:n - T].cuda(), V[:n - T].cuda())
+    assert kv.status() == (n - T, 0)
+    q = synthetic.activations(1, Hq * D, seed=503).view(1, Hq, D)
+    tk = synthetic.activations(2, H * D, seed=504).view(1, 2, H, D)
+    tv = synthetic.activations(2, H * D, seed=505).view(1, 2, H, D)
+    o = cas.draft_attn_decode([kv], q.cuda(), tk.cuda(), tv.cuda())
+    Kall = np.concatenate([oracle_draft_kv(orc, K[:n - T], 64, 3, 1), np16(tk[0])], 0)
+    Vall = np.concatenate([oracle_draft_kv(orc, V[:n - T], 64, 3, 1), np16(tv[0])], 0)
+    ref, nrm = orc.attention(np16(q), Kall, Vall)
+    check_attn(o, ref, nrm, "draft attention, long codes and gaps")
+    kv.append(K[n - T:].cuda(), V[n - T:].cuda())
+    qv = synthetic.activations(T, Hq * D, seed=506).view(1, T, Hq, D)
+    ov = cas.verify_attn([kv], qv.cuda())
+    ref, nrm = orc.attention(np16(qv[0]), np16(K), np16(V), causal_new=T)
+    check_attn(ov[0], ref, nrm, "verify attention, long codes and gaps")
