@@ -21,9 +21,12 @@ forward through the library's C ABI:
 Headline value: draft decode+GEMV GB/s over the algorithmic bytes of the
 speculation streams read (plus x read and y written), timed with CUDA events on
 the launching stream around the draft-GEMV launches of the timed steps.
-Also reported: verify GEMM GB/s, microseconds per decode step, roofline of the
-draft GEMV against the measured HBM copy bandwidth, the end-to-end number
-through the C ABI with host buffers, and the CPU oracle as a reported baseline.
+Also reported: verify GEMM GB/s, microseconds per decode step (the whole step
+replayed as one CUDA graph), roofline of the draft GEMV against the measured
+HBM copy bandwidth, the end-to-end number through the C ABI with host buffers,
+a dense bf16 GEMV of the same shape next to the draft GEMV (the break-even of
+reading fewer bytes), the other configurations of the workload table, and the
+CPU oracle as a reported baseline.
 
 --impl reference times the CPU oracle (the plain C restatement) on the host
 cores on a bounded sample of the same workload.
@@ -622,6 +625,8 @@ def extra_configs(cas, args, dev, main_stk):
 
     import torch
     out = {}
+    if args.workload == "llama3-8b" and args.variant == 1:
+        out["dense_bf16_gemv"] = dense_vs_draft(cas, dev, main_stk)
     for kv in (main_stk.kv or []):
         del kv
     main_stk.kv = None
@@ -649,6 +654,48 @@ def extra_configs(cas, args, dev, main_stk):
         out["qwen3_step_ms"] = out["qwen3_step"]["ms_per_step"]
     out.update(attn_128k(cas, args, dev))
     return out
+
+
+def dense_vs_draft(cas, dev, stk):
+    """The break-even of the draft: a dense bf16 GEMV (cuBLAS through
+    torch.mv) of the fused gate|up shape, 28672 x 4096, against the draft
+    decode + GEMV of the same shape from the stack's encoded matrices. Both
+    rotate over matrices that together exceed L2 (2 dense, 8 encoded); CUDA
+    events, 24 calls each after 6 warm-up calls."""
+    import torch
+
+    import synthetic
+    mats = [stk.mats[i]["gateup"] for i in range(min(8, len(stk.mats)))]
+    N, K = mats[0].N, mats[0].K
+    st = torch.cuda.Stream(device=dev)
+    x = synthetic.activations(1, K, seed=71, device=dev)
+    y = torch.empty(1, N, dtype=torch.float32, device=dev)
+    draft = [cas.prepare("cas_draft_gemv", m, x, 1, y, st) for m in mats]
+    gen = torch.Generator(device=dev).manual_seed(72)
+    dense = [(torch.randn(N, K, device=dev, generator=gen) * 0.02).to(torch.bfloat16) for _ in range(2)]
+    xd = x.view(torch.bfloat16).view(K)
+
+    def timed(calls):
+        with torch.cuda.stream(st):
+            for i in range(6):
+                calls[i % len(calls)]()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            for i in range(24):
+                calls[i % len(calls)]()
+            b.record(st)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / 24
+
+    dense_us = timed([lambda W=W: torch.mv(W, xd) for W in dense])
+    draft_us = timed(draft)
+    spec = sum(m.spec_bytes() for m in mats) / len(mats)
+    del dense
+    torch.cuda.empty_cache()
+    return {"shape": f"{N} x {K}", "dense_us": round(dense_us, 2),
+            "dense_gbs": round(N * K * 2 / (dense_us * 1e-6) / 1e9, 1), "draft_us": round(draft_us, 2),
+            "draft_gbs": round((spec + K * 2 + N * 4) / (draft_us * 1e-6) / 1e9, 1),
+            "draft_speedup_over_dense": round(dense_us / draft_us, 3)}
 
 
 def attn_128k(cas, args, dev):
