@@ -7,11 +7,14 @@ with random-init Student-t(4) bf16 weights split at keep 50% / 3 mantissa bits
 (Cassandra-1), batch 1, draft length 4, and a compressed KV cache of 32K tokens
 (bf16 K/V ~ N(0,1) x LogNormal(0,0.5) channel scales), run as a data-dependent
 forward through the library's C ABI:
-  4 draft forwards : embedding of the previous token; per layer RMSNorm, draft
-                     GEMV Wqkv, RoPE into the bf16 draft tail, draft attention
-                     over the speculation KV + tail, draft GEMVs Wo, Wgate|up,
-                     Wdown with residual adds, RMSNorm and SiLU*mul between;
-                     final RMSNorm, draft LM head, argmax = the next token;
+  4 draft forwards : embedding of the previous token; per layer draft GEMV
+                     Wqkv of the RMSNorm of the residual (the norm runs in the
+                     GEMV's x staging), RoPE into the bf16 draft tail, draft
+                     attention over the speculation KV + tail, draft GEMV Wo
+                     added into the residual, draft GEMV Wgate|up of its
+                     RMSNorm, SiLU*mul, draft GEMV Wdown added into the
+                     residual; final RMSNorm + draft LM head, argmax = the
+                     next token;
   1 verify forward : the same over the exact weights for the 5 tokens (verify
                      GEMMs, online KV append of the 5 tokens, verify attention);
   then the caches are rolled back to the context (fixed schedule: acceptance
@@ -311,9 +314,15 @@ class Step:
             segs.append((kind, fns))
             self.kernels["other" if kind == "other" else kind] += sum(KERNELS_PER_CALL[w] for w in what)
 
-        def gemv(W, xin, y):
-            self.draft_bytes += W.spec_bytes() + B * W.K * 2 + B * W.N * 4
-            add("gemv", [P("cas_draft_gemv", W, xin, B, y, st)], ["gemv"])
+        def gemv_norm(W, xres, gamma, xout, y):
+            # y = D(W) bf16(rmsnorm(xres) * gamma): the norm runs in the GEMV's x staging
+            self.draft_bytes += W.spec_bytes() + B * W.K * 4 + W.K * 2 + B * W.K * 2 + B * W.N * 4
+            add("gemv", [P("cas_draft_gemv_rmsnorm", W, xres, B, gamma, eps, xout, y, st)], ["gemv"])
+
+        def gemv_acc(W, xin, y):
+            # y += D(W) xin: the residual add happens in the GEMV's atomics
+            self.draft_bytes += W.spec_bytes() + B * W.K * 2 + B * W.N * 8
+            add("gemv", [P("cas_draft_gemv_accumulate", W, xin, B, y, st)], ["gemv"])
 
         def gemm(W, Xin, Y):
             self.verify_bytes += W.all_bytes() + B * T * W.K * 2 + B * T * W.N * 4
@@ -324,9 +333,7 @@ class Step:
                           for b in range(B)], ["glue"] * B)
             for layer in range(stk.L):
                 M = stk.mats[layer]
-                add("other", [P("cas_add_rmsnorm", x, yd if layer else None, B, h, stk.g1[layer], eps, xn, st)],
-                    ["glue"])
-                gemv(M["qkv"], xn, qkv)
+                gemv_norm(M["qkv"], x, stk.g1[layer], xn, qkv)
                 fns = [P("cas_rope_split", qkv, B, Hq, Hkv, stk.ctx + d, 1, stk.theta, q, tk[0, d], D * Hkv * hd,
                          tv[0, d], D * Hkv * hd, st)]
                 what = ["glue"]
@@ -338,13 +345,11 @@ class Step:
                 fns.append(P("cas_f32_to_bf16", o, B * Hq * hd, ob, st))
                 what.append("glue")
                 add("other", fns, what)
-                gemv(M["o"], ob, yo)
-                add("other", [P("cas_add_rmsnorm", x, yo, B, h, stk.g2[layer], eps, xn, st)], ["glue"])
-                gemv(M["gateup"], xn, gu)
+                gemv_acc(M["o"], ob, x)
+                gemv_norm(M["gateup"], x, stk.g2[layer], xn, gu)
                 add("other", [P("cas_silu_mul", gu, B, F, hh, st)], ["glue"])
-                gemv(M["down"], hh, yd)
-            add("other", [P("cas_add_rmsnorm", x, yd, B, h, stk.gf, eps, xn, st)], ["glue"])
-            gemv(stk.lm, xn, lg)
+                gemv_acc(M["down"], hh, x)
+            gemv_norm(stk.lm, x, stk.gf, xn, lg)
             add("other", [P("cas_argmax", lg[b:b + 1], 1, V, self.vtok[b * T + 1 + d:b * T + 2 + d], st)
                           for b in range(B)], ["glue"] * B)
         # verify forward of the T tokens of every sequence

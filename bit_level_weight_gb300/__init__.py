@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
             "cas_encode_weights": ([P, P, P, u64, P, u64, P], i32),
             "cas_choose_variant": ([P, i64, i64, i32, i32, P, u64, P, P, P], i32),
             "cas_draft_gemv": ([P, P, i32, P, P], i32),
+            "cas_draft_gemv_accumulate": ([P, P, i32, P, P], i32),
+            "cas_draft_gemv_rmsnorm": ([P, P, i32, P, ctypes.c_float, P, P, P], i32),
             "cas_verify_gemm": ([P, P, i32, P, P], i32),
             "cas_decode_draft": ([P, P, P], i32),
             "cas_reconstruct": ([P, P, P], i32),
@@ -251,6 +253,36 @@ def cas_draft_gemv(W: EncodedWeights, x: torch.Tensor, y: torch.Tensor, stream=N
     _out(y, nvec * W.N, (torch.float32,), "y")
     _check(lib().cas_draft_gemv(ctypes.byref(W.desc), _ptr(x), nvec, _ptr(y), _stream(stream)), "cas_draft_gemv")
     return y
+
+
+def cas_draft_gemv_accumulate(W: EncodedWeights, x: torch.Tensor, y: torch.Tensor, stream=None):
+    """y += D(W) x (y not cleared)."""
+    x = _bits(x)
+    nvec = 1 if x.dim() == 1 else x.shape[0]
+    _shape(x, (W.K,) if x.dim() == 1 else (nvec, W.K), "x")
+    _out(y, nvec * W.N, (torch.float32,), "y")
+    _check(lib().cas_draft_gemv_accumulate(ctypes.byref(W.desc), _ptr(x), nvec, _ptr(y), _stream(stream)),
+           "cas_draft_gemv_accumulate")
+    return y
+
+
+def draft_gemv_rmsnorm(W: EncodedWeights, x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-5,
+                       xn: torch.Tensor | None = None, y: torch.Tensor | None = None, stream=None):
+    """xn = bf16 rmsnorm(x) * gamma, y = D(W) xn; x: fp32 [nvec][K]. Returns (xn, y)."""
+    if x.dtype != torch.float32 or x.dim() != 2 or x.shape[1] != W.K:
+        raise ValueError("draft_gemv_rmsnorm: x must be fp32 [nvec][K]")
+    nvec = x.shape[0]
+    gamma = _bits(gamma)
+    _shape(gamma, (W.K,), "gamma")
+    if xn is None:
+        xn = torch.empty(nvec, W.K, dtype=torch.int16, device=x.device)
+    if y is None:
+        y = torch.empty(nvec, W.N, dtype=torch.float32, device=x.device)
+    _out(xn, nvec * W.K, (torch.int16, torch.bfloat16), "xn")
+    _out(y, nvec * W.N, (torch.float32,), "y")
+    _check(lib().cas_draft_gemv_rmsnorm(ctypes.byref(W.desc), _ptr(x), nvec, _ptr(gamma), float(eps), _ptr(xn),
+                                        _ptr(y), _stream(stream)), "cas_draft_gemv_rmsnorm")
+    return xn, y
 
 
 def cas_verify_gemm(W: EncodedWeights, X: torch.Tensor, Y: torch.Tensor, stream=None):

@@ -26,6 +26,7 @@
 // position), one over the unary stream (code end; rank = distance from the
 // previous end). The rank table gives exponent << 23, OR-ed with the sign and
 // mantissa field into an fp32 value multiplied with x.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -49,6 +50,12 @@ struct GemvArgs {
   const uint16_t* x;
   float* y;
   int sexp_words;  // words of the unary exponent section (read bound)
+  // RMSNorm of an fp32 input in the x staging (lane-per-block kernel only):
+  // x = bf16(xf / sqrt(mean(xf^2) + eps) * gamma), also written to xn by CTA 0
+  const float* xf = nullptr;
+  const uint16_t* gamma = nullptr;
+  uint16_t* xn = nullptr;
+  float eps = 0.f;
 };
 
 // Set when a bounded wait on the x staging copy gave up (read by
@@ -1033,7 +1040,32 @@ __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs
   BlockStage& bs = reinterpret_cast<BlockStage*>(smem + (size_t)NV * xfl * 4 + kBXPad)[warp];
 
   // x -> fp32, position p of vector v at v*xfl + (p/128)*129 + p%128
-  for (int v = 0; v < NV; ++v) {
+  if (a.xf) {  // the input is fp32: RMSNorm first, rounded to bf16 like the unfused glue
+    __shared__ float red[kBWarps];
+    for (int v = 0; v < NV; ++v) {
+      const float* xr = a.xf + (size_t)v * K;
+      float ss = 0.f;
+      for (int i = threadIdx.x; i < K; i += kBThreads) {
+        const float s = __ldg(xr + i);
+        xs[v * xfl + (i >> 7) * kBXRow + (i & 127)] = s;
+        ss = fmaf(s, s, ss);
+      }
+      ss = warp_sumf(ss);
+      if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+      __syncthreads();
+      float tot = (threadIdx.x & 31) < kBWarps ? red[threadIdx.x & 31] : 0.f;
+      tot = warp_sumf(tot);
+      const float inv = rsqrtf(tot / (float)K + a.eps);
+      for (int i = threadIdx.x; i < K; i += kBThreads) {
+        float* d = xs + v * xfl + (i >> 7) * kBXRow + (i & 127);
+        const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(*d * inv * bf2f(__ldg(a.gamma + i))));
+        *d = bf2f(b);
+        if (blockIdx.x == 0) a.xn[(size_t)v * K + i] = (uint16_t)b;
+      }
+      __syncthreads();
+    }
+  }
+  for (int v = 0; v < NV && !a.xf; ++v) {
     const uint4* xv = reinterpret_cast<const uint4*>(a.x + (size_t)v * K);
     for (int i = threadIdx.x; i < K / 8; i += kBThreads) {
       const uint4 pr = __ldg(xv + i);
@@ -1284,13 +1316,21 @@ int launch_word(const GemvArgs& a, cudaStream_t st) {
 // The fast path covers Cassandra-1 with k = 64, m = 3 and rows that are whole
 // superblocks (K % 1024 == 0): every lane then owns exactly 16 ordinals that
 // sit in one 64-bit slice of one block record.
+// Whether the lane-per-block kernel takes a call (it alone stages an fp32
+// input through RMSNorm).
+template <int VAR>
+bool block_path(const GemvArgs& a, int nvec) {
+  return VAR == 1 && nvec <= 2 && a.w.m == 3 && (a.w.k == 64 || a.w.k == 38) && a.w.nbr % CAS_SB == 0 &&
+         a.w.nbr >= 32 && block_smem<2>(a.w.nbr) <= 200 * 1024;
+}
+
 template <int VAR>
 int dispatch(const GemvArgs& a, int nvec, cudaStream_t st) {
   const bool fast = a.w.k == 64 && a.w.m == 3 && a.w.nbr % CAS_SB == 0;
-  const bool block = VAR == 1 && nvec <= 2 && a.w.m == 3 && a.w.nbr % CAS_SB == 0 && a.w.nbr >= 32 &&
-                     block_smem<2>(a.w.nbr) <= 200 * 1024;
-  if (block && a.w.k == 64) return nvec == 1 ? launch_block<1, 64>(a, st) : launch_block<2, 64>(a, st);
-  if (block && a.w.k == 38) return nvec == 1 ? launch_block<1, 38>(a, st) : launch_block<2, 38>(a, st);
+  if (block_path<VAR>(a, nvec)) {
+    if (a.w.k == 64) return nvec == 1 ? launch_block<1, 64>(a, st) : launch_block<2, 64>(a, st);
+    return nvec == 1 ? launch_block<1, 38>(a, st) : launch_block<2, 38>(a, st);
+  }
   if (fast && VAR == 1 && nvec <= 2 && word_smem<2>(a.w.K) <= 200 * 1024)
     return nvec == 1 ? launch_word<1>(a, st) : launch_word<2>(a, st);
   if (fast && VAR == 1) {
@@ -1353,15 +1393,23 @@ int gemv_wait_status(bool clear) {
 
 using namespace cas;
 
-extern "C" int cas_draft_gemv(const cas_weights* W, const uint16_t* x, int nvec, float* y, void* stream) {
+namespace cas {
+namespace {
+
+// y (+)= D(W) x; with xf, x = bf16(rmsnorm(xf) * gamma) written to xn first.
+int draft_gemv_call(const cas_weights* W, const uint16_t* x, const float* xf, const uint16_t* gamma, float eps,
+                    uint16_t* xn, int nvec, float* y, bool accumulate, cudaStream_t st) {
   int s = check_weights(W);
   if (s) return s;
   if (nvec < 1 || nvec > kMaxVec) return CAS_ERR_INVALID;
   if ((int64_t)nvec * W->K * 2 > 200 * 1024) return CAS_ERR_INVALID;  // x must fit in shared memory
-  if (W->N == 0) return CAS_OK;  // nothing to write (y may be an empty tensor)
-  if (!x || !y || !aligned16(x) || !aligned16(y)) return CAS_ERR_INVALID;
-  cudaStream_t st = (cudaStream_t)stream;
-  if (cudaMemsetAsync(y, 0, sizeof(float) * nvec * W->N, st) != cudaSuccess) return CAS_ERR_CUDA;
+  if (xf && (!gamma || !xn || !aligned16(xf) || !aligned16(xn) || !(eps >= 0.f) || W->K < 1 || W->K > 16384))
+    return CAS_ERR_INVALID;
+  if (!xf && (!x || !aligned16(x))) return CAS_ERR_INVALID;
+  if (W->N == 0 && !xf) return CAS_OK;  // nothing to write (y may be an empty tensor)
+  if (W->N > 0 && (!y || !aligned16(y))) return CAS_ERR_INVALID;
+  if (!accumulate && W->N > 0 && cudaMemsetAsync(y, 0, sizeof(float) * nvec * W->N, st) != cudaSuccess)
+    return CAS_ERR_CUDA;
   if (W->K == 0) return CAS_OK;
   // superblock indices stay 32-bit, with room for the grid stride
   if (W->N * ((W->K / CAS_BLK + CAS_SB - 1) / CAS_SB) >= (1ll << 30)) return CAS_ERR_INVALID;
@@ -1371,5 +1419,35 @@ extern "C" int cas_draft_gemv(const cas_weights* W, const uint16_t* x, int nvec,
   a.x = x;
   a.y = y;
   a.sexp_words = (int)(W->len[CAS_SEC_SPEC_EXP] / 4);
+  if (xf) {
+    const bool fused = W->N > 0 && (W->p.variant == 1 ? block_path<1>(a, nvec) : block_path<2>(a, nvec));
+    if (!fused) {  // the normalised input first (the glue kernel), then the plain GEMV
+      s = cas_add_rmsnorm(const_cast<float*>(xf), nullptr, nvec, (int)W->K, gamma, eps, xn, st);
+      if (s || W->N == 0) return s;
+      a.x = xn;
+    } else {
+      a.xf = xf;
+      a.gamma = gamma;
+      a.xn = xn;
+      a.eps = eps;
+    }
+  }
   return W->p.variant == 1 ? dispatch<1>(a, nvec, st) : dispatch<2>(a, nvec, st);
+}
+
+}  // namespace
+}  // namespace cas
+
+extern "C" int cas_draft_gemv(const cas_weights* W, const uint16_t* x, int nvec, float* y, void* stream) {
+  return draft_gemv_call(W, x, nullptr, nullptr, 0.f, nullptr, nvec, y, false, (cudaStream_t)stream);
+}
+
+extern "C" int cas_draft_gemv_accumulate(const cas_weights* W, const uint16_t* x, int nvec, float* y, void* stream) {
+  return draft_gemv_call(W, x, nullptr, nullptr, 0.f, nullptr, nvec, y, true, (cudaStream_t)stream);
+}
+
+extern "C" int cas_draft_gemv_rmsnorm(const cas_weights* W, const float* x, int nvec, const uint16_t* gamma, float eps,
+                                      uint16_t* xn, float* y, void* stream) {
+  if (!x) return CAS_ERR_INVALID;
+  return draft_gemv_call(W, nullptr, x, gamma, eps, xn, nvec, y, false, (cudaStream_t)stream);
 }

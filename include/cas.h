@@ -168,6 +168,24 @@ int cas_choose_variant(const uint16_t* W, int64_t N, int64_t K, int keep_per_blo
  * superblocks or more; CAS_ERR_CUDA on a launch error. N = 0 writes nothing. */
 int cas_draft_gemv(const cas_weights* W, const uint16_t* x, int nvec, float* y, void* stream);
 
+/* Draft GEMV that adds into y: y[v][n] += sum_k D(W)[n][k] * x[v][k], y not
+ * cleared (a residual stream can be y). Same arguments and errors as
+ * cas_draft_gemv. */
+int cas_draft_gemv_accumulate(const cas_weights* W, const uint16_t* x, int nvec, float* y, void* stream);
+
+/* Draft GEMV of a normalised input [B3.1]: xn[v] = bf16(x[v] / sqrt(mean(x[v]^2)
+ * + eps) * gamma) (RMSNorm, as cas_add_rmsnorm without the add; the mean of
+ * squares is reduced in an unspecified order) and y[v][n] = sum_k
+ * D(W)[n][k] * xn[v][k], overwriting y. x: fp32 [nvec][K], 16-byte aligned,
+ * not written; gamma: bf16 [K]; xn: bf16 [nvec][K] out, 16-byte aligned,
+ * written by the call (the normalisation runs inside the GEMV's staging of
+ * x where the lane-per-block kernel takes the tensor, else as a separate
+ * kernel first). Errors: those of cas_draft_gemv; CAS_ERR_INVALID if x,
+ * gamma or xn is null or misaligned, eps is negative or NaN, or K exceeds
+ * 16384. N = 0 still writes xn. */
+int cas_draft_gemv_rmsnorm(const cas_weights* W, const float* x, int nvec, const uint16_t* gamma, float eps,
+                           uint16_t* xn, float* y, void* stream);
+
 /* Verify GEMM [B3.1]: Y[t][n] = sum_k W[n][k] * X[t][k] for t < T (1..16)
  * with W rebuilt bit-exactly from both streams, on tensor cores with fp32
  * accumulation. X: bf16 [T][K]; Y: fp32 [T][N], overwritten. Errors: those

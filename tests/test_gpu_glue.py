@@ -81,3 +81,28 @@ def test_embed_exact(cas):
     tok = torch.tensor([0, 999, 17, 17], dtype=torch.int32)
     x = cas.embed(tok.cuda(), table.cuda()).double().cpu().numpy()
     assert np.array_equal(x, glue.embed(tok.numpy(), table.numpy().view(np.uint16)))
+
+
+@pytest.mark.parametrize("keep", [64, 38])
+@pytest.mark.parametrize("N,K,nvec", [(40, 4096, 1), (24, 14336, 2), (20, 1152, 1), (33, 4096, 2)])
+def test_draft_gemv_rmsnorm_and_accumulate(cas, N, K, nvec, keep):
+    """The draft GEMV of a normalised fp32 input (RMSNorm in the GEMV's x
+    staging where the lane-per-block kernel takes the tensor, K = 4096 and
+    14336; a separate normalisation for K = 1152) against the float64
+    statements, and the accumulating GEMV (y += D(W) x) on top of a given y."""
+    import oracle
+    g = torch.Generator().manual_seed(N + K + nvec + keep)
+    W = synthetic.t4_weight(N, K, seed=N + K)
+    enc = cas.encode_weights(W.cuda(), 1, keep, 3)
+    Wd = oracle.draft_values(W.numpy().view(np.uint16), 1, keep, 3)
+    x = torch.randn(nvec, K, generator=g) * 2.0
+    gamma = synthetic.to_bits(1.0 + 0.1 * torch.randn(K, generator=g))
+    xn, y = cas.draft_gemv_rmsnorm(enc, x.cuda(), gamma.cuda(), 1e-5)
+    ref_xn = glue.rmsnorm(x.double().numpy(), gamma.numpy().view(np.uint16), 1e-5)
+    got_xn = f64(xn)
+    assert (np.abs(got_xn - ref_xn) <= 2.0 ** -8 * np.abs(ref_xn) + 1e-6).all()
+    ref, nrm = oracle.matvec(Wd, xn.cpu().numpy().view(np.uint16))  # y against the xn the call wrote
+    assert (np.abs(y.double().cpu().numpy() - ref) <= 2e-3 * nrm + 1e-30).all()
+    y0 = torch.randn(nvec, N, generator=g)
+    ya = cas.cas_draft_gemv_accumulate(enc, xn, y0.clone().cuda())
+    assert (np.abs(ya.double().cpu().numpy() - (y0.double().numpy() + ref)) <= 2e-3 * nrm + 1e-5).all()
