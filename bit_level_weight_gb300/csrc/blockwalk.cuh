@@ -41,6 +41,13 @@ __device__ __forceinline__ uint32_t fenced(uint32_t a) {
   return r;
 }
 __device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
+// A read-only load whose bytes no other load reads (a warp's whole masks): not
+// kept in L1, which then holds the data that is read again.
+__device__ __forceinline__ uint4 ldg_once(const uint4* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
 // Stores the low 16 bits of v (the instruction truncates the 32-bit register).
 __device__ __forceinline__ void sts_u16(uint32_t a, uint32_t v) { asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "r"(v)); }
 

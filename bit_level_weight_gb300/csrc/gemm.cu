@@ -215,18 +215,41 @@ int launch(const GemmArgs& a, cudaStream_t st) {
 // value is its byte of the pruned record; both are laid out as even and odd
 // bytes per group of 8, so the per-value code is the same for both kinds. Each
 // bf16 goes to its position in the tile. When a lane meets a step of 32 or more
-// (a long gap or code), the stores of its failed walk may land up to 782
-// bytes past its block's start - in the warp's own rows, the next warp's first
-// row, or the slack after the tile - so that warp and the next one rebuild
+// (a long gap or code), the stores of its failed walk may land up to 655
+// positions past its block's start (position 127 at a re-alignment, then 16
+// steps of at most 33) - in the warp's own rows, the next warp's first row, or
+// the slack after the tile - so that warp and the next one rebuild
 // their rows by scanning the staged words instead; streams longer than the
 // stage go to the generic decoder. Then the product runs as in
 // verify_gemm_kernel.
 constexpr int kVThreads = 256;
 constexpr int kVWarps = kVThreads / 32;
 constexpr int kVRows = 2 * kVWarps;
-constexpr int kVPad = 512;                                  // bytes of slack after the tile
-constexpr int kVTile = kVRows * kTileStride + kVPad / 2;     // elements
-__device__ __forceinline__ int vrow(int r) { return r * kTileStride; }
+// Tile layout (bf16 elements): block j of row r at vrow(r) + 132 j. In 4-byte
+// banks a block is 66 words (2 banks on) and a row 528 words plus 4 after
+// every odd row, so the 16 blocks a warp writes (rows 2w and 2w + 1) start on
+// 16 different even banks, and rows 0..7 start on 8 different multiples of 4
+// (conflict-free A-fragment loads). The scattered 16-bit stores of the walk
+// then meet each other on a bank only when two lanes' positions drift apart.
+constexpr int kVBlk = CAS_BLK + 4;
+constexpr int kVRowLen = kVBlk * CAS_SB;
+__host__ __device__ constexpr int vrow(int r) { return r * kVRowLen + 8 * (r >> 1); }
+// slack after the tile (bytes): a failed walk stores up to position
+// 7 * 132 + 655 of the last row
+constexpr int kVPad = ((vrow(kVRows - 1) + 7 * kVBlk + 656 - vrow(kVRows)) * 2 + 127) / 128 * 128;
+constexpr int kVTile = vrow(kVRows) + kVPad / 2;  // elements
+static_assert(vrow(kVRows - 1) + 7 * kVBlk + 656 <= kVTile, "slack covers a failed walk of the last row");
+static_assert(7 * kVBlk + 656 - kVRowLen <= kVRowLen, "a failed walk stays within the next row");
+// The tile's k-step ks (16 columns) and A fragment (mma m16n8k16, row-major):
+// rows g, g + 8 and columns 2 tq (+ 8) of the step, one 32-bit load each.
+__device__ __forceinline__ void vtile_afrag(uint32_t a[4], uint32_t tile_a, int ks, int g, int tq) {
+  const uint32_t c = 2u * (uint32_t)(kVBlk * (ks >> 3) + 16 * (ks & 7) + 2 * tq);
+  const uint32_t r0 = tile_a + 2u * (uint32_t)vrow(g) + c, r1 = tile_a + 2u * (uint32_t)vrow(g + 8) + c;
+  a[0] = lds_u32(r0);
+  a[1] = lds_u32(r1);
+  a[2] = lds_u32(r0 + 16u);
+  a[3] = lds_u32(r1 + 16u);
+}
 
 using VerifyStreams = BlockStreams<3, 80>;
 struct VerifyStage {
@@ -307,48 +330,35 @@ __global__ void __launch_bounds__(kVThreads, 4) verify_gemm_block_kernel(GemmArg
     const int64_t r0 = rt * kVRows + 2 * warp;  // the warp's first row
     const int64_t n = r0 + (t >> 1);            // this lane's row
     const bool valid = n < w.N;
-    // the next task's index words, mask and records, into L1 while this one
-    // decodes (its stream words follow before the walk)
-    const int64_t nxt = task + gridDim.x;
-    const uint32_t nrt32 = (uint32_t)nxt / nsr32;
-    const int64_t nn = (int64_t)nrt32 * kVRows + 2 * warp + (t >> 1);
-    const int ncol = (int)((uint32_t)nxt - nrt32 * nsr32);
-    const bool pf = nxt < ntasks && nn < w.N;
-    if (pf) {
-      const int64_t ngb = nn * w.nbr + CAS_SB * ncol + j;
-      prefetch_l1(w.mask + ngb * 4);
-      prefetch_l1(pruned ? w.vpr + ngb * 16 : w.ssm + ngb * 8);
-      prefetch_l1(pruned ? w.vpr + ngb * 16 + 8 : w.vlo + ngb * 8);
-      if (j == 0) prefetch_l1((pruned ? w.vidx : w.sidx) + nn * w.nsr + ncol);
-    }
     // 1) rebuild rows r0, r0 + 1 of the tile (the stage's zero words first: the
     // previous task's partials and the generic decoder write over them)
     verify_stage_init(vs, lane);
+    // stream u (row r0 + u / 2, kept codes for even u, pruned for odd) is
+    // located by lane u
+    uint32_t ua = 0u, ub = 0u;
+    if (lane < 4 && r0 + (lane >> 1) < w.N) {
+      const int64_t s = (r0 + (lane >> 1)) * w.nsr + col;
+      if (lane & 1)
+        stream_range(w.vidx, s, w.lim_vexp, ua, ub);
+      else
+        stream_range(w.sidx, s, w.lim_sexp, ua, ub);
+    }
+    const int present = r0 + 1 < w.N ? 4 : (r0 < w.N ? 2 : 0);
     const uint32_t* gs[4];
     int nw[4];
-    int present = 0;
     bool fast = true;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      uint32_t a0 = 0u, b0 = 0u;
-      const int64_t ru = r0 + (u >> 1);
-      if (ru < w.N) {
-        const int64_t s = ru * w.nsr + col;
-        if (u & 1)
-          stream_range(w.vidx, s, w.lim_vexp, a0, b0);
-        else
-          stream_range(w.sidx, s, w.lim_sexp, a0, b0);
-        present = u + 1;
-      }
+      const uint32_t a0 = __shfl_sync(CAS_FULL, ua, u);
+      nw[u] = (int)__shfl_sync(CAS_FULL, ub - ua, u);
       gs[u] = ((u & 1) ? w.vexp : w.sexp) + a0;
-      nw[u] = (int)(b0 - a0);
       fast = fast && nw[u] <= VerifyStreams::kWords;
     }
     const int64_t gb = (valid ? n : r0) * w.nbr + CAS_SB * col + j;  // this lane's block
-    const uint32_t tb = tile_a + 2u * (uint32_t)(vrow(2 * warp + (t >> 1)) + kBlkStride * j);
+    const uint32_t tb = tile_a + 2u * (uint32_t)(vrow(2 * warp + (t >> 1)) + kVBlk * j);
     int q0s = 0;
     if (fast) {
-      const uint4 mk = __ldg(reinterpret_cast<const uint4*>(w.mask) + gb);
+      const uint4 mk = ldg_once(reinterpret_cast<const uint4*>(w.mask) + gb);
       // the lane's records: kept, spec_sm and ver_lo words (one each per group
       // of 8); pruned, ver_pr words (two per group)
       const uint32_t* ra = pruned ? w.vpr + gb * 16 : w.ssm + gb * 8;
@@ -366,27 +376,26 @@ __global__ void __launch_bounds__(kVThreads, 4) verify_gemm_block_kernel(GemmArg
       bwindow(ms_a, 128u, 0, 4, Hp, Lp);
       bwindow(st_a, 4u, q0 + 1, VerifyStreams::kRow - 3, Hc, Lc);
       uint32_t used = 0u, cor = 0u;
-      if (pf && j == 0) {  // the next task's stream words (lanes 0, 8, 16, 24), into L1
-        uint32_t a0, b0;
-        if (pruned)
-          stream_range(w.vidx, nn * w.nsr + ncol, w.lim_vexp, a0, b0);
-        else
-          stream_range(w.sidx, nn * w.nsr + ncol, w.lim_sexp, a0, b0);
-        const uint32_t* s0 = (pruned ? w.vexp : w.sexp) + a0;
-        for (uint32_t q = 0; q < b0 - a0 && q < 96u; q += 32u) prefetch_l1(s0 + q);
-      }
       uint32_t an = __ldg(ra), bn = __ldg(rb);  // the next group's record words
 #pragma unroll 1
       for (int gi = 0; gi < 8; ++gi) {
         const uint32_t aw = an, bw = bn;
         if (gi < 7) {
-          an = __ldg(ra + rs * (gi + 1));
-          bn = __ldg(rb + rs * (gi + 1));
+          ra += rs;
+          rb += rs;
+          an = __ldg(ra);
+          bn = __ldg(rb);
         }
         if (gi > 0) {
-          const int cur = min((int)(ta - tb) >> 1, CAS_BLK - 1);
-          ta = tb + 2u * (uint32_t)cur;
-          bwindow(ms_a, 128u, cur + 1, 4, Hp, Lp);  // rows <= 6 since cur <= 127
+          // the position window is re-aligned every 16 values (16 of the
+          // block's 64 positions almost never span more than its 64 bits, and
+          // a window that runs dry is caught like a long gap), the code window
+          // every 8
+          if ((gi & 1) == 0) {
+            const int cur = min((int)(ta - tb) >> 1, CAS_BLK - 1);
+            ta = tb + 2u * (uint32_t)cur;
+            bwindow(ms_a, 128u, cur + 1, 4, Hp, Lp);  // rows <= 6 since cur <= 127
+          }
           bwindow(st_a, 4u, q0 + 1 + (int)used, VerifyStreams::kRow - 3, Hc, Lc);
         }
         // bytes [s f6 .. f0] of the group's values 0, 2, 4, 6 (ev) and 1, 3, 5, 7 (od)
@@ -431,30 +440,27 @@ __global__ void __launch_bounds__(kVThreads, 4) verify_gemm_block_kernel(GemmArg
         const SbInfo in = sb_prepare<1, true>(w, (r0 + u) * w.nsr + col, lut8, sc, lane);
         uint32_t v[16];
         sb_rebuild_word<1, true>(w, in, sc, lane, v);
-        uint4* dst = reinterpret_cast<uint4*>(tile + vrow(2 * warp + u) + kBlkStride * (lane >> 2) + 32 * (lane & 3));
-        dst[0] = make_uint4(v[0], v[1], v[2], v[3]);
-        dst[1] = make_uint4(v[4], v[5], v[6], v[7]);
-        dst[2] = make_uint4(v[8], v[9], v[10], v[11]);
-        dst[3] = make_uint4(v[12], v[13], v[14], v[15]);
+        uint2* dst = reinterpret_cast<uint2*>(tile + vrow(2 * warp + u) + kVBlk * (lane >> 2) + 32 * (lane & 3));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = make_uint2(v[2 * i], v[2 * i + 1]);
         __syncwarp();
       }
     }
-    // 2) tensor-core product of the tile with X[:, tile columns]
+    // 2) tensor-core product of the tile with X[:, tile columns]. The lane's
+    // B fragment words of k-step warp + 8 i: token gq (+ 8), columns
+    // 1024 col + 16 (warp + 8 i) + 2 tq (+ 8), as words of bf16 pairs (K is
+    // a multiple of 1024 here).
     const int gq = lane >> 2, tq = lane & 3;
     constexpr int kKs = CAS_BLK * CAS_SB / 16 / kVWarps;
     uint32_t xb[kKs][NT][2];
 #pragma unroll
-    for (int i = 0; i < kKs; ++i) {
-      const int ks = warp + kVWarps * i;
-      const int c = CAS_BLK * CAS_SB * col + ks * 16 + 2 * tq;
+    for (int q = 0; q < NT; ++q) {
+      const int tok = q * 8 + gq;
+      const uint32_t* xq = X32 + (size_t)min(tok, T - 1) * (size_t)(K / 2) + 512 * col + 8 * warp + tq;
 #pragma unroll
-      for (int q = 0; q < NT; ++q) {
-        const int tok = q * 8 + gq;
-        xb[i][q][0] = xb[i][q][1] = 0u;
-        if (tok < T) {
-          xb[i][q][0] = __ldg(X32 + ((int64_t)tok * K + c) / 2);
-          xb[i][q][1] = __ldg(X32 + ((int64_t)tok * K + c + 8) / 2);
-        }
+      for (int i = 0; i < kKs; ++i) {
+        xb[i][q][0] = tok < T ? __ldg(xq + 64 * i) : 0u;
+        xb[i][q][1] = tok < T ? __ldg(xq + 64 * i + 4) : 0u;
       }
     }
     __syncthreads();
@@ -465,7 +471,7 @@ __global__ void __launch_bounds__(kVThreads, 4) verify_gemm_block_kernel(GemmArg
     for (int i = 0; i < kKs; ++i) {
       const int ks = warp + kVWarps * i;
       uint32_t af[4];
-      ldmatrix_x4(af, tile + vrow(lane & 15) + tile_col(ks) + (lane >> 4) * 8);
+      vtile_afrag(af, fenced(tile_a), ks, gq, tq);
 #pragma unroll
       for (int q = 0; q < NT; ++q) mma_bf16(acc[q], af, xb[i][q][0], xb[i][q][1]);
     }

@@ -958,7 +958,9 @@ inline int word_per(int64_t nsb, int g) { return (int)((nsb + (int64_t)g * kWarp
 // bit-reversed mask words in shared memory; each lane finds where its block's
 // codes start (the bit after the (k j)-th '1' of its superblock's stream, j
 // the block's place in it) by a warp popcount scan and a shuffle search, and
-// then walks two cursors of its own, re-aligned every 8 values:
+// then walks two cursors of its own (the exponent cursor re-aligned from
+// shared memory every 8 values, the position cursor every 16 for k = 64, 8
+// for k = 38):
 //   position: a 64-bit window of the bit-reversed mask starting just after the
 //             last found position; one more than its count of leading zeros
 //             is the distance n to the next kept position, and the window
@@ -977,7 +979,9 @@ inline int word_per(int64_t nsb, int g) { return (int)((nsb + (int64_t)g * kWarp
 constexpr int kBThreads = 512;
 constexpr int kBWarps = kBThreads / 32;
 constexpr int kBXRow = CAS_BLK + 1;   // staged floats per block
-constexpr int kBXPad = 2048;          // bytes after x: reads of a failed walk stay inside
+// bytes after x: the reads of a failed walk (up to position 127 + 16 * 33 of
+// the last block) stay inside
+constexpr int kBXPad = 2304;
 constexpr int kBMaskRows = 8;         // zero row, 4 mask words, 3 zero rows
 
 constexpr int kBStreamWords = BlockStreams<2>::kRow;
@@ -1028,6 +1032,10 @@ template <int NV, int KEEP>
 __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs a) {
   constexpr int kRec = (KEEP * 4 + 31) / 32;  // sign/mantissa record words per block
   constexpr int kGroups = (KEEP + 7) / 8;
+  // groups of 8 values per re-alignment of the position window: 16 of 64
+  // positions in 128 almost never span more than its 64 bits (a window that
+  // runs dry is caught like a long gap); 16 of 38 often would
+  constexpr int kPosGroups = KEEP == 64 ? 2 : 1;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint32_t lut32[256];  // exponent << 23 by rank
   __shared__ uint8_t lut8[256];    // exponent by rank (generic decoder)
@@ -1135,7 +1143,7 @@ __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs
     const bool valid = (int64_t)c * 4 + t < nsb;
     const int64_t gl = valid ? g : (int64_t)c * 32;
     if (fast) {
-      const uint4 mk = __ldg(reinterpret_cast<const uint4*>(w.mask) + gl);
+      const uint4 mk = ldg_once(reinterpret_cast<const uint4*>(w.mask) + gl);
       uint32_t fw[kRec];
       if (KEEP == 64) {
         const uint4 fA = __ldg(reinterpret_cast<const uint4*>(w.ssm + gl * 8));
@@ -1180,9 +1188,11 @@ __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs
 #pragma unroll
       for (int gi = 0; gi < kGroups; ++gi) {
         if (gi > 0) {
-          const int cur = min((int)(xa - xbase) >> 2, CAS_BLK - 1);
-          xa = xbase + 4u * (uint32_t)cur;
-          bwindow(ms_a, 128u, 33 + cur, kBMaskRows - 3, Hp, Lp);  // rows <= 7 since cur <= 127
+          if (gi % kPosGroups == 0) {
+            const int cur = min((int)(xa - xbase) >> 2, CAS_BLK - 1);
+            xa = xbase + 4u * (uint32_t)cur;
+            bwindow(ms_a, 128u, 33 + cur, kBMaskRows - 3, Hp, Lp);  // rows <= 7 since cur <= 127
+          }
           bwindow(st_a, 4u, cq0 + 1 + (int)used, kBStreamWords - 3, Hc, Lc);
         }
         const uint32_t fo = lds_u32(fs_a + 128u * gi), fe = fo << 4;
