@@ -394,20 +394,26 @@ class Step:
 
     def capture(self):
         """The whole step as one CUDA graph (how it runs), and one graph per
-        segment (so the matrix products can be timed on their own)."""
+        segment (so the matrix products can be timed on their own), captured
+        with launch overlap on: the step holds only libcas calls, so each
+        kernel may launch while the one before it drains."""
         import torch
-        self.full = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(self.full, stream=self.st):
-            for _, fns in self.segs:
-                for f in fns:
-                    f()
-        self.graphs = []
-        for kind, fns in self.segs:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=self.st):
-                for f in fns:
-                    f()
-            self.graphs.append((kind, g))
+        self.cas.set_launch_overlap(True)
+        try:
+            self.full = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.full, stream=self.st):
+                for _, fns in self.segs:
+                    for f in fns:
+                        f()
+            self.graphs = []
+            for kind, fns in self.segs:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=self.st):
+                    for f in fns:
+                        f()
+                self.graphs.append((kind, g))
+        finally:
+            self.cas.set_launch_overlap(False)
 
     def replay(self, ev=None):
         """One step from the graphs; with `ev`, events around every matrix-product segment."""

@@ -94,6 +94,7 @@ def lib() -> ctypes.CDLL:
             "cas_verify_attn": ([P, i32, P, i32, i32, P, P, u64, P], i32),
             "cas_device_status": ([P], i32),
             "cas_test_first_wait_spins": ([ctypes.c_uint32], i32),
+            "cas_set_launch_overlap": ([i32], i32),
             "cas_add_rmsnorm": ([P, P, i32, i32, P, ctypes.c_float, P, P], i32),
             "cas_rope_split": ([P, i32, i32, i32, i64, i32, ctypes.c_double, P, P, i64, P, i64, P], i32),
             "cas_silu_mul": ([P, i32, i32, P, P], i32),
@@ -326,6 +327,14 @@ def decode_draft(W: EncodedWeights) -> torch.Tensor:
 def reconstruct(W: EncodedWeights) -> torch.Tensor:
     out = torch.empty(W.N, W.K, dtype=torch.int16, device=W.buf.device)
     return cas_reconstruct(W, out)
+
+
+def set_launch_overlap(on: bool) -> None:
+    """Launch later kernels with programmatic stream serialization (see
+    cas_set_launch_overlap): back-to-back libcas kernels overlap their launch
+    with the previous kernel's tail. The caller must not enqueue its own copy
+    or memset directly before a libcas call while this is on."""
+    _check(lib().cas_set_launch_overlap(1 if on else 0), "cas_set_launch_overlap")
 
 
 def cas_device_status(stream=None) -> int:

@@ -3,6 +3,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <atomic>
 #include <mutex>
 #include <unordered_map>
 
@@ -32,11 +33,17 @@ extern "C" int32_t cas_keep_from_ratio(double r) {
 namespace cas {
 int gemv_wait_status(bool clear);
 int set_first_wait_spins(uint32_t spins);
+void set_launch_overlap(bool on);
 }  // namespace cas
 
 extern "C" int cas_test_first_wait_spins(uint32_t spins) {
   if (cudaDeviceSynchronize() != cudaSuccess) return CAS_ERR_CUDA;
   return cas::set_first_wait_spins(spins == 0xFFFFFFFFu ? cas::kSpinLimit : spins);
+}
+
+extern "C" int cas_set_launch_overlap(int on) {
+  cas::set_launch_overlap(on != 0);
+  return CAS_OK;
 }
 
 extern "C" int cas_device_status(void* stream) {
@@ -90,6 +97,12 @@ int occupancy(const void* func, int threads, size_t smem) {
   cache[k] = n;
   return n;
 }
+
+namespace {
+std::atomic<int> g_launch_overlap{0};
+}
+bool launch_overlap() { return g_launch_overlap.load(std::memory_order_relaxed) != 0; }
+void set_launch_overlap(bool on) { g_launch_overlap.store(on ? 1 : 0, std::memory_order_relaxed); }
 
 int launch_status() {
   cudaError_t e = cudaGetLastError();

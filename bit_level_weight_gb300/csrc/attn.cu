@@ -162,6 +162,8 @@ __device__ __forceinline__ void decode_sb_tile(const KvDev& d, int st, int64_t n
 
 template <bool FULL, int QPW>
 __global__ void __launch_bounds__(kThreads) attn_chunk_kernel(AttnArgs a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(16) uint8_t smem[];
   uint16_t* Kt = reinterpret_cast<uint16_t*>(smem);
   uint16_t* Vt = Kt + kStepTok * kRow;
@@ -423,6 +425,8 @@ __device__ __forceinline__ bool kv_block_tiles(const KvDev& d, int h, int64_t n,
 // warp recomputes the m-tile's S, which is cheap next to the decode).
 template <bool FULL, int MT>
 __global__ void __launch_bounds__(kThreads, MT == 2 ? 4 : 5) attn_mma_kernel(AttnArgs a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(16) uint8_t smem[];
   uint16_t* Kt = reinterpret_cast<uint16_t*>(smem);
   uint16_t* Vt = Kt + kStepTok * kRow;
@@ -753,6 +757,8 @@ __device__ __forceinline__ bool quarter_sb_scores(const KvDev& d, int st, int64_
 // cover (partial, Cassandra-2, other k or m, long streams) are decoded into a
 // K tile and scored from it.
 __global__ void __launch_bounds__(kThreads, 8) attn_draft_fused_kernel(AttnArgs a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(16) uint8_t smem[];
   uint16_t* Kt = reinterpret_cast<uint16_t*>(smem);  // fallback K tile
   uint16_t* Vt = Kt + kStepTok * kRow;
@@ -861,6 +867,8 @@ struct CombineArgs {
 // chunks w, w+32, ... with lane L holding dims 4L..4L+3 (online max / sum);
 // the warp results and the bf16 tail tokens are merged in shared memory.
 __global__ void __launch_bounds__(kCombineWarps * 32) attn_combine_kernel(CombineArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float wm[kCombineWarps], wl[kCombineWarps];
   __shared__ float4 wo[kCombineWarps][32];
   __shared__ float ts[kMaxT];
@@ -955,8 +963,7 @@ int launch_fused(AttnArgs& a, int Hkv, cudaStream_t st) {
                       (size_t)kWarps * a.scr_warp;
   const int s = one_wave(a, Hkv, (const void*)attn_draft_fused_kernel, smem);
   if (s) return s;
-  attn_draft_fused_kernel<<<dim3(a.nchunk, Hkv, a.B), kThreads, smem, st>>>(a);
-  return launch_status();
+  return launch_k(attn_draft_fused_kernel, dim3(a.nchunk, Hkv, a.B), kThreads, smem, st, a);
 }
 
 
@@ -1037,6 +1044,8 @@ __device__ __noinline__ bool draft_v_scan(uint32_t ms_a, uint32_t st_a, int q0, 
 }
 
 __global__ void __launch_bounds__(kThreads, 4) attn_draft_block_kernel(AttnArgs a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(16) uint8_t smem[];
   float4* q4 = reinterpret_cast<float4*>(smem);  // [128] dims x 4 query vectors, scaled
   uint32_t* lutk = reinterpret_cast<uint32_t*>(q4 + CAS_BLK);  // exponent << 23 by rank (K)
@@ -1416,8 +1425,7 @@ int launch_draft_block(AttnArgs& a, int Hkv, cudaStream_t st) {
   const size_t smem = (size_t)CAS_BLK * 16 + 2 * 256 * 4 + 2 * 256 + (size_t)kWarps * sizeof(DraftStage);
   const int s = one_wave(a, Hkv, (const void*)attn_draft_block_kernel, smem);
   if (s) return s;
-  attn_draft_block_kernel<<<dim3(a.nchunk, Hkv, a.B), kThreads, smem, st>>>(a);
-  return launch_status();
+  return launch_k(attn_draft_block_kernel, dim3(a.nchunk, Hkv, a.B), kThreads, smem, st, a);
 }
 
 template <bool FULL, int MT>
@@ -1428,8 +1436,7 @@ int launch_mma(AttnArgs& a, int Hkv, cudaStream_t st) {
   auto kern = attn_mma_kernel<FULL, MT>;
   const int s = one_wave(a, Hkv, (const void*)kern, smem);
   if (s) return s;
-  kern<<<dim3(a.nchunk, Hkv, a.B * a.ngroups), kThreads, smem, st>>>(a);
-  return launch_status();
+  return launch_k(kern, dim3(a.nchunk, Hkv, a.B * a.ngroups), kThreads, smem, st, a);
 }
 
 // a.nchunk on entry: the most chunks the workspace holds; on return: the
@@ -1441,8 +1448,7 @@ int launch_chunk(AttnArgs& a, int Hkv, cudaStream_t st) {
   const int s = one_wave(a, Hkv, (const void*)kern, smem);
   if (s) return s;
   dim3 grid(a.nchunk, Hkv, a.B * a.ngroups);
-  kern<<<grid, kThreads, smem, st>>>(a);
-  return launch_status();
+  return launch_k(kern, grid, kThreads, smem, st, a);
 }
 
 int run_attn(bool full, const cas_kv* const* kv, int B, const uint16_t* q, int T, int Hq, const uint16_t* tail_k,
@@ -1508,8 +1514,7 @@ int run_attn(bool full, const cas_kv* const* kv, int B, const uint16_t* q, int T
   c.nchunk = a.nchunk;
   c.n_tail = full ? 0 : n_tail;
   c.scale = a.scale;
-  attn_combine_kernel<<<dim3(Hq, T, B), kCombineWarps * 32, 0, st>>>(c);
-  return launch_status();
+  return launch_k(attn_combine_kernel, dim3(Hq, T, B), kCombineWarps * 32, 0, st, c);
 }
 
 }  // namespace

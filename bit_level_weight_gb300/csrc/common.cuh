@@ -305,6 +305,47 @@ __device__ __forceinline__ float pow2_biased(int be) {
 
 }  // namespace cas
 
+// ------------------------------------------------------------------ launches
+// Launch overlap (cas_set_launch_overlap, off by default): kernels are then
+// launched with programmatic stream serialization, so a kernel's CTAs may
+// become resident while the kernel before it in the stream is still running.
+// Every kernel starts with pdl_wait(), which returns once that kernel has
+// completed and its writes are visible (at once without such a kernel):
+// nothing global is read or written before it, so what overlaps is the launch
+// and the CTA start-up. pdl_trigger() lets the next kernel's CTAs launch into
+// the SM slots this kernel frees. A kernel that a call enqueues right after
+// its own memset or copy is launched plainly (launch_plain).
+namespace cas {
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+bool launch_overlap();
+
+template <class... P, class... A>
+inline int launch_with(bool overlap, void (*k)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       A... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = overlap ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, args...) == cudaSuccess ? CAS_OK : CAS_ERR_CUDA;
+}
+template <class... P, class... A>
+inline int launch_k(void (*k)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, A... args) {
+  return launch_with(launch_overlap(), k, grid, block, smem, st, args...);
+}
+template <class... P, class... A>
+inline int launch_plain(void (*k)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, A... args) {
+  return launch_with(false, k, grid, block, smem, st, args...);
+}
+}  // namespace cas
+
 // host-side helpers shared by the translation units
 namespace cas {
 WView make_view(const cas_weights* W);

@@ -14,6 +14,8 @@ constexpr int kWarps = kThreads / 32;
 
 template <int VAR, bool FULL>
 __global__ void __launch_bounds__(kThreads) decode_kernel(WView w, Lut lut, uint16_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ uint8_t s_lut[256];
   __shared__ uint8_t s_code[kWarps][1024];
   __shared__ uint8_t s_vcode[kWarps][1024];
@@ -48,11 +50,8 @@ int run_decode(const cas_weights* W, uint16_t* out, void* stream) {
   for (int i = 0; i < 256; ++i) lut.v[i] = W->exp_of_rank[i];
   int64_t g = std::min<int64_t>((v.nsb + kWarps - 1) / kWarps, (int64_t)sm_count() * 8);
   cudaStream_t st = (cudaStream_t)stream;
-  if (v.variant == 1)
-    decode_kernel<1, FULL><<<(int)g, kThreads, 0, st>>>(v, lut, out);
-  else
-    decode_kernel<2, FULL><<<(int)g, kThreads, 0, st>>>(v, lut, out);
-  return launch_status();
+  return v.variant == 1 ? launch_k(decode_kernel<1, FULL>, (int)g, kThreads, 0, st, v, lut, out)
+                        : launch_k(decode_kernel<2, FULL>, (int)g, kThreads, 0, st, v, lut, out);
 }
 
 }  // namespace

@@ -33,6 +33,8 @@ WsLayout ws_layout(int64_t nsb) {
 
 // 256-bin histogram of the biased exponent (8 values per thread per step).
 __global__ void hist_kernel(const uint16_t* __restrict__ W, int64_t n, unsigned long long* counts) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ unsigned int h[256];
   for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0;
   __syncthreads();
@@ -61,6 +63,8 @@ __global__ void __launch_bounds__(kThreads) lengths_kernel(const uint16_t* __res
                                                           int nsr, int64_t nsb, int k, int m,
                                                           const uint8_t* __restrict__ roe_g, uint32_t* lens,
                                                           int64_t stride) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ uint8_t roe[256];
   for (int i = threadIdx.x; i < 256; i += blockDim.x) roe[i] = roe_g[i];
   __syncthreads();
@@ -104,6 +108,8 @@ struct ScanArgs {
   int64_t n;
 };
 __global__ void __launch_bounds__(1024) scan_kernel(ScanArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ unsigned long long sh[1024];
   int which = blockIdx.x;
   const uint32_t* in = a.in[which];
@@ -163,6 +169,8 @@ struct WriteArgs {
 // Pass 2: one warp per superblock writes every section.
 template <int VAR>
 __global__ void __launch_bounds__(kThreads) write_kernel(WriteArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ uint8_t roe[256];
   for (int i = threadIdx.x; i < 256; i += blockDim.x) roe[i] = a.roe[i];
   __syncthreads();
@@ -209,12 +217,13 @@ int run_lengths_scan(const uint16_t* W, const cas_weights* d, uint8_t* ws, const
   if (nsb == 0) return CAS_OK;
   uint32_t* lens = (uint32_t*)(ws + L.lens);
   int g = grid_for(nsb, kWarps);
-  if (d->p.variant == 1)
-    lengths_kernel<1><<<g, kThreads, 0, st>>>(W, d->K, nbr, nsr, nsb, d->p.keep_per_block, d->p.mant_bits,
-                                              ws + L.roe, lens, nsb + 1);
-  else
-    lengths_kernel<2><<<g, kThreads, 0, st>>>(W, d->K, nbr, nsr, nsb, d->p.keep_per_block, d->p.mant_bits,
-                                              ws + L.roe, lens, nsb + 1);
+  {
+    const int e_ = d->p.variant == 1 ? launch_plain(lengths_kernel<1>, g, kThreads, 0, st, W, d->K, nbr, nsr, nsb,
+                                                    d->p.keep_per_block, d->p.mant_bits, ws + L.roe, lens, nsb + 1)
+                                     : launch_plain(lengths_kernel<2>, g, kThreads, 0, st, W, d->K, nbr, nsr, nsb,
+                                                    d->p.keep_per_block, d->p.mant_bits, ws + L.roe, lens, nsb + 1);
+    if (e_) return e_;
+  }
   ScanArgs sa{};
   for (int i = 0; i < 4; ++i) {
     sa.in[i] = lens + i * (nsb + 1);
@@ -222,8 +231,7 @@ int run_lengths_scan(const uint16_t* W, const cas_weights* d, uint8_t* ws, const
   }
   sa.totals = (unsigned long long*)(ws + L.totals);
   sa.n = nsb;
-  scan_kernel<<<4, 1024, 0, st>>>(sa);
-  return launch_status();
+  return launch_plain(scan_kernel, 4, 1024, 0, st, sa);
 }
 
 void fill_sections(cas_weights* d, const uint64_t words[4]) {
@@ -287,8 +295,9 @@ extern "C" int cas_encode_weights_plan(const uint16_t* W, int64_t N, int64_t K, 
   std::vector<unsigned long long> counts(256, 0);
   if (cudaMemsetAsync(ws + L.counts, 0, 256 * 8, st) != cudaSuccess) return CAS_ERR_CUDA;
   if (N * K > 0) {
-    hist_kernel<<<sm_count() * 4, 256, 0, st>>>(W, N * K, (unsigned long long*)(ws + L.counts));
-    if (launch_status()) return CAS_ERR_CUDA;
+    if (const int e_ = launch_plain(hist_kernel, sm_count() * 4, 256, 0, st, W, N * K,
+                                    (unsigned long long*)(ws + L.counts)))
+      return e_;
   }
   if (cudaMemcpyAsync(counts.data(), ws + L.counts, 256 * 8, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
       cudaStreamSynchronize(st) != cudaSuccess)
@@ -377,11 +386,7 @@ extern "C" int cas_encode_weights(const uint16_t* W, cas_weights* d, void* buf, 
   a.vresidx = sec(CAS_SEC_VER_RES_SBIDX);
   a.vres_words = d->len[CAS_SEC_VER_RES] / 4;
   int g = grid_for(nsb, kWarps);
-  if (v1)
-    write_kernel<1><<<g, kThreads, 0, st>>>(a);
-  else
-    write_kernel<2><<<g, kThreads, 0, st>>>(a);
-  return launch_status();
+  return v1 ? launch_plain(write_kernel<1>, g, kThreads, 0, st, a) : launch_plain(write_kernel<2>, g, kThreads, 0, st, a);
 }
 
 extern "C" int cas_choose_variant(const uint16_t* W, int64_t N, int64_t K, int keep_per_block, int mant_bits,

@@ -64,6 +64,8 @@ static_assert(kWarps * scratch_warp<1>() >= kWarps * 256 * 4, "warp partials fit
 // verify_gemm_block_kernel below.)
 template <int VAR, int NT, int MODE>
 __global__ void __launch_bounds__(kThreads, 4) verify_gemm_kernel(GemmArgs a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(128) uint8_t smem[];
   const WView& w = a.w;
   uint16_t* tile = reinterpret_cast<uint16_t*>(smem);  // [16][kTileStride]
@@ -197,8 +199,7 @@ int launch(const GemmArgs& a, cudaStream_t st) {
   if (per_sm < 1) return CAS_ERR_CUDA;
   int64_t ntasks = (a.w.N + kRows - 1) / kRows * a.w.nsr;
   int g = (int)std::max<int64_t>(1, std::min<int64_t>(ntasks, (int64_t)sm_count() * per_sm));
-  kern<<<g, kThreads, smem, st>>>(a);
-  return launch_status();
+  return launch_plain(kern, g, kThreads, smem, st, a);  // after the memset of Y
 }
 
 
@@ -296,6 +297,8 @@ __device__ __noinline__ bool verify_lane_scan(uint32_t ms_a, uint32_t st_a, int 
 
 template <int NT>
 __global__ void __launch_bounds__(kVThreads, 4) verify_gemm_block_kernel(GemmArgs a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint32_t lut7[256];  // exponent << 7 by rank
   __shared__ uint8_t lut8[256];   // exponent by rank (generic decoder)
@@ -509,8 +512,7 @@ int launch_block(const GemmArgs& a, cudaStream_t st) {
   const int64_t ntasks = (a.w.N + kVRows - 1) / kVRows * a.w.nsr;
   if (ntasks + (int64_t)sm_count() * per_sm >= (int64_t)1 << 32) return CAS_ERR_INVALID;  // 32-bit task indices
   const int g = (int)std::max<int64_t>(1, std::min<int64_t>(ntasks, (int64_t)sm_count() * per_sm));
-  kern<<<g, kVThreads, smem, st>>>(a);
-  return launch_status();
+  return launch_plain(kern, g, kVThreads, smem, st, a);  // after the memset of Y
 }
 
 }  // namespace

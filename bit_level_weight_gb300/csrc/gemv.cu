@@ -56,7 +56,17 @@ struct GemvArgs {
   const uint16_t* gamma = nullptr;
   uint16_t* xn = nullptr;
   float eps = 0.f;
+  // How the lane-per-block kernel writes y: 0, fp32 atomics into a y the
+  // caller cleared; rows of exactly 32 blocks (one chunk per row, so one warp
+  // owns each row's sum) 1, a plain store, or 2, a plain add.
+  int ymode = 0;
+  bool cleared = false;  // host only: y was cleared by a memset just before the launch
 };
+
+template <class... P>
+int launch_gemv(void (*k)(P...), int grid, int block, size_t smem, cudaStream_t st, const GemvArgs& a) {
+  return a.cleared ? launch_plain(k, grid, block, smem, st, a) : launch_k(k, grid, block, smem, st, a);
+}
 
 // Set when a bounded wait on the x staging copy gave up (read by
 // cas_device_status).
@@ -93,6 +103,8 @@ struct OnesCursor {
 
 template <int VAR, int NV>
 __global__ void __launch_bounds__(kThreads) draft_gemv_kernel(GemvArgs a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(128) uint8_t smem[];
   const WView& w = a.w;
   const int K = (int)w.K;
@@ -304,6 +316,8 @@ __device__ __forceinline__ void lane_kept_dot(UnaryCursor& uc, uint4 pq, uint2 r
 
 template <int NV>
 __global__ void __launch_bounds__(kThreads, 4) draft_gemv_fast_kernel(GemvArgs a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(128) uint8_t smem[];
   const WView& w = a.w;
   const int K = (int)w.K;
@@ -438,6 +452,8 @@ __device__ __forceinline__ void run_dot(const RunsWarp& rw, UnaryCursor& uc, con
 
 template <int VAR, int NV>
 __global__ void __launch_bounds__(kThreads) draft_gemv_runs_kernel(GemvArgs a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(128) uint8_t smem[];
   const WView& w = a.w;
   const int K = (int)w.K;
@@ -547,6 +563,8 @@ struct Fast2Warp {
 
 template <int NV>
 __global__ void __launch_bounds__(kThreads) draft_gemv_fast2_kernel(GemvArgs a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(128) uint8_t smem[];
   const WView& w = a.w;
   const int K = (int)w.K;
@@ -641,8 +659,7 @@ int launch_fast2(const GemvArgs& a, cudaStream_t st) {
   if (per_sm < 1) return CAS_ERR_CUDA;
   int64_t need = (a.w.nsb + kWarps - 1) / kWarps;
   int g = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sm_count() * per_sm));
-  kern<<<g, kThreads, smem, st>>>(a);
-  return launch_status();
+  return launch_gemv(kern, g, kThreads, smem, st, a);
 }
 
 template <int NV>
@@ -653,8 +670,7 @@ int launch_fast(const GemvArgs& a, cudaStream_t st) {
   if (per_sm < 1) return CAS_ERR_CUDA;
   int64_t need = (a.w.nsb + kWarps - 1) / kWarps;
   int g = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sm_count() * per_sm));
-  kern<<<g, kThreads, smem, st>>>(a);
-  return launch_status();
+  return launch_gemv(kern, g, kThreads, smem, st, a);
 }
 
 template <int VAR, int NV>
@@ -665,8 +681,7 @@ int launch_runs(const GemvArgs& a, cudaStream_t st) {
   if (per_sm < 1) return CAS_ERR_CUDA;
   int64_t need = (a.w.nsb + kWarps - 1) / kWarps;
   int g = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sm_count() * per_sm));
-  kern<<<g, kThreads, smem, st>>>(a);
-  return launch_status();
+  return launch_gemv(kern, g, kThreads, smem, st, a);
 }
 
 template <int VAR, int NV>
@@ -677,8 +692,7 @@ int launch(const GemvArgs& a, cudaStream_t st) {
   if (per_sm < 1) return CAS_ERR_CUDA;
   int64_t need = (a.w.nsb + kWarps - 1) / kWarps;
   int g = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sm_count() * per_sm));
-  kern<<<g, kThreads, smem, st>>>(a);
-  return launch_status();
+  return launch_gemv(kern, g, kThreads, smem, st, a);
 }
 
 // ------------------------------------------------------------------ word path
@@ -746,6 +760,8 @@ __device__ __noinline__ void word_fallback(WView w, int64_t s, const uint8_t* lu
 // done, so nothing of that decoder is live in the hot loop.
 template <int NV>
 __global__ void __launch_bounds__(kThreads, 8) draft_gemv_word_kernel(GemvArgs a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint8_t lut8[256];  // exponent by rank
   const WView& w = a.w;
@@ -1030,6 +1046,8 @@ __device__ __noinline__ ScanSum<NV> block_walk_scan(uint32_t ms_a, uint32_t st_a
 
 template <int NV, int KEEP>
 __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs a) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int kRec = (KEEP * 4 + 31) / 32;  // sign/mantissa record words per block
   constexpr int kGroups = (KEEP + 7) / 8;
   // groups of 8 values per re-alignment of the position window: 16 of 64
@@ -1225,7 +1243,16 @@ __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs
         bad = !r.ok;
       }
       fast = fast && !__any_sync(CAS_FULL, bad);
-      if (fast) {
+      if (fast && a.ymode) {  // the chunk is row nr, all of it
+#pragma unroll
+        for (int q = 0; q < NV; ++q) {
+          const float sA = warp_sumf(part[q]);
+          if (lane == 0) {
+            float* d = a.y + (int64_t)q * w.N + nr;
+            *d = a.ymode == 2 ? *d + sA : sA;
+          }
+        }
+      } else if (fast) {
         const uint32_t nA = __shfl_sync(CAS_FULL, nr, 0);
         const uint32_t nB = __reduce_max_sync(CAS_FULL, valid ? nr : nA);  // rows of a chunk: nA and maybe nA + 1
 #pragma unroll
@@ -1256,17 +1283,29 @@ __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs
   uint8_t* code = reinterpret_cast<uint8_t*>(&bs);
   for (int i = 0; i < nfb; ++i) {
     const int cf = fb[i];
+    float row[NV];  // the chunk's row sum (ymode: the chunk is one whole row)
+#pragma unroll
+    for (int q = 0; q < NV; ++q) row[q] = 0.f;
+    int64_t nf = 0;
     for (int u = 0; u < 4; ++u) {
       const int64_t sf = (int64_t)cf * 4 + u;
       if (sf >= nsb) break;
-      const int64_t nf = sf / w.nsr;
+      nf = sf / w.nsr;
       const int jf = (int)(sf - nf * w.nsr);
       float part[NV];
       word_fallback<NV>(w, sf, lut8, code, xs + (jf * CAS_SB + (lane >> 2)) * kBXRow + 32 * (lane & 3), xfl, part);
 #pragma unroll
       for (int q = 0; q < NV; ++q) {
         const float r = warp_sumf(part[q]);
-        if (lane == 0) atomicAdd(a.y + (int64_t)q * w.N + nf, r);
+        row[q] += r;
+        if (lane == 0 && !a.ymode) atomicAdd(a.y + (int64_t)q * w.N + nf, r);
+      }
+    }
+    if (a.ymode && lane == 0) {
+#pragma unroll
+      for (int q = 0; q < NV; ++q) {
+        float* d = a.y + (int64_t)q * w.N + nf;
+        *d = a.ymode == 2 ? *d + row[q] : row[q];
       }
     }
   }
@@ -1298,8 +1337,7 @@ int launch_block(const GemvArgs& a, cudaStream_t st) {
     g = sm_count() * per_sm;
     smem = block_smem<NV>(a.w.nbr) + (size_t)kBWarps * block_per(a.w.nsb, g) * sizeof(int);
   }
-  kern<<<g, kBThreads, smem, st>>>(a);
-  return launch_status();
+  return launch_gemv(kern, g, kBThreads, smem, st, a);
 }
 
 template <int NV>
@@ -1319,8 +1357,7 @@ int launch_word(const GemvArgs& a, cudaStream_t st) {
     g = sm_count() * per_sm;
     smem = word_smem<NV>(a.w.K) + (size_t)kWarps * word_per(a.w.nsb, g) * sizeof(int);
   }
-  kern<<<g, kThreads, smem, st>>>(a);
-  return launch_status();
+  return launch_gemv(kern, g, kThreads, smem, st, a);
 }
 
 // The fast path covers Cassandra-1 with k = 64, m = 3 and rows that are whole
@@ -1418,19 +1455,24 @@ int draft_gemv_call(const cas_weights* W, const uint16_t* x, const float* xf, co
   if (!xf && (!x || !aligned16(x))) return CAS_ERR_INVALID;
   if (W->N == 0 && !xf) return CAS_OK;  // nothing to write (y may be an empty tensor)
   if (W->N > 0 && (!y || !aligned16(y))) return CAS_ERR_INVALID;
-  if (!accumulate && W->N > 0 && cudaMemsetAsync(y, 0, sizeof(float) * nvec * W->N, st) != cudaSuccess)
-    return CAS_ERR_CUDA;
-  if (W->K == 0) return CAS_OK;
   // superblock indices stay 32-bit, with room for the grid stride
-  if (W->N * ((W->K / CAS_BLK + CAS_SB - 1) / CAS_SB) >= (1ll << 30)) return CAS_ERR_INVALID;
+  if (W->K > 0 && W->N * ((W->K / CAS_BLK + CAS_SB - 1) / CAS_SB) >= (1ll << 30)) return CAS_ERR_INVALID;
   GemvArgs a;
   a.w = make_view(W);
   for (int i = 0; i < 256; ++i) a.lut.v[i] = W->exp_of_rank[i];
   a.x = x;
   a.y = y;
   a.sexp_words = (int)(W->len[CAS_SEC_SPEC_EXP] / 4);
+  const bool block = W->N > 0 && W->K > 0 && (W->p.variant == 1 ? block_path<1>(a, nvec) : block_path<2>(a, nvec));
+  // rows of one chunk: the kernel writes each row once, no clearing first
+  if (block && a.w.nbr == 32) a.ymode = accumulate ? 2 : 1;
+  // y cleared first unless the kernel writes every row once; the memset comes
+  // after the normalisation kernel of an unfused call, right before the GEMV
+  const bool clear = !accumulate && !a.ymode && W->N > 0;
+  if (W->K == 0) return clear && cudaMemsetAsync(y, 0, sizeof(float) * nvec * W->N, st) != cudaSuccess ? CAS_ERR_CUDA
+                                                                                                      : CAS_OK;
   if (xf) {
-    const bool fused = W->N > 0 && (W->p.variant == 1 ? block_path<1>(a, nvec) : block_path<2>(a, nvec));
+    const bool fused = block;
     if (!fused) {  // the normalised input first (the glue kernel), then the plain GEMV
       s = cas_add_rmsnorm(const_cast<float*>(xf), nullptr, nvec, (int)W->K, gamma, eps, xn, st);
       if (s || W->N == 0) return s;
@@ -1441,6 +1483,10 @@ int draft_gemv_call(const cas_weights* W, const uint16_t* x, const float* xf, co
       a.xn = xn;
       a.eps = eps;
     }
+  }
+  if (clear) {
+    if (cudaMemsetAsync(y, 0, sizeof(float) * nvec * W->N, st) != cudaSuccess) return CAS_ERR_CUDA;
+    a.cleared = true;
   }
   return W->p.variant == 1 ? dispatch<1>(a, nvec, st) : dispatch<2>(a, nvec, st);
 }

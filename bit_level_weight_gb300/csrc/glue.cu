@@ -30,6 +30,8 @@ constexpr int kNormVpt = 16;  // dim <= 16384
 __global__ void __launch_bounds__(kNormThreads) add_rmsnorm_kernel(float* __restrict__ x, const float* __restrict__ y,
                                                                    int dim, const uint16_t* __restrict__ gamma,
                                                                    float eps, uint16_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[kNormThreads / 32];
   const int64_t r = blockIdx.x;
   float* xr = x + r * dim;
@@ -70,6 +72,8 @@ __global__ void __launch_bounds__(kNormThreads) add_rmsnorm_kernel(float* __rest
 __global__ void rope_split_kernel(const float* __restrict__ qkv, int Hq, int Hkv, int64_t pos0, int rows_per_seq,
                                   double log_theta, uint16_t* __restrict__ q, uint16_t* __restrict__ k,
                                   int64_t k_stride, uint16_t* __restrict__ v, int64_t v_stride) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float cs[64], sn[64];
   const int r = blockIdx.y;
   if (threadIdx.x < 64) {
@@ -101,6 +105,8 @@ __global__ void rope_split_kernel(const float* __restrict__ qkv, int Hq, int Hkv
 
 // ---------------------------------------------------------------- SiLU(gate) * up
 __global__ void silu_mul_kernel(const float* __restrict__ gu, int F, int64_t n, uint16_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = t / F;
     const int j = (int)(t - r * F);
@@ -110,6 +116,8 @@ __global__ void silu_mul_kernel(const float* __restrict__ gu, int F, int64_t n, 
 }
 
 __global__ void to_bf16_kernel(const float* __restrict__ in, int64_t n, uint16_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x)
     out[t] = to_bf16(in[t]);
 }
@@ -118,6 +126,8 @@ __global__ void to_bf16_kernel(const float* __restrict__ in, int64_t n, uint16_t
 constexpr int kArgThreads = 1024;
 __global__ void __launch_bounds__(kArgThreads) argmax_kernel(const float* __restrict__ logits, int64_t V,
                                                              int32_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float bv[kArgThreads / 32];
   __shared__ int64_t bi[kArgThreads / 32];
   const float* lr = logits + (int64_t)blockIdx.x * V;
@@ -157,6 +167,8 @@ __global__ void __launch_bounds__(kArgThreads) argmax_kernel(const float* __rest
 // ---------------------------------------------------------------- embedding lookup
 __global__ void embed_kernel(const int32_t* __restrict__ tok, const uint16_t* __restrict__ table, int64_t V, int dim,
                              float* __restrict__ x) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.y;
   const int64_t id = tok[r];
   const int64_t row = id < 0 ? 0 : (id >= V ? V - 1 : id);  // an invalid id reads a valid row
@@ -179,8 +191,7 @@ extern "C" int cas_add_rmsnorm(float* x, const float* y, int rows, int dim, cons
   if (rows < 0 || dim < 1 || dim > kNormThreads * kNormVpt || !(eps >= 0.f)) return CAS_ERR_INVALID;
   if (rows == 0) return CAS_OK;
   if (!x || !gamma || !out) return CAS_ERR_INVALID;
-  add_rmsnorm_kernel<<<rows, kNormThreads, 0, (cudaStream_t)stream>>>(x, y, dim, gamma, eps, out);
-  return launch_status();
+  return launch_k(add_rmsnorm_kernel, rows, kNormThreads, 0, (cudaStream_t)stream, x, y, dim, gamma, eps, out);
 }
 
 extern "C" int cas_rope_split(const float* qkv, int rows, int n_q_heads, int n_kv_heads, int64_t pos0,
@@ -194,9 +205,8 @@ extern "C" int cas_rope_split(const float* qkv, int rows, int n_q_heads, int n_k
     return CAS_ERR_INVALID;
   const int pairs = (n_q_heads + 2 * n_kv_heads) * 64;
   dim3 g((pairs + 255) / 256, rows);
-  rope_split_kernel<<<g, 256, 0, (cudaStream_t)stream>>>(qkv, n_q_heads, n_kv_heads, pos0, rows_per_seq,
+  return launch_k(rope_split_kernel, g, 256, 0, (cudaStream_t)stream, qkv, n_q_heads, n_kv_heads, pos0, rows_per_seq,
                                                          std::log(theta), q, k, k_row_stride, v, v_row_stride);
-  return launch_status();
 }
 
 extern "C" int cas_silu_mul(const float* gate_up, int rows, int ffn, uint16_t* out, void* stream) {
@@ -204,24 +214,21 @@ extern "C" int cas_silu_mul(const float* gate_up, int rows, int ffn, uint16_t* o
   if (rows == 0) return CAS_OK;
   if (!gate_up || !out) return CAS_ERR_INVALID;
   const int64_t n = (int64_t)rows * ffn;
-  silu_mul_kernel<<<grid1d(n, 256), 256, 0, (cudaStream_t)stream>>>(gate_up, ffn, n, out);
-  return launch_status();
+  return launch_k(silu_mul_kernel, grid1d(n, 256), 256, 0, (cudaStream_t)stream, gate_up, ffn, n, out);
 }
 
 extern "C" int cas_f32_to_bf16(const float* in, int64_t n, uint16_t* out, void* stream) {
   if (n < 0) return CAS_ERR_INVALID;
   if (n == 0) return CAS_OK;
   if (!in || !out) return CAS_ERR_INVALID;
-  to_bf16_kernel<<<grid1d(n, 256), 256, 0, (cudaStream_t)stream>>>(in, n, out);
-  return launch_status();
+  return launch_k(to_bf16_kernel, grid1d(n, 256), 256, 0, (cudaStream_t)stream, in, n, out);
 }
 
 extern "C" int cas_argmax(const float* logits, int rows, int64_t vocab, int32_t* out, void* stream) {
   if (rows < 0 || vocab < 1 || vocab > 0x7FFFFFFF) return CAS_ERR_INVALID;
   if (rows == 0) return CAS_OK;
   if (!logits || !out) return CAS_ERR_INVALID;
-  argmax_kernel<<<rows, kArgThreads, 0, (cudaStream_t)stream>>>(logits, vocab, out);
-  return launch_status();
+  return launch_k(argmax_kernel, rows, kArgThreads, 0, (cudaStream_t)stream, logits, vocab, out);
 }
 
 extern "C" int cas_embed(const int32_t* tokens, int rows, const uint16_t* table, int64_t vocab, int dim, float* x,
@@ -230,6 +237,5 @@ extern "C" int cas_embed(const int32_t* tokens, int rows, const uint16_t* table,
   if (rows == 0) return CAS_OK;
   if (!tokens || !table || !x) return CAS_ERR_INVALID;
   dim3 g((dim + 255) / 256, rows);
-  embed_kernel<<<g, 256, 0, (cudaStream_t)stream>>>(tokens, table, vocab, dim, x);
-  return launch_status();
+  return launch_k(embed_kernel, g, 256, 0, (cudaStream_t)stream, tokens, table, vocab, dim, x);
 }

@@ -115,6 +115,8 @@ bool kv_layout(int H, int64_t Tm, cas_params p, double est, KvLayout* L) {
 // Exponent histogram of each stream's calibration tokens (u32 counts).
 __global__ void kv_hist_kernel(const uint16_t* __restrict__ ck, const uint16_t* __restrict__ cv, int64_t n, int H,
                                unsigned int* hist) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ unsigned int h[256];
   int st = blockIdx.y;
   const uint16_t* src = st < H ? ck : cv;
@@ -167,6 +169,8 @@ struct RoundSmem {
 
 template <int VAR, bool WRITE>
 __global__ void __launch_bounds__(kThreads) kv_append_kernel(AppendArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ RoundSmem sm;
   __shared__ uint8_t roe[256];
   __shared__ uint64_t cur[3];
@@ -343,6 +347,8 @@ __device__ uint64_t after_nth_one(const uint32_t* words, uint64_t w0, uint64_t w
 // kept values, which are read from their d codes (stream C).
 template <int VAR>
 __global__ void kv_truncate_kernel(KvDev d, int64_t n_req) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ uint8_t s_d[CAS_SB * CAS_BLK];
   const int st = blockIdx.x, lane = threadIdx.x & 31;
   KvState* S = kv_state(d);
@@ -435,8 +441,7 @@ extern "C" int cas_kv_init(cas_kv* kv, void* buf, uint64_t bytes, int H, int64_t
   std::vector<unsigned int> h((size_t)S * 256, 0);
   if (n_calib > 0) {
     dim3 grid((unsigned)std::min<int64_t>((n_calib * CAS_BLK + 255) / 256, 64), S);
-    kv_hist_kernel<<<grid, 256, 0, st>>>(ck, cv, n_calib, H, hist);
-    if (launch_status()) return CAS_ERR_CUDA;
+    if (const int e_ = launch_plain(kv_hist_kernel, grid, 256, 0, st, ck, cv, n_calib, H, hist)) return e_;
     if (cudaMemcpyAsync(h.data(), hist, h.size() * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
         cudaStreamSynchronize(st) != cudaSuccess)
       return CAS_ERR_CUDA;
@@ -470,11 +475,11 @@ extern "C" int cas_encode_kv_append(cas_kv* kv, const uint16_t* knew, const uint
   cudaStream_t st = (cudaStream_t)stream;
   int S = 2 * kv->n_kv_heads;
   if (kv->p.variant == 1) {
-    kv_append_kernel<1, false><<<S, kThreads, 0, st>>>(a);
-    kv_append_kernel<1, true><<<S, kThreads, 0, st>>>(a);
+    if (const int e_ = launch_k(kv_append_kernel<1, false>, S, kThreads, 0, st, a)) return e_;
+    if (const int e_ = launch_k(kv_append_kernel<1, true>, S, kThreads, 0, st, a)) return e_;
   } else {
-    kv_append_kernel<2, false><<<S, kThreads, 0, st>>>(a);
-    kv_append_kernel<2, true><<<S, kThreads, 0, st>>>(a);
+    if (const int e_ = launch_k(kv_append_kernel<2, false>, S, kThreads, 0, st, a)) return e_;
+    if (const int e_ = launch_k(kv_append_kernel<2, true>, S, kThreads, 0, st, a)) return e_;
   }
   return launch_status();
 }
@@ -483,11 +488,9 @@ extern "C" int cas_kv_truncate(cas_kv* kv, int64_t n, void* stream) {
   int s = check_kv(kv);
   if (s) return s;
   if (n < 0) return CAS_ERR_INVALID;
-  if (kv->p.variant == 1)
-    kv_truncate_kernel<1><<<2 * kv->n_kv_heads, 32, 0, (cudaStream_t)stream>>>(make_kv_dev(kv), n);
-  else
-    kv_truncate_kernel<2><<<2 * kv->n_kv_heads, 32, 0, (cudaStream_t)stream>>>(make_kv_dev(kv), n);
-  return launch_status();
+  const cudaStream_t st = (cudaStream_t)stream;
+  return kv->p.variant == 1 ? launch_k(kv_truncate_kernel<1>, 2 * kv->n_kv_heads, 32, 0, st, make_kv_dev(kv), n)
+                            : launch_k(kv_truncate_kernel<2>, 2 * kv->n_kv_heads, 32, 0, st, make_kv_dev(kv), n);
 }
 
 extern "C" int cas_kv_status(const cas_kv* kv, int64_t* n_tokens, void* stream) {

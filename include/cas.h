@@ -123,6 +123,18 @@ int cas_device_status(void* stream);
  * restores the normal limit. Synchronises the device; returns CAS_OK or
  * CAS_ERR_CUDA. */
 int cas_test_first_wait_spins(uint32_t spins);
+/* Launch overlap, process-wide, off by default. When on, the kernels of later
+ * calls are launched with programmatic stream serialization: a kernel's
+ * thread blocks may start while the previous kernel in the stream is still
+ * running, and wait on the device (before touching any global memory) until
+ * that kernel has completed and its writes are visible. This hides the gap
+ * between back-to-back kernels, e.g. in a captured decode step. Contract while
+ * on: the operation enqueued on a stream directly before a libcas call must be
+ * a kernel (any kernel) or a libcas call, not a copy, memset or event wait
+ * issued by the caller; libcas's own memsets and copies are always followed by
+ * plainly launched kernels. Affects launches only (captured graphs keep what
+ * they recorded). Returns CAS_OK. */
+int cas_set_launch_overlap(int on);
 int32_t cas_keep_from_ratio(double ratio);
 /* Device-side scratch that cas_encode_weights_plan / cas_encode_weights need
  * for a tensor of N x K (histogram, per-superblock lengths, scan). */

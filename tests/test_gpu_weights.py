@@ -368,3 +368,30 @@ def test_verify_gemm_block_tiles(cas, orc, N, K, kind, T):
     Y = cas.verify_gemm(enc, X.cuda())
     ref, norm = orc.matvec(np16(W), np16(X))
     check_close(Y, ref, norm, "verify_gemm block tiles")
+
+
+@pytest.mark.parametrize("nvec", [1, 2])
+@pytest.mark.parametrize("kind", ["t4", "wide", "clustered"])
+def test_draft_gemv_rows_of_one_chunk(cas, orc, kind, nvec):
+    """Rows of exactly 32 blocks (K = 4096): one warp owns each row, so the
+    lane-per-block kernel stores the row sum (y is not cleared first) or adds
+    it to y (the accumulating call), also for rows whose long codes send the
+    chunk to the generic decoder or whose clustered masks make a lane scan its
+    block again. y starts as NaN (plain call) or random (accumulating call)."""
+    N, K = 24, 4096
+    if kind == "t4":
+        W = synthetic.t4_weight(N, K, seed=31)
+    elif kind == "wide":
+        W = wide_exponent_rows(N, K, 5, seed=32)
+    else:
+        W = clustered_rows(N, K, seed=33)
+    x = synthetic.activations(nvec, K, seed=34 + nvec).cuda()
+    enc = cas.encode_weights(W.cuda(), 1, 64, 3)
+    ref, norm = orc.matvec(orc.draft_values(np16(W), 1, 64, 3), np16(x.cpu()))
+    y = torch.full((nvec, N), float("nan"), dtype=torch.float32, device="cuda")
+    cas.cas_draft_gemv(enc, x, y)
+    check_close(y, ref, norm, "draft_gemv rows of one chunk")
+    g = torch.Generator().manual_seed(35)
+    y0 = torch.randn(nvec, N, generator=g)
+    ya = cas.cas_draft_gemv_accumulate(enc, x, y0.clone().cuda())
+    check_close(ya - y0.cuda(), ref, norm, "draft_gemv_accumulate rows of one chunk")
