@@ -274,9 +274,11 @@ KERNELS_PER_CALL = {"gemv": 1, "gemm": 1, "draft_attn": 2, "verify_attn": 2, "ap
 class Step:
     """One self-speculative decode step as a data-dependent forward through
     the C ABI: D draft tokens, each a forward of every layer over the
-    speculation data (embedding, RMSNorm, draft GEMV Wqkv, RoPE into a bf16
-    draft tail, draft attention over the compressed KV + tail, Wo, residual +
-    RMSNorm, Wgate|up, SiLU*mul, Wdown, ..., final RMSNorm, LM head, argmax
+    speculation data (embedding, draft GEMV Wqkv of the RMSNorm of the
+    residual, RoPE into a bf16 draft tail, draft attention over the compressed
+    KV + tail, Wo of its bf16-rounded output added into the residual, Wgate|up
+    of the RMSNorm (the rounding and the norm inside the GEMV's staging of x),
+    SiLU*mul, Wdown added into the residual, ..., final RMSNorm, LM head, argmax
     -> next draft token), then one verify forward of the T = D + 1 tokens over
     the exact weights (verify GEMMs, online KV append, verify attention, LM
     head, argmax), then a rollback of the KV caches to the context (fixed
@@ -320,9 +322,14 @@ class Step:
             add("gemv", [P("cas_draft_gemv_rmsnorm", W, xres, B, gamma, eps, xout, y, st)], ["gemv"])
 
         def gemv_acc(W, xin, y):
-            # y += D(W) xin: the residual add happens in the GEMV's atomics
+            # y += D(W) xin: the residual add happens in the GEMV's row writes
             self.draft_bytes += W.spec_bytes() + B * W.K * 2 + B * W.N * 8
             add("gemv", [P("cas_draft_gemv_accumulate", W, xin, B, y, st)], ["gemv"])
+
+        def gemv_f32(W, src, op, width, xout, y):
+            # y += D(W) bf16(op(src)): rounding or SiLU*mul of the fp32 input in the GEMV's x staging
+            self.draft_bytes += W.spec_bytes() + B * width * 4 + B * W.K * 2 + B * W.N * 8
+            add("gemv", [P("cas_draft_gemv_f32", W, src, B, op, None, 0.0, xout, y, 1, st)], ["gemv"])
 
         def gemm(W, Xin, Y):
             self.verify_bytes += W.all_bytes() + B * T * W.K * 2 + B * T * W.N * 4
@@ -342,11 +349,11 @@ class Step:
                         fns.append(cas.prepare_draft_attn([stk.kv[layer][b]], q[b:b + 1], tk[b:b + 1, :d + 1],
                                                           tv[b:b + 1, :d + 1], o[b:b + 1], ws, st))
                         what.append("draft_attn")
-                fns.append(P("cas_f32_to_bf16", o, B * Hq * hd, ob, st))
-                what.append("glue")
                 add("other", fns, what)
-                gemv_acc(M["o"], ob, x)
+                gemv_f32(M["o"], o, cas.X_ROUND, Hq * hd, ob, x)
                 gemv_norm(M["gateup"], x, stk.g2[layer], xn, gu)
+                # SiLU*mul stays a kernel of its own: formed in every CTA's staging it
+                # reads the 2F fp32 gate|up row once per CTA, more than it saves
                 add("other", [P("cas_silu_mul", gu, B, F, hh, st)], ["glue"])
                 gemv_acc(M["down"], hh, x)
             gemv_norm(stk.lm, x, stk.gf, xn, lg)

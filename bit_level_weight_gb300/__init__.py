@@ -80,6 +80,7 @@ def lib() -> ctypes.CDLL:
             "cas_draft_gemv": ([P, P, i32, P, P], i32),
             "cas_draft_gemv_accumulate": ([P, P, i32, P, P], i32),
             "cas_draft_gemv_rmsnorm": ([P, P, i32, P, ctypes.c_float, P, P, P], i32),
+            "cas_draft_gemv_f32": ([P, P, i32, i32, P, ctypes.c_float, P, P, i32, P], i32),
             "cas_verify_gemm": ([P, P, i32, P, P], i32),
             "cas_decode_draft": ([P, P, P], i32),
             "cas_reconstruct": ([P, P, P], i32),
@@ -283,6 +284,40 @@ def draft_gemv_rmsnorm(W: EncodedWeights, x: torch.Tensor, gamma: torch.Tensor, 
     _out(y, nvec * W.N, (torch.float32,), "y")
     _check(lib().cas_draft_gemv_rmsnorm(ctypes.byref(W.desc), _ptr(x), nvec, _ptr(gamma), float(eps), _ptr(xn),
                                         _ptr(y), _stream(stream)), "cas_draft_gemv_rmsnorm")
+    return xn, y
+
+
+X_ROUND, X_RMSNORM, X_SILU_MUL = 0, 1, 2  # input transforms of cas_draft_gemv_f32
+
+
+def draft_gemv_f32(W: EncodedWeights, x: torch.Tensor, op: int, gamma: torch.Tensor | None = None,
+                   eps: float = 1e-5, xn: torch.Tensor | None = None, y: torch.Tensor | None = None,
+                   accumulate: bool = False, stream=None):
+    """xn = the bf16 input made from fp32 x by `op` (X_ROUND: bf16(x); X_RMSNORM:
+    bf16(rmsnorm(x) * gamma); X_SILU_MUL: bf16(silu(g) * u) of rows [g | u] of
+    2K values), y = D(W) xn (added to y with accumulate). Returns (xn, y)."""
+    if op not in (X_ROUND, X_RMSNORM, X_SILU_MUL):
+        raise ValueError("draft_gemv_f32: unknown op")
+    width = 2 * W.K if op == X_SILU_MUL else W.K
+    if x.dtype != torch.float32 or x.dim() != 2 or x.shape[1] != width or not x.is_contiguous():
+        raise ValueError(f"draft_gemv_f32: x must be contiguous fp32 [nvec][{width}]")
+    nvec = x.shape[0]
+    if op == X_RMSNORM:
+        if gamma is None:
+            raise ValueError("draft_gemv_f32: X_RMSNORM needs gamma")
+        gamma = _bits(gamma)
+        _shape(gamma, (W.K,), "gamma")
+    if xn is None:
+        xn = torch.empty(nvec, W.K, dtype=torch.int16, device=x.device)
+    if y is None:
+        if accumulate:
+            raise ValueError("draft_gemv_f32: accumulate needs y")
+        y = torch.empty(nvec, W.N, dtype=torch.float32, device=x.device)
+    _out(xn, nvec * W.K, (torch.int16, torch.bfloat16), "xn")
+    _out(y, nvec * W.N, (torch.float32,), "y")
+    _check(lib().cas_draft_gemv_f32(ctypes.byref(W.desc), _ptr(x), nvec, op, _ptr(gamma) if op == X_RMSNORM else None,
+                                    float(eps), _ptr(xn), _ptr(y), 1 if accumulate else 0, _stream(stream)),
+           "cas_draft_gemv_f32")
     return xn, y
 
 

@@ -892,19 +892,36 @@ __global__ void __launch_bounds__(kCombineWarps * 32) attn_combine_kernel(Combin
   }
   float M = -INFINITY, L = 0.f;
   float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c = warp; c < used; c += kCombineWarps) {
-    const float mc = P[c * kPart + CAS_BLK];
-    if (mc == -INFINITY) continue;
-    const float lc = P[c * kPart + CAS_BLK + 1];
-    // partials sit at a 130-float (520-byte) stride: 8-byte aligned, so two float2 loads
-    const float2 oa = reinterpret_cast<const float2*>(P + c * kPart)[2 * lane];
-    const float2 ob = reinterpret_cast<const float2*>(P + c * kPart)[2 * lane + 1];
-    const float4 oc = make_float4(oa.x, oa.y, ob.x, ob.y);
-    const float mn = fmaxf(M, mc);
-    const float fa = M == -INFINITY ? 0.f : __expf(M - mn), fb = __expf(mc - mn);
-    L = L * fa + lc * fb;
-    O = make_float4(O.x * fa + oc.x * fb, O.y * fa + oc.y * fb, O.z * fa + oc.z * fb, O.w * fa + oc.w * fb);
-    M = mn;
+  // four chunks per warp and pass, their loads issued before any is used
+  constexpr int kU = 4;
+  for (int c0 = warp; c0 < used; c0 += kU * kCombineWarps) {
+    float mc[kU], lc[kU];
+    float4 oc[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int c = c0 + u * kCombineWarps;
+      mc[u] = -INFINITY;
+      lc[u] = 0.f;
+      oc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c < used) {
+        mc[u] = P[c * kPart + CAS_BLK];
+        lc[u] = P[c * kPart + CAS_BLK + 1];
+        // partials sit at a 130-float (520-byte) stride: 8-byte aligned, so two float2 loads
+        const float2 oa = reinterpret_cast<const float2*>(P + c * kPart)[2 * lane];
+        const float2 ob = reinterpret_cast<const float2*>(P + c * kPart)[2 * lane + 1];
+        oc[u] = make_float4(oa.x, oa.y, ob.x, ob.y);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (mc[u] == -INFINITY) continue;
+      const float mn = fmaxf(M, mc[u]);
+      const float fa = M == -INFINITY ? 0.f : __expf(M - mn), fb = __expf(mc[u] - mn);
+      L = L * fa + lc[u] * fb;
+      O = make_float4(O.x * fa + oc[u].x * fb, O.y * fa + oc[u].y * fb, O.z * fa + oc[u].z * fb,
+                      O.w * fa + oc[u].w * fb);
+      M = mn;
+    }
   }
   if (lane == 0) {
     wm[warp] = M;

@@ -7,6 +7,7 @@
 //   (Cassandra blog review, section 3.2: "count zeros until a one");
 //   fixed-width fields are LSB-first in u32 words.
 #pragma once
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -297,6 +298,10 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 
 // bf16 bits -> float
 __device__ __forceinline__ float bf2f(uint32_t b) { return __uint_as_float(b << 16); }
+// float -> bf16 bits, round to nearest even (the glue kernels' rounding)
+__device__ __forceinline__ uint16_t f2bf(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+// SiLU(g) * u in fp32, one expression shared by every kernel that forms it
+__device__ __forceinline__ float silu_mul_f(float g, float u) { return g / (1.f + expf(-g)) * u; }
 
 // 2^(be - 127) as a float for be in [-22, 254] (subnormal below 1).
 __device__ __forceinline__ float pow2_biased(int be) {

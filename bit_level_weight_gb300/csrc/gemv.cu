@@ -50,8 +50,11 @@ struct GemvArgs {
   const uint16_t* x;
   float* y;
   int sexp_words;  // words of the unary exponent section (read bound)
-  // RMSNorm of an fp32 input in the x staging (lane-per-block kernel only):
-  // x = bf16(xf / sqrt(mean(xf^2) + eps) * gamma), also written to xn by CTA 0
+  // An fp32 input transformed in the x staging (lane-per-block kernel only),
+  // the bf16 result also written to xn by CTA 0. xop: 0 none (x is bf16),
+  // 1 RMSNorm, x = bf16(xf / sqrt(mean(xf^2) + eps) * gamma); 2 rounding,
+  // x = bf16(xf); 3 SiLU * mul, x = bf16(silu(g) * u) of xf rows [g | u] of 2K.
+  int xop = 0;
   const float* xf = nullptr;
   const uint16_t* gamma = nullptr;
   uint16_t* xn = nullptr;
@@ -1066,15 +1069,45 @@ __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs
   BlockStage& bs = reinterpret_cast<BlockStage*>(smem + (size_t)NV * xfl * 4 + kBXPad)[warp];
 
   // x -> fp32, position p of vector v at v*xfl + (p/128)*129 + p%128
-  if (a.xf) {  // the input is fp32: RMSNorm first, rounded to bf16 like the unfused glue
+  // fp32 inputs are read 4 values per load, several loads in flight per thread
+  if (a.xop >= 2) {  // an fp32 input, rounded (or SiLU * mul first) to bf16 like the glue kernels
+    for (int v = 0; v < NV; ++v) {
+      const float4* src = reinterpret_cast<const float4*>(a.xf + (size_t)v * (a.xop == 3 ? 2 * K : K));
+#pragma unroll 4
+      for (int i = threadIdx.x; i < K / 4; i += kBThreads) {
+        float4 f = __ldg(src + i);
+        if (a.xop == 3) {
+          const float4 u = __ldg(src + K / 4 + i);
+          f = make_float4(silu_mul_f(f.x, u.x), silu_mul_f(f.y, u.y), silu_mul_f(f.z, u.z), silu_mul_f(f.w, u.w));
+        }
+        const uint32_t b0 = f2bf(f.x), b1 = f2bf(f.y), b2 = f2bf(f.z), b3 = f2bf(f.w);
+        const int p = 4 * i;
+        float* d = xs + v * xfl + (p >> 7) * kBXRow + (p & 127);
+        d[0] = bf2f(b0);
+        d[1] = bf2f(b1);
+        d[2] = bf2f(b2);
+        d[3] = bf2f(b3);
+        if (blockIdx.x == 0) reinterpret_cast<uint2*>(a.xn + (size_t)v * K)[i] = make_uint2(b0 | (b1 << 16), b2 | (b3 << 16));
+      }
+    }
+  } else if (a.xop == 1) {  // the input is fp32: RMSNorm first, rounded to bf16 like the unfused glue
     __shared__ float red[kBWarps];
     for (int v = 0; v < NV; ++v) {
-      const float* xr = a.xf + (size_t)v * K;
+      const float4* xr = reinterpret_cast<const float4*>(a.xf + (size_t)v * K);
       float ss = 0.f;
-      for (int i = threadIdx.x; i < K; i += kBThreads) {
-        const float s = __ldg(xr + i);
-        xs[v * xfl + (i >> 7) * kBXRow + (i & 127)] = s;
-        ss = fmaf(s, s, ss);
+#pragma unroll 4
+      for (int i = threadIdx.x; i < K / 4; i += kBThreads) {
+        const float4 f = __ldg(xr + i);
+        const int p = 4 * i;
+        float* d = xs + v * xfl + (p >> 7) * kBXRow + (p & 127);
+        d[0] = f.x;
+        d[1] = f.y;
+        d[2] = f.z;
+        d[3] = f.w;
+        ss = fmaf(f.x, f.x, ss);
+        ss = fmaf(f.y, f.y, ss);
+        ss = fmaf(f.z, f.z, ss);
+        ss = fmaf(f.w, f.w, ss);
       }
       ss = warp_sumf(ss);
       if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
@@ -1082,16 +1115,24 @@ __global__ void __launch_bounds__(kBThreads, 3) draft_gemv_block_kernel(GemvArgs
       float tot = (threadIdx.x & 31) < kBWarps ? red[threadIdx.x & 31] : 0.f;
       tot = warp_sumf(tot);
       const float inv = rsqrtf(tot / (float)K + a.eps);
-      for (int i = threadIdx.x; i < K; i += kBThreads) {
-        float* d = xs + v * xfl + (i >> 7) * kBXRow + (i & 127);
-        const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(*d * inv * bf2f(__ldg(a.gamma + i))));
-        *d = bf2f(b);
-        if (blockIdx.x == 0) a.xn[(size_t)v * K + i] = (uint16_t)b;
+      const uint2* gm = reinterpret_cast<const uint2*>(a.gamma);
+#pragma unroll 4
+      for (int i = threadIdx.x; i < K / 4; i += kBThreads) {
+        const int p = 4 * i;
+        float* d = xs + v * xfl + (p >> 7) * kBXRow + (p & 127);
+        const uint2 g = __ldg(gm + i);
+        const uint32_t b0 = f2bf(d[0] * inv * bf2f(g.x & 0xFFFFu)), b1 = f2bf(d[1] * inv * bf2f(g.x >> 16));
+        const uint32_t b2 = f2bf(d[2] * inv * bf2f(g.y & 0xFFFFu)), b3 = f2bf(d[3] * inv * bf2f(g.y >> 16));
+        d[0] = bf2f(b0);
+        d[1] = bf2f(b1);
+        d[2] = bf2f(b2);
+        d[3] = bf2f(b3);
+        if (blockIdx.x == 0) reinterpret_cast<uint2*>(a.xn + (size_t)v * K)[i] = make_uint2(b0 | (b1 << 16), b2 | (b3 << 16));
       }
       __syncthreads();
     }
   }
-  for (int v = 0; v < NV && !a.xf; ++v) {
+  for (int v = 0; v < NV && a.xop == 0; ++v) {
     const uint4* xv = reinterpret_cast<const uint4*>(a.x + (size_t)v * K);
     for (int i = threadIdx.x; i < K / 8; i += kBThreads) {
       const uint4 pr = __ldg(xv + i);
@@ -1444,14 +1485,15 @@ namespace cas {
 namespace {
 
 // y (+)= D(W) x; with xf, x = bf16(rmsnorm(xf) * gamma) written to xn first.
-int draft_gemv_call(const cas_weights* W, const uint16_t* x, const float* xf, const uint16_t* gamma, float eps,
-                    uint16_t* xn, int nvec, float* y, bool accumulate, cudaStream_t st) {
+int draft_gemv_call(const cas_weights* W, const uint16_t* x, const float* xf, int xop, const uint16_t* gamma,
+                    float eps, uint16_t* xn, int nvec, float* y, bool accumulate, cudaStream_t st) {
   int s = check_weights(W);
   if (s) return s;
   if (nvec < 1 || nvec > kMaxVec) return CAS_ERR_INVALID;
   if ((int64_t)nvec * W->K * 2 > 200 * 1024) return CAS_ERR_INVALID;  // x must fit in shared memory
-  if (xf && (!gamma || !xn || !aligned16(xf) || !aligned16(xn) || !(eps >= 0.f) || W->K < 1 || W->K > 16384))
-    return CAS_ERR_INVALID;
+  if (xop < 0 || xop > 3 || (xop != 0) != (xf != nullptr)) return CAS_ERR_INVALID;
+  if (xf && (!xn || !aligned16(xf) || !aligned16(xn) || W->K < 1 || W->K > 16384)) return CAS_ERR_INVALID;
+  if (xop == 1 && (!gamma || !(eps >= 0.f))) return CAS_ERR_INVALID;
   if (!xf && (!x || !aligned16(x))) return CAS_ERR_INVALID;
   if (W->N == 0 && !xf) return CAS_OK;  // nothing to write (y may be an empty tensor)
   if (W->N > 0 && (!y || !aligned16(y))) return CAS_ERR_INVALID;
@@ -1473,11 +1515,17 @@ int draft_gemv_call(const cas_weights* W, const uint16_t* x, const float* xf, co
                                                                                                       : CAS_OK;
   if (xf) {
     const bool fused = block;
-    if (!fused) {  // the normalised input first (the glue kernel), then the plain GEMV
-      s = cas_add_rmsnorm(const_cast<float*>(xf), nullptr, nvec, (int)W->K, gamma, eps, xn, st);
+    if (!fused) {  // the transformed input first (the glue kernel), then the plain GEMV
+      if (xop == 1)
+        s = cas_add_rmsnorm(const_cast<float*>(xf), nullptr, nvec, (int)W->K, gamma, eps, xn, st);
+      else if (xop == 2)
+        s = cas_f32_to_bf16(xf, (int64_t)nvec * W->K, xn, st);
+      else
+        s = cas_silu_mul(xf, nvec, (int)W->K, xn, st);
       if (s || W->N == 0) return s;
       a.x = xn;
     } else {
+      a.xop = xop;
       a.xf = xf;
       a.gamma = gamma;
       a.xn = xn;
@@ -1495,15 +1543,22 @@ int draft_gemv_call(const cas_weights* W, const uint16_t* x, const float* xf, co
 }  // namespace cas
 
 extern "C" int cas_draft_gemv(const cas_weights* W, const uint16_t* x, int nvec, float* y, void* stream) {
-  return draft_gemv_call(W, x, nullptr, nullptr, 0.f, nullptr, nvec, y, false, (cudaStream_t)stream);
+  return draft_gemv_call(W, x, nullptr, 0, nullptr, 0.f, nullptr, nvec, y, false, (cudaStream_t)stream);
 }
 
 extern "C" int cas_draft_gemv_accumulate(const cas_weights* W, const uint16_t* x, int nvec, float* y, void* stream) {
-  return draft_gemv_call(W, x, nullptr, nullptr, 0.f, nullptr, nvec, y, true, (cudaStream_t)stream);
+  return draft_gemv_call(W, x, nullptr, 0, nullptr, 0.f, nullptr, nvec, y, true, (cudaStream_t)stream);
 }
 
 extern "C" int cas_draft_gemv_rmsnorm(const cas_weights* W, const float* x, int nvec, const uint16_t* gamma, float eps,
                                       uint16_t* xn, float* y, void* stream) {
   if (!x) return CAS_ERR_INVALID;
-  return draft_gemv_call(W, nullptr, x, gamma, eps, xn, nvec, y, false, (cudaStream_t)stream);
+  return draft_gemv_call(W, nullptr, x, 1, gamma, eps, xn, nvec, y, false, (cudaStream_t)stream);
+}
+
+extern "C" int cas_draft_gemv_f32(const cas_weights* W, const float* x, int nvec, int op, const uint16_t* gamma,
+                                  float eps, uint16_t* xn, float* y, int accumulate, void* stream) {
+  if (!x || op < CAS_X_ROUND || op > CAS_X_SILU_MUL) return CAS_ERR_INVALID;
+  const int xop = op == CAS_X_RMSNORM ? 1 : op == CAS_X_ROUND ? 2 : 3;
+  return draft_gemv_call(W, nullptr, x, xop, gamma, eps, xn, nvec, y, accumulate != 0, (cudaStream_t)stream);
 }

@@ -19,7 +19,7 @@
 namespace cas {
 namespace {
 
-__device__ __forceinline__ uint16_t to_bf16(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+__device__ __forceinline__ uint16_t to_bf16(float f) { return f2bf(f); }
 
 // ---------------------------------------------------------------- add + RMSNorm
 // x[r] += y[r] (when y is given), then out[r] = bf16(x[r] / sqrt(mean(x[r]^2) + eps) * gamma).
@@ -111,7 +111,7 @@ __global__ void silu_mul_kernel(const float* __restrict__ gu, int F, int64_t n, 
     const int64_t r = t / F;
     const int j = (int)(t - r * F);
     const float g = gu[r * 2 * F + j], u = gu[r * 2 * F + F + j];
-    out[t] = to_bf16(g / (1.f + expf(-g)) * u);
+    out[t] = to_bf16(silu_mul_f(g, u));
   }
 }
 

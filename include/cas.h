@@ -198,6 +198,28 @@ int cas_draft_gemv_accumulate(const cas_weights* W, const uint16_t* x, int nvec,
 int cas_draft_gemv_rmsnorm(const cas_weights* W, const float* x, int nvec, const uint16_t* gamma, float eps,
                            uint16_t* xn, float* y, void* stream);
 
+/* Input transforms of cas_draft_gemv_f32 (the forward operation that produces
+ * a matrix product's bf16 input in the evaluated models). */
+enum {
+  CAS_X_ROUND = 0,    /* xn = bf16(x), as cas_f32_to_bf16; x: fp32 [nvec][K]            */
+  CAS_X_RMSNORM = 1,  /* xn = bf16(rmsnorm(x) * gamma), as cas_draft_gemv_rmsnorm       */
+  CAS_X_SILU_MUL = 2  /* xn = bf16(silu(g) * u), as cas_silu_mul; x: fp32 [nvec][2K], g
+                         the first K and u the last K values of a row (fused gate|up)  */
+};
+/* Draft GEMV of an fp32 input [B3.1] with the transform `op` applied while
+ * the GEMV stages x (where the lane-per-block kernel takes the tensor; else a
+ * separate glue kernel writes xn first): xn[v] = the transformed bf16 input,
+ * written by the call (bit-identical to the glue kernel's output for
+ * CAS_X_ROUND and CAS_X_SILU_MUL), and y[v][n] = sum_k D(W)[n][k] * xn[v][k],
+ * overwriting y, or added to y when `accumulate` is non-zero (y not cleared;
+ * a residual stream can be y). gamma: bf16 [K], used by CAS_X_RMSNORM only
+ * (may be NULL otherwise). x, xn, y 16-byte aligned; x is not written.
+ * Errors: those of cas_draft_gemv; CAS_ERR_INVALID for an unknown op, a null
+ * or misaligned x or xn, a missing gamma or a negative / NaN eps with
+ * CAS_X_RMSNORM, or K above 16384. N = 0 still writes xn. */
+int cas_draft_gemv_f32(const cas_weights* W, const float* x, int nvec, int op, const uint16_t* gamma, float eps,
+                       uint16_t* xn, float* y, int accumulate, void* stream);
+
 /* Verify GEMM [B3.1]: Y[t][n] = sum_k W[n][k] * X[t][k] for t < T (1..16)
  * with W rebuilt bit-exactly from both streams, on tensor cores with fp32
  * accumulation. X: bf16 [T][K]; Y: fp32 [T][N], overwritten. Errors: those

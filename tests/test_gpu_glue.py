@@ -106,3 +106,30 @@ def test_draft_gemv_rmsnorm_and_accumulate(cas, N, K, nvec, keep):
     y0 = torch.randn(nvec, N, generator=g)
     ya = cas.cas_draft_gemv_accumulate(enc, xn, y0.clone().cuda())
     assert (np.abs(ya.double().cpu().numpy() - (y0.double().numpy() + ref)) <= 2e-3 * nrm + 1e-5).all()
+
+
+@pytest.mark.parametrize("op", ["round", "silu_mul"])
+@pytest.mark.parametrize("N,K,nvec", [(40, 4096, 1), (24, 14336, 2), (20, 1152, 1), (33, 4096, 2)])
+def test_draft_gemv_f32_inputs(cas, N, K, nvec, op):
+    """The draft GEMV of an fp32 input rounded to bf16, or of SiLU(gate) * up
+    of a fused fp32 gate|up row, formed in the GEMV's x staging (K = 4096 and
+    14336) or by the glue kernel first (K = 1152): xn is bit-identical to
+    cas_f32_to_bf16 / cas_silu_mul, y matches the float64 statements on xn,
+    and the accumulating call adds the same product to a given y."""
+    import oracle
+    g = torch.Generator().manual_seed(N + K + nvec + len(op))
+    W = synthetic.t4_weight(N, K, seed=N + K + 1)
+    enc = cas.encode_weights(W.cuda(), 1, 64, 3)
+    Wd = oracle.draft_values(W.numpy().view(np.uint16), 1, 64, 3)
+    width = 2 * K if op == "silu_mul" else K
+    x = (torch.randn(nvec, width, generator=g) * 3.0).cuda()
+    code = cas.X_SILU_MUL if op == "silu_mul" else cas.X_ROUND
+    xn, y = cas.draft_gemv_f32(enc, x, code)
+    want = cas.silu_mul(x) if op == "silu_mul" else cas.f32_to_bf16(x)
+    assert torch.equal(xn.cpu(), want.cpu())
+    ref, nrm = oracle.matvec(Wd, xn.cpu().numpy().view(np.uint16))
+    assert (np.abs(y.double().cpu().numpy() - ref) <= 2e-3 * nrm + 1e-30).all()
+    y0 = torch.randn(nvec, N, generator=g)
+    xn2, ya = cas.draft_gemv_f32(enc, x, code, y=y0.clone().cuda(), accumulate=True)
+    assert torch.equal(xn2.cpu(), want.cpu())
+    assert (np.abs(ya.double().cpu().numpy() - (y0.double().numpy() + ref)) <= 2e-3 * nrm + 1e-5).all()
