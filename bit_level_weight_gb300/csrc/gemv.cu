@@ -1401,11 +1401,10 @@ int launch_word(const GemvArgs& a, cudaStream_t st) {
   return launch_gemv(kern, g, kThreads, smem, st, a);
 }
 
-// The fast path covers Cassandra-1 with k = 64, m = 3 and rows that are whole
-// superblocks (K % 1024 == 0): every lane then owns exactly 16 ordinals that
-// sit in one 64-bit slice of one block record.
-// Whether the lane-per-block kernel takes a call (it alone stages an fp32
-// input through RMSNorm).
+// Whether the lane-per-block kernel takes a call (it alone forms the bf16
+// input from an fp32 one in its staging). The 3-4 vector kernel (fast) covers
+// Cassandra-1 with k = 64, m = 3 on rows of whole superblocks (K % 1024 == 0):
+// every lane then owns exactly 16 ordinals in one 64-bit slice of one record.
 template <int VAR>
 bool block_path(const GemvArgs& a, int nvec) {
   return VAR == 1 && nvec <= 2 && a.w.m == 3 && (a.w.k == 64 || a.w.k == 38) && a.w.nbr % CAS_SB == 0 &&
