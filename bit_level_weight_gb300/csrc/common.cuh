@@ -363,6 +363,8 @@ int corrupt_status_gemm(bool clear);
 int corrupt_status_decode(bool clear);
 int sm_count();
 int launch_status();
+// Clears n floats at p (16-byte aligned) with a kernel on st.
+int zero_f32(float* p, int64_t n, cudaStream_t st);
 // Resident CTAs per SM of `func` with `threads` threads and `smem` dynamic
 // shared bytes; raises the kernel's dynamic shared-memory limit on first use.
 // Cached per (func, threads, smem), so repeated launches make no query.

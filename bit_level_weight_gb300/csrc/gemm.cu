@@ -199,7 +199,7 @@ int launch(const GemmArgs& a, cudaStream_t st) {
   if (per_sm < 1) return CAS_ERR_CUDA;
   int64_t ntasks = (a.w.N + kRows - 1) / kRows * a.w.nsr;
   int g = (int)std::max<int64_t>(1, std::min<int64_t>(ntasks, (int64_t)sm_count() * per_sm));
-  return launch_plain(kern, g, kThreads, smem, st, a);  // after the memset of Y
+  return launch_k(kern, g, kThreads, smem, st, a);
 }
 
 
@@ -512,7 +512,7 @@ int launch_block(const GemmArgs& a, cudaStream_t st) {
   const int64_t ntasks = (a.w.N + kVRows - 1) / kVRows * a.w.nsr;
   if (ntasks + (int64_t)sm_count() * per_sm >= (int64_t)1 << 32) return CAS_ERR_INVALID;  // 32-bit task indices
   const int g = (int)std::max<int64_t>(1, std::min<int64_t>(ntasks, (int64_t)sm_count() * per_sm));
-  return launch_plain(kern, g, kVThreads, smem, st, a);  // after the memset of Y
+  return launch_k(kern, g, kVThreads, smem, st, a);
 }
 
 }  // namespace
@@ -542,7 +542,7 @@ extern "C" int cas_verify_gemm(const cas_weights* W, const uint16_t* X, int T, f
   if (W->N == 0) return CAS_OK;  // nothing to write (Y may be an empty tensor)
   if (!X || !Y || !aligned16(X) || !aligned16(Y)) return CAS_ERR_INVALID;
   cudaStream_t st = (cudaStream_t)stream;
-  if (cudaMemsetAsync(Y, 0, sizeof(float) * T * W->N, st) != cudaSuccess) return CAS_ERR_CUDA;
+  if (const int e = zero_f32(Y, (int64_t)T * W->N, st)) return e;
   if (W->K == 0) return CAS_OK;
   GemmArgs a;
   a.w = make_view(W);

@@ -63,13 +63,7 @@ struct GemvArgs {
   // caller cleared; rows of exactly 32 blocks (one chunk per row, so one warp
   // owns each row's sum) 1, a plain store, or 2, a plain add.
   int ymode = 0;
-  bool cleared = false;  // host only: y was cleared by a memset just before the launch
 };
-
-template <class... P>
-int launch_gemv(void (*k)(P...), int grid, int block, size_t smem, cudaStream_t st, const GemvArgs& a) {
-  return a.cleared ? launch_plain(k, grid, block, smem, st, a) : launch_k(k, grid, block, smem, st, a);
-}
 
 // Set when a bounded wait on the x staging copy gave up (read by
 // cas_device_status).
@@ -662,7 +656,7 @@ int launch_fast2(const GemvArgs& a, cudaStream_t st) {
   if (per_sm < 1) return CAS_ERR_CUDA;
   int64_t need = (a.w.nsb + kWarps - 1) / kWarps;
   int g = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sm_count() * per_sm));
-  return launch_gemv(kern, g, kThreads, smem, st, a);
+  return launch_k(kern, g, kThreads, smem, st, a);
 }
 
 template <int NV>
@@ -673,7 +667,7 @@ int launch_fast(const GemvArgs& a, cudaStream_t st) {
   if (per_sm < 1) return CAS_ERR_CUDA;
   int64_t need = (a.w.nsb + kWarps - 1) / kWarps;
   int g = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sm_count() * per_sm));
-  return launch_gemv(kern, g, kThreads, smem, st, a);
+  return launch_k(kern, g, kThreads, smem, st, a);
 }
 
 template <int VAR, int NV>
@@ -684,7 +678,7 @@ int launch_runs(const GemvArgs& a, cudaStream_t st) {
   if (per_sm < 1) return CAS_ERR_CUDA;
   int64_t need = (a.w.nsb + kWarps - 1) / kWarps;
   int g = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sm_count() * per_sm));
-  return launch_gemv(kern, g, kThreads, smem, st, a);
+  return launch_k(kern, g, kThreads, smem, st, a);
 }
 
 template <int VAR, int NV>
@@ -695,7 +689,7 @@ int launch(const GemvArgs& a, cudaStream_t st) {
   if (per_sm < 1) return CAS_ERR_CUDA;
   int64_t need = (a.w.nsb + kWarps - 1) / kWarps;
   int g = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sm_count() * per_sm));
-  return launch_gemv(kern, g, kThreads, smem, st, a);
+  return launch_k(kern, g, kThreads, smem, st, a);
 }
 
 // ------------------------------------------------------------------ word path
@@ -1378,7 +1372,7 @@ int launch_block(const GemvArgs& a, cudaStream_t st) {
     g = sm_count() * per_sm;
     smem = block_smem<NV>(a.w.nbr) + (size_t)kBWarps * block_per(a.w.nsb, g) * sizeof(int);
   }
-  return launch_gemv(kern, g, kBThreads, smem, st, a);
+  return launch_k(kern, g, kBThreads, smem, st, a);
 }
 
 template <int NV>
@@ -1398,7 +1392,7 @@ int launch_word(const GemvArgs& a, cudaStream_t st) {
     g = sm_count() * per_sm;
     smem = word_smem<NV>(a.w.K) + (size_t)kWarps * word_per(a.w.nsb, g) * sizeof(int);
   }
-  return launch_gemv(kern, g, kThreads, smem, st, a);
+  return launch_k(kern, g, kThreads, smem, st, a);
 }
 
 // Whether the lane-per-block kernel takes a call (it alone forms the bf16
@@ -1507,11 +1501,9 @@ int draft_gemv_call(const cas_weights* W, const uint16_t* x, const float* xf, in
   const bool block = W->N > 0 && W->K > 0 && (W->p.variant == 1 ? block_path<1>(a, nvec) : block_path<2>(a, nvec));
   // rows of one chunk: the kernel writes each row once, no clearing first
   if (block && a.w.nbr == 32) a.ymode = accumulate ? 2 : 1;
-  // y cleared first unless the kernel writes every row once; the memset comes
-  // after the normalisation kernel of an unfused call, right before the GEMV
+  // y cleared first (a zero-fill kernel) unless the kernel writes every row once
   const bool clear = !accumulate && !a.ymode && W->N > 0;
-  if (W->K == 0) return clear && cudaMemsetAsync(y, 0, sizeof(float) * nvec * W->N, st) != cudaSuccess ? CAS_ERR_CUDA
-                                                                                                      : CAS_OK;
+  if (W->K == 0) return clear ? zero_f32(y, (int64_t)nvec * W->N, st) : CAS_OK;
   if (xf) {
     const bool fused = block;
     if (!fused) {  // the transformed input first (the glue kernel), then the plain GEMV
@@ -1531,10 +1523,8 @@ int draft_gemv_call(const cas_weights* W, const uint16_t* x, const float* xf, in
       a.eps = eps;
     }
   }
-  if (clear) {
-    if (cudaMemsetAsync(y, 0, sizeof(float) * nvec * W->N, st) != cudaSuccess) return CAS_ERR_CUDA;
-    a.cleared = true;
-  }
+  if (clear)
+    if (const int e = zero_f32(y, (int64_t)nvec * W->N, st)) return e;
   return W->p.variant == 1 ? dispatch<1>(a, nvec, st) : dispatch<2>(a, nvec, st);
 }
 

@@ -181,7 +181,26 @@ int grid1d(int64_t n, int threads) {
   return (int)std::min<int64_t>(std::max<int64_t>(g, 1), (int64_t)sm_count() * 8);
 }
 
+// ---------------------------------------------------------------- zero fill
+// Clears an fp32 output before kernels that add into it with atomics: as a
+// kernel (not a memset) it keeps the chain of kernels that launch overlap
+// relies on unbroken.
+__global__ void zero_f32_kernel(float4* __restrict__ p4, int64_t n4, float* __restrict__ tail, int nt) {
+  pdl_wait();
+  pdl_trigger();
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x)
+    p4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (blockIdx.x == 0 && (int)threadIdx.x < nt) tail[threadIdx.x] = 0.f;
+}
+
 }  // namespace
+
+int zero_f32(float* p, int64_t n, cudaStream_t st) {
+  if (n <= 0) return CAS_OK;
+  const int64_t n4 = n / 4;  // p is 16-byte aligned
+  return launch_k(zero_f32_kernel, grid1d(std::max<int64_t>(n4, 1), 256), 256, 0, st, reinterpret_cast<float4*>(p),
+                  n4, p + 4 * n4, (int)(n - 4 * n4));
+}
 }  // namespace cas
 
 using namespace cas;
