@@ -795,10 +795,10 @@ def attn_128k(cas, args, dev):
 # matches the tree is not used (the kernel changed since it was profiled).
 PROFILED = {
     # ncu --set full on the 28672 x 4096 Student-t(4) matrix, one vector
-    # (bench.py --micro draft_gemv --N 28672): dram read + write 61.809 + 0.142 MB
+    # (bench.py --micro draft_gemv --N 28672): dram read + write 61.809 + 0.129 MB
     # for 61.853 MB algorithmic, 46525966 warp instructions
-    "draft_gemv_block_kernel<1>": {"source_sha16": "6d918909d07c62a9", "shape": "28672 x 4096, keep 64, m = 3",
-                                   "traffic_ratio": (61.809152 + 0.142336) / 61.85268,
+    "draft_gemv_block_kernel<1>": {"source_sha16": "c53408e41b703cc8", "shape": "28672 x 4096, keep 64, m = 3",
+                                   "traffic_ratio": (61.80864 + 0.129024) / 61.85268,
                                    "lane_instr_per_elem": 46525966 * 32 / (28672 * 4096),
                                    "spec_bits_per_elem": 4.205},
 }
