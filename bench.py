@@ -268,7 +268,7 @@ class Stack:
 
 # kernels of ours each call launches (the y / Y clear of the matrix products
 # is a memset node, not a kernel)
-KERNELS_PER_CALL = {"gemv": 1, "gemm": 1, "draft_attn": 2, "verify_attn": 2, "append": 2, "truncate": 1, "glue": 1}
+KERNELS_PER_CALL = {"gemv": 1, "gemm": 2, "draft_attn": 2, "verify_attn": 2, "append": 2, "truncate": 1, "glue": 1}
 
 
 class Step:
@@ -387,9 +387,9 @@ class Step:
         fns = [P("cas_argmax", LG, B * T, V, self.vout, st)]
         fns += [P("cas_argmax", LG[b * T + T - 1:b * T + T], 1, V, self.vtok[b * T:b * T + 1], st) for b in range(B)]
         what = ["glue"] * (1 + B)
-        if attn:  # rollback: every cache back to the context
-            fns += [kv.prepare_truncate(stk.ctx, st) for layer_kv in stk.kv for kv in layer_kv]
-            what += ["truncate"] * (stk.L * B)
+        if attn:  # rollback: every cache back to the context, one launch for all of them
+            fns.append(cas.prepare_truncate_many([kv for layer_kv in stk.kv for kv in layer_kv], stk.ctx, st))
+            what.append("truncate")
         add("other", fns, what)
         self.segs = segs
         self.launches = sum(self.kernels.values())

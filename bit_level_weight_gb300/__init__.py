@@ -88,6 +88,7 @@ def lib() -> ctypes.CDLL:
             "cas_kv_init": ([P, P, u64, i32, i64, cas_params, ctypes.c_double, P, P, i64, P], i32),
             "cas_encode_kv_append": ([P, P, P, i32, P], i32),
             "cas_kv_truncate": ([P, i64, P], i32),
+            "cas_kv_truncate_many": ([P, i32, i64, P], i32),
             "cas_kv_status": ([P, P, P], i32),
             "cas_kv_clear_status": ([P, P], i32),
             "cas_attn_workspace_bytes": ([i32, i32, i32, i64], u64),
@@ -478,6 +479,24 @@ class _KvArray:
 
 def _kv_array(kvs):
     return _KvArray(kvs)
+
+
+def kv_truncate_many(kvs, n_tokens: int, stream=None):
+    """Rolls every cache in kvs back to n_tokens tokens (one launch per variant)."""
+    arr = _kv_array(kvs)
+    _check(lib().cas_kv_truncate_many(arr.ptr, len(arr.kvs), n_tokens, _stream(stream)), "cas_kv_truncate_many")
+
+
+def prepare_truncate_many(kvs, n_tokens: int, stream=None):
+    """Zero-argument callable of kv_truncate_many (for launch loops and graphs)."""
+    arr = _kv_array(kvs)
+    f = lib().cas_kv_truncate_many
+    st = _stream(stream or torch.cuda.current_stream())
+
+    def call():
+        _check(f(arr.ptr, len(arr.kvs), n_tokens, st), "cas_kv_truncate_many")
+    call.keep = arr
+    return call
 
 
 def cas_attn_workspace_bytes(batch: int, n_q_heads: int, T: int, max_tokens: int) -> int:

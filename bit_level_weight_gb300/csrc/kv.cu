@@ -345,12 +345,11 @@ __device__ uint64_t after_nth_one(const uint32_t* words, uint64_t w0, uint64_t w
 // the last kept token - after its r*k kept codes (stream A), r*(128-k) pruned
 // codes (stream B) and, for Cassandra-2, after the residual widths of those r*k
 // kept values, which are read from their d codes (stream C).
+// One warp per stream st of the cache; the last of its 2H warps to finish
+// publishes the new token count.
 template <int VAR>
-__global__ void kv_truncate_kernel(KvDev d, int64_t n_req) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ uint8_t s_d[CAS_SB * CAS_BLK];
-  const int st = blockIdx.x, lane = threadIdx.x & 31;
+__device__ __forceinline__ void kv_truncate_stream(const KvDev& d, int64_t n_req, int st, uint8_t* s_d) {
+  const int lane = threadIdx.x & 31;
   KvState* S = kv_state(d);
   const int64_t n0 = *(volatile int64_t*)&S->n_tokens;
   const int64_t n = n_req < n0 ? n_req : n0;
@@ -393,12 +392,35 @@ __global__ void kv_truncate_kernel(KvDev d, int64_t n_req) {
   if (lane == 0) {
     __threadfence();
     unsigned int prev = atomicAdd(&S->done, 1u);
-    if (prev == gridDim.x - 1) {
+    if (prev == 2u * (unsigned)d.H - 1u) {
       S->n_tokens = n;
       S->done = 0;
       __threadfence();
     }
   }
+}
+
+template <int VAR>
+__global__ void kv_truncate_kernel(KvDev d, int64_t n_req) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ uint8_t s_d[CAS_SB * CAS_BLK];
+  kv_truncate_stream<VAR>(d, n_req, blockIdx.x, s_d);
+}
+
+// Several caches of one variant in one launch: blockIdx.y picks the cache,
+// blockIdx.x its stream (caches with fewer heads leave the rest idle).
+constexpr int kTruncBatch = 80;  // descriptors per launch (kernel parameters stay under 32 KB)
+struct TruncBatch {
+  KvDev d[kTruncBatch];
+};
+template <int VAR>
+__global__ void kv_truncate_many_kernel(const __grid_constant__ TruncBatch b, int64_t n_req) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ uint8_t s_d[CAS_SB * CAS_BLK];
+  const KvDev& d = b.d[blockIdx.y];
+  if ((int)blockIdx.x < 2 * d.H) kv_truncate_stream<VAR>(d, n_req, blockIdx.x, s_d);
 }
 
 }  // namespace
@@ -491,6 +513,34 @@ extern "C" int cas_kv_truncate(cas_kv* kv, int64_t n, void* stream) {
   const cudaStream_t st = (cudaStream_t)stream;
   return kv->p.variant == 1 ? launch_k(kv_truncate_kernel<1>, 2 * kv->n_kv_heads, 32, 0, st, make_kv_dev(kv), n)
                             : launch_k(kv_truncate_kernel<2>, 2 * kv->n_kv_heads, 32, 0, st, make_kv_dev(kv), n);
+}
+
+extern "C" int cas_kv_truncate_many(cas_kv* const* kvs, int count, int64_t n, void* stream) {
+  if (count < 0 || (count > 0 && !kvs) || n < 0) return CAS_ERR_INVALID;
+  for (int i = 0; i < count; ++i) {
+    const int s = check_kv(kvs[i]);
+    if (s) return s;
+  }
+  const cudaStream_t st = (cudaStream_t)stream;
+  // one launch per variant and per kTruncBatch caches
+  for (int var = 1; var <= 2; ++var) {
+    TruncBatch b;
+    int m = 0, hmax = 0;
+    for (int i = 0; i <= count; ++i) {
+      if (i < count && kvs[i]->p.variant == var) {
+        b.d[m++] = make_kv_dev(kvs[i]);
+        hmax = std::max(hmax, kvs[i]->n_kv_heads);
+      }
+      if (m > 0 && (m == kTruncBatch || i == count)) {
+        const dim3 grid((unsigned)(2 * hmax), (unsigned)m);
+        const int e = var == 1 ? launch_k(kv_truncate_many_kernel<1>, grid, 32, 0, st, b, n)
+                               : launch_k(kv_truncate_many_kernel<2>, grid, 32, 0, st, b, n);
+        if (e) return e;
+        m = hmax = 0;
+      }
+    }
+  }
+  return CAS_OK;
 }
 
 extern "C" int cas_kv_status(const cas_kv* kv, int64_t* n_tokens, void* stream) {

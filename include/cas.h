@@ -326,6 +326,13 @@ int cas_encode_kv_append(cas_kv* kv, const uint16_t* k_new, const uint16_t* v_ne
  * n_tokens larger than the current count leaves the cache unchanged.
  * Errors: CAS_ERR_INVALID for n_tokens < 0; CAS_ERR_CUDA. */
 int cas_kv_truncate(cas_kv* kv, int64_t n_tokens, void* stream);
+/* cas_kv_truncate of every cache kvs[0..count) to n_tokens, in one launch per
+ * variant (up to 80 caches a launch), e.g. the rollback of all layers at the
+ * end of a decode step. The caches must be distinct. Errors: CAS_ERR_INVALID
+ * for count < 0, a null array with count > 0 or n_tokens < 0; the
+ * descriptor check's errors for any cache; CAS_ERR_CUDA. count = 0 does
+ * nothing. */
+int cas_kv_truncate_many(cas_kv* const* kvs, int count, int64_t n_tokens, void* stream);
 
 /* Reads the device state. Synchronises `stream`. Returns the sticky device
  * status (CAS_OK, CAS_ERR_CAPACITY or CAS_ERR_NONFINITE) and the token count. */

@@ -414,3 +414,33 @@ def test_attention_long_codes_and_gaps(cas, orc):
     ov = cas.verify_attn([kv], qv.cuda())
     ref, nrm = orc.attention(np16(qv[0]), np16(K), np16(V), causal_new=T)
     check_attn(ov[0], ref, nrm, "verify attention, long codes and gaps")
+
+
+@pytest.mark.parametrize("cut", [0, 9, 30])
+def test_truncate_many_equals_truncate(cas, cut):
+    """cas_kv_truncate_many over caches of both variants and of 1, 2 and 4
+    heads (one launch per variant, idle warps for the smaller caches) leaves
+    every stream section and the state exactly as cas_kv_truncate does, and
+    appends after it continue the same way."""
+    T = 40
+    specs = [(2, 1), (1, 2), (4, 1), (2, 2), (1, 1)]  # (heads, variant)
+    made = []
+    for i, (H, var) in enumerate(specs):
+        K, V = make_tokens(T, H, seed=100 + i)
+        K2, V2 = make_tokens(8, H, seed=200 + i)
+        a = new_cache(cas, H, 96, K, V, variant=var)
+        b = new_cache(cas, H, 96, K, V, variant=var)
+        a.append(K.cuda(), V.cuda())
+        b.append(K.cuda(), V.cuda())
+        made.append((H, a, b, K2, V2))
+    for _, a, _, _, _ in made:
+        a.truncate(cut)
+    cas.kv_truncate_many([b for _, _, b, _, _ in made], cut)
+    for H, a, b, K2, V2 in made:
+        assert b.status() == (cut, 0)
+        a.append(K2.cuda(), V2.cuda())
+        b.append(K2.cuda(), V2.cuda())
+        for s in range(2 * H):
+            assert_streams_equal(stream_sections(a, s, cut + 8), stream_sections(b, s, cut + 8))
+        assert torch.equal(state_bytes(a), state_bytes(b))
+    cas.kv_truncate_many([], 0)  # nothing to do
