@@ -83,3 +83,18 @@ def test_kv_append_shapes():
         kv.append(torch.zeros(3, 4, 128, dtype=torch.int16), k)
     with pytest.raises(ValueError, match="v_new"):
         kv.append(k, k[:2])
+
+
+@pytest.mark.parametrize("x,op,kw,what", [
+    (torch.zeros(1, 256), 7, {}, "unknown op"),
+    (torch.zeros(1, 256, dtype=torch.float64), 0, {}, "fp32"),
+    (torch.zeros(1, 256), 2, {}, "fp32 \\[nvec\\]\\[512\\]"),       # SiLU*mul reads rows of 2K
+    (torch.zeros(1, 512), 0, {}, "fp32 \\[nvec\\]\\[256\\]"),
+    (torch.zeros(1, 256), 1, {}, "gamma"),                         # RMSNorm without gamma
+    (torch.zeros(1, 256), 0, {"accumulate": True}, "accumulate needs y"),
+    (torch.zeros(1, 256), 0, {"y": torch.zeros(1, 5)}, "y"),
+    (torch.zeros(1, 256), 0, {"xn": torch.zeros(1, 255, dtype=torch.int16)}, "xn"),
+])
+def test_draft_gemv_f32_checks(x, op, kw, what):
+    with pytest.raises(ValueError, match=what):
+        cas.draft_gemv_f32(W, x, op, **kw)
