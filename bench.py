@@ -268,7 +268,7 @@ class Stack:
 
 # kernels of ours each call launches (the y / Y clear of the matrix products
 # is a memset node, not a kernel)
-KERNELS_PER_CALL = {"gemv": 1, "gemm": 2, "draft_attn": 2, "verify_attn": 2, "append": 2, "truncate": 1, "glue": 1}
+KERNELS_PER_CALL = {"gemv": 1, "gemm": 2, "gemm_acc": 1, "draft_attn": 2, "verify_attn": 2, "append": 2, "truncate": 1, "glue": 1}
 
 
 class Step:
@@ -296,17 +296,17 @@ class Step:
         self.vtok = torch.zeros(B * T, dtype=torch.int32, device=dev)  # per sequence: [t_last, d_1 .. d_D]
         x, xn, qkv, q = E(B, h), E(B, h, dt=i16), E(B, (Hq + 2 * Hkv) * hd), E(B, Hq, hd, dt=i16)
         tk, tv, o, ob = E(B, D, Hkv, hd, dt=i16), E(B, D, Hkv, hd, dt=i16), E(B, Hq, hd), E(B, Hq * hd, dt=i16)
-        yo, gu, hh, yd, lg = E(B, h), E(B, 2 * F), E(B, F, dt=i16), E(B, h), E(B, V)
+        gu, hh, lg = E(B, 2 * F), E(B, F, dt=i16), E(B, V)
         tk.zero_()
         tv.zero_()
         X, Xn, QKV = E(B * T, h), E(B * T, h, dt=i16), E(B * T, (Hq + 2 * Hkv) * hd)
         Q, Kn, Vn = E(B * T, Hq, hd, dt=i16), E(B * T, Hkv, hd, dt=i16), E(B * T, Hkv, hd, dt=i16)
-        O, Ob, Yo = E(B, T, Hq, hd), E(B * T, Hq * hd, dt=i16), E(B * T, h)
-        GU, HH, YD, LG = E(B * T, 2 * F), E(B * T, F, dt=i16), E(B * T, h), E(B * T, V)
+        O, Ob = E(B, T, Hq, hd), E(B * T, Hq * hd, dt=i16)
+        GU, HH, LG = E(B * T, 2 * F), E(B * T, F, dt=i16), E(B * T, V)
         self.vout = torch.zeros(B * T, dtype=torch.int32, device=dev)
         attn = stk.kv is not None
         ws = E(cas.cas_attn_workspace_bytes(B, Hq, T, stk.ctx + 64), dt=torch.uint8) if attn else None
-        self.keep = [x, xn, qkv, q, tk, tv, o, ob, yo, gu, hh, yd, lg, X, Xn, QKV, Q, Kn, Vn, O, Ob, Yo, GU, HH, YD,
+        self.keep = [x, xn, qkv, q, tk, tv, o, ob, gu, hh, lg, X, Xn, QKV, Q, Kn, Vn, O, Ob, GU, HH,
                      LG, ws]
         P, eps = cas.prepare, 1e-5
         segs, self.kernels = [], {"gemv": 0, "gemm": 0, "other": 0}
@@ -334,6 +334,11 @@ class Step:
         def gemm(W, Xin, Y):
             self.verify_bytes += W.all_bytes() + B * T * W.K * 2 + B * T * W.N * 4
             add("gemm", [P("cas_verify_gemm", W, Xin, B * T, Y, st)], ["gemm"])
+
+        def gemm_acc(W, Xin, Y):
+            # Y += W Xin: the residual add happens in the GEMM's atomics
+            self.verify_bytes += W.all_bytes() + B * T * W.K * 2 + B * T * W.N * 8
+            add("gemm", [P("cas_verify_gemm_accumulate", W, Xin, B * T, Y, st)], ["gemm_acc"])
 
         for d in range(D):
             add("other", [P("cas_embed", self.vtok[b * T + d:b * T + d + 1], 1, stk.emb, V, h, x[b:b + 1], st)
@@ -363,8 +368,7 @@ class Step:
         add("other", [P("cas_embed", self.vtok, B * T, stk.emb, V, h, X, st)], ["glue"])
         for layer in range(stk.L):
             M = stk.mats[layer]
-            add("other", [P("cas_add_rmsnorm", X, YD if layer else None, B * T, h, stk.g1[layer], eps, Xn, st)],
-                ["glue"])
+            add("other", [P("cas_add_rmsnorm", X, None, B * T, h, stk.g1[layer], eps, Xn, st)], ["glue"])
             gemm(M["qkv"], Xn, QKV)
             fns = [P("cas_rope_split", QKV, B * T, Hq, Hkv, stk.ctx, T, stk.theta, Q, Kn, Hkv * hd, Vn, Hkv * hd, st)]
             what = ["glue"]
@@ -377,12 +381,12 @@ class Step:
             fns.append(P("cas_f32_to_bf16", O, B * T * Hq * hd, Ob, st))
             what.append("glue")
             add("other", fns, what)
-            gemm(M["o"], Ob, Yo)
-            add("other", [P("cas_add_rmsnorm", X, Yo, B * T, h, stk.g2[layer], eps, Xn, st)], ["glue"])
+            gemm_acc(M["o"], Ob, X)
+            add("other", [P("cas_add_rmsnorm", X, None, B * T, h, stk.g2[layer], eps, Xn, st)], ["glue"])
             gemm(M["gateup"], Xn, GU)
             add("other", [P("cas_silu_mul", GU, B * T, F, HH, st)], ["glue"])
-            gemm(M["down"], HH, YD)
-        add("other", [P("cas_add_rmsnorm", X, YD, B * T, h, stk.gf, eps, Xn, st)], ["glue"])
+            gemm_acc(M["down"], HH, X)
+        add("other", [P("cas_add_rmsnorm", X, None, B * T, h, stk.gf, eps, Xn, st)], ["glue"])
         gemm(stk.lm, Xn, LG)
         fns = [P("cas_argmax", LG, B * T, V, self.vout, st)]
         fns += [P("cas_argmax", LG[b * T + T - 1:b * T + T], 1, V, self.vtok[b * T:b * T + 1], st) for b in range(B)]

@@ -82,6 +82,7 @@ def lib() -> ctypes.CDLL:
             "cas_draft_gemv_rmsnorm": ([P, P, i32, P, ctypes.c_float, P, P, P], i32),
             "cas_draft_gemv_f32": ([P, P, i32, i32, P, ctypes.c_float, P, P, i32, P], i32),
             "cas_verify_gemm": ([P, P, i32, P, P], i32),
+            "cas_verify_gemm_accumulate": ([P, P, i32, P, P], i32),
             "cas_decode_draft": ([P, P, P], i32),
             "cas_reconstruct": ([P, P, P], i32),
             "cas_kv_plan": ([i32, i64, cas_params, ctypes.c_double, P], i32),
@@ -347,6 +348,17 @@ def draft_gemv(W: EncodedWeights, x: torch.Tensor) -> torch.Tensor:
     nvec = 1 if x.dim() == 1 else x.shape[0]
     y = torch.empty(nvec, W.N, dtype=torch.float32, device=x.device)
     return cas_draft_gemv(W, x, y)
+
+
+def cas_verify_gemm_accumulate(W: EncodedWeights, X: torch.Tensor, Y: torch.Tensor, stream=None):
+    """Y += W X (Y not cleared)."""
+    X = _bits(X)
+    T = 1 if X.dim() == 1 else X.shape[0]
+    _shape(X, (W.K,) if X.dim() == 1 else (T, W.K), "X")
+    _out(Y, T * W.N, (torch.float32,), "Y")
+    _check(lib().cas_verify_gemm_accumulate(ctypes.byref(W.desc), _ptr(X), T, _ptr(Y), _stream(stream)),
+           "cas_verify_gemm_accumulate")
+    return Y
 
 
 def verify_gemm(W: EncodedWeights, X: torch.Tensor) -> torch.Tensor:

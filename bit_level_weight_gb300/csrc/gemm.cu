@@ -535,14 +535,15 @@ int corrupt_status_gemm(bool clear) {
 
 using namespace cas;
 
-extern "C" int cas_verify_gemm(const cas_weights* W, const uint16_t* X, int T, float* Y, void* stream) {
+namespace {
+int verify_gemm_call(const cas_weights* W, const uint16_t* X, int T, float* Y, bool accumulate, cudaStream_t st) {
   int s = check_weights(W);
   if (s) return s;
   if (T < 1 || T > 16) return CAS_ERR_INVALID;
   if (W->N == 0) return CAS_OK;  // nothing to write (Y may be an empty tensor)
   if (!X || !Y || !aligned16(X) || !aligned16(Y)) return CAS_ERR_INVALID;
-  cudaStream_t st = (cudaStream_t)stream;
-  if (const int e = zero_f32(Y, (int64_t)T * W->N, st)) return e;
+  if (!accumulate)
+    if (const int e = zero_f32(Y, (int64_t)T * W->N, st)) return e;
   if (W->K == 0) return CAS_OK;
   GemmArgs a;
   a.w = make_view(W);
@@ -561,4 +562,13 @@ extern "C" int cas_verify_gemm(const cas_weights* W, const uint16_t* X, int T, f
   if (fast) return launch_block<2>(a, st);
   if (whole) return v1 ? launch<1, 2, 2>(a, st) : launch<2, 2, 2>(a, st);
   return v1 ? launch<1, 2, 0>(a, st) : launch<2, 2, 0>(a, st);
+}
+}  // namespace
+
+extern "C" int cas_verify_gemm(const cas_weights* W, const uint16_t* X, int T, float* Y, void* stream) {
+  return verify_gemm_call(W, X, T, Y, false, (cudaStream_t)stream);
+}
+
+extern "C" int cas_verify_gemm_accumulate(const cas_weights* W, const uint16_t* X, int T, float* Y, void* stream) {
+  return verify_gemm_call(W, X, T, Y, true, (cudaStream_t)stream);
 }

@@ -227,6 +227,10 @@ int cas_draft_gemv_f32(const cas_weights* W, const float* x, int nvec, int op, c
  * T is outside 1..16 or X or Y is null or not 16-byte aligned; CAS_ERR_CUDA on
  * a launch error. N = 0 writes nothing. */
 int cas_verify_gemm(const cas_weights* W, const uint16_t* X, int T, float* Y, void* stream);
+/* Verify GEMM that adds into Y: Y[t][n] += sum_k W[n][k] * X[t][k], Y not
+ * cleared (a residual stream can be Y). Same arguments and errors as
+ * cas_verify_gemm. */
+int cas_verify_gemm_accumulate(const cas_weights* W, const uint16_t* X, int T, float* Y, void* stream);
 
 /* Materialises the draft values D(W) as bf16 [N][K] (test path) [B3.1].
  * Errors: those of the descriptor check; CAS_ERR_INVALID if out is null or

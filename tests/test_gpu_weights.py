@@ -395,3 +395,19 @@ def test_draft_gemv_rows_of_one_chunk(cas, orc, kind, nvec):
     y0 = torch.randn(nvec, N, generator=g)
     ya = cas.cas_draft_gemv_accumulate(enc, x, y0.clone().cuda())
     check_close(ya - y0.cuda(), ref, norm, "draft_gemv_accumulate rows of one chunk")
+
+
+@pytest.mark.parametrize("N,K,T", [(24, 4096, 5), (40, 2048, 3), (17, 1152, 9)])
+def test_verify_gemm_accumulate(cas, orc, N, K, T):
+    """The accumulating verify GEMM adds W X to a given Y (for the block-walk
+    kernel and the other tile decoders), and the plain one overwrites it."""
+    W = synthetic.t4_weight(N, K, seed=N + K + T)
+    X = synthetic.activations(T, K, seed=T + 3)
+    enc = cas.encode_weights(W.cuda(), 1, 64, 3)
+    ref, norm = orc.matvec(np16(W), np16(X))
+    g = torch.Generator().manual_seed(N)
+    Y0 = torch.randn(T, N, generator=g)
+    Ya = cas.cas_verify_gemm_accumulate(enc, X.cuda(), Y0.clone().cuda())
+    check_close(Ya - Y0.cuda(), ref, norm, "verify_gemm_accumulate")
+    Yp = cas.cas_verify_gemm(enc, X.cuda(), Y0.clone().cuda())
+    check_close(Yp, ref, norm, "verify_gemm over a given Y")
