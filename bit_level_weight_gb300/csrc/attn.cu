@@ -1157,20 +1157,26 @@ __global__ void __launch_bounds__(kThreads, 4) attn_draft_block_kernel(AttnArgs 
         bwindow(ms_a, 128u, 0, 4, Hp, Lp);
         bwindow(st_a, 4u, q0 + 1, BlockStreams<2>::kRow - 3, Hc, Lc);
         uint32_t used = 0u, cor = 0u;
+        bool pstale = false;  // the position window lags the cursor (after a scanned group)
 #pragma unroll 1
         for (int gi = 0; gi < 8; ++gi) {
           const uint32_t fo = fn, fe = fn << 4;
           if (gi < 7) fn = __ldg(rec + gi + 1);
           if (gi > 0) {
-            const int cur = min((int)(xa - q4_a) >> 4, CAS_BLK - 1);
-            xa = q4_a + 16u * (uint32_t)cur;
-            bwindow(ms_a, 128u, cur + 1, 4, Hp, Lp);
+            // the position window every 16 values (a window that runs dry
+            // is caught like a long gap), the code window every 8
+            if ((gi & 1) == 0 || pstale) {
+              const int cur = min((int)(xa - q4_a) >> 4, CAS_BLK - 1);
+              xa = q4_a + 16u * (uint32_t)cur;
+              bwindow(ms_a, 128u, cur + 1, 4, Hp, Lp);
+            }
             bwindow(st_a, 4u, q0 + 1 + (int)used, BlockStreams<2>::kRow - 3, Hc, Lc);
           }
-          // a group whose 8 positions or codes do not all end in the windows
-          // (a code longer than the window: an exponent the tables rank far
-          // down) is taken by scanning; the walk goes on after it
-          if (__popc(Hp) + __popc(Lp) < 8 || __popc(Hc) + __popc(Lc) < 8) {
+          pstale = false;
+          // a group whose 8 codes do not all end in the window (a code longer
+          // than the window: an exponent the tables rank far down) is taken by
+          // scanning; the walk goes on after it
+          if (__popc(Hc) + __popc(Lc) < 8) {
             int cur = (int)(xa - q4_a) >> 4, qt = q0 + (int)used;
             for (int i = 0; i < 8; ++i) {
               const int pb = bnext_one(ms_a, 128u, cur + 1, 6);
@@ -1195,6 +1201,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_draft_block_kernel(AttnArgs 
               acc.w = fmaf(v, qq.w, acc.w);
             }
             xa = q4_a + 16u * (uint32_t)max(cur, -1);
+            pstale = true;
             continue;
           }
 #pragma unroll
@@ -1307,7 +1314,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_draft_block_kernel(AttnArgs 
               bwindow(ms_a, 128u, cur + 1, 4, Hp, Lp);
               bwindow(st_a, 4u, q0 + 1 + (int)used, BlockStreams<2>::kRow - 3, Hc, Lc);
             }
-            if (__popc(Hp) + __popc(Lp) < 8 || __popc(Hc) + __popc(Lc) < 8) {  // as for K
+            if (__popc(Hc) + __popc(Lc) < 8) {  // as for K
               int cur = (int)(ta - row_a) >> 1, qt = q0 + (int)used;
               for (int i = 0; i < 8; ++i) {
                 const int pb = bnext_one(ms_a, 128u, cur + 1, 6);
